@@ -1,0 +1,182 @@
+/*
+ * tp.h -- C ABI of libtpshard.so: the Megatron tensor-parallel transformer
+ * block with t logical shards resident on one GPU (sm_103a).
+ *
+ * The partition math follows the pages this library implements:
+ *   - "02 — Tensor Parallelism" (project-fortress roadmap), sections
+ *     "Column-parallel vs row-parallel — the derivation", "The MLP pairing",
+ *     "The attention pairing", "Sequence parallelism (Megatron-3)";
+ *   - "Tensor and sequence parallelism" (ai-infra handbooks), sections
+ *     "How Megatron partitions" (the f / g operator table), "Sequence
+ *     parallelism" and "The implementation";
+ *   - "Tensor Parallelism's Communication Boundary" (aryanputta.com),
+ *     sections "Follow the coordinates" and "Count the object, then the
+ *     collective" (bias added once);
+ *   - "Parallelism Strategies #1 - Tensor Parallelism" (substack), the
+ *     sharded backward and the local weight-shard gradients;
+ *   - "Megatron-LM: Tensor Parallelism" (vanos001), sections "Attention
+ *     Block" and "MLP Block".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - tp_bf16 is the raw bit pattern of an IEEE bfloat16.  Accumulation is fp32.
+ *  - Activations multiply weights from the left: Y = X W, W stored (in, out)
+ *    in its UNPACKED form.  The t shards own contiguous, rank-ordered blocks
+ *    C_i = [i*F/t, (i+1)*F/t) of the split dimension; t must divide it.
+ *  - PACKED weights are per-shard slices stored (out, in), K contiguous:
+ *      column-parallel W (h, F)  -> [t][F/t][h]      (tp_pack_col)
+ *      row-parallel    W (F, h)  -> [t][h][F/t]      (tp_pack_row)
+ *      SwiGLU gate/up  (h, F)    -> [t][F/t/128][2][128][h]   (tp_pack_swiglu)
+ *      W_qkv (d, 3d) = [Q|K|V]   -> [t][3d/t][d] rows [Q_i|K_i|V_i] (tp_pack_qkv_heads)
+ *      W_o (d, d), rows by head  -> [t][d][d/t]      (tp_pack_row)
+ *    Weight gradients come back in the same packed layouts, in fp32.
+ *  - Memory: every pointer is a DEVICE pointer owned by the caller (the
+ *    library never allocates, never frees and keeps no pointer after a call
+ *    returns).  Pointers must be 16-byte aligned (else TP_ERR_ALIGN); the
+ *    innermost dimension of every matrix must be a multiple of 8 elements.
+ *  - Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and the call returns without synchronising.  Argument
+ *    errors are detected on the host before anything is launched and leave
+ *    outputs untouched.  Device-side errors (a bounded wait that expired) are
+ *    recorded in a per-device error word that tp_get_device_status() reads.
+ *  - Workspace: entry points that need scratch take (ws, ws_bytes); the
+ *    matching *_workspace_size() gives the minimum.  Too small -> TP_ERR_WORKSPACE.
+ *  - Thread safety: calls on different streams may run concurrently; they
+ *    share only the device error word.
+ */
+#ifndef TPSHARD_TP_H
+#define TPSHARD_TP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TP_ABI_VERSION 1
+
+typedef enum {
+  TP_OK = 0,
+  TP_ERR_INVALID_ARG = 1, /* null required pointer, bad enum, t < 1, negative size */
+  TP_ERR_SHAPE = 2,       /* t does not divide the split dim, unsupported size */
+  TP_ERR_ALIGN = 3,       /* pointer not 16-byte aligned, row length not a multiple of 8 */
+  TP_ERR_WORKSPACE = 4,   /* ws_bytes smaller than the *_workspace_size() result */
+  TP_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
+  TP_ERR_TIMEOUT = 6,     /* device: a bounded wait inside a kernel expired */
+  TP_ERR_UNSUPPORTED = 7  /* no sm_103a device, or a combination not built */
+} tp_status;
+
+typedef enum {
+  TP_ACT_IDENTITY = 0,
+  TP_ACT_RELU = 1,
+  TP_ACT_GELU_TANH = 2, /* 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3))) */
+  TP_ACT_GELU_ERF = 3,  /* 0.5 z (1 + erf(z / sqrt 2)) */
+  TP_ACT_SWIGLU = 4     /* silu(X W_gate) * (X W_up); decode entry point only */
+} tp_act;
+
+/* Flags for tp_mlp_forward / tp_mlp_backward / tp_attn_forward. */
+#define TP_FLAG_UNFUSED_REDUCE 1u /* materialise the t partial sums P_i (fp32, in ws) and
+                                     reduce them in a separate kernel instead of in the
+                                     row-parallel GEMM's accumulator */
+
+typedef uint16_t tp_bf16;
+typedef struct CUstream_st* tp_stream; /* identical to cudaStream_t */
+
+/* ------------------------------------------------------------------ misc */
+int tp_abi_version(void);
+const char* tp_status_string(tp_status s);
+
+/* Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns TP_OK, TP_ERR_TIMEOUT (a bounded wait expired), or
+ * TP_ERR_CUDA if the synchronisation itself failed. */
+tp_status tp_get_device_status(tp_stream stream);
+
+/* Fault-path self test: launches one CTA that waits on an mbarrier nothing
+ * will ever complete, with a limit of `timeout_us` microseconds (1..10^7).
+ * The wait gives up, records TP_ERR_TIMEOUT in the error word and the kernel
+ * returns normally; the context stays usable.  tp_get_device_status() then
+ * reports TP_ERR_TIMEOUT. */
+tp_status tp_selftest_bounded_wait(int64_t timeout_us, tp_stream stream);
+
+/* -------------------------------------------------------------- packing
+ * Bit-exact permutations of bf16 weights into the per-shard layouts listed
+ * above ("Tensor and sequence parallelism", section "The implementation":
+ * each rank keeps w1[cols] and w2[:, cols]; "02 — Tensor Parallelism",
+ * section "The attention pairing": each rank owns n_heads/t heads of Q, K, V).
+ * Src and dst must not overlap.  The unpack_* calls are exact inverses, so a
+ * checkpoint sharded t ways is re-sharded t' ways as unpack(t) then pack(t'). */
+tp_status tp_pack_col(const tp_bf16* W, int64_t h, int64_t F, int t, tp_bf16* Wp, tp_stream stream);
+tp_status tp_unpack_col(const tp_bf16* Wp, int64_t h, int64_t F, int t, tp_bf16* W, tp_stream stream);
+tp_status tp_pack_row(const tp_bf16* W, int64_t F, int64_t h, int t, tp_bf16* Wp, tp_stream stream);
+tp_status tp_unpack_row(const tp_bf16* Wp, int64_t F, int64_t h, int t, tp_bf16* W, tp_stream stream);
+/* Wg, Wu: (h, F); (F/t) % 128 == 0. */
+tp_status tp_pack_swiglu(const tp_bf16* Wg, const tp_bf16* Wu, int64_t h, int64_t F, int t, tp_bf16* Wp,
+                         tp_stream stream);
+/* Wqkv: (d, 3d), columns [Q|K|V], head j at columns j*head_dim of each block.
+ * n_heads*head_dim == d, t | n_heads, head_dim % 8 == 0. */
+tp_status tp_pack_qkv_heads(const tp_bf16* Wqkv, int64_t d, int n_heads, int head_dim, int t, tp_bf16* Wp,
+                            tp_stream stream);
+tp_status tp_unpack_qkv_heads(const tp_bf16* Wp, int64_t d, int n_heads, int head_dim, int t, tp_bf16* Wqkv,
+                              tp_stream stream);
+/* b: (3d) -> [t][3d/t] in the same head order. */
+tp_status tp_pack_qkv_bias(const tp_bf16* b, int64_t d, int n_heads, int head_dim, int t, tp_bf16* bp,
+                           tp_stream stream);
+
+/* -------------------------------------------------------------- TP MLP
+ * Forward ("02 — Tensor Parallelism", "The MLP pairing"; "Tensor and
+ * sequence parallelism", f/g table):
+ *   f forward (identity): every shard reads the same X [M][h].
+ *   shard i: Z_i = X W_up,i + b_up[C_i];  A_i = act(Z_i)            (column-parallel)
+ *            P_i = A_i W_down,i                                      (row-parallel)
+ *   g forward (all-reduce): Y = sum_{i=0..t-1} P_i + b_down (+ residual), bias ONCE.
+ * On one GPU the all-reduce is fused: the row-parallel GEMM accumulates the
+ * shards' K ranges one after another into a single fp32 accumulator, i = 0..t-1
+ * in order, and adds b_down once in its epilogue.  With TP_FLAG_UNFUSED_REDUCE
+ * the t partials are written to ws ([t][M][h] fp32) and summed by a separate
+ * fixed-order reduction kernel.
+ *   X [M][h]; Wup_p [t][F/t][h]; bup [F] (nullable); Wdown_p [t][h][F/t];
+ *   bdown [h] (nullable); residual [M][h] (nullable, added after the sum);
+ *   Y [M][h]; Z_save [t][M][F/t] (nullable: inference); A_save [t][M][F/t] (required).
+ * act: IDENTITY, RELU, GELU_TANH or GELU_ERF.  h % 8 == 0, (F/t) % 8 == 0. */
+size_t tp_mlp_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned flags);
+tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int t, tp_act act,
+                         const tp_bf16* Wup_p, const tp_bf16* bup, const tp_bf16* Wdown_p, const tp_bf16* bdown,
+                         const tp_bf16* residual, tp_bf16* Y, tp_bf16* Z_save, tp_bf16* A_save, unsigned flags,
+                         void* ws, size_t ws_bytes, tp_stream stream);
+
+/* Backward of L = <Y, dY> ("Parallelism Strategies #1 - Tensor Parallelism",
+ * sharded backward; "Tensor and sequence parallelism", f/g table):
+ *   g backward (identity): every shard receives dY unchanged; db_down = sum_rows dY once.
+ *   shard i: dZ_i = (dY W_down,i^T) * act'(Z_i);  db_up[C_i] = sum_rows dZ_i
+ *            dW_down,i = A_i^T dY;  dW_up,i = dZ_i^T X      (local, no reduction)
+ *   f backward (all-reduce): dX = sum_{i=0..t-1} dZ_i W_up,i^T (fused as in the forward).
+ * Outputs: dX [M][h] bf16; dWup_p [t][F/t][h] and dWdown_p [t][h][F/t] fp32
+ * (overwritten, or added to when `accumulate` != 0); dbup [F], dbdown [h] fp32
+ * (nullable).  ws holds dZ ([t][M][F/t] bf16) and column-sum scratch. */
+size_t tp_mlp_backward_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned flags);
+tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_save, const tp_bf16* A_save,
+                          int64_t M, int64_t h, int64_t F, int t, tp_act act, const tp_bf16* Wup_p,
+                          const tp_bf16* Wdown_p, tp_bf16* dX, float* dWup_p, float* dWdown_p, float* dbup,
+                          float* dbdown, int accumulate, unsigned flags, void* ws, size_t ws_bytes,
+                          tp_stream stream);
+
+/* ------------------------------------------------------------ utilities
+ * Fixed-order reduction of t partial buffers (the on-device stand-in for an
+ * all-reduce, unfused form): out[r][c] = sum_{i=0..t-1} P[i][r][c] + bias[c]
+ * (once, nullable) + residual[r][c] (nullable).  P fp32 [t][rows][cols];
+ * out_bf16 and/or out_f32 (at least one non-null). */
+tp_status tp_shard_reduce(const float* P, int64_t rows, int64_t cols, int t, const tp_bf16* bias,
+                          const tp_bf16* residual, tp_bf16* out_bf16, float* out_f32, tp_stream stream);
+
+/* Column sums of a bf16 matrix [rows][cols] -> fp32 [cols] in a fixed order
+ * (bias gradients).  ws: tp_colsum_workspace_size(rows, cols) bytes. */
+size_t tp_colsum_workspace_size(int64_t rows, int64_t cols);
+tp_status tp_colsum(const tp_bf16* G, int64_t rows, int64_t cols, float* out, int accumulate, void* ws,
+                    size_t ws_bytes, tp_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPSHARD_TP_H */

@@ -1,0 +1,335 @@
+// extern "C" entry points of libtpshard.so (declared in include/tp.h), the
+// per-device error word, and the fault-path self test.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tp {
+
+// Written by any kernel whose bounded wait expired (first error wins).
+__device__ int g_tp_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+int* g_err_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+int g_is_sm103[kMaxDevices] = {};
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+// Per-device set-up, once, with that device current.
+bool ensure_device(int dev) {
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_err_ptr[dev]) return true;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_tp_error_word) != cudaSuccess) return false;
+  int sms = 0, major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return false;
+  g_sm_count[dev] = sms;
+  g_is_sm103[dev] = (major == 10 && minor == 3);
+  g_err_ptr[dev] = static_cast<int*>(p);
+  return true;
+}
+
+__global__ void selftest_wait_kernel(int* err, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // Nothing ever arrives on `bar`: the wait must give up by itself.
+    ptx::mbar_wait(&bar, 0, &abort_flag, err, 0x1FF, timeout_ns);
+  }
+  __syncthreads();
+}
+
+}  // namespace
+
+int* device_error_word() {
+  const int dev = current_device();
+  if (dev < 0 || !ensure_device(dev)) return nullptr;
+  return g_err_ptr[dev];
+}
+
+int device_sm_count() {
+  const int dev = current_device();
+  if (dev < 0 || !ensure_device(dev)) return 1;
+  return g_sm_count[dev] > 0 ? g_sm_count[dev] : 1;
+}
+
+bool device_is_sm103() {
+  const int dev = current_device();
+  if (dev < 0 || !ensure_device(dev)) return false;
+  return g_is_sm103[dev] != 0;
+}
+
+tp_status ready() {
+  if (!device_error_word()) return TP_ERR_CUDA;
+  if (!device_is_sm103()) return TP_ERR_UNSUPPORTED;
+  return TP_OK;
+}
+
+uint64_t wait_timeout_ns() {
+  static uint64_t ns = [] {
+    const char* e = std::getenv("TP_WAIT_TIMEOUT_MS");
+    long ms = e ? std::atol(e) : 0;
+    if (ms <= 0 || ms > 60000) ms = 2000;
+    return static_cast<uint64_t>(ms) * 1000000ull;
+  }();
+  return ns;
+}
+
+}  // namespace tp
+
+using namespace tp;
+
+namespace {
+
+inline cudaStream_t S(tp_stream s) { return reinterpret_cast<cudaStream_t>(s); }
+
+bool act_ok(int a) { return a >= TP_ACT_IDENTITY && a <= TP_ACT_GELU_ERF; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+extern "C" {
+
+int tp_abi_version(void) { return TP_ABI_VERSION; }
+
+const char* tp_status_string(tp_status s) {
+  switch (s) {
+    case TP_OK: return "TP_OK";
+    case TP_ERR_INVALID_ARG: return "TP_ERR_INVALID_ARG: null pointer, bad enum or negative size";
+    case TP_ERR_SHAPE: return "TP_ERR_SHAPE: t does not divide the split dimension, or unsupported size";
+    case TP_ERR_ALIGN: return "TP_ERR_ALIGN: pointer not 16-byte aligned or row length not a multiple of 8";
+    case TP_ERR_WORKSPACE: return "TP_ERR_WORKSPACE: workspace smaller than the *_workspace_size() result";
+    case TP_ERR_CUDA: return "TP_ERR_CUDA: CUDA runtime call or kernel launch failed";
+    case TP_ERR_TIMEOUT: return "TP_ERR_TIMEOUT: a bounded wait inside a kernel expired";
+    case TP_ERR_UNSUPPORTED: return "TP_ERR_UNSUPPORTED: needs an sm_103a device / combination not built";
+  }
+  return "unknown tp_status";
+}
+
+tp_status tp_get_device_status(tp_stream stream) {
+  if (!device_error_word()) return TP_ERR_CUDA;
+  if (cudaStreamSynchronize(S(stream)) != cudaSuccess) return TP_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_tp_error_word, sizeof(int)) != cudaSuccess) return TP_ERR_CUDA;
+  if (word == 0) return TP_OK;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_tp_error_word, &zero, sizeof(int)) != cudaSuccess) return TP_ERR_CUDA;
+  return TP_ERR_TIMEOUT;
+}
+
+tp_status tp_selftest_bounded_wait(int64_t timeout_us, tp_stream stream) {
+  if (timeout_us < 1 || timeout_us > 10000000) return TP_ERR_INVALID_ARG;
+  TP_RETURN_IF(ready());
+  selftest_wait_kernel<<<1, 32, 0, S(stream)>>>(device_error_word(), static_cast<uint64_t>(timeout_us) * 1000ull);
+  return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ packing
+tp_status tp_pack_col(const tp_bf16* W, int64_t h, int64_t F, int t, tp_bf16* Wp, tp_stream stream) {
+  return pack_col(W, h, F, t, Wp, 0, S(stream));
+}
+tp_status tp_unpack_col(const tp_bf16* Wp, int64_t h, int64_t F, int t, tp_bf16* W, tp_stream stream) {
+  return pack_col(Wp, h, F, t, W, 1, S(stream));
+}
+tp_status tp_pack_row(const tp_bf16* W, int64_t F, int64_t h, int t, tp_bf16* Wp, tp_stream stream) {
+  return pack_row(W, F, h, t, Wp, 0, S(stream));
+}
+tp_status tp_unpack_row(const tp_bf16* Wp, int64_t F, int64_t h, int t, tp_bf16* W, tp_stream stream) {
+  return pack_row(Wp, F, h, t, W, 1, S(stream));
+}
+tp_status tp_pack_swiglu(const tp_bf16* Wg, const tp_bf16* Wu, int64_t h, int64_t F, int t, tp_bf16* Wp,
+                         tp_stream stream) {
+  return pack_swiglu(Wg, Wu, h, F, t, Wp, S(stream));
+}
+tp_status tp_pack_qkv_heads(const tp_bf16* Wqkv, int64_t d, int n_heads, int head_dim, int t, tp_bf16* Wp,
+                            tp_stream stream) {
+  return pack_qkv(Wqkv, d, n_heads, head_dim, t, Wp, 0, S(stream));
+}
+tp_status tp_unpack_qkv_heads(const tp_bf16* Wp, int64_t d, int n_heads, int head_dim, int t, tp_bf16* Wqkv,
+                              tp_stream stream) {
+  return pack_qkv(Wp, d, n_heads, head_dim, t, Wqkv, 1, S(stream));
+}
+tp_status tp_pack_qkv_bias(const tp_bf16* b, int64_t d, int n_heads, int head_dim, int t, tp_bf16* bp,
+                           tp_stream stream) {
+  return pack_qkv_bias(b, d, n_heads, head_dim, t, bp, S(stream));
+}
+
+// ------------------------------------------------------------------ TP MLP
+size_t tp_mlp_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned flags) {
+  if (M < 0 || h < 0 || F < 0 || t < 1) return 0;
+  return (flags & TP_FLAG_UNFUSED_REDUCE) ? static_cast<size_t>(t) * M * h * sizeof(float) : 0;
+}
+
+tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int t, tp_act act,
+                         const tp_bf16* Wup_p, const tp_bf16* bup, const tp_bf16* Wdown_p, const tp_bf16* bdown,
+                         const tp_bf16* residual, tp_bf16* Y, tp_bf16* Z_save, tp_bf16* A_save, unsigned flags,
+                         void* ws, size_t ws_bytes, tp_stream stream) {
+  if (M < 0 || h < 1 || F < 1 || t < 1 || !act_ok(act)) return TP_ERR_INVALID_ARG;
+  if (F % t != 0) return TP_ERR_SHAPE;
+  const int64_t Ft = F / t;
+  if (h % 8 != 0 || Ft % 8 != 0) return TP_ERR_ALIGN;
+  if (M == 0) return TP_OK;  // no tokens: nothing to compute (buffers may be NULL)
+  if (!X || !Wup_p || !Wdown_p || !Y || !A_save) return TP_ERR_INVALID_ARG;
+  const bool unfused = (flags & TP_FLAG_UNFUSED_REDUCE) != 0;
+  if (ws_bytes < tp_mlp_workspace_size(M, h, F, t, flags) || (unfused && !ws)) return TP_ERR_WORKSPACE;
+  const cudaStream_t s = S(stream);
+
+  // Column-parallel: Z_i = X W_up,i + b_up[C_i]; A_i = act(Z_i).  X is read by every shard (f forward).
+  GemmProblem c;
+  c.M = M; c.N = Ft; c.K = h; c.nbatch = t; c.nsum = 1;
+  c.a.ptr = X; c.a.ld = h;
+  c.b.ptr = Wup_p; c.b.ld = h; c.b.sharded = true; c.b.shard_stride = Ft * h;
+  c.epi = EPI_ACT; c.act = act;
+  c.d = Z_save; c.d2 = A_save; c.ldd = Ft; c.d_batch_stride = M * Ft;
+  c.bias = bup; c.bias_batch_stride = Ft;
+  TP_RETURN_IF(run_gemm(c, s));
+
+  // Row-parallel + g: Y = sum_i A_i W_down,i + b_down (once) + residual.
+  GemmProblem r;
+  r.M = M; r.N = h; r.K = Ft;
+  r.a.ptr = A_save; r.a.ld = Ft; r.a.sharded = true; r.a.shard_stride = M * Ft;
+  r.b.ptr = Wdown_p; r.b.ld = Ft; r.b.sharded = true; r.b.shard_stride = h * Ft;
+  if (!unfused) {
+    r.nbatch = 1; r.nsum = t;
+    r.epi = EPI_BF16; r.d = Y; r.ldd = h; r.bias = bdown; r.residual = residual; r.ld_res = h;
+    return run_gemm(r, s);
+  }
+  float* P = static_cast<float*>(ws);
+  r.nbatch = t; r.nsum = 1;
+  r.epi = EPI_F32; r.d = P; r.ldd = h; r.d_batch_stride = M * h;
+  TP_RETURN_IF(run_gemm(r, s));
+  return run_shard_reduce(P, M, h, t, bdown, residual, Y, nullptr, s);
+}
+
+size_t tp_mlp_backward_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned flags) {
+  if (M < 0 || h < 0 || F < 0 || t < 1) return 0;
+  const int64_t Ft = F / t;
+  size_t sz = round_up(static_cast<size_t>(M) * F * 2, 256);  // dZ
+  const size_t cs = std::max(colsum_ws_floats(M, Ft) * t, colsum_ws_floats(M, h));
+  sz += round_up(cs * sizeof(float), 256);
+  if (flags & TP_FLAG_UNFUSED_REDUCE) sz += static_cast<size_t>(t) * M * h * sizeof(float);
+  return sz;
+}
+
+tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_save, const tp_bf16* A_save,
+                          int64_t M, int64_t h, int64_t F, int t, tp_act act, const tp_bf16* Wup_p,
+                          const tp_bf16* Wdown_p, tp_bf16* dX, float* dWup_p, float* dWdown_p, float* dbup,
+                          float* dbdown, int accumulate, unsigned flags, void* ws, size_t ws_bytes,
+                          tp_stream stream) {
+  if (M < 0 || h < 1 || F < 1 || t < 1 || !act_ok(act)) return TP_ERR_INVALID_ARG;
+  if (!dWup_p || !dWdown_p) return TP_ERR_INVALID_ARG;
+  if (M > 0 && (!dY || !X || !A_save || !Wup_p || !Wdown_p || !dX)) return TP_ERR_INVALID_ARG;
+  if (M > 0 && act != TP_ACT_IDENTITY && !Z_save) return TP_ERR_INVALID_ARG;
+  if (F % t != 0) return TP_ERR_SHAPE;
+  const int64_t Ft = F / t;
+  if (h % 8 != 0 || Ft % 8 != 0) return TP_ERR_ALIGN;
+  if (!ws || ws_bytes < tp_mlp_backward_workspace_size(M, h, F, t, flags)) return TP_ERR_WORKSPACE;
+  if (!aligned16(ws)) return TP_ERR_ALIGN;
+  const cudaStream_t s = S(stream);
+  const bool unfused = (flags & TP_FLAG_UNFUSED_REDUCE) != 0;
+
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint16_t* dZ = reinterpret_cast<uint16_t*>(w);
+  w += round_up(static_cast<size_t>(M) * F * 2, 256);
+  float* cs_ws = reinterpret_cast<float*>(w);
+  const size_t cs_floats = std::max(colsum_ws_floats(M, Ft) * t, colsum_ws_floats(M, h));
+  w += round_up(cs_floats * sizeof(float), 256);
+  float* P = reinterpret_cast<float*>(w);
+
+  if (M == 0) {  // no tokens: every gradient is zero (or unchanged when accumulating)
+    if (!accumulate) {
+      TP_RETURN_IF(ready());
+      TP_CUDA_CHECK(cudaMemsetAsync(dWup_p, 0, sizeof(float) * F * h, s));
+      TP_CUDA_CHECK(cudaMemsetAsync(dWdown_p, 0, sizeof(float) * F * h, s));
+      if (dbup) TP_CUDA_CHECK(cudaMemsetAsync(dbup, 0, sizeof(float) * F, s));
+      if (dbdown) TP_CUDA_CHECK(cudaMemsetAsync(dbdown, 0, sizeof(float) * h, s));
+    }
+    return TP_OK;
+  }
+
+  // g backward is the identity: the bias gradient of the row-parallel layer is taken once.
+  if (dbdown) TP_RETURN_IF(run_colsum(dY, M, h, h, dbdown, accumulate, cs_ws, cs_floats, s));
+
+  // dgrad + act': dZ_i = (dY W_down,i^T) * act'(Z_i).
+  GemmProblem g;
+  g.M = M; g.N = Ft; g.K = h; g.nbatch = t;
+  g.a.ptr = dY; g.a.ld = h;
+  g.b.ptr = Wdown_p; g.b.ld = Ft; g.b.sharded = true; g.b.shard_stride = h * Ft; g.b.mn_major = true;
+  g.epi = EPI_DACT; g.act = act; g.aux = Z_save ? Z_save : A_save; g.ld_aux = Ft; g.aux_batch_stride = M * Ft;
+  g.d = dZ; g.ldd = Ft; g.d_batch_stride = M * Ft;
+  TP_RETURN_IF(run_gemm(g, s));
+
+  if (dbup) TP_RETURN_IF(run_colsum_batched(dZ, M, Ft, Ft, t, M * Ft, dbup, accumulate, cs_ws, cs_floats, s));
+
+  // Local weight gradients (no reduction): dW_down,i = A_i^T dY  -> packed [t][h][Ft].
+  GemmProblem wd;
+  wd.M = h; wd.N = Ft; wd.K = M; wd.nbatch = t;
+  wd.a.ptr = dY; wd.a.ld = h; wd.a.mn_major = true;
+  wd.b.ptr = A_save; wd.b.ld = Ft; wd.b.sharded = true; wd.b.shard_stride = M * Ft; wd.b.mn_major = true;
+  wd.epi = EPI_F32; wd.d = dWdown_p; wd.ldd = Ft; wd.d_batch_stride = h * Ft; wd.accumulate = accumulate;
+  TP_RETURN_IF(run_gemm(wd, s));
+
+  // dW_up,i = dZ_i^T X -> packed [t][Ft][h].
+  GemmProblem wu;
+  wu.M = Ft; wu.N = h; wu.K = M; wu.nbatch = t;
+  wu.a.ptr = dZ; wu.a.ld = Ft; wu.a.sharded = true; wu.a.shard_stride = M * Ft; wu.a.mn_major = true;
+  wu.b.ptr = X; wu.b.ld = h; wu.b.mn_major = true;
+  wu.epi = EPI_F32; wu.d = dWup_p; wu.ldd = h; wu.d_batch_stride = Ft * h; wu.accumulate = accumulate;
+  TP_RETURN_IF(run_gemm(wu, s));
+
+  // f backward: dX = sum_i dZ_i W_up,i^T.
+  GemmProblem dx;
+  dx.M = M; dx.N = h; dx.K = Ft;
+  dx.a.ptr = dZ; dx.a.ld = Ft; dx.a.sharded = true; dx.a.shard_stride = M * Ft;
+  dx.b.ptr = Wup_p; dx.b.ld = h; dx.b.sharded = true; dx.b.shard_stride = Ft * h; dx.b.mn_major = true;
+  if (!unfused) {
+    dx.nsum = t;
+    dx.epi = EPI_BF16; dx.d = dX; dx.ldd = h;
+    return run_gemm(dx, s);
+  }
+  dx.nbatch = t;
+  dx.epi = EPI_F32; dx.d = P; dx.ldd = h; dx.d_batch_stride = M * h;
+  TP_RETURN_IF(run_gemm(dx, s));
+  return run_shard_reduce(P, M, h, t, nullptr, nullptr, dX, nullptr, s);
+}
+
+// ------------------------------------------------------------------ utilities
+tp_status tp_shard_reduce(const float* P, int64_t rows, int64_t cols, int t, const tp_bf16* bias,
+                          const tp_bf16* residual, tp_bf16* out_bf16, float* out_f32, tp_stream stream) {
+  return run_shard_reduce(P, rows, cols, t, bias, residual, out_bf16, out_f32, S(stream));
+}
+
+size_t tp_colsum_workspace_size(int64_t rows, int64_t cols) {
+  if (rows < 0 || cols < 0) return 0;
+  return colsum_ws_floats(rows, cols) * sizeof(float);
+}
+
+tp_status tp_colsum(const tp_bf16* G, int64_t rows, int64_t cols, float* out, int accumulate, void* ws,
+                    size_t ws_bytes, tp_stream stream) {
+  return run_colsum(G, rows, cols, cols, out, accumulate, static_cast<float*>(ws), ws_bytes / sizeof(float),
+                    S(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,514 @@
+// Persistent, warp-specialised bf16 GEMM on the 5th-generation tensor cores
+// (tcgen05.mma, accumulators in tensor memory) fed by TMA, for sm_103a.
+//
+// This one kernel carries every dense contraction of the TP block:
+//   column-parallel  Z_i = X W_up,i + b, A_i = act(Z_i)        (output batch = shard)
+//   row-parallel     Y = sum_i A_i W_down,i + b (+ residual)    (shards summed in the accumulator)
+//   dgrad            dZ_i = (dY W_down,i^T) * act'(Z_i)
+//   f backward       dX = sum_i dZ_i W_up,i^T
+//   wgrad            dW_down,i = A_i^T dY, dW_up,i = dZ_i^T X    (MN-major operands)
+// ("02 — Tensor Parallelism", "Column-parallel vs row-parallel — the
+// derivation" and "The MLP pairing"; "Parallelism Strategies #1 - Tensor
+// Parallelism", sharded backward.)
+//
+// The g all-reduce of the row-parallel GEMM needs no buffer on one GPU: shard
+// i's K range is accumulated into the same TMEM accumulator right after shard
+// i-1's, so the accumulator ends holding P_0 + P_1 + ... + P_{t-1} in shard
+// order, and the output bias is added once in the epilogue.
+//
+// CTA layout (192 threads, one CTA per SM, persistent over output tiles):
+//   warp 0     TMA producer: fills a STAGES-deep ring of A/B tiles (128B swizzle)
+//   warp 1     allocates 512 TMEM columns; lane 0 issues tcgen05.mma 128x256x16
+//              into one of two 256-column accumulators (double-buffered so the
+//              epilogue of tile n overlaps the main loop of tile n+1)
+//   warps 2-5  epilogue: tcgen05.ld rows of the accumulator (warp w reads TMEM
+//              lanes 32*(w%4)..+31), apply bias / activation / residual, store.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "devmath.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tp {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;  // one 128-byte swizzle row of bf16
+constexpr int STAGES = 4;
+constexpr int A_TILE_BYTES = BM * BK * 2;
+constexpr int B_TILE_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
+constexpr int MN_CHUNK_BYTES = 64 * BK * 2;  // one 64-wide MN-major TMA box
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int NUM_THREADS = 192;
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+
+enum : int { ERR_WAIT_PRODUCER = 0x101, ERR_WAIT_MMA = 0x102, ERR_WAIT_EPI = 0x103, ERR_WAIT_DRAIN = 0x104 };
+
+struct GemmArgs {
+  int M, N;
+  int nbatch, nsum;
+  int a_sharded, b_sharded;
+  int mt, nt, kt;
+  int epi, act;
+  void* d;
+  int64_t ldd, d_bs;
+  void* d2;
+  const uint16_t* bias;
+  int64_t bias_bs;
+  const uint16_t* aux;
+  int64_t ld_aux, aux_bs;
+  const uint16_t* res;
+  int64_t ld_res;
+  int accumulate;
+  int* err;
+  uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ void decode_tile(int tile, const GemmArgs& p, int& b, int& mb, int& nb) {
+  mb = tile % p.mt;
+  const int rest = tile / p.mt;
+  nb = rest % p.nt;
+  b = rest / p.nt;
+}
+
+__device__ __forceinline__ void load_bf16x32(const uint16_t* src, float (&v)[32]) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 w = s4[q];
+    unpack_bf16x2(w.x, v[8 * q + 0], v[8 * q + 1]);
+    unpack_bf16x2(w.y, v[8 * q + 2], v[8 * q + 3]);
+    unpack_bf16x2(w.z, v[8 * q + 4], v[8 * q + 5]);
+    unpack_bf16x2(w.w, v[8 * q + 6], v[8 * q + 7]);
+  }
+}
+
+__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float (&v)[32]) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+    w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+    w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+    w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+    d4[q] = w;
+  }
+}
+
+// Epilogue for 32 consecutive columns n0..n0+31 of row m of output batch b.
+// `full` = all 32 columns are inside N (vector path); else column-by-column.
+__device__ __forceinline__ void epilogue_chunk(const GemmArgs& p, int b, int m, int n0, const uint32_t (&r)[32]) {
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+  const bool full = (n0 + 32 <= p.N);
+  const int ncols = full ? 32 : (p.N - n0);
+
+  if (p.epi == EPI_F32) {
+    float* dst = static_cast<float*>(p.d) + b * p.d_bs + static_cast<int64_t>(m) * p.ldd + n0;
+    if (full) {
+      float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float4 w = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        if (p.accumulate) {
+          const float4 o = d4[q];
+          w.x += o.x; w.y += o.y; w.z += o.z; w.w += o.w;
+        }
+        d4[q] = w;
+      }
+    } else {
+      _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) dst[j] = v[j] + (p.accumulate ? dst[j] : 0.0f);
+    }
+    return;
+  }
+
+  if (p.epi == EPI_BF16) {
+    if (p.bias) {
+      if (full) {
+        float bb[32];
+        load_bf16x32(p.bias + n0, bb);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += bb[j];
+      } else {
+        _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) v[j] += bf16_bits_to_float(p.bias[n0 + j]);
+      }
+    }
+    if (p.res) {
+      const uint16_t* rp = p.res + static_cast<int64_t>(m) * p.ld_res + n0;
+      if (full) {
+        float rr[32];
+        load_bf16x32(rp, rr);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += rr[j];
+      } else {
+        _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) v[j] += bf16_bits_to_float(rp[j]);
+      }
+    }
+  } else if (p.epi == EPI_ACT) {
+    if (p.bias) {
+      const uint16_t* bp = p.bias + b * p.bias_bs + n0;
+      if (full) {
+        float bb[32];
+        load_bf16x32(bp, bb);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += bb[j];
+      } else {
+        _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) v[j] += bf16_bits_to_float(bp[j]);
+      }
+    }
+    if (p.d) {  // save Z for the backward pass
+      uint16_t* zp = static_cast<uint16_t*>(p.d) + b * p.d_bs + static_cast<int64_t>(m) * p.ldd + n0;
+      if (full) store_bf16x32(zp, v);
+      else _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) zp[j] = float_to_bf16_bits(v[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = act_apply(p.act, v[j]);
+    uint16_t* ap = static_cast<uint16_t*>(p.d2) + b * p.d_bs + static_cast<int64_t>(m) * p.ldd + n0;
+    if (full) store_bf16x32(ap, v);
+    else _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) ap[j] = float_to_bf16_bits(v[j]);
+    return;
+  } else {  // EPI_DACT
+    const uint16_t* zp = p.aux + b * p.aux_bs + static_cast<int64_t>(m) * p.ld_aux + n0;
+    if (full) {
+      float z[32];
+      load_bf16x32(zp, z);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] *= act_grad(p.act, z[j]);
+    } else {
+      _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) v[j] *= act_grad(p.act, bf16_bits_to_float(zp[j]));
+    }
+  }
+  uint16_t* dst = static_cast<uint16_t*>(p.d) + b * p.d_bs + static_cast<int64_t>(m) * p.ldd + n0;
+  if (full) store_bf16x32(dst, v);
+  else _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) dst[j] = float_to_bf16_bits(v[j]);
+}
+
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmArgs p) {
+  extern __shared__ uint8_t dsmem[];
+  const uint32_t pad = (1024u - (ptx::smem_addr(dsmem) & 1023u)) & 1023u;
+  uint8_t* base = dsmem + pad;
+  uint8_t* sA = base;
+  uint8_t* sB = base + STAGES * A_TILE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 128);
+    }
+    ptx::mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total = p.nbatch * p.mt * p.nt;
+  const int ksteps = p.nsum * p.kt;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        int b, mb, nb;
+        decode_tile(tile, p, b, mb, nb);
+        for (int ks = 0; ks < ksteps; ++ks) {
+          const int s = ks / p.kt;
+          const int kb = ks - s * p.kt;
+          if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err, ERR_WAIT_PRODUCER, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          const int ash = p.a_sharded ? (p.nsum > 1 ? s : b) : 0;
+          const int bsh = p.b_sharded ? (p.nsum > 1 ? s : b) : 0;
+          uint8_t* a_dst = sA + stage * A_TILE_BYTES;
+          uint8_t* b_dst = sB + stage * B_TILE_BYTES;
+          if (!A_MN) {
+            ptx::tma_load_3d(a_dst, &tmA, &full[stage], kb * BK, mb * BM, ash);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BM / 64; ++j)
+              ptx::tma_load_3d(a_dst + j * MN_CHUNK_BYTES, &tmA, &full[stage], mb * BM + j * 64, kb * BK, ash);
+          }
+          if (!B_MN) {
+            ptx::tma_load_3d(b_dst, &tmB, &full[stage], kb * BK, nb * BN, bsh);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              ptx::tma_load_3d(b_dst + j * MN_CHUNK_BYTES, &tmB, &full[stage], nb * BN + j * 64, kb * BK, bsh);
+          }
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Every copy issued must land before the CTA may exit, also after an abort.
+      volatile int never = 0;
+      for (int s = 0; s < STAGES && s < issued; ++s) {
+        const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+        ptx::mbar_wait(&full[s], par, &never, p.err, ERR_WAIT_DRAIN, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err, ERR_WAIT_MMA, p.timeout_ns)) break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int ks = 0; ks < ksteps; ++ks) {
+          if (!ptx::mbar_wait(&full[stage], phase, abort_flag, p.err, ERR_WAIT_MMA, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a_addr = ptx::smem_addr(sA + stage * A_TILE_BYTES);
+          const uint32_t b_addr = ptx::smem_addr(sB + stage * B_TILE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // K-major: 16 K-elements = 32 bytes inside the 128-byte swizzle row; 8-row groups 1024 B apart.
+            // MN-major: 16 K-rows = two 1024-byte groups; 64-wide MN chunks MN_CHUNK_BYTES apart.
+            const uint64_t ad = A_MN ? ptx::sdesc_sw128(a_addr + kk * 2048, MN_CHUNK_BYTES, 1024)
+                                     : ptx::sdesc_sw128(a_addr + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? ptx::sdesc_sw128(b_addr + kk * 2048, MN_CHUNK_BYTES, 1024)
+                                     : ptx::sdesc_sw128(b_addr + kk * 32, 16, 1024);
+            ptx::mma_bf16(d_tmem, ad, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(&empty[stage]);  // frees this smem stage once its MMAs are done
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(&tfull[acc]);  // accumulator ready for the epilogue
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // No MMA may still be running when TMEM is released.
+      ptx::mma_commit(mma_done);
+      volatile int never = 0;
+      ptx::mbar_wait(mma_done, 0, &never, p.err, ERR_WAIT_DRAIN, p.timeout_ns);
+    }
+  } else {
+    // ----------------------------------------------------------- epilogue
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int b, mb, nb;
+      decode_tile(tile, p, b, mb, nb);
+      if (!ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err, ERR_WAIT_EPI, p.timeout_ns)) break;
+      ptx::tc_fence_after();
+      const int m = mb * BM + row;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int n0 = nb * BN + c * 32;
+        if (n0 >= p.N) break;  // warp-uniform
+        uint32_t r[32];
+        ptx::tmem_ld32(t_row + c * 32, r);
+        ptx::tmem_ld_wait();
+        if (m < p.M) epilogue_chunk(p, b, m, n0, r);
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 3-D map (inner, outer, shard) over a bf16 operand with a 128-byte swizzle.
+// K-major: inner = K, outer = rows, box = 64 x box_rows.
+// MN-major: inner = rows (MN), outer = K, box = 64 x 64.
+bool make_operand_map(CUtensorMap* map, const GemmOperand& op, int64_t rows, int64_t K, int nshards,
+                      int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3];
+  cuuint64_t strides[2];
+  cuuint32_t box[3];
+  cuuint32_t estr[3] = {1, 1, 1};
+  const int64_t outer = op.mn_major ? K : rows;
+  if (!op.mn_major) {
+    dims[0] = static_cast<cuuint64_t>(K);
+    dims[1] = static_cast<cuuint64_t>(rows);
+    box[0] = BK;
+    box[1] = static_cast<cuuint32_t>(box_rows);
+  } else {
+    dims[0] = static_cast<cuuint64_t>(rows);
+    dims[1] = static_cast<cuuint64_t>(K);
+    box[0] = 64;
+    box[1] = BK;
+  }
+  dims[2] = static_cast<cuuint64_t>(nshards);
+  box[2] = 1;
+  strides[0] = static_cast<cuuint64_t>(op.ld) * 2;
+  const int64_t ss = (op.sharded && nshards > 1) ? op.shard_stride : op.ld * outer;
+  strides[1] = static_cast<cuuint64_t>(ss) * 2;
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(op.ptr), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool A_MN, bool B_MN>
+tp_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid, cudaStream_t s) {
+  static bool configured[64] = {};
+  int dev = 0;
+  TP_CUDA_CHECK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return TP_ERR_CUDA;
+  if (!configured[dev]) {
+    TP_CUDA_CHECK(cudaFuncSetAttribute(gemm_kernel<A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SMEM_BYTES));
+    configured[dev] = true;
+  }
+  gemm_kernel<A_MN, B_MN><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, a);
+  TP_CUDA_CHECK(cudaGetLastError());
+  return TP_OK;
+}
+
+bool operand_ok(const GemmOperand& o) {
+  return o.ptr && aligned16(o.ptr) && o.ld > 0 && o.ld % 8 == 0 && (!o.sharded || o.shard_stride % 8 == 0);
+}
+
+}  // namespace
+
+tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
+  if (P.M < 0 || P.N < 0 || P.K < 0 || P.nbatch < 1 || P.nsum < 1) return TP_ERR_INVALID_ARG;
+  if (P.M == 0 || P.N == 0) return TP_OK;
+  if (P.nbatch > 1 && P.nsum > 1) return TP_ERR_INVALID_ARG;
+  if (!operand_ok(P.a) || !operand_ok(P.b)) return TP_ERR_ALIGN;
+  if (P.epi == EPI_ACT) {
+    if (!P.d2 || !aligned16(P.d2) || (P.d && !aligned16(P.d))) return TP_ERR_ALIGN;
+  } else if (!P.d || !aligned16(P.d)) {
+    return TP_ERR_ALIGN;
+  }
+  if (P.ldd % 8 != 0 || P.d_batch_stride % 8 != 0) return TP_ERR_ALIGN;
+  if (P.bias && (!aligned16(P.bias) || P.bias_batch_stride % 8 != 0)) return TP_ERR_ALIGN;
+  if (P.epi == EPI_DACT && (!P.aux || !aligned16(P.aux) || P.ld_aux % 8 != 0 || P.aux_batch_stride % 8 != 0))
+    return TP_ERR_ALIGN;
+  if (P.residual && (!aligned16(P.residual) || P.ld_res % 8 != 0)) return TP_ERR_ALIGN;
+  if (P.K == 0) return TP_ERR_SHAPE;
+  const int64_t mt = (P.M + BM - 1) / BM, nt = (P.N + BN - 1) / BN, kt = (P.K + BK - 1) / BK;
+  if (mt * nt * P.nbatch > (1LL << 30) || P.M > (1LL << 30) || P.N > (1LL << 30)) return TP_ERR_SHAPE;
+  const int nsh_a = P.a.sharded ? (P.nsum > 1 ? P.nsum : P.nbatch) : 1;
+  const int nsh_b = P.b.sharded ? (P.nsum > 1 ? P.nsum : P.nbatch) : 1;
+
+  TP_RETURN_IF(ready());
+  CUtensorMap ta, tb;
+  if (!make_operand_map(&ta, P.a, P.M, P.K, nsh_a, BM)) return TP_ERR_CUDA;
+  if (!make_operand_map(&tb, P.b, P.N, P.K, nsh_b, BN)) return TP_ERR_CUDA;
+
+  GemmArgs a{};
+  a.M = static_cast<int>(P.M);
+  a.N = static_cast<int>(P.N);
+  a.nbatch = P.nbatch;
+  a.nsum = P.nsum;
+  a.a_sharded = P.a.sharded;
+  a.b_sharded = P.b.sharded;
+  a.mt = static_cast<int>(mt);
+  a.nt = static_cast<int>(nt);
+  a.kt = static_cast<int>(kt);
+  a.epi = P.epi;
+  a.act = P.act;
+  a.d = P.d;
+  a.ldd = P.ldd;
+  a.d_bs = P.d_batch_stride;
+  a.d2 = P.d2;
+  a.bias = P.bias;
+  a.bias_bs = P.bias_batch_stride;
+  a.aux = P.aux;
+  a.ld_aux = P.ld_aux;
+  a.aux_bs = P.aux_batch_stride;
+  a.res = P.residual;
+  a.ld_res = P.ld_res;
+  a.accumulate = P.accumulate;
+  a.err = device_error_word();
+  a.timeout_ns = wait_timeout_ns();
+  if (!a.err) return TP_ERR_CUDA;
+
+  const int64_t tiles = mt * nt * P.nbatch;
+  const int grid = static_cast<int>(tiles < device_sm_count() ? tiles : device_sm_count());
+  const bool amn = P.a.mn_major, bmn = P.b.mn_major;
+  if (!amn && !bmn) return launch<false, false>(ta, tb, a, grid, s);
+  if (!amn && bmn) return launch<false, true>(ta, tb, a, grid, s);
+  if (amn && !bmn) return launch<true, false>(ta, tb, a, grid, s);
+  return launch<true, true>(ta, tb, a, grid, s);
+}
+
+}  // namespace tp

@@ -1,0 +1,95 @@
+// Host-side interfaces shared between the translation units of libtpshard.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "tp.h"
+
+namespace tp {
+
+// ------------------------------------------------------------ device state
+int* device_error_word();          // device address of the error word of the current device
+uint64_t wait_timeout_ns();        // limit for every bounded wait in the library's kernels
+int device_sm_count();             // SMs of the current device
+bool device_is_sm103();            // compute capability 10.3
+tp_status ready();                 // TP_OK if the current device can run this library's kernels
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define TP_RETURN_IF(expr)        \
+  do {                            \
+    tp_status _s = (expr);        \
+    if (_s != TP_OK) return _s;   \
+  } while (0)
+
+#define TP_CUDA_CHECK(expr)                      \
+  do {                                           \
+    cudaError_t _e = (expr);                     \
+    if (_e != cudaSuccess) return TP_ERR_CUDA;   \
+  } while (0)
+
+// ----------------------------------------------------------------- GEMM
+// One launch computes, for every output batch b in [0, nbatch):
+//   D[b] (M x N) = sum_{s < nsum} A_sel (M x K) * B_sel (N x K)^T     (fp32 accumulate)
+// where the operand shard selected is (nsum > 1 ? s : b) for a sharded
+// operand and 0 otherwise.  nsum > 1 is the fused shard reduction: the K
+// ranges of the t shards accumulate one after another, in shard order, into
+// the same accumulator.  Operands are bf16 matrices, either K-major (stored
+// [rows][K], K contiguous) or MN-major (stored [K][rows], rows contiguous).
+struct GemmOperand {
+  const uint16_t* ptr = nullptr;
+  int64_t ld = 0;            // elements between consecutive stored rows
+  int64_t shard_stride = 0;  // elements between shards
+  bool sharded = false;
+  bool mn_major = false;
+};
+
+enum GemmEpilogue : int {
+  EPI_BF16 = 0,   // D = bf16(acc + bias[n] + residual[m][n])      (bias/residual nullable)
+  EPI_ACT = 1,    // Z = acc + bias_b[n];  D = bf16(Z) (nullable);  D2 = bf16(act(Z))
+  EPI_DACT = 2,   // D = bf16(acc * act'(aux_b[m][n]))
+  EPI_F32 = 3,    // D = acc (+ D if accumulate), fp32
+};
+
+struct GemmProblem {
+  int64_t M = 0, N = 0, K = 0;
+  int nbatch = 1, nsum = 1;
+  GemmOperand a, b;
+  int epi = EPI_BF16;
+  int act = TP_ACT_IDENTITY;
+  void* d = nullptr;
+  int64_t ldd = 0, d_batch_stride = 0;
+  void* d2 = nullptr;  // EPI_ACT: activation output, same layout as d
+  const uint16_t* bias = nullptr;
+  int64_t bias_batch_stride = 0;
+  const uint16_t* aux = nullptr;  // EPI_DACT: Z
+  int64_t ld_aux = 0, aux_batch_stride = 0;
+  const uint16_t* residual = nullptr;
+  int64_t ld_res = 0;
+  int accumulate = 0;
+};
+
+tp_status run_gemm(const GemmProblem& p, cudaStream_t s);
+
+// ------------------------------------------------------------- others
+tp_status run_colsum(const uint16_t* G, int64_t rows, int64_t cols, int64_t ld, float* out, int accumulate,
+                     float* ws, size_t ws_floats, cudaStream_t s);
+size_t colsum_ws_floats(int64_t rows, int64_t cols);
+tp_status run_colsum_batched(const uint16_t* G, int64_t rows, int64_t cols, int64_t ld, int nbatch,
+                             int64_t batch_stride, float* out, int accumulate, float* ws, size_t ws_floats,
+                             cudaStream_t s);
+tp_status run_shard_reduce(const float* P, int64_t rows, int64_t cols, int t, const uint16_t* bias,
+                           const uint16_t* residual, uint16_t* out_bf16, float* out_f32, cudaStream_t s);
+
+// packing (pack.cu).  dir 0: src unpacked -> dst packed; dir 1: src packed -> dst unpacked.
+tp_status pack_col(const uint16_t* src, int64_t h, int64_t F, int t, uint16_t* dst, int dir, cudaStream_t s);
+tp_status pack_row(const uint16_t* src, int64_t F, int64_t h, int t, uint16_t* dst, int dir, cudaStream_t s);
+tp_status pack_swiglu(const uint16_t* Wg, const uint16_t* Wu, int64_t h, int64_t F, int t, uint16_t* Wp,
+                      cudaStream_t s);
+tp_status pack_qkv(const uint16_t* src, int64_t d, int n_heads, int head_dim, int t, uint16_t* dst, int dir,
+                   cudaStream_t s);
+tp_status pack_qkv_bias(const uint16_t* b, int64_t d, int n_heads, int head_dim, int t, uint16_t* bp,
+                        cudaStream_t s);
+
+}  // namespace tp

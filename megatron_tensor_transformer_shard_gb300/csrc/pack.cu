@@ -1,0 +1,226 @@
+// Shard-layout packing: bit-exact permutations of bf16 weights into the
+// per-shard slices each logical rank owns ("Tensor and sequence parallelism",
+// section "The implementation": rank r keeps w1[cols] and w2[:, cols];
+// "02 — Tensor Parallelism", section "The attention pairing": each rank owns
+// n_heads/t heads of Q, K and V).
+//
+// Every packed layout is a set of output rows, each row r being one column of
+// an unpacked matrix read down a contiguous run of its rows:
+//     packed[r][k] = src_r[(rowbase(r) + k) * ld + col(r)],   0 <= k < row_len
+// so all of them run through one 32x32 shared-memory transpose kernel; the
+// unpack direction is the same map with reads and writes swapped.
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace tp {
+namespace {
+
+enum PackKind : int { PK_COL = 0, PK_ROW = 1, PK_SWIGLU = 2, PK_QKV = 3 };
+
+struct PackMap {
+  int kind;
+  int64_t R;        // packed rows
+  int64_t row_len;  // packed row length
+  int64_t ld;       // row stride of the unpacked source
+  int64_t Ft;       // F/t (COL, ROW, SWIGLU)
+  int64_t h;        // ROW: columns of W_down; SWIGLU: rows of W_gate
+  int64_t d;        // QKV model dim
+  int64_t dt;       // QKV d/t
+  int head_dim;
+  int heads_per_shard;
+  int group;
+};
+
+// Source column and row base for packed row r; `part` selects the source matrix.
+__device__ __forceinline__ void map_row(const PackMap& m, int64_t r, int64_t& col, int64_t& rowbase, int& part) {
+  part = 0;
+  rowbase = 0;
+  switch (m.kind) {
+    case PK_COL:  // [t][F/t][h] == W^T : packed row r is column r of W (h, F)
+      col = r;
+      break;
+    case PK_ROW: {  // [t][h][F/t] : row (i, c) holds W[i*Ft + k][c]
+      const int64_t i = r / m.h;
+      col = r - i * m.h;
+      rowbase = i * m.Ft;
+      break;
+    }
+    case PK_SWIGLU: {  // [t][Ft/g][2][g][h]
+      const int64_t per_shard = 2 * m.Ft;
+      const int64_t i = r / per_shard;
+      const int64_t rem = r - i * per_shard;
+      const int64_t q = rem / (2 * m.group);
+      const int64_t w = rem - q * 2 * m.group;
+      part = static_cast<int>(w / m.group);
+      col = i * m.Ft + q * m.group + (w - part * m.group);
+      break;
+    }
+    default: {  // PK_QKV: [t][3d/t][d], rows [Q_i | K_i | V_i]
+      const int64_t per_shard = 3 * m.dt;
+      const int64_t i = r / per_shard;
+      const int64_t rr = r - i * per_shard;
+      const int64_t p = rr / m.dt;
+      const int64_t w = rr - p * m.dt;
+      const int64_t jj = w / m.head_dim;
+      const int64_t e = w - jj * m.head_dim;
+      col = p * m.d + (i * m.heads_per_shard + jj) * m.head_dim + e;
+      break;
+    }
+  }
+}
+
+constexpr int TILE = 32;
+
+// dir 0: pack (unpacked -> packed); dir 1: unpack.
+__global__ void pack_kernel(PackMap m, int dir, const uint16_t* __restrict__ u0, const uint16_t* __restrict__ u1,
+                            uint16_t* __restrict__ w0, uint16_t* __restrict__ w1, const uint16_t* __restrict__ p_in,
+                            uint16_t* __restrict__ p_out) {
+  __shared__ uint16_t tile[TILE][TILE + 1];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * TILE;
+  const int64_t k0 = static_cast<int64_t>(blockIdx.y) * TILE;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  if (dir == 0) {
+    // read the unpacked source: consecutive tx -> consecutive packed rows -> (mostly) consecutive columns
+    const int64_t r = r0 + tx;
+    if (r < m.R) {
+      int64_t col, rowbase;
+      int part;
+      map_row(m, r, col, rowbase, part);
+      const uint16_t* src = part ? u1 : u0;
+      for (int k = ty; k < TILE; k += blockDim.y) {
+        const int64_t kk = k0 + k;
+        if (kk < m.row_len) tile[k][tx] = src[(rowbase + kk) * m.ld + col];
+      }
+    }
+    __syncthreads();
+    for (int rr = ty; rr < TILE; rr += blockDim.y) {
+      const int64_t r2 = r0 + rr;
+      const int64_t kk = k0 + tx;
+      if (r2 < m.R && kk < m.row_len) p_out[r2 * m.row_len + kk] = tile[tx][rr];
+    }
+  } else {
+    for (int rr = ty; rr < TILE; rr += blockDim.y) {
+      const int64_t r2 = r0 + rr;
+      const int64_t kk = k0 + tx;
+      if (r2 < m.R && kk < m.row_len) tile[tx][rr] = p_in[r2 * m.row_len + kk];
+    }
+    __syncthreads();
+    const int64_t r = r0 + tx;
+    if (r < m.R) {
+      int64_t col, rowbase;
+      int part;
+      map_row(m, r, col, rowbase, part);
+      uint16_t* dst = part ? w1 : w0;
+      for (int k = ty; k < TILE; k += blockDim.y) {
+        const int64_t kk = k0 + k;
+        if (kk < m.row_len) dst[(rowbase + kk) * m.ld + col] = tile[k][tx];
+      }
+    }
+  }
+}
+
+__global__ void gather_bias_kernel(PackMap m, const uint16_t* __restrict__ b, uint16_t* __restrict__ out) {
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (r >= m.R) return;
+  int64_t col, rowbase;
+  int part;
+  map_row(m, r, col, rowbase, part);
+  out[r] = b[col];
+}
+
+tp_status launch_pack(const PackMap& m, int dir, const uint16_t* u0, const uint16_t* u1, uint16_t* w0,
+                      uint16_t* w1, const uint16_t* p_in, uint16_t* p_out, cudaStream_t s) {
+  if (m.R == 0 || m.row_len == 0) return TP_OK;
+  dim3 grid(static_cast<unsigned>((m.R + TILE - 1) / TILE), static_cast<unsigned>((m.row_len + TILE - 1) / TILE));
+  if (grid.y > 65535u) return TP_ERR_SHAPE;
+  TP_RETURN_IF(ready());
+  pack_kernel<<<grid, dim3(TILE, 8), 0, s>>>(m, dir, u0, u1, w0, w1, p_in, p_out);
+  TP_CUDA_CHECK(cudaGetLastError());
+  return TP_OK;
+}
+
+bool bad_t(int64_t n, int t) { return t < 1 || n % t != 0; }
+
+}  // namespace
+
+// dir 0: src = unpacked W, dst = packed; dir 1: src = packed, dst = unpacked W.
+tp_status pack_col(const uint16_t* src, int64_t h, int64_t F, int t, uint16_t* dst, int dir, cudaStream_t s) {
+  if (!src || !dst || h < 0 || F < 0 || t < 1) return TP_ERR_INVALID_ARG;
+  if (bad_t(F, t)) return TP_ERR_SHAPE;
+  PackMap m{};
+  m.kind = PK_COL;
+  m.R = F;
+  m.row_len = h;
+  m.ld = F;
+  m.Ft = F / t;
+  return dir == 0 ? launch_pack(m, 0, src, nullptr, nullptr, nullptr, nullptr, dst, s)
+                  : launch_pack(m, 1, nullptr, nullptr, dst, nullptr, src, nullptr, s);
+}
+
+tp_status pack_row(const uint16_t* src, int64_t F, int64_t h, int t, uint16_t* dst, int dir, cudaStream_t s) {
+  if (!src || !dst || h < 0 || F < 0 || t < 1) return TP_ERR_INVALID_ARG;
+  if (bad_t(F, t)) return TP_ERR_SHAPE;
+  PackMap m{};
+  m.kind = PK_ROW;
+  m.R = static_cast<int64_t>(t) * h;
+  m.row_len = F / t;
+  m.ld = h;
+  m.Ft = F / t;
+  m.h = h;
+  return dir == 0 ? launch_pack(m, 0, src, nullptr, nullptr, nullptr, nullptr, dst, s)
+                  : launch_pack(m, 1, nullptr, nullptr, dst, nullptr, src, nullptr, s);
+}
+
+tp_status pack_swiglu(const uint16_t* Wg, const uint16_t* Wu, int64_t h, int64_t F, int t, uint16_t* Wp,
+                      cudaStream_t s) {
+  if (!Wg || !Wu || !Wp || h < 0 || F < 0 || t < 1) return TP_ERR_INVALID_ARG;
+  if (bad_t(F, t) || (F / t) % 128 != 0) return TP_ERR_SHAPE;
+  PackMap m{};
+  m.kind = PK_SWIGLU;
+  m.R = 2 * F;
+  m.row_len = h;
+  m.ld = F;
+  m.Ft = F / t;
+  m.h = h;
+  m.group = 128;
+  return launch_pack(m, 0, Wg, Wu, nullptr, nullptr, nullptr, Wp, s);
+}
+
+static bool qkv_map(PackMap& m, int64_t d, int n_heads, int head_dim, int t) {
+  if (t < 1 || n_heads < 1 || head_dim < 1 || n_heads % t != 0 || static_cast<int64_t>(n_heads) * head_dim != d)
+    return false;
+  m = PackMap{};
+  m.kind = PK_QKV;
+  m.R = 3 * d;
+  m.row_len = d;
+  m.ld = 3 * d;
+  m.d = d;
+  m.dt = d / t;
+  m.head_dim = head_dim;
+  m.heads_per_shard = n_heads / t;
+  return true;
+}
+
+tp_status pack_qkv(const uint16_t* src, int64_t d, int n_heads, int head_dim, int t, uint16_t* dst, int dir,
+                   cudaStream_t s) {
+  if (!src || !dst || d < 0) return TP_ERR_INVALID_ARG;
+  PackMap m;
+  if (!qkv_map(m, d, n_heads, head_dim, t)) return TP_ERR_SHAPE;
+  return dir == 0 ? launch_pack(m, 0, src, nullptr, nullptr, nullptr, nullptr, dst, s)
+                  : launch_pack(m, 1, nullptr, nullptr, dst, nullptr, src, nullptr, s);
+}
+
+tp_status pack_qkv_bias(const uint16_t* b, int64_t d, int n_heads, int head_dim, int t, uint16_t* bp,
+                        cudaStream_t s) {
+  if (!b || !bp || d < 0) return TP_ERR_INVALID_ARG;
+  PackMap m;
+  if (!qkv_map(m, d, n_heads, head_dim, t)) return TP_ERR_SHAPE;
+  if (m.R == 0) return TP_OK;
+  TP_RETURN_IF(ready());
+  gather_bias_kernel<<<static_cast<unsigned>((m.R + 255) / 256), 256, 0, s>>>(m, b, bp);
+  TP_CUDA_CHECK(cudaGetLastError());
+  return TP_OK;
+}
+
+}  // namespace tp

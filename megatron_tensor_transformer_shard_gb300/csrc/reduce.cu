@@ -1,0 +1,150 @@
+// HBM-bound reductions of the TP block:
+//   shard_reduce  out = sum_{i=0..t-1} P_i + bias (once) + residual -- the
+//                 unfused stand-in for the g / f all-reduce ("Tensor and sequence
+//                 parallelism", f/g table), summing the t partial buffers in
+//                 shard order;
+//   colsum        fixed-order column sums (bias gradients db = sum over rows).
+#include <cuda_runtime.h>
+
+#include "devmath.cuh"
+#include "internal.h"
+
+namespace tp {
+namespace {
+
+constexpr int COLSUM_ROWS_PER_CHUNK = 64;
+constexpr int COLSUM_THREADS = 128;  // x 2 columns each = 256 columns per CTA
+
+// Phase 1: ws[batch][chunk][col] = sum of rows [chunk*64, chunk*64+64) of batch b, in row order.
+__global__ void colsum_partial_kernel(const uint16_t* __restrict__ G, int64_t rows, int64_t cols, int64_t ld,
+                                      int64_t batch_stride, int nchunks, float* __restrict__ ws) {
+  const int64_t c = (static_cast<int64_t>(blockIdx.x) * COLSUM_THREADS + threadIdx.x) * 2;
+  const int chunk = blockIdx.y;
+  const int b = blockIdx.z;
+  if (c >= cols) return;
+  const int64_t r0 = static_cast<int64_t>(chunk) * COLSUM_ROWS_PER_CHUNK;
+  const int64_t r1 = r0 + COLSUM_ROWS_PER_CHUNK < rows ? r0 + COLSUM_ROWS_PER_CHUNK : rows;
+  const uint16_t* g = G + b * batch_stride + c;
+  float s0 = 0.0f, s1 = 0.0f;
+  if (c + 1 < cols) {
+    for (int64_t r = r0; r < r1; ++r) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(g + r * ld);
+      float a, bb;
+      unpack_bf16x2(w, a, bb);
+      s0 += a;
+      s1 += bb;
+    }
+  } else {
+    for (int64_t r = r0; r < r1; ++r) s0 += bf16_bits_to_float(g[r * ld]);
+  }
+  float* o = ws + (static_cast<int64_t>(b) * nchunks + chunk) * cols + c;
+  o[0] = s0;
+  if (c + 1 < cols) o[1] = s1;
+}
+
+// Phase 2: out[b*cols + c] (+)= sum_{chunk} ws[b][chunk][c], chunks in order.
+__global__ void colsum_final_kernel(const float* __restrict__ ws, int64_t cols, int nchunks, int nbatch,
+                                    float* __restrict__ out, int accumulate) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= cols * nbatch) return;
+  const int64_t b = idx / cols, c = idx - b * cols;
+  const float* w = ws + b * nchunks * cols + c;
+  float s = 0.0f;
+  for (int k = 0; k < nchunks; ++k) s += w[static_cast<int64_t>(k) * cols];
+  out[idx] = accumulate ? out[idx] + s : s;
+}
+
+__global__ void shard_reduce_kernel(const float* __restrict__ P, int64_t rows, int64_t cols, int t,
+                                    const uint16_t* __restrict__ bias, const uint16_t* __restrict__ res,
+                                    uint16_t* __restrict__ out_bf16, float* __restrict__ out_f32) {
+  const int64_t n4 = rows * cols / 4;
+  const int64_t shard = rows * cols;
+  for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q < n4;
+       q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e = q * 4;
+    float4 acc = reinterpret_cast<const float4*>(P + e)[0];
+    for (int i = 1; i < t; ++i) {  // fixed shard order
+      const float4 v = reinterpret_cast<const float4*>(P + i * shard + e)[0];
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    const int64_t c = e % cols;
+    if (bias) {
+      acc.x += bf16_bits_to_float(bias[c]);
+      acc.y += bf16_bits_to_float(bias[c + 1]);
+      acc.z += bf16_bits_to_float(bias[c + 2]);
+      acc.w += bf16_bits_to_float(bias[c + 3]);
+    }
+    if (res) {
+      acc.x += bf16_bits_to_float(res[e]);
+      acc.y += bf16_bits_to_float(res[e + 1]);
+      acc.z += bf16_bits_to_float(res[e + 2]);
+      acc.w += bf16_bits_to_float(res[e + 3]);
+    }
+    if (out_f32) reinterpret_cast<float4*>(out_f32 + e)[0] = acc;
+    if (out_bf16) {
+      uint2 w;
+      w.x = pack_bf16x2(acc.x, acc.y);
+      w.y = pack_bf16x2(acc.z, acc.w);
+      reinterpret_cast<uint2*>(out_bf16 + e)[0] = w;
+    }
+  }
+}
+
+}  // namespace
+
+size_t colsum_ws_floats(int64_t rows, int64_t cols) {
+  const int64_t nchunks = (rows + COLSUM_ROWS_PER_CHUNK - 1) / COLSUM_ROWS_PER_CHUNK;
+  return static_cast<size_t>(nchunks > 0 ? nchunks : 1) * static_cast<size_t>(cols);
+}
+
+// Column sums of `nbatch` matrices [rows][cols] (row stride ld, batch stride
+// rows*ld) -> out[nbatch][cols].  ws must hold nbatch * colsum_ws_floats(rows, cols).
+tp_status run_colsum_batched(const uint16_t* G, int64_t rows, int64_t cols, int64_t ld, int nbatch,
+                             int64_t batch_stride, float* out, int accumulate, float* ws, size_t ws_floats,
+                             cudaStream_t s) {
+  if (rows < 0 || cols < 0 || nbatch < 1) return TP_ERR_INVALID_ARG;
+  if (cols == 0) return TP_OK;
+  if (!G || !out || !ws) return TP_ERR_INVALID_ARG;
+  if ((cols & 1) || (ld & 1) || (batch_stride & 1) || (reinterpret_cast<uintptr_t>(G) & 3)) return TP_ERR_ALIGN;
+  const int nchunks = static_cast<int>((rows + COLSUM_ROWS_PER_CHUNK - 1) / COLSUM_ROWS_PER_CHUNK);
+  if (ws_floats < colsum_ws_floats(rows, cols) * static_cast<size_t>(nbatch)) return TP_ERR_WORKSPACE;
+  TP_RETURN_IF(ready());
+  if (nchunks == 0) {
+    if (!accumulate) TP_CUDA_CHECK(cudaMemsetAsync(out, 0, sizeof(float) * cols * nbatch, s));
+    return TP_OK;
+  }
+  dim3 g1(static_cast<unsigned>((cols / 2 + COLSUM_THREADS - 1) / COLSUM_THREADS), nchunks, nbatch);
+  colsum_partial_kernel<<<g1, COLSUM_THREADS, 0, s>>>(G, rows, cols, ld, batch_stride, nchunks, ws);
+  TP_CUDA_CHECK(cudaGetLastError());
+  const int64_t n = cols * nbatch;
+  colsum_final_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(ws, cols, nchunks, nbatch, out,
+                                                                             accumulate);
+  TP_CUDA_CHECK(cudaGetLastError());
+  return TP_OK;
+}
+
+tp_status run_colsum(const uint16_t* G, int64_t rows, int64_t cols, int64_t ld, float* out, int accumulate,
+                     float* ws, size_t ws_floats, cudaStream_t s) {
+  return run_colsum_batched(G, rows, cols, ld, 1, rows * ld, out, accumulate, ws, ws_floats, s);
+}
+
+tp_status run_shard_reduce(const float* P, int64_t rows, int64_t cols, int t, const uint16_t* bias,
+                           const uint16_t* residual, uint16_t* out_bf16, float* out_f32, cudaStream_t s) {
+  if (rows < 0 || cols < 0 || t < 1) return TP_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return TP_OK;
+  if (!P || (!out_bf16 && !out_f32)) return TP_ERR_INVALID_ARG;
+  if (cols % 8 != 0 || !aligned16(P) || (out_f32 && !aligned16(out_f32)) || (out_bf16 && !aligned16(out_bf16)) ||
+      (residual && !aligned16(residual)) || (bias && !aligned16(bias)))
+    return TP_ERR_ALIGN;
+  TP_RETURN_IF(ready());
+  const int64_t n4 = rows * cols / 4;
+  int64_t blocks = (n4 + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  shard_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(P, rows, cols, t, bias, residual, out_bf16,
+                                                                     out_f32);
+  TP_CUDA_CHECK(cudaGetLastError());
+  return TP_OK;
+}
+
+}  // namespace tp

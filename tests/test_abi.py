@@ -1,0 +1,79 @@
+"""The C-ABI library loads, exports every symbol include/*.h declares, the
+Python binding covers exactly those, and host-side argument validation
+returns the documented status codes before any device work (no GPU needed)."""
+
+import glob
+import os
+import re
+
+import pytest
+
+from megatron_tensor_transformer_shard_gb300 import _lib as L
+from megatron_tensor_transformer_shard_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_lib():
+    B.build()
+    return L.lib()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"^[A-Za-z_][\w \*]*?\b(tp_\w+)\s*\(", src, flags=re.M))
+    return names
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert len(names) >= 15
+    lib = L.lib()
+    missing = [n for n in sorted(names) if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_header():
+    assert declared_functions() == set(L.SIGNATURES)
+
+
+def test_version_and_strings():
+    assert L.tp_abi_version() == 1
+    for code in range(8):
+        assert L.status_string(code).startswith(("TP_OK", "TP_ERR"))
+
+
+def test_workspace_sizes():
+    assert L.tp_mlp_workspace_size(2048, 4096, 16384, 4, 0) == 0
+    assert L.tp_mlp_workspace_size(2048, 4096, 16384, 4, L.TP_FLAG_UNFUSED_REDUCE) == 4 * 2048 * 4096 * 4
+    assert L.tp_mlp_backward_workspace_size(2048, 4096, 16384, 4, 0) >= 2048 * 16384 * 2
+    assert L.tp_colsum_workspace_size(2048, 4096) == 32 * 4096 * 4
+
+
+def test_host_validation_without_device():
+    c = dict(check=False, stream=0)
+    # null input with tokens to process
+    assert L.tp_mlp_forward(None, 4, 64, 128, 2, 2, 16, None, 16, None, None, 16, None, 16, 0, None, 0, **c) \
+        == L.TP_ERR_INVALID_ARG
+    # t does not divide F
+    assert L.tp_mlp_forward(16, 4, 64, 128, 3, 2, 16, None, 16, None, None, 16, None, 16, 0, None, 0, **c) \
+        == L.TP_ERR_SHAPE
+    # hidden size not a multiple of 8
+    assert L.tp_mlp_forward(16, 4, 60, 128, 2, 2, 16, None, 16, None, None, 16, None, 16, 0, None, 0, **c) \
+        == L.TP_ERR_ALIGN
+    # unknown activation
+    assert L.tp_mlp_forward(16, 4, 64, 128, 2, 9, 16, None, 16, None, None, 16, None, 16, 0, None, 0, **c) \
+        == L.TP_ERR_INVALID_ARG
+    # no tokens: nothing to do
+    assert L.tp_mlp_forward(None, 0, 64, 128, 2, 2, None, None, None, None, None, None, None, None, 0, None, 0,
+                            **c) == L.TP_OK
+    # unfused reduction without workspace
+    assert L.tp_mlp_forward(16, 4, 64, 128, 2, 2, 16, None, 16, None, None, 16, None, 16,
+                            L.TP_FLAG_UNFUSED_REDUCE, None, 0, **c) == L.TP_ERR_WORKSPACE
+    # packing: t does not divide F
+    assert L.tp_pack_col(16, 64, 100, 3, 16, **c) == L.TP_ERR_SHAPE
+    assert L.tp_pack_qkv_heads(16, 96, 4, 16, 2, 16, **c) == L.TP_ERR_SHAPE
+    assert L.tp_selftest_bounded_wait(0, **c) == L.TP_ERR_INVALID_ARG

@@ -1,0 +1,297 @@
+"""GPU parity of the TP MLP (packing, forward, backward) against the fp64
+oracle, through the C ABI.
+
+Criterion: bit-exact for packing; max|gpu - oracle| <= 1e-2 * max|oracle| per
+floating-point output tensor.  Sizes span several 128x256 output tiles with
+ragged tails in M, N and K (and the full-size workloads on sampled outputs).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from megatron_tensor_transformer_shard_gb300 import _lib as L
+from megatron_tensor_transformer_shard_gb300 import inputs as I
+from megatron_tensor_transformer_shard_gb300 import tp as T
+
+from gpu_helpers import assert_close, f64, ws_bytes
+
+pytestmark = pytest.mark.gpu
+
+
+def _rand_bits(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randint(0, 65536, shape, generator=g, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+
+
+# ---------------------------------------------------------------- packing
+
+@pytest.mark.parametrize("h,F,t", [(64, 256, 4), (40, 48, 2), (1024, 4096, 2), (136, 1024, 8)])
+def test_pack_col_row_bit_exact(h, F, t):
+    W = _rand_bits((h, F), 1)
+    Wd = _rand_bits((F, h), 2)
+    Wp = torch.empty(t, F // t, h, dtype=torch.bfloat16, device="cuda")
+    Wdp = torch.empty(t, h, F // t, dtype=torch.bfloat16, device="cuda")
+    L.tp_pack_col(W.cuda(), h, F, t, Wp)
+    L.tp_pack_row(Wd.cuda(), F, h, t, Wdp)
+    assert np.array_equal(I.bits(Wp.cpu()), O.pack_col_weight(I.bits(W), t))
+    assert np.array_equal(I.bits(Wdp.cpu()), O.pack_row_weight(I.bits(Wd), t))
+    back = torch.empty(h, F, dtype=torch.bfloat16, device="cuda")
+    L.tp_unpack_col(Wp, h, F, t, back)
+    assert np.array_equal(I.bits(back.cpu()), I.bits(W))
+    backd = torch.empty(F, h, dtype=torch.bfloat16, device="cuda")
+    L.tp_unpack_row(Wdp, F, h, t, backd)
+    assert np.array_equal(I.bits(backd.cpu()), I.bits(Wd))
+
+
+def test_pack_reshard_t_to_t_prime():
+    h, F = 128, 1024
+    W = _rand_bits((h, F), 3).cuda()
+    p4 = torch.empty(4, F // 4, h, dtype=torch.bfloat16, device="cuda")
+    L.tp_pack_col(W, h, F, 4, p4)
+    un = torch.empty(h, F, dtype=torch.bfloat16, device="cuda")
+    L.tp_unpack_col(p4, h, F, 4, un)
+    p8 = torch.empty(8, F // 8, h, dtype=torch.bfloat16, device="cuda")
+    L.tp_pack_col(un, h, F, 8, p8)
+    assert np.array_equal(I.bits(p8.cpu()), O.pack_col_weight(I.bits(W.cpu()), 8))
+
+
+@pytest.mark.parametrize("h,F,t", [(64, 512, 2), (96, 1024, 4)])
+def test_pack_swiglu_bit_exact(h, F, t):
+    Wg, Wu = _rand_bits((h, F), 4), _rand_bits((h, F), 5)
+    out = torch.empty(2 * F, h, dtype=torch.bfloat16, device="cuda")
+    L.tp_pack_swiglu(Wg.cuda(), Wu.cuda(), h, F, t, out)
+    ref = O.pack_swiglu_weight(I.bits(Wg), I.bits(Wu), t, 128).reshape(2 * F, h)
+    assert np.array_equal(I.bits(out.cpu()), ref)
+
+
+@pytest.mark.parametrize("nh,dh,t", [(4, 16, 2), (8, 128, 8), (6, 64, 3)])
+def test_pack_qkv_bit_exact(nh, dh, t):
+    d = nh * dh
+    W = _rand_bits((d, 3 * d), 6)
+    b = _rand_bits((3 * d,), 7)
+    Wp = torch.empty(t, 3 * d // t, d, dtype=torch.bfloat16, device="cuda")
+    bp = torch.empty(t, 3 * d // t, dtype=torch.bfloat16, device="cuda")
+    L.tp_pack_qkv_heads(W.cuda(), d, nh, dh, t, Wp)
+    L.tp_pack_qkv_bias(b.cuda(), d, nh, dh, t, bp)
+    assert np.array_equal(I.bits(Wp.cpu()), O.pack_qkv_weight(I.bits(W), nh, dh, t))
+    assert np.array_equal(I.bits(bp.cpu()), O.pack_qkv_bias(I.bits(b), nh, dh, t))
+    back = torch.empty(d, 3 * d, dtype=torch.bfloat16, device="cuda")
+    L.tp_unpack_qkv_heads(Wp, d, nh, dh, t, back)
+    assert np.array_equal(I.bits(back.cpu()), I.bits(W))
+
+
+# ---------------------------------------------------------------- MLP
+
+def _case(M, h, F, t, seed=0, bias=True):
+    inp = I.mlp_inputs(M, h, F, bias=bias, dy=True, seed=seed)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    ref = {k: (f64(v) if v is not None else None) for k, v in inp.items()}
+    w = T.MLPWeights(dev["W_up"], dev["b_up"], dev["W_down"], dev["b_down"], t)
+    return dev, ref, w
+
+
+SHAPES = [
+    (128, 1024, 4096, 2),   # the forward-only workload, full size
+    (200, 264, 784, 2),     # ragged M, N (F/t = 392) and K (h = 264)
+    (1, 64, 128, 4),        # a single token
+    (300, 512, 2048, 8),
+    (257, 128, 1536, 4),
+]
+
+
+@pytest.mark.parametrize("M,h,F,t", SHAPES)
+def test_mlp_forward_parity(M, h, F, t):
+    dev, ref, w = _case(M, h, F, t)
+    Y, Z, A = T.mlp_forward(dev["X"], w, "gelu_tanh")
+    torch.cuda.synchronize()
+    o = O.mlp_forward_sharded(ref["X"], ref["W_up"], ref["b_up"], ref["W_down"], ref["b_down"], "gelu_tanh", t)
+    assert_close("Y", f64(Y), o["Y"])
+    assert_close("Z", f64(Z), np.stack(o["Z"]))
+    assert_close("A", f64(A), np.stack(o["A"]))
+    assert L.tp_get_device_status(check=False) == L.TP_OK
+
+
+@pytest.mark.parametrize("act", ["identity", "relu", "gelu_tanh", "gelu_erf"])
+def test_mlp_forward_activations(act):
+    M, h, F, t = 192, 256, 1024, 4
+    dev, ref, w = _case(M, h, F, t, seed=1)
+    Y, Z, A = T.mlp_forward(dev["X"], w, act)
+    o = O.mlp_forward_sharded(ref["X"], ref["W_up"], ref["b_up"], ref["W_down"], ref["b_down"], act, t)
+    assert_close("Y", f64(Y), o["Y"])
+    assert_close("A", f64(A), np.stack(o["A"]))
+
+
+def test_mlp_forward_residual_and_no_bias():
+    M, h, F, t = 130, 256, 512, 2
+    dev, ref, w = _case(M, h, F, t, seed=2, bias=False)
+    R = torch.randn(M, h, generator=torch.Generator().manual_seed(9)).to(torch.bfloat16)
+    Y, _, _ = T.mlp_forward(dev["X"], w, "gelu_tanh", residual=R.cuda(), save_z=False)
+    o = O.mlp_forward_sharded(ref["X"], ref["W_up"], None, ref["W_down"], None, "gelu_tanh", t)
+    assert_close("Y", f64(Y), o["Y"] + f64(R))
+
+
+@pytest.mark.parametrize("M,h,F,t", [(200, 264, 784, 2), (256, 512, 2048, 4)])
+def test_unfused_partials_match_oracle(M, h, F, t):
+    """TP_FLAG_UNFUSED_REDUCE writes each shard's partial P_i; check every P_i
+    and the reduced output against the oracle, and against the fused path."""
+    dev, ref, w = _case(M, h, F, t, seed=3)
+    flags = L.TP_FLAG_UNFUSED_REDUCE
+    nws = L.tp_mlp_workspace_size(M, h, F, t, flags)
+    assert nws == t * M * h * 4
+    ws = torch.empty(t, M, h, dtype=torch.float32, device="cuda")
+    Y = torch.empty(M, h, dtype=torch.bfloat16, device="cuda")
+    A = torch.empty(t, M, F // t, dtype=torch.bfloat16, device="cuda")
+    L.tp_mlp_forward(dev["X"], M, h, F, t, L.TP_ACT_GELU_TANH, w.Wup_p, w.b_up, w.Wdown_p, w.b_down, None, Y,
+                     None, A, flags, ws, nws)
+    o = O.mlp_forward_sharded(ref["X"], ref["W_up"], ref["b_up"], ref["W_down"], ref["b_down"], "gelu_tanh", t)
+    for i in range(t):
+        assert_close(f"P_{i}", f64(ws[i]), o["P"][i])
+    assert_close("Y", f64(Y), o["Y"])
+    Yf, _, _ = T.mlp_forward(dev["X"], w, "gelu_tanh")
+    assert_close("fused vs unfused", f64(Yf), f64(Y))
+
+
+def test_bias_added_once_on_gpu():
+    """Zero weights: Y must equal b_down exactly once (not t times)."""
+    M, h, F, t = 64, 128, 512, 4
+    X = torch.randn(M, h).to(torch.bfloat16).cuda()
+    Wu = torch.zeros(h, F, dtype=torch.bfloat16, device="cuda")
+    Wd = torch.zeros(F, h, dtype=torch.bfloat16, device="cuda")
+    bu = torch.zeros(F, dtype=torch.bfloat16, device="cuda")
+    bd = torch.randn(h).to(torch.bfloat16).cuda()
+    w = T.MLPWeights(Wu, bu, Wd, bd, t)
+    for flags in (0, L.TP_FLAG_UNFUSED_REDUCE):
+        Y, _, _ = T.mlp_forward(X, w, "gelu_tanh", flags=flags)
+        assert torch.equal(Y, bd.expand(M, h)), flags
+
+
+def test_mlp_zero_tokens():
+    dev, ref, w = _case(8, 64, 256, 2)
+    Y = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
+    A = torch.empty(2, 0, 128, dtype=torch.bfloat16, device="cuda")
+    L.tp_mlp_forward(dev["X"], 0, 64, 256, 2, 2, w.Wup_p, w.b_up, w.Wdown_p, w.b_down, None, Y, None, A, 0, None, 0)
+
+
+def _backward_check(M, h, F, t, act, seed, flags=0):
+    dev, ref, w = _case(M, h, F, t, seed=seed)
+    Y, Z, A = T.mlp_forward(dev["X"], w, act)
+    g = T.mlp_backward(dev["dY"], dev["X"], Z, A, w, act, flags=flags)
+    torch.cuda.synchronize()
+    o = O.mlp_forward_sharded(ref["X"], ref["W_up"], ref["b_up"], ref["W_down"], ref["b_down"], act, t)
+    b = O.mlp_backward_sharded(ref["dY"], ref["X"], ref["W_up"], ref["W_down"], o, act, t)
+    assert_close("dX", f64(g["dX"]), b["dX"])
+    assert_close("dW_up (packed)", f64(g["dWup_p"]), O.pack_col_weight(b["dW_up"], t))
+    assert_close("dW_down (packed)", f64(g["dWdown_p"]), O.pack_row_weight(b["dW_down"], t))
+    assert_close("db_up", f64(g["dbup"]), b["db_up"])
+    assert_close("db_down", f64(g["dbdown"]), b["db_down"])
+    return dev, w, g, (Y, Z, A)
+
+
+@pytest.mark.parametrize("M,h,F,t", [(200, 264, 784, 2), (256, 512, 2048, 4), (130, 128, 1024, 8)])
+def test_mlp_backward_parity(M, h, F, t):
+    _backward_check(M, h, F, t, "gelu_tanh", seed=4)
+
+
+@pytest.mark.parametrize("act", ["identity", "relu", "gelu_erf"])
+def test_mlp_backward_activations(act):
+    _backward_check(192, 256, 1024, 4, act, seed=5)
+
+
+def test_mlp_backward_unfused_and_accumulate():
+    M, h, F, t = 256, 256, 1024, 4
+    dev, w, g, (Y, Z, A) = _backward_check(M, h, F, t, "gelu_tanh", seed=6, flags=L.TP_FLAG_UNFUSED_REDUCE)
+    g2 = T.mlp_backward(dev["dY"], dev["X"], Z, A, w, "gelu_tanh")
+    assert_close("fused dX vs unfused", f64(g2["dX"]), f64(g["dX"]))
+    base = {k: g2[k].clone() for k in ("dWup_p", "dWdown_p", "dbup", "dbdown")}
+    g3 = T.mlp_backward(dev["dY"], dev["X"], Z, A, w, "gelu_tanh", grads={k: v.clone() for k, v in base.items()})
+    for k in base:
+        assert_close(k + " accumulated", f64(g3[k]), 2 * f64(base[k]))
+
+
+def test_autograd_function():
+    M, h, F, t = 128, 256, 1024, 2
+    dev, ref, w = _case(M, h, F, t, seed=7)
+    X = dev["X"].clone().requires_grad_()
+    Y = T.TPMLPFunction.apply(X, w, "gelu_tanh")
+    Y.backward(dev["dY"])
+    o = O.mlp_forward_sharded(ref["X"], ref["W_up"], ref["b_up"], ref["W_down"], ref["b_down"], "gelu_tanh", t)
+    b = O.mlp_backward_sharded(ref["dY"], ref["X"], ref["W_up"], ref["W_down"], o, "gelu_tanh", t)
+    assert_close("Y", f64(Y), o["Y"])
+    assert_close("dX", f64(X.grad), b["dX"])
+    assert_close("dW_up", f64(w.grads["dWup_p"]), O.pack_col_weight(b["dW_up"], t))
+
+
+# ------------------------------------------------ full-size workloads (sampled)
+
+def _rows(M, n=12):
+    return sorted(set([0, 1, 127, 128, M // 2, M - 129, M - 1] + list(np.random.default_rng(0).integers(0, M, n))))
+
+
+@pytest.mark.slow
+def test_full_size_fwd_bwd_sampled():
+    """The 2048x4096 -> 16384, t = 4 forward+backward in the launch configuration
+    the bench times; compared on sampled rows of Y and dX and sampled rows /
+    columns of the weight gradients, each computed by the oracle one by one."""
+    cfg = I.CONFIGS["c2"]
+    M, h, F, t = cfg["M"], cfg["h"], cfg["F"], cfg["t"]
+    inp = I.mlp_inputs(M, h, F, bias=True, dy=True, seed=0)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    w = T.MLPWeights(dev["W_up"], dev["b_up"], dev["W_down"], dev["b_down"], t)
+    Y, Z, A = T.mlp_forward(dev["X"], w, "gelu_tanh")
+    g = T.mlp_backward(dev["dY"], dev["X"], Z, A, w, "gelu_tanh")
+    torch.cuda.synchronize()
+    assert L.tp_get_device_status(check=False) == L.TP_OK
+    X, Wu, bu, Wd, bd, G = (f64(inp[k]) for k in ("X", "W_up", "b_up", "W_down", "b_down", "dY"))
+    rows = _rows(M)
+    o = O.mlp_forward_sharded(X[rows], Wu, bu, Wd, bd, "gelu_tanh", t)
+    assert_close("Y rows", f64(Y[rows]), o["Y"])
+    b = O.mlp_backward_sharded(G[rows], X[rows], Wu, Wd, o, "gelu_tanh", t)
+    assert_close("dX rows", f64(g["dX"][rows]), b["dX"])
+    # weight-gradient columns need every token: pick a few hidden units f
+    fs = [0, 1, 255, 256, F // t - 1, F // t, F // 2 + 7, F - 1]
+    Zc = X @ Wu[:, fs] + bu[fs]
+    dZc = (G @ Wd[fs, :].T) * O.act_grad("gelu_tanh", Zc)
+    dWu_cols = X.T @ dZc                               # dW_up[:, f]
+    Ac = O.act("gelu_tanh", Zc)
+    dWd_rows = Ac.T @ G                                # dW_down[f, :]
+    Ft = F // t
+    gu = g["dWup_p"].reshape(F, h)                     # packed [t][Ft][h] == dW_up^T
+    gd = g["dWdown_p"].cpu()                           # [t][h][Ft]
+    got_u = f64(gu[fs]).T
+    got_d = np.stack([f64(gd[f // Ft, :, f % Ft]) for f in fs])
+    assert_close("dW_up columns", got_u, dWu_cols)
+    assert_close("dW_down rows", got_d, dWd_rows)
+    assert_close("db_up sampled", f64(g["dbup"])[fs], dZc.sum(axis=0))
+    assert_close("db_down", f64(g["dbdown"]), G.sum(axis=0))
+
+
+# ---------------------------------------------------------------- failure paths
+
+def test_bounded_wait_timeout_reported_and_context_survives():
+    assert L.tp_get_device_status(check=False) == L.TP_OK
+    L.tp_selftest_bounded_wait(20000)   # 20 ms
+    assert L.tp_get_device_status(check=False) == L.TP_ERR_TIMEOUT
+    assert L.tp_get_device_status(check=False) == L.TP_OK   # cleared
+    dev, ref, w = _case(64, 128, 256, 2)
+    Y, _, _ = T.mlp_forward(dev["X"], w, "gelu_tanh")
+    o = O.mlp_forward_sharded(ref["X"], ref["W_up"], ref["b_up"], ref["W_down"], ref["b_down"], "gelu_tanh", 2)
+    assert_close("Y after timeout", f64(Y), o["Y"])
+
+
+def test_host_validation_on_device():
+    dev, ref, w = _case(64, 128, 256, 2)
+    Y = torch.empty(64, 128, dtype=torch.bfloat16, device="cuda")
+    A = torch.empty(2, 64, 128, dtype=torch.bfloat16, device="cuda")
+    base = dev["X"].data_ptr()
+    r = L.tp_mlp_forward(base + 2, 64, 128, 256, 2, 2, w.Wup_p, w.b_up, w.Wdown_p, w.b_down, None, Y, None, A, 0,
+                         None, 0, check=False)
+    assert r == L.TP_ERR_ALIGN
+    r = L.tp_mlp_forward(dev["X"], 64, 128, 256, 3, 2, w.Wup_p, w.b_up, w.Wdown_p, w.b_down, None, Y, None, A, 0,
+                         None, 0, check=False)
+    assert r == L.TP_ERR_SHAPE
+    small = ws_bytes(16)
+    r = L.tp_mlp_forward(dev["X"], 64, 128, 256, 2, 2, w.Wup_p, w.b_up, w.Wdown_p, w.b_down, None, Y, None, A,
+                         L.TP_FLAG_UNFUSED_REDUCE, small, 16, check=False)
+    assert r == L.TP_ERR_WORKSPACE
