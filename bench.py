@@ -1,0 +1,452 @@
+#!/usr/bin/env python3
+"""Benchmark of the TP-MLP block forward+backward on one GB300 (t logical shards).
+
+Workload (one "step"): the 2048-token TP MLP with h = 4096, F = 16384, t = 4,
+GeLU(tanh), biases -- column-parallel GEMM + activation, row-parallel GEMM with
+the fused g reduction, then the backward (dgrad with act', both wgrads, the f
+reduction of dX, bias grads) -- on synthetic seeded bf16 inputs resident in
+HBM.  FLOPs counted: the six GEMMs, 12 * M * h * F = 1.649e12 per step.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
+instead (the only other arm: the pages publish no implementation).  Under
+torchrun with N > 1 every rank runs an independent replica on its own GPU
+(the t shards are logical and live on one GPU, so there is nothing to
+exchange between GPUs); value = all ranks' work / max-over-ranks time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "TP-MLP block fwd+bwd TFLOP/s on 1 GB300 (t logical shards), % of bf16 peak"
+UNIT = "TFLOP/s"
+WORKLOAD = "c2"
+
+
+def flops_per_step(M, h, F):
+    return 12.0 * M * h * F
+
+
+# --------------------------------------------------------------------- ranks
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def init_dist(world):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group("gloo")
+    return dist
+
+
+def reduce_max(dist, value):
+    """Max over ranks of one float (host-side, gloo)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def aggregate(units_per_rank, seconds_max, world):
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    return units_per_rank * world / seconds_max
+
+
+# -------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling in the background; each line is stamped on arrival."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id=None):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if gpu_id:
+            cmd[1:1] = ["-i", gpu_id]
+        self.samples = []
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 7:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        window = [p for ts, p in self.samples if t0 - 0.15 <= ts <= t1 + 0.15]
+        if not window:   # timed region shorter than the sampling period: nearest samples under load
+            window = [min(self.samples, key=lambda s: abs(s[0] - (t0 + t1) / 2))[1]]
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in window if num(p[0]) is not None]
+        mx = [num(p[1]) for p in window if num(p[1]) is not None]
+        reasons = sorted({n for p in window for n, v in zip(self.NAMES, p[3:7]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(window)}
+
+
+# -------------------------------------------------------------- peaks, traffic
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return {"bf16_burst": float(d["bf16_tflops"]), "bf16_sustained": float(d["bf16_tflops_sustained"]),
+                "hbm": float(d["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
+
+
+def gemm_source_hash():
+    h = hashlib.sha256()
+    for name in ("gemm.cu", "ptx.cuh", "devmath.cuh"):
+        with open(os.path.join(ROOT, "megatron_tensor_transformer_shard_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(profile_name):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    kv[k.strip().lstrip("- ").strip("`")] = v.strip().strip("`")
+        if kv.get("source_sha") != gemm_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch_full_size"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    dist = init_dist(world)
+    torch.cuda.set_device(local)
+    from megatron_tensor_transformer_shard_gb300 import build as B
+    B.build()
+    from megatron_tensor_transformer_shard_gb300 import _lib as L
+    from megatron_tensor_transformer_shard_gb300 import inputs as I
+
+    cfg = I.CONFIGS[WORKLOAD]
+    M, h, F, t, act = cfg["M"], cfg["h"], cfg["F"], cfg["t"], L.ACT_BY_NAME[cfg["act"]]
+    Ft = F // t
+    dev = "cuda"
+    # Seeded synthetic inputs drawn on the device (same distributions as the parity tests).
+    inp = I.mlp_inputs(M, h, F, bias=True, dy=True, seed=rank, device=dev)
+    bf16, f32 = torch.bfloat16, torch.float32
+    Wup_p = torch.empty(t, Ft, h, dtype=bf16, device=dev)
+    Wdown_p = torch.empty(t, h, Ft, dtype=bf16, device=dev)
+    L.tp_pack_col(inp["W_up"], h, F, t, Wup_p)
+    L.tp_pack_row(inp["W_down"], F, h, t, Wdown_p)
+    X, dY, bup, bdown = inp["X"], inp["dY"], inp["b_up"], inp["b_down"]
+    del inp["W_up"], inp["W_down"]
+    Y = torch.empty(M, h, dtype=bf16, device=dev)
+    Z = torch.empty(t, M, Ft, dtype=bf16, device=dev)
+    A = torch.empty_like(Z)
+    dX = torch.empty(M, h, dtype=bf16, device=dev)
+    dWup = torch.empty(t, Ft, h, dtype=f32, device=dev)
+    dWdown = torch.empty(t, h, Ft, dtype=f32, device=dev)
+    dbup = torch.empty(F, dtype=f32, device=dev)
+    dbdown = torch.empty(h, dtype=f32, device=dev)
+    nws = L.tp_mlp_backward_workspace_size(M, h, F, t, 0)
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+
+    col_ev = []
+
+    def step(record=False):
+        if record:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+        # forward: f (identity) + column-parallel GEMM + GeLU, then row-parallel GEMM + g (bias once)
+        L.tp_column_parallel_forward(X, M, h, F, t, act, Wup_p, bup, Z, A)
+        if record:
+            e1.record()
+            col_ev.append((e0, e1))
+        L.tp_row_parallel_forward(A, M, F, h, t, Wdown_p, bdown, None, Y)
+        # backward: g (identity), dgrad*act', wgrads, f (fused dX reduction), bias grads
+        L.tp_mlp_backward(dY, X, Z, A, M, h, F, t, act, Wup_p, Wdown_p, dX, dWup, dWdown, dbup, dbdown, 0, 0,
+                          ws, nws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if L.tp_get_device_status(check=False) != L.TP_OK:
+        raise RuntimeError("device error during warm-up")
+
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(gpu_id) if rank == 0 else None
+    time.sleep(0.3 if clocks else 0)
+
+    stream = torch.cuda.current_stream()
+    barrier(dist)
+    torch.cuda.synchronize()
+    n0 = L.tp_kernel_launch_count()
+    ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    ev_a.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    ev_b.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(dist)
+    launches = L.tp_kernel_launch_count() - n0
+    status = L.tp_get_device_status(check=False)
+    if status != L.TP_OK:
+        raise RuntimeError(f"device error in timed region: {L.status_string(status)}")
+    ms = ev_a.elapsed_time(ev_b) / args.steps
+    ms_max = reduce_max(dist, ms)
+    col_ms = statistics.mean(a.elapsed_time(b) for a, b in col_ev)
+    clk = clocks.summary(t_wall0, t_wall1) if clocks else None
+
+    # end to end: host (pinned) inputs copied in, results read back, every step
+    e2e = None
+    if not args.no_e2e:
+        Xh = torch.empty(M, h, dtype=bf16, pin_memory=True).copy_(X.cpu())
+        dYh = torch.empty(M, h, dtype=bf16, pin_memory=True).copy_(dY.cpu())
+        Yh = torch.empty(M, h, dtype=bf16, pin_memory=True)
+        dXh = torch.empty(M, h, dtype=bf16, pin_memory=True)
+
+        def e2e_step():
+            X.copy_(Xh, non_blocking=True)
+            dY.copy_(dYh, non_blocking=True)
+            step()
+            Yh.copy_(Y, non_blocking=True)
+            dXh.copy_(dX, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        barrier(dist)
+        torch.cuda.synchronize()
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        eb.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+        e_ms = reduce_max(dist, ea.elapsed_time(eb) / args.steps)
+        e2e = {"value": round(aggregate(flops_per_step(M, h, F), e_ms / 1e3, world) / 1e12, 2), "unit": UNIT,
+               "h2d_bytes_per_step": 2 * M * h * 2, "d2h_bytes_per_step": 2 * M * h * 2}
+
+    if clocks:
+        clocks.stop()
+
+    secondary = None
+    if not args.no_extras and rank == 0:
+        secondary = run_decode_extra(L, torch, args)
+
+    if rank != 0:
+        return None
+    peaks = measured_peaks()
+    region_s = ms * args.steps / 1e3
+    peak_kind = "bf16_sustained" if region_s >= 2.0 else "bf16_burst"
+    peak = peaks[peak_kind]
+    col_flops = 2.0 * M * h * F
+    achieved = col_flops / (col_ms / 1e3) / 1e12
+    value = aggregate(flops_per_step(M, h, F), ms_max / 1e3, world) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "TP-MLP fwd+bwd, t=4, X 2048x4096, W_up 4096x16384, W_down 16384x4096, GeLU(tanh)",
+                   "global_batch": M * world, "seq_len": M, "parallelism": f"t=4 logical shards x {world} replica(s)",
+                   "l2": "working set ~1.1 GB > 129 MB L2; no flush",
+                   "frac_of_peak": round(value / world / peak, 4), "peak_tflops": peak,
+                   "peak_kind": f"{peak_kind} ({peaks['source']})"},
+        "roofline": {"bound": "tensor", "kernel": "gemm_kernel (column-parallel GEMM + GeLU epilogue)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": UNIT,
+                     "frac": round(achieved / peak, 4), "traffic": recorded_traffic("gemm_colpar_fwd_c2.md"),
+                     "kernel_ms": round(col_ms, 4), "flops_per_launch": col_flops},
+        "clocks": clk, "e2e": e2e, "gpu_launches": int(launches),
+    }
+    if secondary:
+        line["secondary"] = secondary
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
+    return line
+
+
+def run_decode_extra(L, torch, args):
+    """Decode-shaped SwiGLU GEMV (x 1x8192, W_gate/W_up 8192x28672, W_down
+    28672x8192, t = 4): HBM GB/s of the whole decode step (two kernels)."""
+    from megatron_tensor_transformer_shard_gb300 import inputs as I
+    c = I.CONFIGS["c3"]
+    M, h, F, t = c["M"], c["h"], c["F"], c["t"]
+    inp = I.swiglu_inputs(M, h, F, seed=0, device="cuda")
+    Wgu = torch.empty(2 * F, h, dtype=torch.bfloat16, device="cuda")
+    Wd = torch.empty(t, h, F // t, dtype=torch.bfloat16, device="cuda")
+    L.tp_pack_swiglu(inp["W_gate"], inp["W_up"], h, F, t, Wgu)
+    L.tp_pack_row(inp["W_down"], F, h, t, Wd)
+    del inp["W_gate"], inp["W_up"], inp["W_down"]
+    y = torch.empty(M, h, dtype=torch.bfloat16, device="cuda")
+    a = torch.empty(M, F, dtype=torch.bfloat16, device="cuda")
+    for _ in range(5):
+        L.tp_decode_swiglu_forward(inp["X"], M, h, F, t, Wgu, Wd, y, a)
+    torch.cuda.synchronize()
+    n = max(20, args.steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        L.tp_decode_swiglu_forward(inp["X"], M, h, F, t, Wgu, Wd, y, a)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / n * 1e3
+    nbytes = 3 * h * F * 2 + M * h * 2 * 2 + M * F * 2 * 2
+    gbs = nbytes / (us / 1e6) / 1e9
+    peaks = measured_peaks()
+    return {"workload": "decode SwiGLU GEMV, t=4, x 1x8192, W_gate/W_up 8192x28672, W_down 28672x8192",
+            "us_per_step": round(us, 2), "GBps": round(gbs, 1), "bytes_per_step": nbytes,
+            "frac_of_hbm": round(gbs / peaks["hbm"], 4), "hbm_peak_GBps": peaks["hbm"],
+            "frac_of_8TBps": round(gbs / 8000.0, 4), "l2": "1.41 GB of weights > L2; no flush"}
+
+
+# ----------------------------------------------------------- oracle (CPU)
+
+def _oracle_inputs(M_s):
+    import oracle as O
+    from megatron_tensor_transformer_shard_gb300 import inputs as I
+    cfg = I.CONFIGS[WORKLOAD]
+    inp = I.mlp_inputs(cfg["M"], cfg["h"], cfg["F"], bias=True, dy=True, seed=0)
+    r = {k: O.bf16_to_f64(I.bits(v)).reshape(tuple(v.shape)) for k, v in inp.items()}
+    r["X"], r["dY"] = r["X"][:M_s], r["dY"][:M_s]
+    return r, cfg
+
+
+def _oracle_step(O, r, cfg):
+    f = O.mlp_forward_sharded(r["X"], r["W_up"], r["b_up"], r["W_down"], r["b_down"], cfg["act"], cfg["t"])
+    O.mlp_backward_sharded(r["dY"], r["X"], r["W_up"], r["W_down"], f, cfg["act"], cfg["t"])
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(budget_s=12.0):
+    """The fp64 oracle as it stands, on the host cores, on a row sample of the
+    same workload sized to about `budget_s` seconds of CPU work."""
+    import oracle as O
+    r, cfg = _oracle_inputs(cfg_rows := 128)
+    t0 = time.perf_counter()
+    _oracle_step(O, r, cfg)
+    dt = time.perf_counter() - t0
+    rows = int(min(cfg["M"], max(128, (budget_s / max(dt, 1e-3)) * 128 // 128 * 128)))
+    if rows != cfg_rows:
+        r, cfg = _oracle_inputs(rows)
+        t0 = time.perf_counter()
+        _oracle_step(O, r, cfg)
+        dt = time.perf_counter() - t0
+    fl = flops_per_step(rows, cfg["h"], cfg["F"])
+    return {"value": round(fl / dt / 1e12, 5), "unit": UNIT, "cores": _cores(), "kind": "oracle",
+            "sample": f"one fwd+bwd of the same MLP on the first {rows} of {cfg['M']} token rows "
+                      f"(numpy fp64, {dt:.2f} s)", "seconds": round(dt, 3)}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle as O
+    rows = args.reference_rows
+    r, cfg = _oracle_inputs(rows)
+    for _ in range(args.warmup):
+        _oracle_step(O, r, cfg)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(O, r, cfg)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = flops_per_step(rows, cfg["h"], cfg["F"]) / dt / 1e12
+    sample = f"each step one fwd+bwd of the same MLP on the first {rows} of {cfg['M']} token rows (numpy fp64)"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "TP-MLP fwd+bwd, t=4, X 2048x4096, W_up 4096x16384, W_down 16384x4096, "
+                                   "GeLU(tanh)", "global_batch": rows, "seq_len": rows,
+                       "parallelism": "t=4 logical shards (oracle loop)"},
+            "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": _cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-extras", action="store_true")
+    p.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    p.add_argument("--reference-rows", type=int, default=64, help="token rows per oracle step (--impl reference)")
+    args = p.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

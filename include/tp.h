@@ -99,6 +99,10 @@ tp_status tp_get_device_status(tp_stream stream);
  * reports TP_ERR_TIMEOUT. */
 tp_status tp_selftest_bounded_wait(int64_t timeout_us, tp_stream stream);
 
+/* Number of CUDA kernels this library has enqueued in this process so far
+ * (all devices, all streams).  Host-side counter; never synchronises. */
+uint64_t tp_kernel_launch_count(void);
+
 /* -------------------------------------------------------------- packing
  * Bit-exact permutations of bf16 weights into the per-shard layouts listed
  * above ("Tensor and sequence parallelism", section "The implementation":
@@ -122,6 +126,27 @@ tp_status tp_unpack_qkv_heads(const tp_bf16* Wp, int64_t d, int n_heads, int hea
 /* b: (3d) -> [t][3d/t] in the same head order. */
 tp_status tp_pack_qkv_bias(const tp_bf16* b, int64_t d, int n_heads, int head_dim, int t, tp_bf16* bp,
                            tp_stream stream);
+
+/* ------------------------------------------- column / row parallel linear
+ * The two halves of the pairing, each ONE kernel launch ("02 — Tensor
+ * Parallelism", "Column-parallel" and "Row-parallel"):
+ *
+ * Column-parallel (W split along its output dim; f forward = identity, X read
+ * by every shard): Z_i = X W_i + b[C_i];  A_i = act(Z_i).
+ *   X [M][h]; W_p [t][N/t][h] (tp_pack_col of W (h, N)); b [N] nullable;
+ *   Z [t][M][N/t] nullable; A [t][M][N/t] required.  h, N/t multiples of 8. */
+tp_status tp_column_parallel_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t N, int t, tp_act act,
+                                     const tp_bf16* W_p, const tp_bf16* b, tp_bf16* Z, tp_bf16* A,
+                                     tp_stream stream);
+
+/* Row-parallel (W split along its input dim) followed by g: the t partial
+ * products of the sharded input are summed in shard order inside the GEMM's
+ * accumulator, then the bias is added once and the residual after it:
+ *   Y = sum_{i=0..t-1} A_i W_i + b + residual.
+ *   A [t][M][K/t]; W_p [t][h][K/t] (tp_pack_row of W (K, h)); b [h] nullable;
+ *   residual [M][h] nullable; Y [M][h].  h, K/t multiples of 8. */
+tp_status tp_row_parallel_forward(const tp_bf16* A, int64_t M, int64_t K, int64_t h, int t, const tp_bf16* W_p,
+                                  const tp_bf16* b, const tp_bf16* residual, tp_bf16* Y, tp_stream stream);
 
 /* -------------------------------------------------------------- TP MLP
  * Forward ("02 — Tensor Parallelism", "The MLP pairing"; "Tensor and
@@ -160,6 +185,40 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
                           const tp_bf16* Wdown_p, tp_bf16* dX, float* dWup_p, float* dWdown_p, float* dbup,
                           float* dbdown, int accumulate, unsigned flags, void* ws, size_t ws_bytes,
                           tp_stream stream);
+
+/* -------------------------------------------------------- decode SwiGLU
+ * Memory-bound decode step of a SwiGLU MLP ("02 — Tensor Parallelism",
+ * "The core observation" (times 2 for SwiGLU) and "When to use TP": decode is
+ * bandwidth-bound):
+ *   shard i: a_i = silu(x W_gate,i) * (x W_up,i);   y = sum_{i=0..t-1} a_i W_down,i.
+ * x [M][h] with 1 <= M <= 8; Wgu_p from tp_pack_swiglu; Wdown_p from
+ * tp_pack_row; y [M][h]; a_save [M][F] bf16 (required: shard i's hidden
+ * vector at columns C_i; the down projection reads it).  No biases. */
+tp_status tp_decode_swiglu_forward(const tp_bf16* x, int64_t M, int64_t h, int64_t F, int t,
+                                   const tp_bf16* Wgu_p, const tp_bf16* Wdown_p, tp_bf16* y, tp_bf16* a_save,
+                                   tp_stream stream);
+
+/* ------------------------------------------- sequence-parallel LayerNorm
+ * ("Tensor and sequence parallelism", section "Sequence parallelism";
+ * "02 — Tensor Parallelism", "Sequence parallelism (Megatron-3)"):
+ * X_sh [t][s/t][h]: shard j normalises only its own s/t rows,
+ *   y = (x - mean) * rstd * gamma + beta,  rstd = 1/sqrt(biased var + eps).
+ * The all-gather that enters the TP region is zero-copy: [t][s/t][h] is the
+ * same bytes as [s][h].  mean, rstd: [s] fp32 (saved for backward).
+ * t = 1 is an ordinary replicated LayerNorm. */
+tp_status tp_sp_layernorm_forward(const tp_bf16* X_sh, int64_t s, int64_t h, int t, const tp_bf16* gamma,
+                                  const tp_bf16* beta, float eps, tp_bf16* Y_sh, float* mean, float* rstd,
+                                  tp_stream stream);
+
+/* Backward: dX rows per shard (plus dres [s][h] if non-null: the residual
+ * branch's gradient, added in the same pass); per-shard partial weight grads
+ * dgamma_part[j] = sum over shard j's rows of dy*xhat, dbeta_part[j] = sum dy
+ * ([t][h] fp32); then the LayerNorm weight-gradient all-reduce:
+ * dgamma = sum_{j=0..t-1} dgamma_part[j] (fixed order), same for dbeta. */
+tp_status tp_sp_layernorm_backward(const tp_bf16* dY_sh, const tp_bf16* X_sh, const tp_bf16* gamma,
+                                   const float* mean, const float* rstd, const tp_bf16* dres, int64_t s, int64_t h,
+                                   int t, tp_bf16* dX_sh, float* dgamma_part, float* dbeta_part, float* dgamma,
+                                   float* dbeta, tp_stream stream);
 
 /* ------------------------------------------------------------ utilities
  * Fixed-order reduction of t partial buffers (the on-device stand-in for an

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 #include <mutex>
 
@@ -80,6 +81,13 @@ bool device_is_sm103() {
   return g_is_sm103[dev] != 0;
 }
 
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}
+
+void count_launch(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
+uint64_t launches_so_far() { return g_launches.load(std::memory_order_relaxed); }
+
 tp_status ready() {
   if (!device_error_word()) return TP_ERR_CUDA;
   if (!device_is_sm103()) return TP_ERR_UNSUPPORTED;
@@ -114,6 +122,8 @@ extern "C" {
 
 int tp_abi_version(void) { return TP_ABI_VERSION; }
 
+uint64_t tp_kernel_launch_count(void) { return launches_so_far(); }
+
 const char* tp_status_string(tp_status s) {
   switch (s) {
     case TP_OK: return "TP_OK";
@@ -143,6 +153,7 @@ tp_status tp_selftest_bounded_wait(int64_t timeout_us, tp_stream stream) {
   if (timeout_us < 1 || timeout_us > 10000000) return TP_ERR_INVALID_ARG;
   TP_RETURN_IF(ready());
   selftest_wait_kernel<<<1, 32, 0, S(stream)>>>(device_error_word(), static_cast<uint64_t>(timeout_us) * 1000ull);
+  count_launch();
   return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 
@@ -182,6 +193,41 @@ size_t tp_mlp_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned fl
   return (flags & TP_FLAG_UNFUSED_REDUCE) ? static_cast<size_t>(t) * M * h * sizeof(float) : 0;
 }
 
+tp_status tp_column_parallel_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t N, int t, tp_act act,
+                                     const tp_bf16* W_p, const tp_bf16* b, tp_bf16* Z, tp_bf16* A,
+                                     tp_stream stream) {
+  if (M < 0 || h < 1 || N < 1 || t < 1 || !act_ok(act)) return TP_ERR_INVALID_ARG;
+  if (N % t != 0) return TP_ERR_SHAPE;
+  const int64_t Nt = N / t;
+  if (h % 8 != 0 || Nt % 8 != 0) return TP_ERR_ALIGN;
+  if (M == 0) return TP_OK;
+  if (!X || !W_p || !A) return TP_ERR_INVALID_ARG;
+  GemmProblem c;
+  c.M = M; c.N = Nt; c.K = h; c.nbatch = t; c.nsum = 1;
+  c.a.ptr = X; c.a.ld = h;
+  c.b.ptr = W_p; c.b.ld = h; c.b.sharded = true; c.b.shard_stride = Nt * h;
+  c.epi = EPI_ACT; c.act = act;
+  c.d = Z; c.d2 = A; c.ldd = Nt; c.d_batch_stride = M * Nt;
+  c.bias = b; c.bias_batch_stride = Nt;
+  return run_gemm(c, S(stream));
+}
+
+tp_status tp_row_parallel_forward(const tp_bf16* A, int64_t M, int64_t K, int64_t h, int t, const tp_bf16* W_p,
+                                  const tp_bf16* b, const tp_bf16* residual, tp_bf16* Y, tp_stream stream) {
+  if (M < 0 || h < 1 || K < 1 || t < 1) return TP_ERR_INVALID_ARG;
+  if (K % t != 0) return TP_ERR_SHAPE;
+  const int64_t Kt = K / t;
+  if (h % 8 != 0 || Kt % 8 != 0) return TP_ERR_ALIGN;
+  if (M == 0) return TP_OK;
+  if (!A || !W_p || !Y) return TP_ERR_INVALID_ARG;
+  GemmProblem r;
+  r.M = M; r.N = h; r.K = Kt; r.nbatch = 1; r.nsum = t;
+  r.a.ptr = A; r.a.ld = Kt; r.a.sharded = true; r.a.shard_stride = M * Kt;
+  r.b.ptr = W_p; r.b.ld = Kt; r.b.sharded = true; r.b.shard_stride = h * Kt;
+  r.epi = EPI_BF16; r.d = Y; r.ldd = h; r.bias = b; r.residual = residual; r.ld_res = h;
+  return run_gemm(r, S(stream));
+}
+
 tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int t, tp_act act,
                          const tp_bf16* Wup_p, const tp_bf16* bup, const tp_bf16* Wdown_p, const tp_bf16* bdown,
                          const tp_bf16* residual, tp_bf16* Y, tp_bf16* Z_save, tp_bf16* A_save, unsigned flags,
@@ -196,28 +242,16 @@ tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int 
   if (ws_bytes < tp_mlp_workspace_size(M, h, F, t, flags) || (unfused && !ws)) return TP_ERR_WORKSPACE;
   const cudaStream_t s = S(stream);
 
-  // Column-parallel: Z_i = X W_up,i + b_up[C_i]; A_i = act(Z_i).  X is read by every shard (f forward).
-  GemmProblem c;
-  c.M = M; c.N = Ft; c.K = h; c.nbatch = t; c.nsum = 1;
-  c.a.ptr = X; c.a.ld = h;
-  c.b.ptr = Wup_p; c.b.ld = h; c.b.sharded = true; c.b.shard_stride = Ft * h;
-  c.epi = EPI_ACT; c.act = act;
-  c.d = Z_save; c.d2 = A_save; c.ldd = Ft; c.d_batch_stride = M * Ft;
-  c.bias = bup; c.bias_batch_stride = Ft;
-  TP_RETURN_IF(run_gemm(c, s));
+  // f (identity) + column-parallel: Z_i = X W_up,i + b_up[C_i]; A_i = act(Z_i).
+  TP_RETURN_IF(tp_column_parallel_forward(X, M, h, F, t, act, Wup_p, bup, Z_save, A_save, stream));
 
   // Row-parallel + g: Y = sum_i A_i W_down,i + b_down (once) + residual.
+  if (!unfused) return tp_row_parallel_forward(A_save, M, F, h, t, Wdown_p, bdown, residual, Y, stream);
   GemmProblem r;
-  r.M = M; r.N = h; r.K = Ft;
+  r.M = M; r.N = h; r.K = Ft; r.nbatch = t; r.nsum = 1;
   r.a.ptr = A_save; r.a.ld = Ft; r.a.sharded = true; r.a.shard_stride = M * Ft;
   r.b.ptr = Wdown_p; r.b.ld = Ft; r.b.sharded = true; r.b.shard_stride = h * Ft;
-  if (!unfused) {
-    r.nbatch = 1; r.nsum = t;
-    r.epi = EPI_BF16; r.d = Y; r.ldd = h; r.bias = bdown; r.residual = residual; r.ld_res = h;
-    return run_gemm(r, s);
-  }
   float* P = static_cast<float*>(ws);
-  r.nbatch = t; r.nsum = 1;
   r.epi = EPI_F32; r.d = P; r.ldd = h; r.d_batch_stride = M * h;
   TP_RETURN_IF(run_gemm(r, s));
   return run_shard_reduce(P, M, h, t, bdown, residual, Y, nullptr, s);
@@ -313,6 +347,28 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
   dx.epi = EPI_F32; dx.d = P; dx.ldd = h; dx.d_batch_stride = M * h;
   TP_RETURN_IF(run_gemm(dx, s));
   return run_shard_reduce(P, M, h, t, nullptr, nullptr, dX, nullptr, s);
+}
+
+// ------------------------------------------------------------------ decode
+tp_status tp_decode_swiglu_forward(const tp_bf16* x, int64_t M, int64_t h, int64_t F, int t,
+                                   const tp_bf16* Wgu_p, const tp_bf16* Wdown_p, tp_bf16* y, tp_bf16* a_save,
+                                   tp_stream stream) {
+  return run_decode_swiglu(x, M, h, F, t, Wgu_p, Wdown_p, y, a_save, S(stream));
+}
+
+// ------------------------------------------------------------------ LayerNorm
+tp_status tp_sp_layernorm_forward(const tp_bf16* X_sh, int64_t s, int64_t h, int t, const tp_bf16* gamma,
+                                  const tp_bf16* beta, float eps, tp_bf16* Y_sh, float* mean, float* rstd,
+                                  tp_stream stream) {
+  return run_ln_forward(X_sh, s, h, t, gamma, beta, eps, Y_sh, mean, rstd, S(stream));
+}
+
+tp_status tp_sp_layernorm_backward(const tp_bf16* dY_sh, const tp_bf16* X_sh, const tp_bf16* gamma,
+                                   const float* mean, const float* rstd, const tp_bf16* dres, int64_t s, int64_t h,
+                                   int t, tp_bf16* dX_sh, float* dgamma_part, float* dbeta_part, float* dgamma,
+                                   float* dbeta, tp_stream stream) {
+  return run_ln_backward(dY_sh, X_sh, gamma, mean, rstd, dres, s, h, t, dX_sh, dgamma_part, dbeta_part, dgamma,
+                         dbeta, S(stream));
 }
 
 // ------------------------------------------------------------------ utilities

@@ -438,7 +438,7 @@ tp_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a
     configured[dev] = true;
   }
   gemm_kernel<A_MN, B_MN><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, a);
-  TP_CUDA_CHECK(cudaGetLastError());
+  TP_LAUNCHED();
   return TP_OK;
 }
 

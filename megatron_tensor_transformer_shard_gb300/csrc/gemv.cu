@@ -176,9 +176,9 @@ tp_status launch_decode(const uint16_t* x, int64_t h, int64_t F, int t, const ui
   if (g1 > F) g1 = F;
   if (g2 > h) g2 = h;
   swiglu_gate_up_kernel<M><<<static_cast<unsigned>(g1), GEMV_THREADS, 0, s>>>(x, h, F, Wgu, a);
-  TP_CUDA_CHECK(cudaGetLastError());
+  TP_LAUNCHED();
   down_reduce_kernel<M><<<static_cast<unsigned>(g2), GEMV_THREADS, 0, s>>>(a, h, F, t, Wd, y);
-  TP_CUDA_CHECK(cudaGetLastError());
+  TP_LAUNCHED();
   return TP_OK;
 }
 

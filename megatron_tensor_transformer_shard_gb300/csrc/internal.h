@@ -14,6 +14,8 @@ uint64_t wait_timeout_ns();        // limit for every bounded wait in the librar
 int device_sm_count();             // SMs of the current device
 bool device_is_sm103();            // compute capability 10.3
 tp_status ready();                 // TP_OK if the current device can run this library's kernels
+void count_launch(int n = 1);      // every kernel launch of the library is counted
+uint64_t launches_so_far();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -27,6 +29,13 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
   do {                                           \
     cudaError_t _e = (expr);                     \
     if (_e != cudaSuccess) return TP_ERR_CUDA;   \
+  } while (0)
+
+// After a <<<...>>> launch: count it and surface launch errors.
+#define TP_LAUNCHED()                                           \
+  do {                                                          \
+    count_launch();                                             \
+    if (cudaGetLastError() != cudaSuccess) return TP_ERR_CUDA;  \
   } while (0)
 
 // ----------------------------------------------------------------- GEMM
@@ -91,5 +100,14 @@ tp_status pack_qkv(const uint16_t* src, int64_t d, int n_heads, int head_dim, in
                    cudaStream_t s);
 tp_status pack_qkv_bias(const uint16_t* b, int64_t d, int n_heads, int head_dim, int t, uint16_t* bp,
                         cudaStream_t s);
+
+// decode GEMV (gemv.cu), LayerNorm (layernorm.cu)
+tp_status run_decode_swiglu(const uint16_t* x, int64_t M, int64_t h, int64_t F, int t, const uint16_t* Wgu,
+                            const uint16_t* Wd, uint16_t* y, uint16_t* a, cudaStream_t s);
+tp_status run_ln_forward(const uint16_t* X, int64_t s, int64_t h, int t, const uint16_t* gamma,
+                         const uint16_t* beta, float eps, uint16_t* Y, float* mean, float* rstd, cudaStream_t st);
+tp_status run_ln_backward(const uint16_t* dY, const uint16_t* X, const uint16_t* gamma, const float* mean,
+                          const float* rstd, const uint16_t* dres, int64_t s, int64_t h, int t, uint16_t* dX,
+                          float* dg_part, float* db_part, float* dgamma, float* dbeta, cudaStream_t st);
 
 }  // namespace tp

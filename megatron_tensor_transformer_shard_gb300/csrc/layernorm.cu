@@ -1,0 +1,257 @@
+// Sequence-parallel LayerNorm ("Tensor and sequence parallelism", section
+// "Sequence parallelism"; "02 — Tensor Parallelism", "Sequence parallelism
+// (Megatron-3)").  X_sh [t][s/t][h] is the same bytes as [s][h]: the
+// all-gather that enters the TP region and the reduce-scatter that leaves it
+// are layouts, not copies.  What sequence parallelism adds is the weight
+// gradient: each shard j only sees its own rows, so it produces a partial
+// (dgamma_j, dbeta_j) and the partials are summed over j -- the extra
+// all-reduce -- in a fixed shard order.
+//
+//   row kernels     one CTA per row, the row held in registers (8-element
+//                   chunks, up to 4 per thread), block reductions for the
+//                   statistics; HBM-bound: read x (+ dy, dres), write y / dx.
+//   column kernel   one CTA per (64-column block, shard): four warps stride
+//                   the shard's rows, combined in warp order.
+#include <cuda_runtime.h>
+
+#include "devmath.cuh"
+#include "internal.h"
+
+namespace tp {
+namespace {
+
+constexpr int LN_CHUNKS = 4;  // 8-element chunks per thread -> h <= 1024*32
+
+__device__ __forceinline__ void load8(const uint16_t* p, float (&v)[8]) {
+  const uint4 w = *reinterpret_cast<const uint4*>(p);
+  unpack_bf16x2(w.x, v[0], v[1]);
+  unpack_bf16x2(w.y, v[2], v[3]);
+  unpack_bf16x2(w.z, v[4], v[5]);
+  unpack_bf16x2(w.w, v[6], v[7]);
+}
+
+__device__ __forceinline__ void store8(uint16_t* p, const float (&v)[8]) {
+  uint4 w;
+  w.x = pack_bf16x2(v[0], v[1]);
+  w.y = pack_bf16x2(v[2], v[3]);
+  w.z = pack_bf16x2(v[4], v[5]);
+  w.w = pack_bf16x2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(p) = w;
+}
+
+// Fixed-order block sum of two values (warp butterfly, then warps in order).
+__device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+    b += __shfl_xor_sync(0xffffffffu, b, o);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = make_float2(a, b);
+  __syncthreads();
+  float2 s = make_float2(0.0f, 0.0f);
+  const int nw = blockDim.x >> 5;
+  for (int w = 0; w < nw; ++w) {
+    s.x += red[w].x;
+    s.y += red[w].y;
+  }
+  __syncthreads();
+  return s;
+}
+
+__global__ void ln_fwd_kernel(const uint16_t* __restrict__ X, int64_t h, const uint16_t* __restrict__ gamma,
+                              const uint16_t* __restrict__ beta, float eps, uint16_t* __restrict__ Y,
+                              float* __restrict__ mean_out, float* __restrict__ rstd_out) {
+  __shared__ float2 red[32];
+  const int64_t row = blockIdx.x;
+  const uint16_t* x = X + row * h;
+  const int64_t nch = h / 8;
+  float v[LN_CHUNKS][8];
+  float s = 0.0f;
+#pragma unroll
+  for (int k = 0; k < LN_CHUNKS; ++k) {
+    const int64_t c = threadIdx.x + static_cast<int64_t>(k) * blockDim.x;
+    if (c < nch) {
+      load8(x + c * 8, v[k]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s += v[k][e];
+    }
+  }
+  const float mean = block_sum2(s, 0.0f, red).x / static_cast<float>(h);
+  float q = 0.0f;
+#pragma unroll
+  for (int k = 0; k < LN_CHUNKS; ++k) {
+    const int64_t c = threadIdx.x + static_cast<int64_t>(k) * blockDim.x;
+    if (c < nch) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float d = v[k][e] - mean;
+        q += d * d;
+      }
+    }
+  }
+  const float var = block_sum2(q, 0.0f, red).x / static_cast<float>(h);
+  const float rstd = rsqrtf(var + eps);
+#pragma unroll
+  for (int k = 0; k < LN_CHUNKS; ++k) {
+    const int64_t c = threadIdx.x + static_cast<int64_t>(k) * blockDim.x;
+    if (c < nch) {
+      float g[8], b[8], o[8];
+      load8(gamma + c * 8, g);
+      load8(beta + c * 8, b);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = (v[k][e] - mean) * rstd * g[e] + b[e];
+      store8(Y + row * h + c * 8, o);
+    }
+  }
+  if (threadIdx.x == 0) {
+    mean_out[row] = mean;
+    rstd_out[row] = rstd;
+  }
+}
+
+// dx = rstd * (g - mean(g) - xhat * mean(g * xhat)) (+ dres),  g = dy * gamma.
+__global__ void ln_bwd_rows_kernel(const uint16_t* __restrict__ dY, const uint16_t* __restrict__ X,
+                                   const uint16_t* __restrict__ gamma, const float* __restrict__ mean_in,
+                                   const float* __restrict__ rstd_in, const uint16_t* __restrict__ dres, int64_t h,
+                                   uint16_t* __restrict__ dX) {
+  __shared__ float2 red[32];
+  const int64_t row = blockIdx.x;
+  const float mean = mean_in[row], rstd = rstd_in[row];
+  const int64_t nch = h / 8;
+  float xh[LN_CHUNKS][8], g[LN_CHUNKS][8];
+  float sg = 0.0f, sgx = 0.0f;
+#pragma unroll
+  for (int k = 0; k < LN_CHUNKS; ++k) {
+    const int64_t c = threadIdx.x + static_cast<int64_t>(k) * blockDim.x;
+    if (c < nch) {
+      float dy[8], gm[8];
+      load8(X + row * h + c * 8, xh[k]);
+      load8(dY + row * h + c * 8, dy);
+      load8(gamma + c * 8, gm);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        xh[k][e] = (xh[k][e] - mean) * rstd;
+        g[k][e] = dy[e] * gm[e];
+        sg += g[k][e];
+        sgx += g[k][e] * xh[k][e];
+      }
+    }
+  }
+  const float2 tot = block_sum2(sg, sgx, red);
+  const float inv_h = 1.0f / static_cast<float>(h);
+  const float mg = tot.x * inv_h, mgx = tot.y * inv_h;
+#pragma unroll
+  for (int k = 0; k < LN_CHUNKS; ++k) {
+    const int64_t c = threadIdx.x + static_cast<int64_t>(k) * blockDim.x;
+    if (c < nch) {
+      float o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = rstd * (g[k][e] - mg - xh[k][e] * mgx);
+      if (dres) {
+        float r[8];
+        load8(dres + row * h + c * 8, r);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] += r[e];
+      }
+      store8(dX + row * h + c * 8, o);
+    }
+  }
+}
+
+// Partial weight grads of shard j over its rows [j*rows_per, (j+1)*rows_per).
+__global__ void ln_bwd_cols_kernel(const uint16_t* __restrict__ dY, const uint16_t* __restrict__ X,
+                                   const float* __restrict__ mean_in, const float* __restrict__ rstd_in, int64_t h,
+                                   int64_t rows_per, float* __restrict__ dg_part, float* __restrict__ db_part) {
+  __shared__ float4 red[4][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t col = static_cast<int64_t>(blockIdx.x) * 64 + 2 * lane;
+  const int j = blockIdx.y;
+  float dg0 = 0.0f, dg1 = 0.0f, db0 = 0.0f, db1 = 0.0f;
+  if (col < h) {
+    const int64_t r0 = static_cast<int64_t>(j) * rows_per;
+    for (int64_t r = r0 + warp; r < r0 + rows_per; r += 4) {
+      const float mean = mean_in[r], rstd = rstd_in[r];
+      float x0, x1, d0, d1;
+      unpack_bf16x2(*reinterpret_cast<const uint32_t*>(X + r * h + col), x0, x1);
+      unpack_bf16x2(*reinterpret_cast<const uint32_t*>(dY + r * h + col), d0, d1);
+      dg0 += d0 * (x0 - mean) * rstd;
+      dg1 += d1 * (x1 - mean) * rstd;
+      db0 += d0;
+      db1 += d1;
+    }
+  }
+  red[warp][lane] = make_float4(dg0, dg1, db0, db1);
+  __syncthreads();
+  if (warp == 0 && col < h) {
+    float4 s = red[0][lane];
+    for (int w = 1; w < 4; ++w) {
+      const float4 o = red[w][lane];
+      s.x += o.x; s.y += o.y; s.z += o.z; s.w += o.w;
+    }
+    dg_part[static_cast<int64_t>(j) * h + col] = s.x;
+    dg_part[static_cast<int64_t>(j) * h + col + 1] = s.y;
+    db_part[static_cast<int64_t>(j) * h + col] = s.z;
+    db_part[static_cast<int64_t>(j) * h + col + 1] = s.w;
+  }
+}
+
+int row_threads(int64_t h) {
+  const int64_t nch = h / 8;
+  int64_t th = (nch + LN_CHUNKS - 1) / LN_CHUNKS;
+  th = (th + 31) / 32 * 32;
+  return static_cast<int>(th < 32 ? 32 : th);
+}
+
+tp_status check(int64_t s, int64_t h, int t) {
+  if (s < 0 || h < 1 || t < 1) return TP_ERR_INVALID_ARG;
+  if (s % t != 0 || h > 1024LL * 8 * LN_CHUNKS) return TP_ERR_SHAPE;
+  if (h % 8 != 0) return TP_ERR_ALIGN;
+  return TP_OK;
+}
+
+}  // namespace
+
+tp_status run_ln_forward(const uint16_t* X, int64_t s, int64_t h, int t, const uint16_t* gamma,
+                         const uint16_t* beta, float eps, uint16_t* Y, float* mean, float* rstd, cudaStream_t st) {
+  TP_RETURN_IF(check(s, h, t));
+  if (s == 0) return TP_OK;
+  if (!X || !gamma || !beta || !Y || !mean || !rstd || !(eps >= 0.0f)) return TP_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(gamma) || !aligned16(beta) || !aligned16(Y)) return TP_ERR_ALIGN;
+  if (s > 0x7fffffffLL) return TP_ERR_SHAPE;
+  TP_RETURN_IF(ready());
+  ln_fwd_kernel<<<static_cast<unsigned>(s), row_threads(h), 0, st>>>(X, h, gamma, beta, eps, Y, mean, rstd);
+  TP_LAUNCHED();
+  return TP_OK;
+}
+
+tp_status run_ln_backward(const uint16_t* dY, const uint16_t* X, const uint16_t* gamma, const float* mean,
+                          const float* rstd, const uint16_t* dres, int64_t s, int64_t h, int t, uint16_t* dX,
+                          float* dg_part, float* db_part, float* dgamma, float* dbeta, cudaStream_t st) {
+  TP_RETURN_IF(check(s, h, t));
+  if (!dg_part || !db_part || !dgamma || !dbeta) return TP_ERR_INVALID_ARG;
+  if (s > 0 && (!dY || !X || !gamma || !mean || !rstd || !dX)) return TP_ERR_INVALID_ARG;
+  if ((s > 0 && (!aligned16(dY) || !aligned16(X) || !aligned16(gamma) || !aligned16(dX))) ||
+      (dres && !aligned16(dres)) || !aligned16(dg_part) || !aligned16(db_part) || !aligned16(dgamma) ||
+      !aligned16(dbeta))
+    return TP_ERR_ALIGN;
+  if (s > 0x7fffffffLL) return TP_ERR_SHAPE;
+  TP_RETURN_IF(ready());
+  if (s == 0) {
+    TP_CUDA_CHECK(cudaMemsetAsync(dg_part, 0, sizeof(float) * t * h, st));
+    TP_CUDA_CHECK(cudaMemsetAsync(db_part, 0, sizeof(float) * t * h, st));
+    TP_CUDA_CHECK(cudaMemsetAsync(dgamma, 0, sizeof(float) * h, st));
+    TP_CUDA_CHECK(cudaMemsetAsync(dbeta, 0, sizeof(float) * h, st));
+    return TP_OK;
+  }
+  ln_bwd_rows_kernel<<<static_cast<unsigned>(s), row_threads(h), 0, st>>>(dY, X, gamma, mean, rstd, dres, h, dX);
+  TP_LAUNCHED();
+  dim3 g(static_cast<unsigned>((h + 63) / 64), static_cast<unsigned>(t));
+  ln_bwd_cols_kernel<<<g, 128, 0, st>>>(dY, X, mean, rstd, h, s / t, dg_part, db_part);
+  TP_LAUNCHED();
+  // The LayerNorm weight-gradient all-reduce over the sequence shards, fixed order.
+  TP_RETURN_IF(run_shard_reduce(dg_part, 1, h, t, nullptr, nullptr, nullptr, dgamma, st));
+  return run_shard_reduce(db_part, 1, h, t, nullptr, nullptr, nullptr, dbeta, st);
+}
+
+}  // namespace tp

@@ -136,7 +136,7 @@ tp_status launch_pack(const PackMap& m, int dir, const uint16_t* u0, const uint1
   if (grid.y > 65535u) return TP_ERR_SHAPE;
   TP_RETURN_IF(ready());
   pack_kernel<<<grid, dim3(TILE, 8), 0, s>>>(m, dir, u0, u1, w0, w1, p_in, p_out);
-  TP_CUDA_CHECK(cudaGetLastError());
+  TP_LAUNCHED();
   return TP_OK;
 }
 
@@ -219,7 +219,7 @@ tp_status pack_qkv_bias(const uint16_t* b, int64_t d, int n_heads, int head_dim,
   if (m.R == 0) return TP_OK;
   TP_RETURN_IF(ready());
   gather_bias_kernel<<<static_cast<unsigned>((m.R + 255) / 256), 256, 0, s>>>(m, b, bp);
-  TP_CUDA_CHECK(cudaGetLastError());
+  TP_LAUNCHED();
   return TP_OK;
 }
 

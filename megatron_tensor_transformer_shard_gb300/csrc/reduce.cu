@@ -115,11 +115,11 @@ tp_status run_colsum_batched(const uint16_t* G, int64_t rows, int64_t cols, int6
   }
   dim3 g1(static_cast<unsigned>((cols / 2 + COLSUM_THREADS - 1) / COLSUM_THREADS), nchunks, nbatch);
   colsum_partial_kernel<<<g1, COLSUM_THREADS, 0, s>>>(G, rows, cols, ld, batch_stride, nchunks, ws);
-  TP_CUDA_CHECK(cudaGetLastError());
+  TP_LAUNCHED();
   const int64_t n = cols * nbatch;
   colsum_final_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(ws, cols, nchunks, nbatch, out,
                                                                              accumulate);
-  TP_CUDA_CHECK(cudaGetLastError());
+  TP_LAUNCHED();
   return TP_OK;
 }
 
@@ -143,7 +143,7 @@ tp_status run_shard_reduce(const float* P, int64_t rows, int64_t cols, int t, co
   if (blocks > cap) blocks = cap;
   shard_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(P, rows, cols, t, bias, residual, out_bf16,
                                                                      out_f32);
-  TP_CUDA_CHECK(cudaGetLastError());
+  TP_LAUNCHED();
   return TP_OK;
 }
 
