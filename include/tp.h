@@ -234,6 +234,27 @@ size_t tp_colsum_workspace_size(int64_t rows, int64_t cols);
 tp_status tp_colsum(const tp_bf16* G, int64_t rows, int64_t cols, float* out, int accumulate, void* ws,
                     size_t ws_bytes, tp_stream stream);
 
+/* Column sums like tp_colsum, for callers that cannot allocate device memory
+ * and so cannot hand over a workspace (code that must not call cudaMalloc,
+ * code whose device memory is all held by another allocator's pool, plugins
+ * that only receive their input and output pointers).  The pages have no
+ * counterpart to this entry point.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *     The partial sums live in a 4 MiB array inside the library's device image,
+ *     which every GPU that loads the library keeps until the process exits.
+ *   - Limit: ceil(rows / 64) * cols <= 1048576 (e.g. 2048 rows x 32768 columns);
+ *     larger sizes return TP_ERR_SHAPE and touch nothing.
+ *   - The first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress, with the device current); make that first
+ *     call before any stream capture.
+ *   - All calls share the one array: calls that may run at the same time on the
+ *     GPU (different streams without ordering between them) race and give
+ *     wrong sums.  Calls ordered on one stream are fine; each call overwrites
+ *     every partial it reads, so nothing from a previous call leaks in.
+ *   - G [rows][cols] bf16, cols even; out [cols] fp32 (added to when accumulate != 0). */
+tp_status tp_colsum_noalloc(const tp_bf16* G, int64_t rows, int64_t cols, float* out, int accumulate,
+                            tp_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

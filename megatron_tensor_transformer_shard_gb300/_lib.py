@@ -54,6 +54,7 @@ SIGNATURES = {
     "tp_shard_reduce": (_I, [_P, _I64, _I64, _I, _P, _P, _P, _P, _P]),
     "tp_colsum_workspace_size": (_SZ, [_I64, _I64]),
     "tp_colsum": (_I, [_P, _I64, _I64, _P, _I, _P, _SZ, _P]),
+    "tp_colsum_noalloc": (_I, [_P, _I64, _I64, _P, _I, _P]),
 }
 
 
