@@ -75,7 +75,7 @@ typedef enum {
   TP_ACT_SWIGLU = 4     /* silu(X W_gate) * (X W_up); decode entry point only */
 } tp_act;
 
-/* Flags for tp_mlp_forward / tp_mlp_backward / tp_attn_forward. */
+/* Flags for tp_mlp_forward / tp_mlp_backward. */
 #define TP_FLAG_UNFUSED_REDUCE 1u /* materialise the t partial sums P_i (fp32, in ws) and
                                      reduce them in a separate kernel instead of in the
                                      row-parallel GEMM's accumulator */
@@ -197,6 +197,26 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
 tp_status tp_decode_swiglu_forward(const tp_bf16* x, int64_t M, int64_t h, int64_t F, int t,
                                    const tp_bf16* Wgu_p, const tp_bf16* Wdown_p, tp_bf16* y, tp_bf16* a_save,
                                    tp_stream stream);
+
+/* -------------------------------------------------- head-sharded attention
+ * ("02 — Tensor Parallelism", "The attention pairing"; "Megatron-LM: Tensor
+ * Parallelism", "Attention Block"):
+ *   shard i: QKV_i = X W_qkv,i + b_qkv,i   -> [N][3d/t] = [Q_i|K_i|V_i]
+ *            per local head: S = scale Q K^T, causal mask (key > query), P = softmax(S), O = P V
+ *            O_i = local heads side by side [N][d/t];   partial Y_i = O_i W_o,i
+ *   g: Y = sum_i Y_i + b_o (+ residual), bias once.
+ * X [N][d] (already normalised); Wqkv_p [t][3d/t][d]; bqkv_p [t][3d/t]
+ * (nullable); Wo_p [t][d][d/t]; bo [d] (nullable); residual [N][d] (nullable);
+ * Y [N][d]; QKV_save [t][N][3d/t]; O_save [t][N][d/t]; lse_save [t][H/t][N]
+ * fp32 (natural-log log-sum-exp of each scaled score row).  head_dim == 128.
+ * flags must be 0 (TP_ERR_UNSUPPORTED otherwise); ws / ws_bytes are unused
+ * (pass NULL, 0).  The attention kernel runs one CTA per (head, 128-query
+ * block) with an online softmax; no N x N score matrix is ever stored. */
+tp_status tp_attn_forward(const tp_bf16* X, int64_t N, int64_t d, int n_heads, int head_dim, int t, int causal,
+                          float scale, const tp_bf16* Wqkv_p, const tp_bf16* bqkv_p, const tp_bf16* Wo_p,
+                          const tp_bf16* bo, const tp_bf16* residual, tp_bf16* Y, tp_bf16* QKV_save,
+                          tp_bf16* O_save, float* lse_save, unsigned flags, void* ws, size_t ws_bytes,
+                          tp_stream stream);
 
 /* ------------------------------------------- sequence-parallel LayerNorm
  * ("Tensor and sequence parallelism", section "Sequence parallelism";

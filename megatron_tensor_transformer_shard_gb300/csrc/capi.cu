@@ -356,6 +356,28 @@ tp_status tp_decode_swiglu_forward(const tp_bf16* x, int64_t M, int64_t h, int64
   return run_decode_swiglu(x, M, h, F, t, Wgu_p, Wdown_p, y, a_save, S(stream));
 }
 
+// ------------------------------------------------------------------ attention
+tp_status tp_attn_forward(const tp_bf16* X, int64_t N, int64_t d, int n_heads, int head_dim, int t, int causal,
+                          float scale, const tp_bf16* Wqkv_p, const tp_bf16* bqkv_p, const tp_bf16* Wo_p,
+                          const tp_bf16* bo, const tp_bf16* residual, tp_bf16* Y, tp_bf16* QKV_save,
+                          tp_bf16* O_save, float* lse_save, unsigned flags, void* ws, size_t ws_bytes,
+                          tp_stream stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (N < 0 || d < 1 || n_heads < 1 || t < 1 || head_dim < 1) return TP_ERR_INVALID_ARG;
+  if (flags != 0) return TP_ERR_UNSUPPORTED;
+  if (head_dim != 128 || static_cast<int64_t>(n_heads) * head_dim != d || n_heads % t != 0) return TP_ERR_SHAPE;
+  if (N == 0) return TP_OK;
+  if (!X || !Wqkv_p || !Wo_p || !Y || !QKV_save || !O_save || !lse_save) return TP_ERR_INVALID_ARG;
+  // f (identity) + column-parallel W_qkv by head: QKV_i = X W_qkv,i + b_qkv,i.
+  TP_RETURN_IF(tp_column_parallel_forward(X, N, d, 3 * d, t, TP_ACT_IDENTITY, Wqkv_p, bqkv_p, nullptr, QKV_save,
+                                          stream));
+  // Attention on each shard's own heads, no communication.
+  TP_RETURN_IF(run_attention_fwd(QKV_save, N, d, n_heads, head_dim, t, causal, scale, O_save, lse_save, S(stream)));
+  // Row-parallel W_o + g: Y = sum_i O_i W_o,i + b_o (once) + residual.
+  return tp_row_parallel_forward(O_save, N, d, d, t, Wo_p, bo, residual, Y, stream);
+}
+
 // ------------------------------------------------------------------ LayerNorm
 tp_status tp_sp_layernorm_forward(const tp_bf16* X_sh, int64_t s, int64_t h, int t, const tp_bf16* gamma,
                                   const tp_bf16* beta, float eps, tp_bf16* Y_sh, float* mean, float* rstd,

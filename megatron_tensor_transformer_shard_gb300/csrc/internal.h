@@ -110,4 +110,8 @@ tp_status run_ln_backward(const uint16_t* dY, const uint16_t* X, const uint16_t*
                           const float* rstd, const uint16_t* dres, int64_t s, int64_t h, int t, uint16_t* dX,
                           float* dg_part, float* db_part, float* dgamma, float* dbeta, cudaStream_t st);
 
+// attention (attention.cu)
+tp_status run_attention_fwd(const uint16_t* QKV, int64_t N, int64_t d, int n_heads, int head_dim, int t, int causal,
+                            float scale, uint16_t* O, float* lse, cudaStream_t s);
+
 }  // namespace tp
