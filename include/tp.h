@@ -218,6 +218,23 @@ tp_status tp_attn_forward(const tp_bf16* X, int64_t N, int64_t d, int n_heads, i
                           tp_bf16* O_save, float* lse_save, unsigned flags, void* ws, size_t ws_bytes,
                           tp_stream stream);
 
+/* Backward of L = <Y, dY>: g backward identity; per shard dO_i = dY W_o,i^T,
+ * head-local softmax backward, dQKV_i; dW_o,i = O_i^T dY; dW_qkv,i = dQKV_i^T X;
+ * f backward: dX = sum_i dQKV_i W_qkv,i^T (fused).  dWqkv_p [t][3d/t][d],
+ * dbqkv_p [t][3d/t], dWo_p [t][d][d/t], dbo [d]: fp32 (overwritten, or added to when
+ * accumulate != 0; dbqkv_p / dbo nullable).  Inputs are the forward's saved
+ * QKV_save, O_save, lse_save.  flags must be 0.  ws (see the size query) holds,
+ * in order, each 256-byte aligned: dO [t][N][d/t] bf16, D = rowsum(dO * O)
+ * [t][H/t][N] fp32, dQKV [t][N][3d/t] bf16, column-sum scratch.  The
+ * attention gradient runs as two deterministic kernels (dK/dV per key block,
+ * dQ per query block); scores are recomputed from the saved log-sum-exp. */
+size_t tp_attn_backward_workspace_size(int64_t N, int64_t d, int n_heads, int head_dim, int t, unsigned flags);
+tp_status tp_attn_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* QKV_save, const tp_bf16* O_save,
+                           const float* lse_save, int64_t N, int64_t d, int n_heads, int head_dim, int t,
+                           int causal, float scale, const tp_bf16* Wqkv_p, const tp_bf16* Wo_p, tp_bf16* dX,
+                           float* dWqkv_p, float* dbqkv_p, float* dWo_p, float* dbo, int accumulate,
+                           unsigned flags, void* ws, size_t ws_bytes, tp_stream stream);
+
 /* ------------------------------------------- sequence-parallel LayerNorm
  * ("Tensor and sequence parallelism", section "Sequence parallelism";
  * "02 — Tensor Parallelism", "Sequence parallelism (Megatron-3)"):

@@ -310,6 +310,439 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   }
 }
 
+
+// ------------------------------------------------------------------ backward
+//
+// With P = softmax(scale * Q K^T) recomputed from the saved log-sum-exp and
+// D = rowsum(dO * O), the head-local gradients are
+//   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
+// Two kernels, no atomics (deterministic): one CTA per (head, key block) for
+// dK / dV, looping over query blocks; one CTA per (head, query block) for dQ,
+// looping over key blocks.  P and dS are written once into 128B-swizzled
+// tiles with the query index as the row; the same bytes are the K-major A
+// operand of dQ = dS K and the MN-major A operand of dV = P^T dO and
+// dK = dS^T Q, so no transpose is ever materialised.
+
+constexpr int BWD_THREADS = 192;
+constexpr int DKV_SMEM = 1024 + 6 * TILE + 256;
+constexpr int DQ_SMEM = 1024 + 7 * TILE + 256;
+
+struct AttnBwdArgs {
+  int N, H, hpr, nqb, causal;
+  int64_t dt;
+  float scale, scale_log2;
+  const float* lse;   // [t][hpr][N] natural log
+  const float* Dvec;  // [t][hpr][N]
+  uint16_t* dQKV;     // [t][N][3dt]
+  int* err;
+  uint64_t timeout_ns;
+};
+
+// Writes 32 consecutive columns (chunk c of 4) of row `row` into a K-major swizzled tile.
+__device__ __forceinline__ void store_chunk_swizzled(uint8_t* tile, int row, int c, const uint32_t (&w)[16]) {
+  uint8_t* rowp = tile + (c >> 1) * PANEL + row * 128;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int ch = (c & 1) * 4 + k;
+    *reinterpret_cast<uint4*>(rowp + ((ch ^ (row & 7)) << 4)) =
+        make_uint4(w[4 * k + 0], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+  }
+}
+
+// P and dS for 32 columns of one query row; returns them packed as bf16 pairs.
+__device__ __forceinline__ void p_ds_chunk(const uint32_t (&s)[32], const uint32_t (&dp)[32], int q, int kv0,
+                                           const AttnBwdArgs& p, float lse2, float Dq, uint32_t (&wp)[16],
+                                           uint32_t (&wds)[16]) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    float pv[2], dv[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int kv = kv0 + e + u;
+      const bool valid = q < p.N && kv < p.N && (!p.causal || kv <= q);
+      const float pr = valid ? ptx::exp2_approx(__uint_as_float(s[e + u]) * p.scale_log2 - lse2) : 0.0f;
+      pv[u] = pr;
+      dv[u] = pr * (__uint_as_float(dp[e + u]) - Dq);
+    }
+    wp[e >> 1] = pack_bf16x2(pv[0], pv[1]);
+    wds[e >> 1] = pack_bf16x2(dv[0], dv[1]);
+  }
+}
+
+__global__ void attn_bwd_dot_kernel(const uint16_t* __restrict__ dO, const uint16_t* __restrict__ O, int N, int hpr,
+                                    int64_t dt, int64_t total, float* __restrict__ Dvec) {
+  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= total) return;
+  const int64_t i = w / (static_cast<int64_t>(N) * hpr);
+  const int64_t rem = w - i * N * hpr;
+  const int64_t q = rem / hpr, jj = rem - q * hpr;
+  const int64_t off = (i * N + q) * dt + jj * HD + lane * 4;
+  const uint2 a = *reinterpret_cast<const uint2*>(dO + off);
+  const uint2 b = *reinterpret_cast<const uint2*>(O + off);
+  float a0, a1, a2, a3, b0, b1, b2, b3;
+  unpack_bf16x2(a.x, a0, a1);
+  unpack_bf16x2(a.y, a2, a3);
+  unpack_bf16x2(b.x, b0, b1);
+  unpack_bf16x2(b.y, b2, b3);
+  float sum = a0 * b0 + a1 * b1 + a2 * b2 + a3 * b3;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane == 0) Dvec[(i * hpr + jj) * N + q] = sum;
+}
+
+// Writes row `grow` (< N) of a 128-column TMEM accumulator, times `mul`, as bf16 at dst.
+__device__ __forceinline__ void tmem_row_to_bf16(uint32_t taddr, float mul, uint16_t* dst, bool write) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t r[32];
+    ptx::tmem_ld32(taddr + c * 32, r);
+    ptx::tmem_ld_wait();
+    if (write) {
+#pragma unroll
+      for (int e = 0; e < 32; e += 8) {
+        uint4 v;
+        v.x = pack_bf16x2(__uint_as_float(r[e + 0]) * mul, __uint_as_float(r[e + 1]) * mul);
+        v.y = pack_bf16x2(__uint_as_float(r[e + 2]) * mul, __uint_as_float(r[e + 3]) * mul);
+        v.z = pack_bf16x2(__uint_as_float(r[e + 4]) * mul, __uint_as_float(r[e + 5]) * mul);
+        v.w = pack_bf16x2(__uint_as_float(r[e + 6]) * mul, __uint_as_float(r[e + 7]) * mul);
+        *reinterpret_cast<uint4*>(dst + c * 32 + e) = v;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+    attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
+                        const AttnBwdArgs p) {
+  extern __shared__ uint8_t dsmem[];
+  const uint32_t pad = (1024u - (ptx::smem_addr(dsmem) & 1023u)) & 1023u;
+  uint8_t* base = dsmem + pad;
+  uint8_t* sK = base;
+  uint8_t* sV = base + TILE;
+  uint8_t* sQ = base + 2 * TILE;
+  uint8_t* sdO = base + 3 * TILE;
+  uint8_t* sP = base + 4 * TILE;
+  uint8_t* sdS = base + 5 * TILE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + 6 * TILE);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* qdo_full = bars + 1;
+  uint64_t* qdo_empty = bars + 2;
+  uint64_t* sdp_full = bars + 3;
+  uint64_t* sdp_free = bars + 4;
+  uint64_t* pds_full = bars + 5;
+  uint64_t* pds_free = bars + 6;
+  uint64_t* mma_done = bars + 7;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int head = blockIdx.x % p.H;
+  const int kb = static_cast<int>(blockIdx.x / p.H);  // early key blocks see the most query blocks (causal)
+  const int shard = head / p.hpr, jj = head - shard * p.hpr;
+  const int q_first = p.causal ? kb : 0;
+  const int nq = p.nqb - q_first;
+  const int qcol = jj * HD, kcol = static_cast<int>(p.dt) + jj * HD, vcol = static_cast<int>(2 * p.dt) + jj * HD;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(kv_full, 1);
+    ptx::mbar_init(qdo_full, 1);
+    ptx::mbar_init(qdo_empty, 1);
+    ptx::mbar_init(sdp_full, 1);
+    ptx::mbar_init(sdp_free, 128);
+    ptx::mbar_init(pds_full, 128);
+    ptx::mbar_init(pds_free, 1);
+    ptx::mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&tm_qkv);
+      ptx::tma_prefetch_desc(&tm_do);
+      ptx::mbar_arrive_expect_tx(kv_full, 2 * TILE);
+      ptx::tma_load_3d(sK, &tm_qkv, kv_full, kcol, kb * BKV, shard);
+      ptx::tma_load_3d(sK + PANEL, &tm_qkv, kv_full, kcol + 64, kb * BKV, shard);
+      ptx::tma_load_3d(sV, &tm_qkv, kv_full, vcol, kb * BKV, shard);
+      ptx::tma_load_3d(sV + PANEL, &tm_qkv, kv_full, vcol + 64, kb * BKV, shard);
+      int issued = 0;
+      for (int n = 0; n < nq; ++n) {
+        const int qi = q_first + n;
+        if (!ptx::mbar_wait(qdo_empty, (n & 1) ^ 1u, abort_flag, p.err, ERR_ATT_PRODUCER, p.timeout_ns)) break;
+        ptx::mbar_arrive_expect_tx(qdo_full, 2 * TILE);
+        ptx::tma_load_3d(sQ, &tm_qkv, qdo_full, qcol, qi * BQ, shard);
+        ptx::tma_load_3d(sQ + PANEL, &tm_qkv, qdo_full, qcol + 64, qi * BQ, shard);
+        ptx::tma_load_3d(sdO, &tm_do, qdo_full, jj * HD, qi * BQ, shard);
+        ptx::tma_load_3d(sdO + PANEL, &tm_do, qdo_full, jj * HD + 64, qi * BQ, shard);
+        ++issued;
+      }
+      volatile int never = 0;
+      ptx::mbar_wait(kv_full, 0, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
+      if (issued > 0) ptx::mbar_wait(qdo_full, (issued - 1) & 1, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_kk = ptx::idesc_bf16_f32(128, 128, false, false);  // S, dP
+      constexpr uint32_t idesc_mm = ptx::idesc_bf16_f32(128, 128, true, true);    // dV, dK
+      const uint32_t aK = ptx::smem_addr(sK), aV = ptx::smem_addr(sV), aQ = ptx::smem_addr(sQ);
+      const uint32_t adO = ptx::smem_addr(sdO), aP = ptx::smem_addr(sP), adS = ptx::smem_addr(sdS);
+      bool ok = ptx::mbar_wait(kv_full, 0, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns);
+      for (int n = 0; ok && n < nq; ++n) {
+        if (!ptx::mbar_wait(qdo_full, n & 1, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
+        if (n >= 1 && !ptx::mbar_wait(sdp_free, (n - 1) & 1, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_bf16(tS, kmajor_desc(aQ, kk), kmajor_desc(aK, kk), idesc_kk, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_bf16(tdP, kmajor_desc(adO, kk), kmajor_desc(aV, kk), idesc_kk, kk > 0 ? 1u : 0u);
+        ptx::mma_commit(sdp_full);
+        if (!ptx::mbar_wait(pds_full, n & 1, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_bf16(tdV, mnmajor_desc(aP, kk), mnmajor_desc(adO, kk), idesc_mm, (n > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_bf16(tdK, mnmajor_desc(adS, kk), mnmajor_desc(aQ, kk), idesc_mm, (n > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(pds_free);
+        ptx::mma_commit(qdo_empty);
+      }
+      ptx::mma_commit(mma_done);
+      volatile int never = 0;
+      ptx::mbar_wait(mma_done, 0, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
+    }
+  } else {
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const int64_t vec_base = (static_cast<int64_t>(shard) * p.hpr + jj) * p.N;
+    bool ok = true;
+    for (int n = 0; n < nq; ++n) {
+      const int q = (q_first + n) * BQ + row;
+      const float lse2 = q < p.N ? p.lse[vec_base + q] * kLog2e : 0.0f;
+      const float Dq = q < p.N ? p.Dvec[vec_base + q] : 0.0f;
+      if (!ptx::mbar_wait(sdp_full, n & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      if (n >= 1 && !ptx::mbar_wait(pds_free, (n - 1) & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t s[32], dp[32], wp[16], wds[16];
+        ptx::tmem_ld32(tS + lane_base + c * 32, s);
+        ptx::tmem_ld32(tdP + lane_base + c * 32, dp);
+        ptx::tmem_ld_wait();
+        p_ds_chunk(s, dp, q, kb * BKV + c * 32, p, lse2, Dq, wp, wds);
+        store_chunk_swizzled(sP, row, c, wp);
+        store_chunk_swizzled(sdS, row, c, wds);
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(sdp_free);
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(pds_full);
+    }
+    if (ok && nq > 0 && ptx::mbar_wait(pds_free, (nq - 1) & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
+      ptx::tc_fence_after();
+      const int kvrow = kb * BKV + row;  // accumulator rows are key rows
+      uint16_t* drow = p.dQKV + (static_cast<int64_t>(shard) * p.N + kvrow) * (3 * p.dt);
+      tmem_row_to_bf16(tdV + lane_base, 1.0f, drow + vcol, kvrow < p.N);
+      tmem_row_to_bf16(tdK + lane_base, p.scale, drow + kcol, kvrow < p.N);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
+                       const AttnBwdArgs p) {
+  extern __shared__ uint8_t dsmem[];
+  const uint32_t pad = (1024u - (ptx::smem_addr(dsmem) & 1023u)) & 1023u;
+  uint8_t* base = dsmem + pad;
+  uint8_t* sQ = base;
+  uint8_t* sdO = base + TILE;
+  uint8_t* sK = base + 2 * TILE;  // 2 stages
+  uint8_t* sV = base + 4 * TILE;  // 2 stages
+  uint8_t* sdS = base + 6 * TILE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + 7 * TILE);
+  uint64_t* qdo_full = bars + 0;
+  uint64_t* k_full = bars + 1;    // [2]
+  uint64_t* v_full = bars + 3;    // [2]
+  uint64_t* kv_empty = bars + 5;  // [2]
+  uint64_t* sdp_full = bars + 7;
+  uint64_t* sdp_free = bars + 8;
+  uint64_t* ds_full = bars + 9;
+  uint64_t* ds_free = bars + 10;
+  uint64_t* mma_done = bars + 11;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int head = blockIdx.x % p.H;
+  const int qb = p.nqb - 1 - static_cast<int>(blockIdx.x / p.H);
+  const int shard = head / p.hpr, jj = head - shard * p.hpr;
+  const int nkv = p.causal ? qb + 1 : (p.N + BKV - 1) / BKV;
+  const int qcol = jj * HD, kcol = static_cast<int>(p.dt) + jj * HD, vcol = static_cast<int>(2 * p.dt) + jj * HD;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(qdo_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&k_full[s], 1);
+      ptx::mbar_init(&v_full[s], 1);
+      ptx::mbar_init(&kv_empty[s], 1);
+    }
+    ptx::mbar_init(sdp_full, 1);
+    ptx::mbar_init(sdp_free, 128);
+    ptx::mbar_init(ds_full, 128);
+    ptx::mbar_init(ds_free, 1);
+    ptx::mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&tm_qkv);
+      ptx::tma_prefetch_desc(&tm_do);
+      ptx::mbar_arrive_expect_tx(qdo_full, 2 * TILE);
+      ptx::tma_load_3d(sQ, &tm_qkv, qdo_full, qcol, qb * BQ, shard);
+      ptx::tma_load_3d(sQ + PANEL, &tm_qkv, qdo_full, qcol + 64, qb * BQ, shard);
+      ptx::tma_load_3d(sdO, &tm_do, qdo_full, jj * HD, qb * BQ, shard);
+      ptx::tma_load_3d(sdO + PANEL, &tm_do, qdo_full, jj * HD + 64, qb * BQ, shard);
+      int issued = 0;
+      for (int j = 0; j < nkv; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!ptx::mbar_wait(&kv_empty[st], ph ^ 1u, abort_flag, p.err, ERR_ATT_PRODUCER, p.timeout_ns)) break;
+        ptx::mbar_arrive_expect_tx(&k_full[st], TILE);
+        ptx::tma_load_3d(sK + st * TILE, &tm_qkv, &k_full[st], kcol, j * BKV, shard);
+        ptx::tma_load_3d(sK + st * TILE + PANEL, &tm_qkv, &k_full[st], kcol + 64, j * BKV, shard);
+        ptx::mbar_arrive_expect_tx(&v_full[st], TILE);
+        ptx::tma_load_3d(sV + st * TILE, &tm_qkv, &v_full[st], vcol, j * BKV, shard);
+        ptx::tma_load_3d(sV + st * TILE + PANEL, &tm_qkv, &v_full[st], vcol + 64, j * BKV, shard);
+        ++issued;
+      }
+      volatile int never = 0;
+      ptx::mbar_wait(qdo_full, 0, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
+      for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) {
+        const uint32_t ph = (j >> 1) & 1;
+        ptx::mbar_wait(&k_full[j & 1], ph, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
+        ptx::mbar_wait(&v_full[j & 1], ph, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_kk = ptx::idesc_bf16_f32(128, 128, false, false);  // S, dP
+      constexpr uint32_t idesc_q = ptx::idesc_bf16_f32(128, 128, false, true);    // dQ = dS K
+      const uint32_t aQ = ptx::smem_addr(sQ), adO = ptx::smem_addr(sdO), adS = ptx::smem_addr(sdS);
+      bool ok = ptx::mbar_wait(qdo_full, 0, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns);
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!ptx::mbar_wait(&k_full[st], ph, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
+        if (!ptx::mbar_wait(&v_full[st], ph, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
+        if (j >= 1 && !ptx::mbar_wait(sdp_free, (j - 1) & 1, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
+        ptx::tc_fence_after();
+        const uint32_t aK = ptx::smem_addr(sK + st * TILE), aV = ptx::smem_addr(sV + st * TILE);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_bf16(tS, kmajor_desc(aQ, kk), kmajor_desc(aK, kk), idesc_kk, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_bf16(tdP, kmajor_desc(adO, kk), kmajor_desc(aV, kk), idesc_kk, kk > 0 ? 1u : 0u);
+        ptx::mma_commit(sdp_full);
+        if (!ptx::mbar_wait(ds_full, j & 1, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_bf16(tdQ, kmajor_desc(adS, kk), mnmajor_desc(aK, kk), idesc_q, (j > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(ds_free);
+        ptx::mma_commit(&kv_empty[st]);
+      }
+      ptx::mma_commit(mma_done);
+      volatile int never = 0;
+      ptx::mbar_wait(mma_done, 0, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
+    }
+  } else {
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int q = qb * BQ + row;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const int64_t vec_base = (static_cast<int64_t>(shard) * p.hpr + jj) * p.N;
+    const float lse2 = q < p.N ? p.lse[vec_base + q] * kLog2e : 0.0f;
+    const float Dq = q < p.N ? p.Dvec[vec_base + q] : 0.0f;
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      if (!ptx::mbar_wait(sdp_full, j & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      if (j >= 1 && !ptx::mbar_wait(ds_free, (j - 1) & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t s[32], dp[32], wp[16], wds[16];
+        ptx::tmem_ld32(tS + lane_base + c * 32, s);
+        ptx::tmem_ld32(tdP + lane_base + c * 32, dp);
+        ptx::tmem_ld_wait();
+        p_ds_chunk(s, dp, q, j * BKV + c * 32, p, lse2, Dq, wp, wds);
+        store_chunk_swizzled(sdS, row, c, wds);
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(sdp_free);
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(ds_full);
+    }
+    if (ok && ptx::mbar_wait(ds_free, (nkv - 1) & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
+      ptx::tc_fence_after();
+      uint16_t* drow = p.dQKV + (static_cast<int64_t>(shard) * p.N + q) * (3 * p.dt);
+      tmem_row_to_bf16(tdQ + lane_base, p.scale, drow + qcol, q < p.N);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
 }  // namespace
 
 tp_status run_attention_fwd(const uint16_t* QKV, int64_t N, int64_t d, int n_heads, int head_dim, int t, int causal,
@@ -347,6 +780,59 @@ tp_status run_attention_fwd(const uint16_t* QKV, int64_t N, int64_t d, int n_hea
   const int64_t grid = static_cast<int64_t>(n_heads) * a.nqb;
   if (grid > 0x7fffffff) return TP_ERR_SHAPE;
   attn_fwd_kernel<<<static_cast<unsigned>(grid), FWD_THREADS, FWD_SMEM, s>>>(map, a);
+  TP_LAUNCHED();
+  return TP_OK;
+}
+
+}  // namespace tp
+
+namespace tp {
+
+tp_status run_attention_bwd(const uint16_t* QKV, const uint16_t* O, const uint16_t* dO, const float* lse, int64_t N,
+                            int64_t d, int n_heads, int head_dim, int t, int causal, float scale, float* Dvec,
+                            uint16_t* dQKV, cudaStream_t s) {
+  if (N < 0 || d < 1 || n_heads < 1 || t < 1) return TP_ERR_INVALID_ARG;
+  if (head_dim != HD || static_cast<int64_t>(n_heads) * head_dim != d || n_heads % t != 0) return TP_ERR_SHAPE;
+  if (N == 0) return TP_OK;
+  if (!QKV || !O || !dO || !lse || !Dvec || !dQKV) return TP_ERR_INVALID_ARG;
+  if (!aligned16(QKV) || !aligned16(O) || !aligned16(dO) || !aligned16(dQKV)) return TP_ERR_ALIGN;
+  TP_RETURN_IF(ready());
+  const int64_t dt = d / t;
+  const int hpr = n_heads / t;
+  CUtensorMap m_qkv, m_do;
+  if (!make_map_3d_bf16(&m_qkv, QKV, 3 * dt, N, t, 3 * dt * 2, N * 3 * dt * 2, 64, 128)) return TP_ERR_CUDA;
+  if (!make_map_3d_bf16(&m_do, dO, dt, N, t, dt * 2, N * dt * 2, 64, 128)) return TP_ERR_CUDA;
+  const int64_t rows = static_cast<int64_t>(t) * N * hpr;
+  attn_bwd_dot_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, s>>>(dO, O, static_cast<int>(N), hpr,
+                                                                                     dt, rows, Dvec);
+  TP_LAUNCHED();
+  AttnBwdArgs a{};
+  a.N = static_cast<int>(N);
+  a.H = n_heads;
+  a.hpr = hpr;
+  a.nqb = static_cast<int>((N + BQ - 1) / BQ);
+  a.causal = causal ? 1 : 0;
+  a.dt = dt;
+  a.scale = scale;
+  a.scale_log2 = scale * kLog2e;
+  a.lse = lse;
+  a.Dvec = Dvec;
+  a.dQKV = dQKV;
+  a.err = device_error_word();
+  a.timeout_ns = wait_timeout_ns();
+  static bool configured[64] = {};
+  int dev = 0;
+  TP_CUDA_CHECK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return TP_ERR_CUDA;
+  if (!configured[dev]) {
+    TP_CUDA_CHECK(cudaFuncSetAttribute(attn_bwd_dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DKV_SMEM));
+    TP_CUDA_CHECK(cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM));
+    configured[dev] = true;
+  }
+  const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(n_heads) * a.nqb);
+  attn_bwd_dkv_kernel<<<grid, BWD_THREADS, DKV_SMEM, s>>>(m_qkv, m_do, a);
+  TP_LAUNCHED();
+  attn_bwd_dq_kernel<<<grid, BWD_THREADS, DQ_SMEM, s>>>(m_qkv, m_do, a);
   TP_LAUNCHED();
   return TP_OK;
 }

@@ -116,9 +116,106 @@ bool act_ok(int a) { return a >= TP_ACT_IDENTITY && a <= TP_ACT_GELU_ERF; }
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Workspace of tp_attn_backward (each piece 256-byte aligned).
+struct AttnBwdWs {
+  uint16_t* dO;
+  float* Dvec;
+  uint16_t* dQKV;
+  float* cs;
+  size_t cs_floats;
+  size_t total;
+};
+
+AttnBwdWs attn_bwd_layout(void* ws, int64_t N, int64_t d, int n_heads, int t) {
+  AttnBwdWs w{};
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  size_t off = 0;
+  w.dO = reinterpret_cast<uint16_t*>(b + off);
+  off += round_up(static_cast<size_t>(N) * d * 2, 256);
+  w.Dvec = reinterpret_cast<float*>(b + off);
+  off += round_up(static_cast<size_t>(N) * n_heads * 4, 256);
+  w.dQKV = reinterpret_cast<uint16_t*>(b + off);
+  off += round_up(static_cast<size_t>(N) * 3 * d * 2, 256);
+  w.cs = reinterpret_cast<float*>(b + off);
+  w.cs_floats = std::max(colsum_ws_floats(N, 3 * d / t) * t, colsum_ws_floats(N, d));
+  off += round_up(w.cs_floats * 4, 256);
+  w.total = off;
+  return w;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t tp_attn_backward_workspace_size(int64_t N, int64_t d, int n_heads, int head_dim, int t, unsigned flags) {
+  (void)head_dim;
+  (void)flags;
+  if (N < 0 || d < 1 || n_heads < 1 || t < 1) return 0;
+  return attn_bwd_layout(nullptr, N, d, n_heads, t).total;
+}
+
+tp_status tp_attn_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* QKV_save, const tp_bf16* O_save,
+                           const float* lse_save, int64_t N, int64_t d, int n_heads, int head_dim, int t,
+                           int causal, float scale, const tp_bf16* Wqkv_p, const tp_bf16* Wo_p, tp_bf16* dX,
+                           float* dWqkv_p, float* dbqkv_p, float* dWo_p, float* dbo, int accumulate,
+                           unsigned flags, void* ws, size_t ws_bytes, tp_stream stream) {
+  if (N < 0 || d < 1 || n_heads < 1 || t < 1 || head_dim < 1) return TP_ERR_INVALID_ARG;
+  if (flags != 0) return TP_ERR_UNSUPPORTED;
+  if (head_dim != 128 || static_cast<int64_t>(n_heads) * head_dim != d || n_heads % t != 0) return TP_ERR_SHAPE;
+  if (!dWqkv_p || !dWo_p) return TP_ERR_INVALID_ARG;
+  if (N > 0 && (!dY || !X || !QKV_save || !O_save || !lse_save || !Wqkv_p || !Wo_p || !dX)) return TP_ERR_INVALID_ARG;
+  const AttnBwdWs w = attn_bwd_layout(ws, N, d, n_heads, t);
+  if (!ws || ws_bytes < w.total) return TP_ERR_WORKSPACE;
+  if (!aligned16(ws)) return TP_ERR_ALIGN;
+  const cudaStream_t s = S(stream);
+  const int64_t dt = d / t;
+  if (N == 0) {
+    TP_RETURN_IF(ready());
+    if (!accumulate) {
+      TP_CUDA_CHECK(cudaMemsetAsync(dWqkv_p, 0, sizeof(float) * 3 * d * d, s));
+      TP_CUDA_CHECK(cudaMemsetAsync(dWo_p, 0, sizeof(float) * d * d, s));
+      if (dbqkv_p) TP_CUDA_CHECK(cudaMemsetAsync(dbqkv_p, 0, sizeof(float) * 3 * d, s));
+      if (dbo) TP_CUDA_CHECK(cudaMemsetAsync(dbo, 0, sizeof(float) * d, s));
+    }
+    return TP_OK;
+  }
+  // g backward is the identity; the output-bias gradient is taken once.
+  if (dbo) TP_RETURN_IF(run_colsum(dY, N, d, d, dbo, accumulate, w.cs, w.cs_floats, s));
+  // dO_i = dY W_o,i^T  (row-parallel W_o, input grad stays sharded).
+  GemmProblem g;
+  g.M = N; g.N = dt; g.K = d; g.nbatch = t;
+  g.a.ptr = dY; g.a.ld = d;
+  g.b.ptr = Wo_p; g.b.ld = dt; g.b.sharded = true; g.b.shard_stride = d * dt; g.b.mn_major = true;
+  g.epi = EPI_ACT; g.act = TP_ACT_IDENTITY; g.d = nullptr; g.d2 = w.dO; g.ldd = dt; g.d_batch_stride = N * dt;
+  TP_RETURN_IF(run_gemm(g, s));
+  // dW_o,i = O_i^T dY  -> packed [t][d][dt] (local).
+  GemmProblem wo;
+  wo.M = d; wo.N = dt; wo.K = N; wo.nbatch = t;
+  wo.a.ptr = dY; wo.a.ld = d; wo.a.mn_major = true;
+  wo.b.ptr = O_save; wo.b.ld = dt; wo.b.sharded = true; wo.b.shard_stride = N * dt; wo.b.mn_major = true;
+  wo.epi = EPI_F32; wo.d = dWo_p; wo.ldd = dt; wo.d_batch_stride = d * dt; wo.accumulate = accumulate;
+  TP_RETURN_IF(run_gemm(wo, s));
+  // Head-local softmax-attention backward -> dQKV_i.
+  TP_RETURN_IF(run_attention_bwd(QKV_save, O_save, w.dO, lse_save, N, d, n_heads, head_dim, t, causal, scale, w.Dvec,
+                                 w.dQKV, s));
+  if (dbqkv_p)
+    TP_RETURN_IF(run_colsum_batched(w.dQKV, N, 3 * dt, 3 * dt, t, N * 3 * dt, dbqkv_p, accumulate, w.cs, w.cs_floats,
+                                    s));
+  // dW_qkv,i = dQKV_i^T X -> packed [t][3dt][d] (local).
+  GemmProblem wq;
+  wq.M = 3 * dt; wq.N = d; wq.K = N; wq.nbatch = t;
+  wq.a.ptr = w.dQKV; wq.a.ld = 3 * dt; wq.a.sharded = true; wq.a.shard_stride = N * 3 * dt; wq.a.mn_major = true;
+  wq.b.ptr = X; wq.b.ld = d; wq.b.mn_major = true;
+  wq.epi = EPI_F32; wq.d = dWqkv_p; wq.ldd = d; wq.d_batch_stride = 3 * dt * d; wq.accumulate = accumulate;
+  TP_RETURN_IF(run_gemm(wq, s));
+  // f backward: dX = sum_i dQKV_i W_qkv,i (fixed shard order, fused).
+  GemmProblem dx;
+  dx.M = N; dx.N = d; dx.K = 3 * dt; dx.nsum = t;
+  dx.a.ptr = w.dQKV; dx.a.ld = 3 * dt; dx.a.sharded = true; dx.a.shard_stride = N * 3 * dt;
+  dx.b.ptr = Wqkv_p; dx.b.ld = d; dx.b.sharded = true; dx.b.shard_stride = 3 * dt * d; dx.b.mn_major = true;
+  dx.epi = EPI_BF16; dx.d = dX; dx.ldd = d;
+  return run_gemm(dx, s);
+}
 
 int tp_abi_version(void) { return TP_ABI_VERSION; }
 

@@ -113,5 +113,8 @@ tp_status run_ln_backward(const uint16_t* dY, const uint16_t* X, const uint16_t*
 // attention (attention.cu)
 tp_status run_attention_fwd(const uint16_t* QKV, int64_t N, int64_t d, int n_heads, int head_dim, int t, int causal,
                             float scale, uint16_t* O, float* lse, cudaStream_t s);
+tp_status run_attention_bwd(const uint16_t* QKV, const uint16_t* O, const uint16_t* dO, const float* lse, int64_t N,
+                            int64_t d, int n_heads, int head_dim, int t, int causal, float scale, float* Dvec,
+                            uint16_t* dQKV, cudaStream_t s);
 
 }  // namespace tp

@@ -56,3 +56,37 @@ def test_attention_forward_parity(N, nh, t, causal):
     assert_close("O", f64(r["O"]), np.stack(o["O"]))
     assert_close("lse", f64(r["lse"]).reshape(nh, N), o["lse"])
     assert_close("Y", f64(r["Y"]), o["Y"])
+
+
+def _ws_dqkv(ws, N, d, nh, t):
+    """dQKV inside the backward workspace (layout documented in include/tp.h)."""
+    r = lambda v: (v + 255) // 256 * 256
+    off = r(N * d * 2) + r(N * nh * 4)
+    return ws[off:off + N * 3 * d * 2].view(torch.bfloat16).view(t, N, 3 * d // t)
+
+
+@pytest.mark.parametrize("N,nh,t,causal", [(256, 2, 2, True), (200, 4, 4, True), (333, 4, 2, False),
+                                           (128, 2, 1, True), (1, 2, 2, True), (640, 8, 8, True)])
+def test_attention_backward_parity(N, nh, t, causal):
+    dh = 128
+    r = run_fwd(N, nh, t, causal, seed=3)
+    d, dev, ref, o = r["d"], r["dev"], r["ref"], r["o"]
+    Wqkv_p, _, Wo_p = r["packed"]
+    dX = torch.empty(N, d, dtype=torch.bfloat16, device="cuda")
+    dWqkv = torch.empty(t, 3 * d // t, d, dtype=torch.float32, device="cuda")
+    dbqkv = torch.empty(t, 3 * d // t, dtype=torch.float32, device="cuda")
+    dWo = torch.empty(t, d, d // t, dtype=torch.float32, device="cuda")
+    dbo = torch.empty(d, dtype=torch.float32, device="cuda")
+    nws = L.tp_attn_backward_workspace_size(N, d, nh, dh, t, 0)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    L.tp_attn_backward(dev["dY"], dev["X"], r["QKV"], r["O"], r["lse"], N, d, nh, dh, t, int(causal), r["scale"],
+                       Wqkv_p, Wo_p, dX, dWqkv, dbqkv, dWo, dbo, 0, 0, ws, nws)
+    torch.cuda.synchronize()
+    assert L.tp_get_device_status(check=False) == L.TP_OK
+    b = O.attn_backward_sharded(ref["dY"], ref["X"], ref["W_qkv"], ref["W_o"], o, nh, dh, r["scale"], t)
+    assert_close("dQKV", f64(_ws_dqkv(ws, N, d, nh, t)), np.stack(b["dQKV"]))
+    assert_close("dX", f64(dX), b["dXn"])
+    assert_close("dW_qkv (packed)", f64(dWqkv), O.pack_qkv_weight(b["dW_qkv"], nh, dh, t))
+    assert_close("db_qkv (packed)", f64(dbqkv), O.pack_qkv_bias(b["db_qkv"], nh, dh, t))
+    assert_close("dW_o (packed)", f64(dWo), O.pack_row_weight(b["dW_o"], t))
+    assert_close("db_o", f64(dbo), b["db_o"])
