@@ -207,8 +207,11 @@ tp_status tp_decode_swiglu_forward(const tp_bf16* x, int64_t M, int64_t h, int64
  *   g: Y = sum_i Y_i + b_o (+ residual), bias once.
  * X [N][d] (already normalised); Wqkv_p [t][3d/t][d]; bqkv_p [t][3d/t]
  * (nullable); Wo_p [t][d][d/t]; bo [d] (nullable); residual [N][d] (nullable);
- * Y [N][d]; QKV_save [t][N][3d/t]; O_save [t][N][d/t]; lse_save [t][H/t][N]
- * fp32 (natural-log log-sum-exp of each scaled score row).  head_dim == 128.
+ * Y [N][d]; QKV_save [t][N][3d/t] holds IEEE fp16 bits (not bf16: with
+ * logits spread over several units, fp16's 3 extra mantissa bits keep the
+ * softmax of wide models within tolerance); O_save
+ * [t][N][d/t] bf16; lse_save [t][H/t][N] fp32 (natural-log log-sum-exp of
+ * each scaled score row).  head_dim == 128.
  * flags must be 0 (TP_ERR_UNSUPPORTED otherwise); ws / ws_bytes are unused
  * (pass NULL, 0).  The attention kernel runs one CTA per (head, 128-query
  * block) with an online softmax; no N x N score matrix is ever stored. */
@@ -224,7 +227,7 @@ tp_status tp_attn_forward(const tp_bf16* X, int64_t N, int64_t d, int n_heads, i
  * dbqkv_p [t][3d/t], dWo_p [t][d][d/t], dbo [d]: fp32 (overwritten, or added to when
  * accumulate != 0; dbqkv_p / dbo nullable).  Inputs are the forward's saved
  * QKV_save, O_save, lse_save.  flags must be 0.  ws (see the size query) holds,
- * in order, each 256-byte aligned: dO [t][N][d/t] bf16, D = rowsum(dO * O)
+ * in order, each 256-byte aligned: dO [t][N][d/t] fp16, D = rowsum(dO * O)
  * [t][H/t][N] fp32, dQKV [t][N][3d/t] bf16, column-sum scratch.  The
  * attention gradient runs as two deterministic kernels (dK/dV per key block,
  * dQ per query block); scores are recomputed from the saved log-sum-exp. */

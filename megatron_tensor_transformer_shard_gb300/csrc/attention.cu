@@ -5,6 +5,10 @@
 //
 // The QKV buffer is the column-parallel GEMM's output, [t][N][3d/t] with the
 // shard's heads laid out [Q_i | K_i | V_i], head jj at columns jj*128 of each.
+// Q, K, V, P (and in backward dO, dS) are IEEE fp16: the logits of a wide
+// model have a spread of several units, and a 2^-9 relative rounding of Q
+// and K (bf16) turns into a ~1% error of P; fp16 keeps 3 more mantissa bits
+// at the same cost.  Inputs, weights and O / dQKV stay bf16.
 //
 // Forward: one CTA per (head, 128-query block), heavy (late) query blocks first.
 //   warp 0      TMA: Q once, then K_j / V_j through a 2-stage ring
@@ -162,8 +166,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(BQ, BKV, false, false);
-      constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(BQ, HD, false, true);
+      constexpr uint32_t idesc_s = ptx::idesc_f16_f32(BQ, BKV, false, false);
+      constexpr uint32_t idesc_o = ptx::idesc_f16_f32(BQ, HD, false, true);
       const uint32_t aQ = ptx::smem_addr(sQ), aP = ptx::smem_addr(sP);
       bool ok = ptx::mbar_wait(q_full, 0, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns);
       for (int j = 0; ok && j <= nkv; ++j) {
@@ -247,7 +251,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         const float p0 = ptx::exp2_approx(s[c] - m_new);
         const float p1 = ptx::exp2_approx(s[c + 1] - m_new);
         rs += p0 + p1;
-        w[c >> 1] = pack_bf16x2(p0, p1);
+        w[c >> 1] = pack_f16x2(p0, p1);
       }
       l = l * alpha + rs;
       m = m_new;
@@ -364,8 +368,8 @@ __device__ __forceinline__ void p_ds_chunk(const uint32_t (&s)[32], const uint32
       pv[u] = pr;
       dv[u] = pr * (__uint_as_float(dp[e + u]) - Dq);
     }
-    wp[e >> 1] = pack_bf16x2(pv[0], pv[1]);
-    wds[e >> 1] = pack_bf16x2(dv[0], dv[1]);
+    wp[e >> 1] = pack_f16x2(pv[0], pv[1]);
+    wds[e >> 1] = pack_f16x2(dv[0], dv[1]);
   }
 }
 
@@ -381,8 +385,8 @@ __global__ void attn_bwd_dot_kernel(const uint16_t* __restrict__ dO, const uint1
   const uint2 a = *reinterpret_cast<const uint2*>(dO + off);
   const uint2 b = *reinterpret_cast<const uint2*>(O + off);
   float a0, a1, a2, a3, b0, b1, b2, b3;
-  unpack_bf16x2(a.x, a0, a1);
-  unpack_bf16x2(a.y, a2, a3);
+  unpack_f16x2(a.x, a0, a1);  // dO is fp16, O is bf16
+  unpack_f16x2(a.y, a2, a3);
   unpack_bf16x2(b.x, b0, b1);
   unpack_bf16x2(b.y, b2, b3);
   float sum = a0 * b0 + a1 * b1 + a2 * b2 + a3 * b3;
@@ -492,8 +496,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_kk = ptx::idesc_bf16_f32(128, 128, false, false);  // S, dP
-      constexpr uint32_t idesc_mm = ptx::idesc_bf16_f32(128, 128, true, true);    // dV, dK
+      constexpr uint32_t idesc_kk = ptx::idesc_f16_f32(128, 128, false, false);  // S, dP
+      constexpr uint32_t idesc_mm = ptx::idesc_f16_f32(128, 128, true, true);    // dV, dK
       const uint32_t aK = ptx::smem_addr(sK), aV = ptx::smem_addr(sV), aQ = ptx::smem_addr(sQ);
       const uint32_t adO = ptx::smem_addr(sdO), aP = ptx::smem_addr(sP), adS = ptx::smem_addr(sdS);
       bool ok = ptx::mbar_wait(kv_full, 0, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns);
@@ -663,8 +667,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_kk = ptx::idesc_bf16_f32(128, 128, false, false);  // S, dP
-      constexpr uint32_t idesc_q = ptx::idesc_bf16_f32(128, 128, false, true);    // dQ = dS K
+      constexpr uint32_t idesc_kk = ptx::idesc_f16_f32(128, 128, false, false);  // S, dP
+      constexpr uint32_t idesc_q = ptx::idesc_f16_f32(128, 128, false, true);    // dQ = dS K
       const uint32_t aQ = ptx::smem_addr(sQ), adO = ptx::smem_addr(sdO), adS = ptx::smem_addr(sdS);
       bool ok = ptx::mbar_wait(qdo_full, 0, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns);
       for (int j = 0; ok && j < nkv; ++j) {

@@ -186,7 +186,8 @@ tp_status tp_attn_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Q
   g.M = N; g.N = dt; g.K = d; g.nbatch = t;
   g.a.ptr = dY; g.a.ld = d;
   g.b.ptr = Wo_p; g.b.ld = dt; g.b.sharded = true; g.b.shard_stride = d * dt; g.b.mn_major = true;
-  g.epi = EPI_ACT; g.act = TP_ACT_IDENTITY; g.d = nullptr; g.d2 = w.dO; g.ldd = dt; g.d_batch_stride = N * dt;
+  g.epi = EPI_ACT; g.act = TP_ACT_IDENTITY; g.out_f16 = 1;  // dO feeds the fp16 attention kernels
+  g.d = nullptr; g.d2 = w.dO; g.ldd = dt; g.d_batch_stride = N * dt;
   TP_RETURN_IF(run_gemm(g, s));
   // dW_o,i = O_i^T dY  -> packed [t][d][dt] (local).
   GemmProblem wo;
@@ -466,9 +467,16 @@ tp_status tp_attn_forward(const tp_bf16* X, int64_t N, int64_t d, int n_heads, i
   if (head_dim != 128 || static_cast<int64_t>(n_heads) * head_dim != d || n_heads % t != 0) return TP_ERR_SHAPE;
   if (N == 0) return TP_OK;
   if (!X || !Wqkv_p || !Wo_p || !Y || !QKV_save || !O_save || !lse_save) return TP_ERR_INVALID_ARG;
-  // f (identity) + column-parallel W_qkv by head: QKV_i = X W_qkv,i + b_qkv,i.
-  TP_RETURN_IF(tp_column_parallel_forward(X, N, d, 3 * d, t, TP_ACT_IDENTITY, Wqkv_p, bqkv_p, nullptr, QKV_save,
-                                          stream));
+  // f (identity) + column-parallel W_qkv by head: QKV_i = X W_qkv,i + b_qkv,i, stored fp16.
+  const int64_t dt = d / t;
+  GemmProblem c;
+  c.M = N; c.N = 3 * dt; c.K = d; c.nbatch = t;
+  c.a.ptr = X; c.a.ld = d;
+  c.b.ptr = Wqkv_p; c.b.ld = d; c.b.sharded = true; c.b.shard_stride = 3 * dt * d;
+  c.epi = EPI_ACT; c.act = TP_ACT_IDENTITY; c.out_f16 = 1;
+  c.d = nullptr; c.d2 = QKV_save; c.ldd = 3 * dt; c.d_batch_stride = N * 3 * dt;
+  c.bias = bqkv_p; c.bias_batch_stride = 3 * dt;
+  TP_RETURN_IF(run_gemm(c, S(stream)));
   // Attention on each shard's own heads, no communication.
   TP_RETURN_IF(run_attention_fwd(QKV_save, N, d, n_heads, head_dim, t, causal, scale, O_save, lse_save, S(stream)));
   // Row-parallel W_o + g: Y = sum_i O_i W_o,i + b_o (once) + residual.

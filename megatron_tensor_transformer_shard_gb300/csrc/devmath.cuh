@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 #include "tp.h"
@@ -29,6 +30,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 __device__ __forceinline__ void unpack_bf16x2(uint32_t w, float& a, float& b) {
   a = __uint_as_float(w << 16);
   b = __uint_as_float(w & 0xFFFF0000u);
+}
+
+// IEEE fp16 pairs (the attention kernels keep Q, K, V, P, dO and dS in fp16).
+__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void unpack_f16x2(uint32_t w, float& a, float& b) {
+  __half2 h = *reinterpret_cast<__half2*>(&w);
+  const float2 f = __half22float2(h);
+  a = f.x;
+  b = f.y;
 }
 
 __device__ __forceinline__ float tanh_fast(float x) {

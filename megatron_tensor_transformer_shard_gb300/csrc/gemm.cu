@@ -67,6 +67,7 @@ struct GemmArgs {
   const uint16_t* res;
   int64_t ld_res;
   int accumulate;
+  int out_f16;
   int* err;
   uint64_t timeout_ns;
 };
@@ -88,6 +89,24 @@ __device__ __forceinline__ void load_bf16x32(const uint16_t* src, float (&v)[32]
     unpack_bf16x2(w.z, v[8 * q + 4], v[8 * q + 5]);
     unpack_bf16x2(w.w, v[8 * q + 6], v[8 * q + 7]);
   }
+}
+
+__device__ __forceinline__ void store_f16x32(uint16_t* dst, const float (&v)[32]) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w;
+    w.x = pack_f16x2(v[8 * q + 0], v[8 * q + 1]);
+    w.y = pack_f16x2(v[8 * q + 2], v[8 * q + 3]);
+    w.z = pack_f16x2(v[8 * q + 4], v[8 * q + 5]);
+    w.w = pack_f16x2(v[8 * q + 6], v[8 * q + 7]);
+    d4[q] = w;
+  }
+}
+
+__device__ __forceinline__ uint16_t float_to_f16_bits(float f) {
+  __half h = __float2half_rn(f);
+  return *reinterpret_cast<uint16_t*>(&h);
 }
 
 __device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float (&v)[32]) {
@@ -167,14 +186,24 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& p, int b, int m, 
     }
     if (p.d) {  // save Z for the backward pass
       uint16_t* zp = static_cast<uint16_t*>(p.d) + b * p.d_bs + static_cast<int64_t>(m) * p.ldd + n0;
-      if (full) store_bf16x32(zp, v);
-      else _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) zp[j] = float_to_bf16_bits(v[j]);
+      if (full) {
+        if (p.out_f16) store_f16x32(zp, v);
+        else store_bf16x32(zp, v);
+      } else {
+        _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) zp[j] =
+            p.out_f16 ? float_to_f16_bits(v[j]) : float_to_bf16_bits(v[j]);
+      }
     }
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = act_apply(p.act, v[j]);
     uint16_t* ap = static_cast<uint16_t*>(p.d2) + b * p.d_bs + static_cast<int64_t>(m) * p.ldd + n0;
-    if (full) store_bf16x32(ap, v);
-    else _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) ap[j] = float_to_bf16_bits(v[j]);
+    if (full) {
+      if (p.out_f16) store_f16x32(ap, v);
+      else store_bf16x32(ap, v);
+    } else {
+      _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) ap[j] =
+          p.out_f16 ? float_to_f16_bits(v[j]) : float_to_bf16_bits(v[j]);
+    }
     return;
   } else {  // EPI_DACT
     const uint16_t* zp = p.aux + b * p.aux_bs + static_cast<int64_t>(m) * p.ld_aux + n0;
@@ -515,6 +544,7 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
   a.res = P.residual;
   a.ld_res = P.ld_res;
   a.accumulate = P.accumulate;
+  a.out_f16 = P.out_f16;
   a.err = device_error_word();
   a.timeout_ns = wait_timeout_ns();
   if (!a.err) return TP_ERR_CUDA;

@@ -77,6 +77,7 @@ struct GemmProblem {
   const uint16_t* residual = nullptr;
   int64_t ld_res = 0;
   int accumulate = 0;
+  int out_f16 = 0;  // EPI_ACT only: write D / D2 as IEEE fp16 instead of bf16
 };
 
 tp_status run_gemm(const GemmProblem& p, cudaStream_t s);

@@ -96,3 +96,93 @@ class TPMLPFunction(torch.autograd.Function):
         g = mlp_backward(dY.contiguous(), X, Z, A, w, ctx.act, grads=prev)
         w.grads = {k: g[k] for k in ("dWup_p", "dWdown_p", "dbup", "dbdown")}
         return g["dX"], None, None
+
+
+# --------------------------------------------------------------------------
+# One pre-LN transformer layer: X1 = X + Attn(LN1(X)); Y = X1 + MLP(LN2(X1)).
+# With sp=True the LayerNorms and residual adds run on t sequence shards
+# ([t][s/t][h], the same bytes as [s][h], so the all-gather entering each TP
+# region and the reduce-scatter leaving it are zero-copy) and the LayerNorm
+# weight gradients are summed over the shards ("Tensor and sequence
+# parallelism", section "Sequence parallelism").  Without SP the LayerNorms are
+# replicated: on one GPU that is one LayerNorm over all rows.
+# --------------------------------------------------------------------------
+
+class LayerWeights:
+    """Packed per-shard weights of one layer (bf16, device)."""
+
+    def __init__(self, p, n_heads, head_dim, t):
+        d = p["W_qkv"].shape[0]
+        F = p["W_up"].shape[1]
+        dev = p["W_qkv"].device
+        self.d, self.F, self.t, self.n_heads, self.head_dim = d, F, t, n_heads, head_dim
+        self.Wqkv_p = torch.empty(t, 3 * d // t, d, dtype=BF16, device=dev)
+        self.bqkv_p = torch.empty(t, 3 * d // t, dtype=BF16, device=dev)
+        self.Wo_p = torch.empty(t, d, d // t, dtype=BF16, device=dev)
+        L.tp_pack_qkv_heads(p["W_qkv"], d, n_heads, head_dim, t, self.Wqkv_p)
+        L.tp_pack_qkv_bias(p["b_qkv"], d, n_heads, head_dim, t, self.bqkv_p)
+        L.tp_pack_row(p["W_o"], d, d, t, self.Wo_p)
+        self.mlp = MLPWeights(p["W_up"], p["b_up"], p["W_down"], p["b_down"], t)
+        self.b_o = p["b_o"]
+        self.ln1_g, self.ln1_b, self.ln2_g, self.ln2_b = p["ln1_g"], p["ln1_b"], p["ln2_g"], p["ln2_b"]
+
+
+def layer_forward(X, w: LayerWeights, act="gelu_tanh", causal=True, scale=None, eps=1e-5, sp=False):
+    """Returns (Y, saved).  X: [s][h] bf16 ([t][s/t][h] when sp)."""
+    s = X.shape[0] if X.dim() == 2 else X.shape[0] * X.shape[1]
+    X = X.reshape(s, w.d)
+    d, t, dev = w.d, w.t, X.device
+    t_ln = t if sp else 1
+    scale = (1.0 / w.head_dim ** 0.5) if scale is None else scale
+    f32 = torch.float32
+    Xn1 = torch.empty(s, d, dtype=BF16, device=dev)
+    m1 = torch.empty(s, dtype=f32, device=dev)
+    r1 = torch.empty(s, dtype=f32, device=dev)
+    L.tp_sp_layernorm_forward(X, s, d, t_ln, w.ln1_g, w.ln1_b, eps, Xn1, m1, r1)
+    X1 = torch.empty(s, d, dtype=BF16, device=dev)
+    QKV = torch.empty(t, s, 3 * d // t, dtype=torch.float16, device=dev)  # fp16 attention operands
+    O = torch.empty(t, s, d // t, dtype=BF16, device=dev)
+    lse = torch.empty(t, w.n_heads // t, s, dtype=f32, device=dev)
+    L.tp_attn_forward(Xn1, s, d, w.n_heads, w.head_dim, t, int(causal), scale, w.Wqkv_p, w.bqkv_p, w.Wo_p, w.b_o,
+                      X, X1, QKV, O, lse, 0, None, 0)
+    Xn2 = torch.empty(s, d, dtype=BF16, device=dev)
+    m2 = torch.empty(s, dtype=f32, device=dev)
+    r2 = torch.empty(s, dtype=f32, device=dev)
+    L.tp_sp_layernorm_forward(X1, s, d, t_ln, w.ln2_g, w.ln2_b, eps, Xn2, m2, r2)
+    Y, Z, A = mlp_forward(Xn2, w.mlp, act, residual=X1)
+    saved = dict(X=X, Xn1=Xn1, m1=m1, r1=r1, X1=X1, QKV=QKV, O=O, lse=lse, Xn2=Xn2, m2=m2, r2=r2, Z=Z, A=A,
+                 s=s, scale=scale, causal=causal, act=act, t_ln=t_ln)
+    return Y, saved
+
+
+def layer_backward(G, saved, w: LayerWeights):
+    """Gradients of <Y, G>: dict with dX and every parameter gradient (packed, fp32)."""
+    s, d, t, dev = saved["s"], w.d, w.t, G.device
+    G = G.reshape(s, d)
+    f32 = torch.float32
+    g = mlp_backward(G, saved["Xn2"], saved["Z"], saved["A"], w.mlp, saved["act"])
+    t_ln = saved["t_ln"]
+    dX1 = torch.empty(s, d, dtype=BF16, device=dev)
+    ln2 = {k: torch.empty(*shape, dtype=f32, device=dev) for k, shape in
+           (("gp", (t_ln, d)), ("bp", (t_ln, d)), ("g", (d,)), ("b", (d,)))}
+    L.tp_sp_layernorm_backward(g["dX"], saved["X1"], w.ln2_g, saved["m2"], saved["r2"], G, s, d, t_ln, dX1,
+                               ln2["gp"], ln2["bp"], ln2["g"], ln2["b"])
+    dXn1 = torch.empty(s, d, dtype=BF16, device=dev)
+    dWqkv = torch.empty(t, 3 * d // t, d, dtype=f32, device=dev)
+    dbqkv = torch.empty(t, 3 * d // t, dtype=f32, device=dev)
+    dWo = torch.empty(t, d, d // t, dtype=f32, device=dev)
+    dbo = torch.empty(d, dtype=f32, device=dev)
+    nws = L.tp_attn_backward_workspace_size(s, d, w.n_heads, w.head_dim, t, 0)
+    ws = _ws(nws, dev)
+    L.tp_attn_backward(dX1, saved["Xn1"], saved["QKV"], saved["O"], saved["lse"], s, d, w.n_heads, w.head_dim, t,
+                       int(saved["causal"]), saved["scale"], w.Wqkv_p, w.Wo_p, dXn1, dWqkv, dbqkv, dWo, dbo, 0, 0,
+                       ws, nws)
+    dX = torch.empty(s, d, dtype=BF16, device=dev)
+    ln1 = {k: torch.empty(*shape, dtype=f32, device=dev) for k, shape in
+           (("gp", (t_ln, d)), ("bp", (t_ln, d)), ("g", (d,)), ("b", (d,)))}
+    L.tp_sp_layernorm_backward(dXn1, saved["X"], w.ln1_g, saved["m1"], saved["r1"], dX1, s, d, t_ln, dX,
+                               ln1["gp"], ln1["bp"], ln1["g"], ln1["b"])
+    return {"dX": dX, "dX1": dX1, "ln1_g": ln1["g"], "ln1_b": ln1["b"], "ln2_g": ln2["g"], "ln2_b": ln2["b"],
+            "ln1_g_part": ln1["gp"], "ln2_g_part": ln2["gp"],
+            "Wqkv_p": dWqkv, "bqkv_p": dbqkv, "Wo_p": dWo, "b_o": dbo,
+            "Wup_p": g["dWup_p"], "b_up": g["dbup"], "Wdown_p": g["dWdown_p"], "b_down": g["dbdown"]}

@@ -32,7 +32,7 @@ __all__ = [
     "attn_forward_unsplit", "attn_forward_sharded", "attn_backward_unsplit", "attn_backward_sharded",
     "layernorm_forward", "layernorm_backward", "sp_layernorm_forward", "sp_layernorm_backward",
     "all_gather_seq", "reduce_scatter_seq",
-    "layer_forward", "layer_backward",
+    "layer_forward", "layer_backward", "layer_forward_rows",
     "expanded_tensor_bytes", "reduction_tensor_bytes", "allreduce_payload_bytes",
     "mlp_fwd_bwd_flops",
 ]
@@ -666,6 +666,21 @@ def layer_backward(G, X, p, cfg, t, fwd, sp=False):
     return {"dX": dX, "ln1_g": dg1, "ln1_b": db1, "ln2_g": dg2, "ln2_b": db2,
             "W_qkv": ag["dW_qkv"], "b_qkv": ag["db_qkv"], "W_o": ag["dW_o"], "b_o": ag["db_o"],
             "W_up": mg["dW_up"], "b_up": mg["db_up"], "W_down": mg["dW_down"], "b_down": mg["db_down"]}
+
+
+def layer_forward_rows(X, p, cfg, t, rows):
+    """:func:`layer_forward` (replicated LayerNorms) at the output rows `rows`
+    only.  Attention needs every row's K and V, so the attention branch runs on
+    all rows; LN2 and the MLP act row by row, so they run on `rows` alone.
+    The sequence-parallel form gives the same rows (it only regroups them)."""
+    nh, dh, eps = cfg["n_heads"], cfg["head_dim"], cfg["eps"]
+    Xn1, _, _ = layernorm_forward(X, p["ln1_g"], p["ln1_b"], eps)
+    at = attn_forward_sharded(Xn1, p["W_qkv"], p["b_qkv"], p["W_o"], p["b_o"], nh, dh, cfg["causal"],
+                              cfg["scale"], t)
+    X1 = X[rows] + at["Y"][rows]
+    Xn2, _, _ = layernorm_forward(X1, p["ln2_g"], p["ln2_b"], eps)
+    ml = mlp_forward_sharded(Xn2, p["W_up"], p["b_up"], p["W_down"], p["b_down"], cfg["act"], t)
+    return {"X1": X1, "Y": X1 + ml["Y"]}
 
 
 # ---------------------------------------------------------------------------

@@ -33,7 +33,7 @@ def run_fwd(N, nh, t, causal, seed=0, dh=128):
     dev = {k: v.cuda() for k, v in inp.items()}
     Wqkv_p, bqkv_p, Wo_p = pack_attn(dev, d, nh, dh, t)
     Y = torch.empty(N, d, dtype=torch.bfloat16, device="cuda")
-    QKV = torch.empty(t, N, 3 * d // t, dtype=torch.bfloat16, device="cuda")
+    QKV = torch.empty(t, N, 3 * d // t, dtype=torch.float16, device="cuda")
     Osv = torch.empty(t, N, d // t, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(t, nh // t, N, dtype=torch.float32, device="cuda")
     scale = 1.0 / math.sqrt(dh)

@@ -399,3 +399,14 @@ def test_bf16_conversion():
     # round-to-nearest-even: 1 + 2^-8 is halfway between 1 and 1 + 2^-7 -> even (1.0)
     assert O.f64_to_bf16_bits(np.array([1 + 2 ** -8]))[0] == 0x3F80
     assert O.f64_to_bf16_bits(np.array([1 + 3 * 2 ** -8]))[0] == 0x3F82
+
+
+def test_layer_forward_rows_matches_full_layer():
+    rng = np.random.default_rng(32)
+    p, cfg = _tiny_layer(rng, s=6, d=4)
+    X = rng.normal(size=(6, 4))
+    full = O.layer_forward(X, p, cfg, 2, False)
+    rows = [0, 3, 5]
+    part = O.layer_forward_rows(X, p, cfg, 2, rows)
+    assert np.array_equal(part["X1"], full["X1"][rows])
+    assert np.abs(part["Y"] - full["Y"][rows]).max() < 1e-13
