@@ -292,7 +292,11 @@ def run_ours(args):
 
     secondary = None
     if not args.no_extras and rank == 0:
-        secondary = run_decode_extra(L, torch, args)
+        del Z, A, dWup, dWdown, ws
+        torch.cuda.empty_cache()
+        secondary = {"decode_c3": run_decode_extra(L, torch, args), "mlp_fwd_c1": run_mlp_fwd_extra(L, torch, args),
+                     "layer_c4": run_layer_extra(L, torch, args, "c4"),
+                     "sp_layer_c5": run_layer_extra(L, torch, args, "c5")}
 
     if rank != 0:
         return None
@@ -325,6 +329,19 @@ def run_ours(args):
     return line
 
 
+def _time(torch, fn, iters, warmup=3):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters  # ms
+
+
 def run_decode_extra(L, torch, args):
     """Decode-shaped SwiGLU GEMV (x 1x8192, W_gate/W_up 8192x28672, W_down
     28672x8192, t = 4): HBM GB/s of the whole decode step (two kernels)."""
@@ -339,17 +356,8 @@ def run_decode_extra(L, torch, args):
     del inp["W_gate"], inp["W_up"], inp["W_down"]
     y = torch.empty(M, h, dtype=torch.bfloat16, device="cuda")
     a = torch.empty(M, F, dtype=torch.bfloat16, device="cuda")
-    for _ in range(5):
-        L.tp_decode_swiglu_forward(inp["X"], M, h, F, t, Wgu, Wd, y, a)
-    torch.cuda.synchronize()
-    n = max(20, args.steps)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(n):
-        L.tp_decode_swiglu_forward(inp["X"], M, h, F, t, Wgu, Wd, y, a)
-    e1.record()
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) / n * 1e3
+    us = 1e3 * _time(torch, lambda: L.tp_decode_swiglu_forward(inp["X"], M, h, F, t, Wgu, Wd, y, a),
+                     max(20, args.steps), warmup=5)
     nbytes = 3 * h * F * 2 + M * h * 2 * 2 + M * F * 2 * 2
     gbs = nbytes / (us / 1e6) / 1e9
     peaks = measured_peaks()
@@ -357,6 +365,78 @@ def run_decode_extra(L, torch, args):
             "us_per_step": round(us, 2), "GBps": round(gbs, 1), "bytes_per_step": nbytes,
             "frac_of_hbm": round(gbs / peaks["hbm"], 4), "hbm_peak_GBps": peaks["hbm"],
             "frac_of_8TBps": round(gbs / 8000.0, 4), "l2": "1.41 GB of weights > L2; no flush"}
+
+
+def run_mlp_fwd_extra(L, torch, args):
+    """The forward-only MLP workload: t = 2, X 128x1024, 1024 -> 4096 -> 1024."""
+    from megatron_tensor_transformer_shard_gb300 import inputs as I
+    from megatron_tensor_transformer_shard_gb300 import tp as T
+    c = I.CONFIGS["c1"]
+    M, h, F, t = c["M"], c["h"], c["F"], c["t"]
+    inp = I.mlp_inputs(M, h, F, bias=True, dy=False, seed=0, device="cuda")
+    w = T.MLPWeights(inp["W_up"], inp["b_up"], inp["W_down"], inp["b_down"], t)
+    Y = torch.empty(M, h, dtype=torch.bfloat16, device="cuda")
+    A = torch.empty(t, M, F // t, dtype=torch.bfloat16, device="cuda")
+    act = L.ACT_BY_NAME["gelu_tanh"]
+    ms = _time(torch, lambda: L.tp_mlp_forward(inp["X"], M, h, F, t, act, w.Wup_p, w.b_up, w.Wdown_p, w.b_down,
+                                               None, Y, None, A, 0, None, 0), max(50, args.steps), warmup=10)
+    fl = 4.0 * M * h * F
+    return {"workload": "TP-MLP forward, t=2, X 128x1024, W_up 1024x4096, W_down 4096x1024, GeLU(tanh)",
+            "us_per_step": round(ms * 1e3, 2), "TFLOPs": round(fl / (ms / 1e3) / 1e12, 2),
+            "flops_per_step": fl, "l2": "8.4 MB of weights stay in L2 (no flush): latency-bound, 32 + 16 tiles",
+            "page_bytes": {"expanded_tensor": M * F * 2, "output_reduction_tensor": M * h * 2}}
+
+
+def layer_flops(N, d, F):
+    """fwd = QKV + W_o + MLP GEMMs + causal attention (unmasked half); fwd+bwd = 3 x fwd."""
+    fwd = 2.0 * N * d * 3 * d + 2.0 * N * d * d + 4.0 * N * d * F + 2.0 * N * N * d
+    return 3.0 * fwd
+
+
+def run_layer_extra(L, torch, args, name):
+    from megatron_tensor_transformer_shard_gb300 import inputs as I
+    from megatron_tensor_transformer_shard_gb300 import tp as T
+    c = I.CONFIGS[name]
+    N, d, F, t, nh, sp = c["N"], c["d"], c["F"], c["t"], c["n_heads"], c["sp"]
+    inp = I.layer_inputs(N, d, F, seed=0, device="cuda")
+    w = T.LayerWeights(inp, nh, c["head_dim"], t)
+    for k in ("W_qkv", "W_o", "W_up", "W_down"):
+        del inp[k]
+    X, G = inp["X"], inp["dY"]
+
+    def step():
+        Y, saved = T.layer_forward(X, w, sp=sp)
+        T.layer_backward(G, saved, w)
+
+    ms = _time(torch, step, max(5, min(args.steps, 20)), warmup=3)
+    fl = layer_flops(N, d, F)
+    peak = measured_peaks()["bf16_burst"]
+    out = {"workload": (f"{'sequence-parallel ' if sp else ''}TP layer fwd+bwd, t={t}, N={N}, d={d}, "
+                        f"{nh} heads x {c['head_dim']}, MLP {d}->{F}, causal"),
+           "ms_per_step": round(ms, 3), "TFLOPs": round(fl / (ms / 1e3) / 1e12, 1), "flops_per_step": fl,
+           "frac_of_peak": round(fl / (ms / 1e3) / 1e12 / peak, 4)}
+    if sp:   # SP LayerNorm kernels alone (HBM-bound)
+        s, h = N, d
+        Xn = torch.empty(s, h, dtype=torch.bfloat16, device="cuda")
+        mean = torch.empty(s, dtype=torch.float32, device="cuda")
+        rstd = torch.empty(s, dtype=torch.float32, device="cuda")
+        f_ms = _time(torch, lambda: L.tp_sp_layernorm_forward(X, s, h, t, w.ln1_g, w.ln1_b, 1e-5, Xn, mean, rstd), 20)
+        dX = torch.empty(s, h, dtype=torch.bfloat16, device="cuda")
+        parts = [torch.empty(t, h, dtype=torch.float32, device="cuda") for _ in range(2)]
+        dg, db = (torch.empty(h, dtype=torch.float32, device="cuda") for _ in range(2))
+        b_ms = _time(torch, lambda: L.tp_sp_layernorm_backward(G, X, w.ln1_g, mean, rstd, X, s, h, t, dX, parts[0],
+                                                               parts[1], dg, db), 20)
+        fwd_bytes = 2 * s * h * 2 + 2 * h * 2 + 2 * s * 4
+        bwd_bytes = 6 * s * h * 2 + s * 8 + 2 * t * h * 4 * 2
+        hbm = measured_peaks()["hbm"]
+        out["sp_layernorm"] = {"fwd_us": round(f_ms * 1e3, 2), "fwd_GBps": round(fwd_bytes / f_ms / 1e6, 1),
+                               "fwd_frac_of_hbm": round(fwd_bytes / f_ms / 1e6 / hbm, 4),
+                               "bwd_us": round(b_ms * 1e3, 2), "bwd_GBps": round(bwd_bytes / b_ms / 1e6, 1),
+                               "bwd_frac_of_hbm": round(bwd_bytes / b_ms / 1e6 / hbm, 4),
+                               "shape": f"[{t}][{s // t}][{h}]"}
+    del w, inp
+    torch.cuda.empty_cache()
+    return out
 
 
 # ----------------------------------------------------------- oracle (CPU)

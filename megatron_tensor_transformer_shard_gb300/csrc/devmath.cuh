@@ -88,6 +88,38 @@ __device__ __forceinline__ float act_grad(int act, float z) {
   }
 }
 
+// Compile-time forms: one activation per kernel instantiation keeps the
+// unrolled epilogue small.
+template <int ACT>
+__device__ __forceinline__ float act_apply_t(float z) {
+  if constexpr (ACT == TP_ACT_RELU) {
+    return fmaxf(z, 0.0f);
+  } else if constexpr (ACT == TP_ACT_GELU_TANH) {
+    const float u = kSqrt2OverPi * fmaf(kGeluC * z, z * z, z);
+    return 0.5f * z * (1.0f + tanh_fast(u));
+  } else if constexpr (ACT == TP_ACT_GELU_ERF) {
+    return 0.5f * z * (1.0f + erff(z * kInvSqrt2));
+  } else {
+    return z;
+  }
+}
+
+template <int ACT>
+__device__ __forceinline__ float act_grad_t(float z) {
+  if constexpr (ACT == TP_ACT_RELU) {
+    return z > 0.0f ? 1.0f : 0.0f;
+  } else if constexpr (ACT == TP_ACT_GELU_TANH) {
+    const float u = kSqrt2OverPi * fmaf(kGeluC * z, z * z, z);
+    const float th = tanh_fast(u);
+    const float du = kSqrt2OverPi * fmaf(3.0f * kGeluC * z, z, 1.0f);
+    return 0.5f * (1.0f + th) + 0.5f * z * (1.0f - th * th) * du;
+  } else if constexpr (ACT == TP_ACT_GELU_ERF) {
+    return 0.5f * (1.0f + erff(z * kInvSqrt2)) + z * kInvSqrt2Pi * expf(-0.5f * z * z);
+  } else {
+    return 1.0f;
+  }
+}
+
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 }  // namespace tp

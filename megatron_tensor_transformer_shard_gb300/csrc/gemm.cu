@@ -27,6 +27,9 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+#include <cstring>
+#include <type_traits>
 #include <mutex>
 
 #include "devmath.cuh"
@@ -68,6 +71,7 @@ struct GemmArgs {
   int64_t ld_res;
   int accumulate;
   int out_f16;
+  int tma_store;  // pair kernel: outputs staged in shared memory and written by TMA bulk stores
   int* err;
   uint64_t timeout_ns;
 };
@@ -124,6 +128,7 @@ __device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float (&v)[32
 
 // Epilogue for 32 consecutive columns n0..n0+31 of row m of output batch b.
 // `full` = all 32 columns are inside N (vector path); else column-by-column.
+template <int EPI, int ACT>
 __device__ __forceinline__ void epilogue_chunk(const GemmArgs& p, int b, int m, int n0, const uint32_t (&r)[32]) {
   float v[32];
 #pragma unroll
@@ -131,7 +136,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& p, int b, int m, 
   const bool full = (n0 + 32 <= p.N);
   const int ncols = full ? 32 : (p.N - n0);
 
-  if (p.epi == EPI_F32) {
+  if constexpr (EPI == EPI_F32) {
     float* dst = static_cast<float*>(p.d) + b * p.d_bs + static_cast<int64_t>(m) * p.ldd + n0;
     if (full) {
       float4* d4 = reinterpret_cast<float4*>(dst);
@@ -150,7 +155,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& p, int b, int m, 
     return;
   }
 
-  if (p.epi == EPI_BF16) {
+  if constexpr (EPI == EPI_BF16) {
     if (p.bias) {
       if (full) {
         float bb[32];
@@ -172,7 +177,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& p, int b, int m, 
         _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) v[j] += bf16_bits_to_float(rp[j]);
       }
     }
-  } else if (p.epi == EPI_ACT) {
+  } else if constexpr (EPI == EPI_ACT) {
     if (p.bias) {
       const uint16_t* bp = p.bias + b * p.bias_bs + n0;
       if (full) {
@@ -195,7 +200,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& p, int b, int m, 
       }
     }
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = act_apply(p.act, v[j]);
+    for (int j = 0; j < 32; ++j) v[j] = act_apply_t<ACT>(v[j]);
     uint16_t* ap = static_cast<uint16_t*>(p.d2) + b * p.d_bs + static_cast<int64_t>(m) * p.ldd + n0;
     if (full) {
       if (p.out_f16) store_f16x32(ap, v);
@@ -211,9 +216,9 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& p, int b, int m, 
       float z[32];
       load_bf16x32(zp, z);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] *= act_grad(p.act, z[j]);
+      for (int j = 0; j < 32; ++j) v[j] *= act_grad_t<ACT>(z[j]);
     } else {
-      _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) v[j] *= act_grad(p.act, bf16_bits_to_float(zp[j]));
+      _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) v[j] *= act_grad_t<ACT>(bf16_bits_to_float(zp[j]));
     }
   }
   uint16_t* dst = static_cast<uint16_t*>(p.d) + b * p.d_bs + static_cast<int64_t>(m) * p.ldd + n0;
@@ -221,7 +226,88 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& p, int b, int m, 
   else _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) dst[j] = float_to_bf16_bits(v[j]);
 }
 
-template <bool A_MN, bool B_MN>
+// Epilogue math for 32 columns n0..n0+31 of row m, without storing: v receives
+// D's values, v2 the activation output (EPI_ACT only).  Loads past M or N are
+// skipped (their outputs are clipped by the TMA store).
+template <int EPI, int ACT>
+__device__ __forceinline__ void epilogue_values(const GemmArgs& p, int b, int m, int n0, const uint32_t (&r)[32],
+                                                float (&v)[32], float (&v2)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+  if constexpr (EPI == EPI_F32) return;
+  const bool row_ok = m < p.M;
+  const bool full = (n0 + 32 <= p.N);
+  const int ncols = full ? 32 : (p.N - n0);
+  if constexpr (EPI == EPI_BF16 || EPI == EPI_ACT) {
+    if (p.bias) {
+      const uint16_t* bp = p.bias + (EPI == EPI_ACT ? b * p.bias_bs : 0) + n0;
+      if (full) {
+        float bb[32];
+        load_bf16x32(bp, bb);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += bb[j];
+      } else {
+        _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) v[j] += bf16_bits_to_float(bp[j]);
+      }
+    }
+    if (EPI == EPI_BF16 && p.res && row_ok) {
+      const uint16_t* rp = p.res + static_cast<int64_t>(m) * p.ld_res + n0;
+      if (full) {
+        float rr[32];
+        load_bf16x32(rp, rr);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += rr[j];
+      } else {
+        _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) v[j] += bf16_bits_to_float(rp[j]);
+      }
+    }
+    if constexpr (EPI == EPI_ACT) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v2[j] = act_apply_t<ACT>(v[j]);
+    }
+    return;
+  }
+  // EPI_DACT
+  if (!row_ok) return;
+  const uint16_t* zp = p.aux + b * p.aux_bs + static_cast<int64_t>(m) * p.ld_aux + n0;
+  if (full) {
+    float z[32];
+    load_bf16x32(zp, z);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= act_grad_t<ACT>(z[j]);
+  } else {
+    _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) v[j] *= act_grad_t<ACT>(bf16_bits_to_float(zp[j]));
+  }
+}
+
+// One thread's 32 values into 64 bytes (half of a 128-byte staging row), 2-byte format.
+__device__ __forceinline__ void stage_half_row16(uint8_t* buf, int row, int half, const float (&v)[32], bool f16) {
+  uint8_t* rowp = buf + row * 128;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint4 w;
+    if (f16) {
+      w = make_uint4(pack_f16x2(v[8 * k + 0], v[8 * k + 1]), pack_f16x2(v[8 * k + 2], v[8 * k + 3]),
+                     pack_f16x2(v[8 * k + 4], v[8 * k + 5]), pack_f16x2(v[8 * k + 6], v[8 * k + 7]));
+    } else {
+      w = make_uint4(pack_bf16x2(v[8 * k + 0], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
+                     pack_bf16x2(v[8 * k + 4], v[8 * k + 5]), pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+    }
+    const int c = half * 4 + k;
+    *reinterpret_cast<uint4*>(rowp + ((c ^ (row & 7)) << 4)) = w;
+  }
+}
+
+// One thread's 32 fp32 values: a full 128-byte staging row.
+__device__ __forceinline__ void stage_row32(uint8_t* buf, int row, const float (&v)[32]) {
+  uint8_t* rowp = buf + row * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<float4*>(rowp + ((c ^ (row & 7)) << 4)) =
+        make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+}
+
+template <bool A_MN, bool B_MN, int EPI, int ACT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmArgs p) {
@@ -387,7 +473,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t r[32];
         ptx::tmem_ld32(t_row + c * 32, r);
         ptx::tmem_ld_wait();
-        if (m < p.M) epilogue_chunk(p, b, m, n0, r);
+        if (m < p.M) epilogue_chunk<EPI, ACT>(p, b, m, n0, r);
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(&tempty[acc]);
@@ -402,6 +488,278 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+
+// ------------------------------------------------------------ CTA-pair GEMM
+// Same contract as gemm_kernel, computed by clusters of two CTAs on two SMs
+// sharing one 256 x 256 output tile through tcgen05.mma.cta_group::2 (M = 256):
+// CTA rank r of the pair loads rows [128 r, 128 r + 128) of the tile's A and
+// rows [128 r, 128 r + 128) of its B (N) into its own shared memory, so each
+// SM streams 32 KB per 64-deep k-block instead of 48 KB for the same work, and
+// six stages fit.  The leader (rank 0) issues every MMA; its "full" barrier
+// counts both CTAs' TMA bytes; MMA completion is multicast to both CTAs'
+// "empty" and "accumulator full" barriers; both epilogues arrive on the
+// leader's "accumulator empty" barrier.  Each CTA's TMEM holds its own 128
+// rows of the 256-column accumulator (two buffers, 512 columns).
+constexpr int P_BN = 256;                       // tile N (pair)
+constexpr int P_HALF = 128;                     // rows of A and of B per CTA
+constexpr int P_STAGES = 5;
+constexpr int P_A_BYTES = P_HALF * BK * 2;      // 16 KB
+constexpr int P_B_BYTES = P_HALF * BK * 2;      // 16 KB
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+constexpr int STG_BOX_BYTES = 32 * 128;                     // one 32-row x 128-byte output box
+constexpr int STG_WARP_BYTES = 2 * 2 * STG_BOX_BYTES;         // 2 outputs x double buffer
+constexpr int STG_BYTES = 4 * STG_WARP_BYTES;                 // 4 epilogue warps
+constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + STG_BYTES + BAR_BYTES;
+
+template <bool A_MN, bool B_MN, int EPI, int ACT>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
+                     const GemmArgs p) {
+  extern __shared__ uint8_t dsmem[];
+  const uint32_t pad = (1024u - (ptx::smem_addr(dsmem) & 1023u)) & 1023u;
+  uint8_t* base = dsmem + pad;
+  uint8_t* sA = base;
+  uint8_t* sB = base + P_STAGES * P_A_BYTES;
+  uint8_t* sStage = base + P_STAGES * P_STAGE_BYTES;  // epilogue output staging (1024-byte aligned boxes)
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + STG_BYTES);
+  uint64_t* empty = full + P_STAGES;
+  uint64_t* tfull = empty + P_STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool leader = (rank == 0);
+  const int cluster = static_cast<int>(blockIdx.x >> 1);
+  const int nclusters = static_cast<int>(gridDim.x >> 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 256);  // both CTAs' epilogue threads (used in the leader)
+    }
+    ptx::mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int mt2 = (p.M + 2 * P_HALF - 1) / (2 * P_HALF);
+  const int nt2 = (p.N + P_BN - 1) / P_BN;
+  const int total = p.nbatch * mt2 * nt2;
+  const int ksteps = p.nsum * p.kt;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ TMA producer (both CTAs)
+      ptx::tma_prefetch_desc(&tmA);
+      ptx::tma_prefetch_desc(&tmB);
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int tile = cluster; ok && tile < total; tile += nclusters) {
+        const int mb = tile % mt2;
+        const int rest = tile / mt2;
+        const int nb = rest % nt2;
+        const int b = rest / nt2;
+        const int m0 = mb * 2 * P_HALF + static_cast<int>(rank) * P_HALF;
+        const int n0 = nb * P_BN + static_cast<int>(rank) * P_HALF;
+        for (int ks = 0; ks < ksteps; ++ks) {
+          const int s = ks / p.kt;
+          const int kb = ks - s * p.kt;
+          if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err, ERR_WAIT_PRODUCER, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = ptx::mapa_shared(ptx::smem_addr(&full[stage]), 0);
+          if (leader) ptx::mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE_BYTES);
+          const int ash = p.a_sharded ? (p.nsum > 1 ? s : b) : 0;
+          const int bsh = p.b_sharded ? (p.nsum > 1 ? s : b) : 0;
+          uint8_t* a_dst = sA + stage * P_A_BYTES;
+          uint8_t* b_dst = sB + stage * P_B_BYTES;
+          if (!A_MN) {
+            ptx::tma_load_3d_pair(a_dst, &tmA, bar, kb * BK, m0, ash);
+          } else {
+#pragma unroll
+            for (int j = 0; j < P_HALF / 64; ++j)
+              ptx::tma_load_3d_pair(a_dst + j * MN_CHUNK_BYTES, &tmA, bar, m0 + j * 64, kb * BK, ash);
+          }
+          if (!B_MN) {
+            ptx::tma_load_3d_pair(b_dst, &tmB, bar, kb * BK, n0, bsh);
+          } else {
+#pragma unroll
+            for (int j = 0; j < P_HALF / 64; ++j)
+              ptx::tma_load_3d_pair(b_dst + j * MN_CHUNK_BYTES, &tmB, bar, n0 + j * 64, kb * BK, bsh);
+          }
+          ++issued;
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (leader) {  // both CTAs' copies land on the leader's barriers
+        volatile int never = 0;
+        for (int s = 0; s < P_STAGES && s < issued; ++s) {
+          const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+          ptx::mbar_wait_cluster(&full[s], par, &never, p.err, ERR_WAIT_DRAIN, p.timeout_ns);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------------- MMA issuer (leader only)
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(2 * P_HALF, P_BN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = cluster; ok && tile < total; tile += nclusters) {
+        if (!ptx::mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err, ERR_WAIT_MMA, p.timeout_ns))
+          break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * P_BN);
+        for (int ks = 0; ks < ksteps; ++ks) {
+          if (!ptx::mbar_wait_cluster(&full[stage], phase, abort_flag, p.err, ERR_WAIT_MMA, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a_addr = ptx::smem_addr(sA + stage * P_A_BYTES);
+          const uint32_t b_addr = ptx::smem_addr(sB + stage * P_B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = A_MN ? ptx::sdesc_sw128(a_addr + kk * 2048, MN_CHUNK_BYTES, 1024)
+                                     : ptx::sdesc_sw128(a_addr + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? ptx::sdesc_sw128(b_addr + kk * 2048, MN_CHUNK_BYTES, 1024)
+                                     : ptx::sdesc_sw128(b_addr + kk * 32, 16, 1024);
+            ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit_pair_mc(&empty[stage], 0x3);  // frees this stage in both CTAs
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit_pair_mc(&tfull[acc], 0x3);  // accumulator ready in both CTAs
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      ptx::mma_commit_pair_mc(mma_done, 0x1);
+      volatile int never = 0;
+      ptx::mbar_wait(mma_done, 0, &never, p.err, ERR_WAIT_DRAIN, p.timeout_ns);
+    }
+  } else {
+    // ----------------------------------------------------------- epilogue (both CTAs)
+    const int quad = warp & 3;
+    const uint32_t tempty_leader0 = ptx::mapa_shared(ptx::smem_addr(&tempty[0]), 0);
+    uint8_t* stg = sStage + quad * STG_WARP_BYTES;  // [buffer][output] boxes of this warp
+    const bool two_out = (EPI == EPI_ACT) && p.d != nullptr;
+    const bool wide = (EPI == EPI_F32);           // fp32 boxes hold 32 columns, 2-byte boxes 64
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    uint32_t step = 0;
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&tmD);
+      ptx::tma_prefetch_desc(&tmD2);
+    }
+    for (int tile = cluster; tile < total; tile += nclusters) {
+      const int mb = tile % mt2;
+      const int rest = tile / mt2;
+      const int nb = rest % nt2;
+      const int b = rest / nt2;
+      if (!ptx::mbar_wait_cluster(&tfull[acc], acc_phase, abort_flag, p.err, ERR_WAIT_EPI, p.timeout_ns)) break;
+      ptx::tc_fence_after();
+      const int mrow0 = mb * 2 * P_HALF + static_cast<int>(rank) * P_HALF + quad * 32;
+      const int m = mrow0 + lane;
+      const uint32_t t_row =
+          tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * P_BN);
+      if (!p.tma_store) {
+#pragma unroll 1
+        for (int c = 0; c < P_BN / 32; ++c) {
+          const int n0 = nb * P_BN + c * 32;
+          if (n0 >= p.N) break;  // warp-uniform
+          uint32_t r[32];
+          ptx::tmem_ld32(t_row + c * 32, r);
+          ptx::tmem_ld_wait();
+          if (m < p.M) epilogue_chunk<EPI, ACT>(p, b, m, n0, r);
+        }
+      } else if (mrow0 < p.M) {  // warps whose 32 rows are all past M store nothing
+        const int box_cols = wide ? 32 : 64;
+#pragma unroll 1
+        for (int g0 = 0; g0 < P_BN; g0 += box_cols) {
+          const int n0 = nb * P_BN + g0;
+          if (n0 >= p.N) break;  // warp-uniform
+          uint8_t* bufD = stg + (step & 1) * (2 * STG_BOX_BYTES);
+          uint8_t* bufD2 = bufD + STG_BOX_BYTES;
+          // this buffer pair was last handed to TMA two steps ago: it must have been read
+          if (lane == 0) ptx::bulk_wait_group_read<1>();
+          __syncwarp();
+#pragma unroll 1
+          for (int h = 0; h < box_cols / 32; ++h) {
+            uint32_t r[32];
+            ptx::tmem_ld32(t_row + g0 + h * 32, r);
+            ptx::tmem_ld_wait();
+            float v[32], v2[32];
+            epilogue_values<EPI, ACT>(p, b, m, n0 + h * 32, r, v, v2);
+            if (wide) {
+              stage_row32(bufD, lane, v);
+            } else if (EPI == EPI_ACT) {
+              if (two_out) stage_half_row16(bufD, lane, h, v, p.out_f16 != 0);
+              stage_half_row16(bufD2, lane, h, v2, p.out_f16 != 0);
+            } else {
+              stage_half_row16(bufD, lane, h, v, false);
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (EPI == EPI_ACT) {
+              if (two_out) ptx::tma_store_3d(&tmD, bufD, n0, mrow0, b);
+              ptx::tma_store_3d(&tmD2, bufD2, n0, mrow0, b);
+            } else {
+              ptx::tma_store_3d(&tmD, bufD, n0, mrow0, b);
+            }
+            ptx::bulk_commit_group();
+          }
+          ++step;
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive_cluster(tempty_leader0 + static_cast<uint32_t>(acc * sizeof(uint64_t)));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (lane == 0) ptx::bulk_wait_group<0>();  // every output written before the CTA exits
+  }
+
+  __syncwarp();
+  ptx::tc_fence_before();
+  ptx::cluster_sync();  // the peer's shared memory and TMEM stay alive until the pair is done
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
@@ -472,20 +830,120 @@ bool make_map_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t 
 
 namespace {
 
-template <bool A_MN, bool B_MN>
+template <bool A_MN, bool B_MN, int EPI, int ACT>
 tp_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid, cudaStream_t s) {
   static bool configured[64] = {};
   int dev = 0;
   TP_CUDA_CHECK(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return TP_ERR_CUDA;
   if (!configured[dev]) {
-    TP_CUDA_CHECK(cudaFuncSetAttribute(gemm_kernel<A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    TP_CUDA_CHECK(cudaFuncSetAttribute(gemm_kernel<A_MN, B_MN, EPI, ACT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SMEM_BYTES));
     configured[dev] = true;
   }
-  gemm_kernel<A_MN, B_MN><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, a);
+  gemm_kernel<A_MN, B_MN, EPI, ACT><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, a);
   TP_LAUNCHED();
   return TP_OK;
+}
+
+// Clusters of the pair kernel that can be resident at once on this device.
+template <bool A_MN, bool B_MN, int EPI, int ACT>
+int pair_clusters(int dev) {
+  static int cached[64] = {};
+  if (cached[dev] > 0) return cached[dev];
+  if (cudaFuncSetAttribute(gemm_pair_kernel<A_MN, B_MN, EPI, ACT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           P_SMEM_BYTES) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * 256, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = P_SMEM_BYTES;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<A_MN, B_MN, EPI, ACT>, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = device_sm_count() / 2;
+  }
+  cached[dev] = n;
+  return n;
+}
+
+template <bool A_MN, bool B_MN, int EPI, int ACT>
+tp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const CUtensorMap& td2,
+                      const GemmArgs& a, int64_t tiles, cudaStream_t s) {
+  int dev = 0;
+  TP_CUDA_CHECK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return TP_ERR_CUDA;
+  const int nc = pair_clusters<A_MN, B_MN, EPI, ACT>(dev);
+  if (nc <= 0) return TP_ERR_CUDA;
+  const int clusters = static_cast<int>(tiles < nc ? tiles : nc);
+  gemm_pair_kernel<A_MN, B_MN, EPI, ACT><<<2 * clusters, NUM_THREADS, P_SMEM_BYTES, s>>>(ta, tb, td, td2, a);
+  TP_LAUNCHED();
+  return TP_OK;
+}
+
+// The CTA-pair kernel is used when a 256-row output tile is not mostly
+// padding; TP_GEMM_PAIR=0 forces the single-CTA kernel (tests cover both).
+bool use_pair(int64_t M) {
+  const char* e = std::getenv("TP_GEMM_PAIR");
+  if (e && e[0] == '0') return false;
+  return M > 128;
+}
+
+// Output map for the TMA-store epilogue: (N, M, batch), 32-row boxes of 128 bytes, 128B swizzle.
+bool make_output_map(CUtensorMap* map, void* d, CUtensorMapDataType dt, int esz, int64_t N, int64_t M, int nbatch,
+                     int64_t ldd, int64_t dbs) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(nbatch)};
+  const int64_t bs = (nbatch > 1) ? dbs : ldd * M;
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldd * esz), static_cast<cuuint64_t>(bs * esz)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, dt, 3, d, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The (operand majors, epilogue, activation) combinations the library uses;
+// each is its own kernel instantiation.
+template <class F>
+tp_status dispatch(bool amn, bool bmn, int epi, int act, F&& f) {
+  using T = std::true_type;
+  using Fl = std::false_type;
+  using I0 = std::integral_constant<int, 0>;
+  using I1 = std::integral_constant<int, 1>;
+  using I2 = std::integral_constant<int, 2>;
+  using I3 = std::integral_constant<int, 3>;
+  using E_BF16 = std::integral_constant<int, EPI_BF16>;
+  using E_ACT = std::integral_constant<int, EPI_ACT>;
+  using E_DACT = std::integral_constant<int, EPI_DACT>;
+  using E_F32 = std::integral_constant<int, EPI_F32>;
+  if (!amn && !bmn) {  // forward GEMMs
+    if (epi == EPI_ACT) {
+      switch (act) {
+        case 0: return f(Fl{}, Fl{}, E_ACT{}, I0{});
+        case 1: return f(Fl{}, Fl{}, E_ACT{}, I1{});
+        case 2: return f(Fl{}, Fl{}, E_ACT{}, I2{});
+        case 3: return f(Fl{}, Fl{}, E_ACT{}, I3{});
+      }
+    }
+    if (epi == EPI_BF16) return f(Fl{}, Fl{}, E_BF16{}, I0{});
+    if (epi == EPI_F32) return f(Fl{}, Fl{}, E_F32{}, I0{});
+  } else if (!amn && bmn) {  // dgrad and f-reduced dX
+    if (epi == EPI_DACT) {
+      switch (act) {
+        case 0: return f(Fl{}, T{}, E_DACT{}, I0{});
+        case 1: return f(Fl{}, T{}, E_DACT{}, I1{});
+        case 2: return f(Fl{}, T{}, E_DACT{}, I2{});
+        case 3: return f(Fl{}, T{}, E_DACT{}, I3{});
+      }
+    }
+    if (epi == EPI_ACT && act == 0) return f(Fl{}, T{}, E_ACT{}, I0{});
+    if (epi == EPI_BF16) return f(Fl{}, T{}, E_BF16{}, I0{});
+    if (epi == EPI_F32) return f(Fl{}, T{}, E_F32{}, I0{});
+  } else if (amn && bmn) {  // weight gradients
+    if (epi == EPI_F32) return f(T{}, T{}, E_F32{}, I0{});
+  }
+  return TP_ERR_UNSUPPORTED;
 }
 
 bool operand_ok(const GemmOperand& o) {
@@ -516,9 +974,10 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
   const int nsh_b = P.b.sharded ? (P.nsum > 1 ? P.nsum : P.nbatch) : 1;
 
   TP_RETURN_IF(ready());
+  const bool pair = use_pair(P.M);
   CUtensorMap ta, tb;
   if (!make_operand_map(&ta, P.a, P.M, P.K, nsh_a, BM)) return TP_ERR_CUDA;
-  if (!make_operand_map(&tb, P.b, P.N, P.K, nsh_b, BN)) return TP_ERR_CUDA;
+  if (!make_operand_map(&tb, P.b, P.N, P.K, nsh_b, pair ? P_HALF : BN)) return TP_ERR_CUDA;
 
   GemmArgs a{};
   a.M = static_cast<int>(P.M);
@@ -549,13 +1008,37 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
   a.timeout_ns = wait_timeout_ns();
   if (!a.err) return TP_ERR_CUDA;
 
+  const bool amn = P.a.mn_major, bmn = P.b.mn_major;
+  if (pair) {
+    // Outputs go through shared memory and TMA stores, except accumulation into fp32
+    // (a read-modify-write), which keeps the per-thread store path.
+    CUtensorMap td, td2;
+    std::memset(&td, 0, sizeof(td));
+    std::memset(&td2, 0, sizeof(td2));
+    a.tma_store = !(P.epi == EPI_F32 && P.accumulate);
+    if (a.tma_store) {
+      const int esz = (P.epi == EPI_F32) ? 4 : 2;
+      const CUtensorMapDataType dt = (P.epi == EPI_F32) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                     : (P.epi == EPI_ACT && P.out_f16) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+      void* d_main = (P.epi == EPI_ACT) ? (P.d ? P.d : P.d2) : P.d;
+      if (!make_output_map(&td, d_main, dt, esz, P.N, P.M, P.nbatch, P.ldd, P.d_batch_stride)) return TP_ERR_CUDA;
+      if (P.epi == EPI_ACT &&
+          !make_output_map(&td2, P.d2, dt, esz, P.N, P.M, P.nbatch, P.ldd, P.d_batch_stride))
+        return TP_ERR_CUDA;
+    }
+    const int64_t ptiles = ((P.M + 255) / 256) * ((P.N + P_BN - 1) / P_BN) * P.nbatch;
+    return dispatch(amn, bmn, P.epi, P.act, [&](auto am, auto bm, auto ep, auto ac) {
+      return launch_pair<decltype(am)::value, decltype(bm)::value, decltype(ep)::value, decltype(ac)::value>(
+          ta, tb, td, td2, a, ptiles, s);
+    });
+  }
   const int64_t tiles = mt * nt * P.nbatch;
   const int grid = static_cast<int>(tiles < device_sm_count() ? tiles : device_sm_count());
-  const bool amn = P.a.mn_major, bmn = P.b.mn_major;
-  if (!amn && !bmn) return launch<false, false>(ta, tb, a, grid, s);
-  if (!amn && bmn) return launch<false, true>(ta, tb, a, grid, s);
-  if (amn && !bmn) return launch<true, false>(ta, tb, a, grid, s);
-  return launch<true, true>(ta, tb, a, grid, s);
+  return dispatch(amn, bmn, P.epi, P.act, [&](auto am, auto bm, auto ep, auto ac) {
+    return launch<decltype(am)::value, decltype(bm)::value, decltype(ep)::value, decltype(ac)::value>(ta, tb, a, grid,
+                                                                                                      s);
+  });
 }
 
 }  // namespace tp

@@ -167,6 +167,16 @@ def test_bias_added_once_on_gpu():
         assert torch.equal(Y, bd.expand(M, h)), flags
 
 
+@pytest.mark.parametrize("pair", ["0", "1"])
+@pytest.mark.parametrize("M,h,F,t", [(384, 264, 784, 2), (1000, 512, 2048, 4)])
+def test_single_cta_and_pair_gemm_paths(M, h, F, t, pair, monkeypatch):
+    """Both GEMM kernels (one CTA per 128x256 tile, and CTA pairs per 256x256
+    tile through tcgen05 cta_group::2) give the oracle's results, forward and
+    backward (all four operand-major combinations)."""
+    monkeypatch.setenv("TP_GEMM_PAIR", pair)
+    _backward_check(M, h, F, t, "gelu_tanh", seed=8)
+
+
 def test_mlp_zero_tokens():
     dev, ref, w = _case(8, 64, 256, 2)
     Y = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
