@@ -316,7 +316,7 @@ def run_ours(args):
                    "l2": "working set ~1.1 GB > 129 MB L2; no flush",
                    "frac_of_peak": round(value / world / peak, 4), "peak_tflops": peak,
                    "peak_kind": f"{peak_kind} ({peaks['source']})"},
-        "roofline": {"bound": "tensor", "kernel": "gemm_kernel (column-parallel GEMM + GeLU epilogue)",
+        "roofline": {"bound": "tensor", "kernel": "gemm_pair_kernel<K-major, K-major, EPI_ACT, GeLU-tanh> (column-parallel GEMM + GeLU epilogue)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": UNIT,
                      "frac": round(achieved / peak, 4), "traffic": recorded_traffic("gemm_colpar_fwd_c2.md"),
                      "kernel_ms": round(col_ms, 4), "flops_per_launch": col_flops},
