@@ -99,6 +99,12 @@ tp_status tp_get_device_status(tp_stream stream);
  * reports TP_ERR_TIMEOUT. */
 tp_status tp_selftest_bounded_wait(int64_t timeout_us, tp_stream stream);
 
+/* Where the most recent TP_ERR_CUDA returned on this thread came from:
+ * "file:line: cudaErrorName (description)" or a tensor-map failure; "" if
+ * none.  The string belongs to the library and stays valid until this
+ * thread's next failing call. */
+const char* tp_last_error_detail(void);
+
 /* Number of CUDA kernels this library has enqueued in this process so far
  * (all devices, all streams).  Host-side counter; never synchronises. */
 uint64_t tp_kernel_launch_count(void);

@@ -46,6 +46,7 @@ SIGNATURES = {
     "tp_mlp_backward": (_I, [_P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P, _P, _P, _P, _I, _U, _P,
                              _SZ, _P]),
     "tp_kernel_launch_count": (C.c_uint64, []),
+    "tp_last_error_detail": (C.c_char_p, []),
     "tp_column_parallel_forward": (_I, [_P, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P, _P]),
     "tp_row_parallel_forward": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _P, _P]),
     "tp_decode_swiglu_forward": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _P, _P]),
@@ -130,7 +131,10 @@ def _make(name):
             conv.append(_stream(stream))
         r = fn(*conv)
         if returns_status and check and r != TP_OK:
-            raise TPError(name, r, status_string(r))
+            msg = status_string(r)
+            if r == TP_ERR_CUDA:
+                msg += " [" + lib().tp_last_error_detail().decode() + "]"
+            raise TPError(name, r, msg)
         return r
 
     call.__name__ = name

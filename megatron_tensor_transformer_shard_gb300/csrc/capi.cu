@@ -4,7 +4,9 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "internal.h"
@@ -85,10 +87,38 @@ namespace {
 std::atomic<uint64_t> g_launches{0};
 }
 
+namespace {
+thread_local char g_detail[256] = "";
+}
+
+void set_error_detail(const char* file, int line, const char* what) {
+  const char* f = std::strrchr(file, '/');
+  std::snprintf(g_detail, sizeof(g_detail), "%s:%d: %s", f ? f + 1 : file, line, what);
+}
+
+tp_status cuda_failure(const char* file, int line, cudaError_t e) {
+  char buf[160];
+  std::snprintf(buf, sizeof(buf), "%s (%s)", cudaGetErrorName(e), cudaGetErrorString(e));
+  set_error_detail(file, line, buf);
+  return TP_ERR_CUDA;
+}
+
+const char* error_detail() { return g_detail; }
+
 void count_launch(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 uint64_t launches_so_far() { return g_launches.load(std::memory_order_relaxed); }
 
 tp_status ready() {
+  // Driver-API calls (tensor-map encoding) need the device's primary context
+  // current on this thread; threads that reach the library first (e.g. an
+  // autograd worker) may not have it yet.
+  thread_local int ctx_dev = -1;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TP_FAIL_DETAIL("cudaGetDevice failed");
+  if (dev != ctx_dev) {
+    TP_CUDA_CHECK(cudaSetDevice(dev));
+    ctx_dev = dev;
+  }
   if (!device_error_word()) return TP_ERR_CUDA;
   if (!device_is_sm103()) return TP_ERR_UNSUPPORTED;
   return TP_OK;
@@ -137,7 +167,7 @@ AttnBwdWs attn_bwd_layout(void* ws, int64_t N, int64_t d, int n_heads, int t) {
   w.dQKV = reinterpret_cast<uint16_t*>(b + off);
   off += round_up(static_cast<size_t>(N) * 3 * d * 2, 256);
   w.cs = reinterpret_cast<float*>(b + off);
-  w.cs_floats = std::max(colsum_ws_floats(N, 3 * d / t) * t, colsum_ws_floats(N, d));
+  w.cs_floats = colsum2_ws_floats(N, d, 1) + colsum2_ws_floats(N, 3 * d / t, t);
   off += round_up(w.cs_floats * 4, 256);
   w.total = off;
   return w;
@@ -179,8 +209,6 @@ tp_status tp_attn_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Q
     }
     return TP_OK;
   }
-  // g backward is the identity; the output-bias gradient is taken once.
-  if (dbo) TP_RETURN_IF(run_colsum(dY, N, d, d, dbo, accumulate, w.cs, w.cs_floats, s));
   // dO_i = dY W_o,i^T  (row-parallel W_o, input grad stays sharded).
   GemmProblem g;
   g.M = N; g.N = dt; g.K = d; g.nbatch = t;
@@ -199,9 +227,19 @@ tp_status tp_attn_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Q
   // Head-local softmax-attention backward -> dQKV_i.
   TP_RETURN_IF(run_attention_bwd(QKV_save, O_save, w.dO, lse_save, N, d, n_heads, head_dim, t, causal, scale, w.Dvec,
                                  w.dQKV, s));
-  if (dbqkv_p)
-    TP_RETURN_IF(run_colsum_batched(w.dQKV, N, 3 * dt, 3 * dt, t, N * 3 * dt, dbqkv_p, accumulate, w.cs, w.cs_floats,
-                                    s));
+  // Bias gradients in one fused pass: db_o once (g backward is the identity), db_qkv per shard.
+  if (dbo || dbqkv_p) {
+    ColsumJob jo, jq;
+    if (dbo) {
+      jo.G = dY; jo.rows = N; jo.cols = d; jo.ld = d; jo.bs = N * d; jo.nbatch = 1;
+      jo.out = dbo; jo.ws = w.cs; jo.accumulate = accumulate;
+    }
+    if (dbqkv_p) {
+      jq.G = w.dQKV; jq.rows = N; jq.cols = 3 * dt; jq.ld = 3 * dt; jq.bs = N * 3 * dt; jq.nbatch = t;
+      jq.out = dbqkv_p; jq.ws = w.cs + colsum2_ws_floats(N, d, 1); jq.accumulate = accumulate;
+    }
+    TP_RETURN_IF(run_colsum2(jo, jq, s));
+  }
   // dW_qkv,i = dQKV_i^T X -> packed [t][3dt][d] (local).
   GemmProblem wq;
   wq.M = 3 * dt; wq.N = d; wq.K = N; wq.nbatch = t;
@@ -221,6 +259,8 @@ tp_status tp_attn_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Q
 int tp_abi_version(void) { return TP_ABI_VERSION; }
 
 uint64_t tp_kernel_launch_count(void) { return launches_so_far(); }
+
+const char* tp_last_error_detail(void) { return error_detail(); }
 
 const char* tp_status_string(tp_status s) {
   switch (s) {
@@ -359,7 +399,7 @@ size_t tp_mlp_backward_workspace_size(int64_t M, int64_t h, int64_t F, int t, un
   if (M < 0 || h < 0 || F < 0 || t < 1) return 0;
   const int64_t Ft = F / t;
   size_t sz = round_up(static_cast<size_t>(M) * F * 2, 256);  // dZ
-  const size_t cs = std::max(colsum_ws_floats(M, Ft) * t, colsum_ws_floats(M, h));
+  const size_t cs = colsum2_ws_floats(M, h, 1) + colsum2_ws_floats(M, Ft, t);
   sz += round_up(cs * sizeof(float), 256);
   if (flags & TP_FLAG_UNFUSED_REDUCE) sz += static_cast<size_t>(t) * M * h * sizeof(float);
   return sz;
@@ -386,7 +426,7 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
   uint16_t* dZ = reinterpret_cast<uint16_t*>(w);
   w += round_up(static_cast<size_t>(M) * F * 2, 256);
   float* cs_ws = reinterpret_cast<float*>(w);
-  const size_t cs_floats = std::max(colsum_ws_floats(M, Ft) * t, colsum_ws_floats(M, h));
+  const size_t cs_floats = colsum2_ws_floats(M, h, 1) + colsum2_ws_floats(M, Ft, t);
   w += round_up(cs_floats * sizeof(float), 256);
   float* P = reinterpret_cast<float*>(w);
 
@@ -401,9 +441,6 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
     return TP_OK;
   }
 
-  // g backward is the identity: the bias gradient of the row-parallel layer is taken once.
-  if (dbdown) TP_RETURN_IF(run_colsum(dY, M, h, h, dbdown, accumulate, cs_ws, cs_floats, s));
-
   // dgrad + act': dZ_i = (dY W_down,i^T) * act'(Z_i).
   GemmProblem g;
   g.M = M; g.N = Ft; g.K = h; g.nbatch = t;
@@ -413,7 +450,20 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
   g.d = dZ; g.ldd = Ft; g.d_batch_stride = M * Ft;
   TP_RETURN_IF(run_gemm(g, s));
 
-  if (dbup) TP_RETURN_IF(run_colsum_batched(dZ, M, Ft, Ft, t, M * Ft, dbup, accumulate, cs_ws, cs_floats, s));
+  // Bias gradients, one fused pass: db_down = sum_rows dY, taken once (g backward is the
+  // identity); db_up[C_i] = sum_rows dZ_i for every shard.
+  if (dbdown || dbup) {
+    ColsumJob jd, ju;
+    if (dbdown) {
+      jd.G = dY; jd.rows = M; jd.cols = h; jd.ld = h; jd.bs = M * h; jd.nbatch = 1;
+      jd.out = dbdown; jd.ws = cs_ws; jd.accumulate = accumulate;
+    }
+    if (dbup) {
+      ju.G = dZ; ju.rows = M; ju.cols = Ft; ju.ld = Ft; ju.bs = M * Ft; ju.nbatch = t;
+      ju.out = dbup; ju.ws = cs_ws + colsum2_ws_floats(M, h, 1); ju.accumulate = accumulate;
+    }
+    TP_RETURN_IF(run_colsum2(jd, ju, s));
+  }
 
   // Local weight gradients (no reduction): dW_down,i = A_i^T dY  -> packed [t][h][Ft].
   GemmProblem wd;

@@ -27,6 +27,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <type_traits>
@@ -810,6 +811,14 @@ bool make_operand_map(CUtensorMap* map, const GemmOperand& op, int64_t rows, int
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(op.ptr), dims, strides, box,
                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[200];
+    std::snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled=%d ptr=%p dims=%llu,%llu,%llu strides=%llu,%llu box=%u,%u",
+                  static_cast<int>(r), static_cast<const void*>(op.ptr), (unsigned long long)dims[0],
+                  (unsigned long long)dims[1], (unsigned long long)dims[2], (unsigned long long)strides[0],
+                  (unsigned long long)strides[1], box[0], box[1]);
+    set_error_detail(__FILE__, __LINE__, buf);
+  }
   return r == CUDA_SUCCESS;
 }
 
@@ -874,7 +883,7 @@ tp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
   TP_CUDA_CHECK(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return TP_ERR_CUDA;
   const int nc = pair_clusters<A_MN, B_MN, EPI, ACT>(dev);
-  if (nc <= 0) return TP_ERR_CUDA;
+  if (nc <= 0) return TP_FAIL_DETAIL("no co-resident CTA pairs");
   const int clusters = static_cast<int>(tiles < nc ? tiles : nc);
   gemm_pair_kernel<A_MN, B_MN, EPI, ACT><<<2 * clusters, NUM_THREADS, P_SMEM_BYTES, s>>>(ta, tb, td, td2, a);
   TP_LAUNCHED();
@@ -1022,10 +1031,11 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
                                      : (P.epi == EPI_ACT && P.out_f16) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
       void* d_main = (P.epi == EPI_ACT) ? (P.d ? P.d : P.d2) : P.d;
-      if (!make_output_map(&td, d_main, dt, esz, P.N, P.M, P.nbatch, P.ldd, P.d_batch_stride)) return TP_ERR_CUDA;
+      if (!make_output_map(&td, d_main, dt, esz, P.N, P.M, P.nbatch, P.ldd, P.d_batch_stride))
+        return TP_FAIL_DETAIL("tensor map of output D");
       if (P.epi == EPI_ACT &&
           !make_output_map(&td2, P.d2, dt, esz, P.N, P.M, P.nbatch, P.ldd, P.d_batch_stride))
-        return TP_ERR_CUDA;
+        return TP_FAIL_DETAIL("tensor map of output D2");
     }
     const int64_t ptiles = ((P.M + 255) / 256) * ((P.N + P_BN - 1) / P_BN) * P.nbatch;
     return dispatch(amn, bmn, P.epi, P.act, [&](auto am, auto bm, auto ep, auto ac) {

@@ -16,6 +16,7 @@ bool device_is_sm103();            // compute capability 10.3
 tp_status ready();                 // TP_OK if the current device can run this library's kernels
 void count_launch(int n = 1);      // every kernel launch of the library is counted
 uint64_t launches_so_far();
+const char* error_detail();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -25,18 +26,26 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
     if (_s != TP_OK) return _s;   \
   } while (0)
 
-#define TP_CUDA_CHECK(expr)                      \
-  do {                                           \
-    cudaError_t _e = (expr);                     \
-    if (_e != cudaSuccess) return TP_ERR_CUDA;   \
+// Records a human-readable cause of the next TP_ERR_CUDA (thread-local; read
+// with tp_last_error_detail()).
+void set_error_detail(const char* file, int line, const char* what);
+tp_status cuda_failure(const char* file, int line, cudaError_t e);
+
+#define TP_CUDA_CHECK(expr)                                                  \
+  do {                                                                       \
+    cudaError_t _e = (expr);                                                 \
+    if (_e != cudaSuccess) return ::tp::cuda_failure(__FILE__, __LINE__, _e); \
   } while (0)
 
 // After a <<<...>>> launch: count it and surface launch errors.
-#define TP_LAUNCHED()                                           \
-  do {                                                          \
-    count_launch();                                             \
-    if (cudaGetLastError() != cudaSuccess) return TP_ERR_CUDA;  \
+#define TP_LAUNCHED()                                                        \
+  do {                                                                       \
+    count_launch();                                                          \
+    cudaError_t _e = cudaGetLastError();                                     \
+    if (_e != cudaSuccess) return ::tp::cuda_failure(__FILE__, __LINE__, _e); \
   } while (0)
+
+#define TP_FAIL_DETAIL(what) (::tp::set_error_detail(__FILE__, __LINE__, what), TP_ERR_CUDA)
 
 // ----------------------------------------------------------------- GEMM
 // One launch computes, for every output batch b in [0, nbatch):
@@ -89,6 +98,19 @@ size_t colsum_ws_floats(int64_t rows, int64_t cols);
 tp_status run_colsum_batched(const uint16_t* G, int64_t rows, int64_t cols, int64_t ld, int nbatch,
                              int64_t batch_stride, float* out, int accumulate, float* ws, size_t ws_floats,
                              cudaStream_t s);
+// Two column-sum jobs fused into one partial and one final launch.
+struct ColsumJob {
+  const uint16_t* G = nullptr;
+  int64_t rows = 0, cols = 0, ld = 0, bs = 0;
+  int nbatch = 1;
+  float* out = nullptr;
+  float* ws = nullptr;  // colsum2_ws_floats(rows, cols, nbatch) floats
+  int accumulate = 0;
+  int nchunks = 0;      // set by run_colsum2
+  int64_t cblocks = 0;  // set by run_colsum2
+};
+size_t colsum2_ws_floats(int64_t rows, int64_t cols, int nbatch);
+tp_status run_colsum2(ColsumJob a, ColsumJob b, cudaStream_t s);
 tp_status run_shard_reduce(const float* P, int64_t rows, int64_t cols, int t, const uint16_t* bias,
                            const uint16_t* residual, uint16_t* out_bf16, float* out_f32, cudaStream_t s);
 

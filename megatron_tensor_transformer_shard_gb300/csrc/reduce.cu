@@ -90,7 +90,120 @@ __global__ void shard_reduce_kernel(const float* __restrict__ P, int64_t rows, i
   }
 }
 
+// ---- fused column sums of two matrices (e.g. db_down from dY and every
+// shard's db_up from dZ) in two launches: a partial pass with 16-byte loads,
+// 256-row chunks, 8 warps per CTA combined in warp order, and a final pass
+// summing the chunks in order.  Deterministic.
+constexpr int CS2_ROWS = 256;
+constexpr int CS2_THREADS = 256;  // 8 warps x 32 lanes x 8 columns: 256 columns per CTA
+
+__device__ __forceinline__ const ColsumJob& pick(const ColsumJob& a, const ColsumJob& b, bool first) {
+  return first ? a : b;
+}
+
+__global__ void __launch_bounds__(CS2_THREADS) colsum2_partial_kernel(ColsumJob j0, ColsumJob j1, int64_t n0) {
+  __shared__ float red[8][256];
+  const bool first = blockIdx.x < n0;
+  const ColsumJob& j = pick(j0, j1, first);
+  const int64_t local = first ? blockIdx.x : blockIdx.x - n0;
+  const int64_t cb = local % j.cblocks;
+  const int64_t rest = local / j.cblocks;
+  const int chunk = static_cast<int>(rest % j.nchunks);
+  const int b = static_cast<int>(rest / j.nchunks);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t c0 = cb * 256 + lane * 8;
+  const int64_t r0 = static_cast<int64_t>(chunk) * CS2_ROWS;
+  const int64_t r1 = r0 + CS2_ROWS < j.rows ? r0 + CS2_ROWS : j.rows;
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  const uint16_t* g = j.G + b * j.bs;
+  if (c0 + 8 <= j.cols) {
+    int64_t r = r0 + warp;
+    for (; r + 24 < r1; r += 32) {  // four rows in flight per thread
+      uint4 w[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) w[u] = *reinterpret_cast<const uint4*>(g + (r + 8 * u) * j.ld + c0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float a0, a1;
+        unpack_bf16x2(w[u].x, a0, a1); acc[0] += a0; acc[1] += a1;
+        unpack_bf16x2(w[u].y, a0, a1); acc[2] += a0; acc[3] += a1;
+        unpack_bf16x2(w[u].z, a0, a1); acc[4] += a0; acc[5] += a1;
+        unpack_bf16x2(w[u].w, a0, a1); acc[6] += a0; acc[7] += a1;
+      }
+    }
+    for (; r < r1; r += 8) {
+      const uint4 w = *reinterpret_cast<const uint4*>(g + r * j.ld + c0);
+      float a0, a1;
+      unpack_bf16x2(w.x, a0, a1); acc[0] += a0; acc[1] += a1;
+      unpack_bf16x2(w.y, a0, a1); acc[2] += a0; acc[3] += a1;
+      unpack_bf16x2(w.z, a0, a1); acc[4] += a0; acc[5] += a1;
+      unpack_bf16x2(w.w, a0, a1); acc[6] += a0; acc[7] += a1;
+    }
+  } else {
+    for (int64_t r = r0 + warp; r < r1; r += 8)
+      for (int e = 0; e < 8; ++e)
+        if (c0 + e < j.cols) acc[e] += bf16_bits_to_float(g[r * j.ld + c0 + e]);
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) red[warp][lane * 8 + e] = acc[e];
+  __syncthreads();
+  const int64_t c = cb * 256 + threadIdx.x;
+  if (c < j.cols) {
+    float s2 = 0.0f;
+#pragma unroll
+    for (int w2 = 0; w2 < 8; ++w2) s2 += red[w2][threadIdx.x];
+    j.ws[(static_cast<int64_t>(b) * j.nchunks + chunk) * j.cols + c] = s2;
+  }
+}
+
+__global__ void colsum2_final_kernel(ColsumJob j0, ColsumJob j1, int64_t n0) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const bool first = idx < n0;
+  const ColsumJob& j = pick(j0, j1, first);
+  const int64_t local = first ? idx : idx - n0;
+  if (local >= j.cols * j.nbatch) return;
+  const int64_t b = local / j.cols, c = local - b * j.cols;
+  const float* w = j.ws + b * j.nchunks * j.cols + c;
+  float s = 0.0f;
+  for (int k = 0; k < j.nchunks; ++k) s += w[static_cast<int64_t>(k) * j.cols];
+  j.out[local] = j.accumulate ? j.out[local] + s : s;
+}
+
 }  // namespace
+
+size_t colsum2_ws_floats(int64_t rows, int64_t cols, int nbatch) {
+  const int64_t nchunks = (rows + CS2_ROWS - 1) / CS2_ROWS;
+  return static_cast<size_t>(nchunks > 0 ? nchunks : 1) * static_cast<size_t>(cols) * static_cast<size_t>(nbatch);
+}
+
+// Column sums of two jobs ([nbatch][rows][cols], row stride ld, batch stride bs)
+// into job.out[nbatch][cols]; job.ws must hold colsum2_ws_floats() floats.
+tp_status run_colsum2(ColsumJob a, ColsumJob b, cudaStream_t s) {
+  ColsumJob* js[2] = {&a, &b};
+  int64_t ctas[2] = {0, 0}, outs[2] = {0, 0};
+  for (int k = 0; k < 2; ++k) {
+    ColsumJob& j = *js[k];
+    if (j.rows < 0 || j.cols < 0 || j.nbatch < 1) return TP_ERR_INVALID_ARG;
+    if (j.cols == 0) continue;
+    if (!j.G || !j.out || !j.ws || (j.cols & 7) || (j.ld & 7) || (j.bs & 7) || !aligned16(j.G))
+      return TP_ERR_ALIGN;
+    j.nchunks = static_cast<int>((j.rows + CS2_ROWS - 1) / CS2_ROWS);
+    j.cblocks = (j.cols + 255) / 256;
+    if (j.nchunks == 0) {
+      j.nchunks = 1;  // no rows: the partial pass writes zeros
+    }
+    ctas[k] = j.cblocks * j.nchunks * j.nbatch;
+    outs[k] = j.cols * j.nbatch;
+  }
+  if (ctas[0] + ctas[1] == 0) return TP_OK;
+  TP_RETURN_IF(ready());
+  colsum2_partial_kernel<<<static_cast<unsigned>(ctas[0] + ctas[1]), CS2_THREADS, 0, s>>>(a, b, ctas[0]);
+  TP_LAUNCHED();
+  const int64_t n = outs[0] + outs[1];
+  colsum2_final_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(a, b, outs[0]);
+  TP_LAUNCHED();
+  return TP_OK;
+}
 
 size_t colsum_ws_floats(int64_t rows, int64_t cols) {
   const int64_t nchunks = (rows + COLSUM_ROWS_PER_CHUNK - 1) / COLSUM_ROWS_PER_CHUNK;

@@ -233,6 +233,33 @@ def test_autograd_function():
     assert_close("dW_up", f64(w.grads["dWup_p"]), O.pack_col_weight(b["dW_up"], t))
 
 
+def test_first_call_from_a_new_thread():
+    """A thread whose first CUDA work is a library call (the autograd worker
+    thread does this) must get a current context before tensor maps are
+    encoded; the GEMM must not fail with TP_ERR_CUDA there."""
+    import threading
+    M, h, F, t = 128, 256, 1024, 2
+    dev, ref, w = _case(M, h, F, t, seed=12)
+    Y, Z, A = T.mlp_forward(dev["X"], w, "gelu_tanh")
+    torch.cuda.synchronize()
+    box = {}
+
+    def worker():
+        try:
+            box["g"] = T.mlp_backward(dev["dY"], dev["X"], Z, A, w, "gelu_tanh")
+            torch.cuda.synchronize()
+        except Exception as e:  # reported below
+            box["err"] = e
+
+    th = threading.Thread(target=worker)
+    th.start()
+    th.join()
+    assert "err" not in box, box.get("err")
+    o = O.mlp_forward_sharded(ref["X"], ref["W_up"], ref["b_up"], ref["W_down"], ref["b_down"], "gelu_tanh", t)
+    b = O.mlp_backward_sharded(ref["dY"], ref["X"], ref["W_up"], ref["W_down"], o, "gelu_tanh", t)
+    assert_close("dX", f64(box["g"]["dX"]), b["dX"])
+
+
 # ------------------------------------------------ full-size workloads (sampled)
 
 def _rows(M, n=12):
