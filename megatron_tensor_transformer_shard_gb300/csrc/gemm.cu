@@ -506,20 +506,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // rows of the 256-column accumulator (two buffers, 512 columns).
 constexpr int P_BN = 256;                       // tile N (pair)
 constexpr int P_HALF = 128;                     // rows of A and of B per CTA
-constexpr int P_STAGES = 5;
 constexpr int P_A_BYTES = P_HALF * BK * 2;      // 16 KB
 constexpr int P_B_BYTES = P_HALF * BK * 2;      // 16 KB
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
-constexpr int STG_BOX_BYTES = 32 * 128;                     // one 32-row x 128-byte output box
-constexpr int STG_WARP_BYTES = 2 * 2 * STG_BOX_BYTES;         // 2 outputs x double buffer
-constexpr int STG_BYTES = 4 * STG_WARP_BYTES;                 // 4 epilogue warps
-constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + STG_BYTES + BAR_BYTES;
+constexpr int STG_BOX_BYTES = 32 * 128;         // one 32-row x 128-byte output box
+// Epilogues with one output (everything but EPI_ACT) need half the staging,
+// which buys a sixth pipeline stage.
+template <int EPI>
+struct PairCfg {
+  static constexpr int outputs = (EPI == EPI_ACT) ? 2 : 1;
+  static constexpr int stages = (EPI == EPI_ACT) ? 5 : 6;
+  static constexpr int stg_warp_bytes = 2 * outputs * STG_BOX_BYTES;  // double buffer per output
+  static constexpr int stg_bytes = 4 * stg_warp_bytes;                 // 4 epilogue warps
+  static constexpr int smem_bytes = 1024 + stages * P_STAGE_BYTES + stg_bytes + BAR_BYTES;
+};
 
 template <bool A_MN, bool B_MN, int EPI, int ACT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
                      const GemmArgs p) {
+  constexpr int P_STAGES = PairCfg<EPI>::stages;
+  constexpr int STG_BYTES = PairCfg<EPI>::stg_bytes;
+  constexpr int STG_WARP_BYTES = PairCfg<EPI>::stg_warp_bytes;
+  constexpr int NOUT = PairCfg<EPI>::outputs;
   extern __shared__ uint8_t dsmem[];
   const uint32_t pad = (1024u - (ptx::smem_addr(dsmem) & 1023u)) & 1023u;
   uint8_t* base = dsmem + pad;
@@ -712,8 +722,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         for (int g0 = 0; g0 < P_BN; g0 += box_cols) {
           const int n0 = nb * P_BN + g0;
           if (n0 >= p.N) break;  // warp-uniform
-          uint8_t* bufD = stg + (step & 1) * (2 * STG_BOX_BYTES);
-          uint8_t* bufD2 = bufD + STG_BOX_BYTES;
+          uint8_t* bufD = stg + (step & 1) * (NOUT * STG_BOX_BYTES);
+          uint8_t* bufD2 = bufD + (NOUT - 1) * STG_BOX_BYTES;  // second output (EPI_ACT only)
           // this buffer pair was last handed to TMA two steps ago: it must have been read
           if (lane == 0) ptx::bulk_wait_group_read<1>();
           __syncwarp();
@@ -861,12 +871,12 @@ int pair_clusters(int dev) {
   static int cached[64] = {};
   if (cached[dev] > 0) return cached[dev];
   if (cudaFuncSetAttribute(gemm_pair_kernel<A_MN, B_MN, EPI, ACT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           P_SMEM_BYTES) != cudaSuccess)
+                           PairCfg<EPI>::smem_bytes) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * 256, 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = P_SMEM_BYTES;
+  cfg.dynamicSmemBytes = PairCfg<EPI>::smem_bytes;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<A_MN, B_MN, EPI, ACT>, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
@@ -885,7 +895,7 @@ tp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
   const int nc = pair_clusters<A_MN, B_MN, EPI, ACT>(dev);
   if (nc <= 0) return TP_FAIL_DETAIL("no co-resident CTA pairs");
   const int clusters = static_cast<int>(tiles < nc ? tiles : nc);
-  gemm_pair_kernel<A_MN, B_MN, EPI, ACT><<<2 * clusters, NUM_THREADS, P_SMEM_BYTES, s>>>(ta, tb, td, td2, a);
+  gemm_pair_kernel<A_MN, B_MN, EPI, ACT><<<2 * clusters, NUM_THREADS, PairCfg<EPI>::smem_bytes, s>>>(ta, tb, td, td2, a);
   TP_LAUNCHED();
   return TP_OK;
 }

@@ -9,9 +9,11 @@
 //
 //   row kernels     one CTA per row, the row held in registers (8-element
 //                   chunks, up to 4 per thread), block reductions for the
-//                   statistics; HBM-bound: read x (+ dy, dres), write y / dx.
-//   column kernel   one CTA per (64-column block, shard): four warps stride
-//                   the shard's rows, combined in warp order.
+//                   statistics (two-pass mean and variance); HBM-bound:
+//                   read x (+ dy, dres), write y / dx.
+//   column kernel   one CTA per (256-column block, shard), 16-byte loads, eight
+//                   warps striding the shard's rows, combined in warp order;
+//                   then one launch sums the shard partials in shard order.
 #include <cuda_runtime.h>
 
 #include "devmath.cuh"
@@ -159,41 +161,99 @@ __global__ void ln_bwd_rows_kernel(const uint16_t* __restrict__ dY, const uint16
   }
 }
 
-// Partial weight grads of shard j over its rows [j*rows_per, (j+1)*rows_per).
-__global__ void ln_bwd_cols_kernel(const uint16_t* __restrict__ dY, const uint16_t* __restrict__ X,
-                                   const float* __restrict__ mean_in, const float* __restrict__ rstd_in, int64_t h,
-                                   int64_t rows_per, float* __restrict__ dg_part, float* __restrict__ db_part) {
-  __shared__ float4 red[4][32];
+// Partial weight grads of shard j over its rows [j*rows_per, (j+1)*rows_per):
+// one CTA per (256-column block, shard); lane owns 8 columns (16-byte loads),
+// the 8 warps stride the shard's rows and are combined in warp order.
+constexpr int COLS_THREADS = 256;
+
+__global__ void __launch_bounds__(COLS_THREADS)
+    ln_bwd_cols_kernel(const uint16_t* __restrict__ dY, const uint16_t* __restrict__ X,
+                       const float* __restrict__ mean_in, const float* __restrict__ rstd_in, int64_t h,
+                       int64_t rows_per, float* __restrict__ dg_part, float* __restrict__ db_part) {
+  __shared__ float red[2][8][256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t col = static_cast<int64_t>(blockIdx.x) * 64 + 2 * lane;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 256 + lane * 8;
   const int j = blockIdx.y;
-  float dg0 = 0.0f, dg1 = 0.0f, db0 = 0.0f, db1 = 0.0f;
-  if (col < h) {
-    const int64_t r0 = static_cast<int64_t>(j) * rows_per;
-    for (int64_t r = r0 + warp; r < r0 + rows_per; r += 4) {
-      const float mean = mean_in[r], rstd = rstd_in[r];
-      float x0, x1, d0, d1;
-      unpack_bf16x2(*reinterpret_cast<const uint32_t*>(X + r * h + col), x0, x1);
-      unpack_bf16x2(*reinterpret_cast<const uint32_t*>(dY + r * h + col), d0, d1);
-      dg0 += d0 * (x0 - mean) * rstd;
-      dg1 += d1 * (x1 - mean) * rstd;
-      db0 += d0;
-      db1 += d1;
+  float dg[8] = {0, 0, 0, 0, 0, 0, 0, 0}, db[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (c0 < h) {
+    const int64_t r0 = static_cast<int64_t>(j) * rows_per, r1 = r0 + rows_per;
+    int64_t r = r0 + warp;
+    for (; r + 24 < r1; r += 32) {  // four rows in flight
+      uint4 xv[4], dv[4];
+      float mu[4], rs[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t rr = r + 8 * u;
+        xv[u] = *reinterpret_cast<const uint4*>(X + rr * h + c0);
+        dv[u] = *reinterpret_cast<const uint4*>(dY + rr * h + c0);
+        mu[u] = mean_in[rr];
+        rs[u] = rstd_in[rr];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t xw[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+        const uint32_t dw[4] = {dv[u].x, dv[u].y, dv[u].z, dv[u].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float x0, x1, d0, d1;
+          unpack_bf16x2(xw[q], x0, x1);
+          unpack_bf16x2(dw[q], d0, d1);
+          dg[2 * q] += d0 * (x0 - mu[u]) * rs[u];
+          dg[2 * q + 1] += d1 * (x1 - mu[u]) * rs[u];
+          db[2 * q] += d0;
+          db[2 * q + 1] += d1;
+        }
+      }
+    }
+    for (; r < r1; r += 8) {
+      const uint4 xv = *reinterpret_cast<const uint4*>(X + r * h + c0);
+      const uint4 dv = *reinterpret_cast<const uint4*>(dY + r * h + c0);
+      const float mu = mean_in[r], rs = rstd_in[r];
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+      const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float x0, x1, d0, d1;
+        unpack_bf16x2(xw[q], x0, x1);
+        unpack_bf16x2(dw[q], d0, d1);
+        dg[2 * q] += d0 * (x0 - mu) * rs;
+        dg[2 * q + 1] += d1 * (x1 - mu) * rs;
+        db[2 * q] += d0;
+        db[2 * q + 1] += d1;
+      }
     }
   }
-  red[warp][lane] = make_float4(dg0, dg1, db0, db1);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    red[0][warp][lane * 8 + e] = dg[e];
+    red[1][warp][lane * 8 + e] = db[e];
+  }
   __syncthreads();
-  if (warp == 0 && col < h) {
-    float4 s = red[0][lane];
-    for (int w = 1; w < 4; ++w) {
-      const float4 o = red[w][lane];
-      s.x += o.x; s.y += o.y; s.z += o.z; s.w += o.w;
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+  if (c < h) {
+    float sg = 0.0f, sb = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      sg += red[0][w][threadIdx.x];
+      sb += red[1][w][threadIdx.x];
     }
-    dg_part[static_cast<int64_t>(j) * h + col] = s.x;
-    dg_part[static_cast<int64_t>(j) * h + col + 1] = s.y;
-    db_part[static_cast<int64_t>(j) * h + col] = s.z;
-    db_part[static_cast<int64_t>(j) * h + col + 1] = s.w;
+    dg_part[static_cast<int64_t>(j) * h + c] = sg;
+    db_part[static_cast<int64_t>(j) * h + c] = sb;
   }
+}
+
+// The LayerNorm weight-gradient all-reduce: sum of the t shard partials, shard order.
+__global__ void ln_bwd_shard_sum_kernel(const float* __restrict__ dg_part, const float* __restrict__ db_part,
+                                        int64_t h, int t, float* __restrict__ dgamma, float* __restrict__ dbeta) {
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (c >= h) return;
+  float sg = 0.0f, sb = 0.0f;
+  for (int j = 0; j < t; ++j) {
+    sg += dg_part[static_cast<int64_t>(j) * h + c];
+    sb += db_part[static_cast<int64_t>(j) * h + c];
+  }
+  dgamma[c] = sg;
+  dbeta[c] = sb;
 }
 
 int row_threads(int64_t h) {
@@ -246,12 +306,14 @@ tp_status run_ln_backward(const uint16_t* dY, const uint16_t* X, const uint16_t*
   }
   ln_bwd_rows_kernel<<<static_cast<unsigned>(s), row_threads(h), 0, st>>>(dY, X, gamma, mean, rstd, dres, h, dX);
   TP_LAUNCHED();
-  dim3 g(static_cast<unsigned>((h + 63) / 64), static_cast<unsigned>(t));
-  ln_bwd_cols_kernel<<<g, 128, 0, st>>>(dY, X, mean, rstd, h, s / t, dg_part, db_part);
+  dim3 g(static_cast<unsigned>((h + 255) / 256), static_cast<unsigned>(t));
+  ln_bwd_cols_kernel<<<g, COLS_THREADS, 0, st>>>(dY, X, mean, rstd, h, s / t, dg_part, db_part);
   TP_LAUNCHED();
   // The LayerNorm weight-gradient all-reduce over the sequence shards, fixed order.
-  TP_RETURN_IF(run_shard_reduce(dg_part, 1, h, t, nullptr, nullptr, nullptr, dgamma, st));
-  return run_shard_reduce(db_part, 1, h, t, nullptr, nullptr, nullptr, dbeta, st);
+  ln_bwd_shard_sum_kernel<<<static_cast<unsigned>((h + 255) / 256), 256, 0, st>>>(dg_part, db_part, h, t, dgamma,
+                                                                                    dbeta);
+  TP_LAUNCHED();
+  return TP_OK;
 }
 
 }  // namespace tp
