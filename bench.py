@@ -296,7 +296,9 @@ def run_ours(args):
         torch.cuda.empty_cache()
         secondary = {"decode_c3": run_decode_extra(L, torch, args), "mlp_fwd_c1": run_mlp_fwd_extra(L, torch, args),
                      "layer_c4": run_layer_extra(L, torch, args, "c4"),
-                     "sp_layer_c5": run_layer_extra(L, torch, args, "c5")}
+                     "sp_layer_c5": run_layer_extra(L, torch, args, "c5"),
+                     "attention_c5": run_attn_extra(L, torch, args, "c5"),
+                     "sp_layernorm_c5": run_ln_extra(L, torch, args, "c5")}
 
     if rank != 0:
         return None
@@ -387,6 +389,88 @@ def run_mlp_fwd_extra(L, torch, args):
             "page_bytes": {"expanded_tensor": M * F * 2, "output_reduction_tensor": M * h * 2}}
 
 
+def run_attn_extra(L, torch, args, name="c5"):
+    """Head-sharded attention block alone at a layer config's shapes: QKV
+    column-parallel GEMM, per-head causal flash attention, W_o row-parallel
+    GEMM + g; forward and backward."""
+    import math
+    from megatron_tensor_transformer_shard_gb300 import inputs as I
+    from megatron_tensor_transformer_shard_gb300 import tp as T
+    c = I.CONFIGS[name]
+    N, d, t, nh, dh = c["N"], c["d"], c["t"], c["n_heads"], c["head_dim"]
+    inp = I.attn_inputs(N, d, bias=True, dy=True, seed=0, device="cuda")
+    bf16, f32 = torch.bfloat16, torch.float32
+    Wqkv = torch.empty(t, 3 * d // t, d, dtype=bf16, device="cuda")
+    bqkv = torch.empty(t, 3 * d // t, dtype=bf16, device="cuda")
+    Wo = torch.empty(t, d, d // t, dtype=bf16, device="cuda")
+    L.tp_pack_qkv_heads(inp["W_qkv"], d, nh, dh, t, Wqkv)
+    L.tp_pack_qkv_bias(inp["b_qkv"], d, nh, dh, t, bqkv)
+    L.tp_pack_row(inp["W_o"], d, d, t, Wo)
+    del inp["W_qkv"], inp["W_o"]
+    Y = torch.empty(N, d, dtype=bf16, device="cuda")
+    QKV = torch.empty(t, N, 3 * d // t, dtype=torch.float16, device="cuda")
+    O = torch.empty(t, N, d // t, dtype=bf16, device="cuda")
+    lse = torch.empty(t, nh // t, N, dtype=f32, device="cuda")
+    sc = 1.0 / math.sqrt(dh)
+    fwd = lambda: L.tp_attn_forward(inp["X"], N, d, nh, dh, t, 1, sc, Wqkv, bqkv, Wo, inp["b_o"], None, Y, QKV, O,
+                                    lse, 0, None, 0)
+    f_ms = _time(torch, fwd, max(5, min(args.steps, 20)))
+    dX = torch.empty(N, d, dtype=bf16, device="cuda")
+    gq = torch.empty(t, 3 * d // t, d, dtype=f32, device="cuda")
+    gbq = torch.empty(t, 3 * d // t, dtype=f32, device="cuda")
+    go = torch.empty(t, d, d // t, dtype=f32, device="cuda")
+    gbo = torch.empty(d, dtype=f32, device="cuda")
+    nws = L.tp_attn_backward_workspace_size(N, d, nh, dh, t, 0)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    bwd = lambda: L.tp_attn_backward(inp["dY"], inp["X"], QKV, O, lse, N, d, nh, dh, t, 1, sc, Wqkv, Wo, dX, gq, gbq,
+                                     go, gbo, 0, 0, ws, nws)
+    b_ms = _time(torch, bwd, max(5, min(args.steps, 20)))
+    proj = 2.0 * N * d * 3 * d + 2.0 * N * d * d
+    core = 2.0 * N * N * d  # causal: QK^T and PV over the unmasked half
+    return {"workload": f"attention block, t={t}, N={N}, d={d}, {nh} heads x {dh}, causal",
+            "fwd_ms": round(f_ms, 3), "fwd_TFLOPs": round((proj + core) / (f_ms / 1e3) / 1e12, 1),
+            "bwd_ms": round(b_ms, 3), "bwd_TFLOPs": round(2 * (proj + core) / (b_ms / 1e3) / 1e12, 1),
+            "flops_fwd": proj + core, "flops_core_fwd": core}
+
+
+def run_ln_extra(L, torch, args, name="c5"):
+    """Sequence-parallel LayerNorm kernels alone (HBM-bound) at a layer config's shape."""
+    from megatron_tensor_transformer_shard_gb300 import inputs as I
+    c = I.CONFIGS[name]
+    s, h, t = c["N"], c["d"], c["t"]
+    inp = I.ln_inputs(s, h, seed=0, device="cuda")
+    Xn = torch.empty(s, h, dtype=torch.bfloat16, device="cuda")
+    mean = torch.empty(s, dtype=torch.float32, device="cuda")
+    rstd = torch.empty(s, dtype=torch.float32, device="cuda")
+    # inputs of 64 MB stay partly in the 129 MB L2 between launches: flush it between timed calls
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    X = inp["X"]
+
+    def fwd():
+        flush.zero_()
+        L.tp_sp_layernorm_forward(X, s, h, t, inp["gamma"], inp["beta"], 1e-5, Xn, mean, rstd)
+
+    dX = torch.empty(s, h, dtype=torch.bfloat16, device="cuda")
+    parts = [torch.empty(t, h, dtype=torch.float32, device="cuda") for _ in range(2)]
+    dg, db = (torch.empty(h, dtype=torch.float32, device="cuda") for _ in range(2))
+
+    def bwd():
+        flush.zero_()
+        L.tp_sp_layernorm_backward(inp["dY"], X, inp["gamma"], mean, rstd, X, s, h, t, dX, parts[0], parts[1], dg, db)
+
+    fl_ms = _time(torch, flush.zero_, 10)
+    f_ms = _time(torch, fwd, 20) - fl_ms
+    b_ms = _time(torch, bwd, 20) - fl_ms
+    fwd_bytes = 2 * s * h * 2 + 2 * h * 2 + 2 * s * 4
+    bwd_bytes = 6 * s * h * 2 + s * 8 + 2 * t * h * 4 * 2
+    hbm = measured_peaks()["hbm"]
+    return {"workload": f"SP LayerNorm, [{t}][{s // t}][{h}]", "l2": "256 MB buffer written between calls (flush)",
+            "fwd_us": round(f_ms * 1e3, 2), "fwd_GBps": round(fwd_bytes / f_ms / 1e6, 1),
+            "fwd_frac_of_hbm": round(fwd_bytes / f_ms / 1e6 / hbm, 4),
+            "bwd_us": round(b_ms * 1e3, 2), "bwd_GBps": round(bwd_bytes / b_ms / 1e6, 1),
+            "bwd_frac_of_hbm": round(bwd_bytes / b_ms / 1e6 / hbm, 4)}
+
+
 def layer_flops(N, d, F):
     """fwd = QKV + W_o + MLP GEMMs + causal attention (unmasked half); fwd+bwd = 3 x fwd."""
     fwd = 2.0 * N * d * 3 * d + 2.0 * N * d * d + 4.0 * N * d * F + 2.0 * N * N * d
@@ -415,25 +499,6 @@ def run_layer_extra(L, torch, args, name):
                         f"{nh} heads x {c['head_dim']}, MLP {d}->{F}, causal"),
            "ms_per_step": round(ms, 3), "TFLOPs": round(fl / (ms / 1e3) / 1e12, 1), "flops_per_step": fl,
            "frac_of_peak": round(fl / (ms / 1e3) / 1e12 / peak, 4)}
-    if sp:   # SP LayerNorm kernels alone (HBM-bound)
-        s, h = N, d
-        Xn = torch.empty(s, h, dtype=torch.bfloat16, device="cuda")
-        mean = torch.empty(s, dtype=torch.float32, device="cuda")
-        rstd = torch.empty(s, dtype=torch.float32, device="cuda")
-        f_ms = _time(torch, lambda: L.tp_sp_layernorm_forward(X, s, h, t, w.ln1_g, w.ln1_b, 1e-5, Xn, mean, rstd), 20)
-        dX = torch.empty(s, h, dtype=torch.bfloat16, device="cuda")
-        parts = [torch.empty(t, h, dtype=torch.float32, device="cuda") for _ in range(2)]
-        dg, db = (torch.empty(h, dtype=torch.float32, device="cuda") for _ in range(2))
-        b_ms = _time(torch, lambda: L.tp_sp_layernorm_backward(G, X, w.ln1_g, mean, rstd, X, s, h, t, dX, parts[0],
-                                                               parts[1], dg, db), 20)
-        fwd_bytes = 2 * s * h * 2 + 2 * h * 2 + 2 * s * 4
-        bwd_bytes = 6 * s * h * 2 + s * 8 + 2 * t * h * 4 * 2
-        hbm = measured_peaks()["hbm"]
-        out["sp_layernorm"] = {"fwd_us": round(f_ms * 1e3, 2), "fwd_GBps": round(fwd_bytes / f_ms / 1e6, 1),
-                               "fwd_frac_of_hbm": round(fwd_bytes / f_ms / 1e6 / hbm, 4),
-                               "bwd_us": round(b_ms * 1e3, 2), "bwd_GBps": round(bwd_bytes / b_ms / 1e6, 1),
-                               "bwd_frac_of_hbm": round(bwd_bytes / b_ms / 1e6 / hbm, 4),
-                               "shape": f"[{t}][{s // t}][{h}]"}
     del w, inp
     torch.cuda.empty_cache()
     return out
@@ -509,6 +574,23 @@ def run_reference(args):
             "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_only(args):
+    import torch
+    torch.cuda.set_device(dist_env()[2])
+    from megatron_tensor_transformer_shard_gb300 import build as B
+    B.build()
+    from megatron_tensor_transformer_shard_gb300 import _lib as L
+    if args.only == "c1":
+        return {"mlp_fwd_c1": run_mlp_fwd_extra(L, torch, args)}
+    if args.only == "c3":
+        return {"decode_c3": run_decode_extra(L, torch, args)}
+    if args.only == "attn":
+        return {"attention_c5": run_attn_extra(L, torch, args)}
+    if args.only == "ln":
+        return {"sp_layernorm_c5": run_ln_extra(L, torch, args)}
+    return {f"layer_{args.only}": run_layer_extra(L, torch, args, args.only)}
+
+
 def main():
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -520,9 +602,15 @@ def main():
     p.add_argument("--no-extras", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     p.add_argument("--reference-rows", type=int, default=64, help="token rows per oracle step (--impl reference)")
+    p.add_argument("--only", choices=["c1", "c3", "c4", "c5", "attn", "ln"], default=None,
+                   help="run only one secondary workload (forward MLP c1, decode c3, layers c4/c5, the c5-shaped "
+                        "attention block or SP LayerNorm) and print it")
     args = p.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.only:
+        print(json.dumps(run_only(args)), flush=True)
+        return
     line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)
