@@ -298,7 +298,8 @@ def run_ours(args):
                      "layer_c4": run_layer_extra(L, torch, args, "c4"),
                      "sp_layer_c5": run_layer_extra(L, torch, args, "c5"),
                      "attention_c5": run_attn_extra(L, torch, args, "c5"),
-                     "sp_layernorm_c5": run_ln_extra(L, torch, args, "c5")}
+                     "sp_layernorm_c5": run_ln_extra(L, torch, args, "c5"),
+                     "decode_attention": run_decode_attn_extra(L, torch, args)}
 
     if rank != 0:
         return None
@@ -367,6 +368,46 @@ def run_decode_extra(L, torch, args):
             "us_per_step": round(us, 2), "GBps": round(gbs, 1), "bytes_per_step": nbytes,
             "frac_of_hbm": round(gbs / peaks["hbm"], 4), "hbm_peak_GBps": peaks["hbm"],
             "frac_of_8TBps": round(gbs / 8000.0, 4), "l2": "1.41 GB of weights > L2; no flush"}
+
+
+def run_decode_attn_extra(L, torch, args):
+    """Decode attention over a head-sharded KV cache, Llama-3-70B-shaped at
+    TP=4: d=8192, 64 query heads and 8 KV heads of 128 (two KV heads and their
+    two 8-head groups per shard), 8 sequences whose cache lengths are drawn
+    uniformly from 4096..8192 keys.  One step = QKV GEMV + cache append +
+    split-KV attention + combine + W_o GEMV with the g sum."""
+    from megatron_tensor_transformer_shard_gb300 import inputs as I
+    from megatron_tensor_transformer_shard_gb300 import tp as T
+    nh, nkv, hd, t, B, L_max = 64, 8, 128, 4, 8, 8192
+    d = nh * hd
+    inp = I.decode_attn_inputs(B, d, nh, nkv, hd, L_max, bias=False, seed=0, device="cuda")
+    pos = I.decode_positions(B, 4095, L_max - 1, seed=0)
+    w = T.DecodeAttnWeights(inp["W_qkv"], None, inp["W_o"], None, nh, nkv, hd, t)
+    del inp["W_qkv"], inp["W_o"]
+    # n_kv = 8 >= t: shard i holds KV heads 2i, 2i+1, so the per-shard cache is the unsplit one
+    K = inp["K"].view(w.cache_shape(B, L_max))
+    V = inp["V"].view(w.cache_shape(B, L_max))
+    posd = pos.cuda()
+    ws = w.workspace(B, L_max, "cuda")
+    x = inp["x"]
+    step = lambda: T.decode_attn_forward(x, w, K, V, posd, ws=ws)
+    us = 1e3 * _time(torch, step, max(20, args.steps), warmup=5)
+    R = (nh // t + 2 * w.kv_t) * hd
+    w_bytes = t * R * d * 2 + nh * hd * d * 2
+    kv_bytes = sum(2 * t * w.kv_t * (int(p) + 1) * hd * 2 for p in pos.tolist())
+    nbytes = w_bytes + kv_bytes
+    gbs = nbytes / (us / 1e6) / 1e9
+    peaks = measured_peaks()
+    return {"workload": "decode attention, t=4, d=8192, 64 query / 8 KV heads x 128, B=8, cache lengths "
+                        "4096..8192 (seeded uniform), fp16 KV cache",
+            "us_per_step": round(us, 2), "GBps": round(gbs, 1), "bytes_per_step": nbytes,
+            "weight_bytes": w_bytes, "kv_bytes": kv_bytes, "lengths": [int(p) + 1 for p in pos.tolist()],
+            "frac_of_hbm": round(gbs / peaks["hbm"], 4), "hbm_peak_GBps": peaks["hbm"],
+            "l2": "~500 MB of weights and cache per step > L2; no flush",
+            "allreduce_accounting": {"payload_bytes": B * d * 2, "allreduces_per_layer_per_token": 2,
+                                     "allreduces_per_token_80_layers": 160,
+                                     "on_device": "each is the fixed-order shard sum inside the row-parallel "
+                                                  "GEMV (W_o here, W_down in the MLP): no extra HBM bytes"}}
 
 
 def run_mlp_fwd_extra(L, torch, args):
@@ -588,6 +629,8 @@ def run_only(args):
         return {"attention_c5": run_attn_extra(L, torch, args)}
     if args.only == "ln":
         return {"sp_layernorm_c5": run_ln_extra(L, torch, args)}
+    if args.only == "dattn":
+        return {"decode_attention": run_decode_attn_extra(L, torch, args)}
     return {f"layer_{args.only}": run_layer_extra(L, torch, args, args.only)}
 
 
@@ -602,9 +645,9 @@ def main():
     p.add_argument("--no-extras", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     p.add_argument("--reference-rows", type=int, default=64, help="token rows per oracle step (--impl reference)")
-    p.add_argument("--only", choices=["c1", "c3", "c4", "c5", "attn", "ln"], default=None,
+    p.add_argument("--only", choices=["c1", "c3", "c4", "c5", "attn", "ln", "dattn"], default=None,
                    help="run only one secondary workload (forward MLP c1, decode c3, layers c4/c5, the c5-shaped "
-                        "attention block or SP LayerNorm) and print it")
+                        "attention block, SP LayerNorm, or decode attention over a sharded KV cache) and print it")
     args = p.parse_args()
     if args.warmup < 3:
         args.warmup = 3

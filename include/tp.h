@@ -88,8 +88,10 @@ int tp_abi_version(void);
 const char* tp_status_string(tp_status s);
 
 /* Synchronises `stream`, then reads and clears the current device's error
- * word.  Returns TP_OK, TP_ERR_TIMEOUT (a bounded wait expired), or
- * TP_ERR_CUDA if the synchronisation itself failed. */
+ * word.  Returns TP_OK, TP_ERR_TIMEOUT (a bounded wait expired), TP_ERR_SHAPE
+ * (a kernel found an argument that lives in device memory out of range, e.g.
+ * a decode position >= L_max), or TP_ERR_CUDA if the synchronisation itself
+ * failed. */
 tp_status tp_get_device_status(tp_stream stream);
 
 /* Fault-path self test: launches one CTA that waits on an mbarrier nothing
@@ -132,6 +134,25 @@ tp_status tp_unpack_qkv_heads(const tp_bf16* Wp, int64_t d, int n_heads, int hea
 /* b: (3d) -> [t][3d/t] in the same head order. */
 tp_status tp_pack_qkv_bias(const tp_bf16* b, int64_t d, int n_heads, int head_dim, int t, tp_bf16* bp,
                            tp_stream stream);
+
+/* Grouped-query attention ("02 — Tensor Parallelism", "The attention
+ * pairing": with GQA/MQA the heads shard by KV group; "Tensor and sequence
+ * parallelism", exercise 1: with fewer KV heads than shards each KV head is
+ * replicated on t/n_kv shards).
+ * Wqkv: (d, (n_heads + 2 n_kv) * head_dim), columns [Q heads | K heads | V
+ * heads]; query head j reads KV head j / (n_heads / n_kv).
+ * Packed: [t][R][d], R = (n_heads/t + 2 kv_t) * head_dim, rows [shard i's Q
+ * heads | its kv_t K heads | its kv_t V heads], kv_t = n_kv/t when n_kv >= t
+ * (the groups of its query heads), else 1 (KV head i*n_kv/t, a copy).
+ * Requires t | n_heads, n_kv | n_heads, and n_kv % t == 0 or t % n_kv == 0.
+ * Unpack writes every copy of a replicated column (the same bits). */
+tp_status tp_pack_qkv_gqa(const tp_bf16* Wqkv, int64_t d, int n_heads, int n_kv_heads, int head_dim, int t,
+                          tp_bf16* Wp, tp_stream stream);
+tp_status tp_unpack_qkv_gqa(const tp_bf16* Wp, int64_t d, int n_heads, int n_kv_heads, int head_dim, int t,
+                            tp_bf16* Wqkv, tp_stream stream);
+/* b: ((n_heads + 2 n_kv) * head_dim) -> [t][R] in the same order. */
+tp_status tp_pack_qkv_gqa_bias(const tp_bf16* b, int n_heads, int n_kv_heads, int head_dim, int t, tp_bf16* bp,
+                               tp_stream stream);
 
 /* ------------------------------------------- column / row parallel linear
  * The two halves of the pairing, each ONE kernel launch ("02 — Tensor
@@ -203,6 +224,40 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
 tp_status tp_decode_swiglu_forward(const tp_bf16* x, int64_t M, int64_t h, int64_t F, int t,
                                    const tp_bf16* Wgu_p, const tp_bf16* Wdown_p, tp_bf16* y, tp_bf16* a_save,
                                    tp_stream stream);
+
+/* ------------------------------------ decode attention, sharded KV cache
+ * One decode step of the attention block for B sequences ("02 — Tensor
+ * Parallelism", "The critical inference-time subtlety: KV cache also shards":
+ * each shard holds the KV heads of its own query heads, so the cache splits
+ * with the heads; "The count: two all-reduces per block per direction": the
+ * block ends in one all-reduce of B x d elements per token):
+ *   shard i: qkv_i = x W_qkv,i + b_qkv,i                 (column-parallel GEMV)
+ *            K_cache[i][jl][b][pos[b]] = k, V_cache[...] = v  (append, fp16)
+ *            per query head: o = softmax(scale q K[0..pos[b]]^T) V[0..pos[b]]
+ *   g:       y = sum_{i=0..t-1} O_i W_o,i + b_o          (fixed order, bias once)
+ * x [B][d] bf16, 1 <= B <= 256; Wqkv_p / bqkv_p from tp_pack_qkv_gqa(_bias)
+ * (bqkv_p nullable); Wo_p [t][d][n_heads*head_dim/t] from tp_pack_row of W_o
+ * (n_heads*head_dim, d); bo [d] nullable; y [B][d] bf16.
+ * K_cache, V_cache: IEEE fp16 bits, [t][kv_t][B][L_max][head_dim] (kv_t as for
+ * tp_pack_qkv_gqa); a replicated KV head has one copy per shard that holds
+ * it.  Positions 0..pos[b]-1 must hold the sequence's earlier keys/values;
+ * the call writes position pos[b] and attends to keys 0..pos[b].  Bytes past
+ * pos[b] are never used (they may hold anything, even non-finite values).
+ * pos: DEVICE int32 [B], 0 <= pos[b] < L_max; a position out of range is
+ * clamped, its cache write skipped, and tp_get_device_status() reports
+ * TP_ERR_SHAPE.  head_dim == 128; query heads per KV group on one shard
+ * (min(n_heads/n_kv, n_heads/t)) <= 32.  ws: 256-byte aligned,
+ * tp_decode_attn_workspace_size() bytes (Q, the tile plan, split-KV partials
+ * and O); the call allocates nothing.  Four to five kernels: the QKV GEMV
+ * (per group of 8 sequences), the split-KV attention, the combine, and the
+ * W_o GEMV (per group of 8 sequences). */
+size_t tp_decode_attn_workspace_size(int64_t B, int64_t d, int n_heads, int n_kv_heads, int head_dim, int t,
+                                     int64_t L_max);
+tp_status tp_decode_attn_forward(const tp_bf16* x, int64_t B, int64_t d, int n_heads, int n_kv_heads, int head_dim,
+                                 int t, float scale, const tp_bf16* Wqkv_p, const tp_bf16* bqkv_p,
+                                 const tp_bf16* Wo_p, const tp_bf16* bo, uint16_t* K_cache, uint16_t* V_cache,
+                                 int64_t L_max, const int32_t* pos, tp_bf16* y, void* ws, size_t ws_bytes,
+                                 tp_stream stream);
 
 /* -------------------------------------------------- head-sharded attention
  * ("02 — Tensor Parallelism", "The attention pairing"; "Megatron-LM: Tensor

@@ -40,6 +40,9 @@ SIGNATURES = {
     "tp_pack_qkv_heads": (_I, [_P, _I64, _I, _I, _I, _P, _P]),
     "tp_unpack_qkv_heads": (_I, [_P, _I64, _I, _I, _I, _P, _P]),
     "tp_pack_qkv_bias": (_I, [_P, _I64, _I, _I, _I, _P, _P]),
+    "tp_pack_qkv_gqa": (_I, [_P, _I64, _I, _I, _I, _I, _P, _P]),
+    "tp_unpack_qkv_gqa": (_I, [_P, _I64, _I, _I, _I, _I, _P, _P]),
+    "tp_pack_qkv_gqa_bias": (_I, [_P, _I, _I, _I, _I, _P, _P]),
     "tp_mlp_workspace_size": (_SZ, [_I64, _I64, _I64, _I, _U]),
     "tp_mlp_forward": (_I, [_P, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _U, _P, _SZ, _P]),
     "tp_mlp_backward_workspace_size": (_SZ, [_I64, _I64, _I64, _I, _U]),
@@ -50,6 +53,9 @@ SIGNATURES = {
     "tp_column_parallel_forward": (_I, [_P, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P, _P]),
     "tp_row_parallel_forward": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _P, _P]),
     "tp_decode_swiglu_forward": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _P, _P]),
+    "tp_decode_attn_workspace_size": (_SZ, [_I64, _I64, _I, _I, _I, _I, _I64]),
+    "tp_decode_attn_forward": (_I, [_P, _I64, _I64, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _P,
+                                    _SZ, _P]),
     "tp_sp_layernorm_forward": (_I, [_P, _I64, _I64, _I, _P, _P, _F, _P, _P, _P, _P]),
     "tp_sp_layernorm_backward": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I, _P, _P, _P, _P, _P, _P]),
     "tp_attn_forward": (_I, [_P, _I64, _I64, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _U, _P, _SZ,

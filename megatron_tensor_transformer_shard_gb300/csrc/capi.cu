@@ -284,7 +284,8 @@ tp_status tp_get_device_status(tp_stream stream) {
   if (word == 0) return TP_OK;
   const int zero = 0;
   if (cudaMemcpyToSymbol(g_tp_error_word, &zero, sizeof(int)) != cudaSuccess) return TP_ERR_CUDA;
-  return TP_ERR_TIMEOUT;
+  // codes 0x200-0x2ff: an argument the host could not check (it lives in device memory)
+  return (word >= 0x200 && word < 0x300) ? TP_ERR_SHAPE : TP_ERR_TIMEOUT;
 }
 
 tp_status tp_selftest_bounded_wait(int64_t timeout_us, tp_stream stream) {
@@ -323,6 +324,19 @@ tp_status tp_unpack_qkv_heads(const tp_bf16* Wp, int64_t d, int n_heads, int hea
 tp_status tp_pack_qkv_bias(const tp_bf16* b, int64_t d, int n_heads, int head_dim, int t, tp_bf16* bp,
                            tp_stream stream) {
   return pack_qkv_bias(b, d, n_heads, head_dim, t, bp, S(stream));
+}
+
+tp_status tp_pack_qkv_gqa(const tp_bf16* Wqkv, int64_t d, int n_heads, int n_kv_heads, int head_dim, int t,
+                          tp_bf16* Wp, tp_stream stream) {
+  return pack_qkv_gqa(Wqkv, d, n_heads, n_kv_heads, head_dim, t, Wp, 0, S(stream));
+}
+tp_status tp_unpack_qkv_gqa(const tp_bf16* Wp, int64_t d, int n_heads, int n_kv_heads, int head_dim, int t,
+                            tp_bf16* Wqkv, tp_stream stream) {
+  return pack_qkv_gqa(Wp, d, n_heads, n_kv_heads, head_dim, t, Wqkv, 1, S(stream));
+}
+tp_status tp_pack_qkv_gqa_bias(const tp_bf16* b, int n_heads, int n_kv_heads, int head_dim, int t, tp_bf16* bp,
+                               tp_stream stream) {
+  return pack_qkv_gqa_bias(b, n_heads, n_kv_heads, head_dim, t, bp, S(stream));
 }
 
 // ------------------------------------------------------------------ TP MLP
@@ -502,6 +516,21 @@ tp_status tp_decode_swiglu_forward(const tp_bf16* x, int64_t M, int64_t h, int64
                                    const tp_bf16* Wgu_p, const tp_bf16* Wdown_p, tp_bf16* y, tp_bf16* a_save,
                                    tp_stream stream) {
   return run_decode_swiglu(x, M, h, F, t, Wgu_p, Wdown_p, y, a_save, S(stream));
+}
+
+// ----------------------------------------------------------- decode attention
+size_t tp_decode_attn_workspace_size(int64_t B, int64_t d, int n_heads, int n_kv_heads, int head_dim, int t,
+                                     int64_t L_max) {
+  return decode_attn_ws_bytes(B, d, n_heads, n_kv_heads, head_dim, t, L_max);
+}
+
+tp_status tp_decode_attn_forward(const tp_bf16* x, int64_t B, int64_t d, int n_heads, int n_kv_heads, int head_dim,
+                                 int t, float scale, const tp_bf16* Wqkv_p, const tp_bf16* bqkv_p,
+                                 const tp_bf16* Wo_p, const tp_bf16* bo, uint16_t* K_cache, uint16_t* V_cache,
+                                 int64_t L_max, const int32_t* pos, tp_bf16* y, void* ws, size_t ws_bytes,
+                                 tp_stream stream) {
+  return run_decode_attn(x, B, d, n_heads, n_kv_heads, head_dim, t, scale, Wqkv_p, bqkv_p, Wo_p, bo, K_cache, V_cache,
+                         L_max, pos, y, ws, ws_bytes, S(stream));
 }
 
 // ------------------------------------------------------------------ attention

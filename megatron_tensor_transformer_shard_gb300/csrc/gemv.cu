@@ -119,8 +119,9 @@ __global__ void __launch_bounds__(GEMV_THREADS)
 // Wd is [t][h][Ft]: row c of shard i is contiguous.
 template <int M>
 __global__ void __launch_bounds__(GEMV_THREADS)
-    down_reduce_kernel(const uint16_t* __restrict__ a, int64_t h, int64_t F, int t,
-                       const uint16_t* __restrict__ Wd, uint16_t* __restrict__ y) {
+    down_reduce_kernel(const uint16_t* __restrict__ a, int64_t lda, int64_t h, int64_t F, int t,
+                       const uint16_t* __restrict__ Wd, const uint16_t* __restrict__ bias,
+                       uint16_t* __restrict__ y) {
   __shared__ float red[GEMV_WARPS][MAX_T * M];
   __shared__ float tot[MAX_T * M];
   const int64_t Ft = F / t;
@@ -147,7 +148,7 @@ __global__ void __launch_bounds__(GEMV_THREADS)
             if (cc < chunks) {
 #pragma unroll
               for (int m = 0; m < M; ++m) {
-                const uint4 av = __ldg(reinterpret_cast<const uint4*>(ai + m * F) + cc);
+                const uint4 av = __ldg(reinterpret_cast<const uint4*>(ai + m * lda) + cc);
                 acc[i * M + m] += dot8(w[j], av);
               }
             }
@@ -160,6 +161,7 @@ __global__ void __launch_bounds__(GEMV_THREADS)
       const int m = threadIdx.x;
       float s = 0.0f;
       for (int i = 0; i < t; ++i) s += tot[i * M + m];  // g: fixed shard order
+      if (bias) s += bf16_bits_to_float(bias[col]);      // once, after the sum
       y[m * h + col] = float_to_bf16_bits(s);
     }
   }
@@ -177,12 +179,51 @@ tp_status launch_decode(const uint16_t* x, int64_t h, int64_t F, int t, const ui
   if (g2 > h) g2 = h;
   swiglu_gate_up_kernel<M><<<static_cast<unsigned>(g1), GEMV_THREADS, 0, s>>>(x, h, F, Wgu, a);
   TP_LAUNCHED();
-  down_reduce_kernel<M><<<static_cast<unsigned>(g2), GEMV_THREADS, 0, s>>>(a, h, F, t, Wd, y);
+  down_reduce_kernel<M><<<static_cast<unsigned>(g2), GEMV_THREADS, 0, s>>>(a, F, h, F, t, Wd, nullptr, y);
+  TP_LAUNCHED();
+  return TP_OK;
+}
+
+template <int M>
+tp_status launch_row(const uint16_t* a, int64_t K, int64_t h, int t, const uint16_t* Wd, const uint16_t* bias,
+                     uint16_t* y, cudaStream_t s) {
+  int per_sm = 0;
+  TP_CUDA_CHECK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, down_reduce_kernel<M>, GEMV_THREADS, 0));
+  int64_t g = static_cast<int64_t>(device_sm_count()) * (per_sm > 0 ? per_sm : 1);
+  if (g > h) g = h;
+  down_reduce_kernel<M><<<static_cast<unsigned>(g), GEMV_THREADS, 0, s>>>(a, K, h, K, t, Wd, bias, y);
   TP_LAUNCHED();
   return TP_OK;
 }
 
 }  // namespace
+
+// Row-parallel GEMV followed by g: y[m] = sum_{i<t} a[m][C_i] W_i^T + bias (once),
+// a [M][K], W [t][h][K/t].  Rows are taken 8 at a time (each group re-streams W).
+tp_status run_row_gemv(const uint16_t* a, int64_t M, int64_t K, int64_t h, int t, const uint16_t* Wd,
+                       const uint16_t* bias, uint16_t* y, cudaStream_t s) {
+  if (M < 0 || K < 1 || h < 1 || t < 1) return TP_ERR_INVALID_ARG;
+  if (t > MAX_T || K % t != 0 || (K / t) % 8 != 0) return TP_ERR_SHAPE;
+  if (M == 0) return TP_OK;
+  for (int64_t m0 = 0; m0 < M; m0 += 8) {
+    const int mg = static_cast<int>(M - m0 < 8 ? M - m0 : 8);
+    const uint16_t* am = a + m0 * K;
+    uint16_t* ym = y + m0 * h;
+    tp_status st;
+    switch (mg) {
+      case 1: st = launch_row<1>(am, K, h, t, Wd, bias, ym, s); break;
+      case 2: st = launch_row<2>(am, K, h, t, Wd, bias, ym, s); break;
+      case 3: st = launch_row<3>(am, K, h, t, Wd, bias, ym, s); break;
+      case 4: st = launch_row<4>(am, K, h, t, Wd, bias, ym, s); break;
+      case 5: st = launch_row<5>(am, K, h, t, Wd, bias, ym, s); break;
+      case 6: st = launch_row<6>(am, K, h, t, Wd, bias, ym, s); break;
+      case 7: st = launch_row<7>(am, K, h, t, Wd, bias, ym, s); break;
+      default: st = launch_row<8>(am, K, h, t, Wd, bias, ym, s); break;
+    }
+    TP_RETURN_IF(st);
+  }
+  return TP_OK;
+}
 
 tp_status run_decode_swiglu(const uint16_t* x, int64_t M, int64_t h, int64_t F, int t, const uint16_t* Wgu,
                             const uint16_t* Wd, uint16_t* y, uint16_t* a, cudaStream_t s) {

@@ -124,6 +124,51 @@ tp_status pack_qkv(const uint16_t* src, int64_t d, int n_heads, int head_dim, in
 tp_status pack_qkv_bias(const uint16_t* b, int64_t d, int n_heads, int head_dim, int t, uint16_t* bp,
                         cudaStream_t s);
 
+tp_status pack_qkv_gqa(const uint16_t* src, int64_t d, int n_heads, int n_kv, int head_dim, int t, uint16_t* dst,
+                       int dir, cudaStream_t s);
+tp_status pack_qkv_gqa_bias(const uint16_t* b, int n_heads, int n_kv, int head_dim, int t, uint16_t* bp,
+                            cudaStream_t s);
+
+// skinny GEMM (skinny_gemm.cu): y[b][r] = sum_k W[r][k] x[b][k] for 1..32 rows of x.
+enum SkEpilogue : int { SK_EPI_BF16 = 0, SK_EPI_QKV = 1 };
+struct SkGemmJob {
+  const uint16_t* W = nullptr;  // [slabs][R][Kt] bf16, Kt = 128 * ku_per_slab
+  int slabs = 1;
+  int64_t R = 0;
+  int ku_per_slab = 0;
+  const uint16_t* x = nullptr;  // [B][ldx] bf16, K = slabs * Kt columns used
+  int64_t ldx = 0;
+  int B = 0;
+  float* part = nullptr;        // skinny_part_floats(R, B) floats
+  int nrb = 0, nku = 0;         // set by run_skinny_gemm
+  int epi = SK_EPI_BF16;
+  const uint16_t* bias = nullptr;  // [R] nullable, added once after the full K sum
+  uint16_t* y = nullptr;           // SK_EPI_BF16: y[b * ldy + r]
+  int64_t ldy = 0;
+  // SK_EPI_QKV: packed decode QKV rows [t][R_t], routed to q (fp16) or the cache copies
+  int64_t R_t = 0, L_max = 0;
+  int q_t = 0, kv_t = 0, nh = 0;
+  const int32_t* pos = nullptr;
+  uint16_t* q = nullptr;
+  uint16_t* Kc = nullptr;
+  uint16_t* Vc = nullptr;
+  int* tile_start = nullptr;  // SK_EPI_QKV: if non-null, the reduce kernel also writes the tile plan
+  int* done = nullptr;        //   ... and zeroes these per-stream counters
+  int* err = nullptr;
+};
+size_t skinny_part_floats(int64_t R, int B);
+bool skinny_ok(int64_t R, int64_t Kt, int B);
+tp_status run_skinny_gemm(SkGemmJob j, cudaStream_t s);
+
+// decode attention (decode_attn.cu)
+size_t decode_attn_ws_bytes(int64_t B, int64_t d, int n_heads, int n_kv, int head_dim, int t, int64_t L_max);
+tp_status run_decode_attn(const uint16_t* x, int64_t B, int64_t d, int n_heads, int n_kv, int head_dim, int t,
+                          float scale, const uint16_t* Wqkv_p, const uint16_t* bqkv_p, const uint16_t* Wo_p,
+                          const uint16_t* bo, uint16_t* Kc, uint16_t* Vc, int64_t L_max, const int32_t* pos,
+                          uint16_t* y, void* ws, size_t ws_bytes, cudaStream_t s);
+tp_status run_row_gemv(const uint16_t* a, int64_t M, int64_t K, int64_t h, int t, const uint16_t* Wd,
+                       const uint16_t* bias, uint16_t* y, cudaStream_t s);
+
 // decode GEMV (gemv.cu), LayerNorm (layernorm.cu)
 tp_status run_decode_swiglu(const uint16_t* x, int64_t M, int64_t h, int64_t F, int t, const uint16_t* Wgu,
                             const uint16_t* Wd, uint16_t* y, uint16_t* a, cudaStream_t s);

@@ -16,7 +16,7 @@
 namespace tp {
 namespace {
 
-enum PackKind : int { PK_COL = 0, PK_ROW = 1, PK_SWIGLU = 2, PK_QKV = 3 };
+enum PackKind : int { PK_COL = 0, PK_ROW = 1, PK_SWIGLU = 2, PK_QKV = 3, PK_QKV_GQA = 4 };
 
 struct PackMap {
   int kind;
@@ -30,6 +30,8 @@ struct PackMap {
   int head_dim;
   int heads_per_shard;
   int group;
+  int n_heads, n_kv, kv_t;  // QKV_GQA
+  int64_t R_t;              // QKV_GQA rows per shard
 };
 
 // Source column and row base for packed row r; `part` selects the source matrix.
@@ -54,6 +56,25 @@ __device__ __forceinline__ void map_row(const PackMap& m, int64_t r, int64_t& co
       const int64_t w = rem - q * 2 * m.group;
       part = static_cast<int>(w / m.group);
       col = i * m.Ft + q * m.group + (w - part * m.group);
+      break;
+    }
+    case PK_QKV_GQA: {  // [t][R_t][d], rows [Q heads of shard i | its K heads | its V heads]
+      const int64_t i = r / m.R_t;
+      const int64_t rr = r - i * m.R_t;
+      const int64_t qw = static_cast<int64_t>(m.heads_per_shard) * m.head_dim;
+      if (rr < qw) {
+        col = i * qw + rr;
+      } else {
+        const int64_t kvw = static_cast<int64_t>(m.kv_t) * m.head_dim;
+        const int64_t w2 = rr - qw;
+        const int64_t pt = w2 / kvw;  // 0: K, 1: V
+        const int64_t w3 = w2 - pt * kvw;
+        const int64_t jl = w3 / m.head_dim, e = w3 - jl * m.head_dim;
+        // KV heads of shard i: the groups of its query heads; one replicated head when n_kv < t
+        const int64_t t = m.R / m.R_t;
+        const int64_t first = m.n_kv >= t ? i * m.kv_t : (i * m.n_kv) / t;
+        col = static_cast<int64_t>(m.n_heads) * m.head_dim + pt * m.n_kv * m.head_dim + (first + jl) * m.head_dim + e;
+      }
       break;
     }
     default: {  // PK_QKV: [t][3d/t][d], rows [Q_i | K_i | V_i]
@@ -200,6 +221,46 @@ static bool qkv_map(PackMap& m, int64_t d, int n_heads, int head_dim, int t) {
   m.head_dim = head_dim;
   m.heads_per_shard = n_heads / t;
   return true;
+}
+
+static bool qkv_gqa_map(PackMap& m, int64_t d, int n_heads, int n_kv, int head_dim, int t) {
+  if (t < 1 || n_heads < 1 || n_kv < 1 || head_dim < 1 || d < 0) return false;
+  if (n_heads % t != 0 || n_heads % n_kv != 0) return false;
+  if (n_kv >= t ? (n_kv % t != 0) : (t % n_kv != 0)) return false;
+  m = PackMap{};
+  m.kind = PK_QKV_GQA;
+  m.n_heads = n_heads;
+  m.n_kv = n_kv;
+  m.kv_t = n_kv >= t ? n_kv / t : 1;
+  m.heads_per_shard = n_heads / t;
+  m.head_dim = head_dim;
+  m.R_t = static_cast<int64_t>(m.heads_per_shard + 2 * m.kv_t) * head_dim;
+  m.R = m.R_t * t;
+  m.row_len = d;
+  m.ld = static_cast<int64_t>(n_heads + 2 * n_kv) * head_dim;
+  return true;
+}
+
+// dir 1 (unpack) writes a replicated KV column once per copy, the same bits each time.
+tp_status pack_qkv_gqa(const uint16_t* src, int64_t d, int n_heads, int n_kv, int head_dim, int t, uint16_t* dst,
+                       int dir, cudaStream_t s) {
+  if (!src || !dst || d < 0) return TP_ERR_INVALID_ARG;
+  PackMap m;
+  if (!qkv_gqa_map(m, d, n_heads, n_kv, head_dim, t)) return TP_ERR_SHAPE;
+  return dir == 0 ? launch_pack(m, 0, src, nullptr, nullptr, nullptr, nullptr, dst, s)
+                  : launch_pack(m, 1, nullptr, nullptr, dst, nullptr, src, nullptr, s);
+}
+
+tp_status pack_qkv_gqa_bias(const uint16_t* b, int n_heads, int n_kv, int head_dim, int t, uint16_t* bp,
+                            cudaStream_t s) {
+  if (!b || !bp) return TP_ERR_INVALID_ARG;
+  PackMap m;
+  if (!qkv_gqa_map(m, 0, n_heads, n_kv, head_dim, t)) return TP_ERR_SHAPE;
+  if (m.R == 0) return TP_OK;
+  TP_RETURN_IF(ready());
+  gather_bias_kernel<<<static_cast<unsigned>((m.R + 255) / 256), 256, 0, s>>>(m, b, bp);
+  TP_LAUNCHED();
+  return TP_OK;
 }
 
 tp_status pack_qkv(const uint16_t* src, int64_t d, int n_heads, int head_dim, int t, uint16_t* dst, int dir,

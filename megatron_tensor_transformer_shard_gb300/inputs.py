@@ -112,6 +112,37 @@ def layer_inputs(N, d, F, seed=0, device="cpu"):
     return out
 
 
+def decode_attn_inputs(B, d, n_heads, n_kv, head_dim, L_max, bias=True, seed=0, device="cpu"):
+    """One decode step of a grouped-query attention block, drawn in this order:
+    x (B, d) ~ N(0,1); W_qkv (d, (n_heads + 2 n_kv) head_dim) laid out
+    [Q heads | K heads | V heads] and W_o (n_heads head_dim, d) ~ N(0, 0.02);
+    biases 0.01 N(0,1); the cached keys and values of the earlier tokens
+    K, V [n_kv][B][L_max][head_dim] ~ N(0, (0.02 sqrt(d))^2) -- the spread of
+    x W_k for such x and W -- rounded to IEEE fp16, the cache's storage type."""
+    g = make_generator(seed, device)
+    nq, nk = n_heads * head_dim, n_kv * head_dim
+    out = {"x": _draw(g, (B, d), 1.0, device), "W_qkv": _draw(g, (d, nq + 2 * nk), WEIGHT_STD, device)}
+    out["b_qkv"] = _draw(g, (nq + 2 * nk,), BIAS_SCALE, device) if bias else None
+    out["W_o"] = _draw(g, (nq, d), WEIGHT_STD, device)
+    out["b_o"] = _draw(g, (d,), BIAS_SCALE, device) if bias else None
+    kv_std = WEIGHT_STD * float(d) ** 0.5
+    for k in ("K", "V"):
+        out[k] = (kv_std * torch.randn(n_kv, B, L_max, head_dim, generator=g, device=device)).to(torch.float16)
+    return out
+
+
+def decode_positions(B, lo, hi, seed=0):
+    """Seeded cache positions, uniform on [lo, hi] (a ragged length mix), int32."""
+    g = make_generator(seed + 7919, "cpu")
+    return torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int32)
+
+
+def f16_bits(t: torch.Tensor) -> np.ndarray:
+    """Raw IEEE fp16 bit patterns of a (CPU) fp16 tensor as a uint16 array."""
+    assert t.dtype == torch.float16
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
 def bits(t: torch.Tensor) -> np.ndarray:
     """Raw bf16 bit patterns of a (CPU) bf16 tensor as a uint16 array."""
     assert t.dtype == torch.bfloat16

@@ -186,3 +186,51 @@ def layer_backward(G, saved, w: LayerWeights):
             "ln1_g_part": ln1["gp"], "ln2_g_part": ln2["gp"],
             "Wqkv_p": dWqkv, "bqkv_p": dbqkv, "Wo_p": dWo, "b_o": dbo,
             "Wup_p": g["dWup_p"], "b_up": g["dbup"], "Wdown_p": g["dWdown_p"], "b_down": g["dbdown"]}
+
+
+class DecodeAttnWeights:
+    """Packed weights of a TP attention block with grouped-query heads, for
+    decode: W_qkv (d, (n_heads + 2 n_kv) head_dim) -> [t][R][d] sharded by KV
+    group (replicated KV heads when n_kv < t); W_o (n_heads head_dim, d) ->
+    [t][d][n_heads head_dim / t]."""
+
+    def __init__(self, W_qkv, b_qkv, W_o, b_o, n_heads, n_kv, head_dim, t):
+        d = W_qkv.shape[0]
+        self.d, self.n_heads, self.n_kv, self.head_dim, self.t = d, n_heads, n_kv, head_dim, t
+        self.kv_t = n_kv // t if n_kv >= t else 1
+        R = (n_heads // t + 2 * self.kv_t) * head_dim
+        dev = W_qkv.device
+        self.Wqkv_p = torch.empty(t, R, d, dtype=BF16, device=dev)
+        L.tp_pack_qkv_gqa(W_qkv, d, n_heads, n_kv, head_dim, t, self.Wqkv_p)
+        self.bqkv_p = None
+        if b_qkv is not None:
+            self.bqkv_p = torch.empty(t, R, dtype=BF16, device=dev)
+            L.tp_pack_qkv_gqa_bias(b_qkv, n_heads, n_kv, head_dim, t, self.bqkv_p)
+        nq = n_heads * head_dim
+        self.Wo_p = torch.empty(t, d, nq // t, dtype=BF16, device=dev)
+        L.tp_pack_row(W_o, nq, d, t, self.Wo_p)
+        self.b_o = b_o
+
+    def cache_shape(self, B, L_max):
+        """Per-shard KV cache [t][kv_t][B][L_max][head_dim] (fp16)."""
+        return (self.t, self.kv_t, B, L_max, self.head_dim)
+
+    def workspace(self, B, L_max, device):
+        return _ws(L.tp_decode_attn_workspace_size(B, self.d, self.n_heads, self.n_kv, self.head_dim, self.t, L_max),
+                   device)
+
+
+def decode_attn_forward(x, w: DecodeAttnWeights, K_cache, V_cache, pos, scale=None, ws=None):
+    """One decode step: appends each sequence's new key/value at pos[b] in
+    every shard's cache copy and returns y [B][d] = sum_i O_i W_o,i + b_o."""
+    B = x.shape[0]
+    L_max = K_cache.shape[3]
+    assert K_cache.dtype == torch.float16 and V_cache.dtype == torch.float16 and pos.dtype == torch.int32
+    if scale is None:
+        scale = w.head_dim ** -0.5
+    if ws is None:
+        ws = w.workspace(B, L_max, x.device)
+    y = torch.empty(B, w.d, dtype=BF16, device=x.device)
+    L.tp_decode_attn_forward(x, B, w.d, w.n_heads, w.n_kv, w.head_dim, w.t, scale, w.Wqkv_p, w.bqkv_p, w.Wo_p,
+                             w.b_o, K_cache, V_cache, L_max, pos, y, ws, ws.numel())
+    return y

@@ -77,3 +77,20 @@ def test_host_validation_without_device():
     assert L.tp_pack_col(16, 64, 100, 3, 16, **c) == L.TP_ERR_SHAPE
     assert L.tp_pack_qkv_heads(16, 96, 4, 16, 2, 16, **c) == L.TP_ERR_SHAPE
     assert L.tp_selftest_bounded_wait(0, **c) == L.TP_ERR_INVALID_ARG
+
+
+def test_decode_attn_host_validation():
+    c = dict(check=False, stream=0)
+    ok_ws = L.tp_decode_attn_workspace_size(2, 1024, 8, 2, 128, 4, 256)
+    assert ok_ws > 0
+    assert L.tp_decode_attn_workspace_size(2, 1024, 8, 2, 64, 4, 256) == 0     # head_dim != 128
+    assert L.tp_decode_attn_workspace_size(2, 1024, 8, 3, 128, 4, 256) == 0    # 3 KV heads do not group 8 heads
+    args = lambda B, nh, nkv, hd, t, ws, nws: (16, B, nh * 128, nh, nkv, hd, t, 0.1, 16, None, 16, None, 16, 16,
+                                               256, 16, 16, ws, nws)
+    assert L.tp_decode_attn_forward(*args(2, 8, 2, 64, 4, 256, ok_ws), **c) == L.TP_ERR_SHAPE
+    assert L.tp_decode_attn_forward(*args(2, 8, 2, 128, 3, 256, ok_ws), **c) == L.TP_ERR_SHAPE   # t does not divide
+    assert L.tp_decode_attn_forward(*args(2, 12, 3, 128, 2, 256, ok_ws), **c) == L.TP_ERR_SHAPE  # 3 KV over 2 shards
+    assert L.tp_decode_attn_forward(*args(0, 8, 2, 128, 4, None, 0), **c) == L.TP_OK             # nothing to do
+    assert L.tp_decode_attn_forward(*args(2, 8, 2, 128, 4, 256 + 16, ok_ws), **c) == L.TP_ERR_ALIGN
+    assert L.tp_decode_attn_forward(*args(2, 8, 2, 128, 4, 256, ok_ws - 256), **c) == L.TP_ERR_WORKSPACE
+    assert L.tp_pack_qkv_gqa(16, 256, 8, 3, 128, 4, 16, **c) == L.TP_ERR_SHAPE
