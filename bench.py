@@ -390,8 +390,19 @@ def run_decode_attn_extra(L, torch, args):
     posd = pos.cuda()
     ws = w.workspace(B, L_max, "cuda")
     x = inp["x"]
-    step = lambda: T.decode_attn_forward(x, w, K, V, posd, ws=ws)
+    y = torch.empty(B, d, dtype=torch.bfloat16, device="cuda")
+    step = lambda: T.decode_attn_forward(x, w, K, V, posd, ws=ws, out=y)
     us = 1e3 * _time(torch, step, max(20, args.steps), warmup=5)
+    # the same step replayed from a CUDA graph (how a decode loop launches it)
+    graph = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cs):
+        step()
+        with torch.cuda.graph(graph, stream=cs):
+            step()
+    torch.cuda.current_stream().wait_stream(cs)
+    us_graph = 1e3 * _time(torch, graph.replay, max(20, args.steps), warmup=5)
     R = (nh // t + 2 * w.kv_t) * hd
     w_bytes = t * R * d * 2 + nh * hd * d * 2
     kv_bytes = sum(2 * t * w.kv_t * (int(p) + 1) * hd * 2 for p in pos.tolist())
@@ -401,8 +412,10 @@ def run_decode_attn_extra(L, torch, args):
     return {"workload": "decode attention, t=4, d=8192, 64 query / 8 KV heads x 128, B=8, cache lengths "
                         "4096..8192 (seeded uniform), fp16 KV cache",
             "us_per_step": round(us, 2), "GBps": round(gbs, 1), "bytes_per_step": nbytes,
+            "us_per_step_graph": round(us_graph, 2), "GBps_graph": round(nbytes / (us_graph / 1e6) / 1e9, 1),
             "weight_bytes": w_bytes, "kv_bytes": kv_bytes, "lengths": [int(p) + 1 for p in pos.tolist()],
             "frac_of_hbm": round(gbs / peaks["hbm"], 4), "hbm_peak_GBps": peaks["hbm"],
+            "frac_of_hbm_graph": round(nbytes / (us_graph / 1e6) / 1e9 / peaks["hbm"], 4),
             "l2": "~500 MB of weights and cache per step > L2; no flush",
             "allreduce_accounting": {"payload_bytes": B * d * 2, "allreduces_per_layer_per_token": 2,
                                      "allreduces_per_token_80_layers": 160,

@@ -130,6 +130,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
+  __syncwarp();  // lane-0 roles rejoin their warp: bar.sync needs converged warps
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
@@ -306,6 +307,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   }
 
   ptx::tc_fence_before();
+  __syncwarp();  // lane-0 roles rejoin their warp: bar.sync needs converged warps
   __syncthreads();
   if (warp == 1) {
     __syncwarp();
@@ -465,6 +467,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
+  __syncwarp();  // lane-0 roles rejoin their warp: bar.sync needs converged warps
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
@@ -571,6 +574,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   }
 
   ptx::tc_fence_before();
+  __syncwarp();  // lane-0 roles rejoin their warp: bar.sync needs converged warps
   __syncthreads();
   if (warp == 1) {
     __syncwarp();
@@ -630,6 +634,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
+  __syncwarp();  // lane-0 roles rejoin their warp: bar.sync needs converged warps
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
@@ -739,6 +744,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   }
 
   ptx::tc_fence_before();
+  __syncwarp();  // lane-0 roles rejoin their warp: bar.sync needs converged warps
   __syncthreads();
   if (warp == 1) {
     __syncwarp();

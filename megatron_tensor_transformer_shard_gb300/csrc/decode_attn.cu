@@ -62,6 +62,7 @@ constexpr int KV_TILE = 2 * PANEL;
 constexpr int DEC_THREADS = 224;
 constexpr int MAX_GRID = 256;     // attention CTAs per launch at most (sizes the partial slots)
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxPend = 32;      // finished pieces a CTA holds back before counting them
 
 enum : int {
   ERR_DEC_PRODUCER = 0x121,
@@ -80,7 +81,8 @@ struct DecCfg {
   static constexpr int OFF_P = OFF_Q + 2 * QBUF;
   static constexpr int OFF_BAR = OFF_P + 2 * PBUF;
   static constexpr int OFF_RED = OFF_BAR + 512;
-  static constexpr int SMEM = 1024 + OFF_RED + (2 * 4 * NG + 4 * NG + 4) * 4 + 64;
+  static constexpr int OFF_PRE = OFF_RED + (2 * 4 * NG + 4 * NG + 2 * kMaxPend) * 4;
+  static constexpr int SMEM = 1024 + OFF_PRE + 260 * 4 + 64;
   static constexpr uint32_t TMEM_COLS = 4 * NG < 32 ? 32 : 4 * NG;
 };
 
@@ -90,7 +92,6 @@ struct DecArgs {
   int64_t L_max;
   float scale_log2;
   const int32_t* pos;
-  const int* tile_start;  // [S + 1]
   float* o_part;          // [slots][NG][HD]
   float* m_part;          // [slots][NG]
   float* l_part;          // [slots][NG]
@@ -109,21 +110,26 @@ __device__ __forceinline__ int stream_len(const int32_t* pos, int b, int64_t L_m
 
 // Walks the CTA's contiguous range of the flattened tile list; the current
 // stream's first tile and the next stream's first tile stay in registers.
+// Stream s starts at tile (s / B) * TB + pre[s % B] (pre in shared memory).
 struct TileCursor {
-  const int* ts;
+  const int* pre;
+  int B, TB;
   int x, x1, s, ts_s, ts_n;
-  __device__ void init(const int* ts_, int S, int x0, int x1_) {
-    ts = ts_;
+  __device__ int start_of(int st) const { return (st / B) * TB + pre[st % B]; }
+  __device__ void init(const int* pre_, int B_, int S, int x0, int x1_) {
+    pre = pre_;
+    B = B_;
+    TB = pre[B];
     x = x0;
     x1 = x1_;
-    int lo = 0, hi = S - 1;  // largest s with ts[s] <= x0
+    int lo = 0, hi = S - 1;  // largest s with start_of(s) <= x0
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(ts + mid) <= x0) lo = mid; else hi = mid - 1;
+      if (start_of(mid) <= x0) lo = mid; else hi = mid - 1;
     }
     s = lo;
-    ts_s = __ldg(ts + s);
-    ts_n = __ldg(ts + s + 1);
+    ts_s = start_of(s);
+    ts_n = start_of(s + 1);
   }
   __device__ bool valid() const { return x < x1; }
   __device__ int local_tile() const { return x - ts_s; }
@@ -134,7 +140,7 @@ struct TileCursor {
     if (x < x1 && x >= ts_n) {
       ++s;
       ts_s = ts_n;
-      ts_n = __ldg(ts + s + 1);
+      ts_n = start_of(s + 1);
     }
   }
 };
@@ -179,6 +185,7 @@ __device__ __forceinline__ void tmem_ld_ng<32>(uint32_t taddr, float (&v)[32]) {
 // Barrier over the 128 softmax threads that also ORs a predicate across them
 // (a uniform decision to stop after a failed wait).
 __device__ __forceinline__ bool softmax_bar_or(bool pred) {
+  __syncwarp();  // the barrier needs converged warps
   uint32_t out;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
@@ -191,7 +198,10 @@ __device__ __forceinline__ bool softmax_bar_or(bool pred) {
   return out != 0;
 }
 
-__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void softmax_bar() {
+  __syncwarp();
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
 
 template <int NG, int GSZ>
 __global__ void __launch_bounds__(DEC_THREADS, 1)
@@ -219,13 +229,20 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   uint64_t* o_full = q_full + 10;     // [2]
   uint64_t* o_free = q_full + 12;     // [2]
   uint64_t* mma_done = q_full + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 15);
+  uint64_t* all_done = q_full + 15;   // teardown: every thread arrives before TMEM is freed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* red = reinterpret_cast<float*>(base + C::OFF_RED);  // [2][4][NG] tile maxima
   float* red2 = red + 2 * 4 * NG;                             // [4][NG] final sums
 
+  int* pre = reinterpret_cast<int*>(base + C::OFF_PRE);     // [B + 1] tile prefix of the sequences
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = __ldg(p.tile_start + p.S);
+  ptx::griddep_launch_dependents();
+  // The plan comes from pos (an input of the call, complete before the first
+  // kernel of the call started), so it may be read before griddepcontrol.wait.
+  decode_tile_prefix(p.pos, p.B, p.L_max, pre);
+  const int T = (p.S / p.B) * pre[p.B];
   const int G = gridDim.x;
   const int k = blockIdx.x;
   const int x0 = static_cast<int>((static_cast<int64_t>(k) * T) / G);
@@ -249,6 +266,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
       ptx::mbar_init(&o_free[b], 128);
     }
     ptx::mbar_init(mma_done, 1);
+    ptx::mbar_init(all_done, DEC_THREADS);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -257,18 +275,20 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
+  __syncwarp();  // lane-0 roles rejoin their warp: bar.sync needs converged warps
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   TileCursor cur;
-  cur.init(p.tile_start, p.S, x0, x1);
+  cur.init(pre, p.B, p.S, x0, x1);
 
   if (warp == 0) {
     // ------------------------------------------------- producer of Q and K
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tm_k);
       ptx::tma_prefetch_desc(&tm_q);
+      ptx::griddep_wait();  // Q and the newest cache entries come from the previous kernel
       int u = 0, seg = 0;
       bool ok = true;
       for (; ok && cur.valid(); cur.next()) {
@@ -314,6 +334,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     // while a K stage frees right after the S MMA, so K can run further ahead.
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tm_v);
+      ptx::griddep_wait();
       int u = 0;
       for (; cur.valid(); cur.next()) {
         const int st = u % ST;
@@ -415,14 +436,101 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
       m_fin[h] = -INFINITY;
       l_fin[h] = 0.0f;
     }
-    int u = 0, s_prev = 0, s_cur = -1, len = 1, prev_ts = 0, prev_tn = 1;
+    int u = 0, s_prev = 0, s_cur = -1, len = 1;
     bool last_prev = false, ok = true, stopped = false;
 
-    // Writes this CTA's partial for stream s; the CTA that completes the
-    // stream's last piece then merges all pieces in CTA order (deterministic)
-    // and writes O for the group's heads.
-    int* flag = reinterpret_cast<int*>(red2 + 4 * NG);
-    auto finalize = [&](int s, int s_ts, int s_tn, const float (&mf)[GSZ], const float (&lf)[GSZ]) {
+    // A finished piece's partial (O, reference max, sum) is written at once;
+    // counting it towards its stream (fence + atomic) is deferred to the end
+    // of the CTA's range, where all pending pieces share one round trip, and
+    // the CTA that completes a stream's last piece merges its pieces.
+    int* pend = reinterpret_cast<int*>(red2 + 4 * NG);  // [kMaxPend] streams with a written piece
+    int* pend_last = pend + kMaxPend;                     // [kMaxPend] 1: this CTA completed the stream
+    int npend = 0;                                        // uniform over the softmax threads
+    const uint32_t uT = static_cast<uint32_t>(T), uG = static_cast<uint32_t>(G);
+    auto owns = [&](uint32_t kk) { return (kk * uT) / uG != ((kk + 1) * uT) / uG; };
+    auto cta_of32 = [&](uint32_t x) { return ((x + 1) * uG - 1) / uT; };
+
+    auto combine = [&](int s) {
+      const uint32_t k0 = cta_of32(cur.start_of(s)), k1 = cta_of32(cur.start_of(s + 1) - 1);
+      const int b = s % p.B, c = s / p.B;
+      const int i = c / p.kv_t, jl = c - i * p.kv_t;
+      const int qh0 = i * p.q_t + jl * p.Gs;
+      constexpr int CH = GSZ < 8 ? GSZ : 8;  // heads merged per pass (register budget)
+#pragma unroll 1
+      for (int h0 = 0; h0 < Gs; h0 += CH) {
+        float M[CH], num[CH], den[CH], mv[CH], lv[CH], ov[CH];
+#pragma unroll
+        for (int h = 0; h < CH; ++h) {
+          M[h] = -INFINITY;
+          num[h] = 0.0f;
+          den[h] = 0.0f;
+        }
+        auto load = [&](uint32_t kk, float (&m)[CH], float (&l)[CH], float (&o)[CH]) {
+          const int64_t sl = static_cast<int64_t>(s) + kk;
+#pragma unroll
+          for (int h = 0; h < CH; ++h) {
+            m[h] = __ldcg(p.m_part + sl * NG + h0 + h);
+            l[h] = __ldcg(p.l_part + sl * NG + h0 + h);
+            o[h] = __ldcg(p.o_part + (sl * NG + h0 + h) * HD + r);
+          }
+        };
+        uint32_t kk = k0;
+        while (kk <= k1 && !owns(kk)) ++kk;
+        load(kk, mv, lv, ov);
+        while (kk <= k1) {
+          uint32_t kn = kk + 1;
+          while (kn <= k1 && !owns(kn)) ++kn;
+          float mn[CH], ln[CH], on[CH];
+          if (kn <= k1) load(kn, mn, ln, on);  // the next piece's loads fly while this one is folded in
+#pragma unroll
+          for (int h = 0; h < CH; ++h) {
+            const float Mn = fmaxf(M[h], mv[h]);
+            const float sc = ptx::exp2_approx(M[h] - Mn), wk = ptx::exp2_approx(mv[h] - Mn);
+            num[h] = fmaf(num[h], sc, wk * ov[h]);
+            den[h] = fmaf(den[h], sc, wk * lv[h]);
+            M[h] = Mn;
+          }
+          if (kn > k1) break;
+#pragma unroll
+          for (int h = 0; h < CH; ++h) {
+            mv[h] = mn[h];
+            lv[h] = ln[h];
+            ov[h] = on[h];
+          }
+          kk = kn;
+        }
+#pragma unroll
+        for (int h = 0; h < CH; ++h)
+          if (h0 + h < Gs)
+            p.O[(static_cast<int64_t>(b) * p.nh + qh0 + h0 + h) * HD + r] = float_to_bf16_bits(num[h] / den[h]);
+      }
+    };
+
+    auto flush_pending = [&]() {
+      __threadfence();
+      softmax_bar();
+      if (r < npend) {
+        const int s = pend[r];
+        const uint32_t k0 = cta_of32(cur.start_of(s)), k1 = cta_of32(cur.start_of(s + 1) - 1);
+        int npieces = 0;
+        for (uint32_t kk = k0; kk <= k1; ++kk) npieces += owns(kk) ? 1 : 0;
+        pend_last[r] = (atomicAdd(p.done + s, 1) == npieces - 1) ? 1 : 0;
+      }
+      softmax_bar();
+      bool fenced = false;
+      for (int q = 0; q < npend; ++q) {
+        if (pend_last[q]) {
+          if (!fenced) {
+            __threadfence();
+            fenced = true;
+          }
+          combine(pend[q]);
+        }
+      }
+      npend = 0;
+    };
+
+    auto write_piece = [&](int s, const float (&mf)[GSZ], const float (&lf)[GSZ]) {
 #pragma unroll
       for (int h = 0; h < GSZ; ++h) {
         float v = lf[h];
@@ -430,6 +538,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
         if (lane == 0) red2[quad * NG + h] = v;
       }
+      if (npend == kMaxPend) flush_pending();  // (its barriers also order red2)
       softmax_bar();
       const int64_t slot = static_cast<int64_t>(s) + k;
       if (r < Gs) {
@@ -446,57 +555,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
 #pragma unroll
       for (int h = 0; h < GSZ; ++h)
         if (h < Gs) p.o_part[(slot * NG + h) * HD + r] = o_acc[h];
-      // pieces of stream s: CTAs k0..k1 that own tiles
-      const int k0 = cta_of(s_ts, G, T), k1 = cta_of(s_tn - 1, G, T);
-      auto owns = [&](int kk) {
-        return (static_cast<int64_t>(kk) * T) / G != (static_cast<int64_t>(kk + 1) * T) / G;
-      };
-      int npieces = 0;
-      for (int kk = k0; kk <= k1; ++kk) npieces += owns(kk) ? 1 : 0;
-      __threadfence();
-      softmax_bar();
-      if (r == 0) *flag = (atomicAdd(p.done + s, 1) == npieces - 1) ? 1 : 0;
-      softmax_bar();
-      if (*flag) {
-        __threadfence();
-        const int b = s % p.B, c = s / p.B;
-        const int i = c / p.kv_t, jl = c - i * p.kv_t;
-        const int qh0 = i * p.q_t + jl * p.Gs;
-        // all heads at once: every piece costs one round of independent loads
-        float M[GSZ], num[GSZ], den[GSZ];
-#pragma unroll
-        for (int h = 0; h < GSZ; ++h) {
-          M[h] = -INFINITY;
-          num[h] = 0.0f;
-          den[h] = 0.0f;
-        }
-        for (int kk = k0; kk <= k1; ++kk) {
-          if (!owns(kk)) continue;
-          const float* mp = p.m_part + (static_cast<int64_t>(s) + kk) * NG;
-#pragma unroll
-          for (int h = 0; h < GSZ; ++h) M[h] = fmaxf(M[h], __ldcg(mp + h));
-        }
-        for (int kk = k0; kk <= k1; ++kk) {
-          if (!owns(kk)) continue;
-          const int64_t sl = static_cast<int64_t>(s) + kk;
-          float mv[GSZ], lv[GSZ], ov[GSZ];
-#pragma unroll
-          for (int h = 0; h < GSZ; ++h) {
-            mv[h] = __ldcg(p.m_part + sl * NG + h);
-            lv[h] = __ldcg(p.l_part + sl * NG + h);
-            ov[h] = __ldcg(p.o_part + (sl * NG + h) * HD + r);
-          }
-#pragma unroll
-          for (int h = 0; h < GSZ; ++h) {
-            const float wgt = ptx::exp2_approx(mv[h] - M[h]);
-            den[h] = fmaf(wgt, lv[h], den[h]);
-            num[h] = fmaf(wgt, ov[h], num[h]);
-          }
-        }
-#pragma unroll
-        for (int h = 0; h < GSZ; ++h)
-          if (h < Gs) p.O[(static_cast<int64_t>(b) * p.nh + qh0 + h) * HD + r] = float_to_bf16_bits(num[h] / den[h]);
-      }
+      if (r == 0) pend[npend] = s;
+      ++npend;
     };
 
     auto accumulate = [&](int w) -> bool {
@@ -603,24 +663,31 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
       ptx::mbar_arrive(&p_full[sb]);
       if (u >= 1) {
         ok = accumulate(u - 1) && ok;
-        if (last_prev) finalize(s_prev, prev_ts, prev_tn, m_fin, l_fin);
+        if (last_prev) write_piece(s_prev, m_fin, l_fin);
       }
 #pragma unroll
       for (int h = 0; h < GSZ; ++h) alpha_prev[h] = alpha[h];
       s_prev = s;
-      prev_ts = cur.ts_s;
-      prev_tn = cur.ts_n;
       last_prev = last;
       ++u;
     }
     if (!stopped && u >= 1) {
       ok = accumulate(u - 1) && ok;
-      finalize(s_prev, prev_ts, prev_tn, m_ref, l_run);
+      write_piece(s_prev, m_ref, l_run);
+      flush_pending();
     }
   }
 
+  // Teardown through an mbarrier rather than bar.sync 0: after the softmax
+  // group's named-barrier traffic a CTA-wide bar.sync was measured to release
+  // before all warps had arrived, which would free TMEM under a reader.
   ptx::tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  {
+    ptx::mbar_arrive(all_done);
+    volatile int never = 0;
+    ptx::mbar_wait(all_done, 0, &never, p.err, ERR_DEC_DRAIN, p.timeout_ns);
+  }
   if (warp == 1) {
     __syncwarp();
     ptx::tc_fence_after();
@@ -633,8 +700,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
 // iteration (row r of shard i is one output unit: a Q, K or V coordinate of one
 // of its heads), weights streamed once with 16-byte loads; the result goes to
 // the fp16 Q buffer or straight into the shard's cache copy at pos[b].
-// Block 0 of the first launch also writes the tile plan: tile_start[s] = the
-// first flattened tile of stream s = (i*kv_t + jl)*B + b.
+// Block 0 of the first launch also validates the positions and zeroes the
+// per-stream piece counters of the attention kernel.
 constexpr int GEMV_T = 128;
 
 __device__ __forceinline__ uint4 ld_stream(const uint16_t* ptr) {
@@ -664,8 +731,7 @@ struct QkvArgs {
   uint16_t* q;   // [B][nh][HD] fp16
   uint16_t* Kc;  // [t][kv_t][B][L_max][HD] fp16
   uint16_t* Vc;
-  int* tile_start;  // written by block 0 when non-null
-  int* done;        // zeroed with the plan
+  int* done;  // block 0 of the first launch validates pos and zeroes these counters
   int* err;
 };
 
@@ -673,9 +739,7 @@ template <int M>
 __global__ void __launch_bounds__(GEMV_T) decode_qkv_kernel(const QkvArgs a) {
   __shared__ float red[GEMV_T / 32][M];
   __shared__ float tot[M];
-  __shared__ int plan_scratch[260];
-  if (a.tile_start && blockIdx.x == 0)
-    decode_tile_plan(a.pos, a.B, a.L_max, a.t * a.kv_t, a.tile_start, a.done, a.err, plan_scratch);
+  if (a.done && blockIdx.x == 0) decode_plan_prepare(a.pos, a.B, a.L_max, a.t * a.kv_t * a.B, a.done, a.err);
   const int64_t chunks = a.d / 8;
   const int64_t R = a.R_t * a.t;
   const int64_t qw = static_cast<int64_t>(a.q_t) * HD, kvw = static_cast<int64_t>(a.kv_t) * HD;
@@ -780,8 +844,9 @@ tp_status launch_attn(const CUtensorMap& mk, const CUtensorMap& mv, const CUtens
                                        DecCfg<NG>::SMEM));
     configured[dev] = true;
   }
-  decode_attn_kernel<NG, GSZ><<<grid, DEC_THREADS, DecCfg<NG>::SMEM, s>>>(mk, mv, mq, a);
-  TP_LAUNCHED();
+  TP_CUDA_CHECK(launch_pdl(decode_attn_kernel<NG, GSZ>, dim3(grid), dim3(DEC_THREADS), DecCfg<NG>::SMEM, s, mk, mv,
+                           mq, a));
+  count_launch();
   return TP_OK;
 }
 
@@ -811,7 +876,6 @@ inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct DecWs {
   uint16_t* q;
-  int* tile_start;
   int* done;
   float *o_part, *m_part, *l_part;
   uint16_t* O;
@@ -825,7 +889,6 @@ DecWs decode_ws_layout(void* ws, int64_t B, int64_t d, int n_heads, int t, const
   size_t off = 0;
   const size_t slots = static_cast<size_t>(sh.S) + MAX_GRID;
   w.q = reinterpret_cast<uint16_t*>(p + off); off += up256(static_cast<size_t>(B) * n_heads * HD * 2);
-  w.tile_start = reinterpret_cast<int*>(p + off); off += up256((static_cast<size_t>(sh.S) + 1) * 4);
   w.done = reinterpret_cast<int*>(p + off); off += up256(static_cast<size_t>(sh.S) * 4);
   w.o_part = reinterpret_cast<float*>(p + off); off += up256(slots * sh.NG * HD * 4);
   w.m_part = reinterpret_cast<float*>(p + off); off += up256(slots * sh.NG * 4);
@@ -879,7 +942,7 @@ tp_status run_decode_attn(const uint16_t* x, int64_t B, int64_t d, int n_heads, 
     j.x = x; j.ldx = d; j.B = static_cast<int>(B); j.part = w.sk_part;
     j.epi = SK_EPI_QKV; j.bias = bqkv_p;
     j.R_t = sh.R_t; j.L_max = L_max; j.q_t = sh.q_t; j.kv_t = sh.kv_t; j.nh = n_heads;
-    j.pos = pos; j.q = w.q; j.Kc = Kc; j.Vc = Vc; j.tile_start = w.tile_start; j.done = w.done;
+    j.pos = pos; j.q = w.q; j.Kc = Kc; j.Vc = Vc; j.done = w.done;
     j.err = device_error_word();
     TP_RETURN_IF(run_skinny_gemm(j, s));
   } else {
@@ -889,8 +952,7 @@ tp_status run_decode_attn(const uint16_t* x, int64_t B, int64_t d, int n_heads, 
     qa.pos = pos; qa.q = w.q; qa.Kc = Kc; qa.Vc = Vc; qa.err = device_error_word();
     for (int64_t m0 = 0; m0 < B; m0 += 8) {
       qa.m0 = static_cast<int>(m0);
-      qa.tile_start = m0 == 0 ? w.tile_start : nullptr;
-      qa.done = w.done;
+      qa.done = m0 == 0 ? w.done : nullptr;
       TP_RETURN_IF(qkv_dispatch(static_cast<int>(B - m0 < 8 ? B - m0 : 8), qa, s));
     }
   }
@@ -905,7 +967,7 @@ tp_status run_decode_attn(const uint16_t* x, int64_t B, int64_t d, int n_heads, 
     return TP_FAIL_DETAIL("cuTensorMapEncodeTiled failed for the KV cache or Q");
   DecArgs a{};
   a.S = sh.S; a.B = static_cast<int>(B); a.nh = n_heads; a.q_t = sh.q_t; a.kv_t = sh.kv_t; a.Gs = sh.Gs;
-  a.L_max = L_max; a.scale_log2 = scale * kLog2e; a.pos = pos; a.tile_start = w.tile_start;
+  a.L_max = L_max; a.scale_log2 = scale * kLog2e; a.pos = pos;
   a.o_part = w.o_part; a.m_part = w.m_part; a.l_part = w.l_part; a.done = w.done; a.O = w.O;
   a.err = device_error_word(); a.timeout_ns = wait_timeout_ns();
   int64_t grid = device_sm_count();

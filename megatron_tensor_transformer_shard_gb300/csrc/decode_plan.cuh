@@ -1,10 +1,8 @@
 // Tile plan of decode attention over a sharded KV cache: stream
 // s = (i * kv_t + jl) * B + b (shard i, its local KV head jl, sequence b) owns
-// ceil(len_b / 128) tiles of 128 keys, len_b = pos[b] + 1, and
-// tile_start[s] is its first tile in the flattened list of all streams'
-// tiles (tile_start[S] = the total).  Written by one CTA of a kernel that runs
-// before the attention kernel; a position outside [0, L_max) is clamped and
-// recorded as a device-side argument error.
+// ceil(len_b / 128) tiles of 128 keys, len_b = pos[b] + 1; its first tile in
+// the flattened list of all streams' tiles is (s / B) * TB + pre[b], with
+// pre the exclusive prefix of the sequences' tile counts and TB their total.
 #pragma once
 
 #include <cstdint>
@@ -14,38 +12,39 @@ namespace tp {
 constexpr int kDecodeTileKeys = 128;
 constexpr int kDecodeErrPos = 0x201;
 
-// Called by every thread of one CTA (blockDim.x threads); `scratch` holds at
-// least B + 1 ints of shared memory.
-// `done` (S ints, nullable) is zeroed: per-stream counts of finished pieces.
-__device__ __forceinline__ void decode_tile_plan(const int32_t* pos, int B, int64_t L_max, int groups,
-                                                 int* tile_start, int* done, int* err, int* scratch) {
+// Called by every thread of one CTA: validates the positions (a position
+// outside [0, L_max) is recorded as a device-side argument error; the kernels
+// clamp it) and zeroes the per-stream piece counters done[0..S).
+__device__ __forceinline__ void decode_plan_prepare(const int32_t* pos, int B, int64_t L_max, int S, int* done,
+                                                    int* err) {
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
     const int64_t p = pos[b];
-    int64_t len = p + 1;
-    if (p < 0 || p >= L_max) {
-      atomicCAS(err, 0, kDecodeErrPos);
-      len = p < 0 ? 1 : L_max;
-    }
-    scratch[b] = static_cast<int>((len + kDecodeTileKeys - 1) / kDecodeTileKeys);
+    if (p < 0 || p >= L_max) atomicCAS(err, 0, kDecodeErrPos);
+  }
+  for (int s = threadIdx.x; s < S; s += blockDim.x) done[s] = 0;
+}
+
+// Exclusive prefix of the sequences' tile counts into shared memory:
+// pre[b] = sum_{b' < b} ceil(len_b' / 128), pre[B] = the total.  Called by
+// every thread of the CTA (contains __syncthreads).
+__device__ __forceinline__ void decode_tile_prefix(const int32_t* pos, int B, int64_t L_max, int* pre) {
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    int64_t p = pos[b];
+    if (p < 0) p = 0;
+    if (p >= L_max) p = L_max - 1;
+    pre[b] = static_cast<int>((p + 1 + kDecodeTileKeys - 1) / kDecodeTileKeys);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {  // exclusive prefix over the sequences, in place
+  if (threadIdx.x == 0) {
     int run = 0;
     for (int b = 0; b < B; ++b) {
-      const int n = scratch[b];
-      scratch[b] = run;
+      const int n = pre[b];
+      pre[b] = run;
       run += n;
     }
-    scratch[B] = run;
+    pre[B] = run;
   }
   __syncthreads();
-  const int per_group = scratch[B];
-  const int S = groups * B;
-  for (int s = threadIdx.x; s <= S; s += blockDim.x) {
-    const int c = s / B, b = s - c * B;
-    tile_start[s] = c * per_group + scratch[b];
-    if (done && s < S) done[s] = 0;
-  }
 }
 
 }  // namespace tp

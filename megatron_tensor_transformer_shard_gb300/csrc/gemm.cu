@@ -350,6 +350,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
+  __syncwarp();  // lane-0 roles rejoin their warp: bar.sync needs converged warps
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
@@ -484,6 +485,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 
   ptx::tc_fence_before();
+  __syncwarp();  // lane-0 roles rejoin their warp: bar.sync needs converged warps
   __syncthreads();
   if (warp == 1) {
     __syncwarp();
@@ -569,6 +571,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     ptx::tmem_relinquish_pair();
   }
   ptx::tc_fence_before();
+  __syncwarp();  // lane-0 roles rejoin their warp before the cluster barrier
   ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;

@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <utility>
 
 #include "tp.h"
 
@@ -46,6 +47,25 @@ tp_status cuda_failure(const char* file, int line, cudaError_t e);
   } while (0)
 
 #define TP_FAIL_DETAIL(what) (::tp::set_error_detail(__FILE__, __LINE__, what), TP_ERR_CUDA)
+
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel on the stream drains; it must execute
+// griddepcontrol.wait before touching anything that kernel writes.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ----------------------------------------------------------------- GEMM
 // One launch computes, for every output batch b in [0, nbatch):
@@ -152,8 +172,7 @@ struct SkGemmJob {
   uint16_t* q = nullptr;
   uint16_t* Kc = nullptr;
   uint16_t* Vc = nullptr;
-  int* tile_start = nullptr;  // SK_EPI_QKV: if non-null, the reduce kernel also writes the tile plan
-  int* done = nullptr;        //   ... and zeroes these per-stream counters
+  int* done = nullptr;  // SK_EPI_QKV: if non-null, the reduce kernel validates pos and zeroes these counters
   int* err = nullptr;
 };
 size_t skinny_part_floats(int64_t R, int B);

@@ -343,3 +343,22 @@ __device__ __forceinline__ void bulk_wait_group() {
 
 }  // namespace ptx
 }  // namespace tp
+
+namespace tp {
+namespace ptx {
+
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their memory is visible (a no-op without the launch
+// attribute).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the next kernel on the stream (launched with programmatic stream
+// serialization) be scheduled once every CTA of this grid has issued this;
+// its CTAs take SMs as ours leave and must griddep_wait() before reading our
+// results.  Issued early by every CTA, after it is resident.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+}  // namespace ptx
+}  // namespace tp

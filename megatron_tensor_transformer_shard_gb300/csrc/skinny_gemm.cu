@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  ptx::griddep_launch_dependents();
   const int64_t U = static_cast<int64_t>(p.nrb) * p.nku;
   const int G = gridDim.x, k = blockIdx.x;
   const int u0 = static_cast<int>((static_cast<int64_t>(k) * U) / G);
@@ -132,6 +133,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
+  __syncwarp();  // lane-0 roles rejoin their warp: bar.sync needs converged warps
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
@@ -140,8 +142,27 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tm_w);
       ptx::tma_prefetch_desc(&tm_x);
-      int n = 0;
-      for (int u = u0; u < u1; ++u, ++n) {
+      // The weight tiles of the first ST units do not depend on the previous
+      // kernels: stream them while those finish, then wait and add x.
+      const int npre = (u1 - u0) < ST ? (u1 - u0) : ST;
+      for (int n = 0; n < npre; ++n) {
+        const int u = u0 + n;
+        const int rb = u / p.nku, ku = u - rb * p.nku;
+        const int slab = ku / p.ku_per_slab, kin = (ku - slab * p.ku_per_slab) * 128;
+        uint8_t* sw = base + n * C::STAGE;
+        ptx::mbar_arrive_expect_tx(&full[n], C::STAGE);
+        ptx::tma_load_3d(sw, &tm_w, &full[n], kin, rb * 128, slab);
+        ptx::tma_load_3d(sw + SK_PANEL, &tm_w, &full[n], kin + 64, rb * 128, slab);
+      }
+      ptx::griddep_wait();  // x (and the partial slots) belong to the previous kernels
+      for (int n = 0; n < npre; ++n) {
+        const int ku = (u0 + n) % p.nku;
+        uint8_t* sx = base + n * C::STAGE + SK_WTILE;
+        ptx::tma_load_3d(sx, &tm_x, &full[n], ku * 128, 0, 0);
+        ptx::tma_load_3d(sx + NB * 128, &tm_x, &full[n], ku * 128 + 64, 0, 0);
+      }
+      int n = npre;
+      for (int u = u0 + npre; u < u1; ++u, ++n) {
         const int st = n % ST;
         if (!ptx::mbar_wait(&empty[st], ((n / ST) & 1) ^ 1u, abort_flag, p.err, ERR_SK_PRODUCER, p.timeout_ns)) break;
         const int rb = u / p.nku, ku = u - rb * p.nku;
@@ -221,6 +242,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   }
 
   ptx::tc_fence_before();
+  __syncwarp();  // lane-0 roles rejoin their warp: bar.sync needs converged warps
   __syncthreads();
   if (warp == 1) {
     __syncwarp();
@@ -250,10 +272,10 @@ __device__ __forceinline__ float sk_sum(const SkGemmJob& j, uint32_t G, uint32_t
 
 template <int NB>
 __global__ void __launch_bounds__(256) skinny_reduce_kernel(const SkGemmJob j, int G) {
-  __shared__ int plan_scratch[260];
-  if (j.tile_start && blockIdx.x == 0)
-    decode_tile_plan(j.pos, j.B, j.L_max, static_cast<int>(j.R / j.R_t) * j.kv_t, j.tile_start, j.done, j.err,
-                     plan_scratch);
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
+  if (j.done && blockIdx.x == 0)
+    decode_plan_prepare(j.pos, j.B, j.L_max, static_cast<int>(j.R / j.R_t) * j.kv_t * j.B, j.done, j.err);
   const int64_t n = static_cast<int64_t>(j.R) * j.B;
   for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -313,14 +335,16 @@ tp_status launch_skinny(const SkGemmJob& j, cudaStream_t s) {
   int64_t G = device_sm_count();
   if (G > SK_MAX_GRID) G = SK_MAX_GRID;
   if (G > U) G = U;
-  skinny_gemm_kernel<NB><<<static_cast<unsigned>(G), SK_THREADS, SkCfg<NB>::SMEM, s>>>(mw, mx, a);
-  TP_LAUNCHED();
+  TP_CUDA_CHECK(launch_pdl(skinny_gemm_kernel<NB>, dim3(static_cast<unsigned>(G)), dim3(SK_THREADS),
+                           SkCfg<NB>::SMEM, s, mw, mx, a));
+  count_launch();
   const int64_t n = static_cast<int64_t>(j.R) * j.B;
   int64_t rg = (n + 255) / 256;
   const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
   if (rg > cap) rg = cap;
-  skinny_reduce_kernel<NB><<<static_cast<unsigned>(rg), 256, 0, s>>>(j, static_cast<int>(G));
-  TP_LAUNCHED();
+  TP_CUDA_CHECK(launch_pdl(skinny_reduce_kernel<NB>, dim3(static_cast<unsigned>(rg)), dim3(256), 0, s, j,
+                           static_cast<int>(G)));
+  count_launch();
   return TP_OK;
 }
 

@@ -220,9 +220,11 @@ class DecodeAttnWeights:
                    device)
 
 
-def decode_attn_forward(x, w: DecodeAttnWeights, K_cache, V_cache, pos, scale=None, ws=None):
+def decode_attn_forward(x, w: DecodeAttnWeights, K_cache, V_cache, pos, scale=None, ws=None, out=None):
     """One decode step: appends each sequence's new key/value at pos[b] in
-    every shard's cache copy and returns y [B][d] = sum_i O_i W_o,i + b_o."""
+    every shard's cache copy and returns y [B][d] = sum_i O_i W_o,i + b_o.
+    Allocates nothing when ws and out are given (so it can be captured in a
+    CUDA graph)."""
     B = x.shape[0]
     L_max = K_cache.shape[3]
     assert K_cache.dtype == torch.float16 and V_cache.dtype == torch.float16 and pos.dtype == torch.int32
@@ -230,7 +232,7 @@ def decode_attn_forward(x, w: DecodeAttnWeights, K_cache, V_cache, pos, scale=No
         scale = w.head_dim ** -0.5
     if ws is None:
         ws = w.workspace(B, L_max, x.device)
-    y = torch.empty(B, w.d, dtype=BF16, device=x.device)
+    y = out if out is not None else torch.empty(B, w.d, dtype=BF16, device=x.device)
     L.tp_decode_attn_forward(x, B, w.d, w.n_heads, w.n_kv, w.head_dim, w.t, scale, w.Wqkv_p, w.bqkv_p, w.Wo_p,
                              w.b_o, K_cache, V_cache, L_max, pos, y, ws, ws.numel())
     return y

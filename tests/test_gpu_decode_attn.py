@@ -134,6 +134,35 @@ def test_decode_steps_match_causal_prefill(nh, nkv, t):
     assert_close("decode rows", np.concatenate([f64(y) for y in ys]), full)
 
 
+def test_decode_attn_graph_replay_matches_eager():
+    """The step launches through programmatic dependent launches; captured in a
+    CUDA graph and replayed it gives the same bits as the eager call."""
+    nh, nkv, t, B, L_max = 8, 2, 2, 4, 640
+    d = nh * HD
+    inp = I.decode_attn_inputs(B, d, nh, nkv, HD, L_max, seed=21)
+    w = T.DecodeAttnWeights(inp["W_qkv"].cuda(), inp["b_qkv"].cuda(), inp["W_o"].cuda(), inp["b_o"].cuda(),
+                            nh, nkv, HD, t)
+    Kd, Vd = _shard_cache(inp["K"], nh, nkv, t), _shard_cache(inp["V"], nh, nkv, t)
+    posd = torch.tensor([5, 200, 639, 333], dtype=torch.int32).cuda()
+    x = inp["x"].cuda()
+    ws = w.workspace(B, L_max, "cuda")
+    y_eager = T.decode_attn_forward(x, w, Kd, Vd, posd, ws=ws).clone()
+    y = torch.empty_like(y_eager)
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(g, stream=cs):
+            T.decode_attn_forward(x, w, Kd, Vd, posd, ws=ws, out=y)
+    torch.cuda.current_stream().wait_stream(cs)
+    for _ in range(3):
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), y_eager.view(torch.int16))
+    assert L.tp_get_device_status(check=False) == L.TP_OK
+
+
 def test_decode_attn_position_out_of_range_is_reported():
     nh, nkv, t, B, L_max = 8, 2, 2, 2, 256
     d = nh * HD
