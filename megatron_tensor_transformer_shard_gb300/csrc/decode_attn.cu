@@ -62,7 +62,6 @@ constexpr int KV_TILE = 2 * PANEL;
 constexpr int DEC_THREADS = 224;
 constexpr int MAX_GRID = 256;     // attention CTAs per launch at most (sizes the partial slots)
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kMaxPend = 32;      // finished pieces a CTA holds back before counting them
 
 enum : int {
   ERR_DEC_PRODUCER = 0x121,
@@ -81,7 +80,7 @@ struct DecCfg {
   static constexpr int OFF_P = OFF_Q + 2 * QBUF;
   static constexpr int OFF_BAR = OFF_P + 2 * PBUF;
   static constexpr int OFF_RED = OFF_BAR + 512;
-  static constexpr int OFF_PRE = OFF_RED + (2 * 4 * NG + 4 * NG + 2 * kMaxPend) * 4;
+  static constexpr int OFF_PRE = OFF_RED + (2 * 4 * NG + 4 * NG) * 4;
   static constexpr int SMEM = 1024 + OFF_PRE + 260 * 4 + 64;
   static constexpr uint32_t TMEM_COLS = 4 * NG < 32 ? 32 : 4 * NG;
 };
@@ -95,8 +94,9 @@ struct DecArgs {
   float* o_part;          // [slots][NG][HD]
   float* m_part;          // [slots][NG]
   float* l_part;          // [slots][NG]
-  int* done;              // [S] finished pieces per stream (zeroed by the plan)
-  uint16_t* O;            // [B][nh][HD] bf16, written by the CTA that finishes a stream last
+  uint16_t* O;            // [B][nh][HD] bf16, written by the combine kernel
+  int* zero_cnt;          // the combine kernel zeroes these counters (the W_o GEMM's row blocks)
+  int n_zero;
   int* err;
   uint64_t timeout_ns;
 };
@@ -439,97 +439,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     int u = 0, s_prev = 0, s_cur = -1, len = 1;
     bool last_prev = false, ok = true, stopped = false;
 
-    // A finished piece's partial (O, reference max, sum) is written at once;
-    // counting it towards its stream (fence + atomic) is deferred to the end
-    // of the CTA's range, where all pending pieces share one round trip, and
-    // the CTA that completes a stream's last piece merges its pieces.
-    int* pend = reinterpret_cast<int*>(red2 + 4 * NG);  // [kMaxPend] streams with a written piece
-    int* pend_last = pend + kMaxPend;                     // [kMaxPend] 1: this CTA completed the stream
-    int npend = 0;                                        // uniform over the softmax threads
-    const uint32_t uT = static_cast<uint32_t>(T), uG = static_cast<uint32_t>(G);
-    auto owns = [&](uint32_t kk) { return (kk * uT) / uG != ((kk + 1) * uT) / uG; };
-    auto cta_of32 = [&](uint32_t x) { return ((x + 1) * uG - 1) / uT; };
-
-    auto combine = [&](int s) {
-      const uint32_t k0 = cta_of32(cur.start_of(s)), k1 = cta_of32(cur.start_of(s + 1) - 1);
-      const int b = s % p.B, c = s / p.B;
-      const int i = c / p.kv_t, jl = c - i * p.kv_t;
-      const int qh0 = i * p.q_t + jl * p.Gs;
-      constexpr int CH = GSZ < 8 ? GSZ : 8;  // heads merged per pass (register budget)
-#pragma unroll 1
-      for (int h0 = 0; h0 < Gs; h0 += CH) {
-        float M[CH], num[CH], den[CH], mv[CH], lv[CH], ov[CH];
-#pragma unroll
-        for (int h = 0; h < CH; ++h) {
-          M[h] = -INFINITY;
-          num[h] = 0.0f;
-          den[h] = 0.0f;
-        }
-        auto load = [&](uint32_t kk, float (&m)[CH], float (&l)[CH], float (&o)[CH]) {
-          const int64_t sl = static_cast<int64_t>(s) + kk;
-#pragma unroll
-          for (int h = 0; h < CH; ++h) {
-            m[h] = __ldcg(p.m_part + sl * NG + h0 + h);
-            l[h] = __ldcg(p.l_part + sl * NG + h0 + h);
-            o[h] = __ldcg(p.o_part + (sl * NG + h0 + h) * HD + r);
-          }
-        };
-        uint32_t kk = k0;
-        while (kk <= k1 && !owns(kk)) ++kk;
-        load(kk, mv, lv, ov);
-        while (kk <= k1) {
-          uint32_t kn = kk + 1;
-          while (kn <= k1 && !owns(kn)) ++kn;
-          float mn[CH], ln[CH], on[CH];
-          if (kn <= k1) load(kn, mn, ln, on);  // the next piece's loads fly while this one is folded in
-#pragma unroll
-          for (int h = 0; h < CH; ++h) {
-            const float Mn = fmaxf(M[h], mv[h]);
-            const float sc = ptx::exp2_approx(M[h] - Mn), wk = ptx::exp2_approx(mv[h] - Mn);
-            num[h] = fmaf(num[h], sc, wk * ov[h]);
-            den[h] = fmaf(den[h], sc, wk * lv[h]);
-            M[h] = Mn;
-          }
-          if (kn > k1) break;
-#pragma unroll
-          for (int h = 0; h < CH; ++h) {
-            mv[h] = mn[h];
-            lv[h] = ln[h];
-            ov[h] = on[h];
-          }
-          kk = kn;
-        }
-#pragma unroll
-        for (int h = 0; h < CH; ++h)
-          if (h0 + h < Gs)
-            p.O[(static_cast<int64_t>(b) * p.nh + qh0 + h0 + h) * HD + r] = float_to_bf16_bits(num[h] / den[h]);
-      }
-    };
-
-    auto flush_pending = [&]() {
-      __threadfence();
-      softmax_bar();
-      if (r < npend) {
-        const int s = pend[r];
-        const uint32_t k0 = cta_of32(cur.start_of(s)), k1 = cta_of32(cur.start_of(s + 1) - 1);
-        int npieces = 0;
-        for (uint32_t kk = k0; kk <= k1; ++kk) npieces += owns(kk) ? 1 : 0;
-        pend_last[r] = (atomicAdd(p.done + s, 1) == npieces - 1) ? 1 : 0;
-      }
-      softmax_bar();
-      bool fenced = false;
-      for (int q = 0; q < npend; ++q) {
-        if (pend_last[q]) {
-          if (!fenced) {
-            __threadfence();
-            fenced = true;
-          }
-          combine(pend[q]);
-        }
-      }
-      npend = 0;
-    };
-
+    // A finished piece's partial (unnormalised O, reference max, sum) goes to
+    // its slot; the combine kernel merges each stream's pieces afterwards.
     auto write_piece = [&](int s, const float (&mf)[GSZ], const float (&lf)[GSZ]) {
 #pragma unroll
       for (int h = 0; h < GSZ; ++h) {
@@ -538,7 +449,6 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
         if (lane == 0) red2[quad * NG + h] = v;
       }
-      if (npend == kMaxPend) flush_pending();  // (its barriers also order red2)
       softmax_bar();
       const int64_t slot = static_cast<int64_t>(s) + k;
       if (r < Gs) {
@@ -555,8 +465,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
 #pragma unroll
       for (int h = 0; h < GSZ; ++h)
         if (h < Gs) p.o_part[(slot * NG + h) * HD + r] = o_acc[h];
-      if (r == 0) pend[npend] = s;
-      ++npend;
+      softmax_bar();  // red2 is reused by the next piece
     };
 
     auto accumulate = [&](int w) -> bool {
@@ -674,7 +583,6 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     if (!stopped && u >= 1) {
       ok = accumulate(u - 1) && ok;
       write_piece(s_prev, m_ref, l_run);
-      flush_pending();
     }
   }
 
@@ -695,13 +603,81 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   }
 }
 
+// ------------------------------------------------------------ combine
+// One warp per (sequence, query head): merge the pieces of the head's stream,
+// o = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k (M = max_k m_k), in CTA
+// order, and write O [B][n_heads][HD] bf16 -- the W_o projection's input.
+// Each lane owns 4 of the 128 dimensions; the loads of up to 4 pieces are in
+// flight together.
+constexpr int CMB_WARPS = 4;
+
+template <int NG>
+__global__ void __launch_bounds__(CMB_WARPS * 32) decode_combine_kernel(const DecArgs p, int G) {
+  __shared__ int pre[260];
+  ptx::griddep_launch_dependents();
+  decode_tile_prefix(p.pos, p.B, p.L_max, pre);  // from pos: no dependency on the previous kernel
+  if (blockIdx.x == 0)
+    for (int z = threadIdx.x; z < p.n_zero; z += blockDim.x) p.zero_cnt[z] = 0;  // the next kernel's counters
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pair = blockIdx.x * CMB_WARPS + warp;
+  if (pair >= p.B * p.nh) return;
+  const int qh = pair % p.nh, b = pair / p.nh;
+  const int i = qh / p.q_t, w = qh - i * p.q_t;
+  const int jl = w / p.Gs, g = w - jl * p.Gs;
+  const int s = (i * p.kv_t + jl) * p.B + b;
+  const int TB = pre[p.B];
+  const uint32_t T = static_cast<uint32_t>((p.S / p.B) * TB), uG = static_cast<uint32_t>(G);
+  const uint32_t ts = static_cast<uint32_t>((s / p.B) * TB + pre[s % p.B]);
+  const uint32_t te = static_cast<uint32_t>(((s + 1) / p.B) * TB + pre[(s + 1) % p.B]);
+  auto cta_of32 = [&](uint32_t x) { return ((x + 1) * uG - 1) / T; };
+  auto owns = [&](uint32_t kk) { return (kk * T) / uG != ((kk + 1) * T) / uG; };
+  const uint32_t k0 = cta_of32(ts), k1 = cta_of32(te - 1);
+  ptx::griddep_wait();  // the partials come from the attention kernel
+  float M = -INFINITY, num[4] = {0.f, 0.f, 0.f, 0.f}, den = 0.0f;
+  uint32_t kk = k0;
+  while (kk <= k1) {
+    uint32_t ks[4];
+    int n = 0;
+    for (; kk <= k1 && n < 4; ++kk)
+      if (owns(kk)) ks[n++] = kk;
+    float mv[4], lv[4];
+    float4 ov[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (q < n) {
+        const int64_t sl = static_cast<int64_t>(s) + ks[q];
+        mv[q] = __ldcg(p.m_part + sl * NG + g);
+        lv[q] = __ldcg(p.l_part + sl * NG + g);
+        ov[q] = __ldcg(reinterpret_cast<const float4*>(p.o_part + (sl * NG + g) * HD) + lane);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (q < n) {
+        const float Mn = fmaxf(M, mv[q]);
+        const float sc = ptx::exp2_approx(M - Mn), wk = ptx::exp2_approx(mv[q] - Mn);
+        num[0] = fmaf(num[0], sc, wk * ov[q].x);
+        num[1] = fmaf(num[1], sc, wk * ov[q].y);
+        num[2] = fmaf(num[2], sc, wk * ov[q].z);
+        num[3] = fmaf(num[3], sc, wk * ov[q].w);
+        den = fmaf(den, sc, wk * lv[q]);
+        M = Mn;
+      }
+    }
+  }
+  const float inv = 1.0f / den;
+  uint2 out;
+  out.x = pack_bf16x2(num[0] * inv, num[1] * inv);
+  out.y = pack_bf16x2(num[2] * inv, num[3] * inv);
+  *reinterpret_cast<uint2*>(p.O + (static_cast<int64_t>(b) * p.nh + qh) * HD + lane * 4) = out;
+}
+
 // ------------------------------------------------ QKV GEMV + cache append
 // Column-parallel projection of the new tokens, one packed row per CTA
 // iteration (row r of shard i is one output unit: a Q, K or V coordinate of one
 // of its heads), weights streamed once with 16-byte loads; the result goes to
 // the fp16 Q buffer or straight into the shard's cache copy at pos[b].
-// Block 0 of the first launch also validates the positions and zeroes the
-// per-stream piece counters of the attention kernel.
+// Block 0 of the first launch also checks the positions.
 constexpr int GEMV_T = 128;
 
 __device__ __forceinline__ uint4 ld_stream(const uint16_t* ptr) {
@@ -731,7 +707,7 @@ struct QkvArgs {
   uint16_t* q;   // [B][nh][HD] fp16
   uint16_t* Kc;  // [t][kv_t][B][L_max][HD] fp16
   uint16_t* Vc;
-  int* done;  // block 0 of the first launch validates pos and zeroes these counters
+  int check_pos;  // block 0 records positions outside [0, L_max)
   int* err;
 };
 
@@ -739,7 +715,7 @@ template <int M>
 __global__ void __launch_bounds__(GEMV_T) decode_qkv_kernel(const QkvArgs a) {
   __shared__ float red[GEMV_T / 32][M];
   __shared__ float tot[M];
-  if (a.done && blockIdx.x == 0) decode_plan_prepare(a.pos, a.B, a.L_max, a.t * a.kv_t * a.B, a.done, a.err);
+  if (a.check_pos && blockIdx.x == 0) decode_check_positions(a.pos, a.B, a.L_max, a.err);
   const int64_t chunks = a.d / 8;
   const int64_t R = a.R_t * a.t;
   const int64_t qw = static_cast<int64_t>(a.q_t) * HD, kvw = static_cast<int64_t>(a.kv_t) * HD;
@@ -847,6 +823,9 @@ tp_status launch_attn(const CUtensorMap& mk, const CUtensorMap& mv, const CUtens
   TP_CUDA_CHECK(launch_pdl(decode_attn_kernel<NG, GSZ>, dim3(grid), dim3(DEC_THREADS), DecCfg<NG>::SMEM, s, mk, mv,
                            mq, a));
   count_launch();
+  const unsigned cgrid = static_cast<unsigned>((a.B * a.nh + CMB_WARPS - 1) / CMB_WARPS);
+  TP_CUDA_CHECK(launch_pdl(decode_combine_kernel<NG>, dim3(cgrid), dim3(CMB_WARPS * 32), 0, s, a, grid));
+  count_launch();
   return TP_OK;
 }
 
@@ -876,10 +855,10 @@ inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct DecWs {
   uint16_t* q;
-  int* done;
   float *o_part, *m_part, *l_part;
   uint16_t* O;
   float* sk_part;  // skinny-GEMM partials (QKV, then W_o)
+  int* sk_cnt;     // W_o row-block counters
   size_t bytes;
 };
 
@@ -889,7 +868,6 @@ DecWs decode_ws_layout(void* ws, int64_t B, int64_t d, int n_heads, int t, const
   size_t off = 0;
   const size_t slots = static_cast<size_t>(sh.S) + MAX_GRID;
   w.q = reinterpret_cast<uint16_t*>(p + off); off += up256(static_cast<size_t>(B) * n_heads * HD * 2);
-  w.done = reinterpret_cast<int*>(p + off); off += up256(static_cast<size_t>(sh.S) * 4);
   w.o_part = reinterpret_cast<float*>(p + off); off += up256(slots * sh.NG * HD * 4);
   w.m_part = reinterpret_cast<float*>(p + off); off += up256(slots * sh.NG * 4);
   w.l_part = reinterpret_cast<float*>(p + off); off += up256(slots * sh.NG * 4);
@@ -897,6 +875,7 @@ DecWs decode_ws_layout(void* ws, int64_t B, int64_t d, int n_heads, int t, const
   const int bq = B > 32 ? 32 : static_cast<int>(B);
   const size_t skq = skinny_part_floats(sh.R_t * t, bq), sko = skinny_part_floats(d, bq);
   w.sk_part = reinterpret_cast<float*>(p + off); off += up256((skq > sko ? skq : sko) * 4);
+  w.sk_cnt = reinterpret_cast<int*>(p + off); off += up256(static_cast<size_t>(d / 128 + 1) * 4);
   w.bytes = off;
   return w;
 }
@@ -942,7 +921,7 @@ tp_status run_decode_attn(const uint16_t* x, int64_t B, int64_t d, int n_heads, 
     j.x = x; j.ldx = d; j.B = static_cast<int>(B); j.part = w.sk_part;
     j.epi = SK_EPI_QKV; j.bias = bqkv_p;
     j.R_t = sh.R_t; j.L_max = L_max; j.q_t = sh.q_t; j.kv_t = sh.kv_t; j.nh = n_heads;
-    j.pos = pos; j.q = w.q; j.Kc = Kc; j.Vc = Vc; j.done = w.done;
+    j.pos = pos; j.q = w.q; j.Kc = Kc; j.Vc = Vc;
     j.err = device_error_word();
     TP_RETURN_IF(run_skinny_gemm(j, s));
   } else {
@@ -952,7 +931,7 @@ tp_status run_decode_attn(const uint16_t* x, int64_t B, int64_t d, int n_heads, 
     qa.pos = pos; qa.q = w.q; qa.Kc = Kc; qa.Vc = Vc; qa.err = device_error_word();
     for (int64_t m0 = 0; m0 < B; m0 += 8) {
       qa.m0 = static_cast<int>(m0);
-      qa.done = m0 == 0 ? w.done : nullptr;
+      qa.check_pos = m0 == 0 ? 1 : 0;
       TP_RETURN_IF(qkv_dispatch(static_cast<int>(B - m0 < 8 ? B - m0 : 8), qa, s));
     }
   }
@@ -968,7 +947,8 @@ tp_status run_decode_attn(const uint16_t* x, int64_t B, int64_t d, int n_heads, 
   DecArgs a{};
   a.S = sh.S; a.B = static_cast<int>(B); a.nh = n_heads; a.q_t = sh.q_t; a.kv_t = sh.kv_t; a.Gs = sh.Gs;
   a.L_max = L_max; a.scale_log2 = scale * kLog2e; a.pos = pos;
-  a.o_part = w.o_part; a.m_part = w.m_part; a.l_part = w.l_part; a.done = w.done; a.O = w.O;
+  a.o_part = w.o_part; a.m_part = w.m_part; a.l_part = w.l_part; a.O = w.O;
+  a.zero_cnt = w.sk_cnt; a.n_zero = skinny ? static_cast<int>(d / 128) : 0;
   a.err = device_error_word(); a.timeout_ns = wait_timeout_ns();
   int64_t grid = device_sm_count();
   const int64_t max_tiles = S * ((L_max + BK - 1) / BK);
@@ -991,6 +971,7 @@ tp_status run_decode_attn(const uint16_t* x, int64_t B, int64_t d, int n_heads, 
     j.W = Wo_p; j.slabs = t; j.R = d; j.ku_per_slab = static_cast<int>(nq / t / 128);
     j.x = w.O; j.ldx = nq; j.B = static_cast<int>(B); j.part = w.sk_part;
     j.epi = SK_EPI_BF16; j.bias = bo; j.y = y; j.ldy = d; j.err = device_error_word();
+    j.cnt = w.sk_cnt;  // zeroed by the combine kernel
     return run_skinny_gemm(j, s);
   }
   return run_row_gemv(w.O, B, nq, d, t, Wo_p, bo, y, s);

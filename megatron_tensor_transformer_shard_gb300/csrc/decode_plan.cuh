@@ -12,16 +12,13 @@ namespace tp {
 constexpr int kDecodeTileKeys = 128;
 constexpr int kDecodeErrPos = 0x201;
 
-// Called by every thread of one CTA: validates the positions (a position
-// outside [0, L_max) is recorded as a device-side argument error; the kernels
-// clamp it) and zeroes the per-stream piece counters done[0..S).
-__device__ __forceinline__ void decode_plan_prepare(const int32_t* pos, int B, int64_t L_max, int S, int* done,
-                                                    int* err) {
+// Called by every thread of one CTA: a position outside [0, L_max) is
+// recorded as a device-side argument error (the kernels clamp it).
+__device__ __forceinline__ void decode_check_positions(const int32_t* pos, int B, int64_t L_max, int* err) {
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
     const int64_t p = pos[b];
     if (p < 0 || p >= L_max) atomicCAS(err, 0, kDecodeErrPos);
   }
-  for (int s = threadIdx.x; s < S; s += blockDim.x) done[s] = 0;
 }
 
 // Exclusive prefix of the sequences' tile counts into shared memory:

@@ -168,11 +168,11 @@ struct SkGemmJob {
   // SK_EPI_QKV: packed decode QKV rows [t][R_t], routed to q (fp16) or the cache copies
   int64_t R_t = 0, L_max = 0;
   int q_t = 0, kv_t = 0, nh = 0;
+  int* cnt = nullptr;  // SK_EPI_BF16: [R/128] counters, zero on entry -> the reduction runs inside the GEMM
   const int32_t* pos = nullptr;
   uint16_t* q = nullptr;
   uint16_t* Kc = nullptr;
   uint16_t* Vc = nullptr;
-  int* done = nullptr;  // SK_EPI_QKV: if non-null, the reduce kernel validates pos and zeroes these counters
   int* err = nullptr;
 };
 size_t skinny_part_floats(int64_t R, int B);

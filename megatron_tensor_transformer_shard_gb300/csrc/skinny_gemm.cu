@@ -55,6 +55,13 @@ struct SkCfg {
 struct SkArgs {
   int nrb, nku, ku_per_slab;  // row blocks, K units (128 wide) in all, per slab
   float* part;                // [slots][NB][128]
+  // fused reduction (cnt non-null): the CTA that writes a row block's last
+  // piece sums its pieces in K order and writes y[b][r] = bf16(sum + bias[r])
+  int* cnt;                   // [nrb], zero on entry
+  const uint16_t* bias;
+  uint16_t* y;
+  int64_t ldy;
+  int B;
   int* err;
   uint64_t timeout_ns;
 };
@@ -104,8 +111,10 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   uint64_t* acc_full = bars + 2 * ST;   // [2]
   uint64_t* acc_empty = acc_full + 2;   // [2]
   uint64_t* mma_done = acc_full + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 5);
+  uint64_t* all_done = acc_full + 5;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 6);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   ptx::griddep_launch_dependents();
@@ -125,6 +134,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
       ptx::mbar_init(&acc_empty[b], 128);
     }
     ptx::mbar_init(mma_done, 1);
+    ptx::mbar_init(all_done, SK_THREADS);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -227,7 +237,9 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
       const bool last = (u + 1 == u1) || ((u + 1) % p.nku == 0);
       if (!last) continue;
       const int ab = piece & 1;
-      if (!ptx::mbar_wait(&acc_full[ab], (piece >> 1) & 1, abort_flag, p.err, ERR_SK_EPI, p.timeout_ns)) break;
+      // no early exit on a failed (bounded) wait: every epilogue thread must
+      // reach the same named barriers; the error is already recorded
+      ptx::mbar_wait(&acc_full[ab], (piece >> 1) & 1, abort_flag, p.err, ERR_SK_EPI, p.timeout_ns);
       ptx::tc_fence_after();
       float v[NB];
       tmem_ld_nb<NB>(tmem + ab * NB + lane_base, v);
@@ -238,12 +250,59 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
 #pragma unroll
       for (int b = 0; b < NB; ++b) dst[b * 128] = v[b];
       ++piece;
+      if (p.cnt) {
+        // pieces of row block rb: CTAs k0..k1 that own units
+        const uint32_t uU = static_cast<uint32_t>(U), uG = static_cast<uint32_t>(G);
+        auto cta_of = [&](uint32_t x) { return ((x + 1) * uG - 1) / uU; };
+        auto owns = [&](uint32_t kk) { return (kk * uU) / uG != ((kk + 1) * uU) / uG; };
+        const uint32_t ua = static_cast<uint32_t>(rb) * p.nku;
+        const uint32_t k0 = cta_of(ua), k1 = cta_of(ua + p.nku - 1);
+        __threadfence();
+        __syncwarp();
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (row == 0) {
+          int npieces = 0;
+          for (uint32_t kk = k0; kk <= k1; ++kk) npieces += owns(kk) ? 1 : 0;
+          *last_flag = (atomicAdd(p.cnt + rb, 1) == npieces - 1) ? 1 : 0;
+        }
+        __syncwarp();
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (*last_flag) {
+          __threadfence();
+          float acc[NB];
+#pragma unroll
+          for (int b = 0; b < NB; ++b) acc[b] = 0.0f;
+          for (uint32_t kk = k0; kk <= k1; ++kk) {
+            if (!owns(kk)) continue;
+            const float* src = p.part + (static_cast<int64_t>(rb) + kk) * NB * 128 + row;
+            float t[NB];
+#pragma unroll
+            for (int b = 0; b < NB; ++b) t[b] = b < p.B ? __ldcg(src + b * 128) : 0.0f;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) acc[b] += t[b];
+          }
+          const int64_t r = static_cast<int64_t>(rb) * 128 + row;
+          const float bv = p.bias ? bf16_bits_to_float(p.bias[r]) : 0.0f;
+#pragma unroll
+          for (int b = 0; b < NB; ++b)
+            if (b < p.B) p.y[b * p.ldy + r] = float_to_bf16_bits(acc[b] + bv);
+        }
+        __syncwarp();
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // last_flag is rewritten by the next piece
+      }
     }
   }
 
+  // Teardown through an mbarrier (every thread arrives, then waits) rather
+  // than a CTA-wide bar.sync, which the epilogue's named barrier must not
+  // disturb; TMEM is freed only after every reader is done.
   ptx::tc_fence_before();
-  __syncwarp();  // lane-0 roles rejoin their warp: bar.sync needs converged warps
-  __syncthreads();
+  __syncwarp();
+  {
+    ptx::mbar_arrive(all_done);
+    volatile int never = 0;
+    ptx::mbar_wait(all_done, 0, &never, p.err, ERR_SK_DRAIN, p.timeout_ns);
+  }
   if (warp == 1) {
     __syncwarp();
     ptx::tc_fence_after();
@@ -254,7 +313,8 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
 // CTA whose range holds unit u (32-bit: the host keeps U * G below 2^32).
 __device__ __forceinline__ uint32_t sk_cta_of(uint32_t u, uint32_t G, uint32_t U) { return ((u + 1) * G - 1) / U; }
 
-// Sum of row r's partials for batch row b, in K order (CTA order).
+// Sum of row r's partials for batch row b, in K order (CTA order); the loads
+// of up to 4 pieces are issued together.
 template <int NB>
 __device__ __forceinline__ float sk_sum(const SkGemmJob& j, uint32_t G, uint32_t r, int b) {
   const uint32_t nku = static_cast<uint32_t>(j.nku);
@@ -262,10 +322,22 @@ __device__ __forceinline__ float sk_sum(const SkGemmJob& j, uint32_t G, uint32_t
   const uint32_t rb = r >> 7, row = r & 127u;
   const uint32_t ua = rb * nku;
   const uint32_t k0 = sk_cta_of(ua, G, U), k1 = sk_cta_of(ua + nku - 1, G, U);
+  auto owns = [&](uint32_t kk) { return (kk * U) / G != ((kk + 1) * U) / G; };  // else it wrote nothing
   float s = 0.0f;
-  for (uint32_t kk = k0; kk <= k1; ++kk) {
-    if ((kk * U) / G == ((kk + 1) * U) / G) continue;  // CTA without units wrote nothing
-    s += __ldcg(j.part + ((static_cast<size_t>(rb) + kk) * NB + b) * 128 + row);
+  uint32_t kk = k0;
+  while (kk <= k1) {
+    float v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      while (kk <= k1 && !owns(kk)) ++kk;
+      v[q] = 0.0f;
+      if (kk <= k1) {
+        v[q] = __ldcg(j.part + ((static_cast<size_t>(rb) + kk) * NB + b) * 128 + row);
+        ++kk;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) s += v[q];
   }
   return s;
 }
@@ -274,8 +346,7 @@ template <int NB>
 __global__ void __launch_bounds__(256) skinny_reduce_kernel(const SkGemmJob j, int G) {
   ptx::griddep_launch_dependents();
   ptx::griddep_wait();
-  if (j.done && blockIdx.x == 0)
-    decode_plan_prepare(j.pos, j.B, j.L_max, static_cast<int>(j.R / j.R_t) * j.kv_t * j.B, j.done, j.err);
+  if (j.epi == SK_EPI_QKV && blockIdx.x == 0) decode_check_positions(j.pos, j.B, j.L_max, j.err);
   const int64_t n = static_cast<int64_t>(j.R) * j.B;
   for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -329,6 +400,11 @@ tp_status launch_skinny(const SkGemmJob& j, cudaStream_t s) {
   a.nku = j.nku;
   a.ku_per_slab = j.ku_per_slab;
   a.part = j.part;
+  a.cnt = j.cnt;
+  a.bias = j.bias;
+  a.y = j.y;
+  a.ldy = j.ldy;
+  a.B = j.B;
   a.err = device_error_word();
   a.timeout_ns = wait_timeout_ns();
   const int64_t U = static_cast<int64_t>(j.nrb) * j.nku;
@@ -338,6 +414,7 @@ tp_status launch_skinny(const SkGemmJob& j, cudaStream_t s) {
   TP_CUDA_CHECK(launch_pdl(skinny_gemm_kernel<NB>, dim3(static_cast<unsigned>(G)), dim3(SK_THREADS),
                            SkCfg<NB>::SMEM, s, mw, mx, a));
   count_launch();
+  if (j.cnt) return TP_OK;  // reduced in the GEMM kernel
   const int64_t n = static_cast<int64_t>(j.R) * j.B;
   int64_t rg = (n + 255) / 256;
   const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
@@ -363,6 +440,7 @@ bool skinny_ok(int64_t R, int64_t Kt, int B) {
 
 tp_status run_skinny_gemm(SkGemmJob j, cudaStream_t s) {
   if (!skinny_ok(j.R, static_cast<int64_t>(j.ku_per_slab) * 128 * j.slabs, j.B) || j.slabs < 1) return TP_ERR_SHAPE;
+  if (j.cnt && j.epi != SK_EPI_BF16) return TP_ERR_UNSUPPORTED;
   if (!aligned16(j.W) || !aligned16(j.x) || !aligned16(j.part) || j.ldx % 8 != 0) return TP_ERR_ALIGN;
   j.nrb = static_cast<int>(j.R / 128);
   j.nku = j.ku_per_slab * j.slabs;
