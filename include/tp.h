@@ -282,6 +282,20 @@ tp_status tp_attn_forward(const tp_bf16* X, int64_t N, int64_t d, int n_heads, i
                           tp_bf16* O_save, float* lse_save, unsigned flags, void* ws, size_t ws_bytes,
                           tp_stream stream);
 
+/* Grouped-query form of tp_attn_forward ("02 — Tensor Parallelism", "The
+ * attention pairing": GQA/MQA shard by KV group; "Tensor and sequence
+ * parallelism", exercise 1: fewer KV heads than shards -> replicated KV heads).
+ * Wqkv_p / bqkv_p from tp_pack_qkv_gqa(_bias); QKV_save [t][N][R] IEEE fp16 with
+ * R = (n_heads/t + 2 kv_t) * head_dim (rows [Q heads | K heads | V heads] of the
+ * shard); query head j of a shard reads the shard's KV head j / min(n_heads/n_kv,
+ * n_heads/t).  Everything else as tp_attn_forward (which is this call with
+ * n_kv_heads = n_heads). */
+tp_status tp_attn_gqa_forward(const tp_bf16* X, int64_t N, int64_t d, int n_heads, int n_kv_heads, int head_dim,
+                              int t, int causal, float scale, const tp_bf16* Wqkv_p, const tp_bf16* bqkv_p,
+                              const tp_bf16* Wo_p, const tp_bf16* bo, const tp_bf16* residual, tp_bf16* Y,
+                              uint16_t* QKV_save, tp_bf16* O_save, float* lse_save, unsigned flags, void* ws,
+                              size_t ws_bytes, tp_stream stream);
+
 /* Backward of L = <Y, dY>: g backward identity; per shard dO_i = dY W_o,i^T,
  * head-local softmax backward, dQKV_i; dW_o,i = O_i^T dY; dW_qkv,i = dQKV_i^T X;
  * f backward: dX = sum_i dQKV_i W_qkv,i^T (fused).  dWqkv_p [t][3d/t][d],
@@ -298,6 +312,32 @@ tp_status tp_attn_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Q
                            int causal, float scale, const tp_bf16* Wqkv_p, const tp_bf16* Wo_p, tp_bf16* dX,
                            float* dWqkv_p, float* dbqkv_p, float* dWo_p, float* dbo, int accumulate,
                            unsigned flags, void* ws, size_t ws_bytes, tp_stream stream);
+
+/* Grouped-query backward: as tp_attn_backward with the layouts of
+ * tp_attn_gqa_forward.  A KV head's dK / dV sum over the query heads of its
+ * group on the shard; dWqkv_p [t][R][d] and dbqkv_p [t][R] hold each shard's
+ * gradient for its own copy of the columns (a replicated KV head has t/n_kv
+ * copies); tp_reduce_qkv_gqa_grad sums them into the unsplit gradient.
+ * ws: tp_attn_gqa_backward_workspace_size() bytes (dO, D, dQKV [t][N][R] bf16,
+ * column-sum scratch). */
+size_t tp_attn_gqa_backward_workspace_size(int64_t N, int64_t d, int n_heads, int n_kv_heads, int head_dim, int t,
+                                           unsigned flags);
+tp_status tp_attn_gqa_backward(const tp_bf16* dY, const tp_bf16* X, const uint16_t* QKV_save, const tp_bf16* O_save,
+                               const float* lse_save, int64_t N, int64_t d, int n_heads, int n_kv_heads,
+                               int head_dim, int t, int causal, float scale, const tp_bf16* Wqkv_p,
+                               const tp_bf16* Wo_p, tp_bf16* dX, float* dWqkv_p, float* dbqkv_p, float* dWo_p,
+                               float* dbo, int accumulate, unsigned flags, void* ws, size_t ws_bytes,
+                               tp_stream stream);
+
+/* The replica-group reduction of grouped-query weight gradients: dW (d,
+ * (n_heads + 2 n_kv) head_dim) fp32, unsplit layout, gets for every column the
+ * sum, in shard order, of the packed gradients dWp [t][R][d] (fp32) of all shard
+ * copies holding it -- one copy for query columns and when n_kv >= t, t/n_kv
+ * copies for a replicated KV head's columns (the copies' gradients must be
+ * summed, as the LayerNorm weights shared by sequence shards are).  accumulate
+ * != 0 adds to dW.  Src and dst must not overlap. */
+tp_status tp_reduce_qkv_gqa_grad(const float* dWp, int64_t d, int n_heads, int n_kv_heads, int head_dim, int t,
+                                 float* dW, int accumulate, tp_stream stream);
 
 /* ------------------------------------------- sequence-parallel LayerNorm
  * ("Tensor and sequence parallelism", section "Sequence parallelism";

@@ -60,6 +60,12 @@ SIGNATURES = {
     "tp_sp_layernorm_backward": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I, _P, _P, _P, _P, _P, _P]),
     "tp_attn_forward": (_I, [_P, _I64, _I64, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _U, _P, _SZ,
                              _P]),
+    "tp_attn_gqa_forward": (_I, [_P, _I64, _I64, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _U,
+                                 _P, _SZ, _P]),
+    "tp_attn_gqa_backward_workspace_size": (_SZ, [_I64, _I64, _I, _I, _I, _I, _U]),
+    "tp_attn_gqa_backward": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P,
+                                  _P, _I, _U, _P, _SZ, _P]),
+    "tp_reduce_qkv_gqa_grad": (_I, [_P, _I64, _I, _I, _I, _I, _P, _I, _P]),
     "tp_attn_backward_workspace_size": (_SZ, [_I64, _I64, _I, _I, _I, _U]),
     "tp_attn_backward": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _I, _U,
                               _P, _SZ, _P]),

@@ -48,7 +48,9 @@ enum : int { ERR_ATT_PRODUCER = 0x111, ERR_ATT_MMA = 0x112, ERR_ATT_SOFTMAX = 0x
 
 struct AttnFwdArgs {
   int N, H, hpr, nqb, causal;
-  int64_t dt;            // d / t: width of one shard's Q (or K, or V) block
+  int Gs;                // query heads of a shard per KV head (1: multi-head)
+  int64_t dt;            // width of one shard's Q block (and of its O)
+  int64_t kcol0, vcol0;  // first column of the shard's K and V blocks in a QKV row
   float scale_log2;      // softmax scale * log2(e)
   uint16_t* O;           // [t][N][dt]
   float* lse;            // [t][hpr][N]
@@ -107,8 +109,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   const int shard = head / p.hpr, jj = head - shard * p.hpr;
   const int nkv = p.causal ? qb + 1 : (p.N + BKV - 1) / BKV;
   const int qcol = jj * HD;
-  const int kcol = static_cast<int>(p.dt) + jj * HD;
-  const int vcol = static_cast<int>(2 * p.dt) + jj * HD;
+  const int kcol = static_cast<int>(p.kcol0) + (jj / p.Gs) * HD;  // the KV head this query head reads
+  const int vcol = static_cast<int>(p.vcol0) + (jj / p.Gs) * HD;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
@@ -335,11 +337,13 @@ constexpr int DQ_SMEM = 1024 + 7 * TILE + 256;
 
 struct AttnBwdArgs {
   int N, H, hpr, nqb, causal;
-  int64_t dt;
+  int Gs, kv_t, Hkv;     // query heads per KV head in a shard, KV heads per shard, KV heads in all
+  int64_t dt;            // width of a shard's Q block (= its O and dO)
+  int64_t row_w, kcol0, vcol0;  // QKV row width per shard; first K and V columns
   float scale, scale_log2;
   const float* lse;   // [t][hpr][N] natural log
   const float* Dvec;  // [t][hpr][N]
-  uint16_t* dQKV;     // [t][N][3dt]
+  uint16_t* dQKV;     // [t][N][row_w]
   int* err;
   uint64_t timeout_ns;
 };
@@ -443,12 +447,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int head = blockIdx.x % p.H;
-  const int kb = static_cast<int>(blockIdx.x / p.H);  // early key blocks see the most query blocks (causal)
-  const int shard = head / p.hpr, jj = head - shard * p.hpr;
+  // One CTA per (KV head, key block): dK and dV sum over the query heads of
+  // the KV head's group on this shard, so the loop runs over (group head,
+  // query block) pairs and the TMEM accumulators carry across all of them.
+  const int kvh = blockIdx.x % p.Hkv;
+  const int kb = static_cast<int>(blockIdx.x / p.Hkv);  // early key blocks see the most query blocks (causal)
+  const int shard = kvh / p.kv_t, jl = kvh - shard * p.kv_t;
   const int q_first = p.causal ? kb : 0;
   const int nq = p.nqb - q_first;
-  const int qcol = jj * HD, kcol = static_cast<int>(p.dt) + jj * HD, vcol = static_cast<int>(2 * p.dt) + jj * HD;
+  const int nloop = nq * p.Gs;
+  const int kcol = static_cast<int>(p.kcol0) + jl * HD, vcol = static_cast<int>(p.vcol0) + jl * HD;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(kv_full, 1);
@@ -483,14 +491,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       ptx::tma_load_3d(sV, &tm_qkv, kv_full, vcol, kb * BKV, shard);
       ptx::tma_load_3d(sV + PANEL, &tm_qkv, kv_full, vcol + 64, kb * BKV, shard);
       int issued = 0;
-      for (int n = 0; n < nq; ++n) {
-        const int qi = q_first + n;
+      for (int n = 0; n < nloop; ++n) {
+        const int g = n / nq, qi = q_first + (n - g * nq);
+        const int qcol = (jl * p.Gs + g) * HD;
         if (!ptx::mbar_wait(qdo_empty, (n & 1) ^ 1u, abort_flag, p.err, ERR_ATT_PRODUCER, p.timeout_ns)) break;
         ptx::mbar_arrive_expect_tx(qdo_full, 2 * TILE);
         ptx::tma_load_3d(sQ, &tm_qkv, qdo_full, qcol, qi * BQ, shard);
         ptx::tma_load_3d(sQ + PANEL, &tm_qkv, qdo_full, qcol + 64, qi * BQ, shard);
-        ptx::tma_load_3d(sdO, &tm_do, qdo_full, jj * HD, qi * BQ, shard);
-        ptx::tma_load_3d(sdO + PANEL, &tm_do, qdo_full, jj * HD + 64, qi * BQ, shard);
+        ptx::tma_load_3d(sdO, &tm_do, qdo_full, qcol, qi * BQ, shard);
+        ptx::tma_load_3d(sdO + PANEL, &tm_do, qdo_full, qcol + 64, qi * BQ, shard);
         ++issued;
       }
       volatile int never = 0;
@@ -504,7 +513,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const uint32_t aK = ptx::smem_addr(sK), aV = ptx::smem_addr(sV), aQ = ptx::smem_addr(sQ);
       const uint32_t adO = ptx::smem_addr(sdO), aP = ptx::smem_addr(sP), adS = ptx::smem_addr(sdS);
       bool ok = ptx::mbar_wait(kv_full, 0, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns);
-      for (int n = 0; ok && n < nq; ++n) {
+      for (int n = 0; ok && n < nloop; ++n) {
         if (!ptx::mbar_wait(qdo_full, n & 1, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
         if (n >= 1 && !ptx::mbar_wait(sdp_free, (n - 1) & 1, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
         ptx::tc_fence_after();
@@ -534,10 +543,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const int64_t vec_base = (static_cast<int64_t>(shard) * p.hpr + jj) * p.N;
     bool ok = true;
-    for (int n = 0; n < nq; ++n) {
-      const int q = (q_first + n) * BQ + row;
+    for (int n = 0; n < nloop; ++n) {
+      const int g = n / nq;
+      const int64_t vec_base = (static_cast<int64_t>(shard) * p.hpr + jl * p.Gs + g) * p.N;
+      const int q = (q_first + (n - g * nq)) * BQ + row;
       const float lse2 = q < p.N ? p.lse[vec_base + q] * kLog2e : 0.0f;
       const float Dq = q < p.N ? p.Dvec[vec_base + q] : 0.0f;
       if (!ptx::mbar_wait(sdp_full, n & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
@@ -564,10 +574,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(pds_full);
     }
-    if (ok && nq > 0 && ptx::mbar_wait(pds_free, (nq - 1) & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
+    if (ok && nloop > 0 &&
+        ptx::mbar_wait(pds_free, (nloop - 1) & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
       ptx::tc_fence_after();
       const int kvrow = kb * BKV + row;  // accumulator rows are key rows
-      uint16_t* drow = p.dQKV + (static_cast<int64_t>(shard) * p.N + kvrow) * (3 * p.dt);
+      uint16_t* drow = p.dQKV + (static_cast<int64_t>(shard) * p.N + kvrow) * p.row_w;
       tmem_row_to_bf16(tdV + lane_base, 1.0f, drow + vcol, kvrow < p.N);
       tmem_row_to_bf16(tdK + lane_base, p.scale, drow + kcol, kvrow < p.N);
     }
@@ -612,7 +623,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const int qb = p.nqb - 1 - static_cast<int>(blockIdx.x / p.H);
   const int shard = head / p.hpr, jj = head - shard * p.hpr;
   const int nkv = p.causal ? qb + 1 : (p.N + BKV - 1) / BKV;
-  const int qcol = jj * HD, kcol = static_cast<int>(p.dt) + jj * HD, vcol = static_cast<int>(2 * p.dt) + jj * HD;
+  const int qcol = jj * HD;
+  const int kcol = static_cast<int>(p.kcol0) + (jj / p.Gs) * HD, vcol = static_cast<int>(p.vcol0) + (jj / p.Gs) * HD;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(qdo_full, 1);
@@ -738,7 +750,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     }
     if (ok && ptx::mbar_wait(ds_free, (nkv - 1) & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
       ptx::tc_fence_after();
-      uint16_t* drow = p.dQKV + (static_cast<int64_t>(shard) * p.N + q) * (3 * p.dt);
+      uint16_t* drow = p.dQKV + (static_cast<int64_t>(shard) * p.N + q) * p.row_w;
       tmem_row_to_bf16(tdQ + lane_base, p.scale, drow + qcol, q < p.N);
     }
   }
@@ -755,25 +767,50 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 
 }  // namespace
 
-tp_status run_attention_fwd(const uint16_t* QKV, int64_t N, int64_t d, int n_heads, int head_dim, int t, int causal,
-                            float scale, uint16_t* O, float* lse, cudaStream_t s) {
-  if (N < 0 || d < 1 || n_heads < 1 || t < 1) return TP_ERR_INVALID_ARG;
-  if (head_dim != HD || static_cast<int64_t>(n_heads) * head_dim != d || n_heads % t != 0) return TP_ERR_SHAPE;
+// Shape of a shard's QKV row under grouped-query sharding (n_kv = n_heads:
+// multi-head): q_t query heads, kv_t KV heads, Gs query heads per KV head.
+struct AttnShape {
+  int q_t, kv_t, Gs;
+  int64_t dt, row_w, kcol0, vcol0;
+};
+
+bool attn_shape(int64_t d, int n_heads, int n_kv, int head_dim, int t, AttnShape& a) {
+  if (head_dim != HD || t < 1 || n_heads < 1 || n_kv < 1) return false;
+  if (static_cast<int64_t>(n_heads) * head_dim != d || n_heads % t != 0 || n_heads % n_kv != 0) return false;
+  if (n_kv >= t ? (n_kv % t != 0) : (t % n_kv != 0)) return false;
+  a.q_t = n_heads / t;
+  a.kv_t = n_kv >= t ? n_kv / t : 1;
+  const int G = n_heads / n_kv;
+  a.Gs = G < a.q_t ? G : a.q_t;
+  a.dt = static_cast<int64_t>(a.q_t) * HD;
+  a.row_w = static_cast<int64_t>(a.q_t + 2 * a.kv_t) * HD;
+  a.kcol0 = a.dt;
+  a.vcol0 = a.dt + static_cast<int64_t>(a.kv_t) * HD;
+  return true;
+}
+
+tp_status run_attention_fwd(const uint16_t* QKV, int64_t N, int64_t d, int n_heads, int n_kv, int head_dim, int t,
+                            int causal, float scale, uint16_t* O, float* lse, cudaStream_t s) {
+  if (N < 0 || d < 1 || n_heads < 1 || n_kv < 1 || t < 1) return TP_ERR_INVALID_ARG;
+  AttnShape sh;
+  if (!attn_shape(d, n_heads, n_kv, head_dim, t, sh)) return TP_ERR_SHAPE;
   if (N == 0) return TP_OK;
   if (!QKV || !O || !lse) return TP_ERR_INVALID_ARG;
   if (!aligned16(QKV) || !aligned16(O)) return TP_ERR_ALIGN;
   if (N > (1LL << 30) / 1) return TP_ERR_SHAPE;
   TP_RETURN_IF(ready());
-  const int64_t dt = d / t;
   CUtensorMap map;
-  if (!make_map_3d_bf16(&map, QKV, 3 * dt, N, t, 3 * dt * 2, N * 3 * dt * 2, 64, 128)) return TP_ERR_CUDA;
+  if (!make_map_3d_bf16(&map, QKV, sh.row_w, N, t, sh.row_w * 2, N * sh.row_w * 2, 64, 128)) return TP_ERR_CUDA;
   AttnFwdArgs a{};
   a.N = static_cast<int>(N);
   a.H = n_heads;
   a.hpr = n_heads / t;
   a.nqb = static_cast<int>((N + BQ - 1) / BQ);
   a.causal = causal ? 1 : 0;
-  a.dt = dt;
+  a.Gs = sh.Gs;
+  a.dt = sh.dt;
+  a.kcol0 = sh.kcol0;
+  a.vcol0 = sh.vcol0;
   a.scale_log2 = scale * kLog2e;
   a.O = O;
   a.lse = lse;
@@ -799,18 +836,19 @@ tp_status run_attention_fwd(const uint16_t* QKV, int64_t N, int64_t d, int n_hea
 namespace tp {
 
 tp_status run_attention_bwd(const uint16_t* QKV, const uint16_t* O, const uint16_t* dO, const float* lse, int64_t N,
-                            int64_t d, int n_heads, int head_dim, int t, int causal, float scale, float* Dvec,
+                            int64_t d, int n_heads, int n_kv, int head_dim, int t, int causal, float scale, float* Dvec,
                             uint16_t* dQKV, cudaStream_t s) {
-  if (N < 0 || d < 1 || n_heads < 1 || t < 1) return TP_ERR_INVALID_ARG;
-  if (head_dim != HD || static_cast<int64_t>(n_heads) * head_dim != d || n_heads % t != 0) return TP_ERR_SHAPE;
+  if (N < 0 || d < 1 || n_heads < 1 || n_kv < 1 || t < 1) return TP_ERR_INVALID_ARG;
+  AttnShape sh;
+  if (!attn_shape(d, n_heads, n_kv, head_dim, t, sh)) return TP_ERR_SHAPE;
   if (N == 0) return TP_OK;
   if (!QKV || !O || !dO || !lse || !Dvec || !dQKV) return TP_ERR_INVALID_ARG;
   if (!aligned16(QKV) || !aligned16(O) || !aligned16(dO) || !aligned16(dQKV)) return TP_ERR_ALIGN;
   TP_RETURN_IF(ready());
-  const int64_t dt = d / t;
+  const int64_t dt = sh.dt;
   const int hpr = n_heads / t;
   CUtensorMap m_qkv, m_do;
-  if (!make_map_3d_bf16(&m_qkv, QKV, 3 * dt, N, t, 3 * dt * 2, N * 3 * dt * 2, 64, 128)) return TP_ERR_CUDA;
+  if (!make_map_3d_bf16(&m_qkv, QKV, sh.row_w, N, t, sh.row_w * 2, N * sh.row_w * 2, 64, 128)) return TP_ERR_CUDA;
   if (!make_map_3d_bf16(&m_do, dO, dt, N, t, dt * 2, N * dt * 2, 64, 128)) return TP_ERR_CUDA;
   const int64_t rows = static_cast<int64_t>(t) * N * hpr;
   attn_bwd_dot_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, s>>>(dO, O, static_cast<int>(N), hpr,
@@ -822,7 +860,13 @@ tp_status run_attention_bwd(const uint16_t* QKV, const uint16_t* O, const uint16
   a.hpr = hpr;
   a.nqb = static_cast<int>((N + BQ - 1) / BQ);
   a.causal = causal ? 1 : 0;
+  a.Gs = sh.Gs;
+  a.kv_t = sh.kv_t;
+  a.Hkv = t * sh.kv_t;
   a.dt = dt;
+  a.row_w = sh.row_w;
+  a.kcol0 = sh.kcol0;
+  a.vcol0 = sh.vcol0;
   a.scale = scale;
   a.scale_log2 = scale * kLog2e;
   a.lse = lse;
@@ -839,9 +883,10 @@ tp_status run_attention_bwd(const uint16_t* QKV, const uint16_t* O, const uint16
     TP_CUDA_CHECK(cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM));
     configured[dev] = true;
   }
-  const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(n_heads) * a.nqb);
-  attn_bwd_dkv_kernel<<<grid, BWD_THREADS, DKV_SMEM, s>>>(m_qkv, m_do, a);
+  const unsigned grid_kv = static_cast<unsigned>(static_cast<int64_t>(a.Hkv) * a.nqb);
+  attn_bwd_dkv_kernel<<<grid_kv, BWD_THREADS, DKV_SMEM, s>>>(m_qkv, m_do, a);
   TP_LAUNCHED();
+  const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(n_heads) * a.nqb);
   attn_bwd_dq_kernel<<<grid, BWD_THREADS, DQ_SMEM, s>>>(m_qkv, m_do, a);
   TP_LAUNCHED();
   return TP_OK;

@@ -156,7 +156,19 @@ struct AttnBwdWs {
   size_t total;
 };
 
-AttnBwdWs attn_bwd_layout(void* ws, int64_t N, int64_t d, int n_heads, int t) {
+// QKV row width of one shard: [q_t query heads | kv_t K heads | kv_t V heads] x head_dim.
+int64_t qkv_row_width(int n_heads, int n_kv, int head_dim, int t) {
+  const int kv_t = n_kv >= t ? n_kv / t : 1;
+  return static_cast<int64_t>(n_heads / t + 2 * kv_t) * head_dim;
+}
+
+bool gqa_ok(int64_t d, int n_heads, int n_kv, int head_dim, int t) {
+  if (head_dim != 128 || static_cast<int64_t>(n_heads) * head_dim != d || n_heads % t != 0) return false;
+  if (n_kv < 1 || n_heads % n_kv != 0) return false;
+  return n_kv >= t ? n_kv % t == 0 : t % n_kv == 0;
+}
+
+AttnBwdWs attn_bwd_layout(void* ws, int64_t N, int64_t d, int n_heads, int64_t row_w, int t) {
   AttnBwdWs w{};
   uint8_t* b = static_cast<uint8_t*>(ws);
   size_t off = 0;
@@ -165,9 +177,9 @@ AttnBwdWs attn_bwd_layout(void* ws, int64_t N, int64_t d, int n_heads, int t) {
   w.Dvec = reinterpret_cast<float*>(b + off);
   off += round_up(static_cast<size_t>(N) * n_heads * 4, 256);
   w.dQKV = reinterpret_cast<uint16_t*>(b + off);
-  off += round_up(static_cast<size_t>(N) * 3 * d * 2, 256);
+  off += round_up(static_cast<size_t>(N) * t * row_w * 2, 256);
   w.cs = reinterpret_cast<float*>(b + off);
-  w.cs_floats = colsum2_ws_floats(N, d, 1) + colsum2_ws_floats(N, 3 * d / t, t);
+  w.cs_floats = colsum2_ws_floats(N, d, 1) + colsum2_ws_floats(N, row_w, t);
   off += round_up(w.cs_floats * 4, 256);
   w.total = off;
   return w;
@@ -177,24 +189,33 @@ AttnBwdWs attn_bwd_layout(void* ws, int64_t N, int64_t d, int n_heads, int t) {
 
 extern "C" {
 
+size_t tp_attn_gqa_backward_workspace_size(int64_t N, int64_t d, int n_heads, int n_kv_heads, int head_dim, int t,
+                                           unsigned flags) {
+  (void)flags;
+  if (N < 0 || d < 1 || n_heads < 1 || t < 1 || !gqa_ok(d, n_heads, n_kv_heads, head_dim, t)) return 0;
+  return attn_bwd_layout(nullptr, N, d, n_heads, qkv_row_width(n_heads, n_kv_heads, head_dim, t), t).total;
+}
+
 size_t tp_attn_backward_workspace_size(int64_t N, int64_t d, int n_heads, int head_dim, int t, unsigned flags) {
   (void)head_dim;
   (void)flags;
   if (N < 0 || d < 1 || n_heads < 1 || t < 1) return 0;
-  return attn_bwd_layout(nullptr, N, d, n_heads, t).total;
+  return attn_bwd_layout(nullptr, N, d, n_heads, 3 * d / t, t).total;
 }
 
-tp_status tp_attn_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* QKV_save, const tp_bf16* O_save,
-                           const float* lse_save, int64_t N, int64_t d, int n_heads, int head_dim, int t,
-                           int causal, float scale, const tp_bf16* Wqkv_p, const tp_bf16* Wo_p, tp_bf16* dX,
-                           float* dWqkv_p, float* dbqkv_p, float* dWo_p, float* dbo, int accumulate,
-                           unsigned flags, void* ws, size_t ws_bytes, tp_stream stream) {
-  if (N < 0 || d < 1 || n_heads < 1 || t < 1 || head_dim < 1) return TP_ERR_INVALID_ARG;
+tp_status tp_attn_gqa_backward(const tp_bf16* dY, const tp_bf16* X, const uint16_t* QKV_save, const tp_bf16* O_save,
+                               const float* lse_save, int64_t N, int64_t d, int n_heads, int n_kv_heads,
+                               int head_dim, int t, int causal, float scale, const tp_bf16* Wqkv_p,
+                               const tp_bf16* Wo_p, tp_bf16* dX, float* dWqkv_p, float* dbqkv_p, float* dWo_p,
+                               float* dbo, int accumulate, unsigned flags, void* ws, size_t ws_bytes,
+                               tp_stream stream) {
+  if (N < 0 || d < 1 || n_heads < 1 || n_kv_heads < 1 || t < 1 || head_dim < 1) return TP_ERR_INVALID_ARG;
   if (flags != 0) return TP_ERR_UNSUPPORTED;
-  if (head_dim != 128 || static_cast<int64_t>(n_heads) * head_dim != d || n_heads % t != 0) return TP_ERR_SHAPE;
+  if (!gqa_ok(d, n_heads, n_kv_heads, head_dim, t)) return TP_ERR_SHAPE;
   if (!dWqkv_p || !dWo_p) return TP_ERR_INVALID_ARG;
   if (N > 0 && (!dY || !X || !QKV_save || !O_save || !lse_save || !Wqkv_p || !Wo_p || !dX)) return TP_ERR_INVALID_ARG;
-  const AttnBwdWs w = attn_bwd_layout(ws, N, d, n_heads, t);
+  const int64_t rw = qkv_row_width(n_heads, n_kv_heads, head_dim, t);  // one shard's QKV row
+  const AttnBwdWs w = attn_bwd_layout(ws, N, d, n_heads, rw, t);
   if (!ws || ws_bytes < w.total) return TP_ERR_WORKSPACE;
   if (!aligned16(ws)) return TP_ERR_ALIGN;
   const cudaStream_t s = S(stream);
@@ -202,9 +223,9 @@ tp_status tp_attn_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Q
   if (N == 0) {
     TP_RETURN_IF(ready());
     if (!accumulate) {
-      TP_CUDA_CHECK(cudaMemsetAsync(dWqkv_p, 0, sizeof(float) * 3 * d * d, s));
+      TP_CUDA_CHECK(cudaMemsetAsync(dWqkv_p, 0, sizeof(float) * t * rw * d, s));
       TP_CUDA_CHECK(cudaMemsetAsync(dWo_p, 0, sizeof(float) * d * d, s));
-      if (dbqkv_p) TP_CUDA_CHECK(cudaMemsetAsync(dbqkv_p, 0, sizeof(float) * 3 * d, s));
+      if (dbqkv_p) TP_CUDA_CHECK(cudaMemsetAsync(dbqkv_p, 0, sizeof(float) * t * rw, s));
       if (dbo) TP_CUDA_CHECK(cudaMemsetAsync(dbo, 0, sizeof(float) * d, s));
     }
     return TP_OK;
@@ -225,8 +246,8 @@ tp_status tp_attn_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Q
   wo.epi = EPI_F32; wo.d = dWo_p; wo.ldd = dt; wo.d_batch_stride = d * dt; wo.accumulate = accumulate;
   TP_RETURN_IF(run_gemm(wo, s));
   // Head-local softmax-attention backward -> dQKV_i.
-  TP_RETURN_IF(run_attention_bwd(QKV_save, O_save, w.dO, lse_save, N, d, n_heads, head_dim, t, causal, scale, w.Dvec,
-                                 w.dQKV, s));
+  TP_RETURN_IF(run_attention_bwd(QKV_save, O_save, w.dO, lse_save, N, d, n_heads, n_kv_heads, head_dim, t, causal,
+                                 scale, w.Dvec, w.dQKV, s));
   // Bias gradients in one fused pass: db_o once (g backward is the identity), db_qkv per shard.
   if (dbo || dbqkv_p) {
     ColsumJob jo, jq;
@@ -235,25 +256,37 @@ tp_status tp_attn_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Q
       jo.out = dbo; jo.ws = w.cs; jo.accumulate = accumulate;
     }
     if (dbqkv_p) {
-      jq.G = w.dQKV; jq.rows = N; jq.cols = 3 * dt; jq.ld = 3 * dt; jq.bs = N * 3 * dt; jq.nbatch = t;
+      jq.G = w.dQKV; jq.rows = N; jq.cols = rw; jq.ld = rw; jq.bs = N * rw; jq.nbatch = t;
       jq.out = dbqkv_p; jq.ws = w.cs + colsum2_ws_floats(N, d, 1); jq.accumulate = accumulate;
     }
     TP_RETURN_IF(run_colsum2(jo, jq, s));
   }
-  // dW_qkv,i = dQKV_i^T X -> packed [t][3dt][d] (local).
+  // dW_qkv,i = dQKV_i^T X -> packed [t][rw][d] (local; a replicated KV head gets one gradient per copy).
   GemmProblem wq;
-  wq.M = 3 * dt; wq.N = d; wq.K = N; wq.nbatch = t;
-  wq.a.ptr = w.dQKV; wq.a.ld = 3 * dt; wq.a.sharded = true; wq.a.shard_stride = N * 3 * dt; wq.a.mn_major = true;
+  wq.M = rw; wq.N = d; wq.K = N; wq.nbatch = t;
+  wq.a.ptr = w.dQKV; wq.a.ld = rw; wq.a.sharded = true; wq.a.shard_stride = N * rw; wq.a.mn_major = true;
   wq.b.ptr = X; wq.b.ld = d; wq.b.mn_major = true;
-  wq.epi = EPI_F32; wq.d = dWqkv_p; wq.ldd = d; wq.d_batch_stride = 3 * dt * d; wq.accumulate = accumulate;
+  wq.epi = EPI_F32; wq.d = dWqkv_p; wq.ldd = d; wq.d_batch_stride = rw * d; wq.accumulate = accumulate;
   TP_RETURN_IF(run_gemm(wq, s));
   // f backward: dX = sum_i dQKV_i W_qkv,i (fixed shard order, fused).
   GemmProblem dx;
-  dx.M = N; dx.N = d; dx.K = 3 * dt; dx.nsum = t;
-  dx.a.ptr = w.dQKV; dx.a.ld = 3 * dt; dx.a.sharded = true; dx.a.shard_stride = N * 3 * dt;
-  dx.b.ptr = Wqkv_p; dx.b.ld = d; dx.b.sharded = true; dx.b.shard_stride = 3 * dt * d; dx.b.mn_major = true;
+  dx.M = N; dx.N = d; dx.K = rw; dx.nsum = t;
+  dx.a.ptr = w.dQKV; dx.a.ld = rw; dx.a.sharded = true; dx.a.shard_stride = N * rw;
+  dx.b.ptr = Wqkv_p; dx.b.ld = d; dx.b.sharded = true; dx.b.shard_stride = rw * d; dx.b.mn_major = true;
   dx.epi = EPI_BF16; dx.d = dX; dx.ldd = d;
   return run_gemm(dx, s);
+}
+
+tp_status tp_attn_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* QKV_save, const tp_bf16* O_save,
+                           const float* lse_save, int64_t N, int64_t d, int n_heads, int head_dim, int t,
+                           int causal, float scale, const tp_bf16* Wqkv_p, const tp_bf16* Wo_p, tp_bf16* dX,
+                           float* dWqkv_p, float* dbqkv_p, float* dWo_p, float* dbo, int accumulate,
+                           unsigned flags, void* ws, size_t ws_bytes, tp_stream stream) {
+  if (N < 0 || d < 1 || n_heads < 1 || t < 1 || head_dim < 1) return TP_ERR_INVALID_ARG;
+  if (flags != 0) return TP_ERR_UNSUPPORTED;
+  if (head_dim != 128 || static_cast<int64_t>(n_heads) * head_dim != d || n_heads % t != 0) return TP_ERR_SHAPE;
+  return tp_attn_gqa_backward(dY, X, QKV_save, O_save, lse_save, N, d, n_heads, n_heads, head_dim, t, causal, scale,
+                              Wqkv_p, Wo_p, dX, dWqkv_p, dbqkv_p, dWo_p, dbo, accumulate, flags, ws, ws_bytes, stream);
 }
 
 int tp_abi_version(void) { return TP_ABI_VERSION; }
@@ -534,32 +567,53 @@ tp_status tp_decode_attn_forward(const tp_bf16* x, int64_t B, int64_t d, int n_h
 }
 
 // ------------------------------------------------------------------ attention
+tp_status tp_attn_gqa_forward(const tp_bf16* X, int64_t N, int64_t d, int n_heads, int n_kv_heads, int head_dim,
+                              int t, int causal, float scale, const tp_bf16* Wqkv_p, const tp_bf16* bqkv_p,
+                              const tp_bf16* Wo_p, const tp_bf16* bo, const tp_bf16* residual, tp_bf16* Y,
+                              uint16_t* QKV_save, tp_bf16* O_save, float* lse_save, unsigned flags, void* ws,
+                              size_t ws_bytes, tp_stream stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (N < 0 || d < 1 || n_heads < 1 || n_kv_heads < 1 || t < 1 || head_dim < 1) return TP_ERR_INVALID_ARG;
+  if (flags != 0) return TP_ERR_UNSUPPORTED;
+  if (!gqa_ok(d, n_heads, n_kv_heads, head_dim, t)) return TP_ERR_SHAPE;
+  if (N == 0) return TP_OK;
+  if (!X || !Wqkv_p || !Wo_p || !Y || !QKV_save || !O_save || !lse_save) return TP_ERR_INVALID_ARG;
+  // f (identity) + column-parallel W_qkv by KV group: QKV_i = X W_qkv,i + b_qkv,i, stored fp16.
+  const int64_t rw = qkv_row_width(n_heads, n_kv_heads, head_dim, t);
+  GemmProblem c;
+  c.M = N; c.N = rw; c.K = d; c.nbatch = t;
+  c.a.ptr = X; c.a.ld = d;
+  c.b.ptr = Wqkv_p; c.b.ld = d; c.b.sharded = true; c.b.shard_stride = rw * d;
+  c.epi = EPI_ACT; c.act = TP_ACT_IDENTITY; c.out_f16 = 1;
+  c.d = nullptr; c.d2 = QKV_save; c.ldd = rw; c.d_batch_stride = N * rw;
+  c.bias = bqkv_p; c.bias_batch_stride = rw;
+  TP_RETURN_IF(run_gemm(c, S(stream)));
+  // Attention on each shard's own query heads, no communication.
+  TP_RETURN_IF(run_attention_fwd(QKV_save, N, d, n_heads, n_kv_heads, head_dim, t, causal, scale, O_save, lse_save,
+                                 S(stream)));
+  // Row-parallel W_o + g: Y = sum_i O_i W_o,i + b_o (once) + residual.
+  return tp_row_parallel_forward(O_save, N, d, d, t, Wo_p, bo, residual, Y, stream);
+}
+
 tp_status tp_attn_forward(const tp_bf16* X, int64_t N, int64_t d, int n_heads, int head_dim, int t, int causal,
                           float scale, const tp_bf16* Wqkv_p, const tp_bf16* bqkv_p, const tp_bf16* Wo_p,
                           const tp_bf16* bo, const tp_bf16* residual, tp_bf16* Y, tp_bf16* QKV_save,
                           tp_bf16* O_save, float* lse_save, unsigned flags, void* ws, size_t ws_bytes,
                           tp_stream stream) {
-  (void)ws;
-  (void)ws_bytes;
   if (N < 0 || d < 1 || n_heads < 1 || t < 1 || head_dim < 1) return TP_ERR_INVALID_ARG;
   if (flags != 0) return TP_ERR_UNSUPPORTED;
   if (head_dim != 128 || static_cast<int64_t>(n_heads) * head_dim != d || n_heads % t != 0) return TP_ERR_SHAPE;
-  if (N == 0) return TP_OK;
-  if (!X || !Wqkv_p || !Wo_p || !Y || !QKV_save || !O_save || !lse_save) return TP_ERR_INVALID_ARG;
-  // f (identity) + column-parallel W_qkv by head: QKV_i = X W_qkv,i + b_qkv,i, stored fp16.
-  const int64_t dt = d / t;
-  GemmProblem c;
-  c.M = N; c.N = 3 * dt; c.K = d; c.nbatch = t;
-  c.a.ptr = X; c.a.ld = d;
-  c.b.ptr = Wqkv_p; c.b.ld = d; c.b.sharded = true; c.b.shard_stride = 3 * dt * d;
-  c.epi = EPI_ACT; c.act = TP_ACT_IDENTITY; c.out_f16 = 1;
-  c.d = nullptr; c.d2 = QKV_save; c.ldd = 3 * dt; c.d_batch_stride = N * 3 * dt;
-  c.bias = bqkv_p; c.bias_batch_stride = 3 * dt;
-  TP_RETURN_IF(run_gemm(c, S(stream)));
-  // Attention on each shard's own heads, no communication.
-  TP_RETURN_IF(run_attention_fwd(QKV_save, N, d, n_heads, head_dim, t, causal, scale, O_save, lse_save, S(stream)));
-  // Row-parallel W_o + g: Y = sum_i O_i W_o,i + b_o (once) + residual.
-  return tp_row_parallel_forward(O_save, N, d, d, t, Wo_p, bo, residual, Y, stream);
+  return tp_attn_gqa_forward(X, N, d, n_heads, n_heads, head_dim, t, causal, scale, Wqkv_p, bqkv_p, Wo_p, bo, residual,
+                             Y, QKV_save, O_save, lse_save, flags, ws, ws_bytes, stream);
+}
+
+// Sum of the t shards' packed W_qkv gradients into the unsplit (d, (n_heads + 2 n_kv) head_dim)
+// gradient: every column receives the gradient of each shard copy that holds it, added in
+// shard order (the replica-group all-reduce of a replicated KV head's weights).
+tp_status tp_reduce_qkv_gqa_grad(const float* dWp, int64_t d, int n_heads, int n_kv_heads, int head_dim, int t,
+                                 float* dW, int accumulate, tp_stream stream) {
+  return reduce_qkv_gqa_grad(dWp, d, n_heads, n_kv_heads, head_dim, t, dW, accumulate, S(stream));
 }
 
 // ------------------------------------------------------------------ LayerNorm

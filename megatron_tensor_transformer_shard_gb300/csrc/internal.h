@@ -179,6 +179,9 @@ size_t skinny_part_floats(int64_t R, int B);
 bool skinny_ok(int64_t R, int64_t Kt, int B);
 tp_status run_skinny_gemm(SkGemmJob j, cudaStream_t s);
 
+tp_status reduce_qkv_gqa_grad(const float* dWp, int64_t d, int n_heads, int n_kv, int head_dim, int t, float* dW,
+                              int accumulate, cudaStream_t s);
+
 // decode attention (decode_attn.cu)
 size_t decode_attn_ws_bytes(int64_t B, int64_t d, int n_heads, int n_kv, int head_dim, int t, int64_t L_max);
 tp_status run_decode_attn(const uint16_t* x, int64_t B, int64_t d, int n_heads, int n_kv, int head_dim, int t,
@@ -198,10 +201,12 @@ tp_status run_ln_backward(const uint16_t* dY, const uint16_t* X, const uint16_t*
                           float* dg_part, float* db_part, float* dgamma, float* dbeta, cudaStream_t st);
 
 // attention (attention.cu)
-tp_status run_attention_fwd(const uint16_t* QKV, int64_t N, int64_t d, int n_heads, int head_dim, int t, int causal,
-                            float scale, uint16_t* O, float* lse, cudaStream_t s);
+// n_kv: KV heads (n_kv = n_heads for multi-head attention); QKV rows per shard are
+// [q_t query heads | kv_t K heads | kv_t V heads], 128 columns each.
+tp_status run_attention_fwd(const uint16_t* QKV, int64_t N, int64_t d, int n_heads, int n_kv, int head_dim, int t,
+                            int causal, float scale, uint16_t* O, float* lse, cudaStream_t s);
 tp_status run_attention_bwd(const uint16_t* QKV, const uint16_t* O, const uint16_t* dO, const float* lse, int64_t N,
-                            int64_t d, int n_heads, int head_dim, int t, int causal, float scale, float* Dvec,
+                            int64_t d, int n_heads, int n_kv, int head_dim, int t, int causal, float scale, float* Dvec,
                             uint16_t* dQKV, cudaStream_t s);
 
 }  // namespace tp

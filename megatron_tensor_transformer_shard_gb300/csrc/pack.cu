@@ -263,6 +263,91 @@ tp_status pack_qkv_gqa_bias(const uint16_t* b, int n_heads, int n_kv, int head_d
   return TP_OK;
 }
 
+// Gradient of the unsplit W_qkv from the shards' packed gradients: column c
+// of (d, (n_heads + 2 n_kv) head_dim) sums the packed rows of every shard copy
+// that holds it, in shard order.  32x32 tiles: reads run along d (coalesced in
+// the packed layout), writes along the columns.
+struct GqaGradMap {
+  int n_heads, n_kv, head_dim, t, q_t, kv_t, copies;
+  int64_t d, C, R_t;
+};
+
+// Shard and packed row of copy `cp` of unsplit column c.
+__device__ __forceinline__ void gqa_owner(const GqaGradMap& m, int64_t c, int cp, int& shard, int64_t& row) {
+  const int64_t nq = static_cast<int64_t>(m.n_heads) * m.head_dim;
+  const int64_t nk = static_cast<int64_t>(m.n_kv) * m.head_dim;
+  if (c < nq) {
+    const int64_t qh = c / m.head_dim, e = c - qh * m.head_dim;
+    shard = static_cast<int>(qh / m.q_t);
+    row = (qh - static_cast<int64_t>(shard) * m.q_t) * m.head_dim + e;
+    return;
+  }
+  const int part = c < nq + nk ? 0 : 1;  // K or V
+  const int64_t w = c - nq - part * nk;
+  const int64_t j = w / m.head_dim, e = w - j * m.head_dim;
+  const int64_t base = (static_cast<int64_t>(m.q_t) + part * m.kv_t) * m.head_dim;
+  if (m.n_kv >= m.t) {
+    shard = static_cast<int>(j / m.kv_t);
+    row = base + (j - static_cast<int64_t>(shard) * m.kv_t) * m.head_dim + e;
+  } else {
+    shard = static_cast<int>(j * (m.t / m.n_kv) + cp);
+    row = base + e;
+  }
+}
+
+__global__ void gqa_grad_kernel(GqaGradMap m, const float* __restrict__ dWp, float* __restrict__ dW, int accumulate) {
+  __shared__ float tile[TILE][TILE + 1];
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * TILE, k0 = static_cast<int64_t>(blockIdx.y) * TILE;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  for (int cc = ty; cc < TILE; cc += blockDim.y) {
+    const int64_t c = c0 + cc, k = k0 + tx;
+    if (c < m.C && k < m.d) {
+      const int64_t nq = static_cast<int64_t>(m.n_heads) * m.head_dim;
+      const int ncopy = c < nq ? 1 : m.copies;
+      float acc = 0.0f;
+      for (int cp = 0; cp < ncopy; ++cp) {
+        int shard;
+        int64_t row;
+        gqa_owner(m, c, cp, shard, row);
+        acc += dWp[(static_cast<int64_t>(shard) * m.R_t + row) * m.d + k];
+      }
+      tile[cc][tx] = acc;
+    }
+  }
+  __syncthreads();
+  for (int kk = ty; kk < TILE; kk += blockDim.y) {
+    const int64_t k = k0 + kk, c = c0 + tx;
+    if (c < m.C && k < m.d) {
+      float* o = dW + k * m.C + c;
+      *o = accumulate ? *o + tile[tx][kk] : tile[tx][kk];
+    }
+  }
+}
+
+tp_status reduce_qkv_gqa_grad(const float* dWp, int64_t d, int n_heads, int n_kv, int head_dim, int t, float* dW,
+                              int accumulate, cudaStream_t s) {
+  if (!dWp || !dW || d < 0 || head_dim < 1 || t < 1 || n_heads < 1 || n_kv < 1) return TP_ERR_INVALID_ARG;
+  if (n_heads % t != 0 || n_heads % n_kv != 0 || (n_kv >= t ? n_kv % t != 0 : t % n_kv != 0)) return TP_ERR_SHAPE;
+  GqaGradMap m{};
+  m.n_heads = n_heads;
+  m.n_kv = n_kv;
+  m.head_dim = head_dim;
+  m.t = t;
+  m.q_t = n_heads / t;
+  m.kv_t = n_kv >= t ? n_kv / t : 1;
+  m.copies = n_kv >= t ? 1 : t / n_kv;
+  m.d = d;
+  m.C = static_cast<int64_t>(n_heads + 2 * n_kv) * head_dim;
+  m.R_t = static_cast<int64_t>(m.q_t + 2 * m.kv_t) * head_dim;
+  if (d == 0) return TP_OK;
+  dim3 grid(static_cast<unsigned>((m.C + TILE - 1) / TILE), static_cast<unsigned>((d + TILE - 1) / TILE));
+  if (grid.y > 65535u) return TP_ERR_SHAPE;
+  TP_RETURN_IF(ready());
+  gqa_grad_kernel<<<grid, dim3(TILE, 8), 0, s>>>(m, dWp, dW, accumulate);
+  TP_LAUNCHED();
+  return TP_OK;
+}
+
 tp_status pack_qkv(const uint16_t* src, int64_t d, int n_heads, int head_dim, int t, uint16_t* dst, int dir,
                    cudaStream_t s) {
   if (!src || !dst || d < 0) return TP_ERR_INVALID_ARG;

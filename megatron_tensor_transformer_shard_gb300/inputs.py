@@ -131,6 +131,19 @@ def decode_attn_inputs(B, d, n_heads, n_kv, head_dim, L_max, bias=True, seed=0, 
     return out
 
 
+def gqa_attn_inputs(N, d, n_heads, n_kv, head_dim, bias=True, dy=True, seed=0, device="cpu"):
+    """Grouped-query attention block: Xn (N, d), W_qkv (d, (n_heads + 2 n_kv) head_dim)
+    laid out [Q heads | K heads | V heads], b_qkv, W_o (n_heads head_dim, d), b_o, dY."""
+    g = make_generator(seed, device)
+    nq, nk = n_heads * head_dim, n_kv * head_dim
+    out = {"X": _draw(g, (N, d), 1.0, device), "W_qkv": _draw(g, (d, nq + 2 * nk), WEIGHT_STD, device)}
+    out["b_qkv"] = _draw(g, (nq + 2 * nk,), BIAS_SCALE, device) if bias else None
+    out["W_o"] = _draw(g, (nq, d), WEIGHT_STD, device)
+    out["b_o"] = _draw(g, (d,), BIAS_SCALE, device) if bias else None
+    out["dY"] = _draw(g, (N, d), 1.0, device) if dy else None
+    return out
+
+
 def decode_positions(B, lo, hi, seed=0):
     """Seeded cache positions, uniform on [lo, hi] (a ragged length mix), int32."""
     g = make_generator(seed + 7919, "cpu")
