@@ -19,3 +19,4 @@ differences; there is no "parity unpinned" function.
 
 from .tp_oracle import *  # noqa: F401,F403
 from .tp_gqa_decode import *  # noqa: F401,F403
+from .tp_embedding import *  # noqa: F401,F403
