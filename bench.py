@@ -299,7 +299,8 @@ def run_ours(args):
                      "sp_layer_c5": run_layer_extra(L, torch, args, "c5"),
                      "attention_c5": run_attn_extra(L, torch, args, "c5"),
                      "sp_layernorm_c5": run_ln_extra(L, torch, args, "c5"),
-                     "decode_attention": run_decode_attn_extra(L, torch, args)}
+                     "decode_attention": run_decode_attn_extra(L, torch, args),
+                     "vocab_embedding": run_embedding_extra(L, torch, args)}
 
     if rank != 0:
         return None
@@ -421,6 +422,36 @@ def run_decode_attn_extra(L, torch, args):
                                      "allreduces_per_token_80_layers": 160,
                                      "on_device": "each is the fixed-order shard sum inside the row-parallel "
                                                   "GEMV (W_o here, W_down in the MLP): no extra HBM bytes"}}
+
+
+def run_embedding_extra(L, torch, args):
+    """Vocab-parallel embedding, Llama-3-sized vocabulary: V = 128256, h = 8192,
+    t = 4, 4096 Zipf-distributed token ids.  Forward = gather from the owning
+    shard; backward accumulates into the shards' fp32 gradient rows."""
+    from megatron_tensor_transformer_shard_gb300 import inputs as I
+    N, V, h, t = 4096, 128256, 8192, 4
+    ids = I.token_ids(N, V, seed=0).cuda()
+    inp = I.embedding_inputs(N, V, h, seed=0, device="cuda")
+    Y = torch.empty(N, h, dtype=torch.bfloat16, device="cuda")
+    dE = torch.zeros(V, h, dtype=torch.float32, device="cuda")
+    nws = L.tp_vocab_embedding_backward_workspace_size(N)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    fwd = lambda: (flush.zero_(), L.tp_vocab_embedding_forward(ids, N, V, h, t, inp["E"], Y))
+    bwd = lambda: (flush.zero_(), L.tp_vocab_embedding_backward(ids, inp["dY"], N, V, h, t, dE, 1, ws, nws))
+    fl_ms = _time(torch, flush.zero_, 10)
+    f_ms = _time(torch, fwd, 20) - fl_ms
+    b_ms = _time(torch, bwd, 20) - fl_ms
+    uniq = int(torch.unique(ids).numel())
+    fwd_bytes = 2 * N * h * 2
+    bwd_bytes = N * h * 2 + 2 * uniq * h * 4
+    hbm = measured_peaks()["hbm"]
+    return {"workload": f"vocab-parallel embedding, V={V}, h={h}, t={t}, N={N} Zipf(1.1) token ids ({uniq} distinct)",
+            "l2": "256 MB buffer written between calls (flush)",
+            "fwd_us": round(f_ms * 1e3, 2), "fwd_GBps": round(fwd_bytes / f_ms / 1e6, 1),
+            "fwd_frac_of_hbm": round(fwd_bytes / f_ms / 1e6 / hbm, 4),
+            "bwd_us": round(b_ms * 1e3, 2), "bwd_GBps": round(bwd_bytes / b_ms / 1e6, 1),
+            "bwd_frac_of_hbm": round(bwd_bytes / b_ms / 1e6 / hbm, 4), "bwd_mode": "accumulate into dE"}
 
 
 def run_mlp_fwd_extra(L, torch, args):
@@ -644,6 +675,8 @@ def run_only(args):
         return {"sp_layernorm_c5": run_ln_extra(L, torch, args)}
     if args.only == "dattn":
         return {"decode_attention": run_decode_attn_extra(L, torch, args)}
+    if args.only == "emb":
+        return {"vocab_embedding": run_embedding_extra(L, torch, args)}
     return {f"layer_{args.only}": run_layer_extra(L, torch, args, args.only)}
 
 
@@ -658,9 +691,10 @@ def main():
     p.add_argument("--no-extras", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     p.add_argument("--reference-rows", type=int, default=64, help="token rows per oracle step (--impl reference)")
-    p.add_argument("--only", choices=["c1", "c3", "c4", "c5", "attn", "ln", "dattn"], default=None,
+    p.add_argument("--only", choices=["c1", "c3", "c4", "c5", "attn", "ln", "dattn", "emb"], default=None,
                    help="run only one secondary workload (forward MLP c1, decode c3, layers c4/c5, the c5-shaped "
-                        "attention block, SP LayerNorm, or decode attention over a sharded KV cache) and print it")
+                        "attention block, SP LayerNorm, decode attention over a sharded KV cache or the "
+                        "vocab-parallel embedding) and print it")
     args = p.parse_args()
     if args.warmup < 3:
         args.warmup = 3

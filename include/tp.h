@@ -90,8 +90,8 @@ const char* tp_status_string(tp_status s);
 /* Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns TP_OK, TP_ERR_TIMEOUT (a bounded wait expired), TP_ERR_SHAPE
  * (a kernel found an argument that lives in device memory out of range, e.g.
- * a decode position >= L_max), or TP_ERR_CUDA if the synchronisation itself
- * failed. */
+ * a decode position >= L_max or a token id >= V), or TP_ERR_CUDA if the
+ * synchronisation itself failed. */
 tp_status tp_get_device_status(tp_stream stream);
 
 /* Fault-path self test: launches one CTA that waits on an mbarrier nothing
@@ -338,6 +338,29 @@ tp_status tp_attn_gqa_backward(const tp_bf16* dY, const tp_bf16* X, const uint16
  * != 0 adds to dW.  Src and dst must not overlap. */
 tp_status tp_reduce_qkv_gqa_grad(const float* dWp, int64_t d, int n_heads, int n_kv_heads, int head_dim, int t,
                                  float* dW, int accumulate, tp_stream stream);
+
+/* --------------------------------------------- vocab-parallel embedding
+ * ("Megatron-LM: Tensor Parallelism", "Common Pitfalls" item 5: the embedding
+ * lookup is sharded by vocabulary.)  Shard i owns rows [i V/t, (i+1) V/t) of
+ * E (V, h); the packed table E_p [t][V/t][h] bf16 is E's own row-major layout.
+ * Forward: f hands every shard all ids; shard i's partial is E_p[i][id - i V/t]
+ * for the ids it owns and zero elsewhere; g sums the partials (one of them is
+ * non-zero per token, so the fused sum reads only the owning shard).
+ *   ids [N] int32 (device), 0 <= id < V; Y [N][h] bf16.  V % t == 0,
+ *   V < 2^19, h % 8 == 0.  An id out of range gives a zero row and
+ *   tp_get_device_status() reports TP_ERR_SHAPE.
+ * Backward: g backward hands dY to every shard; shard i adds dY[n] into
+ * dE_p[i][id - i V/t] for every token it owns.  Deterministic: the tokens of a
+ * row are added in token order (chunks of 8192 tokens are sorted by (id, token)
+ * on the device).  dE_p [t][V/t][h] fp32, overwritten (zeroed first) or added
+ * to when accumulate != 0; ws: tp_vocab_embedding_backward_workspace_size(N)
+ * bytes.  The LM head on the same split is the column-parallel GEMM against
+ * E^T (tp_column_parallel_forward); the pages define no loss, none is built. */
+tp_status tp_vocab_embedding_forward(const int32_t* ids, int64_t N, int64_t V, int64_t h, int t, const tp_bf16* E_p,
+                                     tp_bf16* Y, tp_stream stream);
+size_t tp_vocab_embedding_backward_workspace_size(int64_t N);
+tp_status tp_vocab_embedding_backward(const int32_t* ids, const tp_bf16* dY, int64_t N, int64_t V, int64_t h, int t,
+                                      float* dE_p, int accumulate, void* ws, size_t ws_bytes, tp_stream stream);
 
 /* ------------------------------------------- sequence-parallel LayerNorm
  * ("Tensor and sequence parallelism", section "Sequence parallelism";

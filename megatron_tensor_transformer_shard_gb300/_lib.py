@@ -56,6 +56,9 @@ SIGNATURES = {
     "tp_decode_attn_workspace_size": (_SZ, [_I64, _I64, _I, _I, _I, _I, _I64]),
     "tp_decode_attn_forward": (_I, [_P, _I64, _I64, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _P,
                                     _SZ, _P]),
+    "tp_vocab_embedding_forward": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P]),
+    "tp_vocab_embedding_backward_workspace_size": (_SZ, [_I64]),
+    "tp_vocab_embedding_backward": (_I, [_P, _P, _I64, _I64, _I64, _I, _P, _I, _P, _SZ, _P]),
     "tp_sp_layernorm_forward": (_I, [_P, _I64, _I64, _I, _P, _P, _F, _P, _P, _P, _P]),
     "tp_sp_layernorm_backward": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I, _P, _P, _P, _P, _P, _P]),
     "tp_attn_forward": (_I, [_P, _I64, _I64, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _U, _P, _SZ,

@@ -551,6 +551,19 @@ tp_status tp_decode_swiglu_forward(const tp_bf16* x, int64_t M, int64_t h, int64
   return run_decode_swiglu(x, M, h, F, t, Wgu_p, Wdown_p, y, a_save, S(stream));
 }
 
+// ----------------------------------------------------------- vocab embedding
+tp_status tp_vocab_embedding_forward(const int32_t* ids, int64_t N, int64_t V, int64_t h, int t, const tp_bf16* E_p,
+                                     tp_bf16* Y, tp_stream stream) {
+  return run_emb_forward(ids, N, V, h, t, E_p, Y, S(stream));
+}
+
+size_t tp_vocab_embedding_backward_workspace_size(int64_t N) { return N < 0 ? 0 : emb_bwd_ws_bytes(N); }
+
+tp_status tp_vocab_embedding_backward(const int32_t* ids, const tp_bf16* dY, int64_t N, int64_t V, int64_t h, int t,
+                                      float* dE_p, int accumulate, void* ws, size_t ws_bytes, tp_stream stream) {
+  return run_emb_backward(ids, dY, N, V, h, t, dE_p, accumulate, ws, ws_bytes, S(stream));
+}
+
 // ----------------------------------------------------------- decode attention
 size_t tp_decode_attn_workspace_size(int64_t B, int64_t d, int n_heads, int n_kv_heads, int head_dim, int t,
                                      int64_t L_max) {

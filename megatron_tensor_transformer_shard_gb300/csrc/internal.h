@@ -182,6 +182,13 @@ tp_status run_skinny_gemm(SkGemmJob j, cudaStream_t s);
 tp_status reduce_qkv_gqa_grad(const float* dWp, int64_t d, int n_heads, int n_kv, int head_dim, int t, float* dW,
                               int accumulate, cudaStream_t s);
 
+// vocab-parallel embedding (embedding.cu)
+size_t emb_bwd_ws_bytes(int64_t N);
+tp_status run_emb_forward(const int32_t* ids, int64_t N, int64_t V, int64_t h, int t, const uint16_t* E, uint16_t* Y,
+                          cudaStream_t s);
+tp_status run_emb_backward(const int32_t* ids, const uint16_t* dY, int64_t N, int64_t V, int64_t h, int t, float* dE,
+                           int accumulate, void* ws, size_t ws_bytes, cudaStream_t s);
+
 // decode attention (decode_attn.cu)
 size_t decode_attn_ws_bytes(int64_t B, int64_t d, int n_heads, int n_kv, int head_dim, int t, int64_t L_max);
 tp_status run_decode_attn(const uint16_t* x, int64_t B, int64_t d, int n_heads, int n_kv, int head_dim, int t,

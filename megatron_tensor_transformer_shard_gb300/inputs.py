@@ -144,6 +144,24 @@ def gqa_attn_inputs(N, d, n_heads, n_kv, head_dim, bias=True, dy=True, seed=0, d
     return out
 
 
+def token_ids(N, V, zipf_s=1.1, seed=0):
+    """Seeded token ids in [0, V): a Zipf-shaped frequency (rank r drawn with
+    weight r^-s, ranks mapped to ids through a seeded permutation) so that a
+    few ids repeat often, as in text.  int32."""
+    g = make_generator(seed + 104729, "cpu")
+    ranks = torch.arange(1, V + 1, dtype=torch.float64)
+    w = ranks.pow(-zipf_s)
+    r = torch.multinomial(w / w.sum(), N, replacement=True, generator=g)
+    perm = torch.randperm(V, generator=g)
+    return perm[r].to(torch.int32)
+
+
+def embedding_inputs(N, V, h, seed=0, device="cpu"):
+    """E (V, h) ~ N(0, 0.02) and dY (N, h) ~ N(0, 1), bf16, drawn in that order."""
+    g = make_generator(seed, device)
+    return {"E": _draw(g, (V, h), WEIGHT_STD, device), "dY": _draw(g, (N, h), 1.0, device)}
+
+
 def decode_positions(B, lo, hi, seed=0):
     """Seeded cache positions, uniform on [lo, hi] (a ragged length mix), int32."""
     g = make_generator(seed + 7919, "cpu")
