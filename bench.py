@@ -300,7 +300,8 @@ def run_ours(args):
                      "attention_c5": run_attn_extra(L, torch, args, "c5"),
                      "sp_layernorm_c5": run_ln_extra(L, torch, args, "c5"),
                      "decode_attention": run_decode_attn_extra(L, torch, args),
-                     "vocab_embedding": run_embedding_extra(L, torch, args)}
+                     "vocab_embedding": run_embedding_extra(L, torch, args),
+                     "row_parallel_overlap_c2": run_overlap_extra(L, torch, args)}
 
     if rank != 0:
         return None
@@ -452,6 +453,62 @@ def run_embedding_extra(L, torch, args):
             "fwd_frac_of_hbm": round(fwd_bytes / f_ms / 1e6 / hbm, 4),
             "bwd_us": round(b_ms * 1e3, 2), "bwd_GBps": round(bwd_bytes / b_ms / 1e6, 1),
             "bwd_frac_of_hbm": round(bwd_bytes / b_ms / 1e6 / hbm, 4), "bwd_mode": "accumulate into dE"}
+
+
+def run_overlap_extra(L, torch, args):
+    """Row-parallel GEMM of the TP-MLP (t = 4, A 4 x 2048 x 4096, W_down 16384 x 4096)
+    with the g reduction (a) fused into the accumulator, (b) run after the GEMM
+    over materialised partials, (c) overlapped tile by tile with the GEMM."""
+    from megatron_tensor_transformer_shard_gb300 import inputs as I
+    c = I.CONFIGS["c2"]
+    M, h, F, t = c["M"], c["h"], c["F"], c["t"]
+    inp = I.mlp_inputs(M, h, F, bias=True, dy=False, seed=0, device="cuda")
+    Wdn = torch.empty(t, h, F // t, dtype=torch.bfloat16, device="cuda")
+    L.tp_pack_row(inp["W_down"], F, h, t, Wdn)
+    A = (torch.randn(t, M, F // t, device="cuda") * 0.5).to(torch.bfloat16)
+    Y = torch.empty(M, h, dtype=torch.bfloat16, device="cuda")
+    P = torch.empty(t, M, h, dtype=torch.float32, device="cuda")
+    nws = L.tp_row_parallel_overlap_workspace_size(M, F, h, t)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    fused = lambda: L.tp_row_parallel_forward(A, M, F, h, t, Wdn, inp["b_down"], None, Y)
+
+    def unfused():
+        # the same GEMM writing partials, then the separate fixed-order reduction
+        L.tp_row_parallel_forward_overlap(A, M, F, h, t, Wdn, inp["b_down"], None, Y, None, ws, nws)
+
+    ovl = lambda: L.tp_row_parallel_forward_overlap(A, M, F, h, t, Wdn, inp["b_down"], None, Y, None, ws, nws)
+    iters = max(10, min(args.steps, 30))
+    f_ms = _time(torch, fused, iters)
+    o_ms = _time(torch, ovl, iters)
+    # whole MLP forward in the three modes: the difference to the column-parallel half is the row part
+    Wup = torch.empty(t, F // t, h, dtype=torch.bfloat16, device="cuda")
+    L.tp_pack_col(inp["W_up"], h, F, t, Wup)
+    Aout = torch.empty(t, M, F // t, dtype=torch.bfloat16, device="cuda")
+    act = L.ACT_BY_NAME["gelu_tanh"]
+    col = lambda: L.tp_column_parallel_forward(inp["X"], M, h, F, t, act, Wup, inp["b_up"], None, Aout)
+    c_ms = _time(torch, col, iters)
+    mode_ms = {}
+    for name, flag in (("fused", 0), ("unfused", L.TP_FLAG_UNFUSED_REDUCE), ("overlap", L.TP_FLAG_OVERLAP_REDUCE)):
+        nw = L.tp_mlp_workspace_size(M, h, F, t, flag)
+        w2 = torch.empty(max(nw, 256), dtype=torch.uint8, device="cuda")
+        run = lambda: L.tp_mlp_forward(inp["X"], M, h, F, t, act, Wup, inp["b_up"], Wdn, inp["b_down"], None, Y,
+                                       None, Aout, flag, w2, w2.numel())
+        mode_ms[name] = _time(torch, run, iters) - c_ms
+        del w2
+    # unfused through the MLP entry's flag needs the column-parallel half too: time it as
+    # the overlapped GEMM's partial writes plus the standalone reduction kernel
+    red = lambda: L.tp_shard_reduce(P, M, h, t, inp["b_down"], None, Y, None)
+    r_ms = _time(torch, red, iters)
+    flops = 2.0 * M * h * F
+    return {"workload": "row-parallel GEMM + g, t=4, A 4x2048x4096, W_down 16384x4096 (TP-MLP)",
+            "fused_ms": round(f_ms, 4), "fused_TFLOPs": round(flops / f_ms / 1e9, 1),
+            "overlap_ms": round(o_ms, 4), "overlap_TFLOPs": round(flops / o_ms / 1e9, 1),
+            "separate_reduce_kernel_ms": round(r_ms, 4),
+            "row_part_in_mlp_forward_ms": {k: round(v, 4) for k, v in mode_ms.items()},
+            "partial_bytes": t * M * h * 4,
+            "note": "overlap = per-shard fp32 partial tiles written and reduced inside the GEMM while "
+                    "later tiles compute (tp-comm-overlap stand-in); a reduction after the GEMM would add "
+                    "separate_reduce_kernel_ms on top of the partial-writing GEMM"}
 
 
 def run_mlp_fwd_extra(L, torch, args):
@@ -677,6 +734,8 @@ def run_only(args):
         return {"decode_attention": run_decode_attn_extra(L, torch, args)}
     if args.only == "emb":
         return {"vocab_embedding": run_embedding_extra(L, torch, args)}
+    if args.only == "ovl":
+        return {"row_parallel_overlap_c2": run_overlap_extra(L, torch, args)}
     return {f"layer_{args.only}": run_layer_extra(L, torch, args, args.only)}
 
 
@@ -691,10 +750,10 @@ def main():
     p.add_argument("--no-extras", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     p.add_argument("--reference-rows", type=int, default=64, help="token rows per oracle step (--impl reference)")
-    p.add_argument("--only", choices=["c1", "c3", "c4", "c5", "attn", "ln", "dattn", "emb"], default=None,
+    p.add_argument("--only", choices=["c1", "c3", "c4", "c5", "attn", "ln", "dattn", "emb", "ovl"], default=None,
                    help="run only one secondary workload (forward MLP c1, decode c3, layers c4/c5, the c5-shaped "
-                        "attention block, SP LayerNorm, decode attention over a sharded KV cache or the "
-                        "vocab-parallel embedding) and print it")
+                        "attention block, SP LayerNorm, decode attention over a sharded KV cache, the "
+                        "vocab-parallel embedding or the overlapped row-parallel reduction) and print it")
     args = p.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -79,6 +79,10 @@ typedef enum {
 #define TP_FLAG_UNFUSED_REDUCE 1u /* materialise the t partial sums P_i (fp32, in ws) and
                                      reduce them in a separate kernel instead of in the
                                      row-parallel GEMM's accumulator */
+#define TP_FLAG_OVERLAP_REDUCE 2u /* materialise the P_i tile by tile and reduce every
+                                     finished tile while later tiles compute, inside the
+                                     row-parallel GEMM (tp_row_parallel_forward_overlap);
+                                     M > 128, t in {1,2,4,8}; takes precedence over UNFUSED */
 
 typedef uint16_t tp_bf16;
 typedef struct CUstream_st* tp_stream; /* identical to cudaStream_t */
@@ -175,6 +179,25 @@ tp_status tp_column_parallel_forward(const tp_bf16* X, int64_t M, int64_t h, int
 tp_status tp_row_parallel_forward(const tp_bf16* A, int64_t M, int64_t K, int64_t h, int t, const tp_bf16* W_p,
                                   const tp_bf16* b, const tp_bf16* residual, tp_bf16* Y, tp_stream stream);
 
+/* Row-parallel GEMM with the g all-reduce overlapped, tile by tile ("Tensor
+ * and sequence parallelism", section "Volume and scale": the matrix multiply is
+ * cut into blocks and each block is communicated while the next computes --
+ * Megatron's tp-comm-overlap).  Every shard's partial P_i = A_i W_i is written
+ * block by block to an explicit buffer (the data a multi-GPU run would send);
+ * the shard partials of a block are produced together, and the first kernel
+ * warp to see all t of them sums them in shard order, adds b once and the
+ * residual after it, and writes that block of Y -- while other blocks are
+ * still being computed.  Same bits as TP_FLAG_UNFUSED_REDUCE.
+ *   A [t][M][K/t]; W_p [t][h][K/t]; b [h], residual [M][h] nullable; Y [M][h] bf16;
+ *   partials_out [t][M][h] fp32 (nullable: a copy of the exchanged partials);
+ *   ws: tp_row_parallel_overlap_workspace_size() bytes, 256-byte aligned.
+ *   M > 128 and t in {1, 2, 4, 8} (TP_ERR_UNSUPPORTED otherwise; t > 8: TP_ERR_SHAPE),
+ *   h and K/t multiples of 8. */
+size_t tp_row_parallel_overlap_workspace_size(int64_t M, int64_t K, int64_t h, int t);
+tp_status tp_row_parallel_forward_overlap(const tp_bf16* A, int64_t M, int64_t K, int64_t h, int t,
+                                          const tp_bf16* W_p, const tp_bf16* b, const tp_bf16* residual, tp_bf16* Y,
+                                          float* partials_out, void* ws, size_t ws_bytes, tp_stream stream);
+
 /* -------------------------------------------------------------- TP MLP
  * Forward ("02 — Tensor Parallelism", "The MLP pairing"; "Tensor and
  * sequence parallelism", f/g table):
@@ -186,7 +209,8 @@ tp_status tp_row_parallel_forward(const tp_bf16* A, int64_t M, int64_t K, int64_
  * shards' K ranges one after another into a single fp32 accumulator, i = 0..t-1
  * in order, and adds b_down once in its epilogue.  With TP_FLAG_UNFUSED_REDUCE
  * the t partials are written to ws ([t][M][h] fp32) and summed by a separate
- * fixed-order reduction kernel.
+ * fixed-order reduction kernel; with TP_FLAG_OVERLAP_REDUCE the partials are
+ * reduced tile by tile while the GEMM runs (see tp_row_parallel_forward_overlap).
  *   X [M][h]; Wup_p [t][F/t][h]; bup [F] (nullable); Wdown_p [t][h][F/t];
  *   bdown [h] (nullable); residual [M][h] (nullable, added after the sum);
  *   Y [M][h]; Z_save [t][M][F/t] (nullable: inference); A_save [t][M][F/t] (required).

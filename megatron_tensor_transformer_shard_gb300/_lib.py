@@ -23,6 +23,7 @@ TP_ACT_IDENTITY, TP_ACT_RELU, TP_ACT_GELU_TANH, TP_ACT_GELU_ERF, TP_ACT_SWIGLU =
 ACT_BY_NAME = {"identity": TP_ACT_IDENTITY, "relu": TP_ACT_RELU, "gelu_tanh": TP_ACT_GELU_TANH,
                "gelu_erf": TP_ACT_GELU_ERF, "swiglu": TP_ACT_SWIGLU}
 TP_FLAG_UNFUSED_REDUCE = 1
+TP_FLAG_OVERLAP_REDUCE = 2
 
 _P, _I64, _I, _U, _SZ, _F = C.c_void_p, C.c_int64, C.c_int, C.c_uint, C.c_size_t, C.c_float
 
@@ -52,6 +53,8 @@ SIGNATURES = {
     "tp_last_error_detail": (C.c_char_p, []),
     "tp_column_parallel_forward": (_I, [_P, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P, _P]),
     "tp_row_parallel_forward": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _P, _P]),
+    "tp_row_parallel_overlap_workspace_size": (_SZ, [_I64, _I64, _I64, _I]),
+    "tp_row_parallel_forward_overlap": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "tp_decode_swiglu_forward": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _P, _P]),
     "tp_decode_attn_workspace_size": (_SZ, [_I64, _I64, _I, _I, _I, _I, _I64]),
     "tp_decode_attn_forward": (_I, [_P, _I64, _I64, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _P,
@@ -161,4 +164,4 @@ for _name in SIGNATURES:
     globals()[_name] = _make(_name)
 
 __all__ = ["lib", "TPError", "status_string", "SIGNATURES", "LIB_PATH", "ACT_BY_NAME",
-           "TP_FLAG_UNFUSED_REDUCE"] + list(SIGNATURES)
+           "TP_FLAG_UNFUSED_REDUCE", "TP_FLAG_OVERLAP_REDUCE"] + list(SIGNATURES)

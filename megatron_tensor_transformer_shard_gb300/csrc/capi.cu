@@ -373,9 +373,51 @@ tp_status tp_pack_qkv_gqa_bias(const tp_bf16* b, int n_heads, int n_kv_heads, in
 }
 
 // ------------------------------------------------------------------ TP MLP
+// Partials [t][M][h] fp32, then (overlapped reduction) the block counters.
+size_t row_partials_ws(int64_t M, int64_t h, int t, bool overlap) {
+  size_t sz = round_up(static_cast<size_t>(t) * M * h * sizeof(float), 256);
+  if (overlap) sz += round_up(static_cast<size_t>(gemm_overlap_counters(M, h)) * sizeof(int), 256);
+  return sz;
+}
+
 size_t tp_mlp_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned flags) {
   if (M < 0 || h < 0 || F < 0 || t < 1) return 0;
+  if (flags & TP_FLAG_OVERLAP_REDUCE) return row_partials_ws(M, h, t, true);
   return (flags & TP_FLAG_UNFUSED_REDUCE) ? static_cast<size_t>(t) * M * h * sizeof(float) : 0;
+}
+
+size_t tp_row_parallel_overlap_workspace_size(int64_t M, int64_t K, int64_t h, int t) {
+  (void)K;
+  if (M < 0 || h < 0 || t < 1) return 0;
+  return row_partials_ws(M, h, t, true);
+}
+
+tp_status tp_row_parallel_forward_overlap(const tp_bf16* A, int64_t M, int64_t K, int64_t h, int t,
+                                          const tp_bf16* W_p, const tp_bf16* b, const tp_bf16* residual, tp_bf16* Y,
+                                          float* partials_out, void* ws, size_t ws_bytes, tp_stream stream) {
+  if (M < 0 || h < 1 || K < 1 || t < 1) return TP_ERR_INVALID_ARG;
+  if (K % t != 0 || t > 8) return TP_ERR_SHAPE;
+  const int64_t Kt = K / t;
+  if (h % 8 != 0 || Kt % 8 != 0) return TP_ERR_ALIGN;
+  if (M == 0) return TP_OK;
+  if (!A || !W_p || !Y) return TP_ERR_INVALID_ARG;
+  if (M <= 128 || (t & (t - 1)) != 0) return TP_ERR_UNSUPPORTED;  // CTA-pair kernel (M > 128), t in {1, 2, 4, 8}
+  const size_t need = row_partials_ws(M, h, t, true);
+  if (!ws || ws_bytes < need) return TP_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return TP_ERR_ALIGN;
+  float* P = static_cast<float*>(ws);
+  int* cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + round_up(static_cast<size_t>(t) * M * h * 4, 256));
+  GemmProblem r;
+  r.M = M; r.N = h; r.K = Kt; r.nbatch = t; r.nsum = 1;
+  r.a.ptr = A; r.a.ld = Kt; r.a.sharded = true; r.a.shard_stride = M * Kt;
+  r.b.ptr = W_p; r.b.ld = Kt; r.b.sharded = true; r.b.shard_stride = h * Kt;
+  r.epi = EPI_F32; r.d = P; r.ldd = h; r.d_batch_stride = M * h;
+  r.ovl_cnt = cnt; r.ovl_y = Y; r.ovl_bias = b; r.ovl_res = residual; r.ovl_ld = h;
+  TP_RETURN_IF(run_gemm(r, S(stream)));
+  if (partials_out)
+    TP_CUDA_CHECK(cudaMemcpyAsync(partials_out, P, static_cast<size_t>(t) * M * h * sizeof(float),
+                                  cudaMemcpyDeviceToDevice, S(stream)));
+  return TP_OK;
 }
 
 tp_status tp_column_parallel_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t N, int t, tp_act act,
@@ -423,12 +465,17 @@ tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int 
   if (h % 8 != 0 || Ft % 8 != 0) return TP_ERR_ALIGN;
   if (M == 0) return TP_OK;  // no tokens: nothing to compute (buffers may be NULL)
   if (!X || !Wup_p || !Wdown_p || !Y || !A_save) return TP_ERR_INVALID_ARG;
-  const bool unfused = (flags & TP_FLAG_UNFUSED_REDUCE) != 0;
-  if (ws_bytes < tp_mlp_workspace_size(M, h, F, t, flags) || (unfused && !ws)) return TP_ERR_WORKSPACE;
+  const bool overlap = (flags & TP_FLAG_OVERLAP_REDUCE) != 0;
+  const bool unfused = !overlap && (flags & TP_FLAG_UNFUSED_REDUCE) != 0;
+  if (ws_bytes < tp_mlp_workspace_size(M, h, F, t, flags) || ((unfused || overlap) && !ws)) return TP_ERR_WORKSPACE;
+  if (overlap && (M <= 128 || t > 8 || (t & (t - 1)) != 0)) return TP_ERR_UNSUPPORTED;
   const cudaStream_t s = S(stream);
 
   // f (identity) + column-parallel: Z_i = X W_up,i + b_up[C_i]; A_i = act(Z_i).
   TP_RETURN_IF(tp_column_parallel_forward(X, M, h, F, t, act, Wup_p, bup, Z_save, A_save, stream));
+  if (overlap)
+    return tp_row_parallel_forward_overlap(A_save, M, F, h, t, Wdown_p, bdown, residual, Y, nullptr, ws, ws_bytes,
+                                           stream);
 
   // Row-parallel + g: Y = sum_i A_i W_down,i + b_down (once) + residual.
   if (!unfused) return tp_row_parallel_forward(A_save, M, F, h, t, Wdown_p, bdown, residual, Y, stream);

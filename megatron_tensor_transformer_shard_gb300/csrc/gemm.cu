@@ -73,9 +73,37 @@ struct GemmArgs {
   int accumulate;
   int out_f16;
   int tma_store;  // pair kernel: outputs staged in shared memory and written by TMA bulk stores
+  // Overlapped shard reduction (pair kernel, EPI_F32 partials D[b], b = shard): tiles run shard
+  // fastest, and the epilogue warp that stores the last shard's partial of a (tile, CTA half,
+  // warp) block sums the t partials in shard order, adds bias and residual, writes ovl_y bf16.
+  int* ovl_cnt;  // [tile positions][2][4], zero on entry
+  uint16_t* ovl_y;
+  const uint16_t* ovl_bias;
+  const uint16_t* ovl_res;
+  int64_t ovl_ld;
   int* err;
   uint64_t timeout_ns;
 };
+
+// Pair kernel tile numbering: batch slowest normally; batch inside the column
+// block when the shard partials are reduced while later tiles compute (so that
+// a tile position's t partials are produced at about the same time).
+__device__ __forceinline__ void pair_tile(int tile, int mt2, int nt2, int nbatch, bool batch_fastest, int& mb, int& nb,
+                                          int& b) {
+  if (batch_fastest) {
+    // row blocks fastest (neighbouring clusters share the weight panel), then the
+    // shards, then the column blocks: a position's t partials come within one wave
+    mb = tile % mt2;
+    const int rest = tile / mt2;
+    b = rest % nbatch;
+    nb = rest / nbatch;
+  } else {
+    mb = tile % mt2;
+    const int rest = tile / mt2;
+    nb = rest % nt2;
+    b = rest / nt2;
+  }
+}
 
 __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& p, int& b, int& mb, int& nb) {
   mb = tile % p.mt;
@@ -523,7 +551,85 @@ struct PairCfg {
   static constexpr int smem_bytes = 1024 + stages * P_STAGE_BYTES + stg_bytes + BAR_BYTES;
 };
 
-template <bool A_MN, bool B_MN, int EPI, int ACT>
+// Sum of the T shard partials of a 32-row block (rows mrow0.., this lane's 8
+// columns from col) in shard order, then bias once and residual, as bf16 --
+// the same arithmetic, in the same order, as the separate shard reduction.
+// 4 (row, shard) pairs per step (4 / T rows, at least one), 8 float4 loads in
+// flight per lane; deeper unrolling pushes this one kernel into spills.
+template <int T>
+__device__ __forceinline__ void ovl_reduce_block_t(const GemmArgs& p, int mrow0, int64_t col) {
+  constexpr int RPI = (4 / T) > 0 ? (4 / T) : 1;  // rows per step
+  const float* D = static_cast<const float*>(p.d);
+  float bv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (p.ovl_bias) {
+    const uint4 w = *reinterpret_cast<const uint4*>(p.ovl_bias + col);
+    unpack_bf16x2(w.x, bv[0], bv[1]);
+    unpack_bf16x2(w.y, bv[2], bv[3]);
+    unpack_bf16x2(w.z, bv[4], bv[5]);
+    unpack_bf16x2(w.w, bv[6], bv[7]);
+  }
+#pragma unroll 1
+  for (int r0 = 0; r0 < 32; r0 += RPI) {
+    float4 v[RPI][T][2];
+#pragma unroll
+    for (int rr = 0; rr < RPI; ++rr) {
+      const int m = mrow0 + r0 + rr;
+#pragma unroll
+      for (int b = 0; b < T; ++b) {
+        if (r0 + rr < 32 && m < p.M) {
+          const float4* src = reinterpret_cast<const float4*>(D + b * p.d_bs + static_cast<int64_t>(m) * p.ldd + col);
+          v[rr][b][0] = __ldcg(src);
+          v[rr][b][1] = __ldcg(src + 1);
+        }
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < RPI; ++rr) {
+      const int m = mrow0 + r0 + rr;
+      if (r0 + rr >= 32 || m >= p.M) continue;
+      float acc[8];
+      acc[0] = v[rr][0][0].x; acc[1] = v[rr][0][0].y; acc[2] = v[rr][0][0].z; acc[3] = v[rr][0][0].w;
+      acc[4] = v[rr][0][1].x; acc[5] = v[rr][0][1].y; acc[6] = v[rr][0][1].z; acc[7] = v[rr][0][1].w;
+#pragma unroll
+      for (int b = 1; b < T; ++b) {  // fixed shard order
+        acc[0] += v[rr][b][0].x; acc[1] += v[rr][b][0].y; acc[2] += v[rr][b][0].z; acc[3] += v[rr][b][0].w;
+        acc[4] += v[rr][b][1].x; acc[5] += v[rr][b][1].y; acc[6] += v[rr][b][1].z; acc[7] += v[rr][b][1].w;
+      }
+      if (p.ovl_bias) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += bv[e];
+      }
+      if (p.ovl_res) {
+        const uint4 w = *reinterpret_cast<const uint4*>(p.ovl_res + static_cast<int64_t>(m) * p.ovl_ld + col);
+        float rv[8];
+        unpack_bf16x2(w.x, rv[0], rv[1]);
+        unpack_bf16x2(w.y, rv[2], rv[3]);
+        unpack_bf16x2(w.z, rv[4], rv[5]);
+        unpack_bf16x2(w.w, rv[6], rv[7]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += rv[e];
+      }
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(p.ovl_y + static_cast<int64_t>(m) * p.ovl_ld + col) = o;
+    }
+  }
+}
+
+__device__ __forceinline__ void ovl_reduce_block(const GemmArgs& p, int mrow0, int64_t col) {
+  if (col >= p.N) return;
+  switch (p.nbatch) {  // the host admits t = 1, 2, 4, 8
+    case 1: ovl_reduce_block_t<1>(p, mrow0, col); break;
+    case 2: ovl_reduce_block_t<2>(p, mrow0, col); break;
+    case 4: ovl_reduce_block_t<4>(p, mrow0, col); break;
+    default: ovl_reduce_block_t<8>(p, mrow0, col); break;
+  }
+}
+
+template <bool A_MN, bool B_MN, int EPI, int ACT, bool OVL = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
@@ -591,10 +697,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       int issued = 0;
       bool ok = true;
       for (int tile = cluster; ok && tile < total; tile += nclusters) {
-        const int mb = tile % mt2;
-        const int rest = tile / mt2;
-        const int nb = rest % nt2;
-        const int b = rest / nt2;
+        int mb, nb, b;
+        pair_tile(tile, mt2, nt2, p.nbatch, OVL, mb, nb, b);
         const int m0 = mb * 2 * P_HALF + static_cast<int>(rank) * P_HALF;
         const int n0 = nb * P_BN + static_cast<int>(rank) * P_HALF;
         for (int ks = 0; ks < ksteps; ++ks) {
@@ -699,10 +803,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       ptx::tma_prefetch_desc(&tmD2);
     }
     for (int tile = cluster; tile < total; tile += nclusters) {
-      const int mb = tile % mt2;
-      const int rest = tile / mt2;
-      const int nb = rest % nt2;
-      const int b = rest / nt2;
+      int mb, nb, b;
+      pair_tile(tile, mt2, nt2, p.nbatch, OVL, mb, nb, b);
       if (!ptx::mbar_wait_cluster(&tfull[acc], acc_phase, abort_flag, p.err, ERR_WAIT_EPI, p.timeout_ns)) break;
       ptx::tc_fence_after();
       const int mrow0 = mb * 2 * P_HALF + static_cast<int>(rank) * P_HALF + quad * 32;
@@ -764,6 +866,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       ptx::mbar_arrive_cluster(tempty_leader0 + static_cast<uint32_t>(acc * sizeof(uint64_t)));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
+      if constexpr (OVL) {
+        if (mrow0 < p.M) {
+        // The accumulator is already handed back, so the next tile's MMAs run
+        // while this warp counts its partial and, if it was the last shard's,
+        // reduces the block.
+        int last = 0;
+        if (lane == 0) {
+          ptx::bulk_wait_group<0>();  // this warp's partial stores are complete in global memory
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          __threadfence();
+          int* cnt = p.ovl_cnt + ((static_cast<int64_t>(nb) * mt2 + mb) * 2 + rank) * 4 + quad;
+          last = atomicAdd(cnt, 1) == p.nbatch - 1;
+          if (last) __threadfence();
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) ovl_reduce_block(p, mrow0, static_cast<int64_t>(nb) * P_BN + lane * 8);
+        }
+      }
     }
     if (lane == 0) ptx::bulk_wait_group<0>();  // every output written before the CTA exits
   }
@@ -869,11 +989,11 @@ tp_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a
 }
 
 // Clusters of the pair kernel that can be resident at once on this device.
-template <bool A_MN, bool B_MN, int EPI, int ACT>
+template <bool A_MN, bool B_MN, int EPI, int ACT, bool OVL = false>
 int pair_clusters(int dev) {
   static int cached[64] = {};
   if (cached[dev] > 0) return cached[dev];
-  if (cudaFuncSetAttribute(gemm_pair_kernel<A_MN, B_MN, EPI, ACT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(gemm_pair_kernel<A_MN, B_MN, EPI, ACT, OVL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            PairCfg<EPI>::smem_bytes) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
@@ -881,7 +1001,7 @@ int pair_clusters(int dev) {
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = PairCfg<EPI>::smem_bytes;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<A_MN, B_MN, EPI, ACT>, &cfg) != cudaSuccess || n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<A_MN, B_MN, EPI, ACT, OVL>, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
     n = device_sm_count() / 2;
   }
@@ -889,16 +1009,17 @@ int pair_clusters(int dev) {
   return n;
 }
 
-template <bool A_MN, bool B_MN, int EPI, int ACT>
+template <bool A_MN, bool B_MN, int EPI, int ACT, bool OVL = false>
 tp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const CUtensorMap& td2,
                       const GemmArgs& a, int64_t tiles, cudaStream_t s) {
   int dev = 0;
   TP_CUDA_CHECK(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return TP_ERR_CUDA;
-  const int nc = pair_clusters<A_MN, B_MN, EPI, ACT>(dev);
+  const int nc = pair_clusters<A_MN, B_MN, EPI, ACT, OVL>(dev);
   if (nc <= 0) return TP_FAIL_DETAIL("no co-resident CTA pairs");
   const int clusters = static_cast<int>(tiles < nc ? tiles : nc);
-  gemm_pair_kernel<A_MN, B_MN, EPI, ACT><<<2 * clusters, NUM_THREADS, PairCfg<EPI>::smem_bytes, s>>>(ta, tb, td, td2, a);
+  gemm_pair_kernel<A_MN, B_MN, EPI, ACT, OVL>
+      <<<2 * clusters, NUM_THREADS, PairCfg<EPI>::smem_bytes, s>>>(ta, tb, td, td2, a);
   TP_LAUNCHED();
   return TP_OK;
 }
@@ -997,6 +1118,16 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
 
   TP_RETURN_IF(ready());
   const bool pair = use_pair(P.M);
+  if (P.ovl_cnt) {
+    // overlapped reduction: pair kernel, fp32 shard partials written by TMA, t <= 8
+    if (!pair || P.epi != EPI_F32 || P.accumulate || !P.ovl_y) return TP_ERR_UNSUPPORTED;
+    if (P.nbatch != 1 && P.nbatch != 2 && P.nbatch != 4 && P.nbatch != 8) return TP_ERR_UNSUPPORTED;
+    if (!aligned16(P.ovl_y) || P.ovl_ld % 8 != 0 || (P.ovl_bias && !aligned16(P.ovl_bias)) ||
+        (P.ovl_res && !aligned16(P.ovl_res)))
+      return TP_ERR_ALIGN;
+    TP_CUDA_CHECK(
+        cudaMemsetAsync(P.ovl_cnt, 0, static_cast<size_t>(gemm_overlap_counters(P.M, P.N)) * sizeof(int), s));
+  }
   CUtensorMap ta, tb;
   if (!make_operand_map(&ta, P.a, P.M, P.K, nsh_a, BM)) return TP_ERR_CUDA;
   if (!make_operand_map(&tb, P.b, P.N, P.K, nsh_b, pair ? P_HALF : BN)) return TP_ERR_CUDA;
@@ -1026,6 +1157,11 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
   a.ld_res = P.ld_res;
   a.accumulate = P.accumulate;
   a.out_f16 = P.out_f16;
+  a.ovl_cnt = P.ovl_cnt;
+  a.ovl_y = P.ovl_y;
+  a.ovl_bias = P.ovl_bias;
+  a.ovl_res = P.ovl_res;
+  a.ovl_ld = P.ovl_ld;
   a.err = device_error_word();
   a.timeout_ns = wait_timeout_ns();
   if (!a.err) return TP_ERR_CUDA;
@@ -1051,6 +1187,10 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
         return TP_FAIL_DETAIL("tensor map of output D2");
     }
     const int64_t ptiles = ((P.M + 255) / 256) * ((P.N + P_BN - 1) / P_BN) * P.nbatch;
+    if (P.ovl_cnt) {  // its own instantiation: the other kernels keep their registers
+      if (amn || bmn || P.act != TP_ACT_IDENTITY) return TP_ERR_UNSUPPORTED;
+      return launch_pair<false, false, EPI_F32, TP_ACT_IDENTITY, true>(ta, tb, td, td2, a, ptiles, s);
+    }
     return dispatch(amn, bmn, P.epi, P.act, [&](auto am, auto bm, auto ep, auto ac) {
       return launch_pair<decltype(am)::value, decltype(bm)::value, decltype(ep)::value, decltype(ac)::value>(
           ta, tb, td, td2, a, ptiles, s);

@@ -107,7 +107,17 @@ struct GemmProblem {
   int64_t ld_res = 0;
   int accumulate = 0;
   int out_f16 = 0;  // EPI_ACT only: write D / D2 as IEEE fp16 instead of bf16
+  // Overlapped shard reduction (EPI_F32, nbatch = t shard partials D[b]): while later tiles
+  // compute, the t partials of each finished block are summed in shard order, the bias added
+  // once and the residual after it, into ovl_y (bf16, row stride ovl_ld).  ovl_cnt: scratch of
+  // gemm_overlap_counters(M, N) ints (zeroed by the launch).
+  int* ovl_cnt = nullptr;
+  uint16_t* ovl_y = nullptr;
+  const uint16_t* ovl_bias = nullptr;
+  const uint16_t* ovl_res = nullptr;
+  int64_t ovl_ld = 0;
 };
+inline int64_t gemm_overlap_counters(int64_t M, int64_t N) { return ((M + 255) / 256) * ((N + 255) / 256) * 8; }
 
 tp_status run_gemm(const GemmProblem& p, cudaStream_t s);
 
