@@ -551,15 +551,122 @@ struct PairCfg {
   static constexpr int smem_bytes = 1024 + stages * P_STAGE_BYTES + stg_bytes + BAR_BYTES;
 };
 
-// Sum of the T shard partials of a 32-row block (rows mrow0.., this lane's 8
+// Overlapped shard reduction.  Epilogue warps write each tile's fp32 partial;
+// the warp whose partial completes a 32-row block's set of t (the last of the
+// block's counter) posts the block to one job queue in global memory, and the
+// OVL_REDUCERS reducer warps of every CTA take blocks from it (8 rows each)
+// while the tensor cores and epilogue warps go on with later tiles.  Which CTA
+// finishes a block's last shard follows the static tile schedule, so the
+// reductions are shared out through the queue rather than left to the poster.
+// No CTA waits for another's progress: a CTA's reducers stop once its own
+// epilogue warps have signed off and the queue is empty, and the only wait on
+// another CTA is for the ready flag of a claimed entry, whose poster has
+// already taken the slot and is writing it.
+constexpr int OVL_REDUCERS = 4;
+constexpr int OVL_ROWS = 32 / OVL_REDUCERS;               // rows of a block per reducer warp
+constexpr int OVL_THREADS = NUM_THREADS + 32 * OVL_REDUCERS;
+constexpr int OVL_Q_BYTES = 64;  // claimed jobs of the two reducer groups (row, column block, state), sign-offs
+constexpr int OVL_BAR = 2;                                // named barrier of the reducer warps
+enum : int { ERR_WAIT_OVL_READY = 0x105 };
+
+// The queues sit in the counter scratch after the block counters: OVL_NQ
+// heads and OVL_NQ tails, each on its own 128-byte line, then OVL_NQ rings of
+// `cap` entries of 4 ints (first row, column block, ready flag, unused).  A
+// block goes to queue (block id mod OVL_NQ), so `cap` = ceil(blocks / OVL_NQ)
+// always suffices; claimers start at their own queue and take from the others
+// when it is empty, so no single head is fought over by every CTA.
+constexpr int OVL_NQ = 32;
+struct OvlQueue {
+  int* head;  // head of queue i at head[32 * i]
+  int* tail;
+  int4* ent;  // queue i at ent[i * cap]
+  int cap;
+};
+
+__device__ __forceinline__ OvlQueue ovl_queue(const GemmArgs& p, int mt2, int nt2) {
+  int* base = p.ovl_cnt + static_cast<int64_t>(mt2) * nt2 * 8;
+  OvlQueue q;
+  q.head = base;
+  q.tail = base + 32 * OVL_NQ;
+  q.ent = reinterpret_cast<int4*>(base + 64 * OVL_NQ);
+  q.cap = (mt2 * nt2 * 8 + OVL_NQ - 1) / OVL_NQ;
+  return q;
+}
+
+__device__ __forceinline__ int ld_volatile(const int* a) { return *reinterpret_cast<const volatile int*>(a); }
+
+// One lane posts a completed block (block id = its counter's index).
+__device__ __forceinline__ void ovl_post(const OvlQueue& q, int64_t block, int mrow0, int nb) {
+  const int qi = static_cast<int>(block % OVL_NQ);
+  const int slot = atomicAdd(q.tail + 32 * qi, 1);
+  int4* e = q.ent + static_cast<int64_t>(qi) * q.cap + slot;
+  e->x = mrow0;
+  e->y = nb;
+  __threadfence();
+  atomicExch(&e->z, 1);
+}
+
+__device__ __forceinline__ bool ovl_all_empty(const OvlQueue& q) {
+  for (int i = 0; i < OVL_NQ; ++i)
+    if (ld_volatile(q.head + 32 * i) < ld_volatile(q.tail + 32 * i)) return false;
+  return true;
+}
+
+// One lane claims a block: 1 with the block in (row, nb), 0 when this CTA's
+// reducers are finished (own epilogue signed off, every queue drained) or the
+// CTA aborted.
+__device__ __forceinline__ int ovl_claim(const OvlQueue& q, int first, const volatile int* signed_off,
+                                         volatile int* abort_flag, const GemmArgs& p, int& row, int& nb) {
+  unsigned ns = 64;
+  while (true) {
+    for (int i = 0; i < OVL_NQ; ++i) {
+      const int qi = (first + i) % OVL_NQ;
+      int* hp = q.head + 32 * qi;
+      const int h = ld_volatile(hp);
+      if (h >= ld_volatile(q.tail + 32 * qi)) continue;
+      if (atomicCAS(hp, h, h + 1) != h) continue;  // taken by another CTA: try the next queue
+      int4* e = q.ent + static_cast<int64_t>(qi) * q.cap + h;
+      if (atomicAdd(&e->z, 0) == 0) {  // the poster holds the slot and is writing it
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (atomicAdd(&e->z, 0) == 0) {
+          if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+            *abort_flag = 1;
+            if (p.err) atomicCAS(p.err, 0, ERR_WAIT_OVL_READY);
+            return 0;
+          }
+        }
+      }
+      __threadfence();
+      row = ld_volatile(&e->x);
+      nb = ld_volatile(&e->y);
+      return 1;
+    }
+    if (*abort_flag) return 0;
+    if (*signed_off == 4) {  // every block this CTA posted is in a tail by now
+      __threadfence();
+      if (ovl_all_empty(q)) return 0;
+      continue;
+    }
+    __nanosleep(ns);
+    if (ns < 1024) ns *= 2;
+  }
+}
+
+// Sum of the T shard partials of OVL_ROWS rows from mrow0 (this lane's 8
 // columns from col) in shard order, then bias once and residual, as bf16 --
 // the same arithmetic, in the same order, as the separate shard reduction.
-// 4 (row, shard) pairs per step (4 / T rows, at least one), 8 float4 loads in
-// flight per lane; deeper unrolling pushes this one kernel into spills.
+// OVL_PAIRS (row, shard) pairs per step, two float4 loads each, all in flight
+// at once; rows past M load row M-1 (in bounds, never stored) so that no load
+// is predicated and the step stays in registers.
+#ifndef OVL_PAIRS
+#define OVL_PAIRS 8
+#endif
 template <int T>
 __device__ __forceinline__ void ovl_reduce_block_t(const GemmArgs& p, int mrow0, int64_t col) {
-  constexpr int RPI = (4 / T) > 0 ? (4 / T) : 1;  // rows per step
-  const float* D = static_cast<const float*>(p.d);
+  constexpr int RPI_ = (OVL_PAIRS / T) > 0 ? (OVL_PAIRS / T) : 1;
+  constexpr int RPI = RPI_ < OVL_ROWS ? RPI_ : OVL_ROWS;  // rows per step
+  static_assert(OVL_ROWS % RPI == 0, "rows per step must divide the reducer's rows");
+  const float* D = static_cast<const float*>(p.d) + col;
   float bv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (p.ovl_bias) {
     const uint4 w = *reinterpret_cast<const uint4*>(p.ovl_bias + col);
@@ -569,24 +676,23 @@ __device__ __forceinline__ void ovl_reduce_block_t(const GemmArgs& p, int mrow0,
     unpack_bf16x2(w.w, bv[6], bv[7]);
   }
 #pragma unroll 1
-  for (int r0 = 0; r0 < 32; r0 += RPI) {
+  for (int r0 = 0; r0 < OVL_ROWS; r0 += RPI) {
     float4 v[RPI][T][2];
 #pragma unroll
     for (int rr = 0; rr < RPI; ++rr) {
-      const int m = mrow0 + r0 + rr;
+      const int m = min(mrow0 + r0 + rr, p.M - 1);
+      const float* row = D + static_cast<int64_t>(m) * p.ldd;
 #pragma unroll
       for (int b = 0; b < T; ++b) {
-        if (r0 + rr < 32 && m < p.M) {
-          const float4* src = reinterpret_cast<const float4*>(D + b * p.d_bs + static_cast<int64_t>(m) * p.ldd + col);
-          v[rr][b][0] = __ldcg(src);
-          v[rr][b][1] = __ldcg(src + 1);
-        }
+        const float4* src = reinterpret_cast<const float4*>(row + b * p.d_bs);
+        v[rr][b][0] = __ldcs(src);  // read once: evict first
+        v[rr][b][1] = __ldcs(src + 1);
       }
     }
 #pragma unroll
     for (int rr = 0; rr < RPI; ++rr) {
       const int m = mrow0 + r0 + rr;
-      if (r0 + rr >= 32 || m >= p.M) continue;
+      if (m >= p.M) continue;
       float acc[8];
       acc[0] = v[rr][0][0].x; acc[1] = v[rr][0][0].y; acc[2] = v[rr][0][0].z; acc[3] = v[rr][0][0].w;
       acc[4] = v[rr][0][1].x; acc[5] = v[rr][0][1].y; acc[6] = v[rr][0][1].z; acc[7] = v[rr][0][1].w;
@@ -629,8 +735,40 @@ __device__ __forceinline__ void ovl_reduce_block(const GemmArgs& p, int mrow0, i
   }
 }
 
+// The loop of a group of 4 reducer warps (named barrier `bar`): the
+// claimer's lane 0 takes a block, the group sums its 32 rows (8 per warp).
+__device__ __forceinline__ void ovl_reduce_loop(const GemmArgs& p, const OvlQueue& q, volatile int* job,
+                                                const volatile int* signed_off, volatile int* abort_flag,
+                                                bool claimer, int bar, int rrow, int lane) {
+  while (true) {
+    if (claimer && lane == 0) {
+      int row = 0, nb = 0;
+      const int st = ovl_claim(q, static_cast<int>(blockIdx.x) % OVL_NQ, signed_off, abort_flag, p, row, nb);
+      job[0] = row;
+      job[1] = nb;
+      job[2] = st;
+    }
+    __syncwarp();
+    ptx::named_bar_sync(bar, 32 * OVL_REDUCERS);  // the claimed block is visible
+    const int row = job[0], nb = job[1], st = job[2];
+    ptx::named_bar_sync(bar, 32 * OVL_REDUCERS);  // read by all before the next claim
+    if (!st) break;
+    __threadfence();
+    ovl_reduce_block(p, row + rrow, static_cast<int64_t>(nb) * P_BN + lane * 8);
+  }
+}
+
+template <bool OVL>
+constexpr int pair_threads() {
+  return OVL ? OVL_THREADS : NUM_THREADS;
+}
+template <int EPI, bool OVL>
+constexpr int pair_smem_bytes() {
+  return PairCfg<EPI>::smem_bytes + (OVL ? OVL_Q_BYTES : 0);
+}
+
 template <bool A_MN, bool B_MN, int EPI, int ACT, bool OVL = false>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(), 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
                      const GemmArgs p) {
@@ -651,6 +789,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   uint64_t* mma_done = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* ovl_s = reinterpret_cast<volatile int*>(sStage + STG_BYTES + BAR_BYTES);  // OVL launches only
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -669,6 +808,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       ptx::mbar_init(&tempty[a], 256);  // both CTAs' epilogue threads (used in the leader)
     }
     ptx::mbar_init(mma_done, 1);
+    if constexpr (OVL) ovl_s[3] = 0;  // epilogue warps signed off
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -788,6 +928,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       volatile int never = 0;
       ptx::mbar_wait(mma_done, 0, &never, p.err, ERR_WAIT_DRAIN, p.timeout_ns);
     }
+  } else if (OVL && warp >= NUM_THREADS / 32) {
+    // ------------------------------------------------ shard reducers (OVL only)
+    ovl_reduce_loop(p, ovl_queue(p, mt2, nt2), ovl_s, ovl_s + 3, abort_flag, warp == NUM_THREADS / 32, OVL_BAR,
+                    (warp - NUM_THREADS / 32) * OVL_ROWS, lane);
   } else {
     // ----------------------------------------------------------- epilogue (both CTAs)
     const int quad = warp & 3;
@@ -867,25 +1011,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
       if constexpr (OVL) {
-        if (mrow0 < p.M) {
         // The accumulator is already handed back, so the next tile's MMAs run
-        // while this warp counts its partial and, if it was the last shard's,
-        // reduces the block.
-        int last = 0;
+        // while this warp counts its partial and, if it completed the block's
+        // set of shards, queues the block for the reducer warps.
         if (lane == 0) {
-          ptx::bulk_wait_group<0>();  // this warp's partial stores are complete in global memory
-          asm volatile("fence.proxy.async.global;" ::: "memory");
-          __threadfence();
-          int* cnt = p.ovl_cnt + ((static_cast<int64_t>(nb) * mt2 + mb) * 2 + rank) * 4 + quad;
-          last = atomicAdd(cnt, 1) == p.nbatch - 1;
-          if (last) __threadfence();
+          if (mrow0 < p.M) {
+            ptx::bulk_wait_group<0>();  // this warp's partial stores are complete in global memory
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            __threadfence();
+            const int64_t block = ((static_cast<int64_t>(nb) * mt2 + mb) * 2 + rank) * 4 + quad;
+            if (atomicAdd(p.ovl_cnt + block, 1) == p.nbatch - 1) {
+              __threadfence();
+              ovl_post(ovl_queue(p, mt2, nt2), block, mrow0, nb);
+            }
+          }
         }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) ovl_reduce_block(p, mrow0, static_cast<int64_t>(nb) * P_BN + lane * 8);
-        }
+        __syncwarp();
       }
     }
     if (lane == 0) ptx::bulk_wait_group<0>();  // every output written before the CTA exits
+    if constexpr (OVL) {
+      if (lane == 0) {
+        __threadfence();  // this warp's posts are in the queue's tail before it signs off
+        atomicAdd(const_cast<int*>(ovl_s + 3), 1);
+      }
+      __syncwarp();
+      // with its tiles done, the epilogue group becomes a second reducer group
+      ptx::named_bar_sync(OVL_BAR + 1, 128);
+      ovl_reduce_loop(p, ovl_queue(p, mt2, nt2), ovl_s + 4, ovl_s + 3, abort_flag, quad == 0, OVL_BAR + 1,
+                      quad * OVL_ROWS, lane);
+    }
   }
 
   __syncwarp();
@@ -994,12 +1149,12 @@ int pair_clusters(int dev) {
   static int cached[64] = {};
   if (cached[dev] > 0) return cached[dev];
   if (cudaFuncSetAttribute(gemm_pair_kernel<A_MN, B_MN, EPI, ACT, OVL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           PairCfg<EPI>::smem_bytes) != cudaSuccess)
+                           pair_smem_bytes<EPI, OVL>()) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * 256, 1, 1);
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = PairCfg<EPI>::smem_bytes;
+  cfg.blockDim = dim3(pair_threads<OVL>(), 1, 1);
+  cfg.dynamicSmemBytes = pair_smem_bytes<EPI, OVL>();
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<A_MN, B_MN, EPI, ACT, OVL>, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
@@ -1019,7 +1174,7 @@ tp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
   if (nc <= 0) return TP_FAIL_DETAIL("no co-resident CTA pairs");
   const int clusters = static_cast<int>(tiles < nc ? tiles : nc);
   gemm_pair_kernel<A_MN, B_MN, EPI, ACT, OVL>
-      <<<2 * clusters, NUM_THREADS, PairCfg<EPI>::smem_bytes, s>>>(ta, tb, td, td2, a);
+      <<<2 * clusters, pair_threads<OVL>(), pair_smem_bytes<EPI, OVL>(), s>>>(ta, tb, td, td2, a);
   TP_LAUNCHED();
   return TP_OK;
 }

@@ -117,7 +117,13 @@ struct GemmProblem {
   const uint16_t* ovl_res = nullptr;
   int64_t ovl_ld = 0;
 };
-inline int64_t gemm_overlap_counters(int64_t M, int64_t N) { return ((M + 255) / 256) * ((N + 255) / 256) * 8; }
+// Scratch ints of the overlapped reduction: 8 block counters per 256x256
+// output tile, 32 queue heads and 32 tails on 128-byte lines, and 32 rings of
+// ceil(blocks / 32) 4-int entries.
+inline int64_t gemm_overlap_counters(int64_t M, int64_t N) {
+  const int64_t blocks = ((M + 255) / 256) * ((N + 255) / 256) * 8;
+  return blocks + 64 * 32 + 32 * ((blocks + 31) / 32) * 4;
+}
 
 tp_status run_gemm(const GemmProblem& p, cudaStream_t s);
 
