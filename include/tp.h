@@ -183,13 +183,14 @@ tp_status tp_row_parallel_forward(const tp_bf16* A, int64_t M, int64_t K, int64_
  * and sequence parallelism", section "Volume and scale": the matrix multiply is
  * cut into blocks and each block is communicated while the next computes --
  * Megatron's tp-comm-overlap).  Every shard's partial P_i = A_i W_i is written
- * block by block to an explicit buffer (the data a multi-GPU run would send);
- * the shard partials of a block are produced together, and the first kernel
- * warp to see all t of them sums them in shard order, adds b once and the
- * residual after it, and writes that block of Y -- while other blocks are
- * still being computed.  Same bits as TP_FLAG_UNFUSED_REDUCE.
+ * block by block to an explicit fp32 buffer in ws (the data a multi-GPU run
+ * would send); the warp whose partial completes a 32-row block's set of t
+ * queues the block, and reducer warps sum its partials in shard order, add b
+ * once and the residual after it, and write that block of Y -- while other
+ * blocks are still being computed.  Same bits as TP_FLAG_UNFUSED_REDUCE.
  *   A [t][M][K/t]; W_p [t][h][K/t]; b [h], residual [M][h] nullable; Y [M][h] bf16;
- *   partials_out [t][M][h] fp32 (nullable: a copy of the exchanged partials);
+ *   partials_out [t][M][h] fp32 (nullable: receives a copy of the exchanged
+ *   partials after the call);
  *   ws: tp_row_parallel_overlap_workspace_size() bytes, 256-byte aligned.
  *   M > 128 and t in {1, 2, 4, 8} (TP_ERR_UNSUPPORTED otherwise; t > 8: TP_ERR_SHAPE),
  *   h and K/t multiples of 8. */
