@@ -567,12 +567,24 @@ def run_attn_extra(L, torch, args, name="c5"):
     bwd = lambda: L.tp_attn_backward(inp["dY"], inp["X"], QKV, O, lse, N, d, nh, dh, t, 1, sc, Wqkv, Wo, dX, gq, gbq,
                                      go, gbo, 0, 0, ws, nws)
     b_ms = _time(torch, bwd, max(5, min(args.steps, 20)))
+    # The attention core alone (one forward kernel; the backward's three kernels) on the block's own QKV.
+    dO = torch.randn(t, N, d // t, device="cuda").to(torch.float16)
+    Dvec = torch.empty(t, nh // t, N, dtype=f32, device="cuda")
+    dQKV = torch.empty(t, N, 3 * d // t, dtype=bf16, device="cuda")
+    cf_ms = _time(torch, lambda: L.tp_attn_core_forward(QKV, N, d, nh, nh, dh, t, 1, sc, O, lse),
+                  max(5, min(args.steps, 20)))
+    cb_ms = _time(torch, lambda: L.tp_attn_core_backward(QKV, O, dO, lse, N, d, nh, nh, dh, t, 1, sc, Dvec, dQKV),
+                  max(5, min(args.steps, 20)))
     proj = 2.0 * N * d * 3 * d + 2.0 * N * d * d
     core = 2.0 * N * N * d  # causal: QK^T and PV over the unmasked half
+    core_bwd = 2.0 * core   # dV, dP, dQ, dK (the recomputed S counted as the forward's)
     return {"workload": f"attention block, t={t}, N={N}, d={d}, {nh} heads x {dh}, causal",
             "fwd_ms": round(f_ms, 3), "fwd_TFLOPs": round((proj + core) / (f_ms / 1e3) / 1e12, 1),
             "bwd_ms": round(b_ms, 3), "bwd_TFLOPs": round(2 * (proj + core) / (b_ms / 1e3) / 1e12, 1),
-            "flops_fwd": proj + core, "flops_core_fwd": core}
+            "flops_fwd": proj + core, "flops_core_fwd": core,
+            "core_fwd_ms": round(cf_ms, 4), "core_fwd_TFLOPs": round(core / (cf_ms / 1e3) / 1e12, 1),
+            "core_bwd_ms": round(cb_ms, 4), "core_bwd_TFLOPs": round(core_bwd / (cb_ms / 1e3) / 1e12, 1),
+            "core_note": "core FLOPs count the unmasked half only: forward 2*N^2*d (QK^T, PV), backward twice that"}
 
 
 def run_ln_extra(L, torch, args, name="c5"):

@@ -299,8 +299,9 @@ tp_status tp_decode_attn_forward(const tp_bf16* x, int64_t B, int64_t d, int n_h
  * [t][N][d/t] bf16; lse_save [t][H/t][N] fp32 (natural-log log-sum-exp of
  * each scaled score row).  head_dim == 128.
  * flags must be 0 (TP_ERR_UNSUPPORTED otherwise); ws / ws_bytes are unused
- * (pass NULL, 0).  The attention kernel runs one CTA per (head, 128-query
- * block) with an online softmax; no N x N score matrix is ever stored. */
+ * (pass NULL, 0).  The attention kernel runs one CTA per (head, pair of
+ * 128-query tiles) with an online softmax; no N x N score matrix is ever
+ * stored. */
 tp_status tp_attn_forward(const tp_bf16* X, int64_t N, int64_t d, int n_heads, int head_dim, int t, int causal,
                           float scale, const tp_bf16* Wqkv_p, const tp_bf16* bqkv_p, const tp_bf16* Wo_p,
                           const tp_bf16* bo, const tp_bf16* residual, tp_bf16* Y, tp_bf16* QKV_save,
@@ -353,6 +354,25 @@ tp_status tp_attn_gqa_backward(const tp_bf16* dY, const tp_bf16* X, const uint16
                                const tp_bf16* Wo_p, tp_bf16* dX, float* dWqkv_p, float* dbqkv_p, float* dWo_p,
                                float* dbo, int accumulate, unsigned flags, void* ws, size_t ws_bytes,
                                tp_stream stream);
+
+/* The head-local attention core alone, between the two projections ("02 —
+ * Tensor Parallelism", "The attention pairing": each shard's heads run with no
+ * communication).  For callers that form QKV themselves, and for timing the
+ * kernels on their own.
+ * Forward: QKV [t][N][R] IEEE fp16 in the layout of tp_attn_gqa_forward's
+ * QKV_save (R = (n_heads/t + 2 kv_t) * head_dim); writes O [t][N][d/t] bf16 and
+ * lse [t][n_heads/t][N] fp32 (natural log).  One kernel launch.
+ * Backward: dO [t][N][d/t] IEEE fp16, O and lse from the forward; Dvec
+ * [t][n_heads/t][N] fp32 is caller-owned scratch (receives rowsum(dO * O));
+ * writes dQKV [t][N][R] bf16 (every element: dQ, dK and dV of each head).
+ * Three launches: the row dot product, dK/dV per key block, dQ per query block.
+ * Pointers 16-byte aligned (TP_ERR_ALIGN); shape rules of tp_attn_gqa_forward
+ * (TP_ERR_SHAPE); N == 0 is a no-op.  Asynchronous on `stream`. */
+tp_status tp_attn_core_forward(const uint16_t* QKV, int64_t N, int64_t d, int n_heads, int n_kv_heads, int head_dim,
+                               int t, int causal, float scale, tp_bf16* O, float* lse, tp_stream stream);
+tp_status tp_attn_core_backward(const uint16_t* QKV, const tp_bf16* O, const uint16_t* dO, const float* lse,
+                                int64_t N, int64_t d, int n_heads, int n_kv_heads, int head_dim, int t, int causal,
+                                float scale, float* Dvec, tp_bf16* dQKV, tp_stream stream);
 
 /* The replica-group reduction of grouped-query weight gradients: dW (d,
  * (n_heads + 2 n_kv) head_dim) fp32, unsplit layout, gets for every column the

@@ -72,6 +72,8 @@ SIGNATURES = {
     "tp_attn_gqa_backward": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P,
                                   _P, _I, _U, _P, _SZ, _P]),
     "tp_reduce_qkv_gqa_grad": (_I, [_P, _I64, _I, _I, _I, _I, _P, _I, _P]),
+    "tp_attn_core_forward": (_I, [_P, _I64, _I64, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
+    "tp_attn_core_backward": (_I, [_P, _P, _P, _P, _I64, _I64, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "tp_attn_backward_workspace_size": (_SZ, [_I64, _I64, _I, _I, _I, _U]),
     "tp_attn_backward": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _I, _U,
                               _P, _SZ, _P]),

@@ -10,14 +10,17 @@
 // and K (bf16) turns into a ~1% error of P; fp16 keeps 3 more mantissa bits
 // at the same cost.  Inputs, weights and O / dQKV stay bf16.
 //
-// Forward: one CTA per (head, 128-query block), heavy (late) query blocks first.
-//   warp 0      TMA: Q once, then K_j / V_j through a 2-stage ring
-//   warp 1      tcgen05.mma: S_j = Q K_j^T into one of two TMEM S buffers (so
-//               S_{j+1} runs while the softmax works on S_j), then O += P_j V_j
-//               (P from shared memory, V read MN-major straight from its tile)
-//   warps 2-5   one query row per thread: online softmax in the log2 domain,
-//               rescale of the O row in TMEM when the row max moves, P written
-//               bf16 into a 128B-swizzled tile, final O / l and log-sum-exp.
+// Forward: one CTA per (head, pair of adjacent 128-query tiles), heavy (late)
+// pairs first.  The two tiles take turns on the tensor pipe, so one tile's
+// softmax runs while the other tile's MMAs do:
+//   warp 0      TMA: both Q tiles once, then K_j, V_j through a 5-slot ring
+//   warp 1      tcgen05.mma, per key block j: O_0 += P_0 V_j, S_0 = Q_0 K_{j+1}^T,
+//               O_1 += P_1 V_j, S_1 = Q_1 K_{j+1}^T (fp32 S and O in TMEM)
+//   warps 2-5   softmax of tile 0, warps 6-9 of tile 1, one query row per
+//               thread: block max in the log2 domain, a reference max raised
+//               only by a jump of more than 2^8 (then O is rescaled in TMEM),
+//               P written as fp16 over its own S columns in TMEM, where the
+//               P V MMA reads it as the A operand; final O / l and log-sum-exp.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -39,15 +42,18 @@ namespace {
 constexpr int BQ = 128, BKV = 128, HD = 128;
 constexpr int PANEL = 128 * 64 * 2;  // 128 rows x 64 bf16 (one 128-byte swizzle row each)
 constexpr int TILE = 2 * PANEL;      // 128 x 128 bf16
-constexpr int FWD_THREADS = 192;
-constexpr int FWD_SMEM = 1024 + 6 * TILE + 256;
+constexpr int FWD_THREADS = 320;  // TMA warp, MMA warp, two softmax warpgroups
+constexpr int KV_SLOTS = 5;       // K and V tiles share one ring
+constexpr int FWD_SMEM = 1024 + (2 + KV_SLOTS) * TILE + 256;
+constexpr float kLazyRescale = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 enum : int { ERR_ATT_PRODUCER = 0x111, ERR_ATT_MMA = 0x112, ERR_ATT_SOFTMAX = 0x113, ERR_ATT_DRAIN = 0x114 };
 
 struct AttnFwdArgs {
-  int N, H, hpr, nqb, causal;
+  int N, H, hpr, causal;
+  int nsb, nkb;          // pairs of 128-row query tiles; 128-row key blocks
   int Gs;                // query heads of a shard per KV head (1: multi-head)
   int64_t dt;            // width of one shard's Q block (and of its O)
   int64_t kcol0, vcol0;  // first column of the shard's K and V blocks in a QKV row
@@ -67,62 +73,49 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int kk) {
   return ptx::sdesc_sw128(base + kk * 2048, PANEL, 1024);
 }
 
-// Thread `row` writes its 128 bf16 values (packed pairs) into a K-major 128x128 swizzled tile.
-__device__ __forceinline__ void store_row_swizzled(uint8_t* tile, int row, const uint32_t (&w)[64]) {
-#pragma unroll
-  for (int p = 0; p < 2; ++p) {
-    uint8_t* rowp = tile + p * PANEL + row * 128;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      uint4 v = make_uint4(w[p * 32 + c * 4 + 0], w[p * 32 + c * 4 + 1], w[p * 32 + c * 4 + 2],
-                           w[p * 32 + c * 4 + 3]);
-      *reinterpret_cast<uint4*>(rowp + ((c ^ (row & 7)) << 4)) = v;
-    }
-  }
-}
 
+template <bool NEG>
 __global__ void __launch_bounds__(FWD_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const AttnFwdArgs p) {
   extern __shared__ uint8_t dsmem[];
   const uint32_t pad = (1024u - (ptx::smem_addr(dsmem) & 1023u)) & 1023u;
   uint8_t* base = dsmem + pad;
-  uint8_t* sQ = base;
-  uint8_t* sK = base + TILE;      // 2 stages
-  uint8_t* sV = base + 3 * TILE;  // 2 stages
-  uint8_t* sP = base + 5 * TILE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + 6 * TILE);
+  uint8_t* sQ = base;              // two query tiles
+  uint8_t* sKV = base + 2 * TILE;  // ring of KV_SLOTS tiles: K_0, V_0, K_1, V_1, ...
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + (2 + KV_SLOTS) * TILE);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;     // [2]
-  uint64_t* v_full = bars + 3;     // [2]
-  uint64_t* kv_empty = bars + 5;   // [2]
-  uint64_t* s_full = bars + 7;     // [2]
-  uint64_t* s_free = bars + 9;     // [2]
-  uint64_t* p_full = bars + 11;
-  uint64_t* o_done = bars + 12;
-  uint64_t* mma_done = bars + 13;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  uint64_t* kv_full = bars + 1;                 // [KV_SLOTS]
+  uint64_t* kv_empty = bars + 1 + KV_SLOTS;     // [KV_SLOTS]
+  uint64_t* s_full = bars + 1 + 2 * KV_SLOTS;   // [2] S_b ready in TMEM
+  uint64_t* p_full = bars + 3 + 2 * KV_SLOTS;   // [2] P_b written over S_b
+  uint64_t* o_full = bars + 5 + 2 * KV_SLOTS;   // [2] last P_b V done
+  uint64_t* mma_done = bars + 7 + 2 * KV_SLOTS;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 + 2 * KV_SLOTS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int head = blockIdx.x % p.H;
-  const int qb = p.nqb - 1 - static_cast<int>(blockIdx.x / p.H);
+  const int sb = p.nsb - 1 - static_cast<int>(blockIdx.x / p.H);  // heavy (late) query pairs first
   const int shard = head / p.hpr, jj = head - shard * p.hpr;
-  const int nkv = p.causal ? qb + 1 : (p.N + BKV - 1) / BKV;
+  int nkv[2];
+#pragma unroll
+  for (int b = 0; b < 2; ++b) nkv[b] = p.causal ? min(2 * sb + b + 1, p.nkb) : p.nkb;
+  const int nkv_max = nkv[1];  // the later tile sees at least as many key blocks
   const int qcol = jj * HD;
   const int kcol = static_cast<int>(p.kcol0) + (jj / p.Gs) * HD;  // the KV head this query head reads
   const int vcol = static_cast<int>(p.vcol0) + (jj / p.Gs) * HD;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(&k_full[s], 1);
-      ptx::mbar_init(&v_full[s], 1);
+    for (int s = 0; s < KV_SLOTS; ++s) {
+      ptx::mbar_init(&kv_full[s], 1);
       ptx::mbar_init(&kv_empty[s], 1);
-      ptx::mbar_init(&s_full[s], 1);
-      ptx::mbar_init(&s_free[s], 128);
     }
-    ptx::mbar_init(p_full, 128);
-    ptx::mbar_init(o_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&s_full[b], 1);
+      ptx::mbar_init(&p_full[b], 128);
+      ptx::mbar_init(&o_full[b], 1);
+    }
     ptx::mbar_init(mma_done, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -136,170 +129,215 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // TMEM columns: S_0 | S_1 | O_0 | O_1, 128 each.  P_b (fp16 pairs) overwrites the first 64 columns of S_b.
   const uint32_t tS[2] = {tmem, tmem + 128};
-  const uint32_t tO = tmem + 256;
+  const uint32_t tO[2] = {tmem + 256, tmem + 384};
 
   if (warp == 0) {
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tm_qkv);
-      ptx::mbar_arrive_expect_tx(q_full, TILE);
-      ptx::tma_load_3d(sQ, &tm_qkv, q_full, qcol, qb * BQ, shard);
-      ptx::tma_load_3d(sQ + PANEL, &tm_qkv, q_full, qcol + 64, qb * BQ, shard);
+      ptx::mbar_arrive_expect_tx(q_full, 2 * TILE);
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        ptx::tma_load_3d(sQ + b * TILE, &tm_qkv, q_full, qcol, (2 * sb + b) * BQ, shard);
+        ptx::tma_load_3d(sQ + b * TILE + PANEL, &tm_qkv, q_full, qcol + 64, (2 * sb + b) * BQ, shard);
+      }
       int issued = 0;
-      for (int j = 0; j < nkv; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!ptx::mbar_wait(&kv_empty[st], ph ^ 1u, abort_flag, p.err, ERR_ATT_PRODUCER, p.timeout_ns)) break;
-        ptx::mbar_arrive_expect_tx(&k_full[st], TILE);
-        ptx::tma_load_3d(sK + st * TILE, &tm_qkv, &k_full[st], kcol, j * BKV, shard);
-        ptx::tma_load_3d(sK + st * TILE + PANEL, &tm_qkv, &k_full[st], kcol + 64, j * BKV, shard);
-        ptx::mbar_arrive_expect_tx(&v_full[st], TILE);
-        ptx::tma_load_3d(sV + st * TILE, &tm_qkv, &v_full[st], vcol, j * BKV, shard);
-        ptx::tma_load_3d(sV + st * TILE + PANEL, &tm_qkv, &v_full[st], vcol + 64, j * BKV, shard);
+      for (int i = 0; i < 2 * nkv_max; ++i) {
+        const int slot = i % KV_SLOTS;
+        const uint32_t ph = (i / KV_SLOTS) & 1;
+        if (!ptx::mbar_wait(&kv_empty[slot], ph ^ 1u, abort_flag, p.err, ERR_ATT_PRODUCER, p.timeout_ns)) break;
+        const int col = (i & 1) ? vcol : kcol;
+        uint8_t* dst = sKV + slot * TILE;
+        ptx::mbar_arrive_expect_tx(&kv_full[slot], TILE);
+        ptx::tma_load_3d(dst, &tm_qkv, &kv_full[slot], col, (i >> 1) * BKV, shard);
+        ptx::tma_load_3d(dst + PANEL, &tm_qkv, &kv_full[slot], col + 64, (i >> 1) * BKV, shard);
         ++issued;
       }
       // drain: every issued copy must land before the CTA exits
       volatile int never = 0;
       ptx::mbar_wait(q_full, 0, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
-      for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) {
-        const uint32_t ph = (j >> 1) & 1;
-        ptx::mbar_wait(&k_full[j & 1], ph, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
-        ptx::mbar_wait(&v_full[j & 1], ph, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
-      }
+      for (int i = (issued > KV_SLOTS ? issued - KV_SLOTS : 0); i < issued; ++i)
+        ptx::mbar_wait(&kv_full[i % KV_SLOTS], (i / KV_SLOTS) & 1, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc_s = ptx::idesc_f16_f32(BQ, BKV, false, false);
       constexpr uint32_t idesc_o = ptx::idesc_f16_f32(BQ, HD, false, true);
-      const uint32_t aQ = ptx::smem_addr(sQ), aP = ptx::smem_addr(sP);
-      bool ok = ptx::mbar_wait(q_full, 0, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns);
-      for (int j = 0; ok && j <= nkv; ++j) {
-        if (j < nkv) {
-          const int st = j & 1;
-          if (!ptx::mbar_wait(&k_full[st], (j >> 1) & 1, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
-          if (j >= 2 && !ptx::mbar_wait(&s_free[st], ((j >> 1) - 1) & 1, abort_flag, p.err, ERR_ATT_MMA,
-                                        p.timeout_ns))
-            break;
-          ptx::tc_fence_after();
-          const uint32_t aK = ptx::smem_addr(sK + st * TILE);
+      const uint32_t aQ[2] = {ptx::smem_addr(sQ), ptx::smem_addr(sQ + TILE)};
+      const uint32_t aKV = ptx::smem_addr(sKV);
+      auto item_ready = [&](int i) {
+        return ptx::mbar_wait(&kv_full[i % KV_SLOTS], (i / KV_SLOTS) & 1, abort_flag, p.err, ERR_ATT_MMA,
+                              p.timeout_ns);
+      };
+      auto issue_s = [&](int b, uint32_t aK) {
 #pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk)
-            ptx::mma_bf16(tS[st], kmajor_desc(aQ, kk), kmajor_desc(aK, kk), idesc_s, kk > 0 ? 1u : 0u);
-          ptx::mma_commit(&s_full[st]);
-        }
-        if (j >= 1) {
-          const int jp = j - 1, stp = jp & 1;
-          if (!ptx::mbar_wait(p_full, jp & 1, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
-          if (!ptx::mbar_wait(&v_full[stp], (jp >> 1) & 1, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
+        for (int kk = 0; kk < HD / 16; ++kk)
+          ptx::mma_bf16(tS[b], kmajor_desc(aQ[b], kk), kmajor_desc(aK, kk), idesc_s, kk > 0 ? 1u : 0u);
+        ptx::mma_commit(&s_full[b]);
+      };
+      bool ok = ptx::mbar_wait(q_full, 0, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns) && item_ready(0);
+      if (ok) {
+        ptx::tc_fence_after();
+        issue_s(0, aKV);
+        issue_s(1, aKV);
+        ptx::mma_commit(&kv_empty[0]);
+      }
+      // Order per key block j: P_0 V_j, S_0 for block j+1, P_1 V_j, S_1 for block j+1.  A tile's next S
+      // overwrites the columns its P occupies; tcgen05 MMAs of one thread run in issue order, so the
+      // P V that reads them has finished with them first.
+      for (int j = 0; ok && j < nkv_max; ++j) {
+        const int iv = 2 * j + 1, ik = 2 * j + 2;
+        if (!item_ready(iv)) break;
+        bool k_next = false;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          if (j >= nkv[b]) continue;
+          if (!ptx::mbar_wait(&p_full[b], j & 1, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
           ptx::tc_fence_after();
-          const uint32_t aV = ptx::smem_addr(sV + stp * TILE);
+          const uint32_t aV = aKV + (iv % KV_SLOTS) * TILE;
 #pragma unroll
           for (int kk = 0; kk < BKV / 16; ++kk)
-            ptx::mma_bf16(tO, kmajor_desc(aP, kk), mnmajor_desc(aV, kk), idesc_o, (jp > 0 || kk > 0) ? 1u : 0u);
-          ptx::mma_commit(&kv_empty[stp]);
-          ptx::mma_commit(o_done);
+            ptx::mma_f16_ts(tO[b], tS[b] + kk * 8, mnmajor_desc(aV, kk), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+          if (j + 1 < nkv[b]) {
+            if (!k_next) {
+              if (!item_ready(ik)) {
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
+              k_next = true;
+            }
+            issue_s(b, aKV + (ik % KV_SLOTS) * TILE);
+          } else {
+            ptx::mma_commit(&o_full[b]);
+          }
         }
+        if (!ok) break;
+        ptx::mma_commit(&kv_empty[iv % KV_SLOTS]);
+        if (k_next) ptx::mma_commit(&kv_empty[ik % KV_SLOTS]);
       }
       ptx::mma_commit(mma_done);
       volatile int never = 0;
       ptx::mbar_wait(mma_done, 0, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
     }
   } else {
-    // ---------------------------------------------------------- softmax rows
+    // ------------------------------------------------------- softmax rows
+    // Warps 2-5 own query tile 0, warps 6-9 tile 1; a warp reads the TMEM lanes
+    // of its rank within a warpgroup (warp & 3), one query row per thread.
+    const int b = (warp - 2) >> 2;
+    const uint32_t tSb = tmem + 128 * b, tOb = tmem + 256 + 128 * b;  // scalars: no local-memory arrays
+    const int nkv_b = p.causal ? min(2 * sb + b + 1, p.nkb) : p.nkb;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
+    const int qb = 2 * sb + b;
     const int q = qb * BQ + row;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const float sl2 = NEG ? -p.scale_log2 : p.scale_log2;  // > = 0 once S is negated under a negative scale
+    // m is the row's reference maximum (log2 domain).  It is raised only when a
+    // block's maximum exceeds it by more than kLazyRescale, so most blocks skip the
+    // O rescale; P is then at most 2^kLazyRescale, well inside fp16.
     float m = -INFINITY, l = 0.0f;
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      const int sb = j & 1;
-      if (!ptx::mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
+    for (int j = 0; j < nkv_b; ++j) {
+      if (!ptx::mbar_wait(&s_full[b], j & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
-      float s[BKV];
-      {
-        uint32_t r[32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          ptx::tmem_ld32(tS[sb] + lane_base + c * 32, r);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
-        }
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&s_free[sb]);
       const int kv0 = j * BKV;
       const bool edge = (p.causal && j == qb) || (kv0 + BKV > p.N);
-      float mx = -INFINITY;
+      // columns c <= lim are visible to this row (key index kv0 + c)
+      const int lim = (p.causal ? min(q, p.N - 1) : p.N - 1) - kv0;
+      // Pass 1: the block's row maximum, 64 columns at a time (S stays in TMEM,
+      // so a thread never holds the whole row: no register spills).
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < BKV; ++c) {
-        float v = s[c] * p.scale_log2;
-        if (edge) {
-          const int kv = kv0 + c;
-          if (kv >= p.N || (p.causal && kv > q)) v = -INFINITY;
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t r[2][32];
+        ptx::tmem_ld32(tSb + lane_base + hf * 64, r[0]);
+        ptx::tmem_ld32(tSb + lane_base + hf * 64 + 32, r[1]);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          const int c = hf * 64 + e;
+          float v = __uint_as_float(r[e >> 5][e & 31]);
+          if (NEG) v = -v;
+          if (edge && c > lim) v = -INFINITY;
+          mx4[e & 3] = fmaxf(mx4[e & 3], v);
         }
-        s[c] = v;
-        mx = fmaxf(mx, v);
       }
-      const float m_new = fmaxf(m, mx);
-      const float alpha = ptx::exp2_approx(m - m_new);  // 0 on the first block (m = -inf)
-      float rs = 0.0f;
-      uint32_t w[64];
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
+      const float m_new = (mx > m + kLazyRescale) ? mx : m;
+      const float alpha = ptx::exp2_approx(m - m_new);  // 0 on the first block (m = -inf), 1 when m stays
+      if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
+        // O_b is idle: the P V of block j-1 finished before S_b of block j was committed.
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          ptx::tmem_ld32(tOb + lane_base + c * 32, o);
+          ptx::tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < BKV; c += 2) {
-        const float p0 = ptx::exp2_approx(s[c] - m_new);
-        const float p1 = ptx::exp2_approx(s[c + 1] - m_new);
-        rs += p0 + p1;
-        w[c >> 1] = pack_f16x2(p0, p1);
-      }
-      l = l * alpha + rs;
-      m = m_new;
-      if (j >= 1) {
-        // P_{j-1} V_{j-1} must be done before O is rescaled and the P tile is rewritten.
-        if (!ptx::mbar_wait(o_done, (j - 1) & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
-          ok = false;
-          break;
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          ptx::tmem_st32(tOb + lane_base + c * 32, o);
         }
-        ptx::tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha < 1.0f)) {
-          uint32_t r[32];
+      }
+      // Pass 2: P = 2^(S scale - m), 32 columns at a time, written as fp16 pairs
+      // over S's first 64 columns.  Chunk h's P lands in columns [16h, 16h + 16),
+      // which pass 2 has already read (chunks 0 .. h), so nothing is overwritten early.
+      const float neg_m = -m_new;
+      float rs4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            ptx::tmem_ld32(tO + lane_base + c * 32, r);
-            ptx::tmem_ld_wait();
+      for (int h = 0; h < 4; ++h) {
+        uint32_t r[32];
+        ptx::tmem_ld32(tSb + lane_base + h * 32, r);
+        ptx::tmem_ld_wait();
+        uint32_t w[16];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            ptx::tmem_st32(tO + lane_base + c * 32, r);
+        for (int e = 0; e < 16; ++e) {
+          const int c = h * 32 + 2 * e;
+          float s0 = __uint_as_float(r[2 * e]), s1 = __uint_as_float(r[2 * e + 1]);
+          if (NEG) {
+            s0 = -s0;
+            s1 = -s1;
           }
-          ptx::tmem_st_wait();
+          float p0 = ptx::exp2_approx(fmaf(s0, sl2, neg_m));
+          float p1 = ptx::exp2_approx(fmaf(s1, sl2, neg_m));
+          if (edge) {
+            p0 = c <= lim ? p0 : 0.0f;
+            p1 = c + 1 <= lim ? p1 : 0.0f;
+          }
+          rs4[e & 3] += p0 + p1;
+          w[e] = pack_f16x2(p0, p1);
         }
+        ptx::tmem_st16(tSb + lane_base + h * 16, w);
       }
-      store_row_swizzled(sP, row, w);
-      ptx::fence_proxy_async_smem();
+      ptx::tmem_st_wait();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(p_full);
+      ptx::mbar_arrive(&p_full[b]);
+      l = fmaf(l, alpha, (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+      m = m_new;
     }
-    if (ok && ptx::mbar_wait(o_done, (nkv - 1) & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
+    if (ok && ptx::mbar_wait(&o_full[b], 0, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
       ptx::tc_fence_after();
       const float inv_l = 1.0f / l;
       uint16_t* orow = p.O + (static_cast<int64_t>(shard) * p.N + q) * p.dt + qcol;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        ptx::tmem_ld32(tO + lane_base + c * 32, r);
+        uint32_t o[32];
+        ptx::tmem_ld32(tOb + lane_base + c * 32, o);
         ptx::tmem_ld_wait();
         if (q < p.N) {
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(r[e + 0]) * inv_l, __uint_as_float(r[e + 1]) * inv_l);
-            v.y = pack_bf16x2(__uint_as_float(r[e + 2]) * inv_l, __uint_as_float(r[e + 3]) * inv_l);
-            v.z = pack_bf16x2(__uint_as_float(r[e + 4]) * inv_l, __uint_as_float(r[e + 5]) * inv_l);
-            v.w = pack_bf16x2(__uint_as_float(r[e + 6]) * inv_l, __uint_as_float(r[e + 7]) * inv_l);
+            v.x = pack_bf16x2(__uint_as_float(o[e + 0]) * inv_l, __uint_as_float(o[e + 1]) * inv_l);
+            v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l);
+            v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv_l, __uint_as_float(o[e + 5]) * inv_l);
+            v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv_l, __uint_as_float(o[e + 7]) * inv_l);
             *reinterpret_cast<uint4*>(orow + c * 32 + e) = v;
           }
         }
@@ -317,7 +355,6 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     ptx::tmem_dealloc(tmem, 512);
   }
 }
-
 
 // ------------------------------------------------------------------ backward
 //
@@ -805,7 +842,8 @@ tp_status run_attention_fwd(const uint16_t* QKV, int64_t N, int64_t d, int n_hea
   a.N = static_cast<int>(N);
   a.H = n_heads;
   a.hpr = n_heads / t;
-  a.nqb = static_cast<int>((N + BQ - 1) / BQ);
+  a.nkb = static_cast<int>((N + BKV - 1) / BKV);
+  a.nsb = (a.nkb + 1) / 2;
   a.causal = causal ? 1 : 0;
   a.Gs = sh.Gs;
   a.dt = sh.dt;
@@ -821,12 +859,18 @@ tp_status run_attention_fwd(const uint16_t* QKV, int64_t N, int64_t d, int n_hea
   TP_CUDA_CHECK(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return TP_ERR_CUDA;
   if (!configured[dev]) {
-    TP_CUDA_CHECK(cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FWD_SMEM));
+    TP_CUDA_CHECK(
+        cudaFuncSetAttribute(attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, FWD_SMEM));
+    TP_CUDA_CHECK(
+        cudaFuncSetAttribute(attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, FWD_SMEM));
     configured[dev] = true;
   }
-  const int64_t grid = static_cast<int64_t>(n_heads) * a.nqb;
+  const int64_t grid = static_cast<int64_t>(n_heads) * a.nsb;
   if (grid > 0x7fffffff) return TP_ERR_SHAPE;
-  attn_fwd_kernel<<<static_cast<unsigned>(grid), FWD_THREADS, FWD_SMEM, s>>>(map, a);
+  if (a.scale_log2 < 0.0f)
+    attn_fwd_kernel<true><<<static_cast<unsigned>(grid), FWD_THREADS, FWD_SMEM, s>>>(map, a);
+  else
+    attn_fwd_kernel<false><<<static_cast<unsigned>(grid), FWD_THREADS, FWD_SMEM, s>>>(map, a);
   TP_LAUNCHED();
   return TP_OK;
 }

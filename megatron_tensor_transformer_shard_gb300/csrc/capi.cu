@@ -668,6 +668,18 @@ tp_status tp_attn_forward(const tp_bf16* X, int64_t N, int64_t d, int n_heads, i
                              Y, QKV_save, O_save, lse_save, flags, ws, ws_bytes, stream);
 }
 
+tp_status tp_attn_core_forward(const uint16_t* QKV, int64_t N, int64_t d, int n_heads, int n_kv_heads, int head_dim,
+                               int t, int causal, float scale, tp_bf16* O, float* lse, tp_stream stream) {
+  return run_attention_fwd(QKV, N, d, n_heads, n_kv_heads, head_dim, t, causal, scale, O, lse, S(stream));
+}
+
+tp_status tp_attn_core_backward(const uint16_t* QKV, const tp_bf16* O, const uint16_t* dO, const float* lse,
+                                int64_t N, int64_t d, int n_heads, int n_kv_heads, int head_dim, int t, int causal,
+                                float scale, float* Dvec, tp_bf16* dQKV, tp_stream stream) {
+  return run_attention_bwd(QKV, O, dO, lse, N, d, n_heads, n_kv_heads, head_dim, t, causal, scale, Dvec, dQKV,
+                           S(stream));
+}
+
 // Sum of the t shards' packed W_qkv gradients into the unsplit (d, (n_heads + 2 n_kv) head_dim)
 // gradient: every column receives the gradient of each shard copy that holds it, added in
 // shard order (the replica-group all-reduce of a replicated KV head's weights).

@@ -27,7 +27,7 @@ def pack_attn(dev, d, nh, dh, t):
     return Wqkv_p, bqkv_p, Wo_p
 
 
-def run_fwd(N, nh, t, causal, seed=0, dh=128):
+def run_fwd(N, nh, t, causal, seed=0, dh=128, scale=None):
     d = nh * dh
     inp = I.attn_inputs(N, d, bias=True, dy=True, seed=seed)
     dev = {k: v.cuda() for k, v in inp.items()}
@@ -36,7 +36,7 @@ def run_fwd(N, nh, t, causal, seed=0, dh=128):
     QKV = torch.empty(t, N, 3 * d // t, dtype=torch.float16, device="cuda")
     Osv = torch.empty(t, N, d // t, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(t, nh // t, N, dtype=torch.float32, device="cuda")
-    scale = 1.0 / math.sqrt(dh)
+    scale = 1.0 / math.sqrt(dh) if scale is None else scale
     L.tp_attn_forward(dev["X"], N, d, nh, dh, t, int(causal), scale, Wqkv_p, bqkv_p, Wo_p, dev["b_o"], None, Y, QKV,
                       Osv, lse, 0, None, 0)
     torch.cuda.synchronize()
@@ -53,6 +53,21 @@ def test_attention_forward_parity(N, nh, t, causal):
     r = run_fwd(N, nh, t, causal)
     o = r["o"]
     assert_close("QKV", f64(r["QKV"]), np.stack(o["QKV"]))
+    assert_close("O", f64(r["O"]), np.stack(o["O"]))
+    assert_close("lse", f64(r["lse"]).reshape(nh, N), o["lse"])
+    assert_close("Y", f64(r["Y"]), o["Y"])
+
+
+@pytest.mark.parametrize("N,causal,scale", [(384, True, 4.0), (333, False, 4.0), (384, True, -0.5),
+                                            (200, False, -0.5), (256, True, 0.0)])
+def test_attention_forward_scales(N, causal, scale):
+    """Logit spreads far beyond the default scale (the row maximum jumps many
+    times, so O is rescaled often), a negative scale (the largest softmax weight
+    sits at the smallest Q K^T entry) and scale 0 (uniform weights over the
+    visible keys)."""
+    nh, t = 4, 2
+    r = run_fwd(N, nh, t, causal, seed=5, scale=scale)
+    o = r["o"]
     assert_close("O", f64(r["O"]), np.stack(o["O"]))
     assert_close("lse", f64(r["lse"]).reshape(nh, N), o["lse"])
     assert_close("Y", f64(r["Y"]), o["Y"])
@@ -90,3 +105,33 @@ def test_attention_backward_parity(N, nh, t, causal):
     assert_close("db_qkv (packed)", f64(dbqkv), O.pack_qkv_bias(b["db_qkv"], nh, dh, t))
     assert_close("dW_o (packed)", f64(dWo), O.pack_row_weight(b["dW_o"], t))
     assert_close("db_o", f64(dbo), b["db_o"])
+
+
+@pytest.mark.parametrize("N,causal", [(333, True), (256, False)])
+def test_attention_core_entry_points(N, causal):
+    """tp_attn_core_forward / tp_attn_core_backward run the same kernels as the
+    full attention block, so on the block's own saved QKV and dO they must give
+    its O, lse and dQKV bit for bit (those are checked against the oracle above)."""
+    nh, t, dh = 4, 2, 128
+    r = run_fwd(N, nh, t, causal, seed=7)
+    d, dev = r["d"], r["dev"]
+    O2 = torch.empty_like(r["O"])
+    lse2 = torch.empty_like(r["lse"])
+    L.tp_attn_core_forward(r["QKV"], N, d, nh, nh, dh, t, int(causal), r["scale"], O2, lse2)
+    torch.cuda.synchronize()
+    assert torch.equal(O2, r["O"]) and torch.equal(lse2, r["lse"])
+
+    Wqkv_p, _, Wo_p = r["packed"]
+    nws = L.tp_attn_backward_workspace_size(N, d, nh, dh, t, 0)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    L.tp_attn_backward(dev["dY"], dev["X"], r["QKV"], r["O"], r["lse"], N, d, nh, dh, t, int(causal), r["scale"],
+                       Wqkv_p, Wo_p, torch.empty(N, d, dtype=torch.bfloat16, device="cuda"),
+                       torch.empty(t, 3 * d // t, d, dtype=torch.float32, device="cuda"), None,
+                       torch.empty(t, d, d // t, dtype=torch.float32, device="cuda"), None, 0, 0, ws, nws)
+    dO = ws[:N * d * 2].view(torch.float16).view(t, N, d // t)
+    Dvec = torch.empty(t, nh // t, N, dtype=torch.float32, device="cuda")
+    dQKV2 = torch.full((t, N, 3 * d // t), float("nan"), dtype=torch.bfloat16, device="cuda")
+    L.tp_attn_core_backward(r["QKV"], r["O"], dO, r["lse"], N, d, nh, nh, dh, t, int(causal), r["scale"], Dvec, dQKV2)
+    torch.cuda.synchronize()
+    assert L.tp_get_device_status(check=False) == L.TP_OK
+    assert torch.equal(dQKV2, _ws_dqkv(ws, N, d, nh, t))
