@@ -361,19 +361,30 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 // With P = softmax(scale * Q K^T) recomputed from the saved log-sum-exp and
 // D = rowsum(dO * O), the head-local gradients are
 //   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
-// Two kernels, no atomics (deterministic): one CTA per (head, key block) for
-// dK / dV, looping over query blocks; one CTA per (head, query block) for dQ,
-// looping over key blocks.  P and dS are written once into 128B-swizzled
-// tiles with the query index as the row; the same bytes are the K-major A
-// operand of dQ = dS K and the MN-major A operand of dV = P^T dO and
-// dK = dS^T Q, so no transpose is ever materialised.
+// Two kernels, no atomics (deterministic):
+//   dK / dV: one CTA per (KV head, 128-key block), looping over 64-row query
+//     blocks of the group's query heads.  It forms S^T = K Q^T and dP^T = V dO^T
+//     with the keys on the TMEM lanes, so P^T and dS^T (fp16, written over their
+//     own S^T / dP^T columns) are the TMEM A operands of dV += P^T dO and
+//     dK += dS^T Q.
+//   dQ: one CTA per (head, 128-query block), looping over 64-key blocks: S and dP
+//     with the queries on the lanes, dS in TMEM as the A operand of dQ += dS K.
+// S^T / dP^T (S / dP) are double-buffered in TMEM: the MMAs of block n+1 run
+// while eight warps turn block n into P and dS.  Each of those warps reads 32
+// of the 64 columns of its lane quarter and writes its fp16 results into the
+// first half of the columns it read, so k-step kk (16 elements) of such an A
+// operand starts at column 32 (kk / 2) + 8 (kk % 2).
 
-constexpr int BWD_THREADS = 192;
-constexpr int DKV_SMEM = 1024 + 6 * TILE + 256;
-constexpr int DQ_SMEM = 1024 + 7 * TILE + 256;
+constexpr int BWD_THREADS = 320;       // TMA warp, MMA warp, eight compute warps
+constexpr int BWD_STAGES = 4;
+constexpr int PANEL64 = 64 * 64 * 2;   // 64 rows x 64 fp16 (one 128-byte swizzle row each)
+constexpr int TILE64 = 2 * PANEL64;    // 64 x 128 fp16
+constexpr int DKV_SMEM = 1024 + 2 * TILE + BWD_STAGES * (2 * TILE64 + 512) + 256;
+constexpr int DQ_SMEM = 1024 + 2 * TILE + BWD_STAGES * 2 * TILE64 + 256;
 
 struct AttnBwdArgs {
   int N, H, hpr, nqb, causal;
+  int nb64;              // 64-row blocks of the sequence
   int Gs, kv_t, Hkv;     // query heads per KV head in a shard, KV heads per shard, KV heads in all
   int64_t dt;            // width of a shard's Q block (= its O and dO)
   int64_t row_w, kcol0, vcol0;  // QKV row width per shard; first K and V columns
@@ -385,35 +396,51 @@ struct AttnBwdArgs {
   uint64_t timeout_ns;
 };
 
-// Writes 32 consecutive columns (chunk c of 4) of row `row` into a K-major swizzled tile.
-__device__ __forceinline__ void store_chunk_swizzled(uint8_t* tile, int row, int c, const uint32_t (&w)[16]) {
-  uint8_t* rowp = tile + (c >> 1) * PANEL + row * 128;
+// K-major 64-row tile in two 64-column panels: descriptor of MMA k-step kk (16 columns).
+__device__ __forceinline__ uint64_t kmajor64_desc(uint32_t base, int kk) {
+  return ptx::sdesc_sw128(base + (kk >> 2) * PANEL64 + (kk & 3) * 32, 16, 1024);
+}
+// The same tile read MN-major: k-step kk = rows 16 kk .. 16 kk + 15.
+__device__ __forceinline__ uint64_t mnmajor64_desc(uint32_t base, int kk) {
+  return ptx::sdesc_sw128(base + kk * 2048, PANEL64, 1024);
+}
+// TMEM column of k-step kk of an fp16 A operand written by the two column halves.
+__device__ __forceinline__ uint32_t half_split_col(int kk) { return (kk >> 1) * 32 + (kk & 1) * 8; }
+
+// Loads a 128-row, 128-column fp16 tile as four 64 x 64 boxes (same bytes as one 128-row box).
+__device__ __forceinline__ void tma_tile128(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int col, int row,
+                                            int shard) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int ch = (c & 1) * 4 + k;
-    *reinterpret_cast<uint4*>(rowp + ((ch ^ (row & 7)) << 4)) =
-        make_uint4(w[4 * k + 0], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-  }
+  for (int pnl = 0; pnl < 2; ++pnl)
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr)
+      ptx::tma_load_3d(dst + pnl * PANEL + hr * PANEL64, map, bar, col + 64 * pnl, row + 64 * hr, shard);
+}
+// A 64-row, 128-column fp16 tile as two 64 x 64 boxes.
+__device__ __forceinline__ void tma_tile64(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int col, int row,
+                                           int shard) {
+  ptx::tma_load_3d(dst, map, bar, col, row, shard);
+  ptx::tma_load_3d(dst + PANEL64, map, bar, col + 64, row, shard);
 }
 
-// P and dS for 32 columns of one query row; returns them packed as bf16 pairs.
-__device__ __forceinline__ void p_ds_chunk(const uint32_t (&s)[32], const uint32_t (&dp)[32], int q, int kv0,
-                                           const AttnBwdArgs& p, float lse2, float Dq, uint32_t (&wp)[16],
-                                           uint32_t (&wds)[16]) {
+// 64 accumulator columns of this thread's TMEM lane, times `mul`, as bf16 at dst.
+__device__ __forceinline__ void tmem_cols64_to_bf16(uint32_t taddr, float mul, uint16_t* dst, bool write) {
+  uint32_t r[2][32];
+  ptx::tmem_ld32(taddr, r[0]);
+  ptx::tmem_ld32(taddr + 32, r[1]);
+  ptx::tmem_ld_wait();
+  if (!write) return;
 #pragma unroll
-  for (int e = 0; e < 32; e += 2) {
-    float pv[2], dv[2];
+  for (int c = 0; c < 2; ++c)
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int kv = kv0 + e + u;
-      const bool valid = q < p.N && kv < p.N && (!p.causal || kv <= q);
-      const float pr = valid ? ptx::exp2_approx(__uint_as_float(s[e + u]) * p.scale_log2 - lse2) : 0.0f;
-      pv[u] = pr;
-      dv[u] = pr * (__uint_as_float(dp[e + u]) - Dq);
+    for (int e = 0; e < 32; e += 8) {
+      uint4 v;
+      v.x = pack_bf16x2(__uint_as_float(r[c][e + 0]) * mul, __uint_as_float(r[c][e + 1]) * mul);
+      v.y = pack_bf16x2(__uint_as_float(r[c][e + 2]) * mul, __uint_as_float(r[c][e + 3]) * mul);
+      v.z = pack_bf16x2(__uint_as_float(r[c][e + 4]) * mul, __uint_as_float(r[c][e + 5]) * mul);
+      v.w = pack_bf16x2(__uint_as_float(r[c][e + 6]) * mul, __uint_as_float(r[c][e + 7]) * mul);
+      *reinterpret_cast<uint4*>(dst + c * 32 + e) = v;
     }
-    wp[e >> 1] = pack_f16x2(pv[0], pv[1]);
-    wds[e >> 1] = pack_f16x2(dv[0], dv[1]);
-  }
 }
 
 __global__ void attn_bwd_dot_kernel(const uint16_t* __restrict__ dO, const uint16_t* __restrict__ O, int N, int hpr,
@@ -438,27 +465,6 @@ __global__ void attn_bwd_dot_kernel(const uint16_t* __restrict__ dO, const uint1
   if (lane == 0) Dvec[(i * hpr + jj) * N + q] = sum;
 }
 
-// Writes row `grow` (< N) of a 128-column TMEM accumulator, times `mul`, as bf16 at dst.
-__device__ __forceinline__ void tmem_row_to_bf16(uint32_t taddr, float mul, uint16_t* dst, bool write) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t r[32];
-    ptx::tmem_ld32(taddr + c * 32, r);
-    ptx::tmem_ld_wait();
-    if (write) {
-#pragma unroll
-      for (int e = 0; e < 32; e += 8) {
-        uint4 v;
-        v.x = pack_bf16x2(__uint_as_float(r[e + 0]) * mul, __uint_as_float(r[e + 1]) * mul);
-        v.y = pack_bf16x2(__uint_as_float(r[e + 2]) * mul, __uint_as_float(r[e + 3]) * mul);
-        v.z = pack_bf16x2(__uint_as_float(r[e + 4]) * mul, __uint_as_float(r[e + 5]) * mul);
-        v.w = pack_bf16x2(__uint_as_float(r[e + 6]) * mul, __uint_as_float(r[e + 7]) * mul);
-        *reinterpret_cast<uint4*>(dst + c * 32 + e) = v;
-      }
-    }
-  }
-}
-
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
                         const AttnBwdArgs p) {
@@ -467,20 +473,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   uint8_t* base = dsmem + pad;
   uint8_t* sK = base;
   uint8_t* sV = base + TILE;
-  uint8_t* sQ = base + 2 * TILE;
-  uint8_t* sdO = base + 3 * TILE;
-  uint8_t* sP = base + 4 * TILE;
-  uint8_t* sdS = base + 5 * TILE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + 6 * TILE);
+  uint8_t* sQd = base + 2 * TILE;  // stage s: Q_n at s * 2 TILE64, dO_n after it
+  float* sLD = reinterpret_cast<float*>(base + 2 * TILE + BWD_STAGES * 2 * TILE64);  // stage s: lse2[64], D[64]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + 2 * TILE + BWD_STAGES * (2 * TILE64 + 512));
   uint64_t* kv_full = bars + 0;
-  uint64_t* qdo_full = bars + 1;
-  uint64_t* qdo_empty = bars + 2;
-  uint64_t* sdp_full = bars + 3;
-  uint64_t* sdp_free = bars + 4;
-  uint64_t* pds_full = bars + 5;
-  uint64_t* pds_free = bars + 6;
-  uint64_t* mma_done = bars + 7;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
+  uint64_t* qd_full = bars + 1;                    // [BWD_STAGES] TMA bytes + 32 lse/D writers
+  uint64_t* qd_empty = bars + 1 + BWD_STAGES;      // [BWD_STAGES]
+  uint64_t* st_full = bars + 1 + 2 * BWD_STAGES;   // [2] S^T, dP^T of a block in TMEM
+  uint64_t* pds_full = bars + 3 + 2 * BWD_STAGES;  // [2] P^T, dS^T written
+  uint64_t* acc_done = bars + 5 + 2 * BWD_STAGES;
+  uint64_t* mma_done = bars + 6 + 2 * BWD_STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7 + 2 * BWD_STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -490,19 +493,22 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const int kvh = blockIdx.x % p.Hkv;
   const int kb = static_cast<int>(blockIdx.x / p.Hkv);  // early key blocks see the most query blocks (causal)
   const int shard = kvh / p.kv_t, jl = kvh - shard * p.kv_t;
-  const int q_first = p.causal ? kb : 0;
-  const int nq = p.nqb - q_first;
+  const int q_first = p.causal ? 2 * kb : 0;  // first 64-row query block that sees this key block
+  const int nq = p.nb64 - q_first;
   const int nloop = nq * p.Gs;
   const int kcol = static_cast<int>(p.kcol0) + jl * HD, vcol = static_cast<int>(p.vcol0) + jl * HD;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(kv_full, 1);
-    ptx::mbar_init(qdo_full, 1);
-    ptx::mbar_init(qdo_empty, 1);
-    ptx::mbar_init(sdp_full, 1);
-    ptx::mbar_init(sdp_free, 128);
-    ptx::mbar_init(pds_full, 128);
-    ptx::mbar_init(pds_free, 1);
+    for (int s = 0; s < BWD_STAGES; ++s) {
+      ptx::mbar_init(&qd_full[s], 33);
+      ptx::mbar_init(&qd_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&st_full[b], 1);
+      ptx::mbar_init(&pds_full[b], 256);
+    }
+    ptx::mbar_init(acc_done, 1);
     ptx::mbar_init(mma_done, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -512,117 +518,167 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
-  __syncwarp();  // lane-0 roles rejoin their warp: bar.sync needs converged warps
+  __syncwarp();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+  // TMEM columns: S^T_0 | S^T_1 (64 each) | dP^T_0 | dP^T_1 (64 each) | dV (128) | dK (128).
+  const uint32_t tdV = tmem + 256, tdK = tmem + 384;
 
   if (warp == 0) {
+    // Producer warp: lane 0 issues the tile copies, all 32 lanes stage lse2 / D.
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tm_qkv);
       ptx::tma_prefetch_desc(&tm_do);
       ptx::mbar_arrive_expect_tx(kv_full, 2 * TILE);
-      ptx::tma_load_3d(sK, &tm_qkv, kv_full, kcol, kb * BKV, shard);
-      ptx::tma_load_3d(sK + PANEL, &tm_qkv, kv_full, kcol + 64, kb * BKV, shard);
-      ptx::tma_load_3d(sV, &tm_qkv, kv_full, vcol, kb * BKV, shard);
-      ptx::tma_load_3d(sV + PANEL, &tm_qkv, kv_full, vcol + 64, kb * BKV, shard);
-      int issued = 0;
-      for (int n = 0; n < nloop; ++n) {
-        const int g = n / nq, qi = q_first + (n - g * nq);
-        const int qcol = (jl * p.Gs + g) * HD;
-        if (!ptx::mbar_wait(qdo_empty, (n & 1) ^ 1u, abort_flag, p.err, ERR_ATT_PRODUCER, p.timeout_ns)) break;
-        ptx::mbar_arrive_expect_tx(qdo_full, 2 * TILE);
-        ptx::tma_load_3d(sQ, &tm_qkv, qdo_full, qcol, qi * BQ, shard);
-        ptx::tma_load_3d(sQ + PANEL, &tm_qkv, qdo_full, qcol + 64, qi * BQ, shard);
-        ptx::tma_load_3d(sdO, &tm_do, qdo_full, qcol, qi * BQ, shard);
-        ptx::tma_load_3d(sdO + PANEL, &tm_do, qdo_full, qcol + 64, qi * BQ, shard);
-        ++issued;
+      tma_tile128(sK, &tm_qkv, kv_full, kcol, kb * BKV, shard);
+      tma_tile128(sV, &tm_qkv, kv_full, vcol, kb * BKV, shard);
+    }
+    int issued = 0;
+    for (int n = 0; n < nloop; ++n) {
+      const int slot = n % BWD_STAGES;
+      bool ok = true;
+      if (lane == 0)
+        ok = ptx::mbar_wait(&qd_empty[slot], ((n / BWD_STAGES) & 1) ^ 1u, abort_flag, p.err, ERR_ATT_PRODUCER,
+                            p.timeout_ns);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      __syncwarp();
+      const int g = n / nq, qi = q_first + (n - g * nq);
+      const int qh = jl * p.Gs + g;
+      const int q0 = qi * 64;
+      uint8_t* dst = sQd + slot * 2 * TILE64;
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(&qd_full[slot], 2 * TILE64);
+        tma_tile64(dst, &tm_qkv, &qd_full[slot], qh * HD, q0, shard);
+        tma_tile64(dst + TILE64, &tm_do, &qd_full[slot], qh * HD, q0, shard);
       }
+      const int64_t vec = (static_cast<int64_t>(shard) * p.hpr + qh) * p.N;
+      float* ld = sLD + slot * 128;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int idx = lane + 32 * k, q = q0 + idx;
+        // A query row past the end gets lse = +inf: its P and dS are exactly 0.
+        ld[idx] = q < p.N ? p.lse[vec + q] * kLog2e : INFINITY;
+        ld[64 + idx] = q < p.N ? p.Dvec[vec + q] : 0.0f;
+      }
+      ptx::mbar_arrive(&qd_full[slot]);
+      ++issued;
+    }
+    __syncwarp();
+    if (lane == 0) {
       volatile int never = 0;
       ptx::mbar_wait(kv_full, 0, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
-      if (issued > 0) ptx::mbar_wait(qdo_full, (issued - 1) & 1, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
+      for (int n = (issued > BWD_STAGES ? issued - BWD_STAGES : 0); n < issued; ++n)
+        ptx::mbar_wait(&qd_full[n % BWD_STAGES], (n / BWD_STAGES) & 1, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_kk = ptx::idesc_f16_f32(128, 128, false, false);  // S, dP
-      constexpr uint32_t idesc_mm = ptx::idesc_f16_f32(128, 128, true, true);    // dV, dK
-      const uint32_t aK = ptx::smem_addr(sK), aV = ptx::smem_addr(sV), aQ = ptx::smem_addr(sQ);
-      const uint32_t adO = ptx::smem_addr(sdO), aP = ptx::smem_addr(sP), adS = ptx::smem_addr(sdS);
+      constexpr uint32_t idesc_st = ptx::idesc_f16_f32(128, 64, false, false);   // S^T, dP^T
+      constexpr uint32_t idesc_acc = ptx::idesc_f16_f32(128, 128, false, true);  // dV, dK
+      const uint32_t aK = ptx::smem_addr(sK), aV = ptx::smem_addr(sV), aQd = ptx::smem_addr(sQd);
+      auto issue_st = [&](int n) {
+        const int slot = n % BWD_STAGES, b = n & 1;
+        if (!ptx::mbar_wait(&qd_full[slot], (n / BWD_STAGES) & 1, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns))
+          return false;
+        ptx::tc_fence_after();
+        const uint32_t aQ = aQd + slot * 2 * TILE64, adO = aQ + TILE64;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_bf16(tmem + 64 * b, kmajor_desc(aK, kk), kmajor64_desc(aQ, kk), idesc_st, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_bf16(tmem + 128 + 64 * b, kmajor_desc(aV, kk), kmajor64_desc(adO, kk), idesc_st, kk > 0 ? 1u : 0u);
+        ptx::mma_commit(&st_full[b]);
+        return true;
+      };
       bool ok = ptx::mbar_wait(kv_full, 0, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns);
+      if (ok && nloop > 0) ok = issue_st(0);
+      // Block n+1's S^T / dP^T go in before block n's dV / dK: the tensor pipe works on
+      // them while the compute warps form P^T_n and dS^T_n.  Buffer (n+1) & 1 was last
+      // read by the dV / dK MMAs of block n-1, issued (and so executed) before.
       for (int n = 0; ok && n < nloop; ++n) {
-        if (!ptx::mbar_wait(qdo_full, n & 1, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
-        if (n >= 1 && !ptx::mbar_wait(sdp_free, (n - 1) & 1, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
+        if (n + 1 < nloop && !issue_st(n + 1)) break;
+        const int b = n & 1, slot = n % BWD_STAGES;
+        if (!ptx::mbar_wait(&pds_full[b], (n >> 1) & 1, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
         ptx::tc_fence_after();
+        const uint32_t aQ = aQd + slot * 2 * TILE64, adO = aQ + TILE64;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16(tS, kmajor_desc(aQ, kk), kmajor_desc(aK, kk), idesc_kk, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::mma_f16_ts(tdV, tmem + 64 * b + half_split_col(kk), mnmajor64_desc(adO, kk), idesc_acc,
+                          (n > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16(tdP, kmajor_desc(adO, kk), kmajor_desc(aV, kk), idesc_kk, kk > 0 ? 1u : 0u);
-        ptx::mma_commit(sdp_full);
-        if (!ptx::mbar_wait(pds_full, n & 1, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16(tdV, mnmajor_desc(aP, kk), mnmajor_desc(adO, kk), idesc_mm, (n > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16(tdK, mnmajor_desc(adS, kk), mnmajor_desc(aQ, kk), idesc_mm, (n > 0 || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(pds_free);
-        ptx::mma_commit(qdo_empty);
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::mma_f16_ts(tdK, tmem + 128 + 64 * b + half_split_col(kk), mnmajor64_desc(aQ, kk), idesc_acc,
+                          (n > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(&qd_empty[slot]);
       }
+      ptx::mma_commit(acc_done);
       ptx::mma_commit(mma_done);
       volatile int never = 0;
       ptx::mbar_wait(mma_done, 0, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
     }
   } else {
-    const int quad = warp & 3;
+    // Compute warps: lane quarter warp & 3 (key rows), column half h of each 64-query block.
+    const int quad = warp & 3, h = (warp - 2) >> 2;
     const int row = quad * 32 + lane;
+    const int kv = kb * BKV + row;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const float sl2 = p.scale_log2;
     bool ok = true;
     for (int n = 0; n < nloop; ++n) {
-      const int g = n / nq;
-      const int64_t vec_base = (static_cast<int64_t>(shard) * p.hpr + jl * p.Gs + g) * p.N;
-      const int q = (q_first + (n - g * nq)) * BQ + row;
-      const float lse2 = q < p.N ? p.lse[vec_base + q] * kLog2e : 0.0f;
-      const float Dq = q < p.N ? p.Dvec[vec_base + q] : 0.0f;
-      if (!ptx::mbar_wait(sdp_full, n & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
-        ok = false;
-        break;
-      }
-      if (n >= 1 && !ptx::mbar_wait(pds_free, (n - 1) & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
+      const int b = n & 1, slot = n % BWD_STAGES;
+      if (!ptx::mbar_wait(&st_full[b], (n >> 1) & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns) ||
+          !ptx::mbar_wait(&qd_full[slot], (n / BWD_STAGES) & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t s[32], dp[32], wp[16], wds[16];
-        ptx::tmem_ld32(tS + lane_base + c * 32, s);
-        ptx::tmem_ld32(tdP + lane_base + c * 32, dp);
-        ptx::tmem_ld_wait();
-        p_ds_chunk(s, dp, q, kb * BKV + c * 32, p, lse2, Dq, wp, wds);
-        store_chunk_swizzled(sP, row, c, wp);
-        store_chunk_swizzled(sdS, row, c, wds);
+      const uint32_t tSb = tmem + 64 * b + lane_base + 32 * h, tdPb = tSb + 128;
+      uint32_t s[32], dp[32];
+      ptx::tmem_ld32(tSb, s);
+      ptx::tmem_ld32(tdPb, dp);
+      ptx::tmem_ld_wait();
+      const int g = n / nq, qi = q_first + (n - g * nq);
+      const int c0 = qi * 64 + 32 * h;  // query index of column 0 of this half
+      // causal: query c0 + e sees key kv only if kv <= c0 + e
+      const bool edge = p.causal && c0 < kv;
+      const float4* l2 = reinterpret_cast<const float4*>(sLD + slot * 128 + 32 * h);
+      const float4* dd = reinterpret_cast<const float4*>(sLD + slot * 128 + 64 + 32 * h);
+      uint32_t wp[16], wds[16];
+#pragma unroll
+      for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 L4 = l2[e4], D4 = dd[e4];
+        const float Lv[4] = {L4.x, L4.y, L4.z, L4.w}, Dv[4] = {D4.x, D4.y, D4.z, D4.w};
+        float pv[4], dv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = 4 * e4 + u;
+          float pr = ptx::exp2_approx(fmaf(__uint_as_float(s[e]), sl2, -Lv[u]));
+          if (edge && c0 + e < kv) pr = 0.0f;
+          pv[u] = pr;
+          dv[u] = pr * (__uint_as_float(dp[e]) - Dv[u]);
+        }
+        wp[2 * e4] = pack_f16x2(pv[0], pv[1]);
+        wp[2 * e4 + 1] = pack_f16x2(pv[2], pv[3]);
+        wds[2 * e4] = pack_f16x2(dv[0], dv[1]);
+        wds[2 * e4 + 1] = pack_f16x2(dv[2], dv[3]);
       }
+      ptx::tmem_st16(tSb, wp);
+      ptx::tmem_st16(tdPb, wds);
+      ptx::tmem_st_wait();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(sdp_free);
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(pds_full);
+      ptx::mbar_arrive(&pds_full[b]);
     }
-    if (ok && nloop > 0 &&
-        ptx::mbar_wait(pds_free, (nloop - 1) & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
+    if (ok && ptx::mbar_wait(acc_done, 0, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
       ptx::tc_fence_after();
-      const int kvrow = kb * BKV + row;  // accumulator rows are key rows
-      uint16_t* drow = p.dQKV + (static_cast<int64_t>(shard) * p.N + kvrow) * p.row_w;
-      tmem_row_to_bf16(tdV + lane_base, 1.0f, drow + vcol, kvrow < p.N);
-      tmem_row_to_bf16(tdK + lane_base, p.scale, drow + kcol, kvrow < p.N);
+      uint16_t* drow = p.dQKV + (static_cast<int64_t>(shard) * p.N + kv) * p.row_w;
+      tmem_cols64_to_bf16(tdV + lane_base + 64 * h, 1.0f, drow + vcol + 64 * h, kv < p.N);
+      tmem_cols64_to_bf16(tdK + lane_base + 64 * h, p.scale, drow + kcol + 64 * h, kv < p.N);
     }
   }
 
   ptx::tc_fence_before();
-  __syncwarp();  // lane-0 roles rejoin their warp: bar.sync needs converged warps
+  __syncwarp();
   __syncthreads();
   if (warp == 1) {
     __syncwarp();
@@ -639,41 +695,37 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   uint8_t* base = dsmem + pad;
   uint8_t* sQ = base;
   uint8_t* sdO = base + TILE;
-  uint8_t* sK = base + 2 * TILE;  // 2 stages
-  uint8_t* sV = base + 4 * TILE;  // 2 stages
-  uint8_t* sdS = base + 6 * TILE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + 7 * TILE);
-  uint64_t* qdo_full = bars + 0;
-  uint64_t* k_full = bars + 1;    // [2]
-  uint64_t* v_full = bars + 3;    // [2]
-  uint64_t* kv_empty = bars + 5;  // [2]
-  uint64_t* sdp_full = bars + 7;
-  uint64_t* sdp_free = bars + 8;
-  uint64_t* ds_full = bars + 9;
-  uint64_t* ds_free = bars + 10;
-  uint64_t* mma_done = bars + 11;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  uint8_t* sKV = base + 2 * TILE;  // stage s: K_j at s * 2 TILE64, V_j after it
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + 2 * TILE + BWD_STAGES * 2 * TILE64);
+  uint64_t* q_full = bars + 0;
+  uint64_t* kv_full = bars + 1;                    // [BWD_STAGES]
+  uint64_t* kv_empty = bars + 1 + BWD_STAGES;      // [BWD_STAGES]
+  uint64_t* s_full = bars + 1 + 2 * BWD_STAGES;    // [2] S, dP of a key block in TMEM
+  uint64_t* ds_full = bars + 3 + 2 * BWD_STAGES;   // [2] dS written
+  uint64_t* acc_done = bars + 5 + 2 * BWD_STAGES;
+  uint64_t* mma_done = bars + 6 + 2 * BWD_STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7 + 2 * BWD_STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int head = blockIdx.x % p.H;
-  const int qb = p.nqb - 1 - static_cast<int>(blockIdx.x / p.H);
+  const int qb = p.nqb - 1 - static_cast<int>(blockIdx.x / p.H);  // heavy (late) query blocks first
   const int shard = head / p.hpr, jj = head - shard * p.hpr;
-  const int nkv = p.causal ? qb + 1 : (p.N + BKV - 1) / BKV;
+  const int nkv = p.causal ? min(2 * qb + 2, p.nb64) : p.nb64;   // 64-key blocks this query block sees
   const int qcol = jj * HD;
   const int kcol = static_cast<int>(p.kcol0) + (jj / p.Gs) * HD, vcol = static_cast<int>(p.vcol0) + (jj / p.Gs) * HD;
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(qdo_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(&k_full[s], 1);
-      ptx::mbar_init(&v_full[s], 1);
+    ptx::mbar_init(q_full, 1);
+    for (int s = 0; s < BWD_STAGES; ++s) {
+      ptx::mbar_init(&kv_full[s], 1);
       ptx::mbar_init(&kv_empty[s], 1);
     }
-    ptx::mbar_init(sdp_full, 1);
-    ptx::mbar_init(sdp_free, 128);
-    ptx::mbar_init(ds_full, 128);
-    ptx::mbar_init(ds_free, 1);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&s_full[b], 1);
+      ptx::mbar_init(&ds_full[b], 256);
+    }
+    ptx::mbar_init(acc_done, 1);
     ptx::mbar_init(mma_done, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -683,117 +735,129 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
-  __syncwarp();  // lane-0 roles rejoin their warp: bar.sync needs converged warps
+  __syncwarp();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256;
+  // TMEM columns: S_0 | S_1 (64 each) | dP_0 | dP_1 (64 each) | dQ (128).
+  const uint32_t tdQ = tmem + 256;
 
   if (warp == 0) {
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tm_qkv);
       ptx::tma_prefetch_desc(&tm_do);
-      ptx::mbar_arrive_expect_tx(qdo_full, 2 * TILE);
-      ptx::tma_load_3d(sQ, &tm_qkv, qdo_full, qcol, qb * BQ, shard);
-      ptx::tma_load_3d(sQ + PANEL, &tm_qkv, qdo_full, qcol + 64, qb * BQ, shard);
-      ptx::tma_load_3d(sdO, &tm_do, qdo_full, jj * HD, qb * BQ, shard);
-      ptx::tma_load_3d(sdO + PANEL, &tm_do, qdo_full, jj * HD + 64, qb * BQ, shard);
+      ptx::mbar_arrive_expect_tx(q_full, 2 * TILE);
+      tma_tile128(sQ, &tm_qkv, q_full, qcol, qb * BQ, shard);
+      tma_tile128(sdO, &tm_do, q_full, jj * HD, qb * BQ, shard);
       int issued = 0;
       for (int j = 0; j < nkv; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!ptx::mbar_wait(&kv_empty[st], ph ^ 1u, abort_flag, p.err, ERR_ATT_PRODUCER, p.timeout_ns)) break;
-        ptx::mbar_arrive_expect_tx(&k_full[st], TILE);
-        ptx::tma_load_3d(sK + st * TILE, &tm_qkv, &k_full[st], kcol, j * BKV, shard);
-        ptx::tma_load_3d(sK + st * TILE + PANEL, &tm_qkv, &k_full[st], kcol + 64, j * BKV, shard);
-        ptx::mbar_arrive_expect_tx(&v_full[st], TILE);
-        ptx::tma_load_3d(sV + st * TILE, &tm_qkv, &v_full[st], vcol, j * BKV, shard);
-        ptx::tma_load_3d(sV + st * TILE + PANEL, &tm_qkv, &v_full[st], vcol + 64, j * BKV, shard);
+        const int slot = j % BWD_STAGES;
+        if (!ptx::mbar_wait(&kv_empty[slot], ((j / BWD_STAGES) & 1) ^ 1u, abort_flag, p.err, ERR_ATT_PRODUCER,
+                            p.timeout_ns))
+          break;
+        uint8_t* dst = sKV + slot * 2 * TILE64;
+        ptx::mbar_arrive_expect_tx(&kv_full[slot], 2 * TILE64);
+        tma_tile64(dst, &tm_qkv, &kv_full[slot], kcol, j * 64, shard);
+        tma_tile64(dst + TILE64, &tm_qkv, &kv_full[slot], vcol, j * 64, shard);
         ++issued;
       }
       volatile int never = 0;
-      ptx::mbar_wait(qdo_full, 0, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
-      for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) {
-        const uint32_t ph = (j >> 1) & 1;
-        ptx::mbar_wait(&k_full[j & 1], ph, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
-        ptx::mbar_wait(&v_full[j & 1], ph, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
-      }
+      ptx::mbar_wait(q_full, 0, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
+      for (int j = (issued > BWD_STAGES ? issued - BWD_STAGES : 0); j < issued; ++j)
+        ptx::mbar_wait(&kv_full[j % BWD_STAGES], (j / BWD_STAGES) & 1, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_kk = ptx::idesc_f16_f32(128, 128, false, false);  // S, dP
-      constexpr uint32_t idesc_q = ptx::idesc_f16_f32(128, 128, false, true);    // dQ = dS K
-      const uint32_t aQ = ptx::smem_addr(sQ), adO = ptx::smem_addr(sdO), adS = ptx::smem_addr(sdS);
-      bool ok = ptx::mbar_wait(qdo_full, 0, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns);
+      constexpr uint32_t idesc_s = ptx::idesc_f16_f32(128, 64, false, false);  // S, dP
+      constexpr uint32_t idesc_q = ptx::idesc_f16_f32(128, 128, false, true);  // dQ = dS K
+      const uint32_t aQ = ptx::smem_addr(sQ), adO = ptx::smem_addr(sdO), aKV = ptx::smem_addr(sKV);
+      auto issue_s = [&](int j) {
+        const int slot = j % BWD_STAGES, b = j & 1;
+        if (!ptx::mbar_wait(&kv_full[slot], (j / BWD_STAGES) & 1, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns))
+          return false;
+        ptx::tc_fence_after();
+        const uint32_t aK = aKV + slot * 2 * TILE64, aV = aK + TILE64;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_bf16(tmem + 64 * b, kmajor_desc(aQ, kk), kmajor64_desc(aK, kk), idesc_s, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_bf16(tmem + 128 + 64 * b, kmajor_desc(adO, kk), kmajor64_desc(aV, kk), idesc_s, kk > 0 ? 1u : 0u);
+        ptx::mma_commit(&s_full[b]);
+        return true;
+      };
+      bool ok = ptx::mbar_wait(q_full, 0, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns);
+      if (ok && nkv > 0) ok = issue_s(0);
       for (int j = 0; ok && j < nkv; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!ptx::mbar_wait(&k_full[st], ph, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
-        if (!ptx::mbar_wait(&v_full[st], ph, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
-        if (j >= 1 && !ptx::mbar_wait(sdp_free, (j - 1) & 1, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
+        if (j + 1 < nkv && !issue_s(j + 1)) break;
+        const int b = j & 1, slot = j % BWD_STAGES;
+        if (!ptx::mbar_wait(&ds_full[b], (j >> 1) & 1, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
         ptx::tc_fence_after();
-        const uint32_t aK = ptx::smem_addr(sK + st * TILE), aV = ptx::smem_addr(sV + st * TILE);
+        const uint32_t aK = aKV + slot * 2 * TILE64;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16(tS, kmajor_desc(aQ, kk), kmajor_desc(aK, kk), idesc_kk, kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16(tdP, kmajor_desc(adO, kk), kmajor_desc(aV, kk), idesc_kk, kk > 0 ? 1u : 0u);
-        ptx::mma_commit(sdp_full);
-        if (!ptx::mbar_wait(ds_full, j & 1, abort_flag, p.err, ERR_ATT_MMA, p.timeout_ns)) break;
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16(tdQ, kmajor_desc(adS, kk), mnmajor_desc(aK, kk), idesc_q, (j > 0 || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(ds_free);
-        ptx::mma_commit(&kv_empty[st]);
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::mma_f16_ts(tdQ, tmem + 64 * b + half_split_col(kk), mnmajor64_desc(aK, kk), idesc_q,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(&kv_empty[slot]);
       }
+      ptx::mma_commit(acc_done);
       ptx::mma_commit(mma_done);
       volatile int never = 0;
       ptx::mbar_wait(mma_done, 0, &never, p.err, ERR_ATT_DRAIN, p.timeout_ns);
     }
   } else {
-    const int quad = warp & 3;
+    // Compute warps: lane quarter warp & 3 (query rows), column half h of each 64-key block.
+    const int quad = warp & 3, h = (warp - 2) >> 2;
     const int row = quad * 32 + lane;
     const int q = qb * BQ + row;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const int64_t vec_base = (static_cast<int64_t>(shard) * p.hpr + jj) * p.N;
-    const float lse2 = q < p.N ? p.lse[vec_base + q] * kLog2e : 0.0f;
-    const float Dq = q < p.N ? p.Dvec[vec_base + q] : 0.0f;
+    const int64_t vec = (static_cast<int64_t>(shard) * p.hpr + jj) * p.N;
+    // A query row past the end gets lse = +inf: its P and dS are exactly 0.
+    const float lse2 = q < p.N ? p.lse[vec + q] * kLog2e : INFINITY;
+    const float Dq = q < p.N ? p.Dvec[vec + q] : 0.0f;
+    const float sl2 = p.scale_log2;
+    const int qlim = p.causal ? min(q, p.N - 1) : p.N - 1;  // last key this row sees
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      if (!ptx::mbar_wait(sdp_full, j & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
-        ok = false;
-        break;
-      }
-      if (j >= 1 && !ptx::mbar_wait(ds_free, (j - 1) & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
+      const int b = j & 1;
+      if (!ptx::mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t s[32], dp[32], wp[16], wds[16];
-        ptx::tmem_ld32(tS + lane_base + c * 32, s);
-        ptx::tmem_ld32(tdP + lane_base + c * 32, dp);
-        ptx::tmem_ld_wait();
-        p_ds_chunk(s, dp, q, j * BKV + c * 32, p, lse2, Dq, wp, wds);
-        store_chunk_swizzled(sdS, row, c, wds);
+      const uint32_t tSb = tmem + 64 * b + lane_base + 32 * h, tdPb = tSb + 128;
+      uint32_t s[32], dp[32];
+      ptx::tmem_ld32(tSb, s);
+      ptx::tmem_ld32(tdPb, dp);
+      ptx::tmem_ld_wait();
+      const int lim = qlim - (j * 64 + 32 * h);  // columns e <= lim are visible keys
+      const bool edge = lim < 31;
+      uint32_t wds[16];
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        float d2[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          float pr = ptx::exp2_approx(fmaf(__uint_as_float(s[e + u]), sl2, -lse2));
+          if (edge && e + u > lim) pr = 0.0f;
+          d2[u] = pr * (__uint_as_float(dp[e + u]) - Dq);
+        }
+        wds[e >> 1] = pack_f16x2(d2[0], d2[1]);
       }
+      ptx::tmem_st16(tSb, wds);
+      ptx::tmem_st_wait();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(sdp_free);
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(ds_full);
+      ptx::mbar_arrive(&ds_full[b]);
     }
-    if (ok && ptx::mbar_wait(ds_free, (nkv - 1) & 1, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
+    if (ok && ptx::mbar_wait(acc_done, 0, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
       ptx::tc_fence_after();
       uint16_t* drow = p.dQKV + (static_cast<int64_t>(shard) * p.N + q) * p.row_w;
-      tmem_row_to_bf16(tdQ + lane_base, p.scale, drow + qcol, q < p.N);
+      tmem_cols64_to_bf16(tdQ + lane_base + 64 * h, p.scale, drow + qcol + 64 * h, q < p.N);
     }
   }
 
   ptx::tc_fence_before();
-  __syncwarp();  // lane-0 roles rejoin their warp: bar.sync needs converged warps
+  __syncwarp();
   __syncthreads();
   if (warp == 1) {
     __syncwarp();
@@ -892,8 +956,8 @@ tp_status run_attention_bwd(const uint16_t* QKV, const uint16_t* O, const uint16
   const int64_t dt = sh.dt;
   const int hpr = n_heads / t;
   CUtensorMap m_qkv, m_do;
-  if (!make_map_3d_bf16(&m_qkv, QKV, sh.row_w, N, t, sh.row_w * 2, N * sh.row_w * 2, 64, 128)) return TP_ERR_CUDA;
-  if (!make_map_3d_bf16(&m_do, dO, dt, N, t, dt * 2, N * dt * 2, 64, 128)) return TP_ERR_CUDA;
+  if (!make_map_3d_bf16(&m_qkv, QKV, sh.row_w, N, t, sh.row_w * 2, N * sh.row_w * 2, 64, 64)) return TP_ERR_CUDA;
+  if (!make_map_3d_bf16(&m_do, dO, dt, N, t, dt * 2, N * dt * 2, 64, 64)) return TP_ERR_CUDA;
   const int64_t rows = static_cast<int64_t>(t) * N * hpr;
   attn_bwd_dot_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, s>>>(dO, O, static_cast<int>(N), hpr,
                                                                                      dt, rows, Dvec);
@@ -903,6 +967,7 @@ tp_status run_attention_bwd(const uint16_t* QKV, const uint16_t* O, const uint16
   a.H = n_heads;
   a.hpr = hpr;
   a.nqb = static_cast<int>((N + BQ - 1) / BQ);
+  a.nb64 = static_cast<int>((N + 63) / 64);
   a.causal = causal ? 1 : 0;
   a.Gs = sh.Gs;
   a.kv_t = sh.kv_t;
