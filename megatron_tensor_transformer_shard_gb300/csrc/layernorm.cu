@@ -7,13 +7,14 @@
 // (dgamma_j, dbeta_j) and the partials are summed over j -- the extra
 // all-reduce -- in a fixed shard order.
 //
-//   row kernels     one CTA per row, the row held in registers (8-element
-//                   chunks, up to 4 per thread), block reductions for the
-//                   statistics (two-pass mean and variance); HBM-bound:
-//                   read x (+ dy, dres), write y / dx.
-//   column kernel   one CTA per (256-column block, shard), 16-byte loads, eight
-//                   warps striding the shard's rows, combined in warp order;
-//                   then one launch sums the shard partials in shard order.
+//   row kernels     one CTA per row, the row held in registers as packed bf16
+//                   words (8-element chunks, up to 4 per thread), block
+//                   reductions for the statistics (two-pass mean and variance);
+//                   HBM-bound: read x (+ dy, dres), write y / dx.
+//   column kernel   one CTA per (64-column block, shard), 16-byte loads, eight
+//                   warps of four rows each striding the shard's rows, combined
+//                   in a fixed order; then one launch sums the shard partials in
+//                   shard order.
 #include <cuda_runtime.h>
 
 #include "devmath.cuh"
@@ -61,6 +62,15 @@ __device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
   return s;
 }
 
+__device__ __forceinline__ void unpack8(const uint4& w, float (&v)[8]) {
+  unpack_bf16x2(w.x, v[0], v[1]);
+  unpack_bf16x2(w.y, v[2], v[3]);
+  unpack_bf16x2(w.z, v[4], v[5]);
+  unpack_bf16x2(w.w, v[6], v[7]);
+}
+
+// The row stays in registers as packed bf16 words (4 registers per 8 elements) and is
+// unpacked in each pass: half the registers of an fp32 copy, so more rows are in flight.
 __global__ void ln_fwd_kernel(const uint16_t* __restrict__ X, int64_t h, const uint16_t* __restrict__ gamma,
                               const uint16_t* __restrict__ beta, float eps, uint16_t* __restrict__ Y,
                               float* __restrict__ mean_out, float* __restrict__ rstd_out) {
@@ -68,15 +78,21 @@ __global__ void ln_fwd_kernel(const uint16_t* __restrict__ X, int64_t h, const u
   const int64_t row = blockIdx.x;
   const uint16_t* x = X + row * h;
   const int64_t nch = h / 8;
-  float v[LN_CHUNKS][8];
+  uint4 xw[LN_CHUNKS];
   float s = 0.0f;
 #pragma unroll
   for (int k = 0; k < LN_CHUNKS; ++k) {
     const int64_t c = threadIdx.x + static_cast<int64_t>(k) * blockDim.x;
-    if (c < nch) {
-      load8(x + c * 8, v[k]);
+    if (c < nch) xw[k] = *reinterpret_cast<const uint4*>(x + c * 8);
+  }
 #pragma unroll
-      for (int e = 0; e < 8; ++e) s += v[k][e];
+  for (int k = 0; k < LN_CHUNKS; ++k) {
+    const int64_t c = threadIdx.x + static_cast<int64_t>(k) * blockDim.x;
+    if (c < nch) {
+      float v[8];
+      unpack8(xw[k], v);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s += v[e];
     }
   }
   const float mean = block_sum2(s, 0.0f, red).x / static_cast<float>(h);
@@ -85,9 +101,11 @@ __global__ void ln_fwd_kernel(const uint16_t* __restrict__ X, int64_t h, const u
   for (int k = 0; k < LN_CHUNKS; ++k) {
     const int64_t c = threadIdx.x + static_cast<int64_t>(k) * blockDim.x;
     if (c < nch) {
+      float v[8];
+      unpack8(xw[k], v);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float d = v[k][e] - mean;
+        const float d = v[e] - mean;
         q += d * d;
       }
     }
@@ -98,11 +116,12 @@ __global__ void ln_fwd_kernel(const uint16_t* __restrict__ X, int64_t h, const u
   for (int k = 0; k < LN_CHUNKS; ++k) {
     const int64_t c = threadIdx.x + static_cast<int64_t>(k) * blockDim.x;
     if (c < nch) {
-      float g[8], b[8], o[8];
+      float v[8], g[8], b[8], o[8];
+      unpack8(xw[k], v);
       load8(gamma + c * 8, g);
       load8(beta + c * 8, b);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = (v[k][e] - mean) * rstd * g[e] + b[e];
+      for (int e = 0; e < 8; ++e) o[e] = (v[e] - mean) * rstd * g[e] + b[e];
       store8(Y + row * h + c * 8, o);
     }
   }
@@ -121,22 +140,31 @@ __global__ void ln_bwd_rows_kernel(const uint16_t* __restrict__ dY, const uint16
   const int64_t row = blockIdx.x;
   const float mean = mean_in[row], rstd = rstd_in[row];
   const int64_t nch = h / 8;
-  float xh[LN_CHUNKS][8], g[LN_CHUNKS][8];
+  // Packed bf16 words of x and dy stay in registers; gamma (the same for every row,
+  // so an L1 / L2 hit) is re-read in each pass instead of taking registers.
+  uint4 xw[LN_CHUNKS], dw[LN_CHUNKS];
+#pragma unroll
+  for (int k = 0; k < LN_CHUNKS; ++k) {
+    const int64_t c = threadIdx.x + static_cast<int64_t>(k) * blockDim.x;
+    if (c < nch) {
+      xw[k] = *reinterpret_cast<const uint4*>(X + row * h + c * 8);
+      dw[k] = *reinterpret_cast<const uint4*>(dY + row * h + c * 8);
+    }
+  }
   float sg = 0.0f, sgx = 0.0f;
 #pragma unroll
   for (int k = 0; k < LN_CHUNKS; ++k) {
     const int64_t c = threadIdx.x + static_cast<int64_t>(k) * blockDim.x;
     if (c < nch) {
-      float dy[8], gm[8];
-      load8(X + row * h + c * 8, xh[k]);
-      load8(dY + row * h + c * 8, dy);
-      load8(gamma + c * 8, gm);
+      float xv[8], dy[8], gm[8];
+      unpack8(xw[k], xv);
+      unpack8(dw[k], dy);
+      unpack8(__ldg(reinterpret_cast<const uint4*>(gamma + c * 8)), gm);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        xh[k][e] = (xh[k][e] - mean) * rstd;
-        g[k][e] = dy[e] * gm[e];
-        sg += g[k][e];
-        sgx += g[k][e] * xh[k][e];
+        const float g = dy[e] * gm[e];
+        sg += g;
+        sgx += g * ((xv[e] - mean) * rstd);
       }
     }
   }
@@ -147,9 +175,12 @@ __global__ void ln_bwd_rows_kernel(const uint16_t* __restrict__ dY, const uint16
   for (int k = 0; k < LN_CHUNKS; ++k) {
     const int64_t c = threadIdx.x + static_cast<int64_t>(k) * blockDim.x;
     if (c < nch) {
-      float o[8];
+      float xv[8], dy[8], gm[8], o[8];
+      unpack8(xw[k], xv);
+      unpack8(dw[k], dy);
+      unpack8(__ldg(reinterpret_cast<const uint4*>(gamma + c * 8)), gm);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = rstd * (g[k][e] - mg - xh[k][e] * mgx);
+      for (int e = 0; e < 8; ++e) o[e] = rstd * (dy[e] * gm[e] - mg - ((xv[e] - mean) * rstd) * mgx);
       if (dres) {
         float r[8];
         load8(dres + row * h + c * 8, r);
@@ -161,84 +192,86 @@ __global__ void ln_bwd_rows_kernel(const uint16_t* __restrict__ dY, const uint16
   }
 }
 
-// Partial weight grads of shard j over its rows [j*rows_per, (j+1)*rows_per):
-// one CTA per (256-column block, shard); lane owns 8 columns (16-byte loads),
-// the 8 warps stride the shard's rows and are combined in warp order.
+// Partial weight grads of shard j over its rows [j*rows_per, (j+1)*rows_per): one CTA
+// per (64-column block, shard), 1024 CTAs at the sequence-parallel layer shape so that
+// the SMs get an even share.  A lane owns 8 columns (16-byte loads) of one of the 4
+// rows a warp covers per step (lane / 8 = row, lane % 8 = column group); the 8 warps
+// step through the shard's rows 32 at a time, 8 rows in flight per lane.  Sums are
+// combined in a fixed order: rows in sequence, then the 4 row lanes, then warps.
 constexpr int COLS_THREADS = 256;
+constexpr int COLS_BLOCK = 64;
+
+__device__ __forceinline__ void cols_accum(const uint4& xv, const uint4& dv, float mu, float rs, float (&dg)[8],
+                                           float (&db)[8]) {
+  const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+  const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float x0, x1, d0, d1;
+    unpack_bf16x2(xw[q], x0, x1);
+    unpack_bf16x2(dw[q], d0, d1);
+    dg[2 * q] += d0 * (x0 - mu) * rs;
+    dg[2 * q + 1] += d1 * (x1 - mu) * rs;
+    db[2 * q] += d0;
+    db[2 * q + 1] += d1;
+  }
+}
 
 __global__ void __launch_bounds__(COLS_THREADS)
     ln_bwd_cols_kernel(const uint16_t* __restrict__ dY, const uint16_t* __restrict__ X,
                        const float* __restrict__ mean_in, const float* __restrict__ rstd_in, int64_t h,
                        int64_t rows_per, float* __restrict__ dg_part, float* __restrict__ db_part) {
-  __shared__ float red[2][8][256];
+  __shared__ float red[2][COLS_THREADS / 32][COLS_BLOCK];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 256 + lane * 8;
+  const int sub = lane >> 3, cg = lane & 7;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * COLS_BLOCK + cg * 8;
   const int j = blockIdx.y;
   float dg[8] = {0, 0, 0, 0, 0, 0, 0, 0}, db[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   if (c0 < h) {
-    const int64_t r0 = static_cast<int64_t>(j) * rows_per, r1 = r0 + rows_per;
-    int64_t r = r0 + warp;
-    for (; r + 24 < r1; r += 32) {  // four rows in flight
-      uint4 xv[4], dv[4];
-      float mu[4], rs[4];
+    const int64_t r1 = static_cast<int64_t>(j + 1) * rows_per;
+    int64_t r = static_cast<int64_t>(j) * rows_per + warp * 4 + sub;
+    for (; r + 7 * 32 < r1; r += 8 * 32) {
+      uint4 xv[8], dv[8];
+      float mu[8], rs[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int64_t rr = r + 8 * u;
+      for (int u = 0; u < 8; ++u) {
+        const int64_t rr = r + 32 * u;
         xv[u] = *reinterpret_cast<const uint4*>(X + rr * h + c0);
         dv[u] = *reinterpret_cast<const uint4*>(dY + rr * h + c0);
         mu[u] = mean_in[rr];
         rs[u] = rstd_in[rr];
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint32_t xw[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
-        const uint32_t dw[4] = {dv[u].x, dv[u].y, dv[u].z, dv[u].w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float x0, x1, d0, d1;
-          unpack_bf16x2(xw[q], x0, x1);
-          unpack_bf16x2(dw[q], d0, d1);
-          dg[2 * q] += d0 * (x0 - mu[u]) * rs[u];
-          dg[2 * q + 1] += d1 * (x1 - mu[u]) * rs[u];
-          db[2 * q] += d0;
-          db[2 * q + 1] += d1;
-        }
-      }
+      for (int u = 0; u < 8; ++u) cols_accum(xv[u], dv[u], mu[u], rs[u], dg, db);
     }
-    for (; r < r1; r += 8) {
-      const uint4 xv = *reinterpret_cast<const uint4*>(X + r * h + c0);
-      const uint4 dv = *reinterpret_cast<const uint4*>(dY + r * h + c0);
-      const float mu = mean_in[r], rs = rstd_in[r];
-      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-      const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float x0, x1, d0, d1;
-        unpack_bf16x2(xw[q], x0, x1);
-        unpack_bf16x2(dw[q], d0, d1);
-        dg[2 * q] += d0 * (x0 - mu) * rs;
-        dg[2 * q + 1] += d1 * (x1 - mu) * rs;
-        db[2 * q] += d0;
-        db[2 * q + 1] += d1;
-      }
-    }
+    for (; r < r1; r += 32)
+      cols_accum(*reinterpret_cast<const uint4*>(X + r * h + c0), *reinterpret_cast<const uint4*>(dY + r * h + c0),
+                 mean_in[r], rstd_in[r], dg, db);
   }
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    red[0][warp][lane * 8 + e] = dg[e];
-    red[1][warp][lane * 8 + e] = db[e];
+    dg[e] += __shfl_xor_sync(0xffffffffu, dg[e], 8);
+    dg[e] += __shfl_xor_sync(0xffffffffu, dg[e], 16);
+    db[e] += __shfl_xor_sync(0xffffffffu, db[e], 8);
+    db[e] += __shfl_xor_sync(0xffffffffu, db[e], 16);
+  }
+  if (sub == 0) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      red[0][warp][cg * 8 + e] = dg[e];
+      red[1][warp][cg * 8 + e] = db[e];
+    }
   }
   __syncthreads();
-  const int64_t c = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
-  if (c < h) {
-    float sg = 0.0f, sb = 0.0f;
+  if (threadIdx.x < 2 * COLS_BLOCK) {
+    const int which = threadIdx.x / COLS_BLOCK, col = threadIdx.x % COLS_BLOCK;
+    const int64_t c = static_cast<int64_t>(blockIdx.x) * COLS_BLOCK + col;
+    if (c < h) {
+      float acc = 0.0f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      sg += red[0][w][threadIdx.x];
-      sb += red[1][w][threadIdx.x];
+      for (int w = 0; w < COLS_THREADS / 32; ++w) acc += red[which][w][col];
+      (which ? db_part : dg_part)[static_cast<int64_t>(j) * h + c] = acc;
     }
-    dg_part[static_cast<int64_t>(j) * h + c] = sg;
-    db_part[static_cast<int64_t>(j) * h + c] = sb;
   }
 }
 
@@ -306,7 +339,7 @@ tp_status run_ln_backward(const uint16_t* dY, const uint16_t* X, const uint16_t*
   }
   ln_bwd_rows_kernel<<<static_cast<unsigned>(s), row_threads(h), 0, st>>>(dY, X, gamma, mean, rstd, dres, h, dX);
   TP_LAUNCHED();
-  dim3 g(static_cast<unsigned>((h + 255) / 256), static_cast<unsigned>(t));
+  dim3 g(static_cast<unsigned>((h + COLS_BLOCK - 1) / COLS_BLOCK), static_cast<unsigned>(t));
   ln_bwd_cols_kernel<<<g, COLS_THREADS, 0, st>>>(dY, X, mean, rstd, h, s / t, dg_part, db_part);
   TP_LAUNCHED();
   // The LayerNorm weight-gradient all-reduce over the sequence shards, fixed order.
