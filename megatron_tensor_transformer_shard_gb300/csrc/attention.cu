@@ -443,26 +443,40 @@ __device__ __forceinline__ void tmem_cols64_to_bf16(uint32_t taddr, float mul, u
     }
 }
 
+// D[i][jj][q] = rowsum(dO * O) over head jj's 128 columns.  One warp per (shard, query)
+// row: a lane reads 8 consecutive columns (16 bytes of dO and of O), so a pass covers two
+// heads and each head's sum is a reduction over 16 lanes.
 __global__ void attn_bwd_dot_kernel(const uint16_t* __restrict__ dO, const uint16_t* __restrict__ O, int N, int hpr,
-                                    int64_t dt, int64_t total, float* __restrict__ Dvec) {
+                                    int64_t dt, int64_t rows, float* __restrict__ Dvec) {
   const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (w >= total) return;
-  const int64_t i = w / (static_cast<int64_t>(N) * hpr);
-  const int64_t rem = w - i * N * hpr;
-  const int64_t q = rem / hpr, jj = rem - q * hpr;
-  const int64_t off = (i * N + q) * dt + jj * HD + lane * 4;
-  const uint2 a = *reinterpret_cast<const uint2*>(dO + off);
-  const uint2 b = *reinterpret_cast<const uint2*>(O + off);
-  float a0, a1, a2, a3, b0, b1, b2, b3;
-  unpack_f16x2(a.x, a0, a1);  // dO is fp16, O is bf16
-  unpack_f16x2(a.y, a2, a3);
-  unpack_bf16x2(b.x, b0, b1);
-  unpack_bf16x2(b.y, b2, b3);
-  float sum = a0 * b0 + a1 * b1 + a2 * b2 + a3 * b3;
+  if (w >= rows) return;
+  const int64_t i = w / N, q = w - i * N;
+  const uint16_t* drow = dO + w * dt;
+  const uint16_t* orow = O + w * dt;
+  for (int64_t c0 = 0; c0 < dt; c0 += 256) {
+    const int64_t c = c0 + lane * 8;
+    float sum = 0.0f;
+    if (c < dt) {
+      const uint4 a = *reinterpret_cast<const uint4*>(drow + c);
+      const uint4 b = *reinterpret_cast<const uint4*>(orow + c);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (lane == 0) Dvec[(i * hpr + jj) * N + q] = sum;
+      for (int k = 0; k < 4; ++k) {
+        float a0, a1, b0, b1;
+        unpack_f16x2(aw[k], a0, a1);  // dO is fp16, O is bf16
+        unpack_bf16x2(bw[k], b0, b1);
+        sum = fmaf(a0, b0, sum);
+        sum = fmaf(a1, b1, sum);
+      }
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if ((lane & 15) == 0 && c < dt) {
+      const int64_t jj = c / HD;
+      Dvec[(i * hpr + jj) * N + q] = sum;
+    }
+  }
 }
 
 __global__ void __launch_bounds__(BWD_THREADS, 1)
@@ -958,7 +972,7 @@ tp_status run_attention_bwd(const uint16_t* QKV, const uint16_t* O, const uint16
   CUtensorMap m_qkv, m_do;
   if (!make_map_3d_bf16(&m_qkv, QKV, sh.row_w, N, t, sh.row_w * 2, N * sh.row_w * 2, 64, 64)) return TP_ERR_CUDA;
   if (!make_map_3d_bf16(&m_do, dO, dt, N, t, dt * 2, N * dt * 2, 64, 64)) return TP_ERR_CUDA;
-  const int64_t rows = static_cast<int64_t>(t) * N * hpr;
+  const int64_t rows = static_cast<int64_t>(t) * N;
   attn_bwd_dot_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, s>>>(dO, O, static_cast<int>(N), hpr,
                                                                                      dt, rows, Dvec);
   TP_LAUNCHED();
