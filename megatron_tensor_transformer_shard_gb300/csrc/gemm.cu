@@ -385,10 +385,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int total = p.nbatch * p.mt * p.nt;
   const int ksteps = p.nsum * p.kt;
+  // Programmatic dependent launch: the next kernel on the stream may be scheduled
+  // now (its CTAs take SMs as ours leave).  Everything this kernel reads from or
+  // writes to global memory comes after the producer's griddepcontrol.wait (the
+  // MMAs and the epilogue follow its loads through the barriers), so the previous
+  // kernel has completed and its writes are visible by then.
+  ptx::griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------ TMA producer
+      ptx::griddep_wait();
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -826,12 +833,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
   const int nt2 = (p.N + P_BN - 1) / P_BN;
   const int total = p.nbatch * mt2 * nt2;
   const int ksteps = p.nsum * p.kt;
+  // Programmatic dependent launch (not for the overlapped form, whose queues are
+  // written before its producers start): as in gemm_kernel, every global access
+  // follows the producers' griddepcontrol.wait.
+  if constexpr (!OVL) ptx::griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------ TMA producer (both CTAs)
       ptx::tma_prefetch_desc(&tmA);
       ptx::tma_prefetch_desc(&tmB);
+      if constexpr (!OVL) ptx::griddep_wait();
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -1138,8 +1150,8 @@ tp_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a
                                        SMEM_BYTES));
     configured[dev] = true;
   }
-  gemm_kernel<A_MN, B_MN, EPI, ACT><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, a);
-  TP_LAUNCHED();
+  TP_CUDA_CHECK(launch_pdl(gemm_kernel<A_MN, B_MN, EPI, ACT>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, s, ta, tb, a));
+  count_launch();
   return TP_OK;
 }
 
@@ -1173,9 +1185,15 @@ tp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
   const int nc = pair_clusters<A_MN, B_MN, EPI, ACT, OVL>(dev);
   if (nc <= 0) return TP_FAIL_DETAIL("no co-resident CTA pairs");
   const int clusters = static_cast<int>(tiles < nc ? tiles : nc);
-  gemm_pair_kernel<A_MN, B_MN, EPI, ACT, OVL>
-      <<<2 * clusters, pair_threads<OVL>(), pair_smem_bytes<EPI, OVL>(), s>>>(ta, tb, td, td2, a);
-  TP_LAUNCHED();
+  if constexpr (OVL) {
+    gemm_pair_kernel<A_MN, B_MN, EPI, ACT, OVL>
+        <<<2 * clusters, pair_threads<OVL>(), pair_smem_bytes<EPI, OVL>(), s>>>(ta, tb, td, td2, a);
+    TP_LAUNCHED();
+  } else {
+    TP_CUDA_CHECK(launch_pdl(gemm_pair_kernel<A_MN, B_MN, EPI, ACT, OVL>, dim3(2 * clusters),
+                             dim3(pair_threads<OVL>()), pair_smem_bytes<EPI, OVL>(), s, ta, tb, td, td2, a));
+    count_launch();
+  }
   return TP_OK;
 }
 
