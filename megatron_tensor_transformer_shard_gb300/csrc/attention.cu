@@ -129,6 +129,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Programmatic dependent launch: set-up above overlapped the previous kernel's tail;
+  // nothing it writes is read before this wait.
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   // TMEM columns: S_0 | S_1 | O_0 | O_1, 128 each.  P_b (fp16 pairs) overwrites the first 64 columns of S_b.
   const uint32_t tS[2] = {tmem, tmem + 128};
   const uint32_t tO[2] = {tmem + 256, tmem + 384};
@@ -448,6 +452,8 @@ __device__ __forceinline__ void tmem_cols64_to_bf16(uint32_t taddr, float mul, u
 // heads and each head's sum is a reduction over 16 lanes.
 __global__ void attn_bwd_dot_kernel(const uint16_t* __restrict__ dO, const uint16_t* __restrict__ O, int N, int hpr,
                                     int64_t dt, int64_t rows, float* __restrict__ Dvec) {
+  ptx::griddep_wait();  // dO comes from the previous kernel
+  ptx::griddep_launch_dependents();
   const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= rows) return;
@@ -536,6 +542,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Programmatic dependent launch: set-up above overlapped the previous kernel's tail;
+  // nothing it writes is read before this wait.
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   // TMEM columns: S^T_0 | S^T_1 (64 each) | dP^T_0 | dP^T_1 (64 each) | dV (128) | dK (128).
   const uint32_t tdV = tmem + 256, tdK = tmem + 384;
 
@@ -753,6 +763,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Programmatic dependent launch: set-up above overlapped the previous kernel's tail;
+  // nothing it writes is read before this wait.
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   // TMEM columns: S_0 | S_1 (64 each) | dP_0 | dP_1 (64 each) | dQ (128).
   const uint32_t tdQ = tmem + 256;
 
@@ -946,10 +960,12 @@ tp_status run_attention_fwd(const uint16_t* QKV, int64_t N, int64_t d, int n_hea
   const int64_t grid = static_cast<int64_t>(n_heads) * a.nsb;
   if (grid > 0x7fffffff) return TP_ERR_SHAPE;
   if (a.scale_log2 < 0.0f)
-    attn_fwd_kernel<true><<<static_cast<unsigned>(grid), FWD_THREADS, FWD_SMEM, s>>>(map, a);
+    TP_CUDA_CHECK(launch_pdl(attn_fwd_kernel<true>, dim3(static_cast<unsigned>(grid)), dim3(FWD_THREADS), FWD_SMEM, s,
+                             map, a));
   else
-    attn_fwd_kernel<false><<<static_cast<unsigned>(grid), FWD_THREADS, FWD_SMEM, s>>>(map, a);
-  TP_LAUNCHED();
+    TP_CUDA_CHECK(launch_pdl(attn_fwd_kernel<false>, dim3(static_cast<unsigned>(grid)), dim3(FWD_THREADS), FWD_SMEM,
+                             s, map, a));
+  count_launch();
   return TP_OK;
 }
 
@@ -973,9 +989,9 @@ tp_status run_attention_bwd(const uint16_t* QKV, const uint16_t* O, const uint16
   if (!make_map_3d_bf16(&m_qkv, QKV, sh.row_w, N, t, sh.row_w * 2, N * sh.row_w * 2, 64, 64)) return TP_ERR_CUDA;
   if (!make_map_3d_bf16(&m_do, dO, dt, N, t, dt * 2, N * dt * 2, 64, 64)) return TP_ERR_CUDA;
   const int64_t rows = static_cast<int64_t>(t) * N;
-  attn_bwd_dot_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, s>>>(dO, O, static_cast<int>(N), hpr,
-                                                                                     dt, rows, Dvec);
-  TP_LAUNCHED();
+  TP_CUDA_CHECK(launch_pdl(attn_bwd_dot_kernel, dim3(static_cast<unsigned>((rows * 32 + 255) / 256)), dim3(256), 0, s,
+                           dO, O, static_cast<int>(N), hpr, dt, rows, Dvec));
+  count_launch();
   AttnBwdArgs a{};
   a.N = static_cast<int>(N);
   a.H = n_heads;
@@ -1007,11 +1023,11 @@ tp_status run_attention_bwd(const uint16_t* QKV, const uint16_t* O, const uint16
     configured[dev] = true;
   }
   const unsigned grid_kv = static_cast<unsigned>(static_cast<int64_t>(a.Hkv) * a.nqb);
-  attn_bwd_dkv_kernel<<<grid_kv, BWD_THREADS, DKV_SMEM, s>>>(m_qkv, m_do, a);
-  TP_LAUNCHED();
+  TP_CUDA_CHECK(launch_pdl(attn_bwd_dkv_kernel, dim3(grid_kv), dim3(BWD_THREADS), DKV_SMEM, s, m_qkv, m_do, a));
+  count_launch();
   const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(n_heads) * a.nqb);
-  attn_bwd_dq_kernel<<<grid, BWD_THREADS, DQ_SMEM, s>>>(m_qkv, m_do, a);
-  TP_LAUNCHED();
+  TP_CUDA_CHECK(launch_pdl(attn_bwd_dq_kernel, dim3(grid), dim3(BWD_THREADS), DQ_SMEM, s, m_qkv, m_do, a));
+  count_launch();
   return TP_OK;
 }
 

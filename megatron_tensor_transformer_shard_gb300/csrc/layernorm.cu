@@ -19,6 +19,7 @@
 
 #include "devmath.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace tp {
 namespace {
@@ -74,6 +75,8 @@ __device__ __forceinline__ void unpack8(const uint4& w, float (&v)[8]) {
 __global__ void ln_fwd_kernel(const uint16_t* __restrict__ X, int64_t h, const uint16_t* __restrict__ gamma,
                               const uint16_t* __restrict__ beta, float eps, uint16_t* __restrict__ Y,
                               float* __restrict__ mean_out, float* __restrict__ rstd_out) {
+  ptx::griddep_wait();  // inputs come from the previous kernel on the stream
+  ptx::griddep_launch_dependents();
   __shared__ float2 red[32];
   const int64_t row = blockIdx.x;
   const uint16_t* x = X + row * h;
@@ -136,6 +139,8 @@ __global__ void ln_bwd_rows_kernel(const uint16_t* __restrict__ dY, const uint16
                                    const uint16_t* __restrict__ gamma, const float* __restrict__ mean_in,
                                    const float* __restrict__ rstd_in, const uint16_t* __restrict__ dres, int64_t h,
                                    uint16_t* __restrict__ dX) {
+  ptx::griddep_wait();  // inputs come from the previous kernel on the stream
+  ptx::griddep_launch_dependents();
   __shared__ float2 red[32];
   const int64_t row = blockIdx.x;
   const float mean = mean_in[row], rstd = rstd_in[row];
@@ -221,6 +226,8 @@ __global__ void __launch_bounds__(COLS_THREADS)
     ln_bwd_cols_kernel(const uint16_t* __restrict__ dY, const uint16_t* __restrict__ X,
                        const float* __restrict__ mean_in, const float* __restrict__ rstd_in, int64_t h,
                        int64_t rows_per, float* __restrict__ dg_part, float* __restrict__ db_part) {
+  ptx::griddep_wait();  // inputs come from the previous kernel on the stream
+  ptx::griddep_launch_dependents();
   __shared__ float red[2][COLS_THREADS / 32][COLS_BLOCK];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane >> 3, cg = lane & 7;
@@ -278,6 +285,8 @@ __global__ void __launch_bounds__(COLS_THREADS)
 // The LayerNorm weight-gradient all-reduce: sum of the t shard partials, shard order.
 __global__ void ln_bwd_shard_sum_kernel(const float* __restrict__ dg_part, const float* __restrict__ db_part,
                                         int64_t h, int t, float* __restrict__ dgamma, float* __restrict__ dbeta) {
+  ptx::griddep_wait();  // inputs come from the previous kernel on the stream
+  ptx::griddep_launch_dependents();
   const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c >= h) return;
   float sg = 0.0f, sb = 0.0f;
@@ -313,8 +322,9 @@ tp_status run_ln_forward(const uint16_t* X, int64_t s, int64_t h, int t, const u
   if (!aligned16(X) || !aligned16(gamma) || !aligned16(beta) || !aligned16(Y)) return TP_ERR_ALIGN;
   if (s > 0x7fffffffLL) return TP_ERR_SHAPE;
   TP_RETURN_IF(ready());
-  ln_fwd_kernel<<<static_cast<unsigned>(s), row_threads(h), 0, st>>>(X, h, gamma, beta, eps, Y, mean, rstd);
-  TP_LAUNCHED();
+  TP_CUDA_CHECK(launch_pdl(ln_fwd_kernel, dim3(static_cast<unsigned>(s)), dim3(row_threads(h)), 0, st, X, h, gamma, beta,
+                           eps, Y, mean, rstd));
+  count_launch();
   return TP_OK;
 }
 
@@ -337,15 +347,17 @@ tp_status run_ln_backward(const uint16_t* dY, const uint16_t* X, const uint16_t*
     TP_CUDA_CHECK(cudaMemsetAsync(dbeta, 0, sizeof(float) * h, st));
     return TP_OK;
   }
-  ln_bwd_rows_kernel<<<static_cast<unsigned>(s), row_threads(h), 0, st>>>(dY, X, gamma, mean, rstd, dres, h, dX);
-  TP_LAUNCHED();
+  TP_CUDA_CHECK(launch_pdl(ln_bwd_rows_kernel, dim3(static_cast<unsigned>(s)), dim3(row_threads(h)), 0, st, dY, X, gamma,
+                           mean, rstd, dres, h, dX));
+  count_launch();
   dim3 g(static_cast<unsigned>((h + COLS_BLOCK - 1) / COLS_BLOCK), static_cast<unsigned>(t));
-  ln_bwd_cols_kernel<<<g, COLS_THREADS, 0, st>>>(dY, X, mean, rstd, h, s / t, dg_part, db_part);
-  TP_LAUNCHED();
+  TP_CUDA_CHECK(launch_pdl(ln_bwd_cols_kernel, g, dim3(COLS_THREADS), 0, st, dY, X, mean, rstd, h, s / t, dg_part,
+                           db_part));
+  count_launch();
   // The LayerNorm weight-gradient all-reduce over the sequence shards, fixed order.
-  ln_bwd_shard_sum_kernel<<<static_cast<unsigned>((h + 255) / 256), 256, 0, st>>>(dg_part, db_part, h, t, dgamma,
-                                                                                    dbeta);
-  TP_LAUNCHED();
+  TP_CUDA_CHECK(launch_pdl(ln_bwd_shard_sum_kernel, dim3(static_cast<unsigned>((h + 255) / 256)), dim3(256), 0, st,
+                           dg_part, db_part, h, t, dgamma, dbeta));
+  count_launch();
   return TP_OK;
 }
 

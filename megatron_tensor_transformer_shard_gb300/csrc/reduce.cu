@@ -8,6 +8,7 @@
 
 #include "devmath.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace tp {
 namespace {
@@ -101,8 +102,13 @@ __device__ __forceinline__ const ColsumJob& pick(const ColsumJob& a, const Colsu
   return first ? a : b;
 }
 
+// Both colsum2 kernels are launched with programmatic dependent launch: they wait
+// for the previous kernel's results before reading anything and let the next
+// kernel on the stream set up while they run.
 __global__ void __launch_bounds__(CS2_THREADS) colsum2_partial_kernel(ColsumJob j0, ColsumJob j1, int64_t n0) {
   __shared__ float red[8][256];
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const bool first = blockIdx.x < n0;
   const ColsumJob& j = pick(j0, j1, first);
   const int64_t local = first ? blockIdx.x : blockIdx.x - n0;
@@ -157,6 +163,8 @@ __global__ void __launch_bounds__(CS2_THREADS) colsum2_partial_kernel(ColsumJob 
 }
 
 __global__ void colsum2_final_kernel(ColsumJob j0, ColsumJob j1, int64_t n0) {
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const bool first = idx < n0;
   const ColsumJob& j = pick(j0, j1, first);
@@ -197,11 +205,13 @@ tp_status run_colsum2(ColsumJob a, ColsumJob b, cudaStream_t s) {
   }
   if (ctas[0] + ctas[1] == 0) return TP_OK;
   TP_RETURN_IF(ready());
-  colsum2_partial_kernel<<<static_cast<unsigned>(ctas[0] + ctas[1]), CS2_THREADS, 0, s>>>(a, b, ctas[0]);
-  TP_LAUNCHED();
+  TP_CUDA_CHECK(launch_pdl(colsum2_partial_kernel, dim3(static_cast<unsigned>(ctas[0] + ctas[1])), dim3(CS2_THREADS),
+                           0, s, a, b, ctas[0]));
+  count_launch();
   const int64_t n = outs[0] + outs[1];
-  colsum2_final_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(a, b, outs[0]);
-  TP_LAUNCHED();
+  TP_CUDA_CHECK(launch_pdl(colsum2_final_kernel, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, s, a, b,
+                           outs[0]));
+  count_launch();
   return TP_OK;
 }
 
