@@ -522,11 +522,24 @@ def run_mlp_fwd_extra(L, torch, args):
     Y = torch.empty(M, h, dtype=torch.bfloat16, device="cuda")
     A = torch.empty(t, M, F // t, dtype=torch.bfloat16, device="cuda")
     act = L.ACT_BY_NAME["gelu_tanh"]
-    ms = _time(torch, lambda: L.tp_mlp_forward(inp["X"], M, h, F, t, act, w.Wup_p, w.b_up, w.Wdown_p, w.b_down,
-                                               None, Y, None, A, 0, None, 0), max(50, args.steps), warmup=10)
+    fwd = lambda: L.tp_mlp_forward(inp["X"], M, h, F, t, act, w.Wup_p, w.b_up, w.Wdown_p, w.b_down, None, Y, None, A,
+                                   0, None, 0)
+    ms = _time(torch, fwd, max(50, args.steps), warmup=10)
+    # The same forward replayed from a CUDA graph: no host work (argument checks, tensor-map
+    # encoding, launches) between the kernels; this size is launch-bound otherwise.
+    graph = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cs):
+        fwd()
+        with torch.cuda.graph(graph, stream=cs):
+            fwd()
+    torch.cuda.current_stream().wait_stream(cs)
+    ms_graph = _time(torch, graph.replay, max(50, args.steps), warmup=10)
     fl = 4.0 * M * h * F
     return {"workload": "TP-MLP forward, t=2, X 128x1024, W_up 1024x4096, W_down 4096x1024, GeLU(tanh)",
             "us_per_step": round(ms * 1e3, 2), "TFLOPs": round(fl / (ms / 1e3) / 1e12, 2),
+            "us_per_step_graph": round(ms_graph * 1e3, 2), "TFLOPs_graph": round(fl / (ms_graph / 1e3) / 1e12, 2),
             "flops_per_step": fl, "l2": "8.4 MB of weights stay in L2 (no flush): latency-bound, 32 + 16 tiles",
             "page_bytes": {"expanded_tensor": M * F * 2, "output_reduction_tensor": M * h * 2}}
 

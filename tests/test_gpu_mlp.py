@@ -332,3 +332,34 @@ def test_host_validation_on_device():
     r = L.tp_mlp_forward(dev["X"], 64, 128, 256, 2, 2, w.Wup_p, w.b_up, w.Wdown_p, w.b_down, None, Y, None, A,
                          L.TP_FLAG_UNFUSED_REDUCE, small, 16, check=False)
     assert r == L.TP_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("M,h,F,t", [(128, 1024, 4096, 2), (512, 512, 2048, 4)])
+def test_mlp_forward_graph_replay_matches_eager(M, h, F, t):
+    """The forward's GEMMs launch with programmatic dependent launch; captured in a
+    CUDA graph and replayed they give the same bits as the eager call."""
+    inp = I.mlp_inputs(M, h, F, bias=True, dy=False, seed=13, device="cuda")
+    w = T.MLPWeights(inp["W_up"], inp["b_up"], inp["W_down"], inp["b_down"], t)
+    act = L.ACT_BY_NAME["gelu_tanh"]
+    Y, A = torch.empty(M, h, dtype=torch.bfloat16, device="cuda"), torch.empty(t, M, F // t, dtype=torch.bfloat16,
+                                                                               device="cuda")
+    fwd = lambda: L.tp_mlp_forward(inp["X"], M, h, F, t, act, w.Wup_p, w.b_up, w.Wdown_p, w.b_down, None, Y, None, A,
+                                   0, None, 0)
+    fwd()
+    torch.cuda.synchronize()
+    Y_eager, A_eager = Y.clone(), A.clone()
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(g, stream=cs):
+            fwd()
+    torch.cuda.current_stream().wait_stream(cs)
+    for _ in range(3):
+        Y.zero_()
+        A.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(Y.view(torch.int16), Y_eager.view(torch.int16))
+        assert torch.equal(A.view(torch.int16), A_eager.view(torch.int16))
+    assert L.tp_get_device_status(check=False) == L.TP_OK
