@@ -88,6 +88,15 @@ def test_sp_layernorm_parity(s, h, t, dres):
     _ln(s, h, t, dres)
 
 
+# More shapes: shard row counts that are not multiples of the column kernel's 32-row
+# step, a row of 4992 columns (a thread's last 8-column chunk past the end for some
+# threads), 8192 columns with dres, and 16 shards.
+@pytest.mark.parametrize("s,h,t,dres", [(320, 512, 8, False), (8 * 21, 4992, 8, True), (8 * 64, 8192, 8, True),
+                                        (16 * 24, 768, 16, False)])
+def test_sp_layernorm_more_shapes(s, h, t, dres):
+    _ln(s, h, t, dres)
+
+
 @pytest.mark.slow
 def test_sp_layernorm_full_size():
     _ln(4096, 8192, 8, True)
