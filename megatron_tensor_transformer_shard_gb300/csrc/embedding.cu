@@ -94,6 +94,84 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* wsum, int* total
   return incl - v + (warp > 0 ? wsum[warp - 1] : 0);
 }
 
+// Bitonic sorting network over key[0, P), all stages from size `size0` on, in shared
+// memory: every compare-exchange step is followed by a block barrier.  A stage
+// starts at stride size / 2; stride_min stops the stage early (smaller strides are
+// left to the caller).
+__device__ __forceinline__ void bitonic_smem_steps(uint32_t* key, int P, int size, int stride_hi, int stride_lo) {
+  for (int stride = stride_hi; stride >= stride_lo; stride >>= 1) {
+    for (int i = threadIdx.x; i < P / 2; i += SORT_THREADS) {
+      const int lo = 2 * i - (i & (stride - 1));  // first element of the i-th compared pair
+      const int hi = lo + stride;
+      const bool up = (lo & size) == 0;
+      const uint32_t a = key[lo], b = key[hi];
+      if ((a > b) == up) {
+        key[lo] = b;
+        key[hi] = a;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+__device__ __forceinline__ void bitonic_smem(uint32_t* key, int P, int size0, int stride_lo) {
+  for (int size = size0; size <= P; size <<= 1) bitonic_smem_steps(key, P, size, size >> 1, stride_lo);
+}
+
+// The same network with E consecutive keys per thread (P = E * SORT_THREADS): strides
+// below E are compare-exchanges in registers, strides below 32 E are exchanges with the
+// lane (stride / E) away, and only larger strides go through shared memory.  On exit the
+// sorted keys are back in key[].
+template <int E>
+__device__ __forceinline__ void bitonic_regs(uint32_t* key) {
+  constexpr int P = E * SORT_THREADS;
+  uint32_t v[E];
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = key[t * E + e];
+  for (int size = 2; size <= P; size <<= 1) {
+    int stride = size >> 1;
+    if (stride >= 32 * E) {  // partner in another warp: shared memory
+#pragma unroll
+      for (int e = 0; e < E; ++e) key[t * E + e] = v[e];
+      __syncthreads();
+      bitonic_smem_steps(key, P, size, stride, 32 * E);
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[e] = key[t * E + e];
+      __syncthreads();  // key[] is rewritten by the next shared-memory step
+      stride = 16 * E;
+    }
+    for (; stride >= E; stride >>= 1) {  // partner lane (stride / E) away in this warp
+      const int dl = stride / E;
+      const bool lower = (t & dl) == 0;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int i = t * E + e;
+        const bool up = (i & size) == 0;
+        const uint32_t o = __shfl_xor_sync(0xffffffffu, v[e], dl);
+        v[e] = (lower == up) ? min(v[e], o) : max(v[e], o);
+      }
+    }
+    for (; stride > 0; stride >>= 1) {  // partner in this thread's registers
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        if ((e & stride) == 0) {
+          const int i = t * E + e;
+          const bool up = (i & size) == 0;
+          const uint32_t a = v[e], b = v[e | stride];
+          if ((a > b) == up) {
+            v[e] = b;
+            v[e | stride] = a;
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) key[t * E + e] = v[e];
+  __syncthreads();
+}
+
 // Sorts the chunk's keys (id << 13 | n) ascending in shared memory and writes
 // them, plus the segments of equal ids in two lists: seg[0] / seg[1] = number
 // of short / long segments, seg[4 + 2j], seg[5 + 2j] = first sorted position and length
@@ -121,21 +199,10 @@ __global__ void __launch_bounds__(SORT_THREADS)
   }
   if (threadIdx.x == 0) nv_s = 0;
   __syncthreads();
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < P / 2; i += SORT_THREADS) {
-        const int lo = 2 * i - (i & (stride - 1));  // first element of the i-th compared pair
-        const int hi = lo + stride;
-        const bool up = (lo & size) == 0;
-        const uint32_t a = key[lo], b = key[hi];
-        if ((a > b) == up) {
-          key[lo] = b;
-          key[hi] = a;
-        }
-      }
-      __syncthreads();
-    }
-  }
+  if (P <= SORT_THREADS) bitonic_smem(key, P, 2, 1);
+  else if (P == 2 * SORT_THREADS) bitonic_regs<2>(key);
+  else if (P == 4 * SORT_THREADS) bitonic_regs<4>(key);
+  else bitonic_regs<8>(key);
   // valid keys: up to the first sentinel (one thread sees the boundary)
   for (int i = threadIdx.x; i < P; i += SORT_THREADS)
     if (key[i] != 0xFFFFFFFFu && (i + 1 == P || key[i + 1] == 0xFFFFFFFFu)) nv_s = i + 1;

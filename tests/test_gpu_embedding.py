@@ -31,7 +31,8 @@ def _bwd(ids, dY, V, h, t, dE=None, accumulate=0):
     return dE
 
 
-@pytest.mark.parametrize("N,V,h,t", [(300, 64, 256, 4), (9000, 1000, 264, 8), (1, 16, 8, 2), (5000, 4096, 512, 1)])
+@pytest.mark.parametrize("N,V,h,t", [(300, 64, 256, 4), (9000, 1000, 264, 8), (1, 16, 8, 2), (5000, 4096, 512, 1),
+                                     (1500, 512, 128, 2), (2048, 96, 64, 4)])
 def test_embedding_parity(N, V, h, t):
     ids = I.token_ids(N, V, seed=N)
     ids[:4] = torch.tensor([0, V - 1, V // t - 1, min(V // t, V - 1)], dtype=torch.int32)[: min(4, N)]
