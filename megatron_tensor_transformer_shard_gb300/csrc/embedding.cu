@@ -405,7 +405,6 @@ tp_status run_emb_backward(const int32_t* ids, const uint16_t* dY, int64_t N, in
   uint32_t* keys = static_cast<uint32_t*>(ws);
   const int64_t cmax = N < SORT_MAX ? N : SORT_MAX;
   int* seg = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + ((static_cast<size_t>(cmax) * 4 + 255) & ~static_cast<size_t>(255)));
-  const int64_t ncc = (h + 255) / 256;
   for (int64_t n0 = 0; n0 < N; n0 += SORT_MAX) {
     const int n = static_cast<int>(N - n0 < SORT_MAX ? N - n0 : SORT_MAX);
     emb_sort_kernel<<<1, SORT_THREADS, 2 * SORT_MAX * 4, s>>>(ids, n0, n, V, keys, seg, device_error_word());
