@@ -143,6 +143,7 @@ namespace {
 inline cudaStream_t S(tp_stream s) { return reinterpret_cast<cudaStream_t>(s); }
 
 bool act_ok(int a) { return a >= TP_ACT_IDENTITY && a <= TP_ACT_GELU_ERF; }
+bool mlp_act_ok(int a) { return act_ok(a) || a == TP_ACT_SWIGLU; }
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -459,20 +460,31 @@ tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int 
                          const tp_bf16* Wup_p, const tp_bf16* bup, const tp_bf16* Wdown_p, const tp_bf16* bdown,
                          const tp_bf16* residual, tp_bf16* Y, tp_bf16* Z_save, tp_bf16* A_save, unsigned flags,
                          void* ws, size_t ws_bytes, tp_stream stream) {
-  if (M < 0 || h < 1 || F < 1 || t < 1 || !act_ok(act)) return TP_ERR_INVALID_ARG;
+  if (M < 0 || h < 1 || F < 1 || t < 1 || !mlp_act_ok(act)) return TP_ERR_INVALID_ARG;
   if (F % t != 0) return TP_ERR_SHAPE;
   const int64_t Ft = F / t;
   if (h % 8 != 0 || Ft % 8 != 0) return TP_ERR_ALIGN;
+  const bool swiglu = act == TP_ACT_SWIGLU;
+  if (swiglu && Ft % 128 != 0) return TP_ERR_SHAPE;
+  if (swiglu && bup) return TP_ERR_UNSUPPORTED;
   if (M == 0) return TP_OK;  // no tokens: nothing to compute (buffers may be NULL)
-  if (!X || !Wup_p || !Wdown_p || !Y || !A_save) return TP_ERR_INVALID_ARG;
+  if (!X || !Wup_p || !Wdown_p || !Y || !A_save || (swiglu && !Z_save)) return TP_ERR_INVALID_ARG;
   const bool overlap = (flags & TP_FLAG_OVERLAP_REDUCE) != 0;
   const bool unfused = !overlap && (flags & TP_FLAG_UNFUSED_REDUCE) != 0;
   if (ws_bytes < tp_mlp_workspace_size(M, h, F, t, flags) || ((unfused || overlap) && !ws)) return TP_ERR_WORKSPACE;
   if (overlap && (M <= 128 || t > 8 || (t & (t - 1)) != 0)) return TP_ERR_UNSUPPORTED;
   const cudaStream_t s = S(stream);
 
-  // f (identity) + column-parallel: Z_i = X W_up,i + b_up[C_i]; A_i = act(Z_i).
-  TP_RETURN_IF(tp_column_parallel_forward(X, M, h, F, t, act, Wup_p, bup, Z_save, A_save, stream));
+  if (swiglu) {
+    // f (identity) + column-parallel over the interleaved gate / up weights: Z_i = X [W_gate | W_up]_i,
+    // then A_i = silu(gate) * up.
+    TP_RETURN_IF(tp_column_parallel_forward(X, M, h, 2 * F, t, TP_ACT_IDENTITY, Wup_p, nullptr, nullptr, Z_save,
+                                            stream));
+    TP_RETURN_IF(run_swiglu_act(Z_save, t * M, Ft, A_save, s));
+  } else {
+    // f (identity) + column-parallel: Z_i = X W_up,i + b_up[C_i]; A_i = act(Z_i).
+    TP_RETURN_IF(tp_column_parallel_forward(X, M, h, F, t, act, Wup_p, bup, Z_save, A_save, stream));
+  }
   if (overlap)
     return tp_row_parallel_forward_overlap(A_save, M, F, h, t, Wdown_p, bdown, residual, Y, nullptr, ws, ws_bytes,
                                            stream);
@@ -492,7 +504,9 @@ tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int 
 size_t tp_mlp_backward_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned flags) {
   if (M < 0 || h < 0 || F < 0 || t < 1) return 0;
   const int64_t Ft = F / t;
-  size_t sz = round_up(static_cast<size_t>(M) * F * 2, 256);  // dZ
+  // dZ (twice as wide under SwiGLU: gate and up), dA (SwiGLU only), column-sum scratch,
+  // partials: sized for every activation.
+  size_t sz = round_up(static_cast<size_t>(M) * F * 2 * 2, 256) + round_up(static_cast<size_t>(M) * F * 2, 256);
   const size_t cs = colsum2_ws_floats(M, h, 1) + colsum2_ws_floats(M, Ft, t);
   sz += round_up(cs * sizeof(float), 256);
   if (flags & TP_FLAG_UNFUSED_REDUCE) sz += static_cast<size_t>(t) * M * h * sizeof(float);
@@ -504,8 +518,11 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
                           const tp_bf16* Wdown_p, tp_bf16* dX, float* dWup_p, float* dWdown_p, float* dbup,
                           float* dbdown, int accumulate, unsigned flags, void* ws, size_t ws_bytes,
                           tp_stream stream) {
-  if (M < 0 || h < 1 || F < 1 || t < 1 || !act_ok(act)) return TP_ERR_INVALID_ARG;
+  if (M < 0 || h < 1 || F < 1 || t < 1 || !mlp_act_ok(act)) return TP_ERR_INVALID_ARG;
   if (!dWup_p || !dWdown_p) return TP_ERR_INVALID_ARG;
+  const bool swiglu = act == TP_ACT_SWIGLU;
+  if (swiglu && (F / t) % 128 != 0) return TP_ERR_SHAPE;
+  if (swiglu && dbup) return TP_ERR_UNSUPPORTED;
   if (M > 0 && (!dY || !X || !A_save || !Wup_p || !Wdown_p || !dX)) return TP_ERR_INVALID_ARG;
   if (M > 0 && act != TP_ACT_IDENTITY && !Z_save) return TP_ERR_INVALID_ARG;
   if (F % t != 0) return TP_ERR_SHAPE;
@@ -516,8 +533,11 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
   const cudaStream_t s = S(stream);
   const bool unfused = (flags & TP_FLAG_UNFUSED_REDUCE) != 0;
 
+  const int64_t Fzt = swiglu ? 2 * Ft : Ft;  // columns of a shard's Z / dZ
   uint8_t* w = static_cast<uint8_t*>(ws);
   uint16_t* dZ = reinterpret_cast<uint16_t*>(w);
+  w += round_up(static_cast<size_t>(M) * F * 2 * 2, 256);
+  uint16_t* dA = reinterpret_cast<uint16_t*>(w);  // SwiGLU: dL/dA before the gate / up split
   w += round_up(static_cast<size_t>(M) * F * 2, 256);
   float* cs_ws = reinterpret_cast<float*>(w);
   const size_t cs_floats = colsum2_ws_floats(M, h, 1) + colsum2_ws_floats(M, Ft, t);
@@ -527,7 +547,7 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
   if (M == 0) {  // no tokens: every gradient is zero (or unchanged when accumulating)
     if (!accumulate) {
       TP_RETURN_IF(ready());
-      TP_CUDA_CHECK(cudaMemsetAsync(dWup_p, 0, sizeof(float) * F * h, s));
+      TP_CUDA_CHECK(cudaMemsetAsync(dWup_p, 0, sizeof(float) * Fzt * t * h, s));
       TP_CUDA_CHECK(cudaMemsetAsync(dWdown_p, 0, sizeof(float) * F * h, s));
       if (dbup) TP_CUDA_CHECK(cudaMemsetAsync(dbup, 0, sizeof(float) * F, s));
       if (dbdown) TP_CUDA_CHECK(cudaMemsetAsync(dbdown, 0, sizeof(float) * h, s));
@@ -535,14 +555,21 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
     return TP_OK;
   }
 
-  // dgrad + act': dZ_i = (dY W_down,i^T) * act'(Z_i).
+  // dgrad + act': dZ_i = (dY W_down,i^T) * act'(Z_i).  SwiGLU: dA_i = dY W_down,i^T, then
+  // d gate = dA u silu'(gate), d up = dA silu(gate), interleaved like Z.
   GemmProblem g;
   g.M = M; g.N = Ft; g.K = h; g.nbatch = t;
   g.a.ptr = dY; g.a.ld = h;
   g.b.ptr = Wdown_p; g.b.ld = Ft; g.b.sharded = true; g.b.shard_stride = h * Ft; g.b.mn_major = true;
-  g.epi = EPI_DACT; g.act = act; g.aux = Z_save ? Z_save : A_save; g.ld_aux = Ft; g.aux_batch_stride = M * Ft;
-  g.d = dZ; g.ldd = Ft; g.d_batch_stride = M * Ft;
+  if (swiglu) {
+    g.epi = EPI_BF16;
+    g.d = dA; g.ldd = Ft; g.d_batch_stride = M * Ft;
+  } else {
+    g.epi = EPI_DACT; g.act = act; g.aux = Z_save ? Z_save : A_save; g.ld_aux = Ft; g.aux_batch_stride = M * Ft;
+    g.d = dZ; g.ldd = Ft; g.d_batch_stride = M * Ft;
+  }
   TP_RETURN_IF(run_gemm(g, s));
+  if (swiglu) TP_RETURN_IF(run_dswiglu(dA, Z_save, t * M, Ft, dZ, s));
 
   // Bias gradients, one fused pass: db_down = sum_rows dY, taken once (g backward is the
   // identity); db_up[C_i] = sum_rows dZ_i for every shard.
@@ -567,19 +594,19 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
   wd.epi = EPI_F32; wd.d = dWdown_p; wd.ldd = Ft; wd.d_batch_stride = h * Ft; wd.accumulate = accumulate;
   TP_RETURN_IF(run_gemm(wd, s));
 
-  // dW_up,i = dZ_i^T X -> packed [t][Ft][h].
+  // dW_up,i = dZ_i^T X -> packed [t][Ft][h] (SwiGLU: [t][2 Ft][h], tp_pack_swiglu's layout).
   GemmProblem wu;
-  wu.M = Ft; wu.N = h; wu.K = M; wu.nbatch = t;
-  wu.a.ptr = dZ; wu.a.ld = Ft; wu.a.sharded = true; wu.a.shard_stride = M * Ft; wu.a.mn_major = true;
+  wu.M = Fzt; wu.N = h; wu.K = M; wu.nbatch = t;
+  wu.a.ptr = dZ; wu.a.ld = Fzt; wu.a.sharded = true; wu.a.shard_stride = M * Fzt; wu.a.mn_major = true;
   wu.b.ptr = X; wu.b.ld = h; wu.b.mn_major = true;
-  wu.epi = EPI_F32; wu.d = dWup_p; wu.ldd = h; wu.d_batch_stride = Ft * h; wu.accumulate = accumulate;
+  wu.epi = EPI_F32; wu.d = dWup_p; wu.ldd = h; wu.d_batch_stride = Fzt * h; wu.accumulate = accumulate;
   TP_RETURN_IF(run_gemm(wu, s));
 
   // f backward: dX = sum_i dZ_i W_up,i^T.
   GemmProblem dx;
-  dx.M = M; dx.N = h; dx.K = Ft;
-  dx.a.ptr = dZ; dx.a.ld = Ft; dx.a.sharded = true; dx.a.shard_stride = M * Ft;
-  dx.b.ptr = Wup_p; dx.b.ld = h; dx.b.sharded = true; dx.b.shard_stride = Ft * h; dx.b.mn_major = true;
+  dx.M = M; dx.N = h; dx.K = Fzt;
+  dx.a.ptr = dZ; dx.a.ld = Fzt; dx.a.sharded = true; dx.a.shard_stride = M * Fzt;
+  dx.b.ptr = Wup_p; dx.b.ld = h; dx.b.sharded = true; dx.b.shard_stride = Fzt * h; dx.b.mn_major = true;
   if (!unfused) {
     dx.nsum = t;
     dx.epi = EPI_BF16; dx.d = dX; dx.ldd = h;

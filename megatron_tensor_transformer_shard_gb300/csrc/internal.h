@@ -226,6 +226,10 @@ tp_status run_ln_backward(const uint16_t* dY, const uint16_t* X, const uint16_t*
 // attention (attention.cu)
 // n_kv: KV heads (n_kv = n_heads for multi-head attention); QKV rows per shard are
 // [q_t query heads | kv_t K heads | kv_t V heads], 128 columns each.
+// SwiGLU of the token-parallel MLP (Z over the interleaved packed gate / up weights).
+tp_status run_swiglu_act(const uint16_t* Z, int64_t rows, int64_t Ft, uint16_t* A, cudaStream_t s);
+tp_status run_dswiglu(const uint16_t* dA, const uint16_t* Z, int64_t rows, int64_t Ft, uint16_t* dZ, cudaStream_t s);
+
 tp_status run_attention_fwd(const uint16_t* QKV, int64_t N, int64_t d, int n_heads, int n_kv, int head_dim, int t,
                             int causal, float scale, uint16_t* O, float* lse, cudaStream_t s);
 tp_status run_attention_bwd(const uint16_t* QKV, const uint16_t* O, const uint16_t* dO, const float* lse, int64_t N,

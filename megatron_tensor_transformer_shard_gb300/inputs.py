@@ -64,11 +64,14 @@ def mlp_inputs(M, h, F, bias=True, dy=True, seed=0, device="cpu"):
     return out
 
 
-def swiglu_inputs(M, h, F, seed=0, device="cpu"):
-    """x, W_gate (h, F), W_up (h, F), W_down (F, h), drawn in that order."""
+def swiglu_inputs(M, h, F, seed=0, device="cpu", dy=False):
+    """x, W_gate (h, F), W_up (h, F), W_down (F, h), and dY (M, h) if asked, drawn in that order."""
     g = make_generator(seed, device)
-    return {"X": _draw(g, (M, h), 1.0, device), "W_gate": _draw(g, (h, F), WEIGHT_STD, device),
-            "W_up": _draw(g, (h, F), WEIGHT_STD, device), "W_down": _draw(g, (F, h), WEIGHT_STD, device)}
+    out = {"X": _draw(g, (M, h), 1.0, device), "W_gate": _draw(g, (h, F), WEIGHT_STD, device),
+           "W_up": _draw(g, (h, F), WEIGHT_STD, device), "W_down": _draw(g, (F, h), WEIGHT_STD, device)}
+    if dy:
+        out["dY"] = _draw(g, (M, h), 1.0, device)
+    return out
 
 
 def attn_inputs(N, d, bias=True, dy=True, seed=0, device="cpu"):

@@ -43,12 +43,36 @@ class MLPWeights:
         self.b_up, self.b_down = b_up, b_down
 
 
+class SwiGLUWeights(MLPWeights):
+    """Packed per-shard weights of a SwiGLU MLP: W_gate and W_up (h, F) -> one
+    [t][2F/t][h] block (tp_pack_swiglu: gate and up rows alternate in groups of
+    128), W_down (F, h) -> [t][h][F/t].  No biases on the gate / up side."""
+
+    def __init__(self, W_gate, W_up, W_down, b_down, t):
+        h, F = W_up.shape
+        assert W_gate.shape == (h, F) and W_down.shape == (F, h) and F % t == 0
+        self.h, self.F, self.t = h, F, t
+        self.Wup_p = torch.empty(t, 2 * F // t, h, dtype=BF16, device=W_up.device)
+        self.Wdown_p = torch.empty(t, h, F // t, dtype=BF16, device=W_up.device)
+        L.tp_pack_swiglu(W_gate, W_up, h, F, t, self.Wup_p)
+        L.tp_pack_row(W_down, F, h, t, self.Wdown_p)
+        self.b_up, self.b_down = None, b_down
+
+
+def _z_cols(w, act):
+    """Columns of a shard's Z / dZ: twice F/t under SwiGLU (gate and up)."""
+    return (2 if _act(act) == L.ACT_BY_NAME["swiglu"] else 1) * (w.F // w.t)
+
+
 def mlp_forward(X, w: MLPWeights, act="gelu_tanh", residual=None, save_z=True, flags=0):
-    """Y = sum_i act(X W_up,i + b_up,i) W_down,i + b_down (+ residual).  Returns (Y, Z, A)."""
+    """Y = sum_i act(X W_up,i + b_up,i) W_down,i + b_down (+ residual).  Returns (Y, Z, A).
+    With act="swiglu" (SwiGLUWeights) A_i = silu(X W_gate,i) * (X W_up,i) and Z holds
+    the gate and up pre-activations, interleaved as in the packed weights."""
     M = X.shape[0]
     Y = torch.empty(M, w.h, dtype=BF16, device=X.device)
     A = torch.empty(w.t, M, w.F // w.t, dtype=BF16, device=X.device)
-    Z = torch.empty_like(A) if save_z else None
+    swiglu = _act(act) == L.ACT_BY_NAME["swiglu"]
+    Z = torch.empty(w.t, M, _z_cols(w, act), dtype=BF16, device=X.device) if (save_z or swiglu) else None
     nws = L.tp_mlp_workspace_size(M, w.h, w.F, w.t, flags)
     ws = _ws(nws, X.device)
     L.tp_mlp_forward(X, M, w.h, w.F, w.t, _act(act), w.Wup_p, w.b_up, w.Wdown_p, w.b_down, residual, Y, Z, A,
@@ -61,10 +85,11 @@ def mlp_backward(dY, X, Z, A, w: MLPWeights, act="gelu_tanh", flags=0, grads=Non
     (weight grads in the packed layouts, fp32).  Pass `grads` to accumulate."""
     M = X.shape[0]
     acc = grads is not None
+    swiglu = _act(act) == L.ACT_BY_NAME["swiglu"]
     if grads is None:
-        grads = {"dWup_p": torch.empty(w.t, w.F // w.t, w.h, dtype=torch.float32, device=X.device),
+        grads = {"dWup_p": torch.empty(w.t, _z_cols(w, act), w.h, dtype=torch.float32, device=X.device),
                  "dWdown_p": torch.empty(w.t, w.h, w.F // w.t, dtype=torch.float32, device=X.device),
-                 "dbup": torch.empty(w.F, dtype=torch.float32, device=X.device),
+                 "dbup": None if swiglu else torch.empty(w.F, dtype=torch.float32, device=X.device),
                  "dbdown": torch.empty(w.h, dtype=torch.float32, device=X.device)}
     dX = torch.empty(M, w.h, dtype=BF16, device=X.device)
     ws = _ws(L.tp_mlp_backward_workspace_size(M, w.h, w.F, w.t, flags), X.device)

@@ -363,3 +363,52 @@ def test_mlp_forward_graph_replay_matches_eager(M, h, F, t):
         assert torch.equal(Y.view(torch.int16), Y_eager.view(torch.int16))
         assert torch.equal(A.view(torch.int16), A_eager.view(torch.int16))
     assert L.tp_get_device_status(check=False) == L.TP_OK
+
+
+def _deinterleave(Z, group=128):
+    """[t][M][2 Ft] with gate / up in alternating groups -> (gate, up), each [t][M][Ft]."""
+    t, M, W = Z.shape
+    z = Z.reshape(t, M, W // (2 * group), 2, group)
+    return z[:, :, :, 0, :].reshape(t, M, W // 2), z[:, :, :, 1, :].reshape(t, M, W // 2)
+
+
+@pytest.mark.parametrize("M,h,F,t", [(256, 512, 2048, 4), (200, 264, 1024, 2), (1, 128, 512, 4),
+                                     (384, 1024, 4096, 8)])
+def test_swiglu_mlp_parity(M, h, F, t):
+    """Token-parallel SwiGLU MLP forward and backward ("(times 2 for SwiGLU)"): gate
+    and up split by the same columns, the row-parallel half and the f / g sums as for
+    GeLU; checked against the fp64 oracle, gradients in the packed layouts."""
+    inp = I.swiglu_inputs(M, h, F, seed=11, dy=True)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    ref = {k: f64(v) for k, v in inp.items()}
+    w = T.SwiGLUWeights(dev["W_gate"], dev["W_up"], dev["W_down"], None, t)
+    Y, Z, A = T.mlp_forward(dev["X"], w, "swiglu")
+    g = T.mlp_backward(dev["dY"], dev["X"], Z, A, w, "swiglu")
+    torch.cuda.synchronize()
+    assert L.tp_get_device_status(check=False) == L.TP_OK
+    o = O.swiglu_forward_sharded(ref["X"], ref["W_gate"], ref["W_up"], ref["W_down"], t)
+    b = O.swiglu_backward_sharded(ref["dY"], ref["X"], ref["W_gate"], ref["W_up"], ref["W_down"], o, t)
+    assert_close("Y", f64(Y), o["Y"])
+    assert_close("A", f64(A), np.stack(o["A"]))
+    zg, zu = _deinterleave(f64(Z))
+    assert_close("Z gate", zg, np.stack(o["Zg"]))
+    assert_close("Z up", zu, np.stack(o["Zu"]))
+    assert_close("dX", f64(g["dX"]), b["dX"])
+    dWgu = O.pack_swiglu_weight(b["dW_gate"], b["dW_up"], t).reshape(t, 2 * F // t, h)
+    assert_close("dW_gate/up (packed)", f64(g["dWup_p"]), dWgu)
+    assert_close("dW_down (packed)", f64(g["dWdown_p"]), O.pack_row_weight(b["dW_down"], t))
+    assert_close("db_down", f64(g["dbdown"]), ref["dY"].sum(axis=0))
+
+
+def test_swiglu_mlp_argument_errors():
+    M, h, F, t = 64, 128, 1024, 4
+    x = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
+    act = L.ACT_BY_NAME["swiglu"]
+    # a gate / up bias is not part of this SwiGLU; F/t must be a multiple of the 128-row groups
+    assert L.tp_mlp_forward(x, M, h, F, t, act, x, x, x, None, None, x, x, x, 0, None, 0,
+                            check=False) == L.TP_ERR_UNSUPPORTED
+    assert L.tp_mlp_forward(x, M, h, 4 * 192, t, act, x, None, x, None, None, x, x, x, 0, None, 0,
+                            check=False) == L.TP_ERR_SHAPE
+    # Z_save is required (the backward reads the gate and up pre-activations)
+    assert L.tp_mlp_forward(x, M, h, F, t, act, x, None, x, None, None, x, None, x, 0, None, 0,
+                            check=False) == L.TP_ERR_INVALID_ARG
