@@ -578,6 +578,37 @@ def run_mlp_fwd_extra(L, torch, args):
             "page_bytes": {"expanded_tensor": M * F * 2, "output_reduction_tensor": M * h * 2}}
 
 
+def run_swiglu_extra(L, torch, args):
+    """Token-parallel SwiGLU MLP fwd+bwd at decode-config weight shapes (Llama-3-70B-sized, t = 4)
+    over 2048 tokens: column-parallel GEMM over the interleaved gate / up weights, silu(gate) * up,
+    row-parallel GEMM + g; backward through dA, the gate / up gradient, both wgrads and the f sum."""
+    from megatron_tensor_transformer_shard_gb300 import inputs as I
+    from megatron_tensor_transformer_shard_gb300 import tp as T
+    M, h, F, t = 2048, 8192, 28672, 4
+    inp = I.swiglu_inputs(M, h, F, seed=0, device="cuda", dy=True)
+    w = T.SwiGLUWeights(inp["W_gate"], inp["W_up"], inp["W_down"], None, t)
+    del inp["W_gate"], inp["W_up"], inp["W_down"]
+    X, dY = inp["X"], inp["dY"]
+    Y, Z, A = T.mlp_forward(X, w, "swiglu")
+    grads = T.mlp_backward(dY, X, Z, A, w, "swiglu")
+    nws_f = L.tp_mlp_workspace_size(M, h, F, t, 0)
+    nws_b = L.tp_mlp_backward_workspace_size(M, h, F, t, 0)
+    wsb = torch.empty(nws_b, dtype=torch.uint8, device="cuda")
+    act = L.ACT_BY_NAME["swiglu"]
+    dX = torch.empty(M, h, dtype=torch.bfloat16, device="cuda")
+
+    def step():
+        L.tp_mlp_forward(X, M, h, F, t, act, w.Wup_p, None, w.Wdown_p, None, None, Y, Z, A, 0, None, nws_f)
+        L.tp_mlp_backward(dY, X, Z, A, M, h, F, t, act, w.Wup_p, w.Wdown_p, dX, grads["dWup_p"], grads["dWdown_p"],
+                          None, grads["dbdown"], 0, 0, wsb, nws_b)
+    ms = _time(torch, step, max(5, min(args.steps, 10)))
+    fl = 18.0 * M * h * F  # forward 6 M h F (gate + up + down), backward twice that
+    return {"workload": f"SwiGLU MLP fwd+bwd, t={t}, X {M}x{h}, W_gate/W_up {h}x{F}, W_down {F}x{h}",
+            "ms_per_step": round(ms, 3), "TFLOPs": round(fl / (ms / 1e3) / 1e12, 1), "flops_per_step": fl,
+            "note": "silu(gate) * up and its gradient run as separate elementwise kernels (not yet fused into "
+                    "the GEMM epilogues)"}
+
+
 def run_attn_extra(L, torch, args, name="c5"):
     """Head-sharded attention block alone at a layer config's shapes: QKV
     column-parallel GEMM, per-head causal flash attention, W_o row-parallel
@@ -793,6 +824,8 @@ def run_only(args):
         return {"decode_attention": run_decode_attn_extra(L, torch, args)}
     if args.only == "emb":
         return {"vocab_embedding": run_embedding_extra(L, torch, args)}
+    if args.only == "swiglu":
+        return {"swiglu_mlp": run_swiglu_extra(L, torch, args)}
     if args.only == "ovl":
         return {"row_parallel_overlap_c2": run_overlap_extra(L, torch, args)}
     return {f"layer_{args.only}": run_layer_extra(L, torch, args, args.only)}
@@ -809,7 +842,7 @@ def main():
     p.add_argument("--no-extras", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     p.add_argument("--reference-rows", type=int, default=64, help="token rows per oracle step (--impl reference)")
-    p.add_argument("--only", choices=["c1", "c3", "c4", "c5", "attn", "ln", "dattn", "emb", "ovl"], default=None,
+    p.add_argument("--only", choices=["c1", "c3", "c4", "c5", "attn", "ln", "dattn", "emb", "ovl", "swiglu"], default=None,
                    help="run only one secondary workload (forward MLP c1, decode c3, layers c4/c5, the c5-shaped "
                         "attention block, SP LayerNorm, decode attention over a sharded KV cache, the "
                         "vocab-parallel embedding or the overlapped row-parallel reduction) and print it")
