@@ -412,3 +412,23 @@ def test_swiglu_mlp_argument_errors():
     # Z_save is required (the backward reads the gate and up pre-activations)
     assert L.tp_mlp_forward(x, M, h, F, t, act, x, None, x, None, None, x, None, x, 0, None, 0,
                             check=False) == L.TP_ERR_INVALID_ARG
+
+
+def test_swiglu_autograd_function_accumulates():
+    """TPMLPFunction with act="swiglu": dX equals the direct backward, and a second
+    backward adds to the packed weight gradients kept on the weights object."""
+    M, h, F, t = 128, 256, 1024, 4
+    inp = I.swiglu_inputs(M, h, F, seed=17, dy=True)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    w = T.SwiGLUWeights(dev["W_gate"], dev["W_up"], dev["W_down"], None, t)
+    _, Z, A = T.mlp_forward(dev["X"], w, "swiglu")
+    ref = T.mlp_backward(dev["dY"], dev["X"], Z, A, w, "swiglu")
+    X = dev["X"].clone().requires_grad_(True)
+    for _ in range(2):
+        Y = T.TPMLPFunction.apply(X, w, "swiglu")
+        (dx,) = torch.autograd.grad(Y, X, dev["dY"])
+        assert torch.equal(dx.view(torch.int16), ref["dX"].view(torch.int16))
+    torch.cuda.synchronize()
+    assert w.grads["dbup"] is None
+    for k in ("dWup_p", "dWdown_p", "dbdown"):
+        assert torch.allclose(w.grads[k], 2 * ref[k], rtol=1e-5, atol=1e-6), k
