@@ -580,8 +580,9 @@ def run_mlp_fwd_extra(L, torch, args):
 
 def run_swiglu_extra(L, torch, args):
     """Token-parallel SwiGLU MLP fwd+bwd at decode-config weight shapes (Llama-3-70B-sized, t = 4)
-    over 2048 tokens: column-parallel GEMM over the interleaved gate / up weights, silu(gate) * up,
-    row-parallel GEMM + g; backward through dA, the gate / up gradient, both wgrads and the f sum."""
+    over 2048 tokens: column-parallel GEMM over the interleaved gate / up weights with silu(gate) * up
+    in its epilogue, row-parallel GEMM + g; backward: the dgrad GEMM whose epilogue forms the gate / up
+    gradient, both wgrads and the f sum."""
     from megatron_tensor_transformer_shard_gb300 import inputs as I
     from megatron_tensor_transformer_shard_gb300 import tp as T
     M, h, F, t = 2048, 8192, 28672, 4
@@ -605,8 +606,7 @@ def run_swiglu_extra(L, torch, args):
     fl = 18.0 * M * h * F  # forward 6 M h F (gate + up + down), backward twice that
     return {"workload": f"SwiGLU MLP fwd+bwd, t={t}, X {M}x{h}, W_gate/W_up {h}x{F}, W_down {F}x{h}",
             "ms_per_step": round(ms, 3), "TFLOPs": round(fl / (ms / 1e3) / 1e12, 1), "flops_per_step": fl,
-            "note": "silu(gate) * up and its gradient run as separate elementwise kernels (not yet fused into "
-                    "the GEMM epilogues)"}
+            "note": "silu(gate) * up and its gradient are computed in the GEMM epilogues"}
 
 
 def run_attn_extra(L, torch, args, name="c5"):

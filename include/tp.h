@@ -221,8 +221,9 @@ tp_status tp_row_parallel_forward_overlap(const tp_bf16* A, int64_t M, int64_t K
  * is twice as wide; gate and up split by the same C_i, so the product is local):
  *   Wup_p is tp_pack_swiglu's [t][2F/t][h] (gate and up rows in alternating groups
  *   of 128); Z_i = X [W_gate | W_up]_i is saved in the same interleaved order,
- *   Z_save [t][M][2F/t] (required); A_i = silu(gate) * up [t][M][F/t].  bup must be
- *   NULL (TP_ERR_UNSUPPORTED otherwise); (F/t) % 128 == 0 (TP_ERR_SHAPE). */
+ *   Z_save [t][M][2F/t] (required); A_i = silu(gate) * up [t][M][F/t], formed in the
+ *   GEMM's epilogue from the fp32 accumulators.  bup must be NULL (TP_ERR_UNSUPPORTED
+ *   otherwise); (F/t) % 128 == 0 (TP_ERR_SHAPE). */
 size_t tp_mlp_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned flags);
 tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int t, tp_act act,
                          const tp_bf16* Wup_p, const tp_bf16* bup, const tp_bf16* Wdown_p, const tp_bf16* bdown,
@@ -237,10 +238,10 @@ tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int 
  *   f backward (all-reduce): dX = sum_{i=0..t-1} dZ_i W_up,i^T (fused as in the forward).
  * Outputs: dX [M][h] bf16; dWup_p [t][F/t][h] and dWdown_p [t][h][F/t] fp32
  * (overwritten, or added to when `accumulate` != 0); dbup [F], dbdown [h] fp32
- * (nullable).  SWIGLU: dA_i = dY W_down,i^T, then d gate = dA u silu'(gate) and
- * d up = dA silu(gate), interleaved like Z_save; dWup_p is [t][2F/t][h] in
- * tp_pack_swiglu's layout; dbup must be NULL.  ws (the size query covers every
- * activation) holds dZ, dA (SwiGLU) and column-sum scratch. */
+ * (nullable).  SWIGLU: dA_i = dY W_down,i^T stays in the GEMM's fp32 accumulators; its
+ * epilogue writes d gate = dA u silu'(gate) and d up = dA silu(gate), interleaved like
+ * Z_save; dWup_p is [t][2F/t][h] in tp_pack_swiglu's layout; dbup must be NULL.  ws (the
+ * size query covers every activation) holds dZ and column-sum scratch. */
 size_t tp_mlp_backward_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned flags);
 tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_save, const tp_bf16* A_save,
                           int64_t M, int64_t h, int64_t F, int t, tp_act act, const tp_bf16* Wup_p,

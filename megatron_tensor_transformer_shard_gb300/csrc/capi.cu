@@ -477,10 +477,15 @@ tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int 
 
   if (swiglu) {
     // f (identity) + column-parallel over the interleaved gate / up weights: Z_i = X [W_gate | W_up]_i,
-    // then A_i = silu(gate) * up.
-    TP_RETURN_IF(tp_column_parallel_forward(X, M, h, 2 * F, t, TP_ACT_IDENTITY, Wup_p, nullptr, nullptr, Z_save,
-                                            stream));
-    TP_RETURN_IF(run_swiglu_act(Z_save, t * M, Ft, A_save, s));
+    // and A_i = silu(gate) * up in the same epilogue (a 256-column tile is one gate / up group).
+    GemmProblem c;
+    c.M = M; c.N = 2 * Ft; c.K = h; c.nbatch = t; c.nsum = 1;
+    c.a.ptr = X; c.a.ld = h;
+    c.b.ptr = Wup_p; c.b.ld = h; c.b.sharded = true; c.b.shard_stride = 2 * Ft * h;
+    c.epi = EPI_GLU;
+    c.d = Z_save; c.ldd = 2 * Ft; c.d_batch_stride = M * 2 * Ft;
+    c.d2 = A_save; c.ldd2 = Ft; c.d2_batch_stride = M * Ft;
+    TP_RETURN_IF(run_gemm(c, s));
   } else {
     // f (identity) + column-parallel: Z_i = X W_up,i + b_up[C_i]; A_i = act(Z_i).
     TP_RETURN_IF(tp_column_parallel_forward(X, M, h, F, t, act, Wup_p, bup, Z_save, A_save, stream));
@@ -504,9 +509,9 @@ tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int 
 size_t tp_mlp_backward_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned flags) {
   if (M < 0 || h < 0 || F < 0 || t < 1) return 0;
   const int64_t Ft = F / t;
-  // dZ (twice as wide under SwiGLU: gate and up), dA (SwiGLU only), column-sum scratch,
-  // partials: sized for every activation.
-  size_t sz = round_up(static_cast<size_t>(M) * F * 2 * 2, 256) + round_up(static_cast<size_t>(M) * F * 2, 256);
+  // dZ (twice as wide under SwiGLU: gate and up), column-sum scratch, partials: sized for
+  // every activation.
+  size_t sz = round_up(static_cast<size_t>(M) * F * 2 * 2, 256);
   const size_t cs = colsum2_ws_floats(M, h, 1) + colsum2_ws_floats(M, Ft, t);
   sz += round_up(cs * sizeof(float), 256);
   if (flags & TP_FLAG_UNFUSED_REDUCE) sz += static_cast<size_t>(t) * M * h * sizeof(float);
@@ -537,8 +542,6 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
   uint8_t* w = static_cast<uint8_t*>(ws);
   uint16_t* dZ = reinterpret_cast<uint16_t*>(w);
   w += round_up(static_cast<size_t>(M) * F * 2 * 2, 256);
-  uint16_t* dA = reinterpret_cast<uint16_t*>(w);  // SwiGLU: dL/dA before the gate / up split
-  w += round_up(static_cast<size_t>(M) * F * 2, 256);
   float* cs_ws = reinterpret_cast<float*>(w);
   const size_t cs_floats = colsum2_ws_floats(M, h, 1) + colsum2_ws_floats(M, Ft, t);
   w += round_up(cs_floats * sizeof(float), 256);
@@ -555,21 +558,20 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
     return TP_OK;
   }
 
-  // dgrad + act': dZ_i = (dY W_down,i^T) * act'(Z_i).  SwiGLU: dA_i = dY W_down,i^T, then
-  // d gate = dA u silu'(gate), d up = dA silu(gate), interleaved like Z.
+  // dgrad + act': dZ_i = (dY W_down,i^T) * act'(Z_i).  SwiGLU: the epilogue turns dA_i =
+  // dY W_down,i^T into d gate = dA u silu'(gate) and d up = dA silu(gate), interleaved like Z.
   GemmProblem g;
   g.M = M; g.N = Ft; g.K = h; g.nbatch = t;
   g.a.ptr = dY; g.a.ld = h;
   g.b.ptr = Wdown_p; g.b.ld = Ft; g.b.sharded = true; g.b.shard_stride = h * Ft; g.b.mn_major = true;
   if (swiglu) {
-    g.epi = EPI_BF16;
-    g.d = dA; g.ldd = Ft; g.d_batch_stride = M * Ft;
+    g.epi = EPI_DGLU; g.aux = Z_save; g.ld_aux = 2 * Ft; g.aux_batch_stride = M * 2 * Ft;
+    g.d = dZ; g.ldd = 2 * Ft; g.d_batch_stride = M * 2 * Ft;
   } else {
     g.epi = EPI_DACT; g.act = act; g.aux = Z_save ? Z_save : A_save; g.ld_aux = Ft; g.aux_batch_stride = M * Ft;
     g.d = dZ; g.ldd = Ft; g.d_batch_stride = M * Ft;
   }
   TP_RETURN_IF(run_gemm(g, s));
-  if (swiglu) TP_RETURN_IF(run_dswiglu(dA, Z_save, t * M, Ft, dZ, s));
 
   // Bias gradients, one fused pass: db_down = sum_rows dY, taken once (g backward is the
   // identity); db_up[C_i] = sum_rows dZ_i for every shard.

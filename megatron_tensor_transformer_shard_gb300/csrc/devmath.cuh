@@ -122,4 +122,12 @@ __device__ __forceinline__ float act_grad_t(float z) {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// Gradient of a = silu(g) u given da:  d up = da silu(g),  d gate = da u silu'(g) with
+// silu'(g) = s (1 + g (1 - s)), s = sigmoid(g).
+__device__ __forceinline__ void swiglu_grad(float g, float u, float da, float& dg, float& du) {
+  const float s = 1.0f / (1.0f + expf(-g));
+  dg = da * u * (s * (1.0f + g * (1.0f - s)));
+  du = da * (g * s);
+}
+
 }  // namespace tp

@@ -7,6 +7,9 @@
 //   dgrad            dZ_i = (dY W_down,i^T) * act'(Z_i)
 //   f backward       dX = sum_i dZ_i W_up,i^T
 //   wgrad            dW_down,i = A_i^T dY, dW_up,i = dZ_i^T X    (MN-major operands)
+//   SwiGLU           Z_i = X [W_gate | W_up]_i, A_i = silu(gate) up in the epilogue; its
+//                    dgrad epilogue turns dA into d gate / d up (gate / up interleaved in
+//                    groups of 128 columns, so one 256-column tile holds both halves)
 // ("02 — Tensor Parallelism", "Column-parallel vs row-parallel — the
 // derivation" and "The MLP pairing"; "Parallelism Strategies #1 - Tensor
 // Parallelism", sharded backward.)
@@ -64,6 +67,7 @@ struct GemmArgs {
   void* d;
   int64_t ldd, d_bs;
   void* d2;
+  int64_t ldd2, d2_bs;  // EPI_GLU: the activation output's strides
   const uint16_t* bias;
   int64_t bias_bs;
   const uint16_t* aux;
@@ -309,6 +313,54 @@ __device__ __forceinline__ void epilogue_values(const GemmArgs& p, int b, int m,
   }
 }
 
+// SwiGLU: columns [256 k, 256 k + 128) of Z hold the gate pre-activations of hidden
+// columns [128 k, 128 k + 128), the next 128 the up ones.
+constexpr int GLU_GROUP = 128;
+__device__ __forceinline__ int glu_gate_col(int c) { return (c / GLU_GROUP) * (2 * GLU_GROUP) + c % GLU_GROUP; }
+
+// EPI_GLU, per-thread stores: gate chunk rg (Z columns zg..zg+31 of row m) and the up chunk
+// 128 columns further -> Z (if kept) and A = silu(g) u at hidden columns glu_col(zg).
+__device__ __forceinline__ void glu_chunk(const GemmArgs& p, int b, int m, int zg, const uint32_t (&rg)[32],
+                                          const uint32_t (&ru)[32]) {
+  float g[32], u[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    g[j] = __uint_as_float(rg[j]);
+    u[j] = __uint_as_float(ru[j]);
+  }
+  if (p.d) {
+    uint16_t* zp = static_cast<uint16_t*>(p.d) + b * p.d_bs + static_cast<int64_t>(m) * p.ldd + zg;
+    store_bf16x32(zp, g);
+    store_bf16x32(zp + GLU_GROUP, u);
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) g[j] = silu(g[j]) * u[j];
+  const int ac = (zg / (2 * GLU_GROUP)) * GLU_GROUP + zg % (2 * GLU_GROUP);
+  store_bf16x32(static_cast<uint16_t*>(p.d2) + b * p.d2_bs + static_cast<int64_t>(m) * p.ldd2 + ac, g);
+}
+
+// EPI_DGLU for 32 hidden columns n0..n0+31 of row m (N is a multiple of 128, so a chunk is
+// whole): v = dA; reads gate / up from Z (aux), returns d gate in v and d up in v2.
+__device__ __forceinline__ void dglu_values(const GemmArgs& p, int b, int m, int n0, float (&v)[32],
+                                            float (&v2)[32]) {
+  const uint16_t* zp = p.aux + b * p.aux_bs + static_cast<int64_t>(m) * p.ld_aux + glu_gate_col(n0);
+  float g[32], u[32];
+  load_bf16x32(zp, g);
+  load_bf16x32(zp + GLU_GROUP, u);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) swiglu_grad(g[j], u[j], v[j], v[j], v2[j]);
+}
+
+__device__ __forceinline__ void dglu_chunk(const GemmArgs& p, int b, int m, int n0, const uint32_t (&r)[32]) {
+  float v[32], v2[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+  dglu_values(p, b, m, n0, v, v2);
+  uint16_t* dst = static_cast<uint16_t*>(p.d) + b * p.d_bs + static_cast<int64_t>(m) * p.ldd + glu_gate_col(n0);
+  store_bf16x32(dst, v);
+  store_bf16x32(dst + GLU_GROUP, v2);
+}
+
 // One thread's 32 values into 64 bytes (half of a 128-byte staging row), 2-byte format.
 __device__ __forceinline__ void stage_half_row16(uint8_t* buf, int row, int half, const float (&v)[32], bool f16) {
   uint8_t* rowp = buf + row * 128;
@@ -503,14 +555,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::tc_fence_after();
       const int m = mb * BM + row;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      if constexpr (EPI == EPI_GLU) {
+        // N is a multiple of 256: the tile is one whole gate / up group
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        const int n0 = nb * BN + c * 32;
-        if (n0 >= p.N) break;  // warp-uniform
-        uint32_t r[32];
-        ptx::tmem_ld32(t_row + c * 32, r);
-        ptx::tmem_ld_wait();
-        if (m < p.M) epilogue_chunk<EPI, ACT>(p, b, m, n0, r);
+        for (int c = 0; c < GLU_GROUP / 32; ++c) {
+          uint32_t rg[32], ru[32];
+          ptx::tmem_ld32(t_row + c * 32, rg);
+          ptx::tmem_ld32(t_row + GLU_GROUP + c * 32, ru);
+          ptx::tmem_ld_wait();
+          if (m < p.M) glu_chunk(p, b, m, nb * BN + c * 32, rg, ru);
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          const int n0 = nb * BN + c * 32;
+          if (n0 >= p.N) break;  // warp-uniform
+          uint32_t r[32];
+          ptx::tmem_ld32(t_row + c * 32, r);
+          ptx::tmem_ld_wait();
+          if (m < p.M) {
+            if constexpr (EPI == EPI_DGLU) dglu_chunk(p, b, m, n0, r);
+            else epilogue_chunk<EPI, ACT>(p, b, m, n0, r);
+          }
+        }
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(&tempty[acc]);
@@ -551,9 +618,12 @@ constexpr int STG_BOX_BYTES = 32 * 128;         // one 32-row x 128-byte output 
 // which buys a sixth pipeline stage.
 template <int EPI>
 struct PairCfg {
-  static constexpr int outputs = (EPI == EPI_ACT) ? 2 : 1;
-  static constexpr int stages = (EPI == EPI_ACT) ? 5 : 6;
-  static constexpr int stg_warp_bytes = 2 * outputs * STG_BOX_BYTES;  // double buffer per output
+  static constexpr int outputs = (EPI == EPI_GLU) ? 3 : (EPI == EPI_ACT || EPI == EPI_DGLU) ? 2 : 1;
+  static constexpr int stages = (EPI == EPI_ACT || EPI == EPI_GLU || EPI == EPI_DGLU) ? 5 : 6;
+  // The SwiGLU forward's three outputs are staged once, not twice, to keep the fifth
+  // operand stage (with four stages its GEMM ran ~7 % slower at K = 8192).
+  static constexpr int buffers = (EPI == EPI_GLU) ? 1 : 2;
+  static constexpr int stg_warp_bytes = buffers * outputs * STG_BOX_BYTES;
   static constexpr int stg_bytes = 4 * stg_warp_bytes;                 // 4 epilogue warps
   static constexpr int smem_bytes = 1024 + stages * P_STAGE_BYTES + stg_bytes + BAR_BYTES;
 };
@@ -949,7 +1019,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
     const int quad = warp & 3;
     const uint32_t tempty_leader0 = ptx::mapa_shared(ptx::smem_addr(&tempty[0]), 0);
     uint8_t* stg = sStage + quad * STG_WARP_BYTES;  // [buffer][output] boxes of this warp
-    const bool two_out = (EPI == EPI_ACT) && p.d != nullptr;
+    const bool two_out = (EPI == EPI_ACT || EPI == EPI_GLU) && p.d != nullptr;
     const bool wide = (EPI == EPI_F32);           // fp32 boxes hold 32 columns, 2-byte boxes 64
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -967,7 +1037,89 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
       const int m = mrow0 + lane;
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * P_BN);
-      if (!p.tma_store) {
+      if constexpr (EPI == EPI_GLU) {
+        // The tile is one gate / up group (N is a multiple of 256).  Per 64 hidden columns:
+        // Z's gate box, Z's up box (when Z is kept) and the activation box, three TMA stores.
+        if (mrow0 < p.M) {
+#pragma unroll 1
+          for (int g0 = 0; g0 < GLU_GROUP; g0 += 64) {
+            uint8_t* bufG = stg;  // one staging set: the previous step's stores must have read it
+            uint8_t* bufU = bufG + STG_BOX_BYTES;
+            uint8_t* bufA = bufU + STG_BOX_BYTES;
+            if (lane == 0) ptx::bulk_wait_group_read<0>();
+            __syncwarp();
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+              uint32_t rg[32], ru[32];
+              ptx::tmem_ld32(t_row + g0 + h * 32, rg);
+              ptx::tmem_ld32(t_row + GLU_GROUP + g0 + h * 32, ru);
+              ptx::tmem_ld_wait();
+              float g[32], u[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                g[j] = __uint_as_float(rg[j]);
+                u[j] = __uint_as_float(ru[j]);
+              }
+              if (two_out) {
+                stage_half_row16(bufG, lane, h, g, false);
+                stage_half_row16(bufU, lane, h, u, false);
+              }
+#pragma unroll
+              for (int j = 0; j < 32; ++j) g[j] = silu(g[j]) * u[j];
+              stage_half_row16(bufA, lane, h, g, false);
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const int zg = nb * P_BN + g0;
+              if (two_out) {
+                ptx::tma_store_3d(&tmD, bufG, zg, mrow0, b);
+                ptx::tma_store_3d(&tmD, bufU, zg + GLU_GROUP, mrow0, b);
+              }
+              ptx::tma_store_3d(&tmD2, bufA, nb * GLU_GROUP + g0, mrow0, b);
+              ptx::bulk_commit_group();
+            }
+            ++step;
+          }
+        }
+      } else if constexpr (EPI == EPI_DGLU) {
+        // dA columns n0.. of the tile -> d gate / d up boxes at their interleaved Z columns.
+        if (mrow0 < p.M) {
+#pragma unroll 1
+          for (int g0 = 0; g0 < P_BN; g0 += 64) {
+            const int n0 = nb * P_BN + g0;
+            if (n0 >= p.N) break;  // warp-uniform; N is a multiple of 128
+            uint8_t* bufG = stg + (step & 1) * (NOUT * STG_BOX_BYTES);
+            uint8_t* bufU = bufG + STG_BOX_BYTES;
+            if (lane == 0) ptx::bulk_wait_group_read<1>();
+            __syncwarp();
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+              uint32_t r[32];
+              ptx::tmem_ld32(t_row + g0 + h * 32, r);
+              ptx::tmem_ld_wait();
+              float v[32], v2[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                v[j] = __uint_as_float(r[j]);
+                v2[j] = 0.0f;
+              }
+              if (m < p.M) dglu_values(p, b, m, n0 + h * 32, v, v2);  // rows past M: clipped by the store
+              stage_half_row16(bufG, lane, h, v, false);
+              stage_half_row16(bufU, lane, h, v2, false);
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const int zg = glu_gate_col(n0);
+              ptx::tma_store_3d(&tmD, bufG, zg, mrow0, b);
+              ptx::tma_store_3d(&tmD, bufU, zg + GLU_GROUP, mrow0, b);
+              ptx::bulk_commit_group();
+            }
+            ++step;
+          }
+        }
+      } else if (!p.tma_store) {
 #pragma unroll 1
         for (int c = 0; c < P_BN / 32; ++c) {
           const int n0 = nb * P_BN + c * 32;
@@ -1233,7 +1385,10 @@ tp_status dispatch(bool amn, bool bmn, int epi, int act, F&& f) {
   using E_ACT = std::integral_constant<int, EPI_ACT>;
   using E_DACT = std::integral_constant<int, EPI_DACT>;
   using E_F32 = std::integral_constant<int, EPI_F32>;
+  using E_GLU = std::integral_constant<int, EPI_GLU>;
+  using E_DGLU = std::integral_constant<int, EPI_DGLU>;
   if (!amn && !bmn) {  // forward GEMMs
+    if (epi == EPI_GLU) return f(Fl{}, Fl{}, E_GLU{}, I0{});
     if (epi == EPI_ACT) {
       switch (act) {
         case 0: return f(Fl{}, Fl{}, E_ACT{}, I0{});
@@ -1245,6 +1400,7 @@ tp_status dispatch(bool amn, bool bmn, int epi, int act, F&& f) {
     if (epi == EPI_BF16) return f(Fl{}, Fl{}, E_BF16{}, I0{});
     if (epi == EPI_F32) return f(Fl{}, Fl{}, E_F32{}, I0{});
   } else if (!amn && bmn) {  // dgrad and f-reduced dX
+    if (epi == EPI_DGLU) return f(Fl{}, T{}, E_DGLU{}, I0{});
     if (epi == EPI_DACT) {
       switch (act) {
         case 0: return f(Fl{}, T{}, E_DACT{}, I0{});
@@ -1273,15 +1429,21 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
   if (P.M == 0 || P.N == 0) return TP_OK;
   if (P.nbatch > 1 && P.nsum > 1) return TP_ERR_INVALID_ARG;
   if (!operand_ok(P.a) || !operand_ok(P.b)) return TP_ERR_ALIGN;
-  if (P.epi == EPI_ACT) {
+  const bool glu = P.epi == EPI_GLU || P.epi == EPI_DGLU;
+  if (P.epi == EPI_ACT || P.epi == EPI_GLU) {
     if (!P.d2 || !aligned16(P.d2) || (P.d && !aligned16(P.d))) return TP_ERR_ALIGN;
   } else if (!P.d || !aligned16(P.d)) {
     return TP_ERR_ALIGN;
   }
   if (P.ldd % 8 != 0 || P.d_batch_stride % 8 != 0) return TP_ERR_ALIGN;
   if (P.bias && (!aligned16(P.bias) || P.bias_batch_stride % 8 != 0)) return TP_ERR_ALIGN;
-  if (P.epi == EPI_DACT && (!P.aux || !aligned16(P.aux) || P.ld_aux % 8 != 0 || P.aux_batch_stride % 8 != 0))
+  if ((P.epi == EPI_DACT || P.epi == EPI_DGLU) &&
+      (!P.aux || !aligned16(P.aux) || P.ld_aux % 8 != 0 || P.aux_batch_stride % 8 != 0))
     return TP_ERR_ALIGN;
+  // SwiGLU epilogues: whole gate / up groups per tile, no bias, no residual, bf16 outputs
+  if (glu && (P.N % (P.epi == EPI_GLU ? 2 * GLU_GROUP : GLU_GROUP) != 0)) return TP_ERR_SHAPE;
+  if (glu && (P.bias || P.residual || P.out_f16 || P.nsum != 1)) return TP_ERR_UNSUPPORTED;
+  if (P.epi == EPI_GLU && (P.ldd2 % 8 != 0 || P.d2_batch_stride % 8 != 0)) return TP_ERR_ALIGN;
   if (P.residual && (!aligned16(P.residual) || P.ld_res % 8 != 0)) return TP_ERR_ALIGN;
   if (P.K == 0) return TP_ERR_SHAPE;
   const int64_t mt = (P.M + BM - 1) / BM, nt = (P.N + BN - 1) / BN, kt = (P.K + BK - 1) / BK;
@@ -1321,6 +1483,8 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
   a.ldd = P.ldd;
   a.d_bs = P.d_batch_stride;
   a.d2 = P.d2;
+  a.ldd2 = P.ldd2;
+  a.d2_bs = P.d2_batch_stride;
   a.bias = P.bias;
   a.bias_bs = P.bias_batch_stride;
   a.aux = P.aux;
@@ -1352,12 +1516,22 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
       const CUtensorMapDataType dt = (P.epi == EPI_F32) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                      : (P.epi == EPI_ACT && P.out_f16) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-      void* d_main = (P.epi == EPI_ACT) ? (P.d ? P.d : P.d2) : P.d;
-      if (!make_output_map(&td, d_main, dt, esz, P.N, P.M, P.nbatch, P.ldd, P.d_batch_stride))
-        return TP_FAIL_DETAIL("tensor map of output D");
-      if (P.epi == EPI_ACT &&
-          !make_output_map(&td2, P.d2, dt, esz, P.N, P.M, P.nbatch, P.ldd, P.d_batch_stride))
-        return TP_FAIL_DETAIL("tensor map of output D2");
+      if (P.epi == EPI_GLU) {
+        // D = Z (N columns; mapped to D2 as a placeholder when Z is not kept), D2 = A (N / 2)
+        if (!make_output_map(&td, P.d ? P.d : P.d2, dt, esz, P.d ? P.N : P.N / 2, P.M, P.nbatch,
+                             P.d ? P.ldd : P.ldd2, P.d ? P.d_batch_stride : P.d2_batch_stride))
+          return TP_FAIL_DETAIL("tensor map of output Z");
+        if (!make_output_map(&td2, P.d2, dt, esz, P.N / 2, P.M, P.nbatch, P.ldd2, P.d2_batch_stride))
+          return TP_FAIL_DETAIL("tensor map of output A");
+      } else {
+        void* d_main = (P.epi == EPI_ACT) ? (P.d ? P.d : P.d2) : P.d;
+        const int64_t n_out = (P.epi == EPI_DGLU) ? 2 * P.N : P.N;  // dZ is twice as wide as dA
+        if (!make_output_map(&td, d_main, dt, esz, n_out, P.M, P.nbatch, P.ldd, P.d_batch_stride))
+          return TP_FAIL_DETAIL("tensor map of output D");
+        if (P.epi == EPI_ACT &&
+            !make_output_map(&td2, P.d2, dt, esz, P.N, P.M, P.nbatch, P.ldd, P.d_batch_stride))
+          return TP_FAIL_DETAIL("tensor map of output D2");
+      }
     }
     const int64_t ptiles = ((P.M + 255) / 256) * ((P.N + P_BN - 1) / P_BN) * P.nbatch;
     if (P.ovl_cnt) {  // its own instantiation: the other kernels keep their registers

@@ -88,6 +88,13 @@ enum GemmEpilogue : int {
   EPI_ACT = 1,    // Z = acc + bias_b[n];  D = bf16(Z) (nullable);  D2 = bf16(act(Z))
   EPI_DACT = 2,   // D = bf16(acc * act'(aux_b[m][n]))
   EPI_F32 = 3,    // D = acc (+ D if accumulate), fp32
+  // SwiGLU over the interleaved gate / up layout of tp_pack_swiglu (groups of 128 columns:
+  // gate, then up).  EPI_GLU: acc columns are Z's; D = bf16(Z) (nullable), D2 = bf16(silu(g) u)
+  // with its own stride (ldd2, d2_batch_stride).  EPI_DGLU: acc columns are dA's (N = the
+  // A width); aux = Z; D = dZ (gate and up interleaved like Z, row stride ldd):
+  // d gate = dA u silu'(g), d up = dA silu(g).
+  EPI_GLU = 4,
+  EPI_DGLU = 5,
 };
 
 struct GemmProblem {
@@ -98,7 +105,8 @@ struct GemmProblem {
   int act = TP_ACT_IDENTITY;
   void* d = nullptr;
   int64_t ldd = 0, d_batch_stride = 0;
-  void* d2 = nullptr;  // EPI_ACT: activation output, same layout as d
+  void* d2 = nullptr;  // EPI_ACT: activation output, same layout as d; EPI_GLU: silu(g) u
+  int64_t ldd2 = 0, d2_batch_stride = 0;  // EPI_GLU only (EPI_ACT's d2 shares d's strides)
   const uint16_t* bias = nullptr;
   int64_t bias_batch_stride = 0;
   const uint16_t* aux = nullptr;  // EPI_DACT: Z
@@ -227,8 +235,6 @@ tp_status run_ln_backward(const uint16_t* dY, const uint16_t* X, const uint16_t*
 // n_kv: KV heads (n_kv = n_heads for multi-head attention); QKV rows per shard are
 // [q_t query heads | kv_t K heads | kv_t V heads], 128 columns each.
 // SwiGLU of the token-parallel MLP (Z over the interleaved packed gate / up weights).
-tp_status run_swiglu_act(const uint16_t* Z, int64_t rows, int64_t Ft, uint16_t* A, cudaStream_t s);
-tp_status run_dswiglu(const uint16_t* dA, const uint16_t* Z, int64_t rows, int64_t Ft, uint16_t* dZ, cudaStream_t s);
 
 tp_status run_attention_fwd(const uint16_t* QKV, int64_t N, int64_t d, int n_heads, int n_kv, int head_dim, int t,
                             int causal, float scale, uint16_t* O, float* lse, cudaStream_t s);

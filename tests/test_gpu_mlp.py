@@ -378,6 +378,19 @@ def test_swiglu_mlp_parity(M, h, F, t):
     """Token-parallel SwiGLU MLP forward and backward ("(times 2 for SwiGLU)"): gate
     and up split by the same columns, the row-parallel half and the f / g sums as for
     GeLU; checked against the fp64 oracle, gradients in the packed layouts."""
+    _check_swiglu_mlp(M, h, F, t)
+
+
+@pytest.mark.parametrize("pair", ["0", "1"])
+def test_swiglu_fused_epilogues_both_kernels(pair, monkeypatch):
+    """silu(gate) * up and its gradient run in the GEMM epilogues of both the single-CTA and
+    the CTA-pair kernel.  F / t = 384: the dgrad's last 256-column tile of dA is half past
+    N, so its second gate / up group is skipped; M = 300 leaves a ragged row tile."""
+    monkeypatch.setenv("TP_GEMM_PAIR", pair)
+    _check_swiglu_mlp(300, 256, 768, 2)
+
+
+def _check_swiglu_mlp(M, h, F, t):
     inp = I.swiglu_inputs(M, h, F, seed=11, dy=True)
     dev = {k: v.cuda() for k, v in inp.items()}
     ref = {k: f64(v) for k, v in inp.items()}
