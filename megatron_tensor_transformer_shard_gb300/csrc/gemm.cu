@@ -62,6 +62,9 @@ struct GemmArgs {
   int M, N;
   int nbatch, nsum;
   int a_sharded, b_sharded;
+  // MN-major operand viewed through a 4-D map (64 columns, K, 64-column chunks, shard): the
+  // whole tile's row range in one copy per stage (only when its row count is a multiple of 64)
+  int a_4d, b_4d;
   int mt, nt, kt;
   int epi, act;
   void* d;
@@ -469,6 +472,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint8_t* b_dst = sB + stage * B_TILE_BYTES;
           if (!A_MN) {
             ptx::tma_load_3d(a_dst, &tmA, &full[stage], kb * BK, mb * BM, ash);
+          } else if (p.a_4d) {
+            ptx::tma_load_4d(a_dst, &tmA, &full[stage], 0, kb * BK, mb * (BM / 64), ash);
           } else {
 #pragma unroll
             for (int j = 0; j < BM / 64; ++j)
@@ -476,6 +481,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           if (!B_MN) {
             ptx::tma_load_3d(b_dst, &tmB, &full[stage], kb * BK, nb * BN, bsh);
+          } else if (p.b_4d) {
+            ptx::tma_load_4d(b_dst, &tmB, &full[stage], 0, kb * BK, nb * (BN / 64), bsh);
           } else {
 #pragma unroll
             for (int j = 0; j < BN / 64; ++j)
@@ -938,6 +945,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
           uint8_t* b_dst = sB + stage * P_B_BYTES;
           if (!A_MN) {
             ptx::tma_load_3d_pair(a_dst, &tmA, bar, kb * BK, m0, ash);
+          } else if (p.a_4d) {
+            ptx::tma_load_4d_pair(a_dst, &tmA, bar, 0, kb * BK, m0 / 64, ash);
           } else {
 #pragma unroll
             for (int j = 0; j < P_HALF / 64; ++j)
@@ -945,6 +954,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
           }
           if (!B_MN) {
             ptx::tma_load_3d_pair(b_dst, &tmB, bar, kb * BK, n0, bsh);
+          } else if (p.b_4d) {
+            ptx::tma_load_4d_pair(b_dst, &tmB, bar, 0, kb * BK, n0 / 64, bsh);
           } else {
 #pragma unroll
             for (int j = 0; j < P_HALF / 64; ++j)
@@ -1236,9 +1247,35 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // K-major: inner = K, outer = rows, box = 64 x box_rows.
 // MN-major: inner = rows (MN), outer = K, box = 64 x 64.
 bool make_operand_map(CUtensorMap* map, const GemmOperand& op, int64_t rows, int64_t K, int nshards,
-                      int box_rows) {
+                      int box_rows, int* four_d) {
   auto enc = encode_fn();
   if (!enc) return false;
+  *four_d = 0;
+  if (op.mn_major && rows % 64 == 0) {
+    // MN-major [shard][K][rows] as (64 columns, K, rows / 64 chunks, shard): the chunk stride
+    // (128 bytes) is below the K stride, so one box of box_rows / 64 chunks lands in shared
+    // memory as [chunk][K][64], the layout of the 64-column boxes it replaces.  A row count
+    // that is not a multiple of 64 keeps the per-chunk boxes (a 4-D box would read past it).
+    const int64_t ss = (op.sharded && nshards > 1) ? op.shard_stride : op.ld * K;
+    cuuint64_t d4[4] = {64, static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows / 64),
+                        static_cast<cuuint64_t>(nshards)};
+    cuuint64_t s4[3] = {static_cast<cuuint64_t>(op.ld) * 2, 128, static_cast<cuuint64_t>(ss) * 2};
+    cuuint32_t b4[4] = {64, BK, static_cast<cuuint32_t>(box_rows / 64), 1};
+    cuuint32_t e4[4] = {1, 1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(op.ptr), d4, s4, b4, e4,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      char buf[200];
+      std::snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled (4-D MN-major)=%d ptr=%p rows=%lld K=%lld ld=%lld",
+                    static_cast<int>(r), static_cast<const void*>(op.ptr), static_cast<long long>(rows),
+                    static_cast<long long>(K), static_cast<long long>(op.ld));
+      set_error_detail(__FILE__, __LINE__, buf);
+      return false;
+    }
+    *four_d = 1;
+    return true;
+  }
   cuuint64_t dims[3];
   cuuint64_t strides[2];
   cuuint32_t box[3];
@@ -1464,8 +1501,9 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
         cudaMemsetAsync(P.ovl_cnt, 0, static_cast<size_t>(gemm_overlap_counters(P.M, P.N)) * sizeof(int), s));
   }
   CUtensorMap ta, tb;
-  if (!make_operand_map(&ta, P.a, P.M, P.K, nsh_a, BM)) return TP_ERR_CUDA;
-  if (!make_operand_map(&tb, P.b, P.N, P.K, nsh_b, pair ? P_HALF : BN)) return TP_ERR_CUDA;
+  int a_4d = 0, b_4d = 0;
+  if (!make_operand_map(&ta, P.a, P.M, P.K, nsh_a, BM, &a_4d)) return TP_ERR_CUDA;
+  if (!make_operand_map(&tb, P.b, P.N, P.K, nsh_b, pair ? P_HALF : BN, &b_4d)) return TP_ERR_CUDA;
 
   GemmArgs a{};
   a.M = static_cast<int>(P.M);
@@ -1474,6 +1512,8 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
   a.nsum = P.nsum;
   a.a_sharded = P.a.sharded;
   a.b_sharded = P.b.sharded;
+  a.a_4d = a_4d;
+  a.b_4d = b_4d;
   a.mt = static_cast<int>(mt);
   a.nt = static_cast<int>(nt);
   a.kt = static_cast<int>(kt);
