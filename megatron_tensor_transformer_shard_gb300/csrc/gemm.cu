@@ -626,10 +626,12 @@ constexpr int STG_BOX_BYTES = 32 * 128;         // one 32-row x 128-byte output 
 template <int EPI>
 struct PairCfg {
   static constexpr int outputs = (EPI == EPI_GLU) ? 3 : (EPI == EPI_ACT || EPI == EPI_DGLU) ? 2 : 1;
-  static constexpr int stages = (EPI == EPI_ACT || EPI == EPI_GLU || EPI == EPI_DGLU) ? 5 : 6;
-  // The SwiGLU forward's three outputs are staged once, not twice, to keep the fifth
-  // operand stage (with four stages its GEMM ran ~7 % slower at K = 8192).
-  static constexpr int buffers = (EPI == EPI_GLU) ? 1 : 2;
+  static constexpr int stages = (EPI == EPI_GLU || EPI == EPI_DGLU) ? 5 : 6;
+  // Staging once instead of twice leaves room for one more operand stage: the epilogue then
+  // waits for the previous box's stores to finish reading shared memory, which costs less
+  // than the stage (SwiGLU forward: 5 stages instead of 4, ~7 % faster at K = 8192; GeLU:
+  // 6 instead of 5, 2-4 % faster).
+  static constexpr int buffers = (EPI == EPI_GLU || EPI == EPI_ACT) ? 1 : 2;
   static constexpr int stg_warp_bytes = buffers * outputs * STG_BOX_BYTES;
   static constexpr int stg_bytes = 4 * stg_warp_bytes;                 // 4 epilogue warps
   static constexpr int smem_bytes = 1024 + stages * P_STAGE_BYTES + stg_bytes + BAR_BYTES;
@@ -1146,10 +1148,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
         for (int g0 = 0; g0 < P_BN; g0 += box_cols) {
           const int n0 = nb * P_BN + g0;
           if (n0 >= p.N) break;  // warp-uniform
-          uint8_t* bufD = stg + (step & 1) * (NOUT * STG_BOX_BYTES);
+          constexpr int NBUF = PairCfg<EPI>::buffers;
+          uint8_t* bufD = stg + (NBUF == 2 ? (step & 1) : 0) * (NOUT * STG_BOX_BYTES);
           uint8_t* bufD2 = bufD + (NOUT - 1) * STG_BOX_BYTES;  // second output (EPI_ACT only)
-          // this buffer pair was last handed to TMA two steps ago: it must have been read
-          if (lane == 0) ptx::bulk_wait_group_read<1>();
+          // a buffer is reused NBUF steps after it was handed to TMA: it must have been read
+          if (lane == 0) ptx::bulk_wait_group_read<NBUF - 1>();
           __syncwarp();
 #pragma unroll 1
           for (int h = 0; h < box_cols / 32; ++h) {
