@@ -62,8 +62,9 @@ struct GemmArgs {
   int M, N;
   int nbatch, nsum;
   int a_sharded, b_sharded;
-  // MN-major operand viewed through a 4-D map (64 columns, K, 64-column chunks, shard): the
-  // whole tile's row range in one copy per stage (only when its row count is a multiple of 64)
+  // Operand viewed through a 4-D map, one copy per stage: MN-major (64 columns, K, 64-column
+  // chunks, shard) when its row count is a multiple of 64; K-major in the pair kernel's
+  // two-k-block stages (64 K, rows, k-blocks, shard) when K is a multiple of 64.
   int a_4d, b_4d;
   int mt, nt, kt;
   int epi, act;
@@ -621,12 +622,17 @@ constexpr int P_A_BYTES = P_HALF * BK * 2;      // 16 KB
 constexpr int P_B_BYTES = P_HALF * BK * 2;      // 16 KB
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 constexpr int STG_BOX_BYTES = 32 * 128;         // one 32-row x 128-byte output box
-// Epilogues with one output (everything but EPI_ACT) need half the staging,
-// which buys a sixth pipeline stage.
+// 64-wide k-blocks per pipeline stage of the pair kernel.  One-output epilogues take two:
+// each operand then arrives in one 32 KB copy per stage (three stages of 64 KB), which halves
+// the copies and barrier round trips per MMA and ran 1.5-3 % faster at K = 2048 (no gain
+// for the GeLU epilogue, which keeps six single-block stages).
+constexpr int pair_kb(int epi) { return (epi == EPI_F32 || epi == EPI_BF16 || epi == EPI_DACT) ? 2 : 1; }
+
 template <int EPI>
 struct PairCfg {
   static constexpr int outputs = (EPI == EPI_GLU) ? 3 : (EPI == EPI_ACT || EPI == EPI_DGLU) ? 2 : 1;
-  static constexpr int stages = (EPI == EPI_GLU || EPI == EPI_DGLU) ? 5 : 6;
+  static constexpr int kb = pair_kb(EPI);
+  static constexpr int stages = (kb == 2) ? 3 : (EPI == EPI_GLU || EPI == EPI_DGLU) ? 5 : 6;
   // Staging once instead of twice leaves room for one more operand stage: the epilogue then
   // waits for the previous box's stores to finish reading shared memory, which costs less
   // than the stage (SwiGLU forward: 5 stages instead of 4, ~7 % faster at K = 8192; GeLU:
@@ -634,7 +640,7 @@ struct PairCfg {
   static constexpr int buffers = (EPI == EPI_GLU || EPI == EPI_ACT) ? 1 : 2;
   static constexpr int stg_warp_bytes = buffers * outputs * STG_BOX_BYTES;
   static constexpr int stg_bytes = 4 * stg_warp_bytes;                 // 4 epilogue warps
-  static constexpr int smem_bytes = 1024 + stages * P_STAGE_BYTES + stg_bytes + BAR_BYTES;
+  static constexpr int smem_bytes = 1024 + stages * kb * P_STAGE_BYTES + stg_bytes + BAR_BYTES;
 };
 
 // Overlapped shard reduction.  Epilogue warps write each tile's fp32 partial;
@@ -862,12 +868,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
   constexpr int STG_BYTES = PairCfg<EPI>::stg_bytes;
   constexpr int STG_WARP_BYTES = PairCfg<EPI>::stg_warp_bytes;
   constexpr int NOUT = PairCfg<EPI>::outputs;
+  constexpr int KB = PairCfg<EPI>::kb;
+  constexpr int SA_BYTES = KB * P_A_BYTES;  // one stage of A (B: the same)
   extern __shared__ uint8_t dsmem[];
   const uint32_t pad = (1024u - (ptx::smem_addr(dsmem) & 1023u)) & 1023u;
   uint8_t* base = dsmem + pad;
   uint8_t* sA = base;
-  uint8_t* sB = base + P_STAGES * P_A_BYTES;
-  uint8_t* sStage = base + P_STAGES * P_STAGE_BYTES;  // epilogue output staging (1024-byte aligned boxes)
+  uint8_t* sB = base + P_STAGES * SA_BYTES;
+  uint8_t* sStage = base + P_STAGES * 2 * SA_BYTES;  // epilogue output staging (1024-byte aligned boxes)
   uint64_t* full = reinterpret_cast<uint64_t*>(sStage + STG_BYTES);
   uint64_t* empty = full + P_STAGES;
   uint64_t* tfull = empty + P_STAGES;
@@ -911,7 +919,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
   const int mt2 = (p.M + 2 * P_HALF - 1) / (2 * P_HALF);
   const int nt2 = (p.N + P_BN - 1) / P_BN;
   const int total = p.nbatch * mt2 * nt2;
-  const int ksteps = p.nsum * p.kt;
+  const int kt2 = (p.kt + KB - 1) / KB;  // stages per shard of K
+  const int ksteps = p.nsum * kt2;
   // Programmatic dependent launch (not for the overlapped form, whose queues are
   // written before its producers start): as in gemm_kernel, every global access
   // follows the producers' griddepcontrol.wait.
@@ -933,35 +942,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
         const int m0 = mb * 2 * P_HALF + static_cast<int>(rank) * P_HALF;
         const int n0 = nb * P_BN + static_cast<int>(rank) * P_HALF;
         for (int ks = 0; ks < ksteps; ++ks) {
-          const int s = ks / p.kt;
-          const int kb = ks - s * p.kt;
+          const int s = ks / kt2;
+          const int kb = (ks - s * kt2) * KB;  // first 64-wide k-block of this stage
           if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err, ERR_WAIT_PRODUCER, p.timeout_ns)) {
             ok = false;
             break;
           }
           const uint32_t bar = ptx::mapa_shared(ptx::smem_addr(&full[stage]), 0);
-          if (leader) ptx::mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE_BYTES);
+          if (leader) ptx::mbar_arrive_expect_tx(&full[stage], 2 * 2 * SA_BYTES);
           const int ash = p.a_sharded ? (p.nsum > 1 ? s : b) : 0;
           const int bsh = p.b_sharded ? (p.nsum > 1 ? s : b) : 0;
-          uint8_t* a_dst = sA + stage * P_A_BYTES;
-          uint8_t* b_dst = sB + stage * P_B_BYTES;
+          uint8_t* a_dst = sA + stage * SA_BYTES;
+          uint8_t* b_dst = sB + stage * SA_BYTES;
+          // One copy per operand where the 4-D view applies; else one copy per k-block
+          // (K-major, 16 KB panels) or per 64-column chunk (MN-major, 64 * KB K-rows deep).
+          // k-blocks past K arrive zero-filled.
           if (!A_MN) {
-            ptx::tma_load_3d_pair(a_dst, &tmA, bar, kb * BK, m0, ash);
+            if (KB == 2 && p.a_4d) {
+              ptx::tma_load_4d_pair(a_dst, &tmA, bar, 0, m0, kb, ash);
+            } else {
+#pragma unroll
+              for (int j = 0; j < KB; ++j) ptx::tma_load_3d_pair(a_dst + j * P_A_BYTES, &tmA, bar, (kb + j) * BK, m0, ash);
+            }
           } else if (p.a_4d) {
             ptx::tma_load_4d_pair(a_dst, &tmA, bar, 0, kb * BK, m0 / 64, ash);
           } else {
 #pragma unroll
             for (int j = 0; j < P_HALF / 64; ++j)
-              ptx::tma_load_3d_pair(a_dst + j * MN_CHUNK_BYTES, &tmA, bar, m0 + j * 64, kb * BK, ash);
+              ptx::tma_load_3d_pair(a_dst + j * KB * MN_CHUNK_BYTES, &tmA, bar, m0 + j * 64, kb * BK, ash);
           }
           if (!B_MN) {
-            ptx::tma_load_3d_pair(b_dst, &tmB, bar, kb * BK, n0, bsh);
+            if (KB == 2 && p.b_4d) {
+              ptx::tma_load_4d_pair(b_dst, &tmB, bar, 0, n0, kb, bsh);
+            } else {
+#pragma unroll
+              for (int j = 0; j < KB; ++j) ptx::tma_load_3d_pair(b_dst + j * P_B_BYTES, &tmB, bar, (kb + j) * BK, n0, bsh);
+            }
           } else if (p.b_4d) {
             ptx::tma_load_4d_pair(b_dst, &tmB, bar, 0, kb * BK, n0 / 64, bsh);
           } else {
 #pragma unroll
             for (int j = 0; j < P_HALF / 64; ++j)
-              ptx::tma_load_3d_pair(b_dst + j * MN_CHUNK_BYTES, &tmB, bar, n0 + j * 64, kb * BK, bsh);
+              ptx::tma_load_3d_pair(b_dst + j * KB * MN_CHUNK_BYTES, &tmB, bar, n0 + j * 64, kb * BK, bsh);
           }
           ++issued;
           if (++stage == P_STAGES) {
@@ -998,14 +1020,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t a_addr = ptx::smem_addr(sA + stage * P_A_BYTES);
-          const uint32_t b_addr = ptx::smem_addr(sB + stage * P_B_BYTES);
+          const uint32_t a_addr = ptx::smem_addr(sA + stage * SA_BYTES);
+          const uint32_t b_addr = ptx::smem_addr(sB + stage * SA_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = A_MN ? ptx::sdesc_sw128(a_addr + kk * 2048, MN_CHUNK_BYTES, 1024)
-                                     : ptx::sdesc_sw128(a_addr + kk * 32, 16, 1024);
-            const uint64_t bd = B_MN ? ptx::sdesc_sw128(b_addr + kk * 2048, MN_CHUNK_BYTES, 1024)
-                                     : ptx::sdesc_sw128(b_addr + kk * 32, 16, 1024);
+          for (int kk = 0; kk < KB * BK / 16; ++kk) {
+            // K-major: a 16 KB panel per 64-wide k-block, 32 bytes per K = 16 inside it.
+            // MN-major: 64 * KB K-rows per 64-column chunk, chunks KB * 8 KB apart.
+            const uint64_t ad = A_MN ? ptx::sdesc_sw128(a_addr + kk * 2048, KB * MN_CHUNK_BYTES, 1024)
+                                     : ptx::sdesc_sw128(a_addr + (kk >> 2) * P_A_BYTES + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = B_MN ? ptx::sdesc_sw128(b_addr + kk * 2048, KB * MN_CHUNK_BYTES, 1024)
+                                     : ptx::sdesc_sw128(b_addr + (kk >> 2) * P_B_BYTES + (kk & 3) * 32, 16, 1024);
             ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
           }
           ptx::mma_commit_pair_mc(&empty[stage], 0x3);  // frees this stage in both CTAs
@@ -1247,13 +1271,38 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 3-D map (inner, outer, shard) over a bf16 operand with a 128-byte swizzle.
-// K-major: inner = K, outer = rows, box = 64 x box_rows.
-// MN-major: inner = rows (MN), outer = K, box = 64 x 64.
+// K-major: inner = K, outer = rows, box = 64 x box_rows (4-D: two k-blocks per box when kb = 2).
+// MN-major: inner = rows (MN), outer = K, box = 64 x 64 kb (4-D: every 64-column chunk of the
+// box_rows in one box).  kb = 64-wide k-blocks per pipeline stage.
 bool make_operand_map(CUtensorMap* map, const GemmOperand& op, int64_t rows, int64_t K, int nshards,
-                      int box_rows, int* four_d) {
+                      int box_rows, int kb, int* four_d) {
   auto enc = encode_fn();
   if (!enc) return false;
   *four_d = 0;
+  if (!op.mn_major && kb == 2 && K % 64 == 0) {
+    // K-major [shard][rows][K] as (64 K, rows, K / 64 blocks, shard): one box of two k-blocks
+    // lands as two [rows][64] panels.  K not a multiple of 64 keeps one box per k-block (a
+    // 4-D box would read the next row's first columns past K instead of zeros).
+    const int64_t ss = (op.sharded && nshards > 1) ? op.shard_stride : op.ld * rows;
+    cuuint64_t d4[4] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(K / 64),
+                        static_cast<cuuint64_t>(nshards)};
+    cuuint64_t s4[3] = {static_cast<cuuint64_t>(op.ld) * 2, 128, static_cast<cuuint64_t>(ss) * 2};
+    cuuint32_t b4[4] = {64, static_cast<cuuint32_t>(box_rows), 2, 1};
+    cuuint32_t e4[4] = {1, 1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(op.ptr), d4, s4, b4, e4,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      char buf[200];
+      std::snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled (4-D K-major)=%d ptr=%p rows=%lld K=%lld ld=%lld",
+                    static_cast<int>(r), static_cast<const void*>(op.ptr), static_cast<long long>(rows),
+                    static_cast<long long>(K), static_cast<long long>(op.ld));
+      set_error_detail(__FILE__, __LINE__, buf);
+      return false;
+    }
+    *four_d = 1;
+    return true;
+  }
   if (op.mn_major && rows % 64 == 0) {
     // MN-major [shard][K][rows] as (64 columns, K, rows / 64 chunks, shard): the chunk stride
     // (128 bytes) is below the K stride, so one box of box_rows / 64 chunks lands in shared
@@ -1263,7 +1312,7 @@ bool make_operand_map(CUtensorMap* map, const GemmOperand& op, int64_t rows, int
     cuuint64_t d4[4] = {64, static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows / 64),
                         static_cast<cuuint64_t>(nshards)};
     cuuint64_t s4[3] = {static_cast<cuuint64_t>(op.ld) * 2, 128, static_cast<cuuint64_t>(ss) * 2};
-    cuuint32_t b4[4] = {64, BK, static_cast<cuuint32_t>(box_rows / 64), 1};
+    cuuint32_t b4[4] = {64, static_cast<cuuint32_t>(BK * kb), static_cast<cuuint32_t>(box_rows / 64), 1};
     cuuint32_t e4[4] = {1, 1, 1, 1};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(op.ptr), d4, s4, b4, e4,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1293,7 +1342,7 @@ bool make_operand_map(CUtensorMap* map, const GemmOperand& op, int64_t rows, int
     dims[0] = static_cast<cuuint64_t>(rows);
     dims[1] = static_cast<cuuint64_t>(K);
     box[0] = 64;
-    box[1] = BK;
+    box[1] = static_cast<cuuint32_t>(BK * kb);
   }
   dims[2] = static_cast<cuuint64_t>(nshards);
   box[2] = 1;
@@ -1505,8 +1554,9 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
   }
   CUtensorMap ta, tb;
   int a_4d = 0, b_4d = 0;
-  if (!make_operand_map(&ta, P.a, P.M, P.K, nsh_a, BM, &a_4d)) return TP_ERR_CUDA;
-  if (!make_operand_map(&tb, P.b, P.N, P.K, nsh_b, pair ? P_HALF : BN, &b_4d)) return TP_ERR_CUDA;
+  const int kb = pair ? pair_kb(P.ovl_cnt ? static_cast<int>(EPI_F32) : P.epi) : 1;  // k-blocks per stage
+  if (!make_operand_map(&ta, P.a, P.M, P.K, nsh_a, BM, kb, &a_4d)) return TP_ERR_CUDA;
+  if (!make_operand_map(&tb, P.b, P.N, P.K, nsh_b, pair ? P_HALF : BN, kb, &b_4d)) return TP_ERR_CUDA;
 
   GemmArgs a{};
   a.M = static_cast<int>(P.M);
