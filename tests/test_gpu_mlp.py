@@ -177,6 +177,23 @@ def test_single_cta_and_pair_gemm_paths(M, h, F, t, pair, monkeypatch):
     _backward_check(M, h, F, t, "gelu_tanh", seed=8)
 
 
+@pytest.mark.parametrize("pair", ["0", "1"])
+def test_gemm_operand_copies_odd_k_blocks(pair, monkeypatch):
+    """Operand tiles arrive in one 4-D TMA copy per stage where K (K-major) or the row count
+    (MN-major) is a multiple of 64, and one-output GEMMs of the pair kernel take two 64-wide
+    k-blocks per stage.  Here every K is a multiple of 64 with an odd number of k-blocks: h =
+    192 (dgrad, 3 blocks), F/t = 320 (row-parallel and dX, 5 blocks per shard, summed over the
+    shards), M = 320 tokens (wgrad, 5 blocks).  So each shard's last stage carries a second,
+    out-of-range k-block that must arrive as zeros and not as the next shard's data."""
+    monkeypatch.setenv("TP_GEMM_PAIR", pair)
+    M, h, F, t = 320, 192, 640, 2
+    dev, ref, w = _case(M, h, F, t, seed=12)
+    Y, _, _ = T.mlp_forward(dev["X"], w, "gelu_tanh")
+    o = O.mlp_forward_sharded(ref["X"], ref["W_up"], ref["b_up"], ref["W_down"], ref["b_down"], "gelu_tanh", t)
+    assert_close("Y", f64(Y), o["Y"])
+    _backward_check(M, h, F, t, "gelu_tanh", seed=12)
+
+
 def test_mlp_zero_tokens():
     dev, ref, w = _case(8, 64, 256, 2)
     Y = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
