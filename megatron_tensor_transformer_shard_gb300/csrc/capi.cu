@@ -506,13 +506,20 @@ tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int 
   return run_shard_reduce(P, M, h, t, bdown, residual, Y, nullptr, s);
 }
 
+// Column-sum scratch of the MLP backward: db_down's partial pass over dY, then db_up's
+// partials, one row per 32-row block of each shard's dZ, written by the dgrad epilogue.
+size_t mlp_cs_floats(int64_t M, int64_t h, int64_t Ft, int t) {
+  const int64_t blocks = (M + 31) / 32;
+  return colsum2_ws_floats(M, h, 1) + static_cast<size_t>(t) * (blocks > 0 ? blocks : 1) * Ft;
+}
+
 size_t tp_mlp_backward_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned flags) {
   if (M < 0 || h < 0 || F < 0 || t < 1) return 0;
   const int64_t Ft = F / t;
   // dZ (twice as wide under SwiGLU: gate and up), column-sum scratch, partials: sized for
   // every activation.
   size_t sz = round_up(static_cast<size_t>(M) * F * 2 * 2, 256);
-  const size_t cs = colsum2_ws_floats(M, h, 1) + colsum2_ws_floats(M, Ft, t);
+  const size_t cs = mlp_cs_floats(M, h, Ft, t);
   sz += round_up(cs * sizeof(float), 256);
   if (flags & TP_FLAG_UNFUSED_REDUCE) sz += static_cast<size_t>(t) * M * h * sizeof(float);
   return sz;
@@ -543,7 +550,8 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
   uint16_t* dZ = reinterpret_cast<uint16_t*>(w);
   w += round_up(static_cast<size_t>(M) * F * 2 * 2, 256);
   float* cs_ws = reinterpret_cast<float*>(w);
-  const size_t cs_floats = colsum2_ws_floats(M, h, 1) + colsum2_ws_floats(M, Ft, t);
+  const size_t cs_floats = mlp_cs_floats(M, h, Ft, t);
+  float* dbup_part = cs_ws + colsum2_ws_floats(M, h, 1);  // [t][(M + 31) / 32][Ft]
   w += round_up(cs_floats * sizeof(float), 256);
   float* P = reinterpret_cast<float*>(w);
 
@@ -570,20 +578,23 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
   } else {
     g.epi = EPI_DACT; g.act = act; g.aux = Z_save ? Z_save : A_save; g.ld_aux = Ft; g.aux_batch_stride = M * Ft;
     g.d = dZ; g.ldd = Ft; g.d_batch_stride = M * Ft;
+    g.colsum = dbup ? dbup_part : nullptr;  // db_up's partial column sums from the epilogue
   }
   TP_RETURN_IF(run_gemm(g, s));
 
-  // Bias gradients, one fused pass: db_down = sum_rows dY, taken once (g backward is the
-  // identity); db_up[C_i] = sum_rows dZ_i for every shard.
+  // Bias gradients: db_down = sum_rows dY, taken once (g backward is the identity), by a
+  // partial and a final pass; db_up[C_i] = sum_rows dZ_i for every shard, whose per-32-row
+  // partials the dgrad epilogue wrote, by the final pass alone (one launch for both sums).
   if (dbdown || dbup) {
     ColsumJob jd, ju;
     if (dbdown) {
       jd.G = dY; jd.rows = M; jd.cols = h; jd.ld = h; jd.bs = M * h; jd.nbatch = 1;
       jd.out = dbdown; jd.ws = cs_ws; jd.accumulate = accumulate;
     }
-    if (dbup) {
-      ju.G = dZ; ju.rows = M; ju.cols = Ft; ju.ld = Ft; ju.bs = M * Ft; ju.nbatch = t;
-      ju.out = dbup; ju.ws = cs_ws + colsum2_ws_floats(M, h, 1); ju.accumulate = accumulate;
+    if (dbup) {  // the dgrad epilogue wrote the partials: only their in-order sum is left
+      ju.rows = M; ju.cols = Ft; ju.nbatch = t;
+      ju.out = dbup; ju.ws = dbup_part; ju.accumulate = accumulate;
+      ju.partials_ready = 1; ju.nchunks = static_cast<int>((M + 31) / 32);
     }
     TP_RETURN_IF(run_colsum2(jd, ju, s));
   }

@@ -76,6 +76,8 @@ struct GemmArgs {
   int64_t bias_bs;
   const uint16_t* aux;
   int64_t ld_aux, aux_bs;
+  float* cs;      // EPI_DACT: per 32-row block column sums [nbatch][cs_chunks][N] (nullable)
+  int cs_chunks;
   const uint16_t* res;
   int64_t ld_res;
   int accumulate;
@@ -392,6 +394,35 @@ __device__ __forceinline__ void stage_row32(uint8_t* buf, int row, const float (
         make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
 }
 
+// Column sums of a warp's 32 rows (one row per lane, 32 columns each): a fixed butterfly of
+// 31 shuffles after which lane j holds the sum of column j (v is consumed).
+__device__ __forceinline__ float warp_column_sum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float keep = upper ? v[i + off] : v[i];
+      const float send = upper ? v[i] : v[i + off];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return v[0];
+}
+
+// The fused bias-gradient pass of EPI_DACT: the warp's rows m0..m0+31 (lanes past M count
+// as zero) and columns n0..n0+31 -> cs[b][m0 / 32][n0 + lane].
+__device__ __forceinline__ void dact_colsum_chunk(const GemmArgs& p, int b, int m0, int n0, int lane,
+                                                  float (&v)[32]) {
+  if (m0 + lane >= p.M) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+  }
+  const float s = warp_column_sum32(v, lane);
+  if (n0 + lane < p.N)
+    p.cs[(static_cast<int64_t>(b) * p.cs_chunks + m0 / 32) * p.N + n0 + lane] = s;
+}
+
 template <bool A_MN, bool B_MN, int EPI, int ACT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -584,6 +615,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (m < p.M) {
             if constexpr (EPI == EPI_DGLU) dglu_chunk(p, b, m, n0, r);
             else epilogue_chunk<EPI, ACT>(p, b, m, n0, r);
+          }
+          if constexpr (EPI == EPI_DACT) {
+            if (p.cs) {  // warp-uniform; this kernel serves M <= 128, so act'(Z) is simply recomputed
+              float v[32], v2[32];
+              epilogue_values<EPI, ACT>(p, b, m, n0, r, v, v2);
+              dact_colsum_chunk(p, b, mb * BM + quad * 32, n0, lane, v);
+            }
           }
         }
       }
@@ -1193,6 +1231,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
             } else {
               stage_half_row16(bufD, lane, h, v, false);
             }
+            if constexpr (EPI == EPI_DACT) {
+              if (p.cs) dact_colsum_chunk(p, b, mrow0, n0 + h * 32, lane, v);  // v is staged: consume it
+            }
           }
           ptx::fence_proxy_async_smem();
           __syncwarp();
@@ -1534,6 +1575,7 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
   if (glu && (P.bias || P.residual || P.out_f16 || P.nsum != 1)) return TP_ERR_UNSUPPORTED;
   if (P.epi == EPI_GLU && (P.ldd2 % 8 != 0 || P.d2_batch_stride % 8 != 0)) return TP_ERR_ALIGN;
   if (P.residual && (!aligned16(P.residual) || P.ld_res % 8 != 0)) return TP_ERR_ALIGN;
+  if (P.colsum && P.epi != EPI_DACT) return TP_ERR_UNSUPPORTED;
   if (P.K == 0) return TP_ERR_SHAPE;
   const int64_t mt = (P.M + BM - 1) / BM, nt = (P.N + BN - 1) / BN, kt = (P.K + BK - 1) / BK;
   if (mt * nt * P.nbatch > (1LL << 30) || P.M > (1LL << 30) || P.N > (1LL << 30)) return TP_ERR_SHAPE;
@@ -1583,6 +1625,8 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
   a.aux = P.aux;
   a.ld_aux = P.ld_aux;
   a.aux_bs = P.aux_batch_stride;
+  a.cs = P.colsum;
+  a.cs_chunks = static_cast<int>((P.M + 31) / 32);
   a.res = P.residual;
   a.ld_res = P.ld_res;
   a.accumulate = P.accumulate;

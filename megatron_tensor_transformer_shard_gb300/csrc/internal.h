@@ -111,6 +111,9 @@ struct GemmProblem {
   int64_t bias_batch_stride = 0;
   const uint16_t* aux = nullptr;  // EPI_DACT: Z
   int64_t ld_aux = 0, aux_batch_stride = 0;
+  // EPI_DACT (nullable): column sums of D before rounding, one row per 32-row block of M,
+  // colsum[b][(M + 31) / 32][N] fp32 -- the partial pass of a fused column sum (bias gradient)
+  float* colsum = nullptr;
   const uint16_t* residual = nullptr;
   int64_t ld_res = 0;
   int accumulate = 0;
@@ -150,7 +153,10 @@ struct ColsumJob {
   float* out = nullptr;
   float* ws = nullptr;  // colsum2_ws_floats(rows, cols, nbatch) floats
   int accumulate = 0;
-  int nchunks = 0;      // set by run_colsum2
+  // ws already holds [nbatch][nchunks][cols] partials (written by a GEMM epilogue): only the
+  // final in-order sum runs, over the caller's nchunks
+  int partials_ready = 0;
+  int nchunks = 0;      // set by run_colsum2 (by the caller when partials_ready)
   int64_t cblocks = 0;  // set by run_colsum2
 };
 size_t colsum2_ws_floats(int64_t rows, int64_t cols, int nbatch);

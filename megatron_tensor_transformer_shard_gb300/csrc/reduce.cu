@@ -193,6 +193,11 @@ tp_status run_colsum2(ColsumJob a, ColsumJob b, cudaStream_t s) {
     ColsumJob& j = *js[k];
     if (j.rows < 0 || j.cols < 0 || j.nbatch < 1) return TP_ERR_INVALID_ARG;
     if (j.cols == 0) continue;
+    if (j.partials_ready) {  // the partials are in ws already: only the final sum
+      if (!j.out || !j.ws || j.nchunks < 1) return TP_ERR_INVALID_ARG;
+      outs[k] = j.cols * j.nbatch;
+      continue;
+    }
     if (!j.G || !j.out || !j.ws || (j.cols & 7) || (j.ld & 7) || (j.bs & 7) || !aligned16(j.G))
       return TP_ERR_ALIGN;
     j.nchunks = static_cast<int>((j.rows + CS2_ROWS - 1) / CS2_ROWS);
@@ -203,12 +208,14 @@ tp_status run_colsum2(ColsumJob a, ColsumJob b, cudaStream_t s) {
     ctas[k] = j.cblocks * j.nchunks * j.nbatch;
     outs[k] = j.cols * j.nbatch;
   }
-  if (ctas[0] + ctas[1] == 0) return TP_OK;
-  TP_RETURN_IF(ready());
-  TP_CUDA_CHECK(launch_pdl(colsum2_partial_kernel, dim3(static_cast<unsigned>(ctas[0] + ctas[1])), dim3(CS2_THREADS),
-                           0, s, a, b, ctas[0]));
-  count_launch();
   const int64_t n = outs[0] + outs[1];
+  if (n == 0) return TP_OK;
+  TP_RETURN_IF(ready());
+  if (ctas[0] + ctas[1] > 0) {
+    TP_CUDA_CHECK(launch_pdl(colsum2_partial_kernel, dim3(static_cast<unsigned>(ctas[0] + ctas[1])),
+                             dim3(CS2_THREADS), 0, s, a, b, ctas[0]));
+    count_launch();
+  }
   TP_CUDA_CHECK(launch_pdl(colsum2_final_kernel, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, s, a, b,
                            outs[0]));
   count_launch();
