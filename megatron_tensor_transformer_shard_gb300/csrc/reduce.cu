@@ -173,6 +173,9 @@ __global__ void colsum2_final_kernel(ColsumJob j0, ColsumJob j1, int64_t n0) {
   const int64_t b = local / j.cols, c = local - b * j.cols;
   const float* w = j.ws + b * j.nchunks * j.cols + c;
   float s = 0.0f;
+  // Up to 16 loads in flight (a GEMM epilogue leaves one partial per 32 rows); the adds keep
+  // their order, so the sum is the same.
+#pragma unroll 16
   for (int k = 0; k < j.nchunks; ++k) s += w[static_cast<int64_t>(k) * j.cols];
   j.out[local] = j.accumulate ? j.out[local] + s : s;
 }
