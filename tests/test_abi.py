@@ -50,6 +50,11 @@ def test_workspace_sizes():
     assert L.tp_mlp_workspace_size(2048, 4096, 16384, 4, 0) == 0
     assert L.tp_mlp_workspace_size(2048, 4096, 16384, 4, L.TP_FLAG_UNFUSED_REDUCE) == 4 * 2048 * 4096 * 4
     assert L.tp_mlp_backward_workspace_size(2048, 4096, 16384, 4, 0) >= 2048 * 16384 * 2
+    # dZ (room for SwiGLU's gate and up) + db_down's partials + db_up's per-32-row partials that
+    # the dgrad epilogue writes ([t][ceil(M / 32)][F / t] fp32), for ragged M as well
+    for M, h, F, t in [(2048, 4096, 16384, 4), (200, 264, 784, 2), (1, 64, 128, 4), (33, 128, 1024, 8)]:
+        need = M * F * 2 * 2 + t * ((M + 31) // 32) * (F // t) * 4 + ((M + 255) // 256) * h * 4
+        assert L.tp_mlp_backward_workspace_size(M, h, F, t, 0) >= need, (M, h, F, t)
     assert L.tp_colsum_workspace_size(2048, 4096) == 32 * 4096 * 4
 
 
