@@ -449,7 +449,9 @@ tp_status tp_shard_reduce(const float* P, int64_t rows, int64_t cols, int t, con
                           const tp_bf16* residual, tp_bf16* out_bf16, float* out_f32, tp_stream stream);
 
 /* Column sums of a bf16 matrix [rows][cols] -> fp32 [cols] in a fixed order
- * (bias gradients).  ws: tp_colsum_workspace_size(rows, cols) bytes. */
+ * (bias gradients).  ws: tp_colsum_workspace_size(rows, cols) bytes.  cols even;
+ * rows are summed in 64-row chunks, and any row count whose chunk count fits in
+ * 2^31 - 1 is accepted (the chunks are spread over the grid's x dimension). */
 size_t tp_colsum_workspace_size(int64_t rows, int64_t cols);
 tp_status tp_colsum(const tp_bf16* G, int64_t rows, int64_t cols, float* out, int accumulate, void* ws,
                     size_t ws_bytes, tp_stream stream);

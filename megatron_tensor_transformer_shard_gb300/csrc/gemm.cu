@@ -411,7 +411,8 @@ __device__ __forceinline__ float warp_column_sum32(float (&v)[32], int lane) {
 }
 
 // The fused bias-gradient pass of EPI_DACT: the warp's rows m0..m0+31 (lanes past M count
-// as zero) and columns n0..n0+31 -> cs[b][m0 / 32][n0 + lane].
+// as zero) and columns n0..n0+31 -> cs[b][m0 / 32][n0 + lane].  Callers pass only m0 < M,
+// so m0 / 32 < cs_chunks.
 __device__ __forceinline__ void dact_colsum_chunk(const GemmArgs& p, int b, int m0, int n0, int lane,
                                                   float (&v)[32]) {
   if (m0 + lane >= p.M) {
@@ -617,10 +618,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             else epilogue_chunk<EPI, ACT>(p, b, m, n0, r);
           }
           if constexpr (EPI == EPI_DACT) {
-            if (p.cs) {  // warp-uniform; this kernel serves M <= 128, so act'(Z) is simply recomputed
+            // Warp-uniform.  A warp whose 32 rows all lie past M owns no 32-row block of the
+            // partials (block m0 / 32 would index the next shard's first block, or past the
+            // buffer for the last shard), so it writes nothing.  This kernel serves M <= 128,
+            // so act'(Z) is simply recomputed.
+            const int m0 = mb * BM + quad * 32;
+            if (p.cs && m0 < p.M) {
               float v[32], v2[32];
               epilogue_values<EPI, ACT>(p, b, m, n0, r, v, v2);
-              dact_colsum_chunk(p, b, mb * BM + quad * 32, n0, lane, v);
+              dact_colsum_chunk(p, b, m0, n0, lane, v);
             }
           }
         }

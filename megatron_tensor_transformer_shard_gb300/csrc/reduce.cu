@@ -17,11 +17,14 @@ constexpr int COLSUM_ROWS_PER_CHUNK = 64;
 constexpr int COLSUM_THREADS = 128;  // x 2 columns each = 256 columns per CTA
 
 // Phase 1: ws[batch][chunk][col] = sum of rows [chunk*64, chunk*64+64) of batch b, in row order.
+// blockIdx.x = chunk * cblocks + column block (the chunk count can exceed gridDim.y's 65535),
+// blockIdx.y = batch.
 __global__ void colsum_partial_kernel(const uint16_t* __restrict__ G, int64_t rows, int64_t cols, int64_t ld,
-                                      int64_t batch_stride, int nchunks, float* __restrict__ ws) {
-  const int64_t c = (static_cast<int64_t>(blockIdx.x) * COLSUM_THREADS + threadIdx.x) * 2;
-  const int chunk = blockIdx.y;
-  const int b = blockIdx.z;
+                                      int64_t batch_stride, int nchunks, int cblocks, float* __restrict__ ws) {
+  const int cb = static_cast<int>(blockIdx.x % static_cast<unsigned>(cblocks));
+  const int chunk = static_cast<int>(blockIdx.x / static_cast<unsigned>(cblocks));
+  const int64_t c = (static_cast<int64_t>(cb) * COLSUM_THREADS + threadIdx.x) * 2;
+  const int b = blockIdx.y;
   if (c >= cols) return;
   const int64_t r0 = static_cast<int64_t>(chunk) * COLSUM_ROWS_PER_CHUNK;
   const int64_t r1 = r0 + COLSUM_ROWS_PER_CHUNK < rows ? r0 + COLSUM_ROWS_PER_CHUNK : rows;
@@ -239,15 +242,21 @@ tp_status run_colsum_batched(const uint16_t* G, int64_t rows, int64_t cols, int6
   if (cols == 0) return TP_OK;
   if (!G || !out || !ws) return TP_ERR_INVALID_ARG;
   if ((cols & 1) || (ld & 1) || (batch_stride & 1) || (reinterpret_cast<uintptr_t>(G) & 3)) return TP_ERR_ALIGN;
-  const int nchunks = static_cast<int>((rows + COLSUM_ROWS_PER_CHUNK - 1) / COLSUM_ROWS_PER_CHUNK);
+  const int64_t nchunks64 = (rows + COLSUM_ROWS_PER_CHUNK - 1) / COLSUM_ROWS_PER_CHUNK;
+  if (nchunks64 > 0x7fffffffLL) return TP_ERR_SHAPE;
+  const int nchunks = static_cast<int>(nchunks64);
   if (ws_floats < colsum_ws_floats(rows, cols) * static_cast<size_t>(nbatch)) return TP_ERR_WORKSPACE;
+  // Grid: (chunks x column blocks, batches); both within CUDA's grid limits, else refused.
+  const int64_t cblocks = (cols / 2 + COLSUM_THREADS - 1) / COLSUM_THREADS;
+  if (static_cast<int64_t>(nchunks) * cblocks > 0x7fffffffLL || nbatch > 65535) return TP_ERR_SHAPE;
   TP_RETURN_IF(ready());
   if (nchunks == 0) {
     if (!accumulate) TP_CUDA_CHECK(cudaMemsetAsync(out, 0, sizeof(float) * cols * nbatch, s));
     return TP_OK;
   }
-  dim3 g1(static_cast<unsigned>((cols / 2 + COLSUM_THREADS - 1) / COLSUM_THREADS), nchunks, nbatch);
-  colsum_partial_kernel<<<g1, COLSUM_THREADS, 0, s>>>(G, rows, cols, ld, batch_stride, nchunks, ws);
+  dim3 g1(static_cast<unsigned>(static_cast<int64_t>(nchunks) * cblocks), static_cast<unsigned>(nbatch));
+  colsum_partial_kernel<<<g1, COLSUM_THREADS, 0, s>>>(G, rows, cols, ld, batch_stride, nchunks,
+                                                      static_cast<int>(cblocks), ws);
   TP_LAUNCHED();
   const int64_t n = cols * nbatch;
   colsum_final_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(ws, cols, nchunks, nbatch, out,

@@ -15,7 +15,7 @@ from megatron_tensor_transformer_shard_gb300 import _lib as L
 from megatron_tensor_transformer_shard_gb300 import inputs as I
 from megatron_tensor_transformer_shard_gb300 import tp as T
 
-from gpu_helpers import assert_close, f64, ws_bytes
+from gpu_helpers import Guarded, assert_close, f64, guarded_ws, ws_bytes
 
 pytestmark = pytest.mark.gpu
 
@@ -214,6 +214,41 @@ def _backward_check(M, h, F, t, act, seed, flags=0):
     assert_close("db_up", f64(g["dbup"]), b["db_up"])
     assert_close("db_down", f64(g["dbdown"]), b["db_down"])
     return dev, w, g, (Y, Z, A)
+
+
+@pytest.mark.parametrize("pair", ["0", "1"])
+@pytest.mark.parametrize("M", [1, 33, 64, 96, 161])
+def test_backward_small_and_ragged_m_guarded(M, pair, monkeypatch):
+    """db_up's per-32-row partials come from the dgrad epilogue.  When the last row tile
+    has 32-row blocks wholly past M (M <= 96 on the single-CTA kernel, or M % 128 in
+    1..96 with TP_GEMM_PAIR=0), those blocks must write nothing: not into the next
+    shard's first block, not past the workspace.  The workspace and every output sit
+    between guard bytes that must come back unchanged, and every gradient (db_up above
+    all) must match the oracle."""
+    monkeypatch.setenv("TP_GEMM_PAIR", pair)
+    h, F, t = 128, 1024, 4
+    dev, ref, w = _case(M, h, F, t, seed=21 + M)
+    Y, Z, A = T.mlp_forward(dev["X"], w, "gelu_tanh")
+    nws = L.tp_mlp_backward_workspace_size(M, h, F, t, 0)
+    ws = guarded_ws(nws)
+    out = {"dX": Guarded((M, h), torch.bfloat16), "dWup_p": Guarded((t, F // t, h), torch.float32),
+           "dWdown_p": Guarded((t, h, F // t), torch.float32), "dbup": Guarded((F,), torch.float32),
+           "dbdown": Guarded((h,), torch.float32)}
+    L.tp_mlp_backward(dev["dY"], dev["X"], Z, A, M, h, F, t, L.TP_ACT_GELU_TANH, w.Wup_p, w.Wdown_p,
+                      out["dX"].t, out["dWup_p"].t, out["dWdown_p"].t, out["dbup"].t, out["dbdown"].t, 0, 0,
+                      ws.t, nws)
+    torch.cuda.synchronize()
+    assert L.tp_get_device_status(check=False) == L.TP_OK
+    ws.check("workspace")
+    for k, g in out.items():
+        g.check(k)
+    o = O.mlp_forward_sharded(ref["X"], ref["W_up"], ref["b_up"], ref["W_down"], ref["b_down"], "gelu_tanh", t)
+    b = O.mlp_backward_sharded(ref["dY"], ref["X"], ref["W_up"], ref["W_down"], o, "gelu_tanh", t)
+    assert_close("dX", f64(out["dX"].t), b["dX"])
+    assert_close("dW_up (packed)", f64(out["dWup_p"].t), O.pack_col_weight(b["dW_up"], t))
+    assert_close("dW_down (packed)", f64(out["dWdown_p"].t), O.pack_row_weight(b["dW_down"], t))
+    assert_close("db_up", f64(out["dbup"].t), b["db_up"])
+    assert_close("db_down", f64(out["dbdown"].t), b["db_down"])
 
 
 @pytest.mark.parametrize("M,h,F,t", [(200, 264, 784, 2), (256, 512, 2048, 4), (130, 128, 1024, 8)])

@@ -211,10 +211,62 @@ def test_gelu_closed_forms():
     assert np.abs(O.act("gelu_erf", z) - erf_ref).max() < 1e-15
     # the tanh form approximates the erf form to a few 1e-4 (Hendrycks & Gimpel)
     assert np.abs(O.act("gelu_tanh", z) - O.act("gelu_erf", z)).max() < 1e-3
-    # silu closed form and its derivative
-    assert np.allclose(O.silu(z), z / (1 + np.exp(-z)))
     num = (O.silu(z + 1e-6) - O.silu(z - 1e-6)) / 2e-6
     assert np.abs(num - O.silu_grad(z)).max() < 1e-8
+
+
+def test_silu_pins():
+    """silu(z) = z * sigmoid(z), the gate of SwiGLU ("02 — Tensor Parallelism", "The
+    core observation": the MLP's FLOPs "times 2 for SwiGLU").  Pinned by identities a
+    wrong formula breaks: silu(z) - silu(-z) = z (sigmoid(z) + sigmoid(-z) = 1),
+    silu(0) = 0, silu'(0) = 1/2, and the asymptotes silu(z) -> z, silu(-z) -> 0 with
+    the exponentially small gap z e^{-z}."""
+    z = np.linspace(-12, 12, 481)
+    assert np.abs((O.silu(z) - O.silu(-z)) - z).max() < 1e-14
+    assert O.silu(np.array([0.0]))[0] == 0.0
+    assert abs(O.silu_grad(np.array([0.0]))[0] - 0.5) < 1e-16
+    big = np.array([30.0, 40.0])
+    gap = big * np.exp(-big)                 # z - silu(z) = z e^{-z} / (1 + e^{-z})
+    # above: silu(z) = z - z e^{-z} / (1 + e^{-z}), equal to z within rounding of z
+    assert np.abs(O.silu(big) - (big - gap / (1 + np.exp(-big)))).max() <= 4 * np.spacing(big).max()
+    # below: silu(-z) = -z e^{-z} / (1 + e^{-z}), a tiny value computed without cancellation
+    assert np.allclose(-O.silu(-big), gap / (1 + np.exp(-big)), rtol=1e-12, atol=0)
+    # the derivative tends to 1 above and 0 below
+    assert abs(O.silu_grad(np.array([40.0]))[0] - 1.0) < 1e-15
+    assert abs(O.silu_grad(np.array([-40.0]))[0]) < 1e-15
+
+
+def _torch_f64(fn, z):
+    import torch
+    return fn(torch.from_numpy(np.asarray(z, dtype=np.float64))).numpy()
+
+
+def test_activations_match_an_independent_library_in_fp64():
+    """The oracle's activations against torch's own float64 implementations (a
+    separate code base): SiLU, GeLU with the tanh approximation (this pins the cubic
+    coefficient 0.044715 and sqrt(2/pi): a coefficient off by 1e-4 moves the value by
+    ~1e-5 at |z| ~ 2, far above 1e-14) and exact GeLU; and their derivatives against
+    torch autograd in float64."""
+    import torch
+    import torch.nn.functional as Fn
+    z = np.concatenate([np.linspace(-10, 10, 2001), [-1e-8, 1e-8, 0.0, 3.7, -2.3]])
+    assert np.abs(O.silu(z) - _torch_f64(Fn.silu, z)).max() <= 1e-14 * max(1.0, np.abs(z).max())
+    gt = _torch_f64(lambda x: Fn.gelu(x, approximate="tanh"), z)
+    assert np.abs(O.act("gelu_tanh", z) - gt).max() <= 1e-14 * max(1.0, np.abs(z).max())
+    ge = _torch_f64(lambda x: Fn.gelu(x, approximate="none"), z)
+    assert np.abs(O.act("gelu_erf", z) - ge).max() <= 1e-14 * max(1.0, np.abs(z).max())
+    for name, fn, grad in (("silu", Fn.silu, O.silu_grad),
+                           ("gelu_tanh", lambda x: Fn.gelu(x, approximate="tanh"),
+                            lambda v: O.act_grad("gelu_tanh", v)),
+                           ("gelu_erf", lambda x: Fn.gelu(x, approximate="none"),
+                            lambda v: O.act_grad("gelu_erf", v))):
+        x = torch.tensor(z, dtype=torch.float64, requires_grad=True)
+        (g,) = torch.autograd.grad(fn(x).sum(), x)
+        assert np.abs(grad(z) - g.numpy()).max() <= 1e-13, name
+    # the planted mistake this catches: a GeLU-tanh with a cubic coefficient 1e-4 off
+    c = 0.044715 + 1e-4
+    wrong = 0.5 * z * (1 + np.tanh(math.sqrt(2 / math.pi) * (z + c * z ** 3)))
+    assert np.abs(wrong - gt).max() > 1e-6
 
 
 # ---------------------------------------------------------------------------

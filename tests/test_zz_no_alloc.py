@@ -26,6 +26,11 @@ def _with_workspace(G, rows, cols):
     return out
 
 
+def _fp64_colsum(G):
+    """The plain definition: every column's sum over all rows, in float64 on the host."""
+    return G.cpu().double().numpy().sum(axis=0)
+
+
 def test_noalloc_matches_workspace_version_twice():
     shapes = [(2048, 4096), (333, 1026)]       # second call: other sizes, ragged rows
     for k, (rows, cols) in enumerate(shapes):
@@ -40,6 +45,24 @@ def test_noalloc_matches_workspace_version_twice():
         assert np.all(np.isfinite(a))
         assert rel_err(a, b) <= TOL
         assert np.array_equal(a, b)               # same reduction order -> identical sums
+        assert rel_err(a, _fp64_colsum(G)) <= TOL  # and both are the column sums
+
+
+def test_noalloc_more_chunks_than_grid_y():
+    """More 64-row chunks (70001) than a grid's y dimension holds (65535): the chunks
+    are spread over x, and both entry points still give the column sums."""
+    rows, cols = 64 * 70000 + 5, 2
+    G = torch.randn(rows, cols, generator=torch.Generator().manual_seed(44)).to(torch.bfloat16).cuda()
+    out = torch.full((cols,), float("nan"), dtype=torch.float32, device="cuda")
+    L.tp_colsum_noalloc(G, rows, cols, out, 0)
+    ref = _with_workspace(G, rows, cols)
+    torch.cuda.synchronize()
+    assert L.tp_get_device_status(check=False) == L.TP_OK
+    a, b = out.double().cpu().numpy(), ref.double().cpu().numpy()
+    exact = _fp64_colsum(G)
+    assert np.array_equal(a, b)
+    # fp32 sums of 4.5M N(0,1) terms: the sum's spread is ~2100, the fp32 rounding far smaller
+    assert np.abs(a - exact).max() <= 1e-3 * np.abs(G.cpu().double().numpy()).sum(axis=0).max()
 
 
 def test_noalloc_accumulate_and_limit():
