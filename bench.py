@@ -328,14 +328,19 @@ def run_ours(args):
     if not args.no_extras and rank == 0:
         del Z, A, dWup, dWdown, ws
         torch.cuda.empty_cache()
-        secondary = {"decode_c3": run_decode_extra(L, torch, args), "mlp_fwd_c1": run_mlp_fwd_extra(L, torch, args),
-                     "layer_c4": run_layer_extra(L, torch, args, "c4"),
-                     "sp_layer_c5": run_layer_extra(L, torch, args, "c5"),
-                     "attention_c5": run_attn_extra(L, torch, args, "c5"),
-                     "sp_layernorm_c5": run_ln_extra(L, torch, args, "c5"),
-                     "decode_attention": run_decode_attn_extra(L, torch, args),
-                     "vocab_embedding": run_embedding_extra(L, torch, args),
-                     "row_parallel_overlap_c2": run_overlap_extra(L, torch, args)}
+        full = {"layer_c4": run_layer_extra(L, torch, args, "c4"),
+                "sp_layer_c5": run_layer_extra(L, torch, args, "c5"),
+                "attention_c5": run_attn_extra(L, torch, args, "c5"),
+                "sp_layernorm_c5": run_ln_extra(L, torch, args, "c5"),
+                "decode_attention": run_decode_attn_extra(L, torch, args),
+                "vocab_embedding": run_embedding_extra(L, torch, args),
+                "row_parallel_overlap_c2": run_overlap_extra(L, torch, args),
+                "mlp_fwd_c1": run_mlp_fwd_extra(L, torch, args),
+                "decode_c3": run_decode_extra(L, torch, args)}
+        # The full records (workload descriptions, byte counts) go to stderr; the JSON line
+        # keeps a few numbers per workload, the two target workloads last.
+        print(json.dumps({"secondary_detail": full}), file=sys.stderr, flush=True)
+        secondary = {k: compact_secondary(k, v) for k, v in full.items()}
 
     if rank != 0:
         return None
@@ -361,11 +366,54 @@ def run_ours(args):
                      "kernel_ms": round(col_ms, 4), "flops_per_launch": col_flops},
         "clocks": clk, "e2e": e2e, "gpu_launches": int(launches),
     }
+    if world == 1 and not args.no_cpu_baseline:
+        cb, parity = cpu_baseline(budget_s=args.cpu_budget, gpu=GpuMlp(L, torch), layers=args.cpu_layers)
+        line["cpu_baseline"] = cb
+        line["parity"] = parity
     if secondary:
         line["secondary"] = secondary
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
     return line
+
+
+# Numbers kept in the JSON line per secondary workload (the rest goes to stderr).
+_COMPACT = {
+    "layer_c4": ("ms_per_step", "TFLOPs", "frac_of_peak"),
+    "sp_layer_c5": ("ms_per_step", "TFLOPs", "frac_of_peak"),
+    "attention_c5": ("fwd_ms", "bwd_ms", "core_fwd_ms", "core_fwd_TFLOPs", "core_bwd_ms", "core_bwd_TFLOPs"),
+    "sp_layernorm_c5": ("fwd_us", "fwd_frac_of_hbm", "bwd_us", "bwd_frac_of_hbm"),
+    "decode_attention": ("us_per_step", "frac_of_hbm", "us_per_step_graph"),
+    "vocab_embedding": ("fwd_us", "fwd_frac_of_hbm", "bwd_us", "bwd_frac_of_hbm"),
+    "row_parallel_overlap_c2": ("fused_ms", "overlap_ms", "separate_reduce_kernel_ms"),
+    "mlp_fwd_c1": ("us_per_step", "TFLOPs", "us_per_step_graph"),
+    "decode_c3": ("us_per_step", "GBps", "frac_of_hbm", "frac_of_8TBps"),
+}
+
+
+def compact_secondary(name, rec):
+    keys = _COMPACT.get(name)
+    return {k: rec[k] for k in keys if k in rec} if keys else rec
+
+
+class GpuMlp:
+    """The TP-MLP path through the C ABI on host-drawn inputs (the parity leg of the
+    oracle baseline compares its rows with the oracle's)."""
+
+    def __init__(self, L, torch):
+        self.L, self.torch = L, torch
+
+    def run(self, inp_cpu, M, h, F, t, act_name, backward):
+        L, torch = self.L, self.torch
+        from megatron_tensor_transformer_shard_gb300 import tp as T
+        d = {k: (v.cuda() if v is not None else None) for k, v in inp_cpu.items()}
+        w = T.MLPWeights(d["W_up"], d["b_up"], d["W_down"], d["b_down"], t)
+        Y, Z, A = T.mlp_forward(d["X"], w, act_name)
+        out = {"Y": Y}
+        if backward:
+            out["dX"] = T.mlp_backward(d["dY"], d["X"], Z, A, w, act_name)["dX"]
+        torch.cuda.synchronize()
+        if L.tp_get_device_status(check=False) != L.TP_OK:
+            raise RuntimeError("device error in the parity run")
+        return {k: v.cpu() for k, v in out.items()}
 
 
 def _time(torch, fn, iters, warmup=3):
@@ -738,19 +786,24 @@ def run_layer_extra(L, torch, args, name):
 
 # ----------------------------------------------------------- oracle (CPU)
 
-def _oracle_inputs(M_s):
+def _f64(O, I, v):
+    return O.bf16_to_f64(I.bits(v)).reshape(tuple(v.shape))
+
+
+def _oracle_inputs(M_s, seed=0, return_cpu=False):
     import oracle as O
     from megatron_tensor_transformer_shard_gb300 import inputs as I
     cfg = I.CONFIGS[WORKLOAD]
-    inp = I.mlp_inputs(cfg["M"], cfg["h"], cfg["F"], bias=True, dy=True, seed=0)
-    r = {k: O.bf16_to_f64(I.bits(v)).reshape(tuple(v.shape)) for k, v in inp.items()}
+    inp = I.mlp_inputs(cfg["M"], cfg["h"], cfg["F"], bias=True, dy=True, seed=seed)
+    r = {k: _f64(O, I, v) for k, v in inp.items()}
     r["X"], r["dY"] = r["X"][:M_s], r["dY"][:M_s]
-    return r, cfg
+    return (r, cfg, inp) if return_cpu else (r, cfg)
 
 
 def _oracle_step(O, r, cfg):
     f = O.mlp_forward_sharded(r["X"], r["W_up"], r["b_up"], r["W_down"], r["b_down"], cfg["act"], cfg["t"])
-    O.mlp_backward_sharded(r["dY"], r["X"], r["W_up"], r["W_down"], f, cfg["act"], cfg["t"])
+    b = O.mlp_backward_sharded(r["dY"], r["X"], r["W_up"], r["W_down"], f, cfg["act"], cfg["t"])
+    return f, b
 
 
 def _cores():
@@ -760,24 +813,154 @@ def _cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(budget_s=12.0):
-    """The fp64 oracle as it stands, on the host cores, on a row sample of the
-    same workload sized to about `budget_s` seconds of CPU work."""
-    import oracle as O
-    r, cfg = _oracle_inputs(cfg_rows := 128)
+def _timed(fn):
     t0 = time.perf_counter()
-    _oracle_step(O, r, cfg)
-    dt = time.perf_counter() - t0
-    rows = int(min(cfg["M"], max(128, (budget_s / max(dt, 1e-3)) * 128 // 128 * 128)))
-    if rows != cfg_rows:
+    out = fn()
+    return time.perf_counter() - t0, out
+
+
+def _rel(gpu, ref):
+    import numpy as np
+    return float(np.abs(gpu - ref).max() / max(np.abs(ref).max(), 1e-30))
+
+
+def oracle_probe(name, rows=0):
+    """Seconds of the fp64 oracle, as it stands, on one configuration (or a stated
+    sample of it); inputs are drawn first and not timed."""
+    import oracle as O
+    from megatron_tensor_transformer_shard_gb300 import inputs as I
+    if name == "c1":
+        c = I.CONFIGS["c1"]
+        inp = I.mlp_inputs(c["M"], c["h"], c["F"], bias=True, dy=False, seed=0)
+        r = {k: _f64(O, I, v) for k, v in inp.items() if v is not None}
+        sec, _ = _timed(lambda: O.mlp_forward_sharded(r["X"], r["W_up"], r["b_up"], r["W_down"], r["b_down"],
+                                                      c["act"], c["t"]))
+        return {"seconds": sec, "sample": "the whole forward (128 tokens)", "scale": 1.0}
+    if name == "c2":
         r, cfg = _oracle_inputs(rows)
-        t0 = time.perf_counter()
-        _oracle_step(O, r, cfg)
-        dt = time.perf_counter() - t0
+        sec, _ = _timed(lambda: _oracle_step(O, r, cfg))
+        return {"seconds": sec, "sample": f"fwd+bwd on the first {rows} of {cfg['M']} token rows",
+                "scale": cfg["M"] / rows}
+    if name == "c3":
+        # one shard's slice of the decode MLP (7168 of 28672 hidden units): the loop body of the
+        # sharded oracle for shard 0; the whole step is t such slices
+        c = I.CONFIGS["c3"]
+        Ft = c["F"] // c["t"]
+        inp = I.swiglu_inputs(c["M"], c["h"], Ft, seed=0)
+        r = {k: _f64(O, I, v) for k, v in inp.items()}
+        sec, _ = _timed(lambda: O.swiglu_forward_sharded(r["X"], r["W_gate"], r["W_up"], r["W_down"], 1))
+        return {"seconds": sec, "sample": f"shard 0's slice ({Ft} of {c['F']} hidden units), x{c['t']}",
+                "scale": float(c["t"])}
+    # c4 / c5: the whole layer's weights, forward + backward on a prefix of the tokens (causal
+    # attention of a prefix depends on the prefix only)
+    import math
+    c = I.CONFIGS[name]
+    d, F, t, nh = c["d"], c["F"], c["t"], c["n_heads"]
+    inp = I.layer_inputs(rows, d, F, seed=0)
+    r = {k: _f64(O, I, v) for k, v in inp.items()}
+    del inp
+    cfg = {"n_heads": nh, "head_dim": c["head_dim"], "causal": True, "scale": 1.0 / math.sqrt(c["head_dim"]),
+           "eps": c["eps"], "act": c["act"]}
+    p = {k: v for k, v in r.items() if k not in ("X", "dY")}
+    X, G = r["X"], r["dY"]
+    if c["sp"]:
+        X, G = X.reshape(t, rows // t, d), G.reshape(t, rows // t, d)
+
+    def step():
+        f = O.layer_forward(X, p, cfg, t, c["sp"])
+        O.layer_backward(G, X, p, cfg, t, f, c["sp"])
+    sec, _ = _timed(step)
+    return {"seconds": sec, "sample": f"fwd+bwd on the first {rows} of {c['N']} tokens, all weights",
+            "scale": None}
+
+
+def _probe_subprocess(name, rows, threads):
+    """oracle_probe in a fresh interpreter whose BLAS and OpenMP use `threads` threads."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = str(threads)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-probe", name, "--probe-rows", str(rows)],
+                       capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        return {"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else f"rc={r.returncode}"}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def _host_mem_available_gb():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) / 2 ** 20
+    except OSError:
+        pass
+    return None
+
+
+def cpu_baseline(budget_s=12.0, gpu=None, layers=False, per_config=True):
+    """The fp64 oracle as it stands, timed on the host cores: on a row sample of the
+    headline workload sized to about `budget_s` seconds (the baseline value), and per
+    configuration (all cores, and single-threaded for the two MLP workloads).  With
+    `gpu`, the same path that was timed also runs on the host-drawn inputs and its
+    rows are compared with the oracle's: max|gpu - oracle| / max|oracle| per output."""
+    import oracle as O
+    from megatron_tensor_transformer_shard_gb300 import inputs as I
+    r, cfg = _oracle_inputs(cfg_rows := 128)
+    dt, _ = _timed(lambda: _oracle_step(O, r, cfg))
+    rows = int(min(cfg["M"], max(128, (budget_s / max(dt, 1e-3)) * 128 // 128 * 128)))
+    r, cfg, inp = _oracle_inputs(rows, return_cpu=True)
+    dt, (f, b) = _timed(lambda: _oracle_step(O, r, cfg))
     fl = flops_per_step(rows, cfg["h"], cfg["F"])
-    return {"value": round(fl / dt / 1e12, 5), "unit": UNIT, "cores": _cores(), "kind": "oracle",
-            "sample": f"one fwd+bwd of the same MLP on the first {rows} of {cfg['M']} token rows "
-                      f"(numpy fp64, {dt:.2f} s)", "seconds": round(dt, 3)}
+    cores = _cores()
+    out = {"value": round(fl / dt / 1e12, 5), "unit": UNIT, "cores": cores, "kind": "oracle",
+           "sample": f"one fwd+bwd of the same MLP on the first {rows} of {cfg['M']} token rows "
+                     f"(numpy fp64, {dt:.2f} s)", "seconds": round(dt, 3)}
+    parity = None
+    if gpu is not None:
+        g = gpu.run(inp, cfg["M"], cfg["h"], cfg["F"], cfg["t"], cfg["act"], backward=True)
+        parity = {"c2": {"rows": rows, "Y": round(_rel(_f64(O, I, g["Y"])[:rows], f["Y"]), 6),
+                         "dX": round(_rel(_f64(O, I, g["dX"])[:rows], b["dX"]), 6)}}
+        c1 = I.CONFIGS["c1"]
+        inp1 = I.mlp_inputs(c1["M"], c1["h"], c1["F"], bias=True, dy=False, seed=0)
+        r1 = {k: _f64(O, I, v) for k, v in inp1.items() if v is not None}
+        f1 = O.mlp_forward_sharded(r1["X"], r1["W_up"], r1["b_up"], r1["W_down"], r1["b_down"], c1["act"], c1["t"])
+        g1 = gpu.run(inp1, c1["M"], c1["h"], c1["F"], c1["t"], c1["act"], backward=False)
+        parity["c1"] = {"rows": c1["M"], "Y": round(_rel(_f64(O, I, g1["Y"]), f1["Y"]), 6)}
+        parity["bound"] = 1e-2
+    del r, inp, f, b
+    if not per_config:
+        return out, parity
+    per = {}
+    probes = [("c1", 0), ("c3", 0)]
+    # The layer probes hold the whole layer's weights and weight gradients in fp64 on the
+    # host (C5 ~13 GB, C4 ~30 GB): C5 runs when the host has room, C4 only when asked.
+    avail = _host_mem_available_gb()
+    for name, need_gb in (("c5", 40.0), ("c4", 90.0)):
+        if (name == "c5" or layers) and avail is not None and avail >= need_gb:
+            probes.append((name, 32))
+        else:
+            per[name] = {"skipped": f"needs --cpu-layers and ~{need_gb:.0f} GB of free host memory "
+                                    f"({avail if avail is None else round(avail)} GB free)"
+                         if name == "c4" else f"needs ~{need_gb:.0f} GB of free host memory ({avail} GB free)"}
+    for name, rows_p in probes:
+        try:
+            pr = oracle_probe(name, rows_p)
+            per[name] = {"seconds": round(pr["seconds"], 3), "cores": cores, "sample": pr["sample"]}
+            if pr.get("scale"):
+                per[name]["seconds_whole_config"] = round(pr["seconds"] * pr["scale"], 3)
+        except Exception as e:  # reported, not fatal: the headline baseline stands
+            per[name] = {"error": f"{type(e).__name__}: {e}"[:160]}
+    for name, rows_p in (("c1", 0), ("c2", 64)):
+        pr = _probe_subprocess(name, rows_p, 1)
+        if "seconds" in pr:
+            per[name + "_1thread"] = {"seconds": round(pr["seconds"], 3), "cores": 1, "sample": pr["sample"]}
+            if pr.get("scale"):
+                per[name + "_1thread"]["seconds_whole_config"] = round(pr["seconds"] * pr["scale"], 3)
+        else:
+            per[name + "_1thread"] = pr
+    out["per_config"] = per
+    return out, parity
 
 
 def run_reference(args):
@@ -841,12 +1024,20 @@ def main():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extras", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    p.add_argument("--cpu-layers", action="store_true",
+                   help="also time the oracle on the 2048-token layer (32-token prefix; ~30 GB of host memory)")
     p.add_argument("--reference-rows", type=int, default=64, help="token rows per oracle step (--impl reference)")
+    p.add_argument("--oracle-probe", choices=["c1", "c2", "c3", "c4", "c5"], default=None,
+                   help=argparse.SUPPRESS)  # one timed oracle run (used by the single-thread baseline)
+    p.add_argument("--probe-rows", type=int, default=64, help=argparse.SUPPRESS)
     p.add_argument("--only", choices=["c1", "c3", "c4", "c5", "attn", "ln", "dattn", "emb", "ovl", "swiglu"], default=None,
                    help="run only one secondary workload (forward MLP c1, decode c3, layers c4/c5, the c5-shaped "
                         "attention block, SP LayerNorm, decode attention over a sharded KV cache, the "
                         "vocab-parallel embedding or the overlapped row-parallel reduction) and print it")
     args = p.parse_args()
+    if args.oracle_probe:
+        print(json.dumps(oracle_probe(args.oracle_probe, args.probe_rows)), flush=True)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.only:

@@ -272,7 +272,7 @@ def mlp_backward_unsplit(G, X, W_up, W_down, Z, A, act_name):
             "dZ": dZ}
 
 
-def mlp_backward_sharded(G, X, W_up, W_down, fwd, act_name, t):
+def mlp_backward_sharded(G, X, W_up, W_down, fwd, act_name, t, weight_grads=True):
     """Backward as t ranks compute it.
 
     g backward is the identity: every shard gets G unchanged.  Shard i forms
@@ -281,6 +281,8 @@ def mlp_backward_sharded(G, X, W_up, W_down, fwd, act_name, t):
     "Parallelism Strategies #1 - Tensor Parallelism", weight-shard gradients),
     and a partial input grad dX_i = dZ_i W_up[:, C_i]^T.  f backward is the
     all-reduce: dX = sum_i dX_i.  The output-bias grad is taken once.
+    weight_grads=False leaves dW_up and dW_down out (zeros): the input grad
+    alone, for callers that only follow the gradient through the block.
     """
     h, F = W_up.shape
     dW_up = np.zeros_like(W_up)
@@ -293,8 +295,9 @@ def mlp_backward_sharded(G, X, W_up, W_down, fwd, act_name, t):
         dA_i = G_i @ W_down[C, :].T
         dZ_i = dA_i * act_grad(act_name, fwd["Z"][i])
         db_up[C] = dZ_i.sum(axis=0)
-        dW_down[C, :] = fwd["A"][i].T @ G_i
-        dW_up[:, C] = X.T @ dZ_i
+        if weight_grads:
+            dW_down[C, :] = fwd["A"][i].T @ G_i
+            dW_up[:, C] = X.T @ dZ_i
         dXs.append(dZ_i @ W_up[:, C].T)
         dZs.append(dZ_i)
     dX = np.zeros_like(dXs[0])

@@ -54,3 +54,47 @@ def test_single_rank_needs_no_process_group():
     assert bench.init_dist(1) is None
     assert bench.reduce_max(None, 3.0) == 3.0
     assert bench.aggregate(10.0, 2.0, 1) == 5.0
+
+
+def test_secondary_line_is_compact_and_ends_with_the_targets():
+    """The driver keeps the tail of the JSON line: the two target workloads come last
+    in `secondary`, each workload reduced to a few numbers."""
+    full = {k: {"workload": "w" * 200, "note": "n" * 200, "lengths": list(range(50)), "us_per_step": 1.0,
+                "GBps": 2.0, "frac_of_hbm": 0.5, "frac_of_8TBps": 0.4, "TFLOPs": 3.0, "us_per_step_graph": 4.0}
+            for k in ("layer_c4", "mlp_fwd_c1", "decode_c3")}
+    comp = {k: bench.compact_secondary(k, v) for k, v in full.items()}
+    assert list(comp)[-2:] == ["mlp_fwd_c1", "decode_c3"]
+    assert comp["decode_c3"] == {"us_per_step": 1.0, "GBps": 2.0, "frac_of_hbm": 0.5, "frac_of_8TBps": 0.4}
+    assert comp["mlp_fwd_c1"] == {"us_per_step": 1.0, "TFLOPs": 3.0, "us_per_step_graph": 4.0}
+    assert all("workload" not in v and "lengths" not in v for v in comp.values())
+
+
+class _RoundedOracleGpu:
+    """Stands in for the GPU leg on CPU: the oracle's own outputs rounded to bf16, so the
+    parity figures must come out small but not zero."""
+
+    def run(self, inp_cpu, M, h, F, t, act_name, backward):
+        import torch
+        import oracle as O
+        from megatron_tensor_transformer_shard_gb300 import inputs as I
+        r = {k: O.bf16_to_f64(I.bits(v)).reshape(tuple(v.shape)) for k, v in inp_cpu.items() if v is not None}
+        f = O.mlp_forward_sharded(r["X"], r["W_up"], r.get("b_up"), r["W_down"], r.get("b_down"), act_name, t)
+        out = {"Y": torch.from_numpy(f["Y"]).to(torch.bfloat16)}
+        if backward:
+            b = O.mlp_backward_sharded(r["dY"], r["X"], r["W_up"], r["W_down"], f, act_name, t)
+            out["dX"] = torch.from_numpy(b["dX"]).to(torch.bfloat16)
+        return out
+
+
+def test_cpu_baseline_reports_parity_of_the_benchmarked_configs():
+    cb, parity = bench.cpu_baseline(budget_s=0.01, gpu=_RoundedOracleGpu(), per_config=False)
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0
+    assert parity["c2"]["rows"] == 128 and parity["c1"]["rows"] == 128
+    for v in (parity["c2"]["Y"], parity["c2"]["dX"], parity["c1"]["Y"]):
+        assert 0 < v < 2 ** -7            # bf16 rounding of the oracle's own values
+    assert parity["bound"] == 1e-2
+
+
+def test_single_thread_oracle_probe_runs_in_its_own_interpreter():
+    r = bench._probe_subprocess("c1", 0, 1)
+    assert r["seconds"] > 0 and r["sample"].startswith("the whole forward")
