@@ -179,6 +179,12 @@ tp_status tp_column_parallel_forward(const tp_bf16* X, int64_t M, int64_t h, int
  *   residual [M][h] nullable; Y [M][h].  h, K/t multiples of 8. */
 tp_status tp_row_parallel_forward(const tp_bf16* A, int64_t M, int64_t K, int64_t h, int t, const tp_bf16* W_p,
                                   const tp_bf16* b, const tp_bf16* residual, tp_bf16* Y, tp_stream stream);
+/* Few tokens (M <= 128, a single 128-row output tile) leave most SMs idle: there, these
+ * two calls, the MLP and the attention blocks split each output tile's K steps -- for the
+ * row-parallel GEMM the t shards' K ranges laid end to end -- over the 2..16 CTAs of a
+ * thread-block cluster, which sum their fp32 partials on chip (distributed shared memory)
+ * in range order before the epilogue.  No workspace is needed and the result does not
+ * depend on timing; only the rounding of the fp32 sum differs from the unsplit GEMM. */
 
 /* Row-parallel GEMM with the g all-reduce overlapped, tile by tile ("Tensor
  * and sequence parallelism", section "Volume and scale": the matrix multiply is
@@ -223,7 +229,8 @@ tp_status tp_row_parallel_forward_overlap(const tp_bf16* A, int64_t M, int64_t K
  *   of 128); Z_i = X [W_gate | W_up]_i is saved in the same interleaved order,
  *   Z_save [t][M][2F/t] (required); A_i = silu(gate) * up [t][M][F/t], formed in the
  *   GEMM's epilogue from the fp32 accumulators.  bup must be NULL (TP_ERR_UNSUPPORTED
- *   otherwise); (F/t) % 128 == 0 (TP_ERR_SHAPE). */
+ *   otherwise); (F/t) % 128 == 0 (TP_ERR_SHAPE).
+ * ws: tp_mlp_workspace_size() bytes (0, and ws may be NULL, without the two flags above). */
 size_t tp_mlp_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned flags);
 tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int t, tp_act act,
                          const tp_bf16* Wup_p, const tp_bf16* bup, const tp_bf16* Wdown_p, const tp_bf16* bdown,

@@ -188,6 +188,57 @@ AttnBwdWs attn_bwd_layout(void* ws, int64_t N, int64_t d, int n_heads, int64_t r
 
 }  // namespace
 
+namespace {
+
+// Partials [t][M][h] fp32, then (overlapped reduction) the block counters.
+size_t row_partials_ws(int64_t M, int64_t h, int t, bool overlap) {
+  size_t sz = round_up(static_cast<size_t>(t) * M * h * sizeof(float), 256);
+  if (overlap) sz += round_up(static_cast<size_t>(gemm_overlap_counters(M, h)) * sizeof(int), 256);
+  return sz;
+}
+
+tp_status column_parallel(const tp_bf16* X, int64_t M, int64_t h, int64_t N, int t, tp_act act, const tp_bf16* W_p,
+                          const tp_bf16* b, tp_bf16* Z, tp_bf16* A, cudaStream_t s) {
+  if (M < 0 || h < 1 || N < 1 || t < 1 || !act_ok(act)) return TP_ERR_INVALID_ARG;
+  if (N % t != 0) return TP_ERR_SHAPE;
+  const int64_t Nt = N / t;
+  if (h % 8 != 0 || Nt % 8 != 0) return TP_ERR_ALIGN;
+  if (M == 0) return TP_OK;
+  if (!X || !W_p || !A) return TP_ERR_INVALID_ARG;
+  GemmProblem c;
+  c.M = M; c.N = Nt; c.K = h; c.nbatch = t; c.nsum = 1;
+  c.a.ptr = X; c.a.ld = h;
+  c.b.ptr = W_p; c.b.ld = h; c.b.sharded = true; c.b.shard_stride = Nt * h;
+  c.epi = EPI_ACT; c.act = act;
+  c.d = Z; c.d2 = A; c.ldd = Nt; c.d_batch_stride = M * Nt;
+  c.bias = b; c.bias_batch_stride = Nt;
+  return run_gemm(c, s);
+}
+
+tp_status row_parallel(const tp_bf16* A, int64_t M, int64_t K, int64_t h, int t, const tp_bf16* W_p,
+                       const tp_bf16* b, const tp_bf16* residual, tp_bf16* Y, cudaStream_t s) {
+  if (M < 0 || h < 1 || K < 1 || t < 1) return TP_ERR_INVALID_ARG;
+  if (K % t != 0) return TP_ERR_SHAPE;
+  const int64_t Kt = K / t;
+  if (h % 8 != 0 || Kt % 8 != 0) return TP_ERR_ALIGN;
+  if (M == 0) return TP_OK;
+  if (!A || !W_p || !Y) return TP_ERR_INVALID_ARG;
+  GemmProblem r;
+  r.M = M; r.N = h; r.K = Kt; r.nbatch = 1; r.nsum = t;
+  r.a.ptr = A; r.a.ld = Kt; r.a.sharded = true; r.a.shard_stride = M * Kt;
+  r.b.ptr = W_p; r.b.ld = Kt; r.b.sharded = true; r.b.shard_stride = h * Kt;
+  r.epi = EPI_BF16; r.d = Y; r.ldd = h; r.bias = b; r.residual = residual; r.ld_res = h;
+  return run_gemm(r, s);
+}
+
+// The forward's scratch: the partials of the unfused / overlapped reduction.
+size_t mlp_fwd_base_ws(int64_t M, int64_t h, int t, unsigned flags) {
+  if (flags & TP_FLAG_OVERLAP_REDUCE) return row_partials_ws(M, h, t, true);
+  return (flags & TP_FLAG_UNFUSED_REDUCE) ? round_up(static_cast<size_t>(t) * M * h * sizeof(float), 256) : 0;
+}
+
+}  // namespace
+
 extern "C" {
 
 size_t tp_attn_gqa_backward_workspace_size(int64_t N, int64_t d, int n_heads, int n_kv_heads, int head_dim, int t,
@@ -374,17 +425,10 @@ tp_status tp_pack_qkv_gqa_bias(const tp_bf16* b, int n_heads, int n_kv_heads, in
 }
 
 // ------------------------------------------------------------------ TP MLP
-// Partials [t][M][h] fp32, then (overlapped reduction) the block counters.
-size_t row_partials_ws(int64_t M, int64_t h, int t, bool overlap) {
-  size_t sz = round_up(static_cast<size_t>(t) * M * h * sizeof(float), 256);
-  if (overlap) sz += round_up(static_cast<size_t>(gemm_overlap_counters(M, h)) * sizeof(int), 256);
-  return sz;
-}
 
 size_t tp_mlp_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned flags) {
   if (M < 0 || h < 0 || F < 0 || t < 1) return 0;
-  if (flags & TP_FLAG_OVERLAP_REDUCE) return row_partials_ws(M, h, t, true);
-  return (flags & TP_FLAG_UNFUSED_REDUCE) ? static_cast<size_t>(t) * M * h * sizeof(float) : 0;
+  return mlp_fwd_base_ws(M, h, t, flags);
 }
 
 size_t tp_row_parallel_overlap_workspace_size(int64_t M, int64_t K, int64_t h, int t) {
@@ -424,36 +468,12 @@ tp_status tp_row_parallel_forward_overlap(const tp_bf16* A, int64_t M, int64_t K
 tp_status tp_column_parallel_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t N, int t, tp_act act,
                                      const tp_bf16* W_p, const tp_bf16* b, tp_bf16* Z, tp_bf16* A,
                                      tp_stream stream) {
-  if (M < 0 || h < 1 || N < 1 || t < 1 || !act_ok(act)) return TP_ERR_INVALID_ARG;
-  if (N % t != 0) return TP_ERR_SHAPE;
-  const int64_t Nt = N / t;
-  if (h % 8 != 0 || Nt % 8 != 0) return TP_ERR_ALIGN;
-  if (M == 0) return TP_OK;
-  if (!X || !W_p || !A) return TP_ERR_INVALID_ARG;
-  GemmProblem c;
-  c.M = M; c.N = Nt; c.K = h; c.nbatch = t; c.nsum = 1;
-  c.a.ptr = X; c.a.ld = h;
-  c.b.ptr = W_p; c.b.ld = h; c.b.sharded = true; c.b.shard_stride = Nt * h;
-  c.epi = EPI_ACT; c.act = act;
-  c.d = Z; c.d2 = A; c.ldd = Nt; c.d_batch_stride = M * Nt;
-  c.bias = b; c.bias_batch_stride = Nt;
-  return run_gemm(c, S(stream));
+  return column_parallel(X, M, h, N, t, act, W_p, b, Z, A, S(stream));
 }
 
 tp_status tp_row_parallel_forward(const tp_bf16* A, int64_t M, int64_t K, int64_t h, int t, const tp_bf16* W_p,
                                   const tp_bf16* b, const tp_bf16* residual, tp_bf16* Y, tp_stream stream) {
-  if (M < 0 || h < 1 || K < 1 || t < 1) return TP_ERR_INVALID_ARG;
-  if (K % t != 0) return TP_ERR_SHAPE;
-  const int64_t Kt = K / t;
-  if (h % 8 != 0 || Kt % 8 != 0) return TP_ERR_ALIGN;
-  if (M == 0) return TP_OK;
-  if (!A || !W_p || !Y) return TP_ERR_INVALID_ARG;
-  GemmProblem r;
-  r.M = M; r.N = h; r.K = Kt; r.nbatch = 1; r.nsum = t;
-  r.a.ptr = A; r.a.ld = Kt; r.a.sharded = true; r.a.shard_stride = M * Kt;
-  r.b.ptr = W_p; r.b.ld = Kt; r.b.sharded = true; r.b.shard_stride = h * Kt;
-  r.epi = EPI_BF16; r.d = Y; r.ldd = h; r.bias = b; r.residual = residual; r.ld_res = h;
-  return run_gemm(r, S(stream));
+  return row_parallel(A, M, K, h, t, W_p, b, residual, Y, S(stream));
 }
 
 tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int t, tp_act act,
@@ -488,14 +508,14 @@ tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int 
     TP_RETURN_IF(run_gemm(c, s));
   } else {
     // f (identity) + column-parallel: Z_i = X W_up,i + b_up[C_i]; A_i = act(Z_i).
-    TP_RETURN_IF(tp_column_parallel_forward(X, M, h, F, t, act, Wup_p, bup, Z_save, A_save, stream));
+    TP_RETURN_IF(column_parallel(X, M, h, F, t, act, Wup_p, bup, Z_save, A_save, s));
   }
   if (overlap)
     return tp_row_parallel_forward_overlap(A_save, M, F, h, t, Wdown_p, bdown, residual, Y, nullptr, ws, ws_bytes,
                                            stream);
 
   // Row-parallel + g: Y = sum_i A_i W_down,i + b_down (once) + residual.
-  if (!unfused) return tp_row_parallel_forward(A_save, M, F, h, t, Wdown_p, bdown, residual, Y, stream);
+  if (!unfused) return row_parallel(A_save, M, F, h, t, Wdown_p, bdown, residual, Y, s);
   GemmProblem r;
   r.M = M; r.N = h; r.K = Ft; r.nbatch = t; r.nsum = 1;
   r.a.ptr = A_save; r.a.ld = Ft; r.a.sharded = true; r.a.shard_stride = M * Ft;

@@ -91,6 +91,9 @@ struct GemmArgs {
   const uint16_t* ovl_bias;
   const uint16_t* ovl_res;
   int64_t ovl_ld;
+  // K ranges per output tile: 1, except in gemm_splitc_kernel, where the nsum * kt k-steps of
+  // a tile are cut into ksplit nearly equal ranges, one per CTA of a cluster.
+  int ksplit;
   int* err;
   uint64_t timeout_ns;
 };
@@ -115,11 +118,19 @@ __device__ __forceinline__ void pair_tile(int tile, int mt2, int nt2, int nbatch
   }
 }
 
-__device__ __forceinline__ void decode_tile(int tile, const GemmArgs& p, int& b, int& mb, int& nb) {
+__device__ __forceinline__ void decode_tile(int tile, const GemmArgs& p, int& b, int& mb, int& nb, int& j) {
   mb = tile % p.mt;
-  const int rest = tile / p.mt;
+  int rest = tile / p.mt;
   nb = rest % p.nt;
-  b = rest / p.nt;
+  rest /= p.nt;
+  b = rest % p.nbatch;
+  j = rest / p.nbatch;  // K range (0 unless split)
+}
+
+// K steps [lo, hi) of range j when `ksteps` are cut into `ksplit` nearly equal ranges.
+__device__ __forceinline__ void split_range(int ksteps, int ksplit, int j, int& lo, int& hi) {
+  lo = static_cast<int>((static_cast<int64_t>(j) * ksteps) / ksplit);
+  hi = static_cast<int>((static_cast<int64_t>(j + 1) * ksteps) / ksplit);
 }
 
 __device__ __forceinline__ void load_bf16x32(const uint16_t* src, float (&v)[32]) {
@@ -424,6 +435,53 @@ __device__ __forceinline__ void dact_colsum_chunk(const GemmArgs& p, int b, int 
     p.cs[(static_cast<int64_t>(b) * p.cs_chunks + m0 / 32) * p.N + n0 + lane] = s;
 }
 
+// One k-step of the single-CTA kernels: the TMA copies of A's and B's tiles for k-step ks
+// of output tile (b, mb, nb) into stage buffers a_dst / b_dst, completing on `bar`.
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ void load_stage(const GemmArgs& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                           uint8_t* a_dst, uint8_t* b_dst, uint64_t* bar, int ks, int b, int mb,
+                                           int nb) {
+  const int s = ks / p.kt;
+  const int kb = ks - s * p.kt;
+  ptx::mbar_arrive_expect_tx(bar, STAGE_BYTES);
+  const int ash = p.a_sharded ? (p.nsum > 1 ? s : b) : 0;
+  const int bsh = p.b_sharded ? (p.nsum > 1 ? s : b) : 0;
+  if (!A_MN) {
+    ptx::tma_load_3d(a_dst, tmA, bar, kb * BK, mb * BM, ash);
+  } else if (p.a_4d) {
+    ptx::tma_load_4d(a_dst, tmA, bar, 0, kb * BK, mb * (BM / 64), ash);
+  } else {
+#pragma unroll
+    for (int j = 0; j < BM / 64; ++j)
+      ptx::tma_load_3d(a_dst + j * MN_CHUNK_BYTES, tmA, bar, mb * BM + j * 64, kb * BK, ash);
+  }
+  if (!B_MN) {
+    ptx::tma_load_3d(b_dst, tmB, bar, kb * BK, nb * BN, bsh);
+  } else if (p.b_4d) {
+    ptx::tma_load_4d(b_dst, tmB, bar, 0, kb * BK, nb * (BN / 64), bsh);
+  } else {
+#pragma unroll
+    for (int j = 0; j < BN / 64; ++j)
+      ptx::tma_load_3d(b_dst + j * MN_CHUNK_BYTES, tmB, bar, nb * BN + j * 64, kb * BK, bsh);
+  }
+}
+
+// The MMAs of one stage (BK deep) into the accumulator at d_tmem; `first` starts it afresh.
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr, bool first) {
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, A_MN, B_MN);
+#pragma unroll
+  for (int kk = 0; kk < BK / 16; ++kk) {
+    // K-major: 16 K-elements = 32 bytes inside the 128-byte swizzle row; 8-row groups 1024 B apart.
+    // MN-major: 16 K-rows = two 1024-byte groups; 64-wide MN chunks MN_CHUNK_BYTES apart.
+    const uint64_t ad = A_MN ? ptx::sdesc_sw128(a_addr + kk * 2048, MN_CHUNK_BYTES, 1024)
+                             : ptx::sdesc_sw128(a_addr + kk * 32, 16, 1024);
+    const uint64_t bd = B_MN ? ptx::sdesc_sw128(b_addr + kk * 2048, MN_CHUNK_BYTES, 1024)
+                             : ptx::sdesc_sw128(b_addr + kk * 32, 16, 1024);
+    ptx::mma_bf16(d_tmem, ad, bd, idesc, (!first || kk > 0) ? 1u : 0u);
+  }
+}
+
 template <bool A_MN, bool B_MN, int EPI, int ACT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -489,38 +547,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int issued = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        int b, mb, nb;
-        decode_tile(tile, p, b, mb, nb);
+        int b, mb, nb, j;
+        decode_tile(tile, p, b, mb, nb, j);
         for (int ks = 0; ks < ksteps; ++ks) {
-          const int s = ks / p.kt;
-          const int kb = ks - s * p.kt;
           if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err, ERR_WAIT_PRODUCER, p.timeout_ns)) {
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-          const int ash = p.a_sharded ? (p.nsum > 1 ? s : b) : 0;
-          const int bsh = p.b_sharded ? (p.nsum > 1 ? s : b) : 0;
-          uint8_t* a_dst = sA + stage * A_TILE_BYTES;
-          uint8_t* b_dst = sB + stage * B_TILE_BYTES;
-          if (!A_MN) {
-            ptx::tma_load_3d(a_dst, &tmA, &full[stage], kb * BK, mb * BM, ash);
-          } else if (p.a_4d) {
-            ptx::tma_load_4d(a_dst, &tmA, &full[stage], 0, kb * BK, mb * (BM / 64), ash);
-          } else {
-#pragma unroll
-            for (int j = 0; j < BM / 64; ++j)
-              ptx::tma_load_3d(a_dst + j * MN_CHUNK_BYTES, &tmA, &full[stage], mb * BM + j * 64, kb * BK, ash);
-          }
-          if (!B_MN) {
-            ptx::tma_load_3d(b_dst, &tmB, &full[stage], kb * BK, nb * BN, bsh);
-          } else if (p.b_4d) {
-            ptx::tma_load_4d(b_dst, &tmB, &full[stage], 0, kb * BK, nb * (BN / 64), bsh);
-          } else {
-#pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              ptx::tma_load_3d(b_dst + j * MN_CHUNK_BYTES, &tmB, &full[stage], nb * BN + j * 64, kb * BK, bsh);
-          }
+          load_stage<A_MN, B_MN>(p, &tmA, &tmB, sA + stage * A_TILE_BYTES, sB + stage * B_TILE_BYTES,
+                                 &full[stage], ks, b, mb, nb);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -538,7 +573,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -554,18 +588,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t a_addr = ptx::smem_addr(sA + stage * A_TILE_BYTES);
-          const uint32_t b_addr = ptx::smem_addr(sB + stage * B_TILE_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            // K-major: 16 K-elements = 32 bytes inside the 128-byte swizzle row; 8-row groups 1024 B apart.
-            // MN-major: 16 K-rows = two 1024-byte groups; 64-wide MN chunks MN_CHUNK_BYTES apart.
-            const uint64_t ad = A_MN ? ptx::sdesc_sw128(a_addr + kk * 2048, MN_CHUNK_BYTES, 1024)
-                                     : ptx::sdesc_sw128(a_addr + kk * 32, 16, 1024);
-            const uint64_t bd = B_MN ? ptx::sdesc_sw128(b_addr + kk * 2048, MN_CHUNK_BYTES, 1024)
-                                     : ptx::sdesc_sw128(b_addr + kk * 32, 16, 1024);
-            ptx::mma_bf16(d_tmem, ad, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
-          }
+          mma_stage<A_MN, B_MN>(d_tmem, ptx::smem_addr(sA + stage * A_TILE_BYTES),
+                                ptx::smem_addr(sB + stage * B_TILE_BYTES), ks == 0);
           ptx::mma_commit(&empty[stage]);  // frees this smem stage once its MMAs are done
           if (++stage == STAGES) {
             stage = 0;
@@ -589,8 +613,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      int b, mb, nb;
-      decode_tile(tile, p, b, mb, nb);
+      int b, mb, nb, j;
+      decode_tile(tile, p, b, mb, nb, j);
       if (!ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err, ERR_WAIT_EPI, p.timeout_ns)) break;
       ptx::tc_fence_after();
       const int m = mb * BM + row;
@@ -648,6 +672,245 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+
+// ------------------------------------------------- split K inside a cluster
+// For problems with too few output tiles to occupy the GPU (M <= 128, one 128-row tile of
+// tokens): the S = ksplit CTAs of a cluster compute the same 128 x 256 output tile, CTA j
+// (its cluster rank) over K range j -- for a row-parallel GEMM the t shards' K ranges laid
+// end to end.  The partial sums never leave the chip: once every CTA's MMAs are complete
+// (cluster barrier), each epilogue thread reads its accumulator row from TMEM and writes it
+// into the shared memory of the CTA that owns that row (R = 128 / S rows per CTA), in the
+// slot of its K range; the operand stages, idle by then, hold what arrives.  After a second
+// cluster barrier each CTA sums its R rows over the S ranges in range order -- the result
+// does not depend on timing -- and applies the epilogue with coalesced stores.
+constexpr int SPLITC_ROWF = BN + 4;  // floats per received row (16 bytes of padding spread the banks)
+// Per epilogue warp, a 32 x 32 block of its partial on its way out: written row per lane,
+// read back as 128-byte row segments so that every remote store moves whole segments.
+constexpr int SPLITC_XF = 32 + 4;  // floats per staged row
+constexpr int SPLITC_RECV_BYTES = BM * SPLITC_ROWF * 4;
+constexpr int SPLITC_XBYTES = 32 * SPLITC_XF * 4;
+static_assert(SPLITC_RECV_BYTES + 4 * SPLITC_XBYTES <= STAGES * STAGE_BYTES,
+              "received partials and the staging blocks must fit the operand stages");
+
+// Epilogue of two adjacent columns n, n + 1 (n even, N even) of row m after the split sum;
+// (b0, b1) is the bias of the two columns (zeros without one).
+template <int EPI, int ACT>
+__device__ __forceinline__ void splitc_store2(const GemmArgs& p, int b, int m, int n, float v0, float v1, float b0,
+                                              float b1) {
+  const int64_t off = b * p.d_bs + static_cast<int64_t>(m) * p.ldd + n;
+  if constexpr (EPI == EPI_F32) {
+    float2* d = reinterpret_cast<float2*>(static_cast<float*>(p.d) + off);
+    if (p.accumulate) {
+      const float2 o = *d;
+      v0 += o.x;
+      v1 += o.y;
+    }
+    *d = make_float2(v0, v1);
+    return;
+  }
+  v0 += b0;
+  v1 += b1;
+  if constexpr (EPI == EPI_BF16) {
+    if (p.res) {
+      float r0, r1;
+      unpack_bf16x2(*reinterpret_cast<const uint32_t*>(p.res + static_cast<int64_t>(m) * p.ld_res + n), r0, r1);
+      v0 += r0;
+      v1 += r1;
+    }
+    *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.d) + off) = pack_bf16x2(v0, v1);
+  } else {  // EPI_ACT
+    if (p.d)
+      *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.d) + off) =
+          p.out_f16 ? pack_f16x2(v0, v1) : pack_bf16x2(v0, v1);
+    v0 = act_apply_t<ACT>(v0);
+    v1 = act_apply_t<ACT>(v1);
+    *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.d2) + off) =
+        p.out_f16 ? pack_f16x2(v0, v1) : pack_bf16x2(v0, v1);
+  }
+}
+
+template <bool A_MN, bool B_MN, int EPI, int ACT>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_splitc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const GemmArgs p) {
+  extern __shared__ uint8_t dsmem[];
+  const uint32_t pad = (1024u - (ptx::smem_addr(dsmem) & 1023u)) & 1023u;
+  uint8_t* base = dsmem + pad;
+  uint8_t* sA = base;
+  uint8_t* sB = base + STAGES * A_TILE_BYTES;
+  float* recv = reinterpret_cast<float*>(base);  // after the main loop: [S][R][SPLITC_ROWF]
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int S = p.ksplit;
+  const int R = BM / S;
+  const int j = static_cast<int>(ptx::cluster_ctarank());
+  int b, mb, nb, unused;
+  decode_tile(static_cast<int>(blockIdx.x) / S, p, b, mb, nb, unused);
+  int klo, khi;
+  split_range(p.nsum * p.kt, S, j, klo, khi);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    ptx::mbar_init(tfull, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, BN);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncwarp();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // Programmatic dependent launch, as in gemm_kernel: every global access follows the
+  // producer's griddepcontrol.wait through the barriers.
+  ptx::griddep_launch_dependents();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ TMA producer
+      ptx::griddep_wait();
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      for (int ks = klo; ks < khi; ++ks) {
+        if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err, ERR_WAIT_PRODUCER, p.timeout_ns)) break;
+        load_stage<A_MN, B_MN>(p, &tmA, &tmB, sA + stage * A_TILE_BYTES, sB + stage * B_TILE_BYTES, &full[stage],
+                               ks, b, mb, nb);
+        ++issued;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      volatile int never = 0;  // every copy issued lands before the stages are reused
+      for (int s = 0; s < STAGES && s < issued; ++s) {
+        const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+        ptx::mbar_wait(&full[s], par, &never, p.err, ERR_WAIT_DRAIN, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------- MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int ks = klo; ks < khi; ++ks) {
+        if (!ptx::mbar_wait(&full[stage], phase, abort_flag, p.err, ERR_WAIT_MMA, p.timeout_ns)) break;
+        ptx::tc_fence_after();
+        mma_stage<A_MN, B_MN>(tmem_base, ptx::smem_addr(sA + stage * A_TILE_BYTES),
+                              ptx::smem_addr(sB + stage * B_TILE_BYTES), ks == klo);
+        ptx::mma_commit(&empty[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      // Always committed, also after an abort: once it completes no MMA is running.
+      ptx::mma_commit(tfull);
+      volatile int never = 0;
+      ptx::mbar_wait(tfull, 0, &never, p.err, ERR_WAIT_DRAIN, p.timeout_ns);
+    }
+  } else {
+    ptx::mbar_wait(tfull, 0, abort_flag, p.err, ERR_WAIT_EPI, p.timeout_ns);
+  }
+
+  // Barrier 1: every CTA's MMAs are complete, so every CTA's operand stages are free.
+  ptx::tc_fence_before();
+  __syncwarp();
+  ptx::cluster_sync();
+  if (warp >= 2) {
+    ptx::tc_fence_after();
+    const int quad = warp & 3;  // TMEM lanes 32 * (warp % 4) .. + 31
+    const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+    float* xs = reinterpret_cast<float*>(base + SPLITC_RECV_BYTES + quad * SPLITC_XBYTES);
+    // After the transpose through xs, lane l carries columns 4 (l % 8) .. + 3 of rows
+    // 4 i + l / 8 (i = 0..7) of the warp's 32: eight lanes cover a row's 128 bytes.
+    const int seg = lane & 7;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      if (nb * BN + c * 32 >= p.N) break;  // warp-uniform: columns past N are never summed
+      uint32_t r[32];
+      ptx::tmem_ld32(t_row + c * 32, r);
+      ptx::tmem_ld_wait();
+      float* mine = xs + lane * SPLITC_XF;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<uint4*>(mine + 4 * q) = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rl = 4 * i + (lane >> 3);  // row within the warp's 32
+        const int row = quad * 32 + rl;
+        const uint4 v = *reinterpret_cast<const uint4*>(xs + rl * SPLITC_XF + 4 * seg);
+        const uint32_t dst = ptx::mapa_shared(
+            ptx::smem_addr(recv + (static_cast<int64_t>(j) * R + row % R) * SPLITC_ROWF + c * 32 + 4 * seg),
+            static_cast<uint32_t>(row / R));
+        ptx::st_cluster_v4(dst, v.x, v.y, v.z, v.w);
+      }
+      __syncwarp();  // xs is rewritten by the next chunk
+    }
+  }
+  // Barrier 2: every partial row has arrived where it is summed.
+  ptx::tc_fence_before();
+  __syncwarp();
+  ptx::cluster_sync();
+  if (warp >= 2) {
+    const int e = static_cast<int>(threadIdx.x) - 64;  // columns 2e, 2e + 1 of each owned row
+    const int n = nb * BN + 2 * e;
+    if (n < p.N) {
+      float b0 = 0.0f, b1 = 0.0f;
+      if (EPI != EPI_F32 && p.bias)
+        unpack_bf16x2(*reinterpret_cast<const uint32_t*>(p.bias + (EPI == EPI_ACT ? b * p.bias_bs : 0) + n), b0, b1);
+      const int rows = min(R, p.M - (mb * BM + j * R));
+      // Eight rows at a time: every load of the batch is issued before the first store, so
+      // the shared-memory latency is paid once per batch rather than once per row.
+      const float* __restrict__ rbase = recv + 2 * e;
+#pragma unroll 1
+      for (int r0 = 0; r0 < rows; r0 += 8) {
+        float2 acc[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          acc[u] = *reinterpret_cast<const float2*>(rbase + min(r0 + u, R - 1) * SPLITC_ROWF);
+        for (int k = 1; k < S; ++k) {  // K ranges in order
+          const float* __restrict__ src = rbase + static_cast<int64_t>(k) * R * SPLITC_ROWF;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float2 x = *reinterpret_cast<const float2*>(src + min(r0 + u, R - 1) * SPLITC_ROWF);
+            acc[u].x += x.x;
+            acc[u].y += x.y;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (r0 + u < rows) splitc_store2<EPI, ACT>(p, b, mb * BM + j * R + r0 + u, n, acc[u].x, acc[u].y, b0, b1);
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncwarp();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, BN);
+  }
+}
 
 // ------------------------------------------------------------ CTA-pair GEMM
 // Same contract as gemm_kernel, computed by clusters of two CTAs on two SMs
@@ -1554,6 +1817,113 @@ tp_status dispatch(bool amn, bool bmn, int epi, int act, F&& f) {
   return TP_ERR_UNSUPPORTED;
 }
 
+// ----------------------------------------------------- split K: launch
+// Clusters of S CTAs that can be resident at once for this instance (0 if none).
+template <bool A_MN, bool B_MN, int EPI, int ACT>
+int splitc_clusters(int dev, int S) {
+  static int cached[64][5] = {};  // [device][log2 S - 1] + 1
+  int li = 0;
+  while ((2 << li) < S) ++li;
+  if (dev < 0 || dev >= 64 || li > 4) return 0;
+  if (cached[dev][li]) return cached[dev][li] - 1;
+  auto kern = gemm_splitc_kernel<A_MN, B_MN, EPI, ACT>;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) == cudaSuccess &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S * 16, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = S;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  cached[dev][li] = n + 1;
+  return n;
+}
+
+template <bool A_MN, bool B_MN, int EPI, int ACT>
+tp_status launch_splitc(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int64_t tiles, int S,
+                        cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles * S), 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = S;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  TP_CUDA_CHECK(cudaLaunchKernelEx(&cfg, gemm_splitc_kernel<A_MN, B_MN, EPI, ACT>, ta, tb, a));
+  count_launch();
+  return TP_OK;
+}
+
+// Instances of the cluster-split kernel: the epilogues a small-M problem can have.
+template <class F>
+tp_status dispatch_splitc(bool amn, bool bmn, int epi, int act, F&& f) {
+  using T = std::true_type;
+  using Fl = std::false_type;
+  using E_BF16 = std::integral_constant<int, EPI_BF16>;
+  using E_ACT = std::integral_constant<int, EPI_ACT>;
+  using E_F32 = std::integral_constant<int, EPI_F32>;
+  using I0 = std::integral_constant<int, 0>;
+  if (!amn && !bmn) {
+    if (epi == EPI_ACT) {
+      switch (act) {
+        case 0: return f(Fl{}, Fl{}, E_ACT{}, I0{});
+        case 1: return f(Fl{}, Fl{}, E_ACT{}, std::integral_constant<int, 1>{});
+        case 2: return f(Fl{}, Fl{}, E_ACT{}, std::integral_constant<int, 2>{});
+        case 3: return f(Fl{}, Fl{}, E_ACT{}, std::integral_constant<int, 3>{});
+      }
+    }
+    if (epi == EPI_BF16) return f(Fl{}, Fl{}, E_BF16{}, I0{});
+    if (epi == EPI_F32) return f(Fl{}, Fl{}, E_F32{}, I0{});
+  } else if (!amn && bmn) {
+    if (epi == EPI_ACT && act == 0) return f(Fl{}, T{}, E_ACT{}, I0{});
+    if (epi == EPI_BF16) return f(Fl{}, T{}, E_BF16{}, I0{});
+    if (epi == EPI_F32) return f(Fl{}, T{}, E_F32{}, I0{});
+  }
+  return TP_ERR_UNSUPPORTED;
+}
+
+// K ranges per tile for a small-M problem: a power of two up to 8 such that the tiles
+// times S CTAs about fill the GPU and every range keeps at least kSplitMinSteps k-blocks.
+// (On a GB300, the 128-token forward: 8 ranges of the row-parallel GEMM ran 21.9 us against
+// 22.2 us for 16, whose exchange through distributed shared memory waits longer for the
+// slowest CTA.)  TP_SPLITK=<S> asks for S, up to 16 (rounded down to a power of two;
+// 1 disables the split).
+constexpr int kSplitMinSteps = 4;
+constexpr int kSplitAutoMax = 8;
+int splitc_ranges(int64_t tiles, int64_t ksteps) {
+  int64_t want;
+  const char* e = std::getenv("TP_SPLITK");
+  if (e && e[0]) {
+    want = std::atol(e);
+  } else {
+    const int64_t sms = device_sm_count();
+    if (tiles * 2 > sms) return 1;
+    want = sms / tiles;
+    if (want > ksteps / kSplitMinSteps) want = ksteps / kSplitMinSteps;
+    if (want > kSplitAutoMax) want = kSplitAutoMax;
+  }
+  if (want > ksteps) want = ksteps;
+  int S = 1;
+  while (S * 2 <= want && S < 16) S *= 2;
+  return S;
+}
+
 bool operand_ok(const GemmOperand& o) {
   return o.ptr && aligned16(o.ptr) && o.ld > 0 && o.ld % 8 == 0 && (!o.sharded || o.shard_stride % 8 == 0);
 }
@@ -1642,6 +2012,7 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
   a.ovl_bias = P.ovl_bias;
   a.ovl_res = P.ovl_res;
   a.ovl_ld = P.ovl_ld;
+  a.ksplit = 1;
   a.err = device_error_word();
   a.timeout_ns = wait_timeout_ns();
   if (!a.err) return TP_ERR_CUDA;
@@ -1687,6 +2058,31 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
     });
   }
   const int64_t tiles = mt * nt * P.nbatch;
+  // Split K inside a cluster when few output tiles would leave most SMs idle (M <= 128):
+  // the S CTAs of a cluster compute one tile's K ranges and sum them on chip, in order.
+  if (P.M <= 128 && P.N % 8 == 0 && !P.colsum && (P.epi == EPI_BF16 || P.epi == EPI_ACT || P.epi == EPI_F32)) {
+    int dev = 0;
+    TP_CUDA_CHECK(cudaGetDevice(&dev));
+    int S = splitc_ranges(tiles, static_cast<int64_t>(P.nsum) * kt);
+    tp_status st = TP_ERR_UNSUPPORTED;
+    while (S > 1) {  // the largest cluster size this device can schedule
+      st = dispatch_splitc(amn, bmn, P.epi, P.act, [&](auto am, auto bm, auto ep, auto ac) {
+        return splitc_clusters<decltype(am)::value, decltype(bm)::value, decltype(ep)::value, decltype(ac)::value>(
+                   dev, S) > 0
+                   ? TP_OK
+                   : TP_ERR_UNSUPPORTED;
+      });
+      if (st == TP_OK) break;
+      S /= 2;
+    }
+    if (S > 1) {
+      a.ksplit = S;
+      return dispatch_splitc(amn, bmn, P.epi, P.act, [&](auto am, auto bm, auto ep, auto ac) {
+        return launch_splitc<decltype(am)::value, decltype(bm)::value, decltype(ep)::value, decltype(ac)::value>(
+            ta, tb, a, tiles, S, s);
+      });
+    }
+  }
   const int grid = static_cast<int>(tiles < device_sm_count() ? tiles : device_sm_count());
   return dispatch(amn, bmn, P.epi, P.act, [&](auto am, auto bm, auto ep, auto ac) {
     return launch<decltype(am)::value, decltype(bm)::value, decltype(ep)::value, decltype(ac)::value>(ta, tb, a, grid,
