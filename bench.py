@@ -204,6 +204,9 @@ def run_ours(args):
     dbdown = torch.empty(h, dtype=f32, device=dev)
     nws = L.tp_mlp_backward_workspace_size(M, h, F, t, 0)
     ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+    # forward GEMMs' workspace (stream-K partials); the calls run one after the other
+    nfw = max(L.tp_column_parallel_workspace_size(M, h, F, t), L.tp_row_parallel_workspace_size(M, F, h, t))
+    fws = torch.empty(nfw, dtype=torch.uint8, device=dev)
 
     col_ev = []
 
@@ -212,11 +215,11 @@ def run_ours(args):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
         # forward: f (identity) + column-parallel GEMM + GeLU, then row-parallel GEMM + g (bias once)
-        L.tp_column_parallel_forward(X, M, h, F, t, act, Wup_p, bup, Z, A)
+        L.tp_column_parallel_forward_ws(X, M, h, F, t, act, Wup_p, bup, Z, A, fws, nfw)
         if record:
             e1.record()
             col_ev.append((e0, e1))
-        L.tp_row_parallel_forward(A, M, F, h, t, Wdown_p, bdown, None, Y)
+        L.tp_row_parallel_forward_ws(A, M, F, h, t, Wdown_p, bdown, None, Y, fws, nfw)
         # backward: g (identity), dgrad*act', wgrads, f (fused dX reduction), bias grads
         L.tp_mlp_backward(dY, X, Z, A, M, h, F, t, act, Wup_p, Wdown_p, dX, dWup, dWdown, dbup, dbdown, 0, 0,
                           ws, nws)
@@ -360,7 +363,7 @@ def run_ours(args):
                    "l2": "working set ~1.1 GB > 129 MB L2; no flush",
                    "frac_of_peak": round(value / world / peak, 4), "peak_tflops": peak,
                    "peak_kind": f"{peak_kind} ({peaks['source']})"},
-        "roofline": {"bound": "tensor", "kernel": "gemm_pair_kernel<K-major, K-major, EPI_ACT, GeLU-tanh> (column-parallel GEMM + GeLU epilogue)",
+        "roofline": {"bound": "tensor", "kernel": "gemm_pair_kernel<K-major, K-major, EPI_ACT, GeLU-tanh> (column-parallel GEMM + GeLU epilogue, stream-K schedule)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": UNIT,
                      "frac": round(achieved / peak, 4), "traffic": recorded_traffic("gemm_colpar_fwd_c2.md"),
                      "kernel_ms": round(col_ms, 4), "flops_per_launch": col_flops},
@@ -383,7 +386,7 @@ _COMPACT = {
     "sp_layernorm_c5": ("fwd_us", "fwd_frac_of_hbm", "bwd_us", "bwd_frac_of_hbm"),
     "decode_attention": ("us_per_step", "frac_of_hbm", "us_per_step_graph"),
     "vocab_embedding": ("fwd_us", "fwd_frac_of_hbm", "bwd_us", "bwd_frac_of_hbm"),
-    "row_parallel_overlap_c2": ("fused_ms", "overlap_ms", "separate_reduce_kernel_ms"),
+    "row_parallel_overlap_c2": ("fused_ms", "fused_streamk_ms", "overlap_ms", "separate_reduce_kernel_ms"),
     "mlp_fwd_c1": ("us_per_step", "TFLOPs", "us_per_step_graph"),
     "decode_c3": ("us_per_step", "GBps", "frac_of_hbm", "frac_of_8TBps"),
 }
@@ -552,7 +555,10 @@ def run_overlap_extra(L, torch, args):
     P = torch.empty(t, M, h, dtype=torch.float32, device="cuda")
     nws = L.tp_row_parallel_overlap_workspace_size(M, F, h, t)
     ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    nsk = L.tp_row_parallel_workspace_size(M, F, h, t)
+    skws = torch.empty(nsk, dtype=torch.uint8, device="cuda")
     fused = lambda: L.tp_row_parallel_forward(A, M, F, h, t, Wdn, inp["b_down"], None, Y)
+    fused_sk = lambda: L.tp_row_parallel_forward_ws(A, M, F, h, t, Wdn, inp["b_down"], None, Y, skws, nsk)
 
     def unfused():
         # the same GEMM writing partials, then the separate fixed-order reduction
@@ -561,6 +567,7 @@ def run_overlap_extra(L, torch, args):
     ovl = lambda: L.tp_row_parallel_forward_overlap(A, M, F, h, t, Wdn, inp["b_down"], None, Y, None, ws, nws)
     iters = max(10, min(args.steps, 30))
     f_ms = _time(torch, fused, iters)
+    fsk_ms = _time(torch, fused_sk, iters)
     o_ms = _time(torch, ovl, iters)
     # whole MLP forward in the three modes: the difference to the column-parallel half is the row part
     Wup = torch.empty(t, F // t, h, dtype=torch.bfloat16, device="cuda")
@@ -584,6 +591,7 @@ def run_overlap_extra(L, torch, args):
     flops = 2.0 * M * h * F
     return {"workload": "row-parallel GEMM + g, t=4, A 4x2048x4096, W_down 16384x4096 (TP-MLP)",
             "fused_ms": round(f_ms, 4), "fused_TFLOPs": round(flops / f_ms / 1e9, 1),
+            "fused_streamk_ms": round(fsk_ms, 4), "fused_streamk_TFLOPs": round(flops / fsk_ms / 1e9, 1),
             "overlap_ms": round(o_ms, 4), "overlap_TFLOPs": round(flops / o_ms / 1e9, 1),
             "separate_reduce_kernel_ms": round(r_ms, 4),
             "row_part_in_mlp_forward_ms": {k: round(v, 4) for k, v in mode_ms.items()},
@@ -643,11 +651,12 @@ def run_swiglu_extra(L, torch, args):
     nws_f = L.tp_mlp_workspace_size(M, h, F, t, 0)
     nws_b = L.tp_mlp_backward_workspace_size(M, h, F, t, 0)
     wsb = torch.empty(nws_b, dtype=torch.uint8, device="cuda")
+    wsf = torch.empty(nws_f, dtype=torch.uint8, device="cuda")
     act = L.ACT_BY_NAME["swiglu"]
     dX = torch.empty(M, h, dtype=torch.bfloat16, device="cuda")
 
     def step():
-        L.tp_mlp_forward(X, M, h, F, t, act, w.Wup_p, None, w.Wdown_p, None, None, Y, Z, A, 0, None, nws_f)
+        L.tp_mlp_forward(X, M, h, F, t, act, w.Wup_p, None, w.Wdown_p, None, None, Y, Z, A, 0, wsf, nws_f)
         L.tp_mlp_backward(dY, X, Z, A, M, h, F, t, act, w.Wup_p, w.Wdown_p, dX, grads["dWup_p"], grads["dWdown_p"],
                           None, grads["dbdown"], 0, 0, wsb, nws_b)
     ms = _time(torch, step, max(5, min(args.steps, 10)))
@@ -680,8 +689,10 @@ def run_attn_extra(L, torch, args, name="c5"):
     O = torch.empty(t, N, d // t, dtype=bf16, device="cuda")
     lse = torch.empty(t, nh // t, N, dtype=f32, device="cuda")
     sc = 1.0 / math.sqrt(dh)
+    naw = L.tp_attn_forward_workspace_size(N, d, nh, dh, t, 0)
+    aws = torch.empty(naw, dtype=torch.uint8, device="cuda")
     fwd = lambda: L.tp_attn_forward(inp["X"], N, d, nh, dh, t, 1, sc, Wqkv, bqkv, Wo, inp["b_o"], None, Y, QKV, O,
-                                    lse, 0, None, 0)
+                                    lse, 0, aws, naw)
     f_ms = _time(torch, fwd, max(5, min(args.steps, 20)))
     dX = torch.empty(N, d, dtype=bf16, device="cuda")
     gq = torch.empty(t, 3 * d // t, d, dtype=f32, device="cuda")

@@ -85,6 +85,15 @@ typedef enum {
                                      row-parallel GEMM (tp_row_parallel_forward_overlap);
                                      M > 128, t in {1,2,4,8}; takes precedence over UNFUSED */
 
+/* Flag of the attention entry points (tp_attn_forward / backward and their grouped-query
+ * forms): the attention input X and the packed W_qkv hold IEEE fp16 bits instead of bf16
+ * (tp_sp_layernorm_forward_f16 and tp_convert_bf16_to_f16 produce them), and the backward
+ * keeps dQKV in fp16 too.  A wide model's attention logits spread over several units (about
+ * 5 at d = 12288 with N(0, 0.02) weights), so the 2^-9 rounding of a bf16 X becomes a
+ * logit error of a few hundredths and a relative error of the softmax of a few percent;
+ * fp16 keeps 3 more mantissa bits at the same cost. */
+#define TP_ATTN_F16_INPUT 1u
+
 typedef uint16_t tp_bf16;
 typedef struct CUstream_st* tp_stream; /* identical to cudaStream_t */
 
@@ -186,6 +195,26 @@ tp_status tp_row_parallel_forward(const tp_bf16* A, int64_t M, int64_t K, int64_
  * in range order before the epilogue.  No workspace is needed and the result does not
  * depend on timing; only the rounding of the fp32 sum differs from the unsplit GEMM. */
 
+/* The same two calls with a workspace (tp_*_workspace_size() bytes, 256-byte aligned; a
+ * smaller one is used as far as it goes, NULL runs the calls above).  It lets a GEMM of
+ * more than 128 rows with fewer 256 x 256 output tiles than the GPU has CTA pairs use a
+ * stream-K schedule: the tiles' k-stages (a row-parallel GEMM's t shard ranges laid end to
+ * end) are cut into one contiguous range per CTA pair, so that every pair works.  A range that does not start at k = 0
+ * leaves its fp32 partial in ws; the range that starts at k = 0 adds the partials of the
+ * ranges after it in k order, then applies the epilogue.  The sums are deterministic for a
+ * given device (the ranges depend on its SM count); only the rounding of the fp32 sum
+ * differs from the data-parallel schedule.  The MLP and attention calls take the same
+ * room at the end of their workspaces.  Workspaces must not be shared by calls that may
+ * run at the same time. */
+size_t tp_column_parallel_workspace_size(int64_t M, int64_t h, int64_t N, int t);
+tp_status tp_column_parallel_forward_ws(const tp_bf16* X, int64_t M, int64_t h, int64_t N, int t, tp_act act,
+                                        const tp_bf16* W_p, const tp_bf16* b, tp_bf16* Z, tp_bf16* A, void* ws,
+                                        size_t ws_bytes, tp_stream stream);
+size_t tp_row_parallel_workspace_size(int64_t M, int64_t K, int64_t h, int t);
+tp_status tp_row_parallel_forward_ws(const tp_bf16* A, int64_t M, int64_t K, int64_t h, int t, const tp_bf16* W_p,
+                                     const tp_bf16* b, const tp_bf16* residual, tp_bf16* Y, void* ws,
+                                     size_t ws_bytes, tp_stream stream);
+
 /* Row-parallel GEMM with the g all-reduce overlapped, tile by tile ("Tensor
  * and sequence parallelism", section "Volume and scale": the matrix multiply is
  * cut into blocks and each block is communicated while the next computes --
@@ -230,7 +259,9 @@ tp_status tp_row_parallel_forward_overlap(const tp_bf16* A, int64_t M, int64_t K
  *   Z_save [t][M][2F/t] (required); A_i = silu(gate) * up [t][M][F/t], formed in the
  *   GEMM's epilogue from the fp32 accumulators.  bup must be NULL (TP_ERR_UNSUPPORTED
  *   otherwise); (F/t) % 128 == 0 (TP_ERR_SHAPE).
- * ws: tp_mlp_workspace_size() bytes (0, and ws may be NULL, without the two flags above). */
+ * ws: tp_mlp_workspace_size() bytes: the two flags' partials (required with them; NULL,
+ * 0 otherwise), then room for the GEMMs' stream-K partials (see
+ * tp_row_parallel_forward_ws), used when present. */
 size_t tp_mlp_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned flags);
 tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int t, tp_act act,
                          const tp_bf16* Wup_p, const tp_bf16* bup, const tp_bf16* Wdown_p, const tp_bf16* bdown,
@@ -248,7 +279,8 @@ tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int 
  * (nullable).  SWIGLU: dA_i = dY W_down,i^T stays in the GEMM's fp32 accumulators; its
  * epilogue writes d gate = dA u silu'(gate) and d up = dA silu(gate), interleaved like
  * Z_save; dWup_p is [t][2F/t][h] in tp_pack_swiglu's layout; dbup must be NULL.  ws (the
- * size query covers every activation) holds dZ and column-sum scratch. */
+ * size query covers every activation) holds dZ and column-sum scratch -- the required
+ * part -- then room for the GEMMs' stream-K partials, used when present. */
 size_t tp_mlp_backward_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned flags);
 tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_save, const tp_bf16* A_save,
                           int64_t M, int64_t h, int64_t F, int t, tp_act act, const tp_bf16* Wup_p,
@@ -316,10 +348,13 @@ tp_status tp_decode_attn_forward(const tp_bf16* x, int64_t B, int64_t d, int n_h
  * softmax of wide models within tolerance); O_save
  * [t][N][d/t] bf16; lse_save [t][H/t][N] fp32 (natural-log log-sum-exp of
  * each scaled score row).  head_dim == 128.
- * flags must be 0 (TP_ERR_UNSUPPORTED otherwise); ws / ws_bytes are unused
- * (pass NULL, 0).  The attention kernel runs one CTA per (head, pair of
- * 128-query tiles) with an online softmax; no N x N score matrix is ever
- * stored. */
+ * flags: 0 or TP_ATTN_F16_INPUT (X and Wqkv_p in IEEE fp16; other bits: TP_ERR_UNSUPPORTED).
+ * ws is optional: NULL, 0 runs
+ * the GEMMs' data-parallel schedule; tp_attn_forward_workspace_size() bytes (256-byte
+ * aligned) let them use stream-K (see tp_row_parallel_forward_ws).  The attention
+ * kernel runs one CTA per (head, pair of 128-query tiles) with an online softmax; no
+ * N x N score matrix is ever stored. */
+size_t tp_attn_forward_workspace_size(int64_t N, int64_t d, int n_heads, int head_dim, int t, unsigned flags);
 tp_status tp_attn_forward(const tp_bf16* X, int64_t N, int64_t d, int n_heads, int head_dim, int t, int causal,
                           float scale, const tp_bf16* Wqkv_p, const tp_bf16* bqkv_p, const tp_bf16* Wo_p,
                           const tp_bf16* bo, const tp_bf16* residual, tp_bf16* Y, tp_bf16* QKV_save,
@@ -345,9 +380,12 @@ tp_status tp_attn_gqa_forward(const tp_bf16* X, int64_t N, int64_t d, int n_head
  * f backward: dX = sum_i dQKV_i W_qkv,i^T (fused).  dWqkv_p [t][3d/t][d],
  * dbqkv_p [t][3d/t], dWo_p [t][d][d/t], dbo [d]: fp32 (overwritten, or added to when
  * accumulate != 0; dbqkv_p / dbo nullable).  Inputs are the forward's saved
- * QKV_save, O_save, lse_save.  flags must be 0.  ws (see the size query) holds,
+ * QKV_save, O_save, lse_save.  flags: 0, or TP_ATTN_F16_INPUT when the forward had it (X and
+ * Wqkv_p fp16; dQKV in ws is then fp16).  ws (see the size query) holds,
  * in order, each 256-byte aligned: dO [t][N][d/t] fp16, D = rowsum(dO * O)
- * [t][H/t][N] fp32, dQKV [t][N][3d/t] bf16, column-sum scratch.  The
+ * [t][H/t][N] fp32, dQKV [t][N][3d/t] bf16, column-sum scratch -- the required part
+ * (TP_ERR_WORKSPACE below it) -- then room for the GEMMs' stream-K partials, used
+ * when present.  The
  * attention gradient runs as two deterministic kernels (dK/dV per key block,
  * dQ per query block); scores are recomputed from the saved log-sum-exp. */
 size_t tp_attn_backward_workspace_size(int64_t N, int64_t d, int n_heads, int head_dim, int t, unsigned flags);
@@ -442,6 +480,18 @@ tp_status tp_sp_layernorm_forward(const tp_bf16* X_sh, int64_t s, int64_t h, int
  * dgamma_part[j] = sum over shard j's rows of dy*xhat, dbeta_part[j] = sum dy
  * ([t][h] fp32); then the LayerNorm weight-gradient all-reduce:
  * dgamma = sum_{j=0..t-1} dgamma_part[j] (fixed order), same for dbeta. */
+/* tp_sp_layernorm_forward with Y_sh written as IEEE fp16 bits (the attention block's input
+ * under TP_ATTN_F16_INPUT); same arguments and statistics. */
+tp_status tp_sp_layernorm_forward_f16(const tp_bf16* X_sh, int64_t s, int64_t h, int t, const tp_bf16* gamma,
+                                      const tp_bf16* beta, float eps, uint16_t* Y_sh, float* mean, float* rstd,
+                                      tp_stream stream);
+
+/* dst[i] = fp16(src[i]) for n bf16 values, round to nearest even: exact for bf16 values in
+ * fp16's normal range (2^-14 .. 65504); smaller ones become fp16 subnormals (zero below
+ * 2^-25), larger ones infinity.  For weights packed once (e.g. W_qkv under
+ * TP_ATTN_F16_INPUT).  src, dst 16-byte aligned, not overlapping. */
+tp_status tp_convert_bf16_to_f16(const tp_bf16* src, int64_t n, uint16_t* dst, tp_stream stream);
+
 tp_status tp_sp_layernorm_backward(const tp_bf16* dY_sh, const tp_bf16* X_sh, const tp_bf16* gamma,
                                    const float* mean, const float* rstd, const tp_bf16* dres, int64_t s, int64_t h,
                                    int t, tp_bf16* dX_sh, float* dgamma_part, float* dbeta_part, float* dgamma,

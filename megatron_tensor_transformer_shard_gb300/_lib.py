@@ -24,6 +24,7 @@ ACT_BY_NAME = {"identity": TP_ACT_IDENTITY, "relu": TP_ACT_RELU, "gelu_tanh": TP
                "gelu_erf": TP_ACT_GELU_ERF, "swiglu": TP_ACT_SWIGLU}
 TP_FLAG_UNFUSED_REDUCE = 1
 TP_FLAG_OVERLAP_REDUCE = 2
+TP_ATTN_F16_INPUT = 1
 
 _P, _I64, _I, _U, _SZ, _F = C.c_void_p, C.c_int64, C.c_int, C.c_uint, C.c_size_t, C.c_float
 
@@ -53,6 +54,11 @@ SIGNATURES = {
     "tp_last_error_detail": (C.c_char_p, []),
     "tp_column_parallel_forward": (_I, [_P, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P, _P]),
     "tp_row_parallel_forward": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _P, _P]),
+    "tp_column_parallel_workspace_size": (_SZ, [_I64, _I64, _I64, _I]),
+    "tp_column_parallel_forward_ws": (_I, [_P, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "tp_row_parallel_workspace_size": (_SZ, [_I64, _I64, _I64, _I]),
+    "tp_row_parallel_forward_ws": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "tp_attn_forward_workspace_size": (_SZ, [_I64, _I64, _I, _I, _I, _U]),
     "tp_row_parallel_overlap_workspace_size": (_SZ, [_I64, _I64, _I64, _I]),
     "tp_row_parallel_forward_overlap": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "tp_decode_swiglu_forward": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _P, _P]),
@@ -64,6 +70,8 @@ SIGNATURES = {
     "tp_vocab_embedding_backward": (_I, [_P, _P, _I64, _I64, _I64, _I, _P, _I, _P, _SZ, _P]),
     "tp_sp_layernorm_forward": (_I, [_P, _I64, _I64, _I, _P, _P, _F, _P, _P, _P, _P]),
     "tp_sp_layernorm_backward": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I, _P, _P, _P, _P, _P, _P]),
+    "tp_sp_layernorm_forward_f16": (_I, [_P, _I64, _I64, _I, _P, _P, _F, _P, _P, _P, _P]),
+    "tp_convert_bf16_to_f16": (_I, [_P, _I64, _P, _P]),
     "tp_attn_forward": (_I, [_P, _I64, _I64, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _U, _P, _SZ,
                              _P]),
     "tp_attn_gqa_forward": (_I, [_P, _I64, _I64, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _U,

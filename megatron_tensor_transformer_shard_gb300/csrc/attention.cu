@@ -8,7 +8,8 @@
 // Q, K, V, P (and in backward dO, dS) are IEEE fp16: the logits of a wide
 // model have a spread of several units, and a 2^-9 relative rounding of Q
 // and K (bf16) turns into a ~1% error of P; fp16 keeps 3 more mantissa bits
-// at the same cost.  Inputs, weights and O / dQKV stay bf16.
+// at the same cost.  O stays bf16; dQKV is bf16, or fp16 for callers whose attention
+// input and W_qkv are fp16 (the QKV GEMM's operands set the precision of Q and K).
 //
 // Forward: one CTA per (head, pair of adjacent 128-query tiles), heavy (late)
 // pairs first.  The two tiles take turns on the tensor pipe, so one tile's
@@ -396,6 +397,7 @@ struct AttnBwdArgs {
   const float* lse;   // [t][hpr][N] natural log
   const float* Dvec;  // [t][hpr][N]
   uint16_t* dQKV;     // [t][N][row_w]
+  int dqkv_f16;       // dQKV as IEEE fp16 (else bf16)
   int* err;
   uint64_t timeout_ns;
 };
@@ -427,8 +429,9 @@ __device__ __forceinline__ void tma_tile64(uint8_t* dst, const CUtensorMap* map,
   ptx::tma_load_3d(dst + PANEL64, map, bar, col + 64, row, shard);
 }
 
-// 64 accumulator columns of this thread's TMEM lane, times `mul`, as bf16 at dst.
-__device__ __forceinline__ void tmem_cols64_to_bf16(uint32_t taddr, float mul, uint16_t* dst, bool write) {
+// 64 accumulator columns of this thread's TMEM lane, times `mul`, as bf16 (or IEEE fp16 when
+// f16) at dst.
+__device__ __forceinline__ void tmem_cols64_to_16(uint32_t taddr, float mul, uint16_t* dst, bool write, bool f16) {
   uint32_t r[2][32];
   ptx::tmem_ld32(taddr, r[0]);
   ptx::tmem_ld32(taddr + 32, r[1]);
@@ -438,11 +441,16 @@ __device__ __forceinline__ void tmem_cols64_to_bf16(uint32_t taddr, float mul, u
   for (int c = 0; c < 2; ++c)
 #pragma unroll
     for (int e = 0; e < 32; e += 8) {
+      float f[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) f[k] = __uint_as_float(r[c][e + k]) * mul;
       uint4 v;
-      v.x = pack_bf16x2(__uint_as_float(r[c][e + 0]) * mul, __uint_as_float(r[c][e + 1]) * mul);
-      v.y = pack_bf16x2(__uint_as_float(r[c][e + 2]) * mul, __uint_as_float(r[c][e + 3]) * mul);
-      v.z = pack_bf16x2(__uint_as_float(r[c][e + 4]) * mul, __uint_as_float(r[c][e + 5]) * mul);
-      v.w = pack_bf16x2(__uint_as_float(r[c][e + 6]) * mul, __uint_as_float(r[c][e + 7]) * mul);
+      if (f16) {
+        v = make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]), pack_f16x2(f[6], f[7]));
+      } else {
+        v = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                       pack_bf16x2(f[6], f[7]));
+      }
       *reinterpret_cast<uint4*>(dst + c * 32 + e) = v;
     }
 }
@@ -696,8 +704,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     if (ok && ptx::mbar_wait(acc_done, 0, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
       ptx::tc_fence_after();
       uint16_t* drow = p.dQKV + (static_cast<int64_t>(shard) * p.N + kv) * p.row_w;
-      tmem_cols64_to_bf16(tdV + lane_base + 64 * h, 1.0f, drow + vcol + 64 * h, kv < p.N);
-      tmem_cols64_to_bf16(tdK + lane_base + 64 * h, p.scale, drow + kcol + 64 * h, kv < p.N);
+      tmem_cols64_to_16(tdV + lane_base + 64 * h, 1.0f, drow + vcol + 64 * h, kv < p.N, p.dqkv_f16 != 0);
+      tmem_cols64_to_16(tdK + lane_base + 64 * h, p.scale, drow + kcol + 64 * h, kv < p.N, p.dqkv_f16 != 0);
     }
   }
 
@@ -880,7 +888,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     if (ok && ptx::mbar_wait(acc_done, 0, abort_flag, p.err, ERR_ATT_SOFTMAX, p.timeout_ns)) {
       ptx::tc_fence_after();
       uint16_t* drow = p.dQKV + (static_cast<int64_t>(shard) * p.N + q) * p.row_w;
-      tmem_cols64_to_bf16(tdQ + lane_base + 64 * h, p.scale, drow + qcol + 64 * h, q < p.N);
+      tmem_cols64_to_16(tdQ + lane_base + 64 * h, p.scale, drow + qcol + 64 * h, q < p.N, p.dqkv_f16 != 0);
     }
   }
 
@@ -975,7 +983,7 @@ namespace tp {
 
 tp_status run_attention_bwd(const uint16_t* QKV, const uint16_t* O, const uint16_t* dO, const float* lse, int64_t N,
                             int64_t d, int n_heads, int n_kv, int head_dim, int t, int causal, float scale, float* Dvec,
-                            uint16_t* dQKV, cudaStream_t s) {
+                            uint16_t* dQKV, cudaStream_t s, int dqkv_f16) {
   if (N < 0 || d < 1 || n_heads < 1 || n_kv < 1 || t < 1) return TP_ERR_INVALID_ARG;
   AttnShape sh;
   if (!attn_shape(d, n_heads, n_kv, head_dim, t, sh)) return TP_ERR_SHAPE;
@@ -1011,6 +1019,7 @@ tp_status run_attention_bwd(const uint16_t* QKV, const uint16_t* O, const uint16
   a.lse = lse;
   a.Dvec = Dvec;
   a.dQKV = dQKV;
+  a.dqkv_f16 = dqkv_f16;
   a.err = device_error_word();
   a.timeout_ns = wait_timeout_ns();
   static bool configured[64] = {};

@@ -198,7 +198,7 @@ size_t row_partials_ws(int64_t M, int64_t h, int t, bool overlap) {
 }
 
 tp_status column_parallel(const tp_bf16* X, int64_t M, int64_t h, int64_t N, int t, tp_act act, const tp_bf16* W_p,
-                          const tp_bf16* b, tp_bf16* Z, tp_bf16* A, cudaStream_t s) {
+                          const tp_bf16* b, tp_bf16* Z, tp_bf16* A, void* sk_ws, size_t sk_bytes, cudaStream_t s) {
   if (M < 0 || h < 1 || N < 1 || t < 1 || !act_ok(act)) return TP_ERR_INVALID_ARG;
   if (N % t != 0) return TP_ERR_SHAPE;
   const int64_t Nt = N / t;
@@ -212,11 +212,13 @@ tp_status column_parallel(const tp_bf16* X, int64_t M, int64_t h, int64_t N, int
   c.epi = EPI_ACT; c.act = act;
   c.d = Z; c.d2 = A; c.ldd = Nt; c.d_batch_stride = M * Nt;
   c.bias = b; c.bias_batch_stride = Nt;
+  c.sk_ws = sk_ws; c.sk_ws_bytes = sk_bytes;
   return run_gemm(c, s);
 }
 
 tp_status row_parallel(const tp_bf16* A, int64_t M, int64_t K, int64_t h, int t, const tp_bf16* W_p,
-                       const tp_bf16* b, const tp_bf16* residual, tp_bf16* Y, cudaStream_t s) {
+                       const tp_bf16* b, const tp_bf16* residual, tp_bf16* Y, void* sk_ws, size_t sk_bytes,
+                       cudaStream_t s) {
   if (M < 0 || h < 1 || K < 1 || t < 1) return TP_ERR_INVALID_ARG;
   if (K % t != 0) return TP_ERR_SHAPE;
   const int64_t Kt = K / t;
@@ -228,13 +230,27 @@ tp_status row_parallel(const tp_bf16* A, int64_t M, int64_t K, int64_t h, int t,
   r.a.ptr = A; r.a.ld = Kt; r.a.sharded = true; r.a.shard_stride = M * Kt;
   r.b.ptr = W_p; r.b.ld = Kt; r.b.sharded = true; r.b.shard_stride = h * Kt;
   r.epi = EPI_BF16; r.d = Y; r.ldd = h; r.bias = b; r.residual = residual; r.ld_res = h;
+  r.sk_ws = sk_ws; r.sk_ws_bytes = sk_bytes;
   return run_gemm(r, s);
 }
 
-// The forward's scratch: the partials of the unfused / overlapped reduction.
+// The forward's required scratch: the partials of the unfused / overlapped reduction.  A
+// workspace that also holds gemm_sk_ws_bytes() after it lets the GEMMs use stream-K.
 size_t mlp_fwd_base_ws(int64_t M, int64_t h, int t, unsigned flags) {
   if (flags & TP_FLAG_OVERLAP_REDUCE) return row_partials_ws(M, h, t, true);
   return (flags & TP_FLAG_UNFUSED_REDUCE) ? round_up(static_cast<size_t>(t) * M * h * sizeof(float), 256) : 0;
+}
+
+// The part of a caller's workspace past `base` bytes, 256-byte aligned, for stream-K (NULL
+// when there is none).
+void* sk_part_of(void* ws, size_t ws_bytes, size_t base, size_t* sk_bytes) {
+  *sk_bytes = 0;
+  if (!ws || ws_bytes <= base) return nullptr;
+  uint8_t* p = static_cast<uint8_t*>(ws) + base;
+  const size_t skew = (256 - (reinterpret_cast<uintptr_t>(p) & 255u)) & 255u;
+  if (ws_bytes - base <= skew) return nullptr;
+  *sk_bytes = ws_bytes - base - skew;
+  return p + skew;
 }
 
 }  // namespace
@@ -245,14 +261,16 @@ size_t tp_attn_gqa_backward_workspace_size(int64_t N, int64_t d, int n_heads, in
                                            unsigned flags) {
   (void)flags;
   if (N < 0 || d < 1 || n_heads < 1 || t < 1 || !gqa_ok(d, n_heads, n_kv_heads, head_dim, t)) return 0;
-  return attn_bwd_layout(nullptr, N, d, n_heads, qkv_row_width(n_heads, n_kv_heads, head_dim, t), t).total;
+  // the required part, then room for the GEMMs' stream-K partials
+  return attn_bwd_layout(nullptr, N, d, n_heads, qkv_row_width(n_heads, n_kv_heads, head_dim, t), t).total +
+         gemm_sk_ws_bytes();
 }
 
 size_t tp_attn_backward_workspace_size(int64_t N, int64_t d, int n_heads, int head_dim, int t, unsigned flags) {
   (void)head_dim;
   (void)flags;
   if (N < 0 || d < 1 || n_heads < 1 || t < 1) return 0;
-  return attn_bwd_layout(nullptr, N, d, n_heads, 3 * d / t, t).total;
+  return attn_bwd_layout(nullptr, N, d, n_heads, 3 * d / t, t).total + gemm_sk_ws_bytes();
 }
 
 tp_status tp_attn_gqa_backward(const tp_bf16* dY, const tp_bf16* X, const uint16_t* QKV_save, const tp_bf16* O_save,
@@ -262,7 +280,8 @@ tp_status tp_attn_gqa_backward(const tp_bf16* dY, const tp_bf16* X, const uint16
                                float* dbo, int accumulate, unsigned flags, void* ws, size_t ws_bytes,
                                tp_stream stream) {
   if (N < 0 || d < 1 || n_heads < 1 || n_kv_heads < 1 || t < 1 || head_dim < 1) return TP_ERR_INVALID_ARG;
-  if (flags != 0) return TP_ERR_UNSUPPORTED;
+  if ((flags & ~TP_ATTN_F16_INPUT) != 0) return TP_ERR_UNSUPPORTED;
+  const int f16in = (flags & TP_ATTN_F16_INPUT) ? 1 : 0;  // X, W_qkv and so dQKV in IEEE fp16
   if (!gqa_ok(d, n_heads, n_kv_heads, head_dim, t)) return TP_ERR_SHAPE;
   if (!dWqkv_p || !dWo_p) return TP_ERR_INVALID_ARG;
   if (N > 0 && (!dY || !X || !QKV_save || !O_save || !lse_save || !Wqkv_p || !Wo_p || !dX)) return TP_ERR_INVALID_ARG;
@@ -270,6 +289,8 @@ tp_status tp_attn_gqa_backward(const tp_bf16* dY, const tp_bf16* X, const uint16
   const AttnBwdWs w = attn_bwd_layout(ws, N, d, n_heads, rw, t);
   if (!ws || ws_bytes < w.total) return TP_ERR_WORKSPACE;
   if (!aligned16(ws)) return TP_ERR_ALIGN;
+  size_t sk_bytes = 0;
+  void* sk_ws = sk_part_of(ws, ws_bytes, w.total, &sk_bytes);  // stream-K, when the workspace has room
   const cudaStream_t s = S(stream);
   const int64_t dt = d / t;
   if (N == 0) {
@@ -289,6 +310,7 @@ tp_status tp_attn_gqa_backward(const tp_bf16* dY, const tp_bf16* X, const uint16
   g.b.ptr = Wo_p; g.b.ld = dt; g.b.sharded = true; g.b.shard_stride = d * dt; g.b.mn_major = true;
   g.epi = EPI_ACT; g.act = TP_ACT_IDENTITY; g.out_f16 = 1;  // dO feeds the fp16 attention kernels
   g.d = nullptr; g.d2 = w.dO; g.ldd = dt; g.d_batch_stride = N * dt;
+  g.sk_ws = sk_ws; g.sk_ws_bytes = sk_bytes;
   TP_RETURN_IF(run_gemm(g, s));
   // dW_o,i = O_i^T dY  -> packed [t][d][dt] (local).
   GemmProblem wo;
@@ -296,10 +318,11 @@ tp_status tp_attn_gqa_backward(const tp_bf16* dY, const tp_bf16* X, const uint16
   wo.a.ptr = dY; wo.a.ld = d; wo.a.mn_major = true;
   wo.b.ptr = O_save; wo.b.ld = dt; wo.b.sharded = true; wo.b.shard_stride = N * dt; wo.b.mn_major = true;
   wo.epi = EPI_F32; wo.d = dWo_p; wo.ldd = dt; wo.d_batch_stride = d * dt; wo.accumulate = accumulate;
+  wo.sk_ws = sk_ws; wo.sk_ws_bytes = sk_bytes;
   TP_RETURN_IF(run_gemm(wo, s));
   // Head-local softmax-attention backward -> dQKV_i.
   TP_RETURN_IF(run_attention_bwd(QKV_save, O_save, w.dO, lse_save, N, d, n_heads, n_kv_heads, head_dim, t, causal,
-                                 scale, w.Dvec, w.dQKV, s));
+                                 scale, w.Dvec, w.dQKV, s, f16in));
   // Bias gradients in one fused pass: db_o once (g backward is the identity), db_qkv per shard.
   if (dbo || dbqkv_p) {
     ColsumJob jo, jq;
@@ -309,7 +332,7 @@ tp_status tp_attn_gqa_backward(const tp_bf16* dY, const tp_bf16* X, const uint16
     }
     if (dbqkv_p) {
       jq.G = w.dQKV; jq.rows = N; jq.cols = rw; jq.ld = rw; jq.bs = N * rw; jq.nbatch = t;
-      jq.out = dbqkv_p; jq.ws = w.cs + colsum2_ws_floats(N, d, 1); jq.accumulate = accumulate;
+      jq.out = dbqkv_p; jq.ws = w.cs + colsum2_ws_floats(N, d, 1); jq.accumulate = accumulate; jq.f16 = f16in;
     }
     TP_RETURN_IF(run_colsum2(jo, jq, s));
   }
@@ -319,6 +342,8 @@ tp_status tp_attn_gqa_backward(const tp_bf16* dY, const tp_bf16* X, const uint16
   wq.a.ptr = w.dQKV; wq.a.ld = rw; wq.a.sharded = true; wq.a.shard_stride = N * rw; wq.a.mn_major = true;
   wq.b.ptr = X; wq.b.ld = d; wq.b.mn_major = true;
   wq.epi = EPI_F32; wq.d = dWqkv_p; wq.ldd = d; wq.d_batch_stride = rw * d; wq.accumulate = accumulate;
+  wq.f16_ab = f16in;
+  wq.sk_ws = sk_ws; wq.sk_ws_bytes = sk_bytes;
   TP_RETURN_IF(run_gemm(wq, s));
   // f backward: dX = sum_i dQKV_i W_qkv,i (fixed shard order, fused).
   GemmProblem dx;
@@ -326,6 +351,8 @@ tp_status tp_attn_gqa_backward(const tp_bf16* dY, const tp_bf16* X, const uint16
   dx.a.ptr = w.dQKV; dx.a.ld = rw; dx.a.sharded = true; dx.a.shard_stride = N * rw;
   dx.b.ptr = Wqkv_p; dx.b.ld = d; dx.b.sharded = true; dx.b.shard_stride = rw * d; dx.b.mn_major = true;
   dx.epi = EPI_BF16; dx.d = dX; dx.ldd = d;
+  dx.f16_ab = f16in;
+  dx.sk_ws = sk_ws; dx.sk_ws_bytes = sk_bytes;
   return run_gemm(dx, s);
 }
 
@@ -335,7 +362,7 @@ tp_status tp_attn_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Q
                            float* dWqkv_p, float* dbqkv_p, float* dWo_p, float* dbo, int accumulate,
                            unsigned flags, void* ws, size_t ws_bytes, tp_stream stream) {
   if (N < 0 || d < 1 || n_heads < 1 || t < 1 || head_dim < 1) return TP_ERR_INVALID_ARG;
-  if (flags != 0) return TP_ERR_UNSUPPORTED;
+  if ((flags & ~TP_ATTN_F16_INPUT) != 0) return TP_ERR_UNSUPPORTED;
   if (head_dim != 128 || static_cast<int64_t>(n_heads) * head_dim != d || n_heads % t != 0) return TP_ERR_SHAPE;
   return tp_attn_gqa_backward(dY, X, QKV_save, O_save, lse_save, N, d, n_heads, n_heads, head_dim, t, causal, scale,
                               Wqkv_p, Wo_p, dX, dWqkv_p, dbqkv_p, dWo_p, dbo, accumulate, flags, ws, ws_bytes, stream);
@@ -428,7 +455,7 @@ tp_status tp_pack_qkv_gqa_bias(const tp_bf16* b, int n_heads, int n_kv_heads, in
 
 size_t tp_mlp_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned flags) {
   if (M < 0 || h < 0 || F < 0 || t < 1) return 0;
-  return mlp_fwd_base_ws(M, h, t, flags);
+  return mlp_fwd_base_ws(M, h, t, flags) + gemm_sk_ws_bytes();
 }
 
 size_t tp_row_parallel_overlap_workspace_size(int64_t M, int64_t K, int64_t h, int t) {
@@ -468,12 +495,38 @@ tp_status tp_row_parallel_forward_overlap(const tp_bf16* A, int64_t M, int64_t K
 tp_status tp_column_parallel_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t N, int t, tp_act act,
                                      const tp_bf16* W_p, const tp_bf16* b, tp_bf16* Z, tp_bf16* A,
                                      tp_stream stream) {
-  return column_parallel(X, M, h, N, t, act, W_p, b, Z, A, S(stream));
+  return column_parallel(X, M, h, N, t, act, W_p, b, Z, A, nullptr, 0, S(stream));
 }
 
 tp_status tp_row_parallel_forward(const tp_bf16* A, int64_t M, int64_t K, int64_t h, int t, const tp_bf16* W_p,
                                   const tp_bf16* b, const tp_bf16* residual, tp_bf16* Y, tp_stream stream) {
-  return row_parallel(A, M, K, h, t, W_p, b, residual, Y, S(stream));
+  return row_parallel(A, M, K, h, t, W_p, b, residual, Y, nullptr, 0, S(stream));
+}
+
+size_t tp_column_parallel_workspace_size(int64_t M, int64_t h, int64_t N, int t) {
+  (void)M; (void)h; (void)N; (void)t;
+  return gemm_sk_ws_bytes();
+}
+
+tp_status tp_column_parallel_forward_ws(const tp_bf16* X, int64_t M, int64_t h, int64_t N, int t, tp_act act,
+                                        const tp_bf16* W_p, const tp_bf16* b, tp_bf16* Z, tp_bf16* A, void* ws,
+                                        size_t ws_bytes, tp_stream stream) {
+  size_t sk = 0;
+  void* skp = sk_part_of(ws, ws_bytes, 0, &sk);
+  return column_parallel(X, M, h, N, t, act, W_p, b, Z, A, skp, sk, S(stream));
+}
+
+size_t tp_row_parallel_workspace_size(int64_t M, int64_t K, int64_t h, int t) {
+  (void)M; (void)K; (void)h; (void)t;
+  return gemm_sk_ws_bytes();
+}
+
+tp_status tp_row_parallel_forward_ws(const tp_bf16* A, int64_t M, int64_t K, int64_t h, int t, const tp_bf16* W_p,
+                                     const tp_bf16* b, const tp_bf16* residual, tp_bf16* Y, void* ws,
+                                     size_t ws_bytes, tp_stream stream) {
+  size_t sk = 0;
+  void* skp = sk_part_of(ws, ws_bytes, 0, &sk);
+  return row_parallel(A, M, K, h, t, W_p, b, residual, Y, skp, sk, S(stream));
 }
 
 tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int t, tp_act act,
@@ -491,7 +544,10 @@ tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int 
   if (!X || !Wup_p || !Wdown_p || !Y || !A_save || (swiglu && !Z_save)) return TP_ERR_INVALID_ARG;
   const bool overlap = (flags & TP_FLAG_OVERLAP_REDUCE) != 0;
   const bool unfused = !overlap && (flags & TP_FLAG_UNFUSED_REDUCE) != 0;
-  if (ws_bytes < tp_mlp_workspace_size(M, h, F, t, flags) || ((unfused || overlap) && !ws)) return TP_ERR_WORKSPACE;
+  const size_t base_ws = mlp_fwd_base_ws(M, h, t, flags);
+  if (ws_bytes < base_ws || ((unfused || overlap) && !ws)) return TP_ERR_WORKSPACE;
+  size_t sk_bytes = 0;
+  void* sk_ws = sk_part_of(ws, ws_bytes, base_ws, &sk_bytes);  // stream-K, when the workspace has room
   if (overlap && (M <= 128 || t > 8 || (t & (t - 1)) != 0)) return TP_ERR_UNSUPPORTED;
   const cudaStream_t s = S(stream);
 
@@ -508,20 +564,21 @@ tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int 
     TP_RETURN_IF(run_gemm(c, s));
   } else {
     // f (identity) + column-parallel: Z_i = X W_up,i + b_up[C_i]; A_i = act(Z_i).
-    TP_RETURN_IF(column_parallel(X, M, h, F, t, act, Wup_p, bup, Z_save, A_save, s));
+    TP_RETURN_IF(column_parallel(X, M, h, F, t, act, Wup_p, bup, Z_save, A_save, sk_ws, sk_bytes, s));
   }
   if (overlap)
     return tp_row_parallel_forward_overlap(A_save, M, F, h, t, Wdown_p, bdown, residual, Y, nullptr, ws, ws_bytes,
                                            stream);
 
   // Row-parallel + g: Y = sum_i A_i W_down,i + b_down (once) + residual.
-  if (!unfused) return row_parallel(A_save, M, F, h, t, Wdown_p, bdown, residual, Y, s);
+  if (!unfused) return row_parallel(A_save, M, F, h, t, Wdown_p, bdown, residual, Y, sk_ws, sk_bytes, s);
   GemmProblem r;
   r.M = M; r.N = h; r.K = Ft; r.nbatch = t; r.nsum = 1;
   r.a.ptr = A_save; r.a.ld = Ft; r.a.sharded = true; r.a.shard_stride = M * Ft;
   r.b.ptr = Wdown_p; r.b.ld = Ft; r.b.sharded = true; r.b.shard_stride = h * Ft;
   float* P = static_cast<float*>(ws);
   r.epi = EPI_F32; r.d = P; r.ldd = h; r.d_batch_stride = M * h;
+  // data-parallel schedule: the partials are then the same bits as the overlapped path's
   TP_RETURN_IF(run_gemm(r, s));
   return run_shard_reduce(P, M, h, t, bdown, residual, Y, nullptr, s);
 }
@@ -533,16 +590,21 @@ size_t mlp_cs_floats(int64_t M, int64_t h, int64_t Ft, int t) {
   return colsum2_ws_floats(M, h, 1) + static_cast<size_t>(t) * (blocks > 0 ? blocks : 1) * Ft;
 }
 
-size_t tp_mlp_backward_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned flags) {
-  if (M < 0 || h < 0 || F < 0 || t < 1) return 0;
+// Required scratch of the MLP backward: dZ (twice as wide under SwiGLU: gate and up),
+// column-sum scratch, partials; sized for every activation.
+size_t mlp_bwd_base_ws(int64_t M, int64_t h, int64_t F, int t, unsigned flags) {
   const int64_t Ft = F / t;
-  // dZ (twice as wide under SwiGLU: gate and up), column-sum scratch, partials: sized for
-  // every activation.
   size_t sz = round_up(static_cast<size_t>(M) * F * 2 * 2, 256);
   const size_t cs = mlp_cs_floats(M, h, Ft, t);
   sz += round_up(cs * sizeof(float), 256);
   if (flags & TP_FLAG_UNFUSED_REDUCE) sz += static_cast<size_t>(t) * M * h * sizeof(float);
   return sz;
+}
+
+size_t tp_mlp_backward_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned flags) {
+  if (M < 0 || h < 0 || F < 0 || t < 1) return 0;
+  // the required part, then room for the GEMMs' stream-K partials
+  return round_up(mlp_bwd_base_ws(M, h, F, t, flags), 256) + gemm_sk_ws_bytes();
 }
 
 tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_save, const tp_bf16* A_save,
@@ -560,7 +622,10 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
   if (F % t != 0) return TP_ERR_SHAPE;
   const int64_t Ft = F / t;
   if (h % 8 != 0 || Ft % 8 != 0) return TP_ERR_ALIGN;
-  if (!ws || ws_bytes < tp_mlp_backward_workspace_size(M, h, F, t, flags)) return TP_ERR_WORKSPACE;
+  const size_t base_ws = mlp_bwd_base_ws(M, h, F, t, flags);
+  if (!ws || ws_bytes < base_ws) return TP_ERR_WORKSPACE;
+  size_t sk_bytes = 0;
+  void* sk_ws = sk_part_of(ws, ws_bytes, base_ws, &sk_bytes);  // stream-K, when the workspace has room
   if (!aligned16(ws)) return TP_ERR_ALIGN;
   const cudaStream_t s = S(stream);
   const bool unfused = (flags & TP_FLAG_UNFUSED_REDUCE) != 0;
@@ -600,6 +665,7 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
     g.d = dZ; g.ldd = Ft; g.d_batch_stride = M * Ft;
     g.colsum = dbup ? dbup_part : nullptr;  // db_up's partial column sums from the epilogue
   }
+  g.sk_ws = sk_ws; g.sk_ws_bytes = sk_bytes;
   TP_RETURN_IF(run_gemm(g, s));
 
   // Bias gradients: db_down = sum_rows dY, taken once (g backward is the identity), by a
@@ -625,6 +691,7 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
   wd.a.ptr = dY; wd.a.ld = h; wd.a.mn_major = true;
   wd.b.ptr = A_save; wd.b.ld = Ft; wd.b.sharded = true; wd.b.shard_stride = M * Ft; wd.b.mn_major = true;
   wd.epi = EPI_F32; wd.d = dWdown_p; wd.ldd = Ft; wd.d_batch_stride = h * Ft; wd.accumulate = accumulate;
+  wd.sk_ws = sk_ws; wd.sk_ws_bytes = sk_bytes;  // stream-K needs the TMA-store (non-accumulating) epilogue
   TP_RETURN_IF(run_gemm(wd, s));
 
   // dW_up,i = dZ_i^T X -> packed [t][Ft][h] (SwiGLU: [t][2 Ft][h], tp_pack_swiglu's layout).
@@ -633,6 +700,7 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
   wu.a.ptr = dZ; wu.a.ld = Fzt; wu.a.sharded = true; wu.a.shard_stride = M * Fzt; wu.a.mn_major = true;
   wu.b.ptr = X; wu.b.ld = h; wu.b.mn_major = true;
   wu.epi = EPI_F32; wu.d = dWup_p; wu.ldd = h; wu.d_batch_stride = Fzt * h; wu.accumulate = accumulate;
+  wu.sk_ws = sk_ws; wu.sk_ws_bytes = sk_bytes;
   TP_RETURN_IF(run_gemm(wu, s));
 
   // f backward: dX = sum_i dZ_i W_up,i^T.
@@ -640,6 +708,7 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
   dx.M = M; dx.N = h; dx.K = Fzt;
   dx.a.ptr = dZ; dx.a.ld = Fzt; dx.a.sharded = true; dx.a.shard_stride = M * Fzt;
   dx.b.ptr = Wup_p; dx.b.ld = h; dx.b.sharded = true; dx.b.shard_stride = Fzt * h; dx.b.mn_major = true;
+  dx.sk_ws = sk_ws; dx.sk_ws_bytes = sk_bytes;
   if (!unfused) {
     dx.nsum = t;
     dx.epi = EPI_BF16; dx.d = dX; dx.ldd = h;
@@ -692,10 +761,8 @@ tp_status tp_attn_gqa_forward(const tp_bf16* X, int64_t N, int64_t d, int n_head
                               const tp_bf16* Wo_p, const tp_bf16* bo, const tp_bf16* residual, tp_bf16* Y,
                               uint16_t* QKV_save, tp_bf16* O_save, float* lse_save, unsigned flags, void* ws,
                               size_t ws_bytes, tp_stream stream) {
-  (void)ws;
-  (void)ws_bytes;
   if (N < 0 || d < 1 || n_heads < 1 || n_kv_heads < 1 || t < 1 || head_dim < 1) return TP_ERR_INVALID_ARG;
-  if (flags != 0) return TP_ERR_UNSUPPORTED;
+  if ((flags & ~TP_ATTN_F16_INPUT) != 0) return TP_ERR_UNSUPPORTED;
   if (!gqa_ok(d, n_heads, n_kv_heads, head_dim, t)) return TP_ERR_SHAPE;
   if (N == 0) return TP_OK;
   if (!X || !Wqkv_p || !Wo_p || !Y || !QKV_save || !O_save || !lse_save) return TP_ERR_INVALID_ARG;
@@ -706,14 +773,23 @@ tp_status tp_attn_gqa_forward(const tp_bf16* X, int64_t N, int64_t d, int n_head
   c.a.ptr = X; c.a.ld = d;
   c.b.ptr = Wqkv_p; c.b.ld = d; c.b.sharded = true; c.b.shard_stride = rw * d;
   c.epi = EPI_ACT; c.act = TP_ACT_IDENTITY; c.out_f16 = 1;
+  c.f16_ab = (flags & TP_ATTN_F16_INPUT) ? 1 : 0;  // X and W_qkv in IEEE fp16
   c.d = nullptr; c.d2 = QKV_save; c.ldd = rw; c.d_batch_stride = N * rw;
   c.bias = bqkv_p; c.bias_batch_stride = rw;
+  size_t sk_bytes = 0;
+  void* sk_ws = sk_part_of(ws, ws_bytes, 0, &sk_bytes);  // optional: the GEMMs' stream-K partials
+  c.sk_ws = sk_ws; c.sk_ws_bytes = sk_bytes;
   TP_RETURN_IF(run_gemm(c, S(stream)));
   // Attention on each shard's own query heads, no communication.
   TP_RETURN_IF(run_attention_fwd(QKV_save, N, d, n_heads, n_kv_heads, head_dim, t, causal, scale, O_save, lse_save,
                                  S(stream)));
   // Row-parallel W_o + g: Y = sum_i O_i W_o,i + b_o (once) + residual.
-  return tp_row_parallel_forward(O_save, N, d, d, t, Wo_p, bo, residual, Y, stream);
+  return row_parallel(O_save, N, d, d, t, Wo_p, bo, residual, Y, sk_ws, sk_bytes, S(stream));
+}
+
+size_t tp_attn_forward_workspace_size(int64_t N, int64_t d, int n_heads, int head_dim, int t, unsigned flags) {
+  (void)N; (void)d; (void)n_heads; (void)head_dim; (void)t; (void)flags;
+  return gemm_sk_ws_bytes();
 }
 
 tp_status tp_attn_forward(const tp_bf16* X, int64_t N, int64_t d, int n_heads, int head_dim, int t, int causal,
@@ -722,7 +798,7 @@ tp_status tp_attn_forward(const tp_bf16* X, int64_t N, int64_t d, int n_heads, i
                           tp_bf16* O_save, float* lse_save, unsigned flags, void* ws, size_t ws_bytes,
                           tp_stream stream) {
   if (N < 0 || d < 1 || n_heads < 1 || t < 1 || head_dim < 1) return TP_ERR_INVALID_ARG;
-  if (flags != 0) return TP_ERR_UNSUPPORTED;
+  if ((flags & ~TP_ATTN_F16_INPUT) != 0) return TP_ERR_UNSUPPORTED;
   if (head_dim != 128 || static_cast<int64_t>(n_heads) * head_dim != d || n_heads % t != 0) return TP_ERR_SHAPE;
   return tp_attn_gqa_forward(X, N, d, n_heads, n_heads, head_dim, t, causal, scale, Wqkv_p, bqkv_p, Wo_p, bo, residual,
                              Y, QKV_save, O_save, lse_save, flags, ws, ws_bytes, stream);
@@ -753,6 +829,16 @@ tp_status tp_sp_layernorm_forward(const tp_bf16* X_sh, int64_t s, int64_t h, int
                                   const tp_bf16* beta, float eps, tp_bf16* Y_sh, float* mean, float* rstd,
                                   tp_stream stream) {
   return run_ln_forward(X_sh, s, h, t, gamma, beta, eps, Y_sh, mean, rstd, S(stream));
+}
+
+tp_status tp_sp_layernorm_forward_f16(const tp_bf16* X_sh, int64_t s, int64_t h, int t, const tp_bf16* gamma,
+                                      const tp_bf16* beta, float eps, uint16_t* Y_sh, float* mean, float* rstd,
+                                      tp_stream stream) {
+  return run_ln_forward(X_sh, s, h, t, gamma, beta, eps, Y_sh, mean, rstd, S(stream), 1);
+}
+
+tp_status tp_convert_bf16_to_f16(const tp_bf16* src, int64_t n, uint16_t* dst, tp_stream stream) {
+  return run_bf16_to_f16(src, n, dst, S(stream));
 }
 
 tp_status tp_sp_layernorm_backward(const tp_bf16* dY_sh, const tp_bf16* X_sh, const tp_bf16* gamma,

@@ -34,6 +34,8 @@
 #include <cstdlib>
 #include <cstring>
 #include <type_traits>
+#include <atomic>
+#include <ctime>
 #include <mutex>
 
 #include "devmath.cuh"
@@ -56,7 +58,8 @@ constexpr int NUM_THREADS = 192;
 constexpr int BAR_BYTES = 256;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
 
-enum : int { ERR_WAIT_PRODUCER = 0x101, ERR_WAIT_MMA = 0x102, ERR_WAIT_EPI = 0x103, ERR_WAIT_DRAIN = 0x104 };
+enum : int { ERR_WAIT_PRODUCER = 0x101, ERR_WAIT_MMA = 0x102, ERR_WAIT_EPI = 0x103, ERR_WAIT_DRAIN = 0x104,
+              ERR_WAIT_SK = 0x106 };
 
 struct GemmArgs {
   int M, N;
@@ -68,6 +71,7 @@ struct GemmArgs {
   int a_4d, b_4d;
   int mt, nt, kt;
   int epi, act;
+  int f16ab;  // A and B are IEEE fp16 (else bf16)
   void* d;
   int64_t ldd, d_bs;
   void* d2;
@@ -94,6 +98,18 @@ struct GemmArgs {
   // K ranges per output tile: 1, except in gemm_splitc_kernel, where the nsum * kt k-steps of
   // a tile are cut into ksplit nearly equal ranges, one per CTA of a cluster.
   int ksplit;
+  // Split K across CTA pairs (pair kernel), for problems with fewer output tiles than
+  // resident clusters: the k-stages (sk_units) of each of the sk_tiles tiles are cut into
+  // sk_split equal ranges at the same points for every tile; cluster c takes range c / T of
+  // tile c % T (T = sk_tiles), so the clusters on one range walk the same k-slices together
+  // and share operand slices through L2.  A range other than the first writes its fp32
+  // partial to slot c of sk_part and sets its flags to sk_epoch; the first range waits for
+  // the others' flags, adds their partials in k order, applies the epilogue and clears the
+  // flags.  sk_tiles = 0: every tile whole.
+  int sk_tiles, sk_units, sk_split;
+  float* sk_part;     // [sk_split * sk_tiles][256][256] fp32 (slot = cluster)
+  uint64_t* sk_flag;  // [sk_split * sk_tiles][2 CTAs][4 epilogue warps]
+  uint64_t sk_epoch;
   int* err;
   uint64_t timeout_ns;
 };
@@ -466,10 +482,16 @@ __device__ __forceinline__ void load_stage(const GemmArgs& p, const CUtensorMap*
   }
 }
 
+// Instruction descriptor of the 128 x 256 MMA for this launch's operand format.
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ uint32_t single_idesc(const GemmArgs& p) {
+  return p.f16ab ? ptx::idesc_f16_f32(BM, BN, A_MN, B_MN) : ptx::idesc_bf16_f32(BM, BN, A_MN, B_MN);
+}
+
 // The MMAs of one stage (BK deep) into the accumulator at d_tmem; `first` starts it afresh.
 template <bool A_MN, bool B_MN>
-__device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr, bool first) {
-  constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, A_MN, B_MN);
+__device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr, bool first,
+                                          uint32_t idesc) {
 #pragma unroll
   for (int kk = 0; kk < BK / 16; ++kk) {
     // K-major: 16 K-elements = 32 bytes inside the 128-byte swizzle row; 8-row groups 1024 B apart.
@@ -589,7 +611,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           ptx::tc_fence_after();
           mma_stage<A_MN, B_MN>(d_tmem, ptx::smem_addr(sA + stage * A_TILE_BYTES),
-                                ptx::smem_addr(sB + stage * B_TILE_BYTES), ks == 0);
+                                ptx::smem_addr(sB + stage * B_TILE_BYTES), ks == 0, single_idesc<A_MN, B_MN>(p));
           ptx::mma_commit(&empty[stage]);  // frees this smem stage once its MMAs are done
           if (++stage == STAGES) {
             stage = 0;
@@ -813,7 +835,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ptx::mbar_wait(&full[stage], phase, abort_flag, p.err, ERR_WAIT_MMA, p.timeout_ns)) break;
         ptx::tc_fence_after();
         mma_stage<A_MN, B_MN>(tmem_base, ptx::smem_addr(sA + stage * A_TILE_BYTES),
-                              ptx::smem_addr(sB + stage * B_TILE_BYTES), ks == klo);
+                              ptx::smem_addr(sB + stage * B_TILE_BYTES), ks == klo, single_idesc<A_MN, B_MN>(p));
         ptx::mma_commit(&empty[stage]);
         if (++stage == STAGES) {
           stage = 0;
@@ -911,6 +933,62 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::tmem_dealloc(tmem_base, BN);
   }
 }
+
+// ---------------------------------------------------- split-K items (pair kernel)
+enum : int { ITEM_WHOLE = 0, ITEM_HEAD = 1, ITEM_PART = 2 };
+struct PairItem {
+  int tile, klo, khi, kind;
+};
+
+// Work item idx of cluster c.  Split K: one range of one tile (none past sk_split * T
+// clusters).  Otherwise the whole tiles c, c + nclusters, ...  False past the last item.
+// Every role of the kernel enumerates the same items.
+__device__ __forceinline__ bool pair_item(const GemmArgs& p, int c, int nclusters, int total, int ksteps, int idx,
+                                          PairItem& it) {
+  if (p.sk_tiles > 0) {
+    if (idx > 0 || c >= p.sk_split * p.sk_tiles) return false;
+    const int j = c / p.sk_tiles;
+    it.tile = c - j * p.sk_tiles;
+    it.klo = static_cast<int>(static_cast<int64_t>(j) * p.sk_units / p.sk_split);
+    it.khi = static_cast<int>(static_cast<int64_t>(j + 1) * p.sk_units / p.sk_split);
+    it.kind = j == 0 ? ITEM_HEAD : ITEM_PART;
+    return true;
+  }
+  const int tile = c + idx * nclusters;
+  if (tile >= total) return false;
+  it.tile = tile;
+  it.klo = 0;
+  it.khi = ksteps;
+  it.kind = ITEM_WHOLE;
+  return true;
+}
+
+// Adds to this thread's 32 accumulator values (row trow of the 256 x 256 tile, columns
+// col .. col + 31) the split-K partials of the tile's other ranges: clusters c + T j for
+// j = 1 .. nparts, in that (k) order.
+__device__ __forceinline__ void sk_add_partials(const GemmArgs& p, uint32_t (&r)[32], int c, int nparts, int trow,
+                                                int col) {
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+  for (int jj = 1; jj <= nparts; ++jj) {
+    const int cp = c + jj * p.sk_tiles;
+    const float4* src = reinterpret_cast<const float4*>(p.sk_part + (static_cast<int64_t>(cp) * 256 + trow) * 256 + col);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 x = __ldcg(src + q);
+      v[4 * q] += x.x;
+      v[4 * q + 1] += x.y;
+      v[4 * q + 2] += x.z;
+      v[4 * q + 3] += x.w;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(v[j]);
+}
+
+// Epilogues whose pair-kernel launches may split K (TMA-store outputs).
+constexpr bool sk_epi(int epi) { return epi == EPI_BF16 || epi == EPI_ACT || epi == EPI_F32 || epi == EPI_DACT; }
 
 // ------------------------------------------------------------ CTA-pair GEMM
 // Same contract as gemm_kernel, computed by clusters of two CTAs on two SMs
@@ -1170,7 +1248,7 @@ template <bool A_MN, bool B_MN, int EPI, int ACT, bool OVL = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(), 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
-                     const GemmArgs p) {
+                     const __grid_constant__ CUtensorMap tmP, const GemmArgs p) {
   constexpr int P_STAGES = PairCfg<EPI>::stages;
   constexpr int STG_BYTES = PairCfg<EPI>::stg_bytes;
   constexpr int STG_WARP_BYTES = PairCfg<EPI>::stg_warp_bytes;
@@ -1243,12 +1321,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      for (int tile = cluster; ok && tile < total; tile += nclusters) {
+      PairItem it;
+      for (int idx = 0; ok && pair_item(p, cluster, nclusters, total, ksteps, idx, it); ++idx) {
         int mb, nb, b;
-        pair_tile(tile, mt2, nt2, p.nbatch, OVL, mb, nb, b);
+        pair_tile(it.tile, mt2, nt2, p.nbatch, OVL, mb, nb, b);
         const int m0 = mb * 2 * P_HALF + static_cast<int>(rank) * P_HALF;
         const int n0 = nb * P_BN + static_cast<int>(rank) * P_HALF;
-        for (int ks = 0; ks < ksteps; ++ks) {
+        for (int ks = it.klo; ks < it.khi; ++ks) {
           const int s = ks / kt2;
           const int kb = (ks - s * kt2) * KB;  // first 64-wide k-block of this stage
           if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err, ERR_WAIT_PRODUCER, p.timeout_ns)) {
@@ -1310,18 +1389,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------------------- MMA issuer (leader only)
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(2 * P_HALF, P_BN, A_MN, B_MN);
+      const uint32_t idesc = p.f16ab ? ptx::idesc_f16_f32(2 * P_HALF, P_BN, A_MN, B_MN)
+                                     : ptx::idesc_bf16_f32(2 * P_HALF, P_BN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = cluster; ok && tile < total; tile += nclusters) {
+      PairItem it;
+      for (int idx = 0; ok && pair_item(p, cluster, nclusters, total, ksteps, idx, it); ++idx) {
         if (!ptx::mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err, ERR_WAIT_MMA, p.timeout_ns))
           break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * P_BN);
-        for (int ks = 0; ks < ksteps; ++ks) {
+        for (int ks = it.klo; ks < it.khi; ++ks) {
           if (!ptx::mbar_wait_cluster(&full[stage], phase, abort_flag, p.err, ERR_WAIT_MMA, p.timeout_ns)) {
             ok = false;
             break;
@@ -1337,7 +1418,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
                                      : ptx::sdesc_sw128(a_addr + (kk >> 2) * P_A_BYTES + (kk & 3) * 32, 16, 1024);
             const uint64_t bd = B_MN ? ptx::sdesc_sw128(b_addr + kk * 2048, KB * MN_CHUNK_BYTES, 1024)
                                      : ptx::sdesc_sw128(b_addr + (kk >> 2) * P_B_BYTES + (kk & 3) * 32, 16, 1024);
-            ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (ks > it.klo || kk > 0) ? 1u : 0u);
           }
           ptx::mma_commit_pair_mc(&empty[stage], 0x3);  // frees this stage in both CTAs
           if (++stage == P_STAGES) {
@@ -1368,20 +1449,86 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t step = 0;
+    constexpr bool SK_OK = sk_epi(EPI) && !OVL;
+    static_assert(!SK_OK || STG_WARP_BYTES >= 2 * STG_BOX_BYTES, "stream-K partials need two fp32 staging boxes");
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tmD);
       ptx::tma_prefetch_desc(&tmD2);
+      if (SK_OK && p.sk_tiles > 0) ptx::tma_prefetch_desc(&tmP);
     }
-    for (int tile = cluster; tile < total; tile += nclusters) {
+    PairItem it;
+    for (int idx = 0; pair_item(p, cluster, nclusters, total, ksteps, idx, it); ++idx) {
       int mb, nb, b;
-      pair_tile(tile, mt2, nt2, p.nbatch, OVL, mb, nb, b);
+      pair_tile(it.tile, mt2, nt2, p.nbatch, OVL, mb, nb, b);
       if (!ptx::mbar_wait_cluster(&tfull[acc], acc_phase, abort_flag, p.err, ERR_WAIT_EPI, p.timeout_ns)) break;
       ptx::tc_fence_after();
       const int mrow0 = mb * 2 * P_HALF + static_cast<int>(rank) * P_HALF + quad * 32;
       const int m = mrow0 + lane;
+      const int trow = static_cast<int>(rank) * P_HALF + quad * 32 + lane;  // row within the tile
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * P_BN);
-      if constexpr (EPI == EPI_GLU) {
+      // First K range of a split tile: wait until the tile's other ranges have written their
+      // partials of this warp's 32 rows.
+      int sk_parts = 0;
+      if (SK_OK && it.kind == ITEM_HEAD && mrow0 < p.M) {
+        sk_parts = p.sk_split - 1;
+        for (int jj = 1; jj <= p.sk_split - 1; ++jj) {
+          const int cp = cluster + jj * p.sk_tiles;
+          const uint64_t* f = p.sk_flag + (static_cast<int64_t>(cp) * 2 + rank) * 4 + quad;
+          if (ptx::ld_acquire_u64(f) != p.sk_epoch) {
+            const uint64_t t0 = ptx::globaltimer_ns();
+            while (ptx::ld_acquire_u64(f) != p.sk_epoch) {
+              if (*abort_flag || ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+                *abort_flag = 1;
+                if (p.err) atomicCAS(p.err, 0, ERR_WAIT_SK);
+                sk_parts = 0;  // add nothing: the error word already reports the result void
+                break;
+              }
+            }
+          }
+          if (sk_parts == 0) break;
+        }
+        sk_parts = __reduce_min_sync(0xffffffffu, sk_parts);  // one decision for the warp
+      }
+      if (it.kind == ITEM_PART) {
+        if constexpr (SK_OK) {
+          // A K range other than a tile's first: its fp32 partial goes to slot `cluster` through
+          // two alternating 32 x 32 staging boxes, then the flag tells the first range.
+          if (mrow0 < p.M) {
+            if (lane == 0) ptx::bulk_wait_group_read<0>();  // the staging boxes are free
+            __syncwarp();
+#pragma unroll 1
+            for (int c = 0; c < P_BN / 32; ++c) {
+              if (nb * P_BN + c * 32 >= p.N) break;  // warp-uniform
+              uint8_t* buf = stg + (c & 1) * STG_BOX_BYTES;
+              if (c >= 2) {
+                if (lane == 0) ptx::bulk_wait_group_read<1>();
+                __syncwarp();
+              }
+              uint32_t r[32];
+              ptx::tmem_ld32(t_row + c * 32, r);
+              ptx::tmem_ld_wait();
+              float v[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+              stage_row32(buf, lane, v);
+              ptx::fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                ptx::tma_store_3d(&tmP, buf, c * 32, static_cast<int>(rank) * P_HALF + quad * 32, cluster);
+                ptx::bulk_commit_group();
+              }
+            }
+            if (lane == 0) {
+              ptx::bulk_wait_group<0>();  // the partial is in global memory
+              asm volatile("fence.proxy.async.global;" ::: "memory");
+              __threadfence();
+              ptx::st_release_u64(p.sk_flag + (static_cast<int64_t>(cluster) * 2 + rank) * 4 + quad, p.sk_epoch);
+            }
+            __syncwarp();
+          }
+        }
+      } else if constexpr (EPI == EPI_GLU) {
         // The tile is one gate / up group (N is a multiple of 256).  Per 64 hidden columns:
         // Z's gate box, Z's up box (when Z is kept) and the activation box, three TMA stores.
         if (mrow0 < p.M) {
@@ -1490,6 +1637,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
             uint32_t r[32];
             ptx::tmem_ld32(t_row + g0 + h * 32, r);
             ptx::tmem_ld_wait();
+            if (SK_OK && sk_parts > 0) sk_add_partials(p, r, cluster, sk_parts, trow, g0 + h * 32);
             float v[32], v2[32];
             epilogue_values<EPI, ACT>(p, b, m, n0 + h * 32, r, v, v2);
             if (wide) {
@@ -1522,6 +1670,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
       ptx::mbar_arrive_cluster(tempty_leader0 + static_cast<uint32_t>(acc * sizeof(uint64_t)));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
+      if (SK_OK && sk_parts > 0 && lane == 0) {  // consumed: ready for the next launch
+        for (int jj = 1; jj <= sk_parts; ++jj)
+          p.sk_flag[(static_cast<int64_t>(cluster + jj * p.sk_tiles) * 2 + rank) * 4 + quad] = 0;
+      }
       if constexpr (OVL) {
         // The accumulator is already handed back, so the next tile's MMAs run
         // while this warp counts its partial and, if it completed the block's
@@ -1727,22 +1879,86 @@ int pair_clusters(int dev) {
   return n;
 }
 
+// Split-K plan of a pair-kernel launch: T tiles of U k-stages on nc resident clusters.  With
+// fewer tiles than clusters the data-parallel schedule leaves nc - T clusters idle; cutting
+// every tile into S = nc / T equal k-ranges (the same cut points for every tile) puts up to
+// S T clusters to work, and the clusters on one range still walk the same k-slices together,
+// so operand slices shared between tiles come through L2 once.  Ranges keep at least
+// kSkMinUnits k-stages and the workspace bounds the clusters that write partials.
+// (Contiguous stream-K ranges were measured first and lost: ranges that start at staggered
+// k break that lockstep -- the 2048 x 4096 x 16384 row-parallel GEMM, 128 tiles on 76
+// clusters, read 575 MB from DRAM against 276 MB and ran 185 us against 167 us, and a
+// 32-tile one ran 109 us against 87 us.)  TP_STREAMK=0 turns the split off.
+constexpr int kSkMinUnits = 8;
+bool make_output_map(CUtensorMap* map, void* d, CUtensorMapDataType dt, int esz, int64_t N, int64_t M, int nbatch,
+                     int64_t ldd, int64_t dbs);
+struct SkPlan {
+  int tiles = 0, split = 0;
+};
+SkPlan sk_plan(int64_t T, int U, int nc, int max_slots) {
+  SkPlan pl;
+  const char* e = std::getenv("TP_STREAMK");
+  if ((e && e[0] == '0') || T <= 0 || U <= 0 || T * 2 > nc) return pl;
+  int64_t S = nc / T;
+  if (S > U / kSkMinUnits) S = U / kSkMinUnits;
+  if (S * T > max_slots) S = max_slots / T;
+  if (S < 2) return pl;
+  pl.tiles = static_cast<int>(T);
+  pl.split = static_cast<int>(S);
+  return pl;
+}
+
+// Launch order of the split-K flags: a value no earlier launch with the same workspace used
+// (the flags are cleared when consumed, and a fresh workspace would have to hold this exact
+// 64-bit value by chance).
+uint64_t next_sk_epoch() {
+  static std::atomic<uint64_t> ctr{(static_cast<uint64_t>(std::time(nullptr)) << 32) ^
+                                   reinterpret_cast<uintptr_t>(&ctr)};
+  uint64_t v;
+  do {
+    v = ctr.fetch_add(0x9E3779B97F4A7C15ull);
+  } while (v == 0);
+  return v;
+}
+
 template <bool A_MN, bool B_MN, int EPI, int ACT, bool OVL = false>
 tp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const CUtensorMap& td2,
-                      const GemmArgs& a, int64_t tiles, cudaStream_t s) {
+                      const GemmArgs& a0, int64_t tiles, cudaStream_t s, void* sk_ws = nullptr,
+                      size_t sk_ws_bytes = 0) {
   int dev = 0;
   TP_CUDA_CHECK(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return TP_ERR_CUDA;
   const int nc = pair_clusters<A_MN, B_MN, EPI, ACT, OVL>(dev);
   if (nc <= 0) return TP_FAIL_DETAIL("no co-resident CTA pairs");
-  const int clusters = static_cast<int>(tiles < nc ? tiles : nc);
+  int clusters = static_cast<int>(tiles < nc ? tiles : nc);
+  GemmArgs a = a0;
+  CUtensorMap tp_map;
+  std::memset(&tp_map, 0, sizeof(tp_map));
+  if (sk_epi(EPI) && !OVL && sk_ws) {
+    const int U = a.nsum * ((a.kt + PairCfg<EPI>::kb - 1) / PairCfg<EPI>::kb);
+    const int slots = static_cast<int>(sk_ws_bytes / (kSkSlotBytes + kSkFlagBytes));
+    const SkPlan pl = sk_plan(tiles, U, nc, slots < kSkMaxClusters ? slots : kSkMaxClusters);
+    if (pl.tiles > 0) {
+      const int used = pl.tiles * pl.split;  // clusters (and partial slots, first ranges included)
+      a.sk_tiles = pl.tiles;
+      a.sk_units = U;
+      a.sk_split = pl.split;
+      a.sk_part = static_cast<float*>(sk_ws);
+      a.sk_flag = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(sk_ws) + static_cast<size_t>(used) * kSkSlotBytes);
+      a.sk_epoch = next_sk_epoch();
+      if (!make_output_map(&tp_map, a.sk_part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 256, 256, used, 256, 256 * 256))
+        return TP_FAIL_DETAIL("tensor map of the split-K partials");
+      clusters = used;
+    }
+  }
   if constexpr (OVL) {
     gemm_pair_kernel<A_MN, B_MN, EPI, ACT, OVL>
-        <<<2 * clusters, pair_threads<OVL>(), pair_smem_bytes<EPI, OVL>(), s>>>(ta, tb, td, td2, a);
+        <<<2 * clusters, pair_threads<OVL>(), pair_smem_bytes<EPI, OVL>(), s>>>(ta, tb, td, td2, tp_map, a);
     TP_LAUNCHED();
   } else {
     TP_CUDA_CHECK(launch_pdl(gemm_pair_kernel<A_MN, B_MN, EPI, ACT, OVL>, dim3(2 * clusters),
-                             dim3(pair_threads<OVL>()), pair_smem_bytes<EPI, OVL>(), s, ta, tb, td, td2, a));
+                             dim3(pair_threads<OVL>()), pair_smem_bytes<EPI, OVL>(), s, ta, tb, td, td2, tp_map,
+                             a));
     count_launch();
   }
   return TP_OK;
@@ -1990,6 +2206,7 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
   a.kt = static_cast<int>(kt);
   a.epi = P.epi;
   a.act = P.act;
+  a.f16ab = P.f16_ab;
   a.d = P.d;
   a.ldd = P.ldd;
   a.d_bs = P.d_batch_stride;
@@ -2052,9 +2269,11 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
       if (amn || bmn || P.act != TP_ACT_IDENTITY) return TP_ERR_UNSUPPORTED;
       return launch_pair<false, false, EPI_F32, TP_ACT_IDENTITY, true>(ta, tb, td, td2, a, ptiles, s);
     }
+    // Stream-K needs the TMA-store epilogue and a 256-byte aligned workspace.
+    void* sk_ws = (P.sk_ws && a.tma_store && (reinterpret_cast<uintptr_t>(P.sk_ws) & 255u) == 0) ? P.sk_ws : nullptr;
     return dispatch(amn, bmn, P.epi, P.act, [&](auto am, auto bm, auto ep, auto ac) {
       return launch_pair<decltype(am)::value, decltype(bm)::value, decltype(ep)::value, decltype(ac)::value>(
-          ta, tb, td, td2, a, ptiles, s);
+          ta, tb, td, td2, a, ptiles, s, sk_ws, P.sk_ws_bytes);
     });
   }
   const int64_t tiles = mt * nt * P.nbatch;

@@ -101,6 +101,7 @@ struct GemmProblem {
   int64_t M = 0, N = 0, K = 0;
   int nbatch = 1, nsum = 1;
   GemmOperand a, b;
+  int f16_ab = 0;  // both operands IEEE fp16 instead of bf16 (the MMA takes one type for both)
   int epi = EPI_BF16;
   int act = TP_ACT_IDENTITY;
   void* d = nullptr;
@@ -127,7 +128,18 @@ struct GemmProblem {
   const uint16_t* ovl_bias = nullptr;
   const uint16_t* ovl_res = nullptr;
   int64_t ovl_ld = 0;
+  // Stream-K workspace (nullable, 256-byte aligned): lets the CTA-pair kernel split the
+  // k-stages of the tiles past its last full wave over every cluster (BF16, ACT, F32 without
+  // accumulate, DACT epilogues).  gemm_sk_ws_bytes() bytes cover any device; less limits
+  // how many clusters share that work.
+  void* sk_ws = nullptr;
+  size_t sk_ws_bytes = 0;
 };
+// Stream-K workspace: per participating cluster a 256 x 256 fp32 partial and its 8 flags.
+constexpr int kSkMaxClusters = 128;
+constexpr size_t kSkSlotBytes = 256 * 256 * 4;
+constexpr size_t kSkFlagBytes = 8 * 8;
+inline size_t gemm_sk_ws_bytes() { return kSkMaxClusters * (kSkSlotBytes + kSkFlagBytes); }
 // Scratch ints of the overlapped reduction: 8 block counters per 256x256
 // output tile, 32 queue heads and 32 tails on 128-byte lines, and 32 rings of
 // ceil(blocks / 32) 4-int entries.
@@ -153,6 +165,7 @@ struct ColsumJob {
   float* out = nullptr;
   float* ws = nullptr;  // colsum2_ws_floats(rows, cols, nbatch) floats
   int accumulate = 0;
+  int f16 = 0;  // G holds IEEE fp16 values (else bf16)
   // ws already holds [nbatch][nchunks][cols] partials (written by a GEMM epilogue): only the
   // final in-order sum runs, over the caller's nchunks
   int partials_ready = 0;
@@ -231,8 +244,12 @@ tp_status run_row_gemv(const uint16_t* a, int64_t M, int64_t K, int64_t h, int t
 // decode GEMV (gemv.cu), LayerNorm (layernorm.cu)
 tp_status run_decode_swiglu(const uint16_t* x, int64_t M, int64_t h, int64_t F, int t, const uint16_t* Wgu,
                             const uint16_t* Wd, uint16_t* y, uint16_t* a, cudaStream_t s);
+// out_f16: Y is written as IEEE fp16 (else bf16).
 tp_status run_ln_forward(const uint16_t* X, int64_t s, int64_t h, int t, const uint16_t* gamma,
-                         const uint16_t* beta, float eps, uint16_t* Y, float* mean, float* rstd, cudaStream_t st);
+                         const uint16_t* beta, float eps, uint16_t* Y, float* mean, float* rstd, cudaStream_t st,
+                         int out_f16 = 0);
+// dst[i] = fp16(src[i]) for n bf16 values (round to nearest even).
+tp_status run_bf16_to_f16(const uint16_t* src, int64_t n, uint16_t* dst, cudaStream_t s);
 tp_status run_ln_backward(const uint16_t* dY, const uint16_t* X, const uint16_t* gamma, const float* mean,
                           const float* rstd, const uint16_t* dres, int64_t s, int64_t h, int t, uint16_t* dX,
                           float* dg_part, float* db_part, float* dgamma, float* dbeta, cudaStream_t st);
@@ -244,8 +261,9 @@ tp_status run_ln_backward(const uint16_t* dY, const uint16_t* X, const uint16_t*
 
 tp_status run_attention_fwd(const uint16_t* QKV, int64_t N, int64_t d, int n_heads, int n_kv, int head_dim, int t,
                             int causal, float scale, uint16_t* O, float* lse, cudaStream_t s);
+// dqkv_f16: dQKV is written as IEEE fp16 (else bf16).
 tp_status run_attention_bwd(const uint16_t* QKV, const uint16_t* O, const uint16_t* dO, const float* lse, int64_t N,
                             int64_t d, int n_heads, int n_kv, int head_dim, int t, int causal, float scale, float* Dvec,
-                            uint16_t* dQKV, cudaStream_t s);
+                            uint16_t* dQKV, cudaStream_t s, int dqkv_f16 = 0);
 
 }  // namespace tp

@@ -43,6 +43,11 @@ __device__ __forceinline__ void store8(uint16_t* p, const float (&v)[8]) {
   *reinterpret_cast<uint4*>(p) = w;
 }
 
+__device__ __forceinline__ void store8_f16(uint16_t* p, const float (&v)[8]) {
+  *reinterpret_cast<uint4*>(p) =
+      make_uint4(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]), pack_f16x2(v[4], v[5]), pack_f16x2(v[6], v[7]));
+}
+
 // Fixed-order block sum of two values (warp butterfly, then warps in order).
 __device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
 #pragma unroll
@@ -72,6 +77,9 @@ __device__ __forceinline__ void unpack8(const uint4& w, float (&v)[8]) {
 
 // The row stays in registers as packed bf16 words (4 registers per 8 elements) and is
 // unpacked in each pass: half the registers of an fp32 copy, so more rows are in flight.
+// OUT_F16: Y is written as IEEE fp16 (the attention block's input, whose rounding sets the
+// precision of Q and K), else bf16.
+template <bool OUT_F16>
 __global__ void ln_fwd_kernel(const uint16_t* __restrict__ X, int64_t h, const uint16_t* __restrict__ gamma,
                               const uint16_t* __restrict__ beta, float eps, uint16_t* __restrict__ Y,
                               float* __restrict__ mean_out, float* __restrict__ rstd_out) {
@@ -125,7 +133,8 @@ __global__ void ln_fwd_kernel(const uint16_t* __restrict__ X, int64_t h, const u
       load8(beta + c * 8, b);
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] = (v[e] - mean) * rstd * g[e] + b[e];
-      store8(Y + row * h + c * 8, o);
+      if (OUT_F16) store8_f16(Y + row * h + c * 8, o);
+      else store8(Y + row * h + c * 8, o);
     }
   }
   if (threadIdx.x == 0) {
@@ -315,15 +324,20 @@ tp_status check(int64_t s, int64_t h, int t) {
 }  // namespace
 
 tp_status run_ln_forward(const uint16_t* X, int64_t s, int64_t h, int t, const uint16_t* gamma,
-                         const uint16_t* beta, float eps, uint16_t* Y, float* mean, float* rstd, cudaStream_t st) {
+                         const uint16_t* beta, float eps, uint16_t* Y, float* mean, float* rstd, cudaStream_t st,
+                         int out_f16) {
   TP_RETURN_IF(check(s, h, t));
   if (s == 0) return TP_OK;
   if (!X || !gamma || !beta || !Y || !mean || !rstd || !(eps >= 0.0f)) return TP_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(gamma) || !aligned16(beta) || !aligned16(Y)) return TP_ERR_ALIGN;
   if (s > 0x7fffffffLL) return TP_ERR_SHAPE;
   TP_RETURN_IF(ready());
-  TP_CUDA_CHECK(launch_pdl(ln_fwd_kernel, dim3(static_cast<unsigned>(s)), dim3(row_threads(h)), 0, st, X, h, gamma, beta,
-                           eps, Y, mean, rstd));
+  if (out_f16)
+    TP_CUDA_CHECK(launch_pdl(ln_fwd_kernel<true>, dim3(static_cast<unsigned>(s)), dim3(row_threads(h)), 0, st, X, h,
+                             gamma, beta, eps, Y, mean, rstd));
+  else
+    TP_CUDA_CHECK(launch_pdl(ln_fwd_kernel<false>, dim3(static_cast<unsigned>(s)), dim3(row_threads(h)), 0, st, X,
+                             h, gamma, beta, eps, Y, mean, rstd));
   count_launch();
   return TP_OK;
 }

@@ -11,6 +11,7 @@
 // unpack direction is the same map with reads and writes swapped.
 #include <cuda_runtime.h>
 
+#include "devmath.cuh"
 #include "internal.h"
 
 namespace tp {
@@ -365,6 +366,46 @@ tp_status pack_qkv_bias(const uint16_t* b, int64_t d, int n_heads, int head_dim,
   if (m.R == 0) return TP_OK;
   TP_RETURN_IF(ready());
   gather_bias_kernel<<<static_cast<unsigned>((m.R + 255) / 256), 256, 0, s>>>(m, b, bp);
+  TP_LAUNCHED();
+  return TP_OK;
+}
+
+namespace {
+// bf16 -> IEEE fp16, 8 values per thread (n % 8 == 0 handled by the host; a tail loop
+// takes the rest).  Round to nearest even; bf16 values below fp16's normal range become
+// fp16 subnormals (or zero under 2^-25), values above 65504 become infinity.
+__global__ void bf16_to_f16_kernel(const uint16_t* __restrict__ src, int64_t n, uint16_t* __restrict__ dst) {
+  const int64_t n8 = n / 8;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 w = reinterpret_cast<const uint4*>(src)[i];
+    float a0, a1, b0, b1, c0, c1, d0, d1;
+    unpack_bf16x2(w.x, a0, a1);
+    unpack_bf16x2(w.y, b0, b1);
+    unpack_bf16x2(w.z, c0, c1);
+    unpack_bf16x2(w.w, d0, d1);
+    reinterpret_cast<uint4*>(dst)[i] =
+        make_uint4(pack_f16x2(a0, a1), pack_f16x2(b0, b1), pack_f16x2(c0, c1), pack_f16x2(d0, d1));
+  }
+  if (blockIdx.x == 0 && threadIdx.x < n - n8 * 8) {
+    const int64_t i = n8 * 8 + threadIdx.x;
+    const __half h = __float2half_rn(bf16_bits_to_float(src[i]));
+    dst[i] = *reinterpret_cast<const uint16_t*>(&h);
+  }
+}
+}  // namespace
+
+tp_status run_bf16_to_f16(const uint16_t* src, int64_t n, uint16_t* dst, cudaStream_t s) {
+  if (n < 0) return TP_ERR_INVALID_ARG;
+  if (n == 0) return TP_OK;
+  if (!src || !dst) return TP_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(dst)) return TP_ERR_ALIGN;
+  TP_RETURN_IF(ready());
+  int64_t blocks = (n / 8 + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  bf16_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(src, n, dst);
   TP_LAUNCHED();
   return TP_OK;
 }

@@ -105,6 +105,12 @@ __device__ __forceinline__ const ColsumJob& pick(const ColsumJob& a, const Colsu
   return first ? a : b;
 }
 
+// Two 16-bit values of a job's matrix (bf16, or IEEE fp16 when f16) as floats.
+__device__ __forceinline__ void unpack2(uint32_t w, bool f16, float& a, float& b) {
+  if (f16) unpack_f16x2(w, a, b);
+  else unpack_bf16x2(w, a, b);
+}
+
 // Both colsum2 kernels are launched with programmatic dependent launch: they wait
 // for the previous kernel's results before reading anything and let the next
 // kernel on the stream set up while they run.
@@ -125,6 +131,7 @@ __global__ void __launch_bounds__(CS2_THREADS) colsum2_partial_kernel(ColsumJob 
   const int64_t r1 = r0 + CS2_ROWS < j.rows ? r0 + CS2_ROWS : j.rows;
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   const uint16_t* g = j.G + b * j.bs;
+  const bool f16 = j.f16 != 0;
   if (c0 + 8 <= j.cols) {
     int64_t r = r0 + warp;
     for (; r + 24 < r1; r += 32) {  // four rows in flight per thread
@@ -134,24 +141,27 @@ __global__ void __launch_bounds__(CS2_THREADS) colsum2_partial_kernel(ColsumJob 
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         float a0, a1;
-        unpack_bf16x2(w[u].x, a0, a1); acc[0] += a0; acc[1] += a1;
-        unpack_bf16x2(w[u].y, a0, a1); acc[2] += a0; acc[3] += a1;
-        unpack_bf16x2(w[u].z, a0, a1); acc[4] += a0; acc[5] += a1;
-        unpack_bf16x2(w[u].w, a0, a1); acc[6] += a0; acc[7] += a1;
+        unpack2(w[u].x, f16, a0, a1); acc[0] += a0; acc[1] += a1;
+        unpack2(w[u].y, f16, a0, a1); acc[2] += a0; acc[3] += a1;
+        unpack2(w[u].z, f16, a0, a1); acc[4] += a0; acc[5] += a1;
+        unpack2(w[u].w, f16, a0, a1); acc[6] += a0; acc[7] += a1;
       }
     }
     for (; r < r1; r += 8) {
       const uint4 w = *reinterpret_cast<const uint4*>(g + r * j.ld + c0);
       float a0, a1;
-      unpack_bf16x2(w.x, a0, a1); acc[0] += a0; acc[1] += a1;
-      unpack_bf16x2(w.y, a0, a1); acc[2] += a0; acc[3] += a1;
-      unpack_bf16x2(w.z, a0, a1); acc[4] += a0; acc[5] += a1;
-      unpack_bf16x2(w.w, a0, a1); acc[6] += a0; acc[7] += a1;
+      unpack2(w.x, f16, a0, a1); acc[0] += a0; acc[1] += a1;
+      unpack2(w.y, f16, a0, a1); acc[2] += a0; acc[3] += a1;
+      unpack2(w.z, f16, a0, a1); acc[4] += a0; acc[5] += a1;
+      unpack2(w.w, f16, a0, a1); acc[6] += a0; acc[7] += a1;
     }
   } else {
     for (int64_t r = r0 + warp; r < r1; r += 8)
       for (int e = 0; e < 8; ++e)
-        if (c0 + e < j.cols) acc[e] += bf16_bits_to_float(g[r * j.ld + c0 + e]);
+        if (c0 + e < j.cols) {
+          const uint16_t x = g[r * j.ld + c0 + e];
+          acc[e] += f16 ? __half2float(*reinterpret_cast<const __half*>(&x)) : bf16_bits_to_float(x);
+        }
   }
 #pragma unroll
   for (int e = 0; e < 8; ++e) red[warp][lane * 8 + e] = acc[e];

@@ -134,7 +134,9 @@ class TPMLPFunction(torch.autograd.Function):
 # --------------------------------------------------------------------------
 
 class LayerWeights:
-    """Packed per-shard weights of one layer (bf16, device)."""
+    """Packed per-shard weights of one layer (device).  W_qkv is kept in IEEE fp16: the
+    layer runs its attention block on an fp16 input (TP_ATTN_F16_INPUT), which the
+    softmax of a wide model needs to stay within tolerance."""
 
     def __init__(self, p, n_heads, head_dim, t):
         d = p["W_qkv"].shape[0]
@@ -145,6 +147,9 @@ class LayerWeights:
         self.bqkv_p = torch.empty(t, 3 * d // t, dtype=BF16, device=dev)
         self.Wo_p = torch.empty(t, d, d // t, dtype=BF16, device=dev)
         L.tp_pack_qkv_heads(p["W_qkv"], d, n_heads, head_dim, t, self.Wqkv_p)
+        wq16 = torch.empty(t, 3 * d // t, d, dtype=torch.float16, device=dev)
+        L.tp_convert_bf16_to_f16(self.Wqkv_p, self.Wqkv_p.numel(), wq16)
+        self.Wqkv_p = wq16
         L.tp_pack_qkv_bias(p["b_qkv"], d, n_heads, head_dim, t, self.bqkv_p)
         L.tp_pack_row(p["W_o"], d, d, t, self.Wo_p)
         self.mlp = MLPWeights(p["W_up"], p["b_up"], p["W_down"], p["b_down"], t)
@@ -160,16 +165,18 @@ def layer_forward(X, w: LayerWeights, act="gelu_tanh", causal=True, scale=None, 
     t_ln = t if sp else 1
     scale = (1.0 / w.head_dim ** 0.5) if scale is None else scale
     f32 = torch.float32
-    Xn1 = torch.empty(s, d, dtype=BF16, device=dev)
+    # the attention block's input in IEEE fp16 (TP_ATTN_F16_INPUT)
+    Xn1 = torch.empty(s, d, dtype=torch.float16, device=dev)
     m1 = torch.empty(s, dtype=f32, device=dev)
     r1 = torch.empty(s, dtype=f32, device=dev)
-    L.tp_sp_layernorm_forward(X, s, d, t_ln, w.ln1_g, w.ln1_b, eps, Xn1, m1, r1)
+    L.tp_sp_layernorm_forward_f16(X, s, d, t_ln, w.ln1_g, w.ln1_b, eps, Xn1, m1, r1)
     X1 = torch.empty(s, d, dtype=BF16, device=dev)
     QKV = torch.empty(t, s, 3 * d // t, dtype=torch.float16, device=dev)  # fp16 attention operands
     O = torch.empty(t, s, d // t, dtype=BF16, device=dev)
     lse = torch.empty(t, w.n_heads // t, s, dtype=f32, device=dev)
+    aws = _ws(L.tp_attn_forward_workspace_size(s, d, w.n_heads, w.head_dim, t, 0), dev)  # stream-K room
     L.tp_attn_forward(Xn1, s, d, w.n_heads, w.head_dim, t, int(causal), scale, w.Wqkv_p, w.bqkv_p, w.Wo_p, w.b_o,
-                      X, X1, QKV, O, lse, 0, None, 0)
+                      X, X1, QKV, O, lse, L.TP_ATTN_F16_INPUT, aws, aws.numel())
     Xn2 = torch.empty(s, d, dtype=BF16, device=dev)
     m2 = torch.empty(s, dtype=f32, device=dev)
     r2 = torch.empty(s, dtype=f32, device=dev)
@@ -200,8 +207,8 @@ def layer_backward(G, saved, w: LayerWeights):
     nws = L.tp_attn_backward_workspace_size(s, d, w.n_heads, w.head_dim, t, 0)
     ws = _ws(nws, dev)
     L.tp_attn_backward(dX1, saved["Xn1"], saved["QKV"], saved["O"], saved["lse"], s, d, w.n_heads, w.head_dim, t,
-                       int(saved["causal"]), saved["scale"], w.Wqkv_p, w.Wo_p, dXn1, dWqkv, dbqkv, dWo, dbo, 0, 0,
-                       ws, nws)
+                       int(saved["causal"]), saved["scale"], w.Wqkv_p, w.Wo_p, dXn1, dWqkv, dbqkv, dWo, dbo, 0,
+                       L.TP_ATTN_F16_INPUT, ws, nws)
     dX = torch.empty(s, d, dtype=BF16, device=dev)
     ln1 = {k: torch.empty(*shape, dtype=f32, device=dev) for k, shape in
            (("gp", (t_ln, d)), ("bp", (t_ln, d)), ("g", (d,)), ("b", (d,)))}

@@ -47,8 +47,14 @@ def test_version_and_strings():
 
 
 def test_workspace_sizes():
-    assert L.tp_mlp_workspace_size(2048, 4096, 16384, 4, 0) == 0
-    assert L.tp_mlp_workspace_size(2048, 4096, 16384, 4, L.TP_FLAG_UNFUSED_REDUCE) == 4 * 2048 * 4096 * 4
+    # forward: the flags' partials, then room for the GEMMs' stream-K partials (256 KB per
+    # cluster of up to 128, plus 64 bytes of flags each)
+    sk = 128 * (256 * 256 * 4 + 64)
+    assert L.tp_mlp_workspace_size(2048, 4096, 16384, 4, 0) == sk
+    assert L.tp_mlp_workspace_size(2048, 4096, 16384, 4, L.TP_FLAG_UNFUSED_REDUCE) == 4 * 2048 * 4096 * 4 + sk
+    assert L.tp_row_parallel_workspace_size(2048, 16384, 4096, 4) == sk
+    assert L.tp_column_parallel_workspace_size(2048, 4096, 16384, 4) == sk
+    assert L.tp_attn_forward_workspace_size(2048, 12288, 96, 128, 8, 0) == sk
     assert L.tp_mlp_backward_workspace_size(2048, 4096, 16384, 4, 0) >= 2048 * 16384 * 2
     # dZ (room for SwiGLU's gate and up) + db_down's partials + db_up's per-32-row partials that
     # the dgrad epilogue writes ([t][ceil(M / 32)][F / t] fp32), for ragged M as well

@@ -135,3 +135,66 @@ def test_attention_core_entry_points(N, causal):
     torch.cuda.synchronize()
     assert L.tp_get_device_status(check=False) == L.TP_OK
     assert torch.equal(dQKV2, _ws_dqkv(ws, N, d, nh, t))
+
+
+# ---------------------------------------------------------------------------
+# The fp16 attention input (TP_ATTN_F16_INPUT): X and the packed W_qkv in IEEE fp16,
+# dQKV in fp16 in the backward.  The oracle's inputs are the same values (bf16 -> fp16
+# is exact for them), so the criterion is unchanged.
+# ---------------------------------------------------------------------------
+
+def test_convert_bf16_to_f16_exact():
+    """bf16 values in fp16's normal range convert exactly; the ragged tail too."""
+    g = torch.Generator().manual_seed(90)
+    x = (torch.randn(1037, generator=g) * 3).to(torch.bfloat16)
+    out = torch.empty(1037, dtype=torch.float16, device="cuda")
+    L.tp_convert_bf16_to_f16(x.cuda(), x.numel(), out)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu().float(), x.float())
+
+
+@pytest.mark.parametrize("N,nh,t,causal", [(256, 2, 2, True), (333, 4, 2, False), (640, 8, 8, True)])
+def test_attention_f16_input_forward_backward(N, nh, t, causal):
+    dh = 128
+    d = nh * dh
+    inp = I.attn_inputs(N, d, bias=True, dy=True, seed=91)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    Wqkv_p, bqkv_p, Wo_p = pack_attn(dev, d, nh, dh, t)
+    W16 = torch.empty(Wqkv_p.shape, dtype=torch.float16, device="cuda")
+    L.tp_convert_bf16_to_f16(Wqkv_p, Wqkv_p.numel(), W16)
+    X16 = dev["X"].to(torch.float16)
+    flag = L.TP_ATTN_F16_INPUT
+    scale = 1.0 / math.sqrt(dh)
+    Y = torch.empty(N, d, dtype=torch.bfloat16, device="cuda")
+    QKV = torch.empty(t, N, 3 * d // t, dtype=torch.float16, device="cuda")
+    Osv = torch.empty(t, N, d // t, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(t, nh // t, N, dtype=torch.float32, device="cuda")
+    naw = L.tp_attn_forward_workspace_size(N, d, nh, dh, t, flag)
+    aws = torch.empty(naw, dtype=torch.uint8, device="cuda")
+    L.tp_attn_forward(X16, N, d, nh, dh, t, int(causal), scale, W16, bqkv_p, Wo_p, dev["b_o"], None, Y, QKV, Osv, lse,
+                      flag, aws, naw)
+    dX = torch.empty(N, d, dtype=torch.bfloat16, device="cuda")
+    dWqkv = torch.empty(t, 3 * d // t, d, dtype=torch.float32, device="cuda")
+    dbqkv = torch.empty(t, 3 * d // t, dtype=torch.float32, device="cuda")
+    dWo = torch.empty(t, d, d // t, dtype=torch.float32, device="cuda")
+    dbo = torch.empty(d, dtype=torch.float32, device="cuda")
+    nws = L.tp_attn_backward_workspace_size(N, d, nh, dh, t, flag)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    L.tp_attn_backward(dev["dY"], X16, QKV, Osv, lse, N, d, nh, dh, t, int(causal), scale, W16, Wo_p, dX, dWqkv, dbqkv,
+                       dWo, dbo, 0, flag, ws, nws)
+    torch.cuda.synchronize()
+    assert L.tp_get_device_status(check=False) == L.TP_OK
+    ref = {k: f64(v) for k, v in inp.items()}
+    o = O.attn_forward_sharded(ref["X"], ref["W_qkv"], ref["b_qkv"], ref["W_o"], ref["b_o"], nh, dh, causal, scale, t)
+    assert_close("QKV", f64(QKV), np.stack(o["QKV"]))
+    assert_close("O", f64(Osv), np.stack(o["O"]))
+    assert_close("Y", f64(Y), o["Y"])
+    b = O.attn_backward_sharded(ref["dY"], ref["X"], ref["W_qkv"], ref["W_o"], o, nh, dh, scale, t)
+    off = ((N * d * 2 + 255) // 256) * 256 + ((N * nh * 4 + 255) // 256) * 256
+    dqkv = ws[off:off + N * 3 * d * 2].view(torch.float16).view(t, N, 3 * d // t)
+    assert_close("dQKV (fp16)", f64(dqkv), np.stack(b["dQKV"]))
+    assert_close("dX", f64(dX), b["dXn"])
+    assert_close("dW_qkv (packed)", f64(dWqkv), O.pack_qkv_weight(b["dW_qkv"], nh, dh, t))
+    assert_close("db_qkv (packed)", f64(dbqkv), O.pack_qkv_bias(b["db_qkv"], nh, dh, t))
+    assert_close("dW_o (packed)", f64(dWo), O.pack_row_weight(b["dW_o"], t))
+    assert_close("db_o", f64(dbo), b["db_o"])
