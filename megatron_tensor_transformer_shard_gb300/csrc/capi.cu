@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "trace.h"
 #include "ptx.cuh"
 
 namespace tp {
@@ -279,6 +280,7 @@ tp_status tp_attn_gqa_backward(const tp_bf16* dY, const tp_bf16* X, const uint16
                                const tp_bf16* Wo_p, tp_bf16* dX, float* dWqkv_p, float* dbqkv_p, float* dWo_p,
                                float* dbo, int accumulate, unsigned flags, void* ws, size_t ws_bytes,
                                tp_stream stream) {
+  TP_TRACE();
   if (N < 0 || d < 1 || n_heads < 1 || n_kv_heads < 1 || t < 1 || head_dim < 1) return TP_ERR_INVALID_ARG;
   if ((flags & ~TP_ATTN_F16_INPUT) != 0) return TP_ERR_UNSUPPORTED;
   const int f16in = (flags & TP_ATTN_F16_INPUT) ? 1 : 0;  // X, W_qkv and so dQKV in IEEE fp16
@@ -361,6 +363,7 @@ tp_status tp_attn_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Q
                            int causal, float scale, const tp_bf16* Wqkv_p, const tp_bf16* Wo_p, tp_bf16* dX,
                            float* dWqkv_p, float* dbqkv_p, float* dWo_p, float* dbo, int accumulate,
                            unsigned flags, void* ws, size_t ws_bytes, tp_stream stream) {
+  TP_TRACE();
   if (N < 0 || d < 1 || n_heads < 1 || t < 1 || head_dim < 1) return TP_ERR_INVALID_ARG;
   if ((flags & ~TP_ATTN_F16_INPUT) != 0) return TP_ERR_UNSUPPORTED;
   if (head_dim != 128 || static_cast<int64_t>(n_heads) * head_dim != d || n_heads % t != 0) return TP_ERR_SHAPE;
@@ -389,6 +392,7 @@ const char* tp_status_string(tp_status s) {
 }
 
 tp_status tp_get_device_status(tp_stream stream) {
+  TP_TRACE();
   if (!device_error_word()) return TP_ERR_CUDA;
   if (cudaStreamSynchronize(S(stream)) != cudaSuccess) return TP_ERR_CUDA;
   int word = 0;
@@ -401,6 +405,7 @@ tp_status tp_get_device_status(tp_stream stream) {
 }
 
 tp_status tp_selftest_bounded_wait(int64_t timeout_us, tp_stream stream) {
+  TP_TRACE();
   if (timeout_us < 1 || timeout_us > 10000000) return TP_ERR_INVALID_ARG;
   TP_RETURN_IF(ready());
   selftest_wait_kernel<<<1, 32, 0, S(stream)>>>(device_error_word(), static_cast<uint64_t>(timeout_us) * 1000ull);
@@ -410,44 +415,55 @@ tp_status tp_selftest_bounded_wait(int64_t timeout_us, tp_stream stream) {
 
 // ------------------------------------------------------------------ packing
 tp_status tp_pack_col(const tp_bf16* W, int64_t h, int64_t F, int t, tp_bf16* Wp, tp_stream stream) {
+  TP_TRACE();
   return pack_col(W, h, F, t, Wp, 0, S(stream));
 }
 tp_status tp_unpack_col(const tp_bf16* Wp, int64_t h, int64_t F, int t, tp_bf16* W, tp_stream stream) {
+  TP_TRACE();
   return pack_col(Wp, h, F, t, W, 1, S(stream));
 }
 tp_status tp_pack_row(const tp_bf16* W, int64_t F, int64_t h, int t, tp_bf16* Wp, tp_stream stream) {
+  TP_TRACE();
   return pack_row(W, F, h, t, Wp, 0, S(stream));
 }
 tp_status tp_unpack_row(const tp_bf16* Wp, int64_t F, int64_t h, int t, tp_bf16* W, tp_stream stream) {
+  TP_TRACE();
   return pack_row(Wp, F, h, t, W, 1, S(stream));
 }
 tp_status tp_pack_swiglu(const tp_bf16* Wg, const tp_bf16* Wu, int64_t h, int64_t F, int t, tp_bf16* Wp,
                          tp_stream stream) {
+  TP_TRACE();
   return pack_swiglu(Wg, Wu, h, F, t, Wp, S(stream));
 }
 tp_status tp_pack_qkv_heads(const tp_bf16* Wqkv, int64_t d, int n_heads, int head_dim, int t, tp_bf16* Wp,
                             tp_stream stream) {
+  TP_TRACE();
   return pack_qkv(Wqkv, d, n_heads, head_dim, t, Wp, 0, S(stream));
 }
 tp_status tp_unpack_qkv_heads(const tp_bf16* Wp, int64_t d, int n_heads, int head_dim, int t, tp_bf16* Wqkv,
                               tp_stream stream) {
+  TP_TRACE();
   return pack_qkv(Wp, d, n_heads, head_dim, t, Wqkv, 1, S(stream));
 }
 tp_status tp_pack_qkv_bias(const tp_bf16* b, int64_t d, int n_heads, int head_dim, int t, tp_bf16* bp,
                            tp_stream stream) {
+  TP_TRACE();
   return pack_qkv_bias(b, d, n_heads, head_dim, t, bp, S(stream));
 }
 
 tp_status tp_pack_qkv_gqa(const tp_bf16* Wqkv, int64_t d, int n_heads, int n_kv_heads, int head_dim, int t,
                           tp_bf16* Wp, tp_stream stream) {
+  TP_TRACE();
   return pack_qkv_gqa(Wqkv, d, n_heads, n_kv_heads, head_dim, t, Wp, 0, S(stream));
 }
 tp_status tp_unpack_qkv_gqa(const tp_bf16* Wp, int64_t d, int n_heads, int n_kv_heads, int head_dim, int t,
                             tp_bf16* Wqkv, tp_stream stream) {
+  TP_TRACE();
   return pack_qkv_gqa(Wp, d, n_heads, n_kv_heads, head_dim, t, Wqkv, 1, S(stream));
 }
 tp_status tp_pack_qkv_gqa_bias(const tp_bf16* b, int n_heads, int n_kv_heads, int head_dim, int t, tp_bf16* bp,
                                tp_stream stream) {
+  TP_TRACE();
   return pack_qkv_gqa_bias(b, n_heads, n_kv_heads, head_dim, t, bp, S(stream));
 }
 
@@ -467,6 +483,7 @@ size_t tp_row_parallel_overlap_workspace_size(int64_t M, int64_t K, int64_t h, i
 tp_status tp_row_parallel_forward_overlap(const tp_bf16* A, int64_t M, int64_t K, int64_t h, int t,
                                           const tp_bf16* W_p, const tp_bf16* b, const tp_bf16* residual, tp_bf16* Y,
                                           float* partials_out, void* ws, size_t ws_bytes, tp_stream stream) {
+  TP_TRACE();
   if (M < 0 || h < 1 || K < 1 || t < 1) return TP_ERR_INVALID_ARG;
   if (K % t != 0 || t > 8) return TP_ERR_SHAPE;
   const int64_t Kt = K / t;
@@ -495,11 +512,13 @@ tp_status tp_row_parallel_forward_overlap(const tp_bf16* A, int64_t M, int64_t K
 tp_status tp_column_parallel_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t N, int t, tp_act act,
                                      const tp_bf16* W_p, const tp_bf16* b, tp_bf16* Z, tp_bf16* A,
                                      tp_stream stream) {
+  TP_TRACE();
   return column_parallel(X, M, h, N, t, act, W_p, b, Z, A, nullptr, 0, S(stream));
 }
 
 tp_status tp_row_parallel_forward(const tp_bf16* A, int64_t M, int64_t K, int64_t h, int t, const tp_bf16* W_p,
                                   const tp_bf16* b, const tp_bf16* residual, tp_bf16* Y, tp_stream stream) {
+  TP_TRACE();
   return row_parallel(A, M, K, h, t, W_p, b, residual, Y, nullptr, 0, S(stream));
 }
 
@@ -511,6 +530,7 @@ size_t tp_column_parallel_workspace_size(int64_t M, int64_t h, int64_t N, int t)
 tp_status tp_column_parallel_forward_ws(const tp_bf16* X, int64_t M, int64_t h, int64_t N, int t, tp_act act,
                                         const tp_bf16* W_p, const tp_bf16* b, tp_bf16* Z, tp_bf16* A, void* ws,
                                         size_t ws_bytes, tp_stream stream) {
+  TP_TRACE();
   size_t sk = 0;
   void* skp = sk_part_of(ws, ws_bytes, 0, &sk);
   return column_parallel(X, M, h, N, t, act, W_p, b, Z, A, skp, sk, S(stream));
@@ -524,6 +544,7 @@ size_t tp_row_parallel_workspace_size(int64_t M, int64_t K, int64_t h, int t) {
 tp_status tp_row_parallel_forward_ws(const tp_bf16* A, int64_t M, int64_t K, int64_t h, int t, const tp_bf16* W_p,
                                      const tp_bf16* b, const tp_bf16* residual, tp_bf16* Y, void* ws,
                                      size_t ws_bytes, tp_stream stream) {
+  TP_TRACE();
   size_t sk = 0;
   void* skp = sk_part_of(ws, ws_bytes, 0, &sk);
   return row_parallel(A, M, K, h, t, W_p, b, residual, Y, skp, sk, S(stream));
@@ -533,6 +554,7 @@ tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int 
                          const tp_bf16* Wup_p, const tp_bf16* bup, const tp_bf16* Wdown_p, const tp_bf16* bdown,
                          const tp_bf16* residual, tp_bf16* Y, tp_bf16* Z_save, tp_bf16* A_save, unsigned flags,
                          void* ws, size_t ws_bytes, tp_stream stream) {
+  TP_TRACE();
   if (M < 0 || h < 1 || F < 1 || t < 1 || !mlp_act_ok(act)) return TP_ERR_INVALID_ARG;
   if (F % t != 0) return TP_ERR_SHAPE;
   const int64_t Ft = F / t;
@@ -612,6 +634,7 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
                           const tp_bf16* Wdown_p, tp_bf16* dX, float* dWup_p, float* dWdown_p, float* dbup,
                           float* dbdown, int accumulate, unsigned flags, void* ws, size_t ws_bytes,
                           tp_stream stream) {
+  TP_TRACE();
   if (M < 0 || h < 1 || F < 1 || t < 1 || !mlp_act_ok(act)) return TP_ERR_INVALID_ARG;
   if (!dWup_p || !dWdown_p) return TP_ERR_INVALID_ARG;
   const bool swiglu = act == TP_ACT_SWIGLU;
@@ -724,12 +747,14 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
 tp_status tp_decode_swiglu_forward(const tp_bf16* x, int64_t M, int64_t h, int64_t F, int t,
                                    const tp_bf16* Wgu_p, const tp_bf16* Wdown_p, tp_bf16* y, tp_bf16* a_save,
                                    tp_stream stream) {
+  TP_TRACE();
   return run_decode_swiglu(x, M, h, F, t, Wgu_p, Wdown_p, y, a_save, S(stream));
 }
 
 // ----------------------------------------------------------- vocab embedding
 tp_status tp_vocab_embedding_forward(const int32_t* ids, int64_t N, int64_t V, int64_t h, int t, const tp_bf16* E_p,
                                      tp_bf16* Y, tp_stream stream) {
+  TP_TRACE();
   return run_emb_forward(ids, N, V, h, t, E_p, Y, S(stream));
 }
 
@@ -737,6 +762,7 @@ size_t tp_vocab_embedding_backward_workspace_size(int64_t N) { return N < 0 ? 0 
 
 tp_status tp_vocab_embedding_backward(const int32_t* ids, const tp_bf16* dY, int64_t N, int64_t V, int64_t h, int t,
                                       float* dE_p, int accumulate, void* ws, size_t ws_bytes, tp_stream stream) {
+  TP_TRACE();
   return run_emb_backward(ids, dY, N, V, h, t, dE_p, accumulate, ws, ws_bytes, S(stream));
 }
 
@@ -751,6 +777,7 @@ tp_status tp_decode_attn_forward(const tp_bf16* x, int64_t B, int64_t d, int n_h
                                  const tp_bf16* Wo_p, const tp_bf16* bo, uint16_t* K_cache, uint16_t* V_cache,
                                  int64_t L_max, const int32_t* pos, tp_bf16* y, void* ws, size_t ws_bytes,
                                  tp_stream stream) {
+  TP_TRACE();
   return run_decode_attn(x, B, d, n_heads, n_kv_heads, head_dim, t, scale, Wqkv_p, bqkv_p, Wo_p, bo, K_cache, V_cache,
                          L_max, pos, y, ws, ws_bytes, S(stream));
 }
@@ -761,6 +788,7 @@ tp_status tp_attn_gqa_forward(const tp_bf16* X, int64_t N, int64_t d, int n_head
                               const tp_bf16* Wo_p, const tp_bf16* bo, const tp_bf16* residual, tp_bf16* Y,
                               uint16_t* QKV_save, tp_bf16* O_save, float* lse_save, unsigned flags, void* ws,
                               size_t ws_bytes, tp_stream stream) {
+  TP_TRACE();
   if (N < 0 || d < 1 || n_heads < 1 || n_kv_heads < 1 || t < 1 || head_dim < 1) return TP_ERR_INVALID_ARG;
   if ((flags & ~TP_ATTN_F16_INPUT) != 0) return TP_ERR_UNSUPPORTED;
   if (!gqa_ok(d, n_heads, n_kv_heads, head_dim, t)) return TP_ERR_SHAPE;
@@ -797,6 +825,7 @@ tp_status tp_attn_forward(const tp_bf16* X, int64_t N, int64_t d, int n_heads, i
                           const tp_bf16* bo, const tp_bf16* residual, tp_bf16* Y, tp_bf16* QKV_save,
                           tp_bf16* O_save, float* lse_save, unsigned flags, void* ws, size_t ws_bytes,
                           tp_stream stream) {
+  TP_TRACE();
   if (N < 0 || d < 1 || n_heads < 1 || t < 1 || head_dim < 1) return TP_ERR_INVALID_ARG;
   if ((flags & ~TP_ATTN_F16_INPUT) != 0) return TP_ERR_UNSUPPORTED;
   if (head_dim != 128 || static_cast<int64_t>(n_heads) * head_dim != d || n_heads % t != 0) return TP_ERR_SHAPE;
@@ -806,12 +835,14 @@ tp_status tp_attn_forward(const tp_bf16* X, int64_t N, int64_t d, int n_heads, i
 
 tp_status tp_attn_core_forward(const uint16_t* QKV, int64_t N, int64_t d, int n_heads, int n_kv_heads, int head_dim,
                                int t, int causal, float scale, tp_bf16* O, float* lse, tp_stream stream) {
+  TP_TRACE();
   return run_attention_fwd(QKV, N, d, n_heads, n_kv_heads, head_dim, t, causal, scale, O, lse, S(stream));
 }
 
 tp_status tp_attn_core_backward(const uint16_t* QKV, const tp_bf16* O, const uint16_t* dO, const float* lse,
                                 int64_t N, int64_t d, int n_heads, int n_kv_heads, int head_dim, int t, int causal,
                                 float scale, float* Dvec, tp_bf16* dQKV, tp_stream stream) {
+  TP_TRACE();
   return run_attention_bwd(QKV, O, dO, lse, N, d, n_heads, n_kv_heads, head_dim, t, causal, scale, Dvec, dQKV,
                            S(stream));
 }
@@ -821,6 +852,7 @@ tp_status tp_attn_core_backward(const uint16_t* QKV, const tp_bf16* O, const uin
 // shard order (the replica-group all-reduce of a replicated KV head's weights).
 tp_status tp_reduce_qkv_gqa_grad(const float* dWp, int64_t d, int n_heads, int n_kv_heads, int head_dim, int t,
                                  float* dW, int accumulate, tp_stream stream) {
+  TP_TRACE();
   return reduce_qkv_gqa_grad(dWp, d, n_heads, n_kv_heads, head_dim, t, dW, accumulate, S(stream));
 }
 
@@ -828,16 +860,19 @@ tp_status tp_reduce_qkv_gqa_grad(const float* dWp, int64_t d, int n_heads, int n
 tp_status tp_sp_layernorm_forward(const tp_bf16* X_sh, int64_t s, int64_t h, int t, const tp_bf16* gamma,
                                   const tp_bf16* beta, float eps, tp_bf16* Y_sh, float* mean, float* rstd,
                                   tp_stream stream) {
+  TP_TRACE();
   return run_ln_forward(X_sh, s, h, t, gamma, beta, eps, Y_sh, mean, rstd, S(stream));
 }
 
 tp_status tp_sp_layernorm_forward_f16(const tp_bf16* X_sh, int64_t s, int64_t h, int t, const tp_bf16* gamma,
                                       const tp_bf16* beta, float eps, uint16_t* Y_sh, float* mean, float* rstd,
                                       tp_stream stream) {
+  TP_TRACE();
   return run_ln_forward(X_sh, s, h, t, gamma, beta, eps, Y_sh, mean, rstd, S(stream), 1);
 }
 
 tp_status tp_convert_bf16_to_f16(const tp_bf16* src, int64_t n, uint16_t* dst, tp_stream stream) {
+  TP_TRACE();
   return run_bf16_to_f16(src, n, dst, S(stream));
 }
 
@@ -845,6 +880,7 @@ tp_status tp_sp_layernorm_backward(const tp_bf16* dY_sh, const tp_bf16* X_sh, co
                                    const float* mean, const float* rstd, const tp_bf16* dres, int64_t s, int64_t h,
                                    int t, tp_bf16* dX_sh, float* dgamma_part, float* dbeta_part, float* dgamma,
                                    float* dbeta, tp_stream stream) {
+  TP_TRACE();
   return run_ln_backward(dY_sh, X_sh, gamma, mean, rstd, dres, s, h, t, dX_sh, dgamma_part, dbeta_part, dgamma,
                          dbeta, S(stream));
 }
@@ -852,6 +888,7 @@ tp_status tp_sp_layernorm_backward(const tp_bf16* dY_sh, const tp_bf16* X_sh, co
 // ------------------------------------------------------------------ utilities
 tp_status tp_shard_reduce(const float* P, int64_t rows, int64_t cols, int t, const tp_bf16* bias,
                           const tp_bf16* residual, tp_bf16* out_bf16, float* out_f32, tp_stream stream) {
+  TP_TRACE();
   return run_shard_reduce(P, rows, cols, t, bias, residual, out_bf16, out_f32, S(stream));
 }
 
@@ -862,6 +899,7 @@ size_t tp_colsum_workspace_size(int64_t rows, int64_t cols) {
 
 tp_status tp_colsum(const tp_bf16* G, int64_t rows, int64_t cols, float* out, int accumulate, void* ws,
                     size_t ws_bytes, tp_stream stream) {
+  TP_TRACE();
   return run_colsum(G, rows, cols, cols, out, accumulate, static_cast<float*>(ws), ws_bytes / sizeof(float),
                     S(stream));
 }

@@ -21,6 +21,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "trace.h"
 
 namespace tp {
 namespace {
@@ -51,6 +52,7 @@ float* scratch_for_current_device() {
 
 extern "C" tp_status tp_colsum_noalloc(const tp_bf16* G, int64_t rows, int64_t cols, float* out, int accumulate,
                                        tp_stream stream) {
+  TP_TRACE();
   using namespace tp;
   if (rows < 0 || cols < 0) return TP_ERR_INVALID_ARG;
   if (cols == 0) return TP_OK;
