@@ -83,7 +83,7 @@ typedef enum {
 #define TP_FLAG_OVERLAP_REDUCE 2u /* materialise the P_i tile by tile and reduce every
                                      finished tile while later tiles compute, inside the
                                      row-parallel GEMM (tp_row_parallel_forward_overlap);
-                                     M > 128, t in {1,2,4,8}; takes precedence over UNFUSED */
+                                     M > 128, t <= 8; takes precedence over UNFUSED */
 
 /* Flag of the attention entry points (tp_attn_forward / backward and their grouped-query
  * forms): the attention input X and the packed W_qkv hold IEEE fp16 bits instead of bf16
@@ -197,15 +197,19 @@ tp_status tp_row_parallel_forward(const tp_bf16* A, int64_t M, int64_t K, int64_
 
 /* The same two calls with a workspace (tp_*_workspace_size() bytes, 256-byte aligned; a
  * smaller one is used as far as it goes, NULL runs the calls above).  It lets a GEMM of
- * more than 128 rows with fewer 256 x 256 output tiles than the GPU has CTA pairs use a
- * stream-K schedule: the tiles' k-stages (a row-parallel GEMM's t shard ranges laid end to
- * end) are cut into one contiguous range per CTA pair, so that every pair works.  A range that does not start at k = 0
- * leaves its fp32 partial in ws; the range that starts at k = 0 adds the partials of the
- * ranges after it in k order, then applies the epilogue.  The sums are deterministic for a
- * given device (the ranges depend on its SM count); only the rounding of the fp32 sum
- * differs from the data-parallel schedule.  The MLP and attention calls take the same
- * room at the end of their workspaces.  Workspaces must not be shared by calls that may
- * run at the same time. */
+ * more than 128 rows split K where its 256 x 256 output tiles do not fill the GPU's CTA
+ * pairs evenly: the full rounds of whole tiles stay whole, and the remaining tiles (all of
+ * them, when they are fewer than the pairs) are cut into S equal ranges of k-steps (a
+ * row-parallel GEMM's t shard ranges laid end to end) at the same cut points for every
+ * tile, dealt to all pairs -- S is chosen to finish first, and no cut is made when it
+ * would save under 7 % of the time.  Every range leaves its fp32 partial in ws and counts
+ * itself; the range that completes a tile's count adds the tile's partials in range order
+ * and applies the epilogue, so the sums are deterministic for a given device (the plan
+ * depends on its SM count) and only the rounding of the fp32 sum differs from the
+ * data-parallel schedule.  Nothing waits on another CTA pair, and the counters reset
+ * themselves (CUDA-graph replay is fine; any initial contents are).  The MLP and attention
+ * calls take the same room at the end of their workspaces.  Workspaces must not be shared
+ * by calls that may run at the same time. */
 size_t tp_column_parallel_workspace_size(int64_t M, int64_t h, int64_t N, int t);
 tp_status tp_column_parallel_forward_ws(const tp_bf16* X, int64_t M, int64_t h, int64_t N, int t, tp_act act,
                                         const tp_bf16* W_p, const tp_bf16* b, tp_bf16* Z, tp_bf16* A, void* ws,
@@ -219,16 +223,21 @@ tp_status tp_row_parallel_forward_ws(const tp_bf16* A, int64_t M, int64_t K, int
  * and sequence parallelism", section "Volume and scale": the matrix multiply is
  * cut into blocks and each block is communicated while the next computes --
  * Megatron's tp-comm-overlap).  Every shard's partial P_i = A_i W_i is written
- * block by block to an explicit fp32 buffer in ws (the data a multi-GPU run
- * would send); the warp whose partial completes a 32-row block's set of t
- * queues the block, and reducer warps sum its partials in shard order, add b
- * once and the residual after it, and write that block of Y -- while other
- * blocks are still being computed.  Same bits as TP_FLAG_UNFUSED_REDUCE.
+ * tile by tile to an explicit fp32 buffer in ws (the data a multi-GPU run would
+ * send): each 256 x 256 output tile's t shard products are separate work items.
+ * The CTA pairs' full rounds walk a tile's shards one after another (so the
+ * operand panels of one shard are shared by all pairs, as in the fused GEMM), the
+ * remaining tiles' shards are dealt to all pairs, and the item that completes a
+ * tile's set of t (per 32-row block) sums its partials in shard order, adds b once
+ * and the residual after it, and writes that block of Y -- while the tensor cores
+ * go on with the next tiles.  Same bits as TP_FLAG_UNFUSED_REDUCE.
  *   A [t][M][K/t]; W_p [t][h][K/t]; b [h], residual [M][h] nullable; Y [M][h] bf16;
  *   partials_out [t][M][h] fp32 (nullable: receives a copy of the exchanged
  *   partials after the call);
- *   ws: tp_row_parallel_overlap_workspace_size() bytes, 256-byte aligned.
- *   M > 128 and t in {1, 2, 4, 8} (TP_ERR_UNSUPPORTED otherwise; t > 8: TP_ERR_SHAPE),
+ *   ws: tp_row_parallel_overlap_workspace_size() bytes, 256-byte aligned: the
+ *   partials [t][M][h] fp32, then 64 bytes of counters per output tile (any initial
+ *   contents; they reset themselves).
+ *   M > 128 (TP_ERR_UNSUPPORTED otherwise), 1 <= t <= 8 (t > 8: TP_ERR_SHAPE),
  *   h and K/t multiples of 8. */
 size_t tp_row_parallel_overlap_workspace_size(int64_t M, int64_t K, int64_t h, int t);
 tp_status tp_row_parallel_forward_overlap(const tp_bf16* A, int64_t M, int64_t K, int64_t h, int t,
@@ -260,7 +269,7 @@ tp_status tp_row_parallel_forward_overlap(const tp_bf16* A, int64_t M, int64_t K
  *   GEMM's epilogue from the fp32 accumulators.  bup must be NULL (TP_ERR_UNSUPPORTED
  *   otherwise); (F/t) % 128 == 0 (TP_ERR_SHAPE).
  * ws: tp_mlp_workspace_size() bytes: the two flags' partials (required with them; NULL,
- * 0 otherwise), then room for the GEMMs' stream-K partials (see
+ * 0 otherwise), then room for the GEMMs' split-K partials (see
  * tp_row_parallel_forward_ws), used when present. */
 size_t tp_mlp_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned flags);
 tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int t, tp_act act,
@@ -280,7 +289,7 @@ tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int 
  * epilogue writes d gate = dA u silu'(gate) and d up = dA silu(gate), interleaved like
  * Z_save; dWup_p is [t][2F/t][h] in tp_pack_swiglu's layout; dbup must be NULL.  ws (the
  * size query covers every activation) holds dZ and column-sum scratch -- the required
- * part -- then room for the GEMMs' stream-K partials, used when present. */
+ * part -- then room for the GEMMs' split-K partials, used when present. */
 size_t tp_mlp_backward_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned flags);
 tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_save, const tp_bf16* A_save,
                           int64_t M, int64_t h, int64_t F, int t, tp_act act, const tp_bf16* Wup_p,
@@ -351,7 +360,7 @@ tp_status tp_decode_attn_forward(const tp_bf16* x, int64_t B, int64_t d, int n_h
  * flags: 0 or TP_ATTN_F16_INPUT (X and Wqkv_p in IEEE fp16; other bits: TP_ERR_UNSUPPORTED).
  * ws is optional: NULL, 0 runs
  * the GEMMs' data-parallel schedule; tp_attn_forward_workspace_size() bytes (256-byte
- * aligned) let them use stream-K (see tp_row_parallel_forward_ws).  The attention
+ * aligned) let them split K (see tp_row_parallel_forward_ws).  The attention
  * kernel runs one CTA per (head, pair of 128-query tiles) with an online softmax; no
  * N x N score matrix is ever stored. */
 size_t tp_attn_forward_workspace_size(int64_t N, int64_t d, int n_heads, int head_dim, int t, unsigned flags);
@@ -384,7 +393,7 @@ tp_status tp_attn_gqa_forward(const tp_bf16* X, int64_t N, int64_t d, int n_head
  * Wqkv_p fp16; dQKV in ws is then fp16).  ws (see the size query) holds,
  * in order, each 256-byte aligned: dO [t][N][d/t] fp16, D = rowsum(dO * O)
  * [t][H/t][N] fp32, dQKV [t][N][3d/t] bf16, column-sum scratch -- the required part
- * (TP_ERR_WORKSPACE below it) -- then room for the GEMMs' stream-K partials, used
+ * (TP_ERR_WORKSPACE below it) -- then room for the GEMMs' split-K partials, used
  * when present.  The
  * attention gradient runs as two deterministic kernels (dK/dV per key block,
  * dQ per query block); scores are recomputed from the saved log-sum-exp. */

@@ -191,10 +191,10 @@ AttnBwdWs attn_bwd_layout(void* ws, int64_t N, int64_t d, int n_heads, int64_t r
 
 namespace {
 
-// Partials [t][M][h] fp32, then (overlapped reduction) the block counters.
+// Partials [t][M][h] fp32, then (overlapped reduction) the CTA pairs' running sums.
 size_t row_partials_ws(int64_t M, int64_t h, int t, bool overlap) {
   size_t sz = round_up(static_cast<size_t>(t) * M * h * sizeof(float), 256);
-  if (overlap) sz += round_up(static_cast<size_t>(gemm_overlap_counters(M, h)) * sizeof(int), 256);
+  if (overlap) sz += round_up(gemm_overlap_scratch_bytes(M, h), 256);
   return sz;
 }
 
@@ -236,13 +236,13 @@ tp_status row_parallel(const tp_bf16* A, int64_t M, int64_t K, int64_t h, int t,
 }
 
 // The forward's required scratch: the partials of the unfused / overlapped reduction.  A
-// workspace that also holds gemm_sk_ws_bytes() after it lets the GEMMs use stream-K.
+// workspace that also holds gemm_sk_ws_bytes() after it lets the GEMMs split K.
 size_t mlp_fwd_base_ws(int64_t M, int64_t h, int t, unsigned flags) {
   if (flags & TP_FLAG_OVERLAP_REDUCE) return row_partials_ws(M, h, t, true);
   return (flags & TP_FLAG_UNFUSED_REDUCE) ? round_up(static_cast<size_t>(t) * M * h * sizeof(float), 256) : 0;
 }
 
-// The part of a caller's workspace past `base` bytes, 256-byte aligned, for stream-K (NULL
+// The part of a caller's workspace past `base` bytes, 256-byte aligned, for split K (NULL
 // when there is none).
 void* sk_part_of(void* ws, size_t ws_bytes, size_t base, size_t* sk_bytes) {
   *sk_bytes = 0;
@@ -262,7 +262,7 @@ size_t tp_attn_gqa_backward_workspace_size(int64_t N, int64_t d, int n_heads, in
                                            unsigned flags) {
   (void)flags;
   if (N < 0 || d < 1 || n_heads < 1 || t < 1 || !gqa_ok(d, n_heads, n_kv_heads, head_dim, t)) return 0;
-  // the required part, then room for the GEMMs' stream-K partials
+  // the required part, then room for the GEMMs' split-K partials
   return attn_bwd_layout(nullptr, N, d, n_heads, qkv_row_width(n_heads, n_kv_heads, head_dim, t), t).total +
          gemm_sk_ws_bytes();
 }
@@ -292,7 +292,7 @@ tp_status tp_attn_gqa_backward(const tp_bf16* dY, const tp_bf16* X, const uint16
   if (!ws || ws_bytes < w.total) return TP_ERR_WORKSPACE;
   if (!aligned16(ws)) return TP_ERR_ALIGN;
   size_t sk_bytes = 0;
-  void* sk_ws = sk_part_of(ws, ws_bytes, w.total, &sk_bytes);  // stream-K, when the workspace has room
+  void* sk_ws = sk_part_of(ws, ws_bytes, w.total, &sk_bytes);  // split K, when the workspace has room
   const cudaStream_t s = S(stream);
   const int64_t dt = d / t;
   if (N == 0) {
@@ -490,18 +490,18 @@ tp_status tp_row_parallel_forward_overlap(const tp_bf16* A, int64_t M, int64_t K
   if (h % 8 != 0 || Kt % 8 != 0) return TP_ERR_ALIGN;
   if (M == 0) return TP_OK;
   if (!A || !W_p || !Y) return TP_ERR_INVALID_ARG;
-  if (M <= 128 || (t & (t - 1)) != 0) return TP_ERR_UNSUPPORTED;  // CTA-pair kernel (M > 128), t in {1, 2, 4, 8}
+  if (M <= 128) return TP_ERR_UNSUPPORTED;  // CTA-pair kernel (M > 128)
   const size_t need = row_partials_ws(M, h, t, true);
   if (!ws || ws_bytes < need) return TP_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return TP_ERR_ALIGN;
   float* P = static_cast<float*>(ws);
-  int* cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + round_up(static_cast<size_t>(t) * M * h * 4, 256));
+  float* run = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + round_up(static_cast<size_t>(t) * M * h * 4, 256));
   GemmProblem r;
-  r.M = M; r.N = h; r.K = Kt; r.nbatch = t; r.nsum = 1;
+  r.M = M; r.N = h; r.K = Kt; r.nbatch = 1; r.nsum = t;
   r.a.ptr = A; r.a.ld = Kt; r.a.sharded = true; r.a.shard_stride = M * Kt;
   r.b.ptr = W_p; r.b.ld = Kt; r.b.sharded = true; r.b.shard_stride = h * Kt;
-  r.epi = EPI_F32; r.d = P; r.ldd = h; r.d_batch_stride = M * h;
-  r.ovl_cnt = cnt; r.ovl_y = Y; r.ovl_bias = b; r.ovl_res = residual; r.ovl_ld = h;
+  r.epi = EPI_BF16; r.d = Y; r.ldd = h; r.bias = b; r.residual = residual; r.ld_res = h;
+  r.ovl_part = P; r.ovl_run = run;
   TP_RETURN_IF(run_gemm(r, S(stream)));
   if (partials_out)
     TP_CUDA_CHECK(cudaMemcpyAsync(partials_out, P, static_cast<size_t>(t) * M * h * sizeof(float),
@@ -569,8 +569,9 @@ tp_status tp_mlp_forward(const tp_bf16* X, int64_t M, int64_t h, int64_t F, int 
   const size_t base_ws = mlp_fwd_base_ws(M, h, t, flags);
   if (ws_bytes < base_ws || ((unfused || overlap) && !ws)) return TP_ERR_WORKSPACE;
   size_t sk_bytes = 0;
-  void* sk_ws = sk_part_of(ws, ws_bytes, base_ws, &sk_bytes);  // stream-K, when the workspace has room
-  if (overlap && (M <= 128 || t > 8 || (t & (t - 1)) != 0)) return TP_ERR_UNSUPPORTED;
+  void* sk_ws = sk_part_of(ws, ws_bytes, base_ws, &sk_bytes);  // split K, when the workspace has room
+  if (overlap && t > 8) return TP_ERR_SHAPE;
+  if (overlap && M <= 128) return TP_ERR_UNSUPPORTED;
   const cudaStream_t s = S(stream);
 
   if (swiglu) {
@@ -625,7 +626,7 @@ size_t mlp_bwd_base_ws(int64_t M, int64_t h, int64_t F, int t, unsigned flags) {
 
 size_t tp_mlp_backward_workspace_size(int64_t M, int64_t h, int64_t F, int t, unsigned flags) {
   if (M < 0 || h < 0 || F < 0 || t < 1) return 0;
-  // the required part, then room for the GEMMs' stream-K partials
+  // the required part, then room for the GEMMs' split-K partials
   return round_up(mlp_bwd_base_ws(M, h, F, t, flags), 256) + gemm_sk_ws_bytes();
 }
 
@@ -648,7 +649,7 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
   const size_t base_ws = mlp_bwd_base_ws(M, h, F, t, flags);
   if (!ws || ws_bytes < base_ws) return TP_ERR_WORKSPACE;
   size_t sk_bytes = 0;
-  void* sk_ws = sk_part_of(ws, ws_bytes, base_ws, &sk_bytes);  // stream-K, when the workspace has room
+  void* sk_ws = sk_part_of(ws, ws_bytes, base_ws, &sk_bytes);  // split K, when the workspace has room
   if (!aligned16(ws)) return TP_ERR_ALIGN;
   const cudaStream_t s = S(stream);
   const bool unfused = (flags & TP_FLAG_UNFUSED_REDUCE) != 0;
@@ -714,7 +715,7 @@ tp_status tp_mlp_backward(const tp_bf16* dY, const tp_bf16* X, const tp_bf16* Z_
   wd.a.ptr = dY; wd.a.ld = h; wd.a.mn_major = true;
   wd.b.ptr = A_save; wd.b.ld = Ft; wd.b.sharded = true; wd.b.shard_stride = M * Ft; wd.b.mn_major = true;
   wd.epi = EPI_F32; wd.d = dWdown_p; wd.ldd = Ft; wd.d_batch_stride = h * Ft; wd.accumulate = accumulate;
-  wd.sk_ws = sk_ws; wd.sk_ws_bytes = sk_bytes;  // stream-K needs the TMA-store (non-accumulating) epilogue
+  wd.sk_ws = sk_ws; wd.sk_ws_bytes = sk_bytes;  // split K needs the TMA-store (non-accumulating) epilogue
   TP_RETURN_IF(run_gemm(wd, s));
 
   // dW_up,i = dZ_i^T X -> packed [t][Ft][h] (SwiGLU: [t][2 Ft][h], tp_pack_swiglu's layout).
@@ -805,7 +806,7 @@ tp_status tp_attn_gqa_forward(const tp_bf16* X, int64_t N, int64_t d, int n_head
   c.d = nullptr; c.d2 = QKV_save; c.ldd = rw; c.d_batch_stride = N * rw;
   c.bias = bqkv_p; c.bias_batch_stride = rw;
   size_t sk_bytes = 0;
-  void* sk_ws = sk_part_of(ws, ws_bytes, 0, &sk_bytes);  // optional: the GEMMs' stream-K partials
+  void* sk_ws = sk_part_of(ws, ws_bytes, 0, &sk_bytes);  // optional: the GEMMs' split-K partials
   c.sk_ws = sk_ws; c.sk_ws_bytes = sk_bytes;
   TP_RETURN_IF(run_gemm(c, S(stream)));
   // Attention on each shard's own query heads, no communication.

@@ -59,7 +59,7 @@ constexpr int BAR_BYTES = 256;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
 
 enum : int { ERR_WAIT_PRODUCER = 0x101, ERR_WAIT_MMA = 0x102, ERR_WAIT_EPI = 0x103, ERR_WAIT_DRAIN = 0x104,
-              ERR_WAIT_SK = 0x106 };
+              ERR_WAIT_OVL = 0x105, ERR_WAIT_SK = 0x106 };
 
 struct GemmArgs {
   int M, N;
@@ -87,51 +87,38 @@ struct GemmArgs {
   int accumulate;
   int out_f16;
   int tma_store;  // pair kernel: outputs staged in shared memory and written by TMA bulk stores
-  // Overlapped shard reduction (pair kernel, EPI_F32 partials D[b], b = shard): tiles run shard
-  // fastest, and the epilogue warp that stores the last shard's partial of a (tile, CTA half,
-  // warp) block sums the t partials in shard order, adds bias and residual, writes ovl_y bf16.
-  int* ovl_cnt;  // [tile positions][2][4], zero on entry
-  uint16_t* ovl_y;
-  const uint16_t* ovl_bias;
-  const uint16_t* ovl_res;
-  int64_t ovl_ld;
   // K ranges per output tile: 1, except in gemm_splitc_kernel, where the nsum * kt k-steps of
   // a tile are cut into ksplit nearly equal ranges, one per CTA of a cluster.
   int ksplit;
-  // Split K across CTA pairs (pair kernel), for problems with fewer output tiles than
-  // resident clusters: the k-stages (sk_units) of each of the sk_tiles tiles are cut into
-  // sk_split equal ranges at the same points for every tile; cluster c takes range c / T of
-  // tile c % T (T = sk_tiles), so the clusters on one range walk the same k-slices together
-  // and share operand slices through L2.  A range other than the first writes its fp32
-  // partial to slot c of sk_part and sets its flags to sk_epoch; the first range waits for
-  // the others' flags, adds their partials in k order, applies the epilogue and clears the
-  // flags.  sk_tiles = 0: every tile whole.
-  int sk_tiles, sk_units, sk_split;
-  float* sk_part;     // [sk_split * sk_tiles][256][256] fp32 (slot = cluster)
-  uint64_t* sk_flag;  // [sk_split * sk_tiles][2 CTAs][4 epilogue warps]
-  uint64_t sk_epoch;
+  // Split K across CTA pairs (pair kernel).  The first sp_rounds * nclusters tiles are
+  // whole; the next sp_tiles tiles are cut into sp_split K ranges at the same k-stages (range
+  // j covers [j U / S, (j + 1) U / S) of the sp_units stages).  Every range writes its fp32
+  // partial to a slot, then counts itself in the tile's counter for its CTA and warp; the
+  // range that completes the count adds the partials in range order and applies the
+  // epilogue.  sp_split = 0: every tile whole.
+  // Overlapped shard reduction (sp_seq, EPI_BF16): every tile is cut at its sp_split shard
+  // boundaries, each shard an item; shard j's fp32 partial goes to the caller's [S][M][N]
+  // buffer (sp_user = 1) and, by TMA, into the tile's fp32 running sum (stored for shard 0,
+  // added in L2 for the next ones, each after the previous shard's flag sp_cnt = epoch << 32
+  // | j says its add is complete); the last shard adds its accumulator to the running sum
+  // and applies the epilogue.
+  int sp_rounds, sp_tiles, sp_split, sp_units, sp_seq;
+  int sp_user;              // partials in the caller's [S][M][N] buffer, else 256 x 256 slots
+  float* sp_part;           // slots [split tiles * S][256][256], or the caller's buffer
+  int64_t sp_ld, sp_bs;     // sp_user: row and range strides in floats
+  unsigned long long* sp_cnt;  // [split tiles][2 CTAs][4 warps]
+  uint32_t sp_epoch;
   int* err;
   uint64_t timeout_ns;
 };
 
-// Pair kernel tile numbering: batch slowest normally; batch inside the column
-// block when the shard partials are reduced while later tiles compute (so that
-// a tile position's t partials are produced at about the same time).
-__device__ __forceinline__ void pair_tile(int tile, int mt2, int nt2, int nbatch, bool batch_fastest, int& mb, int& nb,
-                                          int& b) {
-  if (batch_fastest) {
-    // row blocks fastest (neighbouring clusters share the weight panel), then the
-    // shards, then the column blocks: a position's t partials come within one wave
-    mb = tile % mt2;
-    const int rest = tile / mt2;
-    b = rest % nbatch;
-    nb = rest / nbatch;
-  } else {
-    mb = tile % mt2;
-    const int rest = tile / mt2;
-    nb = rest % nt2;
-    b = rest / nt2;
-  }
+// Pair kernel tile numbering: row blocks fastest (neighbouring clusters share the weight
+// panel), then column blocks, then the batch.
+__device__ __forceinline__ void pair_tile(int tile, int mt2, int nt2, int& mb, int& nb, int& b) {
+  mb = tile % mt2;
+  const int rest = tile / mt2;
+  nb = rest % nt2;
+  b = rest / nt2;
 }
 
 __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& p, int& b, int& mb, int& nb, int& j) {
@@ -935,23 +922,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // ---------------------------------------------------- split-K items (pair kernel)
-enum : int { ITEM_WHOLE = 0, ITEM_HEAD = 1, ITEM_PART = 2 };
+enum : int { ITEM_WHOLE = 0, ITEM_RANGE = 1 };
 struct PairItem {
   int tile, klo, khi, kind;
+  int range;  // ITEM_RANGE: which of the tile's sp_split K ranges
+  int st;     // ITEM_RANGE: index of the tile among those that are split (counters, partial slots)
 };
 
-// Work item idx of cluster c.  Split K: one range of one tile (none past sk_split * T
-// clusters).  Otherwise the whole tiles c, c + nclusters, ...  False past the last item.
-// Every role of the kernel enumerates the same items.
+__device__ __forceinline__ void sp_cut(const GemmArgs& p, int j, PairItem& it) {
+  it.kind = ITEM_RANGE;
+  it.range = j;
+  it.klo = static_cast<int>(static_cast<int64_t>(j) * p.sp_units / p.sp_split);
+  it.khi = static_cast<int>(static_cast<int64_t>(j + 1) * p.sp_units / p.sp_split);
+}
+
+// Work item idx of cluster c (nclusters launched); false past the cluster's last item.
+// Without split K: the whole tiles c, c + nclusters, ...  Overlapped shard reduction
+// (sp_seq): every tile's shard ranges as items, shard-major (all tiles' shard 0, then shard
+// 1, ...), dealt round-robin, so a tile's shard j comes `total` items after its shard j - 1.  Split K:
+// first the sp_rounds whole rounds, then items u = c, c + nclusters, ... of the sp_tiles
+// remaining tiles, u = S i + j being range j of remaining tile i: a tile's ranges run side
+// by side on neighbouring clusters.  Every role of the kernel enumerates the same items.
 __device__ __forceinline__ bool pair_item(const GemmArgs& p, int c, int nclusters, int total, int ksteps, int idx,
                                           PairItem& it) {
-  if (p.sk_tiles > 0) {
-    if (idx > 0 || c >= p.sk_split * p.sk_tiles) return false;
-    const int j = c / p.sk_tiles;
-    it.tile = c - j * p.sk_tiles;
-    it.klo = static_cast<int>(static_cast<int64_t>(j) * p.sk_units / p.sk_split);
-    it.khi = static_cast<int>(static_cast<int64_t>(j + 1) * p.sk_units / p.sk_split);
-    it.kind = j == 0 ? ITEM_HEAD : ITEM_PART;
+  it.range = 0;
+  it.st = 0;
+  if (p.sp_seq) {  // shard-major: item u = c + idx nclusters is shard u / total of tile u % total
+    const int64_t u = c + static_cast<int64_t>(idx) * nclusters;
+    if (u >= static_cast<int64_t>(total) * p.sp_split) return false;
+    const int j = static_cast<int>(u / total);
+    it.tile = static_cast<int>(u - static_cast<int64_t>(j) * total);
+    it.st = it.tile;
+    sp_cut(p, j, it);
+    return true;
+  }
+  if (p.sp_split > 0) {
+    const int S = p.sp_split;
+    if (idx < p.sp_rounds) {
+      it.tile = c + idx * nclusters;
+      it.klo = 0;
+      it.khi = ksteps;
+      it.kind = ITEM_WHOLE;
+      return true;
+    }
+    const int64_t u = c + static_cast<int64_t>(idx - p.sp_rounds) * nclusters;
+    if (u >= static_cast<int64_t>(p.sp_tiles) * S) return false;
+    const int i = static_cast<int>(u / S);
+    it.tile = p.sp_rounds * nclusters + i;
+    it.st = i;
+    sp_cut(p, static_cast<int>(u - static_cast<int64_t>(i) * S), it);
     return true;
   }
   const int tile = c + idx * nclusters;
@@ -963,28 +982,28 @@ __device__ __forceinline__ bool pair_item(const GemmArgs& p, int c, int ncluster
   return true;
 }
 
-// Adds to this thread's 32 accumulator values (row trow of the 256 x 256 tile, columns
-// col .. col + 31) the split-K partials of the tile's other ranges: clusters c + T j for
-// j = 1 .. nparts, in that (k) order.
-__device__ __forceinline__ void sk_add_partials(const GemmArgs& p, uint32_t (&r)[32], int c, int nparts, int trow,
-                                                int col) {
-  float v[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-  for (int jj = 1; jj <= nparts; ++jj) {
-    const int cp = c + jj * p.sk_tiles;
-    const float4* src = reinterpret_cast<const float4*>(p.sk_part + (static_cast<int64_t>(cp) * 256 + trow) * 256 + col);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float4 x = __ldcg(src + q);
-      v[4 * q] += x.x;
-      v[4 * q + 1] += x.y;
-      v[4 * q + 2] += x.z;
-      v[4 * q + 3] += x.w;
+// Counts one finished range of a split tile in its (tile, CTA, warp) counter: a 64-bit word
+// (launch epoch << 32 | ranges counted); a word left by another launch counts as zero.
+// Returns true for the range that completes the count, which then owns the sum and resets
+// the word (so a graph replay, which repeats the epoch, starts from zero).  The partial
+// must be globally visible before the call.
+__device__ __forceinline__ bool sp_arrive(const GemmArgs& p, unsigned long long* w, volatile int* abort_flag) {
+  const unsigned long long ep = static_cast<unsigned long long>(p.sp_epoch) << 32;
+  unsigned long long old = atomicAdd(w, 0ull);
+  for (int tries = 0; tries < (1 << 20); ++tries) {
+    const unsigned long long n = ((old & 0xffffffff00000000ull) == ep) ? (old & 0xffffffffull) : 0ull;
+    const unsigned long long prev = atomicCAS(w, old, ep | (n + 1));
+    if (prev == old) {
+      if (n + 1 < static_cast<unsigned long long>(p.sp_split)) return false;
+      atomicExch(w, 0ull);
+      __threadfence();  // the other ranges' partials are read after their counts
+      return true;
     }
+    old = prev;
   }
-#pragma unroll
-  for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(v[j]);
+  *abort_flag = 1;
+  if (p.err) atomicCAS(p.err, 0, ERR_WAIT_SK);
+  return false;
 }
 
 // Epilogues whose pair-kernel launches may split K (TMA-store outputs).
@@ -1028,228 +1047,166 @@ struct PairCfg {
   static constexpr int smem_bytes = 1024 + stages * kb * P_STAGE_BYTES + stg_bytes + BAR_BYTES;
 };
 
-// Overlapped shard reduction.  Epilogue warps write each tile's fp32 partial;
-// the warp whose partial completes a 32-row block's set of t (the last of the
-// block's counter) posts the block to one job queue in global memory, and the
-// OVL_REDUCERS reducer warps of every CTA take blocks from it (8 rows each)
-// while the tensor cores and epilogue warps go on with later tiles.  Which CTA
-// finishes a block's last shard follows the static tile schedule, so the
-// reductions are shared out through the queue rather than left to the poster.
-// No CTA waits for another's progress: a CTA's reducers stop once its own
-// epilogue warps have signed off and the queue is empty, and the only wait on
-// another CTA is for the ready flag of a claimed entry, whose poster has
-// already taken the slot and is writing it.
-constexpr int OVL_REDUCERS = 4;
-constexpr int OVL_ROWS = 32 / OVL_REDUCERS;               // rows of a block per reducer warp
-constexpr int OVL_THREADS = NUM_THREADS + 32 * OVL_REDUCERS;
-constexpr int OVL_Q_BYTES = 64;  // claimed jobs of the two reducer groups (row, column block, state), sign-offs
-constexpr int OVL_BAR = 2;                                // named barrier of the reducer warps
-enum : int { ERR_WAIT_OVL_READY = 0x105 };
-
-// The queues sit in the counter scratch after the block counters: OVL_NQ
-// heads and OVL_NQ tails, each on its own 128-byte line, then OVL_NQ rings of
-// `cap` entries of 4 ints (first row, column block, ready flag, unused).  A
-// block goes to queue (block id mod OVL_NQ), so `cap` = ceil(blocks / OVL_NQ)
-// always suffices; claimers start at their own queue and take from the others
-// when it is empty, so no single head is fought over by every CTA.
-constexpr int OVL_NQ = 32;
-struct OvlQueue {
-  int* head;  // head of queue i at head[32 * i]
-  int* tail;
-  int4* ent;  // queue i at ent[i * cap]
-  int cap;
-};
-
-__device__ __forceinline__ OvlQueue ovl_queue(const GemmArgs& p, int mt2, int nt2) {
-  int* base = p.ovl_cnt + static_cast<int64_t>(mt2) * nt2 * 8;
-  OvlQueue q;
-  q.head = base;
-  q.tail = base + 32 * OVL_NQ;
-  q.ent = reinterpret_cast<int4*>(base + 64 * OVL_NQ);
-  q.cap = (mt2 * nt2 * 8 + OVL_NQ - 1) / OVL_NQ;
-  return q;
-}
-
-__device__ __forceinline__ int ld_volatile(const int* a) { return *reinterpret_cast<const volatile int*>(a); }
-
-// One lane posts a completed block (block id = its counter's index).
-__device__ __forceinline__ void ovl_post(const OvlQueue& q, int64_t block, int mrow0, int nb) {
-  const int qi = static_cast<int>(block % OVL_NQ);
-  const int slot = atomicAdd(q.tail + 32 * qi, 1);
-  int4* e = q.ent + static_cast<int64_t>(qi) * q.cap + slot;
-  e->x = mrow0;
-  e->y = nb;
-  __threadfence();
-  atomicExch(&e->z, 1);
-}
-
-__device__ __forceinline__ bool ovl_all_empty(const OvlQueue& q) {
-  for (int i = 0; i < OVL_NQ; ++i)
-    if (ld_volatile(q.head + 32 * i) < ld_volatile(q.tail + 32 * i)) return false;
+// Bounded wait until *f == want (acquire).  False (abort flag raised, error recorded) when
+// the limit passes or the CTA is aborting.
+__device__ __forceinline__ bool sp_wait_flag(const unsigned long long* f, unsigned long long want,
+                                             volatile int* abort_flag, const GemmArgs& p) {
+  const uint64_t* q = reinterpret_cast<const uint64_t*>(f);
+  if (ptx::ld_acquire_u64(q) == want) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (ptx::ld_acquire_u64(q) != want) {
+    if (*abort_flag || ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+      *abort_flag = 1;
+      if (p.err) atomicCAS(p.err, 0, ERR_WAIT_OVL);
+      return false;
+    }
+    __nanosleep(128);
+  }
   return true;
 }
 
-// One lane claims a block: 1 with the block in (row, nb), 0 when this CTA's
-// reducers are finished (own epilogue signed off, every queue drained) or the
-// CTA aborted.
-__device__ __forceinline__ int ovl_claim(const OvlQueue& q, int first, const volatile int* signed_off,
-                                         volatile int* abort_flag, const GemmArgs& p, int& row, int& nb) {
-  unsigned ns = 64;
-  while (true) {
-    for (int i = 0; i < OVL_NQ; ++i) {
-      const int qi = (first + i) % OVL_NQ;
-      int* hp = q.head + 32 * qi;
-      const int h = ld_volatile(hp);
-      if (h >= ld_volatile(q.tail + 32 * qi)) continue;
-      if (atomicCAS(hp, h, h + 1) != h) continue;  // taken by another CTA: try the next queue
-      int4* e = q.ent + static_cast<int64_t>(qi) * q.cap + h;
-      if (atomicAdd(&e->z, 0) == 0) {  // the poster holds the slot and is writing it
-        const uint64_t t0 = ptx::globaltimer_ns();
-        while (atomicAdd(&e->z, 0) == 0) {
-          if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
-            *abort_flag = 1;
-            if (p.err) atomicCAS(p.err, 0, ERR_WAIT_OVL_READY);
-            return 0;
+// Start of row r of range j's partial, at this lane's 8 columns: row trow of slot (st S + j)
+// (tile column tc), or row m of range j in the caller's [S][M][N] buffer (column n).
+__device__ __forceinline__ const float4* sp_row(const GemmArgs& p, int st, int j, int trow, int m, int n, int tc) {
+  if (p.sp_user) return reinterpret_cast<const float4*>(p.sp_part + j * p.sp_bs + static_cast<int64_t>(m) * p.sp_ld + n);
+  return reinterpret_cast<const float4*>(p.sp_part + (static_cast<int64_t>(st * p.sp_split + j) * 256 + trow) * 256 + tc);
+}
+
+__device__ __forceinline__ void unpack8_bf16(const uint4& w, float (&v)[8]) {
+  unpack_bf16x2(w.x, v[0], v[1]);
+  unpack_bf16x2(w.y, v[2], v[3]);
+  unpack_bf16x2(w.z, v[4], v[5]);
+  unpack_bf16x2(w.w, v[6], v[7]);
+}
+
+// (row, range) partial loads in flight per lane while a completed tile is summed.
+constexpr int SP_PAIRS = 8;
+
+// A split tile whose ranges are all counted: this warp's 32 rows (from mrow0; tile rows from
+// trow0) are summed over the S partials in range order and run through the epilogue.  The
+// accumulator is already handed back, so the tensor cores go on with the next item meanwhile.
+// Lane l holds tile columns 8 l .. 8 l + 7 of one row at a time (a warp reads a 1 KB row
+// segment per partial: coalesced), SP_PAIRS (row, range) loads are in flight, and outputs go
+// out as direct 16-byte stores.  The epilogue arithmetic is epilogue_values' (bias, then the
+// residual; act / act'); the DACT column sums add the warp's rows in row order.
+template <int EPI, int ACT>
+__device__ __forceinline__ void sp_reduce_rows(const GemmArgs& p, const PairItem& it, int b, int mrow0, int trow0,
+                                               int nb, int lane) {
+  const int S = p.sp_split;
+  const int tc = lane * 8;
+  const int n = nb * P_BN + tc;
+  if (n >= p.N) return;  // N % 8 == 0: a lane's 8 columns are all inside or all outside
+  const int nrows = min(32, p.M - mrow0);
+  float bv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if constexpr (EPI == EPI_BF16 || EPI == EPI_ACT) {
+    if (p.bias)
+      unpack8_bf16(*reinterpret_cast<const uint4*>(p.bias + (EPI == EPI_ACT ? b * p.bias_bs : 0) + n), bv);
+  }
+  float cs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float acc[8];
+  const int pairs = nrows * S;
+#pragma unroll 1
+  for (int base = 0; base < pairs; base += SP_PAIRS) {
+    float4 x[SP_PAIRS][2];
+    uint4 y[SP_PAIRS];  // the row's residual (BF16) or Z (DACT), loaded with its last range
+#pragma unroll
+    for (int q = 0; q < SP_PAIRS; ++q) {
+      const int pq = min(base + q, pairs - 1);  // past the end: reload the last pair (unused)
+      const int r = pq / S, j = pq - r * S;
+      const int m = mrow0 + r;
+      const float4* src = sp_row(p, it.st, j, trow0 + r, m, n, tc);
+      x[q][0] = __ldcg(src);
+      x[q][1] = __ldcg(src + 1);
+      y[q] = make_uint4(0u, 0u, 0u, 0u);
+      if (EPI == EPI_BF16 && p.res && j == S - 1)
+        y[q] = *reinterpret_cast<const uint4*>(p.res + static_cast<int64_t>(m) * p.ld_res + n);
+      if (EPI == EPI_DACT && j == S - 1)
+        y[q] = *reinterpret_cast<const uint4*>(p.aux + b * p.aux_bs + static_cast<int64_t>(m) * p.ld_aux + n);
+    }
+#pragma unroll
+    for (int q = 0; q < SP_PAIRS; ++q) {
+      const int pq = base + q;
+      if (pq < pairs) {
+        const int r = pq / S, j = pq - r * S;
+        const float xv[8] = {x[q][0].x, x[q][0].y, x[q][0].z, x[q][0].w, x[q][1].x, x[q][1].y, x[q][1].z, x[q][1].w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = (j == 0) ? xv[e] : acc[e] + xv[e];
+        if (j == S - 1) {
+          const int m = mrow0 + r;
+          const int64_t off = b * p.d_bs + static_cast<int64_t>(m) * p.ldd + n;
+          float v[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] = acc[e];
+          if constexpr (EPI == EPI_F32) {
+            float4* d = reinterpret_cast<float4*>(static_cast<float*>(p.d) + off);
+            d[0] = make_float4(v[0], v[1], v[2], v[3]);
+            d[1] = make_float4(v[4], v[5], v[6], v[7]);
+          } else if constexpr (EPI == EPI_BF16) {
+            if (p.bias) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v[e] += bv[e];
+            }
+            if (p.res) {
+              float rv[8];
+              unpack8_bf16(y[q], rv);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v[e] += rv[e];
+            }
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.d) + off) =
+                make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                           pack_bf16x2(v[6], v[7]));
+          } else if constexpr (EPI == EPI_ACT) {
+            if (p.bias) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v[e] += bv[e];
+            }
+            const bool f16 = p.out_f16 != 0;
+            auto pk = [f16](float a0, float a1) { return f16 ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1); };
+            if (p.d)
+              *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.d) + off) =
+                  make_uint4(pk(v[0], v[1]), pk(v[2], v[3]), pk(v[4], v[5]), pk(v[6], v[7]));
+            float a[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) a[e] = act_apply_t<ACT>(v[e]);
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.d2) + off) =
+                make_uint4(pk(a[0], a[1]), pk(a[2], a[3]), pk(a[4], a[5]), pk(a[6], a[7]));
+          } else if constexpr (EPI == EPI_DACT) {
+            float z[8];
+            unpack8_bf16(y[q], z);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              v[e] *= act_grad_t<ACT>(z[e]);
+              cs[e] += v[e];
+            }
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.d) + off) =
+                make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                           pack_bf16x2(v[6], v[7]));
           }
         }
       }
-      __threadfence();
-      row = ld_volatile(&e->x);
-      nb = ld_volatile(&e->y);
-      return 1;
     }
-    if (*abort_flag) return 0;
-    if (*signed_off == 4) {  // every block this CTA posted is in a tail by now
-      __threadfence();
-      if (ovl_all_empty(q)) return 0;
-      continue;
-    }
-    __nanosleep(ns);
-    if (ns < 1024) ns *= 2;
   }
-}
-
-// Sum of the T shard partials of OVL_ROWS rows from mrow0 (this lane's 8
-// columns from col) in shard order, then bias once and residual, as bf16 --
-// the same arithmetic, in the same order, as the separate shard reduction.
-// OVL_PAIRS (row, shard) pairs per step, two float4 loads each, all in flight
-// at once; rows past M load row M-1 (in bounds, never stored) so that no load
-// is predicated and the step stays in registers.
-#ifndef OVL_PAIRS
-#define OVL_PAIRS 8
-#endif
-template <int T>
-__device__ __forceinline__ void ovl_reduce_block_t(const GemmArgs& p, int mrow0, int64_t col) {
-  constexpr int RPI_ = (OVL_PAIRS / T) > 0 ? (OVL_PAIRS / T) : 1;
-  constexpr int RPI = RPI_ < OVL_ROWS ? RPI_ : OVL_ROWS;  // rows per step
-  static_assert(OVL_ROWS % RPI == 0, "rows per step must divide the reducer's rows");
-  const float* D = static_cast<const float*>(p.d) + col;
-  float bv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  if (p.ovl_bias) {
-    const uint4 w = *reinterpret_cast<const uint4*>(p.ovl_bias + col);
-    unpack_bf16x2(w.x, bv[0], bv[1]);
-    unpack_bf16x2(w.y, bv[2], bv[3]);
-    unpack_bf16x2(w.z, bv[4], bv[5]);
-    unpack_bf16x2(w.w, bv[6], bv[7]);
-  }
-#pragma unroll 1
-  for (int r0 = 0; r0 < OVL_ROWS; r0 += RPI) {
-    float4 v[RPI][T][2];
-#pragma unroll
-    for (int rr = 0; rr < RPI; ++rr) {
-      const int m = min(mrow0 + r0 + rr, p.M - 1);
-      const float* row = D + static_cast<int64_t>(m) * p.ldd;
-#pragma unroll
-      for (int b = 0; b < T; ++b) {
-        const float4* src = reinterpret_cast<const float4*>(row + b * p.d_bs);
-        v[rr][b][0] = __ldcs(src);  // read once: evict first
-        v[rr][b][1] = __ldcs(src + 1);
-      }
-    }
-#pragma unroll
-    for (int rr = 0; rr < RPI; ++rr) {
-      const int m = mrow0 + r0 + rr;
-      if (m >= p.M) continue;
-      float acc[8];
-      acc[0] = v[rr][0][0].x; acc[1] = v[rr][0][0].y; acc[2] = v[rr][0][0].z; acc[3] = v[rr][0][0].w;
-      acc[4] = v[rr][0][1].x; acc[5] = v[rr][0][1].y; acc[6] = v[rr][0][1].z; acc[7] = v[rr][0][1].w;
-#pragma unroll
-      for (int b = 1; b < T; ++b) {  // fixed shard order
-        acc[0] += v[rr][b][0].x; acc[1] += v[rr][b][0].y; acc[2] += v[rr][b][0].z; acc[3] += v[rr][b][0].w;
-        acc[4] += v[rr][b][1].x; acc[5] += v[rr][b][1].y; acc[6] += v[rr][b][1].z; acc[7] += v[rr][b][1].w;
-      }
-      if (p.ovl_bias) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] += bv[e];
-      }
-      if (p.ovl_res) {
-        const uint4 w = *reinterpret_cast<const uint4*>(p.ovl_res + static_cast<int64_t>(m) * p.ovl_ld + col);
-        float rv[8];
-        unpack_bf16x2(w.x, rv[0], rv[1]);
-        unpack_bf16x2(w.y, rv[2], rv[3]);
-        unpack_bf16x2(w.z, rv[4], rv[5]);
-        unpack_bf16x2(w.w, rv[6], rv[7]);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] += rv[e];
-      }
-      uint4 o;
-      o.x = pack_bf16x2(acc[0], acc[1]);
-      o.y = pack_bf16x2(acc[2], acc[3]);
-      o.z = pack_bf16x2(acc[4], acc[5]);
-      o.w = pack_bf16x2(acc[6], acc[7]);
-      *reinterpret_cast<uint4*>(p.ovl_y + static_cast<int64_t>(m) * p.ovl_ld + col) = o;
+  if constexpr (EPI == EPI_DACT) {
+    if (p.cs) {
+      float4* c = reinterpret_cast<float4*>(p.cs + (static_cast<int64_t>(b) * p.cs_chunks + mrow0 / 32) * p.N + n);
+      c[0] = make_float4(cs[0], cs[1], cs[2], cs[3]);
+      c[1] = make_float4(cs[4], cs[5], cs[6], cs[7]);
     }
   }
 }
 
-__device__ __forceinline__ void ovl_reduce_block(const GemmArgs& p, int mrow0, int64_t col) {
-  if (col >= p.N) return;
-  switch (p.nbatch) {  // the host admits t = 1, 2, 4, 8
-    case 1: ovl_reduce_block_t<1>(p, mrow0, col); break;
-    case 2: ovl_reduce_block_t<2>(p, mrow0, col); break;
-    case 4: ovl_reduce_block_t<4>(p, mrow0, col); break;
-    default: ovl_reduce_block_t<8>(p, mrow0, col); break;
-  }
-}
-
-// The loop of a group of 4 reducer warps (named barrier `bar`): the
-// claimer's lane 0 takes a block, the group sums its 32 rows (8 per warp).
-__device__ __forceinline__ void ovl_reduce_loop(const GemmArgs& p, const OvlQueue& q, volatile int* job,
-                                                const volatile int* signed_off, volatile int* abort_flag,
-                                                bool claimer, int bar, int rrow, int lane) {
-  while (true) {
-    if (claimer && lane == 0) {
-      int row = 0, nb = 0;
-      const int st = ovl_claim(q, static_cast<int>(blockIdx.x) % OVL_NQ, signed_off, abort_flag, p, row, nb);
-      job[0] = row;
-      job[1] = nb;
-      job[2] = st;
-    }
-    __syncwarp();
-    ptx::named_bar_sync(bar, 32 * OVL_REDUCERS);  // the claimed block is visible
-    const int row = job[0], nb = job[1], st = job[2];
-    ptx::named_bar_sync(bar, 32 * OVL_REDUCERS);  // read by all before the next claim
-    if (!st) break;
-    __threadfence();
-    ovl_reduce_block(p, row + rrow, static_cast<int64_t>(nb) * P_BN + lane * 8);
-  }
-}
-
-template <bool OVL>
-constexpr int pair_threads() {
-  return OVL ? OVL_THREADS : NUM_THREADS;
-}
-template <int EPI, bool OVL>
+template <int EPI>
 constexpr int pair_smem_bytes() {
-  return PairCfg<EPI>::smem_bytes + (OVL ? OVL_Q_BYTES : 0);
+  return PairCfg<EPI>::smem_bytes;
 }
 
-template <bool A_MN, bool B_MN, int EPI, int ACT, bool OVL = false>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(), 1)
+template <bool A_MN, bool B_MN, int EPI, int ACT>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
                      const __grid_constant__ CUtensorMap tmP, const GemmArgs p) {
   constexpr int P_STAGES = PairCfg<EPI>::stages;
+  static_assert((2 * P_STAGES + 14) * 8 <= BAR_BYTES, "barriers, TMEM slot and abort flag fit their region");
   constexpr int STG_BYTES = PairCfg<EPI>::stg_bytes;
   constexpr int STG_WARP_BYTES = PairCfg<EPI>::stg_warp_bytes;
   constexpr int NOUT = PairCfg<EPI>::outputs;
@@ -1268,7 +1225,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
   uint64_t* mma_done = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* ovl_s = reinterpret_cast<volatile int*>(sStage + STG_BYTES + BAR_BYTES);  // OVL launches only
+  uint64_t* ebar = mma_done + 2;  // two per epilogue warp: its running-sum loads (overlapped form)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -1287,7 +1244,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
       ptx::mbar_init(&tempty[a], 256);  // both CTAs' epilogue threads (used in the leader)
     }
     ptx::mbar_init(mma_done, 1);
-    if constexpr (OVL) ovl_s[3] = 0;  // epilogue warps signed off
+    for (int q = 0; q < 8; ++q) ptx::mbar_init(&ebar[q], 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -1306,17 +1263,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
   const int total = p.nbatch * mt2 * nt2;
   const int kt2 = (p.kt + KB - 1) / KB;  // stages per shard of K
   const int ksteps = p.nsum * kt2;
-  // Programmatic dependent launch (not for the overlapped form, whose queues are
-  // written before its producers start): as in gemm_kernel, every global access
-  // follows the producers' griddepcontrol.wait.
-  if constexpr (!OVL) ptx::griddep_launch_dependents();
+  // Programmatic dependent launch: as in gemm_kernel, every global access follows the
+  // producers' griddepcontrol.wait.
+  ptx::griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------ TMA producer (both CTAs)
       ptx::tma_prefetch_desc(&tmA);
       ptx::tma_prefetch_desc(&tmB);
-      if constexpr (!OVL) ptx::griddep_wait();
+      ptx::griddep_wait();
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -1324,7 +1280,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
       PairItem it;
       for (int idx = 0; ok && pair_item(p, cluster, nclusters, total, ksteps, idx, it); ++idx) {
         int mb, nb, b;
-        pair_tile(it.tile, mt2, nt2, p.nbatch, OVL, mb, nb, b);
+        pair_tile(it.tile, mt2, nt2, mb, nb, b);
         const int m0 = mb * 2 * P_HALF + static_cast<int>(rank) * P_HALF;
         const int n0 = nb * P_BN + static_cast<int>(rank) * P_HALF;
         for (int ks = it.klo; ks < it.khi; ++ks) {
@@ -1435,10 +1391,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
       volatile int never = 0;
       ptx::mbar_wait(mma_done, 0, &never, p.err, ERR_WAIT_DRAIN, p.timeout_ns);
     }
-  } else if (OVL && warp >= NUM_THREADS / 32) {
-    // ------------------------------------------------ shard reducers (OVL only)
-    ovl_reduce_loop(p, ovl_queue(p, mt2, nt2), ovl_s, ovl_s + 3, abort_flag, warp == NUM_THREADS / 32, OVL_BAR,
-                    (warp - NUM_THREADS / 32) * OVL_ROWS, lane);
   } else {
     // ----------------------------------------------------------- epilogue (both CTAs)
     const int quad = warp & 3;
@@ -1449,17 +1401,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t step = 0;
-    constexpr bool SK_OK = sk_epi(EPI) && !OVL;
-    static_assert(!SK_OK || STG_WARP_BYTES >= 2 * STG_BOX_BYTES, "stream-K partials need two fp32 staging boxes");
+    constexpr bool SK_OK = sk_epi(EPI);
+    static_assert(!SK_OK || STG_WARP_BYTES >= 2 * STG_BOX_BYTES, "split-K partials need two fp32 staging boxes");
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tmD);
       ptx::tma_prefetch_desc(&tmD2);
-      if (SK_OK && p.sk_tiles > 0) ptx::tma_prefetch_desc(&tmP);
+      if (SK_OK && p.sp_split > 0) ptx::tma_prefetch_desc(&tmP);
     }
+    uint32_t ephase = 0;  // phases of this warp's two running-sum load barriers (bits 0, 1)
     PairItem it;
     for (int idx = 0; pair_item(p, cluster, nclusters, total, ksteps, idx, it); ++idx) {
       int mb, nb, b;
-      pair_tile(it.tile, mt2, nt2, p.nbatch, OVL, mb, nb, b);
+      pair_tile(it.tile, mt2, nt2, mb, nb, b);
       if (!ptx::mbar_wait_cluster(&tfull[acc], acc_phase, abort_flag, p.err, ERR_WAIT_EPI, p.timeout_ns)) break;
       ptx::tc_fence_after();
       const int mrow0 = mb * 2 * P_HALF + static_cast<int>(rank) * P_HALF + quad * 32;
@@ -1467,67 +1420,185 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
       const int trow = static_cast<int>(rank) * P_HALF + quad * 32 + lane;  // row within the tile
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * P_BN);
-      // First K range of a split tile: wait until the tile's other ranges have written their
-      // partials of this warp's 32 rows.
-      int sk_parts = 0;
-      if (SK_OK && it.kind == ITEM_HEAD && mrow0 < p.M) {
-        sk_parts = p.sk_split - 1;
-        for (int jj = 1; jj <= p.sk_split - 1; ++jj) {
-          const int cp = cluster + jj * p.sk_tiles;
-          const uint64_t* f = p.sk_flag + (static_cast<int64_t>(cp) * 2 + rank) * 4 + quad;
-          if (ptx::ld_acquire_u64(f) != p.sk_epoch) {
-            const uint64_t t0 = ptx::globaltimer_ns();
-            while (ptx::ld_acquire_u64(f) != p.sk_epoch) {
-              if (*abort_flag || ptx::globaltimer_ns() - t0 > p.timeout_ns) {
-                *abort_flag = 1;
-                if (p.err) atomicCAS(p.err, 0, ERR_WAIT_SK);
-                sk_parts = 0;  // add nothing: the error word already reports the result void
-                break;
-              }
-            }
-          }
-          if (sk_parts == 0) break;
-        }
-        sk_parts = __reduce_min_sync(0xffffffffu, sk_parts);  // one decision for the warp
-      }
-      if (it.kind == ITEM_PART) {
-        if constexpr (SK_OK) {
-          // A K range other than a tile's first: its fp32 partial goes to slot `cluster` through
-          // two alternating 32 x 32 staging boxes, then the flag tells the first range.
+      // A K range of a split tile: its fp32 partial of this warp's 32 rows goes out through two
+      // alternating 32 x 32 staging boxes (to slot st S + j, or to range j of the caller's
+      // buffer), then the range counts itself; the range that completes the count goes on to
+      // the epilogue below with the sum of all ranges, the others are done with the tile.
+      bool sp_last = false;
+      bool ovl_item = false;
+      unsigned long long* ovl_flag = nullptr;  // set (to ovl_set) once this shard's adds are complete
+      unsigned long long ovl_set = 0;
+      if constexpr (EPI == EPI_BF16) {
+        if (p.sp_seq) {
+          // Overlapped shard reduction: shard j = it.range of tile it.tile.  Its fp32 partial is
+          // staged 32 columns at a time in two alternating boxes; from a box it goes to the
+          // caller's buffer with coalesced stores (a warp store covers four 128-byte rows; TMA
+          // stores of these scattered rows held up the operand loads) and, by TMA, into the
+          // tile's running sum (stored for shard 0, added in L2 for the next shards).  Shard j
+          // adds only after shard j - 1's flag (epoch << 32 | j) says its adds are complete, so
+          // the sum runs in shard order; that shard was dealt a whole pass of the tiles earlier,
+          // so the flag is normally set long before.  The last shard loads the running sum one
+          // box ahead, adds its accumulator, and writes its own partial and Y (bias once, then
+          // the residual) with coalesced stores.
+          ovl_item = true;
           if (mrow0 < p.M) {
-            if (lane == 0) ptx::bulk_wait_group_read<0>();  // the staging boxes are free
-            __syncwarp();
-#pragma unroll 1
-            for (int c = 0; c < P_BN / 32; ++c) {
-              if (nb * P_BN + c * 32 >= p.N) break;  // warp-uniform
-              uint8_t* buf = stg + (c & 1) * STG_BOX_BYTES;
-              if (c >= 2) {
-                if (lane == 0) ptx::bulk_wait_group_read<1>();
-                __syncwarp();
-              }
-              uint32_t r[32];
-              ptx::tmem_ld32(t_row + c * 32, r);
-              ptx::tmem_ld_wait();
-              float v[32];
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-              stage_row32(buf, lane, v);
+            const int S = p.sp_split, j = it.range;
+            const int rrow = static_cast<int>(rank) * P_HALF + quad * 32;  // rows in the running sum
+            float* part = p.sp_part + j * p.sp_bs;
+            const unsigned long long ep = static_cast<unsigned long long>(p.sp_epoch) << 32;
+            unsigned long long* flag = p.sp_cnt + (static_cast<int64_t>(it.tile) * 2 + rank) * 4 + quad;
+            if (lane == 0) ptx::bulk_wait_group<0>();
+            int use_sum = 1;  // this shard touches the running sum (0 after a failed wait: result void)
+            if (j > 0 && lane == 0) use_sum = sp_wait_flag(flag, ep | static_cast<unsigned long long>(j), abort_flag, p);
+            use_sum = __shfl_sync(0xffffffffu, use_sum, 0);
+            int nch = 0;  // 32-column chunks inside N
+            while (nch < P_BN / 32 && nb * P_BN + nch * 32 < p.N) ++nch;
+            const bool load_sum = (j == S - 1) && S > 1 && use_sum;
+            if (load_sum) {
               ptx::fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {
-                ptx::tma_store_3d(&tmP, buf, c * 32, static_cast<int>(rank) * P_HALF + quad * 32, cluster);
-                ptx::bulk_commit_group();
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                for (int c = 0; c < 2 && c < nch; ++c) {
+                  ptx::mbar_arrive_expect_tx(&ebar[quad * 2 + c], STG_BOX_BYTES);
+                  ptx::tma_load_3d(stg + c * STG_BOX_BYTES, &tmD2, &ebar[quad * 2 + c], c * 32, rrow, it.tile);
+                }
               }
             }
-            if (lane == 0) {
-              ptx::bulk_wait_group<0>();  // the partial is in global memory
-              asm volatile("fence.proxy.async.global;" ::: "memory");
-              __threadfence();
-              ptx::st_release_u64(p.sk_flag + (static_cast<int64_t>(cluster) * 2 + rank) * 4 + quad, p.sk_epoch);
+#pragma unroll 1
+            for (int c = 0; c < nch; ++c) {
+              const int n0 = nb * P_BN + c * 32;
+              uint8_t* buf = stg + (c & 1) * STG_BOX_BYTES;
+              if (j < S - 1 && c >= 2) {
+                if (lane == 0) ptx::bulk_wait_group_read<1>();  // the box's running-sum copy read it
+              }
+              __syncwarp();
+              uint32_t r[32];
+              ptx::tmem_ld32(t_row + c * 32, r);
+              ptx::tmem_ld_wait();
+              float v[32], sum[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) v[e] = sum[e] = __uint_as_float(r[e]);
+              if (load_sum) {
+                const int eb = quad * 2 + (c & 1);
+                if (!ptx::mbar_wait(&ebar[eb], (ephase >> (c & 1)) & 1u, abort_flag, p.err, ERR_WAIT_EPI,
+                                    p.timeout_ns)) {
+                  volatile int never = 0;  // the copy may still land: wait for it (bounded) first
+                  ptx::mbar_wait(&ebar[eb], (ephase >> (c & 1)) & 1u, &never, nullptr, 0, p.timeout_ns);
+                }
+                ephase ^= 1u << (c & 1);
+                const uint8_t* rowp = buf + lane * 128;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                  const float4 x = *reinterpret_cast<const float4*>(rowp + ((k ^ (lane & 7)) << 4));
+                  sum[4 * k] = x.x + v[4 * k];
+                  sum[4 * k + 1] = x.y + v[4 * k + 1];
+                  sum[4 * k + 2] = x.z + v[4 * k + 2];
+                  sum[4 * k + 3] = x.w + v[4 * k + 3];
+                }
+              }
+              stage_row32(buf, lane, v);  // a lane overwrites only the row it read
+              ptx::fence_proxy_async_smem();
+              __syncwarp();
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {  // rows 4 i .. 4 i + 3, 16 bytes a lane
+                const int row = 4 * i + (lane >> 3), k = lane & 7;
+                const float4 x = *reinterpret_cast<const float4*>(buf + row * 128 + ((k ^ (row & 7)) << 4));
+                if (mrow0 + row < p.M && n0 + 4 * k < p.N)
+                  *reinterpret_cast<float4*>(part + static_cast<int64_t>(mrow0 + row) * p.sp_ld + n0 + 4 * k) = x;
+              }
+              if (j < S - 1) {
+                if (lane == 0 && use_sum) {
+                  if (j == 0)
+                    ptx::tma_store_3d(&tmD2, buf, c * 32, rrow, it.tile);
+                  else
+                    ptx::tma_reduce_add_3d(&tmD2, buf, c * 32, rrow, it.tile);
+                  ptx::bulk_commit_group();
+                }
+                continue;
+              }
+              // last shard: Y = running sum + own accumulator, + bias, + residual
+              uint32_t sb[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) sb[e] = __float_as_uint(sum[e]);
+              float y[32], y2[32];
+              epilogue_values<EPI, ACT>(p, b, m, n0, sb, y, y2);
+              __syncwarp();  // the partial's rows are read out of the box
+              {
+                uint8_t* rowp = buf + lane * 64;  // 64-byte rows, 16-byte chunks rotated by (row / 2) % 4
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  *reinterpret_cast<uint4*>(rowp + ((k ^ ((lane >> 1) & 3)) << 4)) =
+                      make_uint4(pack_bf16x2(y[8 * k], y[8 * k + 1]), pack_bf16x2(y[8 * k + 2], y[8 * k + 3]),
+                                 pack_bf16x2(y[8 * k + 4], y[8 * k + 5]), pack_bf16x2(y[8 * k + 6], y[8 * k + 7]));
+              }
+              __syncwarp();
+              uint16_t* Y = static_cast<uint16_t*>(p.d);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {  // rows 8 i .. 8 i + 7, 16 bytes a lane
+                const int row = 8 * i + (lane >> 2), k = lane & 3;
+                const uint4 x = *reinterpret_cast<const uint4*>(buf + row * 64 + ((k ^ ((row >> 1) & 3)) << 4));
+                if (mrow0 + row < p.M && n0 + 8 * k < p.N)
+                  *reinterpret_cast<uint4*>(Y + static_cast<int64_t>(mrow0 + row) * p.ldd + n0 + 8 * k) = x;
+              }
+              if (load_sum && c + 2 < nch) {  // the box takes the running sum two chunks on
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                  ptx::mbar_arrive_expect_tx(&ebar[quad * 2 + (c & 1)], STG_BOX_BYTES);
+                  ptx::tma_load_3d(buf, &tmD2, &ebar[quad * 2 + (c & 1)], (c + 2) * 32, rrow, it.tile);
+                }
+              }
             }
-            __syncwarp();
+            if (use_sum) {
+              ovl_flag = flag;  // next shard may add (or, after the last, reset for the next launch)
+              ovl_set = (j < S - 1) ? (ep | static_cast<unsigned long long>(j + 1)) : 0ull;
+            }
           }
         }
+      }
+      if (!ovl_item && SK_OK && it.kind == ITEM_RANGE && mrow0 < p.M) {
+        if (lane == 0) ptx::bulk_wait_group_read<0>();  // the staging boxes are free
+        __syncwarp();
+#pragma unroll 1
+        for (int c = 0; c < P_BN / 32; ++c) {
+          if (nb * P_BN + c * 32 >= p.N) break;  // warp-uniform
+          uint8_t* buf = stg + (c & 1) * STG_BOX_BYTES;
+          if (c >= 2) {
+            if (lane == 0) ptx::bulk_wait_group_read<1>();
+            __syncwarp();
+          }
+          uint32_t r[32];
+          ptx::tmem_ld32(t_row + c * 32, r);
+          ptx::tmem_ld_wait();
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          stage_row32(buf, lane, v);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (p.sp_user)
+              ptx::tma_store_3d(&tmP, buf, nb * P_BN + c * 32, mrow0, it.range);
+            else
+              ptx::tma_store_3d(&tmP, buf, c * 32, static_cast<int>(rank) * P_HALF + quad * 32,
+                                it.st * p.sp_split + it.range);
+            ptx::bulk_commit_group();
+          }
+        }
+        int last = 0;
+        if (lane == 0) {
+          ptx::bulk_wait_group<0>();  // the partial is in global memory
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          __threadfence();
+          last = sp_arrive(p, p.sp_cnt + (static_cast<int64_t>(it.st) * 2 + rank) * 4 + quad, abort_flag) ? 1 : 0;
+        }
+        sp_last = __shfl_sync(0xffffffffu, last, 0) != 0;
+        if (sp_last) __threadfence();  // every lane reads the ranges' partials after the count
+      }
+      if (ovl_item || it.kind == ITEM_RANGE) {
+        // partial written (or rows past M); a completing range sums the tile below, after the
+        // accumulator is handed back
       } else if constexpr (EPI == EPI_GLU) {
         // The tile is one gate / up group (N is a multiple of 256).  Per 64 hidden columns:
         // Z's gate box, Z's up box (when Z is kept) and the activation box, three TMA stores.
@@ -1637,7 +1708,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
             uint32_t r[32];
             ptx::tmem_ld32(t_row + g0 + h * 32, r);
             ptx::tmem_ld_wait();
-            if (SK_OK && sk_parts > 0) sk_add_partials(p, r, cluster, sk_parts, trow, g0 + h * 32);
             float v[32], v2[32];
             epilogue_values<EPI, ACT>(p, b, m, n0 + h * 32, r, v, v2);
             if (wide) {
@@ -1670,41 +1740,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<OVL>(),
       ptx::mbar_arrive_cluster(tempty_leader0 + static_cast<uint32_t>(acc * sizeof(uint64_t)));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
-      if (SK_OK && sk_parts > 0 && lane == 0) {  // consumed: ready for the next launch
-        for (int jj = 1; jj <= sk_parts; ++jj)
-          p.sk_flag[(static_cast<int64_t>(cluster + jj * p.sk_tiles) * 2 + rank) * 4 + quad] = 0;
+      if (ovl_flag && lane == 0) {  // with the accumulator handed back: the adds complete, then the flag
+        ptx::bulk_wait_group<0>();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __threadfence();
+        ptx::st_release_u64(reinterpret_cast<uint64_t*>(ovl_flag), ovl_set);
       }
-      if constexpr (OVL) {
-        // The accumulator is already handed back, so the next tile's MMAs run
-        // while this warp counts its partial and, if it completed the block's
-        // set of shards, queues the block for the reducer warps.
-        if (lane == 0) {
-          if (mrow0 < p.M) {
-            ptx::bulk_wait_group<0>();  // this warp's partial stores are complete in global memory
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            __threadfence();
-            const int64_t block = ((static_cast<int64_t>(nb) * mt2 + mb) * 2 + rank) * 4 + quad;
-            if (atomicAdd(p.ovl_cnt + block, 1) == p.nbatch - 1) {
-              __threadfence();
-              ovl_post(ovl_queue(p, mt2, nt2), block, mrow0, nb);
-            }
-          }
-        }
-        __syncwarp();
+      if constexpr (SK_OK) {
+        if (sp_last) sp_reduce_rows<EPI, ACT>(p, it, b, mrow0, trow - lane, nb, lane);
       }
     }
     if (lane == 0) ptx::bulk_wait_group<0>();  // every output written before the CTA exits
-    if constexpr (OVL) {
-      if (lane == 0) {
-        __threadfence();  // this warp's posts are in the queue's tail before it signs off
-        atomicAdd(const_cast<int*>(ovl_s + 3), 1);
-      }
-      __syncwarp();
-      // with its tiles done, the epilogue group becomes a second reducer group
-      ptx::named_bar_sync(OVL_BAR + 1, 128);
-      ovl_reduce_loop(p, ovl_queue(p, mt2, nt2), ovl_s + 4, ovl_s + 3, abort_flag, quad == 0, OVL_BAR + 1,
-                      quad * OVL_ROWS, lane);
-    }
   }
 
   __syncwarp();
@@ -1859,19 +1905,19 @@ tp_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a
 }
 
 // Clusters of the pair kernel that can be resident at once on this device.
-template <bool A_MN, bool B_MN, int EPI, int ACT, bool OVL = false>
+template <bool A_MN, bool B_MN, int EPI, int ACT>
 int pair_clusters(int dev) {
   static int cached[64] = {};
   if (cached[dev] > 0) return cached[dev];
-  if (cudaFuncSetAttribute(gemm_pair_kernel<A_MN, B_MN, EPI, ACT, OVL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           pair_smem_bytes<EPI, OVL>()) != cudaSuccess)
+  if (cudaFuncSetAttribute(gemm_pair_kernel<A_MN, B_MN, EPI, ACT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           pair_smem_bytes<EPI>()) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * 256, 1, 1);
-  cfg.blockDim = dim3(pair_threads<OVL>(), 1, 1);
-  cfg.dynamicSmemBytes = pair_smem_bytes<EPI, OVL>();
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = pair_smem_bytes<EPI>();
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<A_MN, B_MN, EPI, ACT, OVL>, &cfg) != cudaSuccess || n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<A_MN, B_MN, EPI, ACT>, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
     n = device_sm_count() / 2;
   }
@@ -1879,88 +1925,137 @@ int pair_clusters(int dev) {
   return n;
 }
 
-// Split-K plan of a pair-kernel launch: T tiles of U k-stages on nc resident clusters.  With
-// fewer tiles than clusters the data-parallel schedule leaves nc - T clusters idle; cutting
-// every tile into S = nc / T equal k-ranges (the same cut points for every tile) puts up to
-// S T clusters to work, and the clusters on one range still walk the same k-slices together,
-// so operand slices shared between tiles come through L2 once.  Ranges keep at least
-// kSkMinUnits k-stages and the workspace bounds the clusters that write partials.
-// (Contiguous stream-K ranges were measured first and lost: ranges that start at staggered
-// k break that lockstep -- the 2048 x 4096 x 16384 row-parallel GEMM, 128 tiles on 76
-// clusters, read 575 MB from DRAM against 276 MB and ran 185 us against 167 us, and a
-// 32-tile one ran 109 us against 87 us.)  TP_STREAMK=0 turns the split off.
+// Split-K plan of a pair-kernel launch: T tiles of U k-stages on nc resident clusters.  The
+// data-parallel schedule takes ceil(T / nc) rounds of whole tiles, the last one with only
+// T mod nc clusters busy.  Here the full rounds stay whole and the remaining tiles are cut
+// into S equal k-ranges (the same cut points for every tile), dealt to all the clusters:
+// ceil(rem S / nc) items of U / S stages instead of one more round of U, plus the completing
+// range's sum of the S partials.  That sum reads about 16 GB/s per SM (generic loads, with
+// the stages holding nearly all shared memory: 8 us per 128 KB partial of a CTA, measured),
+// about kSkSumStages k-stages per range.  S is the cut that finishes first by this count;
+// ties keep fewer partials; a cut that saves less than kSkMinGain is not taken.  Ranges keep
+// at least kSkMinUnits k-stages, and the workspace bounds the partial slots.  (Contiguous
+// stream-K ranges were measured first and lost: ranges that start at staggered k break the
+// clusters' lockstep -- the 2048 x 4096 x 16384 row-parallel GEMM, 128 tiles on 76 clusters,
+// read 575 MB from DRAM against 276 MB and ran 185 us against 167 us, and a 32-tile one ran
+// 109 us against 87 us.)  TP_STREAMK=0 turns the split off.
 constexpr int kSkMinUnits = 8;
+constexpr int kSkSumStages = 10;
+constexpr double kSkMinGain = 0.1;
 bool make_output_map(CUtensorMap* map, void* d, CUtensorMapDataType dt, int esz, int64_t N, int64_t M, int nbatch,
                      int64_t ldd, int64_t dbs);
-struct SkPlan {
-  int tiles = 0, split = 0;
+struct SpPlan {
+  int rounds = 0, tiles = 0, split = 0, clusters = 0;
 };
-SkPlan sk_plan(int64_t T, int U, int nc, int max_slots) {
-  SkPlan pl;
+SpPlan sp_plan(int64_t T, int U, int nc, int64_t max_slots) {
+  SpPlan pl;
   const char* e = std::getenv("TP_STREAMK");
-  if ((e && e[0] == '0') || T <= 0 || U <= 0 || T * 2 > nc) return pl;
-  int64_t S = nc / T;
-  if (S > U / kSkMinUnits) S = U / kSkMinUnits;
-  if (S * T > max_slots) S = max_slots / T;
-  if (S < 2) return pl;
-  pl.tiles = static_cast<int>(T);
-  pl.split = static_cast<int>(S);
+  if ((e && e[0] == '0') || T <= 0 || U <= 0 || nc <= 0) return pl;
+  const int64_t R = T / nc, rem = T - R * nc;
+  if (rem == 0) return pl;
+  const double whole = static_cast<double>((R + 1) * U);
+  double best = whole;
+  int bestS = 0;
+  for (int S = 2; U / S >= kSkMinUnits && rem * S <= max_slots; ++S) {
+    const double tm = static_cast<double>(R * U) + static_cast<double>((rem * S + nc - 1) / nc) * U / S +
+                      static_cast<double>(S) * kSkSumStages;
+    if (tm < best - 1e-9) {
+      best = tm;
+      bestS = S;
+    }
+  }
+  if (bestS == 0 || best > whole * (1.0 - kSkMinGain)) return pl;
+  pl.rounds = static_cast<int>(R);
+  pl.tiles = static_cast<int>(rem);
+  pl.split = bestS;
+  pl.clusters = R > 0 ? nc : static_cast<int>(rem * bestS < nc ? rem * bestS : nc);
   return pl;
 }
 
-// Launch order of the split-K flags: a value no earlier launch with the same workspace used
-// (the flags are cleared when consumed, and a fresh workspace would have to hold this exact
-// 64-bit value by chance).
-uint64_t next_sk_epoch() {
-  static std::atomic<uint64_t> ctr{(static_cast<uint64_t>(std::time(nullptr)) << 32) ^
-                                   reinterpret_cast<uintptr_t>(&ctr)};
-  uint64_t v;
+// Launch tag of the split-K counters: a value no recent launch used (counters are reset by
+// the range that completes them, and a fresh workspace would have to hold this exact value
+// in a counter's upper half by chance).
+uint32_t next_sp_epoch() {
+  static std::atomic<uint32_t> ctr{static_cast<uint32_t>(std::time(nullptr)) ^
+                                   static_cast<uint32_t>(reinterpret_cast<uintptr_t>(&ctr) >> 4)};
+  uint32_t v;
   do {
-    v = ctr.fetch_add(0x9E3779B97F4A7C15ull);
+    v = ctr.fetch_add(0x9E3779B9u);  // odd step: every 32-bit value once per 2^32 launches
   } while (v == 0);
   return v;
 }
 
-template <bool A_MN, bool B_MN, int EPI, int ACT, bool OVL = false>
+// The completing range of a split tile writes its outputs with 16-byte accesses of 8 columns.
+bool sp_layout_ok(const GemmArgs& a) {
+  auto al = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+  if (a.N % 8 != 0 || !al(a.d) || !al(a.d2) || !al(a.bias) || !al(a.res) || !al(a.aux) || !al(a.cs)) return false;
+  return a.ldd % 8 == 0 && a.d_bs % 8 == 0 && a.ld_res % 8 == 0 && a.ld_aux % 8 == 0 && a.aux_bs % 8 == 0 &&
+         a.bias_bs % 8 == 0;
+}
+
+// Overlapped shard reduction (ovl_part != NULL): the tiles' K ranges are the t shards, every
+// shard's fp32 partial goes to ovl_part [t][M][N], and ovl_run holds a 256 x 256 fp32 running
+// sum per output tile followed by 8 flags per tile (gemm_overlap_scratch_bytes).
+template <bool A_MN, bool B_MN, int EPI, int ACT>
 tp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const CUtensorMap& td2,
                       const GemmArgs& a0, int64_t tiles, cudaStream_t s, void* sk_ws = nullptr,
-                      size_t sk_ws_bytes = 0) {
+                      size_t sk_ws_bytes = 0, float* ovl_part = nullptr, float* ovl_run = nullptr) {
   int dev = 0;
   TP_CUDA_CHECK(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return TP_ERR_CUDA;
-  const int nc = pair_clusters<A_MN, B_MN, EPI, ACT, OVL>(dev);
+  const int nc = pair_clusters<A_MN, B_MN, EPI, ACT>(dev);
   if (nc <= 0) return TP_FAIL_DETAIL("no co-resident CTA pairs");
   int clusters = static_cast<int>(tiles < nc ? tiles : nc);
   GemmArgs a = a0;
-  CUtensorMap tp_map;
+  CUtensorMap tp_map, run_map;
   std::memset(&tp_map, 0, sizeof(tp_map));
-  if (sk_epi(EPI) && !OVL && sk_ws) {
-    const int U = a.nsum * ((a.kt + PairCfg<EPI>::kb - 1) / PairCfg<EPI>::kb);
-    const int slots = static_cast<int>(sk_ws_bytes / (kSkSlotBytes + kSkFlagBytes));
-    const SkPlan pl = sk_plan(tiles, U, nc, slots < kSkMaxClusters ? slots : kSkMaxClusters);
-    if (pl.tiles > 0) {
-      const int used = pl.tiles * pl.split;  // clusters (and partial slots, first ranges included)
-      a.sk_tiles = pl.tiles;
-      a.sk_units = U;
-      a.sk_split = pl.split;
-      a.sk_part = static_cast<float*>(sk_ws);
-      a.sk_flag = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(sk_ws) + static_cast<size_t>(used) * kSkSlotBytes);
-      a.sk_epoch = next_sk_epoch();
-      if (!make_output_map(&tp_map, a.sk_part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 256, 256, used, 256, 256 * 256))
-        return TP_FAIL_DETAIL("tensor map of the split-K partials");
-      clusters = used;
+  std::memset(&run_map, 0, sizeof(run_map));
+  const int U = a.nsum * ((a.kt + PairCfg<EPI>::kb - 1) / PairCfg<EPI>::kb);
+  if constexpr (sk_epi(EPI)) {
+    if (ovl_part) {
+      // every tile cut at its shard boundaries, one cluster walking a tile's shards in turn
+      if constexpr (EPI != EPI_BF16) return TP_ERR_UNSUPPORTED;
+      if (!sp_layout_ok(a)) return TP_ERR_ALIGN;
+      clusters = static_cast<int>(tiles * a.nsum < nc ? tiles * a.nsum : nc);
+      a.sp_split = a.nsum;
+      a.sp_units = U;
+      a.sp_seq = 1;
+      a.sp_user = 1;
+      a.sp_part = ovl_part;
+      a.sp_ld = a.N;
+      a.sp_bs = static_cast<int64_t>(a.M) * a.N;
+      if (!make_output_map(&tp_map, ovl_part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.N, a.M, a.nsum, a.N, a.sp_bs))
+        return TP_FAIL_DETAIL("tensor map of the shard partials");
+      if (!make_output_map(&run_map, ovl_run, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 256, 256, static_cast<int>(tiles),
+                           256, 256 * 256))
+        return TP_FAIL_DETAIL("tensor map of the running sums");
+      a.sp_cnt = reinterpret_cast<unsigned long long*>(ovl_run + static_cast<size_t>(tiles) * 256 * 256);
+      a.sp_epoch = next_sp_epoch();
+    } else if (sk_ws && sp_layout_ok(a)) {
+      int64_t slots = static_cast<int64_t>(sk_ws_bytes / (kSkSlotBytes + kSkCounterBytes));
+      if (slots > kSkMaxSlots) slots = kSkMaxSlots;
+      const SpPlan pl = sp_plan(tiles, U, nc, slots);
+      if (pl.split > 0) {
+        const int used = pl.tiles * pl.split;  // partial slots
+        a.sp_rounds = pl.rounds;
+        a.sp_tiles = pl.tiles;
+        a.sp_split = pl.split;
+        a.sp_units = U;
+        a.sp_part = static_cast<float*>(sk_ws);
+        a.sp_cnt = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(sk_ws) +
+                                                         static_cast<size_t>(used) * kSkSlotBytes);
+        a.sp_epoch = next_sp_epoch();
+        if (!make_output_map(&tp_map, a.sp_part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 256, 256, used, 256, 256 * 256))
+          return TP_FAIL_DETAIL("tensor map of the split-K partials");
+        clusters = pl.clusters;
+      }
     }
+  } else if (ovl_part) {
+    return TP_ERR_UNSUPPORTED;
   }
-  if constexpr (OVL) {
-    gemm_pair_kernel<A_MN, B_MN, EPI, ACT, OVL>
-        <<<2 * clusters, pair_threads<OVL>(), pair_smem_bytes<EPI, OVL>(), s>>>(ta, tb, td, td2, tp_map, a);
-    TP_LAUNCHED();
-  } else {
-    TP_CUDA_CHECK(launch_pdl(gemm_pair_kernel<A_MN, B_MN, EPI, ACT, OVL>, dim3(2 * clusters),
-                             dim3(pair_threads<OVL>()), pair_smem_bytes<EPI, OVL>(), s, ta, tb, td, td2, tp_map,
-                             a));
-    count_launch();
-  }
+  TP_CUDA_CHECK(launch_pdl(gemm_pair_kernel<A_MN, B_MN, EPI, ACT>, dim3(2 * clusters), dim3(NUM_THREADS),
+                           pair_smem_bytes<EPI>(), s, ta, tb, td, ovl_part ? run_map : td2, tp_map, a));
+  count_launch();
   return TP_OK;
 }
 
@@ -2176,19 +2271,14 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
 
   TP_RETURN_IF(ready());
   const bool pair = use_pair(P.M);
-  if (P.ovl_cnt) {
-    // overlapped reduction: pair kernel, fp32 shard partials written by TMA, t <= 8
-    if (!pair || P.epi != EPI_F32 || P.accumulate || !P.ovl_y) return TP_ERR_UNSUPPORTED;
-    if (P.nbatch != 1 && P.nbatch != 2 && P.nbatch != 4 && P.nbatch != 8) return TP_ERR_UNSUPPORTED;
-    if (!aligned16(P.ovl_y) || P.ovl_ld % 8 != 0 || (P.ovl_bias && !aligned16(P.ovl_bias)) ||
-        (P.ovl_res && !aligned16(P.ovl_res)))
-      return TP_ERR_ALIGN;
-    TP_CUDA_CHECK(
-        cudaMemsetAsync(P.ovl_cnt, 0, static_cast<size_t>(gemm_overlap_counters(P.M, P.N)) * sizeof(int), s));
+  if (P.ovl_part) {
+    // overlapped reduction: pair kernel, the nsum shards' fp32 partials written by TMA
+    if (!pair || P.epi != EPI_BF16 || P.accumulate || P.nbatch != 1 || !P.ovl_run) return TP_ERR_UNSUPPORTED;
+    if (!aligned16(P.ovl_part) || !aligned16(P.ovl_run)) return TP_ERR_ALIGN;
   }
   CUtensorMap ta, tb;
   int a_4d = 0, b_4d = 0;
-  const int kb = pair ? pair_kb(P.ovl_cnt ? static_cast<int>(EPI_F32) : P.epi) : 1;  // k-blocks per stage
+  const int kb = pair ? pair_kb(P.epi) : 1;  // k-blocks per stage
   if (!make_operand_map(&ta, P.a, P.M, P.K, nsh_a, BM, kb, &a_4d)) return TP_ERR_CUDA;
   if (!make_operand_map(&tb, P.b, P.N, P.K, nsh_b, pair ? P_HALF : BN, kb, &b_4d)) return TP_ERR_CUDA;
 
@@ -2224,11 +2314,6 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
   a.ld_res = P.ld_res;
   a.accumulate = P.accumulate;
   a.out_f16 = P.out_f16;
-  a.ovl_cnt = P.ovl_cnt;
-  a.ovl_y = P.ovl_y;
-  a.ovl_bias = P.ovl_bias;
-  a.ovl_res = P.ovl_res;
-  a.ovl_ld = P.ovl_ld;
   a.ksplit = 1;
   a.err = device_error_word();
   a.timeout_ns = wait_timeout_ns();
@@ -2265,11 +2350,12 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
       }
     }
     const int64_t ptiles = ((P.M + 255) / 256) * ((P.N + P_BN - 1) / P_BN) * P.nbatch;
-    if (P.ovl_cnt) {  // its own instantiation: the other kernels keep their registers
-      if (amn || bmn || P.act != TP_ACT_IDENTITY) return TP_ERR_UNSUPPORTED;
-      return launch_pair<false, false, EPI_F32, TP_ACT_IDENTITY, true>(ta, tb, td, td2, a, ptiles, s);
+    if (P.ovl_part) {
+      if (amn || bmn || !a.tma_store) return TP_ERR_UNSUPPORTED;
+      return launch_pair<false, false, EPI_BF16, TP_ACT_IDENTITY>(ta, tb, td, td2, a, ptiles, s, nullptr, 0,
+                                                                   P.ovl_part, P.ovl_run);
     }
-    // Stream-K needs the TMA-store epilogue and a 256-byte aligned workspace.
+    // Split K needs the TMA-store epilogue and a 256-byte aligned workspace.
     void* sk_ws = (P.sk_ws && a.tma_store && (reinterpret_cast<uintptr_t>(P.sk_ws) & 255u) == 0) ? P.sk_ws : nullptr;
     return dispatch(amn, bmn, P.epi, P.act, [&](auto am, auto bm, auto ep, auto ac) {
       return launch_pair<decltype(am)::value, decltype(bm)::value, decltype(ep)::value, decltype(ac)::value>(

@@ -119,33 +119,33 @@ struct GemmProblem {
   int64_t ld_res = 0;
   int accumulate = 0;
   int out_f16 = 0;  // EPI_ACT only: write D / D2 as IEEE fp16 instead of bf16
-  // Overlapped shard reduction (EPI_F32, nbatch = t shard partials D[b]): while later tiles
-  // compute, the t partials of each finished block are summed in shard order, the bias added
-  // once and the residual after it, into ovl_y (bf16, row stride ovl_ld).  ovl_cnt: scratch of
-  // gemm_overlap_counters(M, N) ints (zeroed by the launch).
-  int* ovl_cnt = nullptr;
-  uint16_t* ovl_y = nullptr;
-  const uint16_t* ovl_bias = nullptr;
-  const uint16_t* ovl_res = nullptr;
-  int64_t ovl_ld = 0;
-  // Stream-K workspace (nullable, 256-byte aligned): lets the CTA-pair kernel split the
-  // k-stages of the tiles past its last full wave over every cluster (BF16, ACT, F32 without
-  // accumulate, DACT epilogues).  gemm_sk_ws_bytes() bytes cover any device; less limits
-  // how many clusters share that work.
+  // Overlapped shard reduction (CTA-pair kernel, EPI_BF16, nbatch = 1, nsum = t shards):
+  // each tile's t shard K ranges are separate work items (shard-major order), whose fp32
+  // partials P_i go to ovl_part [t][M][N] (the data a multi-GPU run would
+  // exchange) and are summed in shard order in an fp32 running sum per tile (ovl_run:
+  // gemm_overlap_scratch_bytes(M, N) bytes, 16-byte aligned, any contents) while the tensor
+  // cores go on; the last shard adds its accumulator, then the epilogue adds the bias once
+  // and the residual after it.
+  float* ovl_part = nullptr;
+  float* ovl_run = nullptr;
+  // Split-K workspace (nullable, 256-byte aligned): lets the CTA-pair kernel cut the tiles
+  // past its last full round into K ranges dealt to every cluster (BF16, ACT, F32 without
+  // accumulate, DACT epilogues).  gemm_sk_ws_bytes() bytes cover any plan; less limits the
+  // ranges.
   void* sk_ws = nullptr;
   size_t sk_ws_bytes = 0;
 };
-// Stream-K workspace: per participating cluster a 256 x 256 fp32 partial and its 8 flags.
-constexpr int kSkMaxClusters = 128;
+// Split-K workspace: up to kSkMaxSlots 256 x 256 fp32 partials, then per split tile 8
+// counters of 8 bytes (kSkCounterBytes per slot over-provisions them).
+constexpr int64_t kSkMaxSlots = 256;
 constexpr size_t kSkSlotBytes = 256 * 256 * 4;
-constexpr size_t kSkFlagBytes = 8 * 8;
-inline size_t gemm_sk_ws_bytes() { return kSkMaxClusters * (kSkSlotBytes + kSkFlagBytes); }
-// Scratch ints of the overlapped reduction: 8 block counters per 256x256
-// output tile, 32 queue heads and 32 tails on 128-byte lines, and 32 rings of
-// ceil(blocks / 32) 4-int entries.
-inline int64_t gemm_overlap_counters(int64_t M, int64_t N) {
-  const int64_t blocks = ((M + 255) / 256) * ((N + 255) / 256) * 8;
-  return blocks + 64 * 32 + 32 * ((blocks + 31) / 32) * 4;
+constexpr size_t kSkCounterBytes = 8 * 8;
+inline size_t gemm_sk_ws_bytes() { return kSkMaxSlots * (kSkSlotBytes + kSkCounterBytes); }
+// Scratch of the overlapped reduction: a 256 x 256 fp32 running sum per output tile, then 8
+// flags of 8 bytes (two CTAs x four warps) per tile.
+inline size_t gemm_overlap_scratch_bytes(int64_t M, int64_t N) {
+  const int64_t tiles = ((M + 255) / 256) * ((N + 255) / 256);
+  return static_cast<size_t>(tiles) * (256 * 256 * 4 + 64);
 }
 
 tp_status run_gemm(const GemmProblem& p, cudaStream_t s);

@@ -47,9 +47,9 @@ def test_version_and_strings():
 
 
 def test_workspace_sizes():
-    # forward: the flags' partials, then room for the GEMMs' stream-K partials (256 KB per
-    # cluster of up to 128, plus 64 bytes of flags each)
-    sk = 128 * (256 * 256 * 4 + 64)
+    # forward: the flags' partials, then room for the GEMMs' split-K partials (256 KB per
+    # slot of up to 256, plus 64 bytes of counters each)
+    sk = 256 * (256 * 256 * 4 + 64)
     assert L.tp_mlp_workspace_size(2048, 4096, 16384, 4, 0) == sk
     assert L.tp_mlp_workspace_size(2048, 4096, 16384, 4, L.TP_FLAG_UNFUSED_REDUCE) == 4 * 2048 * 4096 * 4 + sk
     assert L.tp_row_parallel_workspace_size(2048, 16384, 4096, 4) == sk
@@ -62,6 +62,12 @@ def test_workspace_sizes():
         need = M * F * 2 * 2 + t * ((M + 31) // 32) * (F // t) * 4 + ((M + 255) // 256) * h * 4
         assert L.tp_mlp_backward_workspace_size(M, h, F, t, 0) >= need, (M, h, F, t)
     assert L.tp_colsum_workspace_size(2048, 4096) == 32 * 4096 * 4
+    # overlapped reduction: the t partials [t][M][h] fp32, then per 256 x 256 output tile an
+    # fp32 running sum and 8 flags of 8 bytes
+    assert L.tp_row_parallel_overlap_workspace_size(2048, 16384, 4096, 4) == \
+        4 * 2048 * 4096 * 4 + 128 * (256 * 256 * 4 + 64)
+    assert L.tp_row_parallel_overlap_workspace_size(300, 1024, 264, 3) == \
+        (3 * 300 * 264 * 4 + 255) // 256 * 256 + 4 * (256 * 256 * 4 + 64)
 
 
 def test_host_validation_without_device():

@@ -1,16 +1,16 @@
-"""Split K across CTA pairs for GEMMs with fewer output tiles than CTA pairs, against
-the fp64 oracle through the C ABI.
+"""Split K across CTA pairs, against the fp64 oracle through the C ABI.
 
-With a workspace, each 256 x 256 output tile's k-stages are cut into S equal ranges (the
-same cut points for every tile), one CTA pair per range.  A range other than the first
-leaves its fp32 partial in the workspace and raises flags; the first range waits for
-them, adds the partials in k order and applies the epilogue.  Covered here: the
-row-parallel GEMM with its fused shard sum (ranges that cross shard boundaries, ragged
-M, N and K), the column-parallel GEMM with each activation, the backward's dgrad (with
-the fused bias-gradient partials), both wgrads and the f-reduced dX, a workspace that
-holds only a few partials (fewer ranges), a problem with more tiles than CTA pairs (no
-split), determinism, CUDA-graph replay with new inputs between replays (the flags are
-cleared when consumed), and guard bytes around the workspace and every output.
+With a workspace, the tiles past the pair kernel's last full round of whole tiles (all
+tiles, when there are fewer tiles than CTA pairs) may be cut into S equal K ranges at the
+same k-stages, dealt to every pair, when the plan's time model says it pays (long K, few
+tiles).  Each range leaves its fp32 partial in the workspace and counts itself; the range
+that completes a tile's count adds the partials in range order and applies the epilogue.
+Covered here: the row-parallel GEMM with its fused shard sum (ranges that cross shard
+boundaries, ragged M, N and K; shapes the plan keeps whole), the column-parallel GEMM with
+each activation, the backward's dgrad (with the fused bias-gradient partials), both
+wgrads and the f-reduced dX, a workspace that holds only a few partials (fewer ranges),
+determinism, CUDA-graph replay with new inputs between replays (the counters reset
+themselves), and guard bytes around the workspace and every output.
 Criterion: max|gpu - oracle| <= 1e-2 * max|oracle| per output.
 """
 
@@ -27,7 +27,7 @@ from gpu_helpers import Guarded, assert_close, f64, guarded_ws
 
 pytestmark = pytest.mark.gpu
 
-SK_BYTES = 128 * (256 * 256 * 4 + 64)
+SK_BYTES = 256 * (256 * 256 * 4 + 64)
 
 
 def _case(M, h, F, t, seed, bias=True):
@@ -38,10 +38,11 @@ def _case(M, h, F, t, seed, bias=True):
 
 
 @pytest.mark.parametrize("M,h,F,t", [
-    (1000, 1536, 2048, 4),   # 24 tiles: every tile's 16 k-stages in 2 ranges
-    (520, 1032, 1568, 4),    # ragged M (3 row tiles), N (1032 = 4 x 256 + 8), K (392 per shard)
-    (300, 1024, 16384, 4),   # 8 tiles, 128 k-stages: up to 9 ranges, boundaries inside shards
-    (2048, 4096, 8192, 4),   # 128 tiles, more than CTA pairs: whole tiles
+    (1000, 1024, 16384, 4),  # 16 tiles, 128 k-stages: 4 ranges, one per shard
+    (520, 1032, 15680, 4),   # ragged M (3 row tiles), N (1032 = 4 x 256 + 8), K (3920 per shard)
+    (300, 1024, 16384, 4),   # 8 tiles, 128 k-stages: 4 ranges
+    (272, 776, 24576, 3),    # 8 tiles, t = 3: range boundaries inside shards
+    (2048, 4096, 8192, 4),   # 128 tiles, more than CTA pairs: whole tiles (a split would not pay)
 ])
 def test_row_parallel_streamk_matches_oracle(M, h, F, t):
     dev, ref, w = _case(M, h, F, t, seed=60 + t)
@@ -68,7 +69,7 @@ def test_row_parallel_streamk_matches_oracle(M, h, F, t):
 
 @pytest.mark.parametrize("act", ["identity", "relu", "gelu_tanh", "gelu_erf"])
 def test_column_parallel_streamk_activations(act):
-    M, h, F, t = 600, 2056, 2560, 2       # 3 x 5 x 2 = 30 tiles, 33 k-blocks (ragged): 2 ranges each
+    M, h, F, t = 600, 8200, 1024, 2       # 3 x 2 x 2 = 12 tiles, 129 k-blocks (ragged K): 4 ranges
     dev, ref, w = _case(M, h, F, t, seed=63)
     nws = L.tp_column_parallel_workspace_size(M, h, F, t)
     ws = guarded_ws(nws)
@@ -83,9 +84,9 @@ def test_column_parallel_streamk_activations(act):
     assert_close("A", f64(A.t), np.stack(o["A"]))
 
 
-@pytest.mark.parametrize("M,h,F,t", [(1000, 1536, 2048, 4),   # dX split
+@pytest.mark.parametrize("M,h,F,t", [(1000, 1024, 16384, 4),  # dX split
                                      (400, 4096, 1024, 2),    # dgrad * act' (and its db_up partials) split
-                                     (4096, 512, 1024, 2)])   # both weight gradients split
+                                     (16384, 512, 1024, 2)])  # both weight gradients split
 def test_mlp_backward_streamk(M, h, F, t):
     """dgrad * act' with the fused db_up partials, both weight gradients and the f-reduced
     dX, with K split across CTA pairs where their tiles are few."""
@@ -113,10 +114,11 @@ def test_mlp_backward_streamk(M, h, F, t):
     assert_close("db_down", f64(out["dbdown"].t), b["db_down"])
 
 
-@pytest.mark.parametrize("slots", [2, 5])
+@pytest.mark.parametrize("slots", [2, 32, 48])
 def test_partial_workspace_limits_the_clusters(slots):
-    """A workspace with room for only a few clusters' partials still gives the result."""
-    M, h, F, t = 1000, 1536, 2048, 4
+    """A workspace with room for only a few partials (16 tiles: none, two or three ranges
+    each) still gives the result."""
+    M, h, F, t = 1000, 1024, 16384, 4
     dev, ref, w = _case(M, h, F, t, seed=65)
     A = (torch.randn(t, M, F // t, generator=torch.Generator().manual_seed(66)) * 0.5).to(torch.bfloat16).cuda()
     nws = slots * (256 * 256 * 4 + 64)
@@ -132,9 +134,10 @@ def test_partial_workspace_limits_the_clusters(slots):
 
 def test_streamk_deterministic_and_graph_replay_with_new_inputs():
     """Same inputs, same bits; captured in a CUDA graph, each replay (with new inputs
-    written between replays) gives the eager result for those inputs -- the flags of one
-    replay do not satisfy the next one's waits."""
-    M, h, F, t = 1000, 1536, 2048, 4
+    written between replays) gives the eager result for those inputs -- every replay
+    repeats the counters' launch tag, and the counters start from zero because the range
+    that completes a count resets it."""
+    M, h, F, t = 1000, 1024, 16384, 4
     dev, ref, w = _case(M, h, F, t, seed=67)
     nws = L.tp_row_parallel_workspace_size(M, F, h, t)
     ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
