@@ -47,6 +47,38 @@ constexpr int FWD_THREADS = 320;  // TMA warp, MMA warp, two softmax warpgroups
 constexpr int KV_SLOTS = 5;       // K and V tiles share one ring
 constexpr int FWD_SMEM = 1024 + (2 + KV_SLOTS) * TILE + 256;
 constexpr float kLazyRescale = 8.0f;
+
+// Packed two-lane fp32 arithmetic (one instruction for two values) and a three-input
+// maximum: the softmax of an interior key block is bound by instruction issue, not by the
+// exponential unit, so these cut its instruction count per score.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -260,22 +292,34 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
       // Pass 1: the block's row maximum, 64 columns at a time (S stays in TMEM,
       // so a thread never holds the whole row: no register spills).
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      const bool plain = !NEG && !edge;  // interior block: no negation, no mask
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t r[2][32];
         ptx::tmem_ld32(tSb + lane_base + hf * 64, r[0]);
         ptx::tmem_ld32(tSb + lane_base + hf * 64 + 32, r[1]);
         ptx::tmem_ld_wait();
+        if (plain) {
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          const int c = hf * 64 + e;
-          float v = __uint_as_float(r[e >> 5][e & 31]);
-          if (NEG) v = -v;
-          if (edge && c > lim) v = -INFINITY;
-          mx4[e & 3] = fmaxf(mx4[e & 3], v);
+          for (int e = 0; e < 64; e += 8) {
+            const uint32_t* x = &r[e >> 5][e & 31];
+            mx4[0] = max3f(mx4[0], __uint_as_float(x[0]), __uint_as_float(x[1]));
+            mx4[1] = max3f(mx4[1], __uint_as_float(x[2]), __uint_as_float(x[3]));
+            mx4[2] = max3f(mx4[2], __uint_as_float(x[4]), __uint_as_float(x[5]));
+            mx4[3] = max3f(mx4[3], __uint_as_float(x[6]), __uint_as_float(x[7]));
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            const int c = hf * 64 + e;
+            float v = __uint_as_float(r[e >> 5][e & 31]);
+            if (NEG) v = -v;
+            if (edge && c > lim) v = -INFINITY;
+            mx4[e & 3] = fmaxf(mx4[e & 3], v);
+          }
         }
       }
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
+      const float mx = max3f(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3])) * sl2;
       const float m_new = (mx > m + kLazyRescale) ? mx : m;
       const float alpha = ptx::exp2_approx(m - m_new);  // 0 on the first block (m = -inf), 1 when m stays
       if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
@@ -295,8 +339,33 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
       // which pass 2 has already read (chunks 0 .. h), so nothing is overwritten early.
       const float neg_m = -m_new;
       float rs4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if (plain) {
+        // two scores per instruction: x = s scale - m and the running row sums, packed
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(neg_m, neg_m);
+        uint64_t rs2[2] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f)};
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
+        for (int h = 0; h < 4; ++h) {
+          uint32_t r[32];
+          ptx::tmem_ld32(tSb + lane_base + h * 32, r);
+          ptx::tmem_ld_wait();
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const uint64_t x2 =
+                f2_fma(f2_pack(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])), sl2x2, negm2);
+            float x0, x1;
+            f2_unpack(x2, x0, x1);
+            const float p0 = ptx::exp2_approx(x0), p1 = ptx::exp2_approx(x1);
+            rs2[e & 1] = f2_add(rs2[e & 1], f2_pack(p0, p1));
+            w[e] = pack_f16x2(p0, p1);
+          }
+          ptx::tmem_st16(tSb + lane_base + h * 16, w);
+        }
+        f2_unpack(rs2[0], rs4[0], rs4[1]);
+        f2_unpack(rs2[1], rs4[2], rs4[3]);
+      }
+#pragma unroll
+      for (int h = 0; h < (plain ? 0 : 4); ++h) {
         uint32_t r[32];
         ptx::tmem_ld32(tSb + lane_base + h * 32, r);
         ptx::tmem_ld_wait();
@@ -502,7 +571,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   uint8_t* sK = base;
   uint8_t* sV = base + TILE;
   uint8_t* sQd = base + 2 * TILE;  // stage s: Q_n at s * 2 TILE64, dO_n after it
-  float* sLD = reinterpret_cast<float*>(base + 2 * TILE + BWD_STAGES * 2 * TILE64);  // stage s: lse2[64], D[64]
+  float* sLD = reinterpret_cast<float*>(base + 2 * TILE + BWD_STAGES * 2 * TILE64);  // stage s: -lse2[64], -D[64]
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + 2 * TILE + BWD_STAGES * (2 * TILE64 + 512));
   uint64_t* kv_full = bars + 0;
   uint64_t* qd_full = bars + 1;                    // [BWD_STAGES] TMA bytes + 32 lse/D writers
@@ -589,9 +658,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int idx = lane + 32 * k, q = q0 + idx;
-        // A query row past the end gets lse = +inf: its P and dS are exactly 0.
-        ld[idx] = q < p.N ? p.lse[vec + q] * kLog2e : INFINITY;
-        ld[64 + idx] = q < p.N ? p.Dvec[vec + q] : 0.0f;
+        // Stored negated (the compute warps add them).  A query row past the end gets
+        // lse = +inf: its P and dS are exactly 0.
+        ld[idx] = q < p.N ? -(p.lse[vec + q] * kLog2e) : -INFINITY;
+        ld[64 + idx] = q < p.N ? -p.Dvec[vec + q] : 0.0f;
       }
       ptx::mbar_arrive(&qd_full[slot]);
       ++issued;
@@ -677,23 +747,47 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const float4* l2 = reinterpret_cast<const float4*>(sLD + slot * 128 + 32 * h);
       const float4* dd = reinterpret_cast<const float4*>(sLD + slot * 128 + 64 + 32 * h);
       uint32_t wp[16], wds[16];
+      if (!edge) {
+        // two columns per instruction: x = s scale - L, dP - D, P (dP - D), packed
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
-      for (int e4 = 0; e4 < 8; ++e4) {
-        const float4 L4 = l2[e4], D4 = dd[e4];
-        const float Lv[4] = {L4.x, L4.y, L4.z, L4.w}, Dv[4] = {D4.x, D4.y, D4.z, D4.w};
-        float pv[4], dv[4];
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 L4 = l2[e4], D4 = dd[e4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int e = 4 * e4 + u;
-          float pr = ptx::exp2_approx(fmaf(__uint_as_float(s[e]), sl2, -Lv[u]));
-          if (edge && c0 + e < kv) pr = 0.0f;
-          pv[u] = pr;
-          dv[u] = pr * (__uint_as_float(dp[e]) - Dv[u]);
+          for (int u2 = 0; u2 < 2; ++u2) {
+            const int e = 4 * e4 + 2 * u2;
+            const uint64_t nl2 = u2 ? f2_pack(L4.z, L4.w) : f2_pack(L4.x, L4.y);
+            const uint64_t nd2 = u2 ? f2_pack(D4.z, D4.w) : f2_pack(D4.x, D4.y);
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sl2x2, nl2), x0, x1);
+            const float p0 = ptx::exp2_approx(x0), p1 = ptx::exp2_approx(x1);
+            float d0, d1;
+            f2_unpack(f2_mul(f2_pack(p0, p1),
+                             f2_add(f2_pack(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd2)),
+                      d0, d1);
+            wp[2 * e4 + u2] = pack_f16x2(p0, p1);
+            wds[2 * e4 + u2] = pack_f16x2(d0, d1);
+          }
         }
-        wp[2 * e4] = pack_f16x2(pv[0], pv[1]);
-        wp[2 * e4 + 1] = pack_f16x2(pv[2], pv[3]);
-        wds[2 * e4] = pack_f16x2(dv[0], dv[1]);
-        wds[2 * e4 + 1] = pack_f16x2(dv[2], dv[3]);
+      } else {
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 L4 = l2[e4], D4 = dd[e4];
+          const float Lv[4] = {L4.x, L4.y, L4.z, L4.w}, Dv[4] = {D4.x, D4.y, D4.z, D4.w};
+          float pv[4], dv[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int e = 4 * e4 + u;
+            float pr = ptx::exp2_approx(fmaf(__uint_as_float(s[e]), sl2, Lv[u]));
+            if (c0 + e < kv) pr = 0.0f;
+            pv[u] = pr;
+            dv[u] = pr * (__uint_as_float(dp[e]) + Dv[u]);
+          }
+          wp[2 * e4] = pack_f16x2(pv[0], pv[1]);
+          wp[2 * e4 + 1] = pack_f16x2(pv[2], pv[3]);
+          wds[2 * e4] = pack_f16x2(dv[0], dv[1]);
+          wds[2 * e4 + 1] = pack_f16x2(dv[2], dv[3]);
+        }
       }
       ptx::tmem_st16(tSb, wp);
       ptx::tmem_st16(tdPb, wds);
@@ -869,16 +963,31 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const int lim = qlim - (j * 64 + 32 * h);  // columns e <= lim are visible keys
       const bool edge = lim < 31;
       uint32_t wds[16];
+      if (!edge) {
+        // two columns per instruction: x = s scale - lse, dP - D, P (dP - D), packed
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(-lse2, -lse2), nd2 = f2_pack(-Dq, -Dq);
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        float d2[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          float pr = ptx::exp2_approx(fmaf(__uint_as_float(s[e + u]), sl2, -lse2));
-          if (edge && e + u > lim) pr = 0.0f;
-          d2[u] = pr * (__uint_as_float(dp[e + u]) - Dq);
+        for (int e = 0; e < 32; e += 2) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sl2x2, nl2), x0, x1);
+          const float p0 = ptx::exp2_approx(x0), p1 = ptx::exp2_approx(x1);
+          float d0, d1;
+          f2_unpack(f2_mul(f2_pack(p0, p1), f2_add(f2_pack(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd2)),
+                    d0, d1);
+          wds[e >> 1] = pack_f16x2(d0, d1);
         }
-        wds[e >> 1] = pack_f16x2(d2[0], d2[1]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float d2[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            float pr = ptx::exp2_approx(fmaf(__uint_as_float(s[e + u]), sl2, -lse2));
+            if (e + u > lim) pr = 0.0f;
+            d2[u] = pr * (__uint_as_float(dp[e + u]) - Dq);
+          }
+          wds[e >> 1] = pack_f16x2(d2[0], d2[1]);
+        }
       }
       ptx::tmem_st16(tSb, wds);
       ptx::tmem_st_wait();
