@@ -102,9 +102,14 @@ struct GemmArgs {
   // added in L2 for the next ones, each after the previous shard's flag sp_cnt = epoch << 32
   // | j says its add is complete); the last shard adds its accumulator to the running sum
   // and applies the epilogue.
-  int sp_rounds, sp_tiles, sp_split, sp_units, sp_seq;
+  // Chained ranges (sp_chain, EPI_BF16): the ranges of a split tile add into the tile's fp32
+  // running sum in range order, as the shards do in the overlapped reduction, and no range
+  // writes a partial of its own: range 0 stores, the middle ranges add in L2, the last range
+  // loads the sum, adds its accumulator and applies the epilogue.  The overlapped reduction
+  // is the chained form with sp_seq and sp_user set.
+  int sp_rounds, sp_tiles, sp_split, sp_units, sp_seq, sp_chain;
   int sp_user;              // partials in the caller's [S][M][N] buffer, else 256 x 256 slots
-  float* sp_part;           // slots [split tiles * S][256][256], or the caller's buffer
+  float* sp_part;           // slots [split tiles * S][256][256], or the caller's buffer (unused when chained)
   int64_t sp_ld, sp_bs;     // sp_user: row and range strides in floats
   unsigned long long* sp_cnt;  // [split tiles][2 CTAs][4 warps]
   uint32_t sp_epoch;
@@ -1406,7 +1411,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tmD);
       ptx::tma_prefetch_desc(&tmD2);
-      if (SK_OK && p.sp_split > 0) ptx::tma_prefetch_desc(&tmP);
+      if (SK_OK && p.sp_split > 0 && !p.sp_chain) ptx::tma_prefetch_desc(&tmP);
     }
     uint32_t ephase = 0;  // phases of this warp's two running-sum load barriers (bits 0, 1)
     PairItem it;
@@ -1429,8 +1434,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       unsigned long long* ovl_flag = nullptr;  // set (to ovl_set) once this shard's adds are complete
       unsigned long long ovl_set = 0;
       if constexpr (EPI == EPI_BF16) {
-        if (p.sp_seq) {
-          // Overlapped shard reduction: shard j = it.range of tile it.tile.  Its fp32 partial is
+        if (p.sp_chain && it.kind == ITEM_RANGE) {
+          // Overlapped shard reduction: shard j = it.range of tile it.tile (the chained split
+          // K: range j of split tile it.st, with no partial of its own written).  Its fp32 partial is
           // staged 32 columns at a time in two alternating boxes; from a box it goes to the
           // caller's buffer with coalesced stores (a warp store covers four 128-byte rows; TMA
           // stores of these scattered rows held up the operand loads) and, by TMA, into the
@@ -1444,9 +1450,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           if (mrow0 < p.M) {
             const int S = p.sp_split, j = it.range;
             const int rrow = static_cast<int>(rank) * P_HALF + quad * 32;  // rows in the running sum
-            float* part = p.sp_part + j * p.sp_bs;
+            float* part = p.sp_user ? p.sp_part + j * p.sp_bs : nullptr;
             const unsigned long long ep = static_cast<unsigned long long>(p.sp_epoch) << 32;
-            unsigned long long* flag = p.sp_cnt + (static_cast<int64_t>(it.tile) * 2 + rank) * 4 + quad;
+            unsigned long long* flag = p.sp_cnt + (static_cast<int64_t>(it.st) * 2 + rank) * 4 + quad;
             if (lane == 0) ptx::bulk_wait_group<0>();
             int use_sum = 1;  // this shard touches the running sum (0 after a failed wait: result void)
             if (j > 0 && lane == 0) use_sum = sp_wait_flag(flag, ep | static_cast<unsigned long long>(j), abort_flag, p);
@@ -1461,7 +1467,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 for (int c = 0; c < 2 && c < nch; ++c) {
                   ptx::mbar_arrive_expect_tx(&ebar[quad * 2 + c], STG_BOX_BYTES);
-                  ptx::tma_load_3d(stg + c * STG_BOX_BYTES, &tmD2, &ebar[quad * 2 + c], c * 32, rrow, it.tile);
+                  ptx::tma_load_3d(stg + c * STG_BOX_BYTES, &tmD2, &ebar[quad * 2 + c], c * 32, rrow, it.st);
                 }
               }
             }
@@ -1497,22 +1503,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                   sum[4 * k + 3] = x.w + v[4 * k + 3];
                 }
               }
-              stage_row32(buf, lane, v);  // a lane overwrites only the row it read
-              ptx::fence_proxy_async_smem();
-              __syncwarp();
+              if (part || j < S - 1) {  // the last chained range has nothing to stage
+                stage_row32(buf, lane, v);  // a lane overwrites only the row it read
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+              }
+              if (part) {
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {  // rows 4 i .. 4 i + 3, 16 bytes a lane
-                const int row = 4 * i + (lane >> 3), k = lane & 7;
-                const float4 x = *reinterpret_cast<const float4*>(buf + row * 128 + ((k ^ (row & 7)) << 4));
-                if (mrow0 + row < p.M && n0 + 4 * k < p.N)
-                  *reinterpret_cast<float4*>(part + static_cast<int64_t>(mrow0 + row) * p.sp_ld + n0 + 4 * k) = x;
+                for (int i = 0; i < 8; ++i) {  // rows 4 i .. 4 i + 3, 16 bytes a lane
+                  const int row = 4 * i + (lane >> 3), k = lane & 7;
+                  const float4 x = *reinterpret_cast<const float4*>(buf + row * 128 + ((k ^ (row & 7)) << 4));
+                  if (mrow0 + row < p.M && n0 + 4 * k < p.N)
+                    *reinterpret_cast<float4*>(part + static_cast<int64_t>(mrow0 + row) * p.sp_ld + n0 + 4 * k) = x;
+                }
               }
               if (j < S - 1) {
                 if (lane == 0 && use_sum) {
                   if (j == 0)
-                    ptx::tma_store_3d(&tmD2, buf, c * 32, rrow, it.tile);
+                    ptx::tma_store_3d(&tmD2, buf, c * 32, rrow, it.st);
                   else
-                    ptx::tma_reduce_add_3d(&tmD2, buf, c * 32, rrow, it.tile);
+                    ptx::tma_reduce_add_3d(&tmD2, buf, c * 32, rrow, it.st);
                   ptx::bulk_commit_group();
                 }
                 continue;
@@ -1546,7 +1556,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) {
                   ptx::mbar_arrive_expect_tx(&ebar[quad * 2 + (c & 1)], STG_BOX_BYTES);
-                  ptx::tma_load_3d(buf, &tmD2, &ebar[quad * 2 + (c & 1)], (c + 2) * 32, rrow, it.tile);
+                  ptx::tma_load_3d(buf, &tmD2, &ebar[quad * 2 + (c & 1)], (c + 2) * 32, rrow, it.st);
                 }
               }
             }
@@ -1939,32 +1949,44 @@ int pair_clusters(int dev) {
 // clusters' lockstep -- the 2048 x 4096 x 16384 row-parallel GEMM, 128 tiles on 76 clusters,
 // read 575 MB from DRAM against 276 MB and ran 185 us against 167 us, and a 32-tile one ran
 // 109 us against 87 us.)  TP_STREAMK=0 turns the split off.
+//
+// Chained ranges (EPI_BF16) sum through a running sum in L2 instead: each range's TMA store
+// or add runs while its cluster's MMAs go on with the next item, so only the last round's
+// chain of S adds is exposed, about 2.2 us a link (a 4-tile, 19-range tail of the 2048 x
+// 12288 x 49152 row-parallel GEMM).  Charged kChainLinkStages per range, and taken from a
+// gain of kChainMinGain.  Chains are planned only for at most half a round of split tiles:
+// with more (the 2048 x 4096 x 16384 GEMM: 52 tiles past a round of 76) the ranges that run
+// side by side at different k read several K slices of the same panels at once, and the
+// split measured slower than the partial round it replaces (178.8 against 172.7 us).
 constexpr int kSkMinUnits = 8;
 constexpr int kSkSumStages = 10;
 constexpr double kSkMinGain = 0.1;
+constexpr int kChainLinkStages = 4;
+constexpr double kChainMinGain = 0.03;
 bool make_output_map(CUtensorMap* map, void* d, CUtensorMapDataType dt, int esz, int64_t N, int64_t M, int nbatch,
                      int64_t ldd, int64_t dbs);
 struct SpPlan {
   int rounds = 0, tiles = 0, split = 0, clusters = 0;
 };
-SpPlan sp_plan(int64_t T, int U, int nc, int64_t max_slots) {
+SpPlan sp_plan(int64_t T, int U, int nc, int64_t max_slots, bool chain) {
   SpPlan pl;
   const char* e = std::getenv("TP_STREAMK");
   if ((e && e[0] == '0') || T <= 0 || U <= 0 || nc <= 0) return pl;
   const int64_t R = T / nc, rem = T - R * nc;
   if (rem == 0) return pl;
+  if (chain && (rem > max_slots || 2 * rem > nc)) return pl;  // one running sum per split tile
   const double whole = static_cast<double>((R + 1) * U);
   double best = whole;
   int bestS = 0;
-  for (int S = 2; U / S >= kSkMinUnits && rem * S <= max_slots; ++S) {
+  for (int S = 2; U / S >= kSkMinUnits && (chain || rem * S <= max_slots); ++S) {
     const double tm = static_cast<double>(R * U) + static_cast<double>((rem * S + nc - 1) / nc) * U / S +
-                      static_cast<double>(S) * kSkSumStages;
+                      static_cast<double>(S) * (chain ? kChainLinkStages : kSkSumStages);
     if (tm < best - 1e-9) {
       best = tm;
       bestS = S;
     }
   }
-  if (bestS == 0 || best > whole * (1.0 - kSkMinGain)) return pl;
+  if (bestS == 0 || best > whole * (1.0 - (chain ? kChainMinGain : kSkMinGain))) return pl;
   pl.rounds = static_cast<int>(R);
   pl.tiles = static_cast<int>(rem);
   pl.split = bestS;
@@ -2020,6 +2042,7 @@ tp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
       a.sp_split = a.nsum;
       a.sp_units = U;
       a.sp_seq = 1;
+      a.sp_chain = 1;
       a.sp_user = 1;
       a.sp_part = ovl_part;
       a.sp_ld = a.N;
@@ -2034,8 +2057,28 @@ tp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
     } else if (sk_ws && sp_layout_ok(a)) {
       int64_t slots = static_cast<int64_t>(sk_ws_bytes / (kSkSlotBytes + kSkCounterBytes));
       if (slots > kSkMaxSlots) slots = kSkMaxSlots;
-      const SpPlan pl = sp_plan(tiles, U, nc, slots);
-      if (pl.split > 0) {
+      const char* ec = std::getenv("TP_SPLIT_CHAIN");
+      bool chain = EPI == EPI_BF16 && !(ec && ec[0] == '0');
+      SpPlan pl = sp_plan(tiles, U, nc, slots, chain);
+      if (chain && pl.split == 0) {  // no chain planned: the counted form may still pay
+        chain = false;
+        pl = sp_plan(tiles, U, nc, slots, false);
+      }
+      if (pl.split > 0 && chain) {
+        // a running sum (slot) and 8 flags per split tile: [tiles][256][256] fp32, then flags
+        a.sp_rounds = pl.rounds;
+        a.sp_tiles = pl.tiles;
+        a.sp_split = pl.split;
+        a.sp_units = U;
+        a.sp_chain = 1;
+        a.sp_cnt = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(sk_ws) +
+                                                         static_cast<size_t>(pl.tiles) * kSkSlotBytes);
+        a.sp_epoch = next_sp_epoch();
+        if (!make_output_map(&run_map, sk_ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 256, 256, pl.tiles, 256,
+                             256 * 256))
+          return TP_FAIL_DETAIL("tensor map of the split-K running sums");
+        clusters = pl.clusters;
+      } else if (pl.split > 0) {
         const int used = pl.tiles * pl.split;  // partial slots
         a.sp_rounds = pl.rounds;
         a.sp_tiles = pl.tiles;
@@ -2054,7 +2097,7 @@ tp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
     return TP_ERR_UNSUPPORTED;
   }
   TP_CUDA_CHECK(launch_pdl(gemm_pair_kernel<A_MN, B_MN, EPI, ACT>, dim3(2 * clusters), dim3(NUM_THREADS),
-                           pair_smem_bytes<EPI>(), s, ta, tb, td, ovl_part ? run_map : td2, tp_map, a));
+                           pair_smem_bytes<EPI>(), s, ta, tb, td, a.sp_chain ? run_map : td2, tp_map, a));
   count_launch();
   return TP_OK;
 }

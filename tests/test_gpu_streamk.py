@@ -3,14 +3,20 @@
 With a workspace, the tiles past the pair kernel's last full round of whole tiles (all
 tiles, when there are fewer tiles than CTA pairs) may be cut into S equal K ranges at the
 same k-stages, dealt to every pair, when the plan's time model says it pays (long K, few
-tiles).  Each range leaves its fp32 partial in the workspace and counts itself; the range
-that completes a tile's count adds the partials in range order and applies the epilogue.
+tiles).  bf16-output GEMMs chain their ranges: range 0 stores its fp32 partial into the
+tile's running sum in the workspace, each next range adds into it in L2 after the previous
+range's flag, and the last range adds its accumulator and applies the epilogue.  The other
+epilogues (and bf16 with TP_SPLIT_CHAIN=0) count their ranges: each range leaves its fp32
+partial in the workspace and counts itself; the range that completes a tile's count adds
+the partials in range order and applies the epilogue.
 Covered here: the row-parallel GEMM with its fused shard sum (ranges that cross shard
-boundaries, ragged M, N and K; shapes the plan keeps whole), the column-parallel GEMM with
-each activation, the backward's dgrad (with the fused bias-gradient partials), both
-wgrads and the f-reduced dX, a workspace that holds only a few partials (fewer ranges),
-determinism, CUDA-graph replay with new inputs between replays (the counters reset
-themselves), and guard bytes around the workspace and every output.
+boundaries, ragged M, N and K; a split past a full round of whole tiles; both forms), the
+column-parallel GEMM with each activation, the backward's dgrad (with the fused
+bias-gradient partials), both wgrads and the f-reduced dX, a workspace that holds only a
+few partials or running sums,
+determinism, CUDA-graph replay with new inputs between replays (the counters and flags
+reset themselves), and guard bytes around the workspace (which starts with arbitrary
+bytes) and every output.
 Criterion: max|gpu - oracle| <= 1e-2 * max|oracle| per output.
 """
 
@@ -37,14 +43,17 @@ def _case(M, h, F, t, seed, bias=True):
     return dev, ref, T.MLPWeights(dev["W_up"], dev["b_up"], dev["W_down"], dev["b_down"], t)
 
 
+@pytest.mark.parametrize("chain", [True, False])
 @pytest.mark.parametrize("M,h,F,t", [
-    (1000, 1024, 16384, 4),  # 16 tiles, 128 k-stages: 4 ranges, one per shard
+    (1000, 1024, 16384, 4),  # 16 tiles, 128 k-stages
     (520, 1032, 15680, 4),   # ragged M (3 row tiles), N (1032 = 4 x 256 + 8), K (3920 per shard)
-    (300, 1024, 16384, 4),   # 8 tiles, 128 k-stages: 4 ranges
+    (300, 1024, 16384, 4),   # 8 tiles, 128 k-stages
     (272, 776, 24576, 3),    # 8 tiles, t = 3: range boundaries inside shards
-    (2048, 4096, 8192, 4),   # 128 tiles, more than CTA pairs: whole tiles (a split would not pay)
+    (2048, 4096, 8192, 4),   # 128 tiles: a round of whole tiles, then 52 (kept whole: a split would not pay)
+    (2560, 2048, 4096, 4),   # 80 tiles: a round of whole tiles, then the last few split
 ])
-def test_row_parallel_streamk_matches_oracle(M, h, F, t):
+def test_row_parallel_streamk_matches_oracle(M, h, F, t, chain, monkeypatch):
+    monkeypatch.setenv("TP_SPLIT_CHAIN", "1" if chain else "0")
     dev, ref, w = _case(M, h, F, t, seed=60 + t)
     A = (torch.randn(t, M, F // t, generator=torch.Generator().manual_seed(61)) * 0.5).to(torch.bfloat16)
     R = torch.randn(M, h, generator=torch.Generator().manual_seed(62)).to(torch.bfloat16)
@@ -116,8 +125,9 @@ def test_mlp_backward_streamk(M, h, F, t):
 
 @pytest.mark.parametrize("slots", [2, 32, 48])
 def test_partial_workspace_limits_the_clusters(slots):
-    """A workspace with room for only a few partials (16 tiles: none, two or three ranges
-    each) still gives the result."""
+    """A workspace with room for only a few partials or running sums (16 tiles: chained
+    ranges need one running sum per tile, so 2 slots keep the tiles whole) still gives the
+    result."""
     M, h, F, t = 1000, 1024, 16384, 4
     dev, ref, w = _case(M, h, F, t, seed=65)
     A = (torch.randn(t, M, F // t, generator=torch.Generator().manual_seed(66)) * 0.5).to(torch.bfloat16).cuda()
@@ -135,8 +145,8 @@ def test_partial_workspace_limits_the_clusters(slots):
 def test_streamk_deterministic_and_graph_replay_with_new_inputs():
     """Same inputs, same bits; captured in a CUDA graph, each replay (with new inputs
     written between replays) gives the eager result for those inputs -- every replay
-    repeats the counters' launch tag, and the counters start from zero because the range
-    that completes a count resets it."""
+    repeats the flags' launch tag, and the flags start from zero because the last range of
+    a tile resets them."""
     M, h, F, t = 1000, 1024, 16384, 4
     dev, ref, w = _case(M, h, F, t, seed=67)
     nws = L.tp_row_parallel_workspace_size(M, F, h, t)
