@@ -445,13 +445,13 @@ __device__ __forceinline__ void dact_colsum_chunk(const GemmArgs& p, int b, int 
 
 // One k-step of the single-CTA kernels: the TMA copies of A's and B's tiles for k-step ks
 // of output tile (b, mb, nb) into stage buffers a_dst / b_dst, completing on `bar`.
-template <bool A_MN, bool B_MN>
+template <bool A_MN, bool B_MN, int NB = BN>
 __device__ __forceinline__ void load_stage(const GemmArgs& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
                                            uint8_t* a_dst, uint8_t* b_dst, uint64_t* bar, int ks, int b, int mb,
                                            int nb) {
   const int s = ks / p.kt;
   const int kb = ks - s * p.kt;
-  ptx::mbar_arrive_expect_tx(bar, STAGE_BYTES);
+  ptx::mbar_arrive_expect_tx(bar, A_TILE_BYTES + NB * BK * 2);
   const int ash = p.a_sharded ? (p.nsum > 1 ? s : b) : 0;
   const int bsh = p.b_sharded ? (p.nsum > 1 ? s : b) : 0;
   if (!A_MN) {
@@ -464,20 +464,20 @@ __device__ __forceinline__ void load_stage(const GemmArgs& p, const CUtensorMap*
       ptx::tma_load_3d(a_dst + j * MN_CHUNK_BYTES, tmA, bar, mb * BM + j * 64, kb * BK, ash);
   }
   if (!B_MN) {
-    ptx::tma_load_3d(b_dst, tmB, bar, kb * BK, nb * BN, bsh);
+    ptx::tma_load_3d(b_dst, tmB, bar, kb * BK, nb * NB, bsh);
   } else if (p.b_4d) {
-    ptx::tma_load_4d(b_dst, tmB, bar, 0, kb * BK, nb * (BN / 64), bsh);
+    ptx::tma_load_4d(b_dst, tmB, bar, 0, kb * BK, nb * (NB / 64), bsh);
   } else {
 #pragma unroll
-    for (int j = 0; j < BN / 64; ++j)
-      ptx::tma_load_3d(b_dst + j * MN_CHUNK_BYTES, tmB, bar, nb * BN + j * 64, kb * BK, bsh);
+    for (int j = 0; j < NB / 64; ++j)
+      ptx::tma_load_3d(b_dst + j * MN_CHUNK_BYTES, tmB, bar, nb * NB + j * 64, kb * BK, bsh);
   }
 }
 
-// Instruction descriptor of the 128 x 256 MMA for this launch's operand format.
-template <bool A_MN, bool B_MN>
+// Instruction descriptor of the 128 x NB MMA for this launch's operand format.
+template <bool A_MN, bool B_MN, int NB = BN>
 __device__ __forceinline__ uint32_t single_idesc(const GemmArgs& p) {
-  return p.f16ab ? ptx::idesc_f16_f32(BM, BN, A_MN, B_MN) : ptx::idesc_bf16_f32(BM, BN, A_MN, B_MN);
+  return p.f16ab ? ptx::idesc_f16_f32(BM, NB, A_MN, B_MN) : ptx::idesc_bf16_f32(BM, NB, A_MN, B_MN);
 }
 
 // The MMAs of one stage (BK deep) into the accumulator at d_tmem; `first` starts it afresh.
@@ -697,11 +697,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // slot of its K range; the operand stages, idle by then, hold what arrives.  After a second
 // cluster barrier each CTA sums its R rows over the S ranges in range order -- the result
 // does not depend on timing -- and applies the epilogue with coalesced stores.
-constexpr int SPLITC_ROWF = BN + 4;  // floats per received row (16 bytes of padding spread the banks)
+template <int SBN>
+constexpr int splitc_rowf() { return SBN + 4; }  // floats per received row (16 bytes of padding spread the banks)
 // Per epilogue warp, a 32 x 32 block of its partial on its way out: written row per lane,
 // read back as 128-byte row segments so that every remote store moves whole segments.
 constexpr int SPLITC_XF = 32 + 4;  // floats per staged row
-constexpr int SPLITC_RECV_BYTES = BM * SPLITC_ROWF * 4;
+constexpr int SPLITC_RECV_BYTES = BM * splitc_rowf<BN>() * 4;  // room for the widest tile
 constexpr int SPLITC_XBYTES = 32 * SPLITC_XF * 4;
 static_assert(SPLITC_RECV_BYTES + 4 * SPLITC_XBYTES <= STAGES * STAGE_BYTES,
               "received partials and the staging blocks must fit the operand stages");
@@ -743,10 +744,12 @@ __device__ __forceinline__ void splitc_store2(const GemmArgs& p, int b, int m, i
   }
 }
 
-template <bool A_MN, bool B_MN, int EPI, int ACT>
+template <bool A_MN, bool B_MN, int EPI, int ACT, int SBN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_splitc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const GemmArgs p) {
+  static_assert(SBN == BN || SBN == BN / 2, "tile width of the split kernel");
+  constexpr int ROWF = splitc_rowf<SBN>();
   extern __shared__ uint8_t dsmem[];
   const uint32_t pad = (1024u - (ptx::smem_addr(dsmem) & 1023u)) & 1023u;
   uint8_t* base = dsmem + pad;
@@ -783,7 +786,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(tmem_slot, BN);
+    ptx::tmem_alloc(tmem_slot, SBN);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
@@ -804,7 +807,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int issued = 0;
       for (int ks = klo; ks < khi; ++ks) {
         if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err, ERR_WAIT_PRODUCER, p.timeout_ns)) break;
-        load_stage<A_MN, B_MN>(p, &tmA, &tmB, sA + stage * A_TILE_BYTES, sB + stage * B_TILE_BYTES, &full[stage],
+        load_stage<A_MN, B_MN, SBN>(p, &tmA, &tmB, sA + stage * A_TILE_BYTES, sB + stage * B_TILE_BYTES, &full[stage],
                                ks, b, mb, nb);
         ++issued;
         if (++stage == STAGES) {
@@ -827,7 +830,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ptx::mbar_wait(&full[stage], phase, abort_flag, p.err, ERR_WAIT_MMA, p.timeout_ns)) break;
         ptx::tc_fence_after();
         mma_stage<A_MN, B_MN>(tmem_base, ptx::smem_addr(sA + stage * A_TILE_BYTES),
-                              ptx::smem_addr(sB + stage * B_TILE_BYTES), ks == klo, single_idesc<A_MN, B_MN>(p));
+                              ptx::smem_addr(sB + stage * B_TILE_BYTES), ks == klo,
+                              single_idesc<A_MN, B_MN, SBN>(p));
         ptx::mma_commit(&empty[stage]);
         if (++stage == STAGES) {
           stage = 0;
@@ -856,8 +860,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // 4 i + l / 8 (i = 0..7) of the warp's 32: eight lanes cover a row's 128 bytes.
     const int seg = lane & 7;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      if (nb * BN + c * 32 >= p.N) break;  // warp-uniform: columns past N are never summed
+    for (int c = 0; c < SBN / 32; ++c) {
+      if (nb * SBN + c * 32 >= p.N) break;  // warp-uniform: columns past N are never summed
       uint32_t r[32];
       ptx::tmem_ld32(t_row + c * 32, r);
       ptx::tmem_ld_wait();
@@ -872,7 +876,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int row = quad * 32 + rl;
         const uint4 v = *reinterpret_cast<const uint4*>(xs + rl * SPLITC_XF + 4 * seg);
         const uint32_t dst = ptx::mapa_shared(
-            ptx::smem_addr(recv + (static_cast<int64_t>(j) * R + row % R) * SPLITC_ROWF + c * 32 + 4 * seg),
+            ptx::smem_addr(recv + (static_cast<int64_t>(j) * R + row % R) * ROWF + c * 32 + 4 * seg),
             static_cast<uint32_t>(row / R));
         ptx::st_cluster_v4(dst, v.x, v.y, v.z, v.w);
       }
@@ -884,8 +888,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncwarp();
   ptx::cluster_sync();
   if (warp >= 2) {
-    const int e = static_cast<int>(threadIdx.x) - 64;  // columns 2e, 2e + 1 of each owned row
-    const int n = nb * BN + 2 * e;
+    // Thread e takes columns 2 cp, 2 cp + 1 of the owned rows rg, rg + RG, ... (RG = 1 for
+    // 256-wide tiles, 2 for 128-wide ones).
+    constexpr int CP = SBN / 2, RG = 128 / CP;
+    const int e = static_cast<int>(threadIdx.x) - 64;
+    const int cp = e % CP, rg = e / CP;
+    const int n = nb * SBN + 2 * cp;
     if (n < p.N) {
       float b0 = 0.0f, b1 = 0.0f;
       if (EPI != EPI_F32 && p.bias)
@@ -893,25 +901,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int rows = min(R, p.M - (mb * BM + j * R));
       // Eight rows at a time: every load of the batch is issued before the first store, so
       // the shared-memory latency is paid once per batch rather than once per row.
-      const float* __restrict__ rbase = recv + 2 * e;
+      const float* __restrict__ rbase = recv + 2 * cp;
 #pragma unroll 1
-      for (int r0 = 0; r0 < rows; r0 += 8) {
+      for (int r0 = rg; r0 < rows; r0 += 8 * RG) {
         float2 acc[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          acc[u] = *reinterpret_cast<const float2*>(rbase + min(r0 + u, R - 1) * SPLITC_ROWF);
+          acc[u] = *reinterpret_cast<const float2*>(rbase + min(r0 + u * RG, R - 1) * ROWF);
         for (int k = 1; k < S; ++k) {  // K ranges in order
-          const float* __restrict__ src = rbase + static_cast<int64_t>(k) * R * SPLITC_ROWF;
+          const float* __restrict__ src = rbase + static_cast<int64_t>(k) * R * ROWF;
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            const float2 x = *reinterpret_cast<const float2*>(src + min(r0 + u, R - 1) * SPLITC_ROWF);
+            const float2 x = *reinterpret_cast<const float2*>(src + min(r0 + u * RG, R - 1) * ROWF);
             acc[u].x += x.x;
             acc[u].y += x.y;
           }
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          if (r0 + u < rows) splitc_store2<EPI, ACT>(p, b, mb * BM + j * R + r0 + u, n, acc[u].x, acc[u].y, b0, b1);
+          if (r0 + u * RG < rows)
+            splitc_store2<EPI, ACT>(p, b, mb * BM + j * R + r0 + u * RG, n, acc[u].x, acc[u].y, b0, b1);
       }
     }
   }
@@ -922,7 +931,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 1) {
     __syncwarp();
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, BN);
+    ptx::tmem_dealloc(tmem_base, SBN);
   }
 }
 
@@ -2173,14 +2182,14 @@ tp_status dispatch(bool amn, bool bmn, int epi, int act, F&& f) {
 
 // ----------------------------------------------------- split K: launch
 // Clusters of S CTAs that can be resident at once for this instance (0 if none).
-template <bool A_MN, bool B_MN, int EPI, int ACT>
+template <bool A_MN, bool B_MN, int EPI, int ACT, int SBN>
 int splitc_clusters(int dev, int S) {
   static int cached[64][5] = {};  // [device][log2 S - 1] + 1
   int li = 0;
   while ((2 << li) < S) ++li;
   if (dev < 0 || dev >= 64 || li > 4) return 0;
   if (cached[dev][li]) return cached[dev][li] - 1;
-  auto kern = gemm_splitc_kernel<A_MN, B_MN, EPI, ACT>;
+  auto kern = gemm_splitc_kernel<A_MN, B_MN, EPI, ACT, SBN>;
   int n = 0;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) == cudaSuccess &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
@@ -2202,7 +2211,7 @@ int splitc_clusters(int dev, int S) {
   return n;
 }
 
-template <bool A_MN, bool B_MN, int EPI, int ACT>
+template <bool A_MN, bool B_MN, int EPI, int ACT, int SBN>
 tp_status launch_splitc(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int64_t tiles, int S,
                         cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
@@ -2219,7 +2228,7 @@ tp_status launch_splitc(const CUtensorMap& ta, const CUtensorMap& tb, const Gemm
   at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 2;
-  TP_CUDA_CHECK(cudaLaunchKernelEx(&cfg, gemm_splitc_kernel<A_MN, B_MN, EPI, ACT>, ta, tb, a));
+  TP_CUDA_CHECK(cudaLaunchKernelEx(&cfg, gemm_splitc_kernel<A_MN, B_MN, EPI, ACT, SBN>, ta, tb, a));
   count_launch();
   return TP_OK;
 }
@@ -2411,23 +2420,43 @@ tp_status run_gemm(const GemmProblem& P, cudaStream_t s) {
   if (P.M <= 128 && P.N % 8 == 0 && !P.colsum && (P.epi == EPI_BF16 || P.epi == EPI_ACT || P.epi == EPI_F32)) {
     int dev = 0;
     TP_CUDA_CHECK(cudaGetDevice(&dev));
-    int S = splitc_ranges(tiles, static_cast<int64_t>(P.nsum) * kt);
-    tp_status st = TP_ERR_UNSUPPORTED;
-    while (S > 1) {  // the largest cluster size this device can schedule
-      st = dispatch_splitc(amn, bmn, P.epi, P.act, [&](auto am, auto bm, auto ep, auto ac) {
-        return splitc_clusters<decltype(am)::value, decltype(bm)::value, decltype(ep)::value, decltype(ac)::value>(
-                   dev, S) > 0
-                   ? TP_OK
-                   : TP_ERR_UNSUPPORTED;
+    // 128-column tiles (K-major operands) where even they leave SMs idle: twice the CTAs,
+    // each with half the operand bytes, half the partial to exchange and half the rows'
+    // columns to sum.  TP_SPLITC_NARROW=0 keeps 256-column tiles, =1 asks for 128.
+    const char* en = std::getenv("TP_SPLITC_NARROW");
+    const bool narrow = !amn && !bmn && (en && en[0] ? en[0] == '1' : tiles * 4 <= device_sm_count());
+    const int64_t snt = narrow ? (P.N + BN / 2 - 1) / (BN / 2) : nt;
+    const int64_t stiles = mt * snt * P.nbatch;
+    auto clusters_ok = [&](int S) {
+      return dispatch_splitc(amn, bmn, P.epi, P.act, [&](auto am, auto bm, auto ep, auto ac) {
+        constexpr bool AM = decltype(am)::value, BM_ = decltype(bm)::value;
+        constexpr int EP = decltype(ep)::value, AC = decltype(ac)::value;
+        int n = 0;
+        if constexpr (!AM && !BM_)
+          n = narrow ? splitc_clusters<AM, BM_, EP, AC, BN / 2>(dev, S) : splitc_clusters<AM, BM_, EP, AC, BN>(dev, S);
+        else
+          n = splitc_clusters<AM, BM_, EP, AC, BN>(dev, S);
+        return n > 0 ? TP_OK : TP_ERR_UNSUPPORTED;
       });
-      if (st == TP_OK) break;
-      S /= 2;
-    }
+    };
+    int S = splitc_ranges(stiles, static_cast<int64_t>(P.nsum) * kt);
+    while (S > 1 && clusters_ok(S) != TP_OK) S /= 2;  // the largest cluster size this device can schedule
     if (S > 1) {
       a.ksplit = S;
+      CUtensorMap tbn = tb;
+      if (narrow) {
+        int b4 = 0;
+        if (!make_operand_map(&tbn, P.b, P.N, P.K, nsh_b, BN / 2, 1, &b4)) return TP_ERR_CUDA;
+        a.b_4d = b4;
+        a.nt = static_cast<int>(snt);
+      }
       return dispatch_splitc(amn, bmn, P.epi, P.act, [&](auto am, auto bm, auto ep, auto ac) {
-        return launch_splitc<decltype(am)::value, decltype(bm)::value, decltype(ep)::value, decltype(ac)::value>(
-            ta, tb, a, tiles, S, s);
+        constexpr bool AM = decltype(am)::value, BM_ = decltype(bm)::value;
+        constexpr int EP = decltype(ep)::value, AC = decltype(ac)::value;
+        if constexpr (!AM && !BM_) {
+          if (narrow) return launch_splitc<AM, BM_, EP, AC, BN / 2>(ta, tbn, a, stiles, S, s);
+        }
+        return launch_splitc<AM, BM_, EP, AC, BN>(ta, tbn, a, stiles, S, s);
       });
     }
   }

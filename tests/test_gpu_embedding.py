@@ -32,7 +32,9 @@ def _bwd(ids, dY, V, h, t, dE=None, accumulate=0):
 
 
 @pytest.mark.parametrize("N,V,h,t", [(300, 64, 256, 4), (9000, 1000, 264, 8), (1, 16, 8, 2), (5000, 4096, 512, 1),
-                                     (1500, 512, 128, 2), (2048, 96, 64, 4)])
+                                     (1500, 512, 128, 2), (2048, 96, 64, 4),
+                                     (4000, 40000, 1032, 4),    # mostly ids seen once; three column slices
+                                     (700, 2, 64, 2)])          # two ids: two long segments
 def test_embedding_parity(N, V, h, t):
     ids = I.token_ids(N, V, seed=N)
     ids[:4] = torch.tensor([0, V - 1, V // t - 1, min(V // t, V - 1)], dtype=torch.int32)[: min(4, N)]
@@ -80,6 +82,23 @@ def test_embedding_id_out_of_range_is_reported():
     dE = _bwd(ids, dY, V, h, t)
     assert L.tp_get_device_status(check=False) == L.TP_ERR_SHAPE
     assert dE[3].eq(1).all() and dE[5].eq(1).all() and dE.sum().item() == 2 * h
+
+
+def test_embedding_backward_skips_out_of_range_ids_among_many():
+    """Ids outside [0, V) spread through a chunk (negative and too large) are reported
+    and add nothing; every other token's row is summed as the oracle sums the valid
+    tokens alone."""
+    N, V, h, t = 3000, 700, 520, 4
+    ids = I.token_ids(N, V, seed=11)
+    bad = torch.arange(5, N, 97)
+    ids[bad] = torch.where(bad % 2 == 0, torch.full_like(bad, -3), torch.full_like(bad, V + 5)).to(torch.int32)
+    inp = I.embedding_inputs(N, V, h, seed=12)
+    dE = _bwd(ids.cuda(), inp["dY"].cuda(), V, h, t)
+    torch.cuda.synchronize()
+    assert L.tp_get_device_status(check=False) == L.TP_ERR_SHAPE
+    ok = ((ids >= 0) & (ids < V)).numpy()
+    want = O.embedding_backward_unsplit(ids.numpy()[ok], f64(inp["dY"])[ok], V)
+    assert_close("dE", f64(dE), want)
 
 
 def test_embedding_rejects_bad_shapes():

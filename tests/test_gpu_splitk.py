@@ -6,7 +6,8 @@ its K steps -- for the row-parallel GEMM the t shards' K ranges laid end to end 
 sum their fp32 partials through distributed shared memory in range order before the
 epilogue (bias, activation, residual).  TP_SPLITK sets S (a power of two up to 16) so
 that ragged ranges (S not dividing the k-steps, ranges that cross a shard boundary, K
-not a multiple of the 64-deep k-block) are exercised.  Criterion as everywhere:
+not a multiple of the 64-deep k-block) are exercised; TP_SPLITC_NARROW picks 128- or
+256-column tiles (N ragged against either).  Criterion as everywhere:
 max|gpu - oracle| <= 1e-2 * max|oracle| per output, and the outputs sit between guard
 bytes that must come back unchanged.
 """
@@ -45,14 +46,16 @@ def _forward_guarded(dev, w, M, h, F, t, act, residual=None):
     return Y.t, Z.t, A.t
 
 
+@pytest.mark.parametrize("narrow", ["0", "1"])
 @pytest.mark.parametrize("S", ["", "2", "4", "8", "16"])
 @pytest.mark.parametrize("M,h,F,t", [(128, 1024, 4096, 2), (100, 392, 1296, 2), (37, 264, 3072, 4)])
-def test_split_forward_matches_oracle(M, h, F, t, S, monkeypatch):
+def test_split_forward_matches_oracle(M, h, F, t, S, narrow, monkeypatch):
     """h = 392 and 264 are not multiples of 64 (the last k-block is ragged); F/t = 648
     gives 11 k-blocks per shard, so the row-parallel GEMM's 22 k-steps cut into 4 or 8
     ranges put a boundary inside a shard's K range; 16 ranges of the column GEMM's 7
     k-steps are capped at 4 (a power of two no larger than the k-steps)."""
     monkeypatch.setenv("TP_SPLITK", S)
+    monkeypatch.setenv("TP_SPLITC_NARROW", narrow)
     dev, ref, w = _case(M, h, F, t, seed=30 + M)
     Y, Z, A = _forward_guarded(dev, w, M, h, F, t, "gelu_tanh")
     o = O.mlp_forward_sharded(ref["X"], ref["W_up"], ref["b_up"], ref["W_down"], ref["b_down"], "gelu_tanh", t)
