@@ -887,11 +887,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   ptx::tc_fence_before();
   __syncwarp();
   ptx::cluster_sync();
-  if (warp >= 2) {
-    // Thread e takes columns 2 cp, 2 cp + 1 of the owned rows rg, rg + RG, ... (RG = 1 for
-    // 256-wide tiles, 2 for 128-wide ones).
-    constexpr int CP = SBN / 2, RG = 128 / CP;
-    const int e = static_cast<int>(threadIdx.x) - 64;
+  // The sums: 256-column tiles on the four epilogue warps, thread e taking columns 2 e,
+  // 2 e + 1 of every owned row; 128-column tiles on all six warps, thread e taking columns
+  // 2 cp, 2 cp + 1 of the owned rows rg, rg + 3, ...
+  constexpr int SUM_T = SBN == BN ? 128 : NUM_THREADS;
+  if (SUM_T == NUM_THREADS || warp >= 2) {
+    constexpr int CP = SBN / 2, RG = SUM_T / CP;
+    const int e = static_cast<int>(threadIdx.x) - (NUM_THREADS - SUM_T);
     const int cp = e % CP, rg = e / CP;
     const int n = nb * SBN + 2 * cp;
     if (n < p.N) {
