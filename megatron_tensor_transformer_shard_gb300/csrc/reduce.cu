@@ -96,9 +96,10 @@ __global__ void shard_reduce_kernel(const float* __restrict__ P, int64_t rows, i
 
 // ---- fused column sums of two matrices (e.g. db_down from dY and every
 // shard's db_up from dZ) in two launches: a partial pass with 16-byte loads,
-// 256-row chunks, 8 warps per CTA combined in warp order, and a final pass
-// summing the chunks in order.  Deterministic.
-constexpr int CS2_ROWS = 256;
+// 64-row chunks (a warp's 8 rows all in flight), 8 warps per CTA combined in warp
+// order, and a final pass in which 8 warps take consecutive runs of a column's
+// chunks, each run summed in order, and the runs are added in order.  Deterministic.
+constexpr int CS2_ROWS = 64;
 constexpr int CS2_THREADS = 256;  // 8 warps x 32 lanes x 8 columns: 256 columns per CTA
 
 __device__ __forceinline__ const ColsumJob& pick(const ColsumJob& a, const ColsumJob& b, bool first) {
@@ -134,12 +135,12 @@ __global__ void __launch_bounds__(CS2_THREADS) colsum2_partial_kernel(ColsumJob 
   const bool f16 = j.f16 != 0;
   if (c0 + 8 <= j.cols) {
     int64_t r = r0 + warp;
-    for (; r + 24 < r1; r += 32) {  // four rows in flight per thread
-      uint4 w[4];
+    for (; r + 56 < r1; r += 64) {  // eight rows in flight per thread
+      uint4 w[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) w[u] = *reinterpret_cast<const uint4*>(g + (r + 8 * u) * j.ld + c0);
+      for (int u = 0; u < 8; ++u) w[u] = *reinterpret_cast<const uint4*>(g + (r + 8 * u) * j.ld + c0);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 8; ++u) {
         float a0, a1;
         unpack2(w[u].x, f16, a0, a1); acc[0] += a0; acc[1] += a1;
         unpack2(w[u].y, f16, a0, a1); acc[2] += a0; acc[3] += a1;
@@ -175,22 +176,36 @@ __global__ void __launch_bounds__(CS2_THREADS) colsum2_partial_kernel(ColsumJob 
   }
 }
 
-__global__ void colsum2_final_kernel(ColsumJob j0, ColsumJob j1, int64_t n0) {
+constexpr int CS2F_WARPS = 8;  // final pass: 32 columns per CTA, a run of chunks per warp
+
+__global__ void __launch_bounds__(CS2F_WARPS * 32) colsum2_final_kernel(ColsumJob j0, ColsumJob j1, int64_t n0,
+                                                                        int64_t n) {
+  __shared__ float red[CS2F_WARPS][32];
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
-  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * 32 + lane;
   const bool first = idx < n0;
   const ColsumJob& j = pick(j0, j1, first);
   const int64_t local = first ? idx : idx - n0;
-  if (local >= j.cols * j.nbatch) return;
-  const int64_t b = local / j.cols, c = local - b * j.cols;
-  const float* w = j.ws + b * j.nchunks * j.cols + c;
   float s = 0.0f;
-  // Up to 16 loads in flight (a GEMM epilogue leaves one partial per 32 rows); the adds keep
-  // their order, so the sum is the same.
+  if (idx < n) {
+    const int64_t b = local / j.cols, c = local - b * j.cols;
+    const float* w = j.ws + b * j.nchunks * j.cols + c;
+    // warp `warp` sums chunks [k0, k1) in order, up to 16 loads in flight
+    const int k0 = static_cast<int>(static_cast<int64_t>(j.nchunks) * warp / CS2F_WARPS);
+    const int k1 = static_cast<int>(static_cast<int64_t>(j.nchunks) * (warp + 1) / CS2F_WARPS);
 #pragma unroll 16
-  for (int k = 0; k < j.nchunks; ++k) s += w[static_cast<int64_t>(k) * j.cols];
-  j.out[local] = j.accumulate ? j.out[local] + s : s;
+    for (int k = k0; k < k1; ++k) s += w[static_cast<int64_t>(k) * j.cols];
+  }
+  red[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && idx < n) {
+    float t = 0.0f;
+#pragma unroll
+    for (int w2 = 0; w2 < CS2F_WARPS; ++w2) t += red[w2][lane];  // the runs in order
+    j.out[local] = j.accumulate ? j.out[local] + t : t;
+  }
 }
 
 }  // namespace
@@ -232,8 +247,8 @@ tp_status run_colsum2(ColsumJob a, ColsumJob b, cudaStream_t s) {
                              dim3(CS2_THREADS), 0, s, a, b, ctas[0]));
     count_launch();
   }
-  TP_CUDA_CHECK(launch_pdl(colsum2_final_kernel, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, s, a, b,
-                           outs[0]));
+  TP_CUDA_CHECK(launch_pdl(colsum2_final_kernel, dim3(static_cast<unsigned>((n + 31) / 32)), dim3(CS2F_WARPS * 32), 0,
+                           s, a, b, outs[0], n));
   count_launch();
   return TP_OK;
 }
