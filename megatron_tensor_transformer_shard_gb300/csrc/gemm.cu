@@ -107,6 +107,8 @@ struct GemmArgs {
   // writes a partial of its own: range 0 stores, the middle ranges add in L2, the last range
   // loads the sum, adds its accumulator and applies the epilogue.  The overlapped reduction
   // is the chained form with sp_seq and sp_user set.
+  // Chained ranges are dealt range-major (every split tile's range 0, then every tile's range
+  // 1, ...), so the pairs working side by side mostly share one K slice of the panels.
   int sp_rounds, sp_tiles, sp_split, sp_units, sp_seq, sp_chain;
   int sp_user;              // partials in the caller's [S][M][N] buffer, else 256 x 256 slots
   float* sp_part;           // slots [split tiles * S][256][256], or the caller's buffer (unused when chained)
@@ -957,8 +959,10 @@ __device__ __forceinline__ void sp_cut(const GemmArgs& p, int j, PairItem& it) {
 // (sp_seq): every tile's shard ranges as items, shard-major (all tiles' shard 0, then shard
 // 1, ...), dealt round-robin, so a tile's shard j comes `total` items after its shard j - 1.  Split K:
 // first the sp_rounds whole rounds, then items u = c, c + nclusters, ... of the sp_tiles
-// remaining tiles, u = S i + j being range j of remaining tile i: a tile's ranges run side
-// by side on neighbouring clusters.  Every role of the kernel enumerates the same items.
+// remaining tiles: counted ranges u = S i + j (range j of remaining tile i; a tile's ranges
+// run side by side on neighbouring clusters), chained ranges u = sp_tiles j + i (range-major:
+// a tile's range j comes sp_tiles items after its range j - 1, the item it waits for).  Every
+// role of the kernel enumerates the same items.
 __device__ __forceinline__ bool pair_item(const GemmArgs& p, int c, int nclusters, int total, int ksteps, int idx,
                                           PairItem& it) {
   it.range = 0;
@@ -983,10 +987,12 @@ __device__ __forceinline__ bool pair_item(const GemmArgs& p, int c, int ncluster
     }
     const int64_t u = c + static_cast<int64_t>(idx - p.sp_rounds) * nclusters;
     if (u >= static_cast<int64_t>(p.sp_tiles) * S) return false;
-    const int i = static_cast<int>(u / S);
+    // chained: range-major (range u / tiles of tile u % tiles); counted: a tile's ranges side by side
+    const int i = static_cast<int>(p.sp_chain ? u % p.sp_tiles : u / S);
+    const int j = static_cast<int>(p.sp_chain ? u / p.sp_tiles : u - static_cast<int64_t>(i) * S);
     it.tile = p.sp_rounds * nclusters + i;
     it.st = i;
-    sp_cut(p, static_cast<int>(u - static_cast<int64_t>(i) * S), it);
+    sp_cut(p, j, it);
     return true;
   }
   const int tile = c + idx * nclusters;
@@ -1965,10 +1971,13 @@ int pair_clusters(int dev) {
 // or add runs while its cluster's MMAs go on with the next item, so only the last round's
 // chain of S adds is exposed, about 2.2 us a link (a 4-tile, 19-range tail of the 2048 x
 // 12288 x 49152 row-parallel GEMM).  Charged kChainLinkStages per range, and taken from a
-// gain of kChainMinGain.  Chains are planned only for at most half a round of split tiles:
-// with more (the 2048 x 4096 x 16384 GEMM: 52 tiles past a round of 76) the ranges that run
-// side by side at different k read several K slices of the same panels at once, and the
-// split measured slower than the partial round it replaces (178.8 against 172.7 us).
+// gain of kChainMinGain.  The chained ranges are dealt range-major, so the pairs that run side
+// by side work on one or two K slices of the panels (dealt tile by tile, a tile's S ranges on
+// neighbouring pairs, the 2048 x 4096 x 16384 GEMM's split -- 52 tiles past a round of 76, four
+// ranges each -- read four K slices at once and ran 178.8 us against 172.7 us whole; range-major,
+// 168.6 against 170.7 us).  Chains are planned only for at most half a round of split tiles: a
+// partial round that keeps more than half the pairs busy runs each tile faster than a full round
+// does, and against it the split gained 1 % (and lost 1 % at K = 12288).
 constexpr int kSkMinUnits = 8;
 constexpr int kSkSumStages = 10;
 constexpr double kSkMinGain = 0.1;

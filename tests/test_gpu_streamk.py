@@ -49,7 +49,7 @@ def _case(M, h, F, t, seed, bias=True):
     (520, 1032, 15680, 4),   # ragged M (3 row tiles), N (1032 = 4 x 256 + 8), K (3920 per shard)
     (300, 1024, 16384, 4),   # 8 tiles, 128 k-stages
     (272, 776, 24576, 3),    # 8 tiles, t = 3: range boundaries inside shards
-    (2048, 4096, 8192, 4),   # 128 tiles: a round of whole tiles, then 52 (kept whole: a split would not pay)
+    (2048, 4096, 12288, 4),  # 128 tiles: a round of whole tiles, then 52 kept whole (a split would not pay)
     (2560, 2048, 4096, 4),   # 80 tiles: a round of whole tiles, then the last few split
 ])
 def test_row_parallel_streamk_matches_oracle(M, h, F, t, chain, monkeypatch):
