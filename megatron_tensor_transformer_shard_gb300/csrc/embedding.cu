@@ -121,14 +121,14 @@ __global__ void __launch_bounds__(PREFETCH_THREADS)
 // lane load) counts per token i: `before`, the tokens of its id before it; `total`,
 // the tokens of its id; `first`, its id's first token.  An id outside [0, V) is
 // reported and gets first = INT_MAX, total = 0: it joins no segment.
-// Pass 2 (256 tokens per CTA) places the tokens in the order (first token of the id,
+// Pass 2 (1024 tokens per CTA) places the tokens in the order (first token of the id,
 // token): every CTA scans the chunk's per-token flags itself (n <= 8192) for each id's
 // offset and short-list index, then writes its tokens: keys[offset(first) + before] =
 // id << 13 | i; a short id's descriptor (id, length, tokens) with every token filling
 // its own slot; a long id's (start, length) at its rank, longest first (ties by first
 // token).  seg[0], seg[1] = the numbers of short and long segments.
 constexpr int COUNT_WARPS = 16;   // tokens per CTA in pass 1
-constexpr int PLACE_THREADS = 256;
+constexpr int PLACE_THREADS = 1024;  // short serial runs in the scans (the pass is latency-bound)
 constexpr int kPlaceSmem = (5 * (SORT_MAX + SORT_MAX / 32 + 2) + SORT_MAX) * 4;
 
 __global__ void __launch_bounds__(COUNT_WARPS * 32)
@@ -162,13 +162,18 @@ __global__ void __launch_bounds__(COUNT_WARPS * 32)
   const int me = sid[i];
   int b = 0, tt = 0, f = 0x7fffffff;
   const int4* s4 = reinterpret_cast<const int4*>(sid);
+  // Nearly every group of four holds no match: one combined test, the counts only on a hit
+  // (the loop was issue-bound at about 11 instructions an id).
+#pragma unroll 4
   for (int q = lane; q < npad / 4; q += 32) {
     const int4 v = s4[q];
-    const int m = 4 * q;
-    if (v.x == me) { ++tt; b += m < i; f = min(f, m); }
-    if (v.y == me) { ++tt; b += m + 1 < i; f = min(f, m + 1); }
-    if (v.z == me) { ++tt; b += m + 2 < i; f = min(f, m + 2); }
-    if (v.w == me) { ++tt; b += m + 3 < i; f = min(f, m + 3); }
+    if ((v.x == me) | (v.y == me) | (v.z == me) | (v.w == me)) {
+      const int m = 4 * q;
+      if (v.x == me) { ++tt; b += m < i; f = min(f, m); }
+      if (v.y == me) { ++tt; b += m + 1 < i; f = min(f, m + 1); }
+      if (v.z == me) { ++tt; b += m + 2 < i; f = min(f, m + 2); }
+      if (v.w == me) { ++tt; b += m + 3 < i; f = min(f, m + 3); }
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
