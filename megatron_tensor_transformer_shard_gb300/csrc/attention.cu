@@ -99,11 +99,11 @@ struct AttnFwdArgs {
 
 // K-major 128x128 bf16 tile in two 64-column panels: descriptor of MMA k-step kk (16 columns).
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
-  return ptx::sdesc_sw128(base + (kk >> 2) * PANEL + (kk & 3) * 32, 16, 1024);
+  return ptx::sdesc_at(ptx::sdesc_sw128(base, 16, 1024), (kk >> 2) * PANEL + (kk & 3) * 32);
 }
 // Same tile read MN-major (the 64-column panels are the MN chunks): k-step kk = 16 rows.
 __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int kk) {
-  return ptx::sdesc_sw128(base + kk * 2048, PANEL, 1024);
+  return ptx::sdesc_at(ptx::sdesc_sw128(base, PANEL, 1024), kk * 2048);
 }
 
 
@@ -473,11 +473,11 @@ struct AttnBwdArgs {
 
 // K-major 64-row tile in two 64-column panels: descriptor of MMA k-step kk (16 columns).
 __device__ __forceinline__ uint64_t kmajor64_desc(uint32_t base, int kk) {
-  return ptx::sdesc_sw128(base + (kk >> 2) * PANEL64 + (kk & 3) * 32, 16, 1024);
+  return ptx::sdesc_at(ptx::sdesc_sw128(base, 16, 1024), (kk >> 2) * PANEL64 + (kk & 3) * 32);
 }
 // The same tile read MN-major: k-step kk = rows 16 kk .. 16 kk + 15.
 __device__ __forceinline__ uint64_t mnmajor64_desc(uint32_t base, int kk) {
-  return ptx::sdesc_sw128(base + kk * 2048, PANEL64, 1024);
+  return ptx::sdesc_at(ptx::sdesc_sw128(base, PANEL64, 1024), kk * 2048);
 }
 // TMEM column of k-step kk of an fp16 A operand written by the two column halves.
 __device__ __forceinline__ uint32_t half_split_col(int kk) { return (kk >> 1) * 32 + (kk & 1) * 8; }

@@ -490,10 +490,10 @@ __device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t a_addr, uint
   for (int kk = 0; kk < BK / 16; ++kk) {
     // K-major: 16 K-elements = 32 bytes inside the 128-byte swizzle row; 8-row groups 1024 B apart.
     // MN-major: 16 K-rows = two 1024-byte groups; 64-wide MN chunks MN_CHUNK_BYTES apart.
-    const uint64_t ad = A_MN ? ptx::sdesc_sw128(a_addr + kk * 2048, MN_CHUNK_BYTES, 1024)
-                             : ptx::sdesc_sw128(a_addr + kk * 32, 16, 1024);
-    const uint64_t bd = B_MN ? ptx::sdesc_sw128(b_addr + kk * 2048, MN_CHUNK_BYTES, 1024)
-                             : ptx::sdesc_sw128(b_addr + kk * 32, 16, 1024);
+    const uint64_t ad = A_MN ? ptx::sdesc_at(ptx::sdesc_sw128(a_addr, MN_CHUNK_BYTES, 1024), kk * 2048)
+                             : ptx::sdesc_at(ptx::sdesc_sw128(a_addr, 16, 1024), kk * 32);
+    const uint64_t bd = B_MN ? ptx::sdesc_at(ptx::sdesc_sw128(b_addr, MN_CHUNK_BYTES, 1024), kk * 2048)
+                             : ptx::sdesc_at(ptx::sdesc_sw128(b_addr, 16, 1024), kk * 32);
     ptx::mma_bf16(d_tmem, ad, bd, idesc, (!first || kk > 0) ? 1u : 0u);
   }
 }
@@ -1392,10 +1392,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           for (int kk = 0; kk < KB * BK / 16; ++kk) {
             // K-major: a 16 KB panel per 64-wide k-block, 32 bytes per K = 16 inside it.
             // MN-major: 64 * KB K-rows per 64-column chunk, chunks KB * 8 KB apart.
-            const uint64_t ad = A_MN ? ptx::sdesc_sw128(a_addr + kk * 2048, KB * MN_CHUNK_BYTES, 1024)
-                                     : ptx::sdesc_sw128(a_addr + (kk >> 2) * P_A_BYTES + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = B_MN ? ptx::sdesc_sw128(b_addr + kk * 2048, KB * MN_CHUNK_BYTES, 1024)
-                                     : ptx::sdesc_sw128(b_addr + (kk >> 2) * P_B_BYTES + (kk & 3) * 32, 16, 1024);
+            const uint64_t ad =
+                A_MN ? ptx::sdesc_at(ptx::sdesc_sw128(a_addr, KB * MN_CHUNK_BYTES, 1024), kk * 2048)
+                     : ptx::sdesc_at(ptx::sdesc_sw128(a_addr, 16, 1024), (kk >> 2) * P_A_BYTES + (kk & 3) * 32);
+            const uint64_t bd =
+                B_MN ? ptx::sdesc_at(ptx::sdesc_sw128(b_addr, KB * MN_CHUNK_BYTES, 1024), kk * 2048)
+                     : ptx::sdesc_at(ptx::sdesc_sw128(b_addr, 16, 1024), (kk >> 2) * P_B_BYTES + (kk & 3) * 32);
             ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (ks > it.klo || kk > 0) ? 1u : 0u);
           }
           ptx::mma_commit_pair_mc(&empty[stage], 0x3);  // frees this stage in both CTAs

@@ -177,6 +177,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// The descriptor of the same layout `off` bytes further on (off a multiple of 16): one add
+// to the start-address field, which cannot carry out of its 14 bits because shared-memory
+// addresses stay below 2^18.  Cheaper for an issuing thread than rebuilding the descriptor
+// for every k-step.
+__device__ __forceinline__ uint64_t sdesc_at(uint64_t desc, uint32_t off) { return desc + (off >> 4); }
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
 //   bits 4-5 D format (1 = f32)   bits 7-9 A format (1 = bf16)  bits 10-12 B format (1 = bf16)
 //   bit 15 A major (1 = MN-major) bit 16 B major                bits 17-22 N >> 3
