@@ -174,7 +174,7 @@ def layer_forward(X, w: LayerWeights, act="gelu_tanh", causal=True, scale=None, 
     QKV = torch.empty(t, s, 3 * d // t, dtype=torch.float16, device=dev)  # fp16 attention operands
     O = torch.empty(t, s, d // t, dtype=BF16, device=dev)
     lse = torch.empty(t, w.n_heads // t, s, dtype=f32, device=dev)
-    aws = _ws(L.tp_attn_forward_workspace_size(s, d, w.n_heads, w.head_dim, t, 0), dev)  # stream-K room
+    aws = _ws(L.tp_attn_forward_workspace_size(s, d, w.n_heads, w.head_dim, t, 0), dev)  # room for the split-K partials
     L.tp_attn_forward(Xn1, s, d, w.n_heads, w.head_dim, t, int(causal), scale, w.Wqkv_p, w.bqkv_p, w.Wo_p, w.b_o,
                       X, X1, QKV, O, lse, L.TP_ATTN_F16_INPUT, aws, aws.numel())
     Xn2 = torch.empty(s, d, dtype=BF16, device=dev)

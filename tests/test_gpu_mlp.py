@@ -139,7 +139,7 @@ def test_unfused_partials_match_oracle(M, h, F, t):
     dev, ref, w = _case(M, h, F, t, seed=3)
     flags = L.TP_FLAG_UNFUSED_REDUCE
     nws = L.tp_mlp_workspace_size(M, h, F, t, flags)
-    assert nws >= t * M * h * 4                     # the partials first, then stream-K room
+    assert nws >= t * M * h * 4                     # the partials first, then the split-K room
     wsb = torch.empty(nws, dtype=torch.uint8, device="cuda")
     ws = wsb[:t * M * h * 4].view(torch.float32).view(t, M, h)
     Y = torch.empty(M, h, dtype=torch.bfloat16, device="cuda")
