@@ -201,15 +201,19 @@ tp_status tp_row_parallel_forward(const tp_bf16* A, int64_t M, int64_t K, int64_
  * pairs evenly: the full rounds of whole tiles stay whole, and the remaining tiles (all of
  * them, when they are fewer than the pairs) are cut into S equal ranges of k-steps (a
  * row-parallel GEMM's t shard ranges laid end to end) at the same cut points for every
- * tile, dealt to all pairs -- S is chosen to finish first, and no cut is made when it
- * would save under 7 % of the time.  Every range leaves its fp32 partial in ws and counts
- * itself; the range that completes a tile's count adds the tile's partials in range order
- * and applies the epilogue, so the sums are deterministic for a given device (the plan
- * depends on its SM count) and only the rounding of the fp32 sum differs from the
- * data-parallel schedule.  Nothing waits on another CTA pair, and the counters reset
- * themselves (CUDA-graph replay is fine; any initial contents are).  The MLP and attention
- * calls take the same room at the end of their workspaces.  Workspaces must not be shared
- * by calls that may run at the same time. */
+ * tile, dealt to all pairs -- S is chosen by a time model to finish first, and no cut is
+ * made when it would save too little.  bf16 outputs (the row-parallel GEMM, the f-reduced
+ * dX) chain their ranges when at most half a round of tiles is split: range 0 stores its
+ * fp32 partial into the tile's running sum in ws, each next range adds into it after the
+ * previous range's flag (a bounded wait on a range dealt earlier), and the last range adds
+ * its accumulator and applies the epilogue.  The other outputs count their ranges: every
+ * range leaves its fp32 partial in ws and counts itself; the range that completes a tile's
+ * count adds the tile's partials in range order and applies the epilogue.  Either way the
+ * sums run in range order, so they are deterministic for a given device (the plan depends
+ * on its SM count) and only the rounding of the fp32 sum differs from the data-parallel
+ * schedule.  Flags and counters reset themselves (CUDA-graph replay is fine; any initial
+ * contents are).  The MLP and attention calls take the same room at the end of their
+ * workspaces.  Workspaces must not be shared by calls that may run at the same time. */
 size_t tp_column_parallel_workspace_size(int64_t M, int64_t h, int64_t N, int t);
 tp_status tp_column_parallel_forward_ws(const tp_bf16* X, int64_t M, int64_t h, int64_t N, int t, tp_act act,
                                         const tp_bf16* W_p, const tp_bf16* b, tp_bf16* Z, tp_bf16* A, void* ws,
