@@ -192,8 +192,10 @@ tp_status tp_row_parallel_forward(const tp_bf16* A, int64_t M, int64_t K, int64_
  * two calls, the MLP and the attention blocks split each output tile's K steps -- for the
  * row-parallel GEMM the t shards' K ranges laid end to end -- over the 2..16 CTAs of a
  * thread-block cluster, which sum their fp32 partials on chip (distributed shared memory)
- * in range order before the epilogue.  No workspace is needed and the result does not
- * depend on timing; only the rounding of the fp32 sum differs from the unsplit GEMM. */
+ * in range order before the epilogue; output tiles are 128 columns wide when 256-column
+ * tiles would keep under a quarter of the SMs busy.  No workspace is needed and the result
+ * does not depend on timing; only the rounding of the fp32 sum differs from the unsplit
+ * GEMM. */
 
 /* The same two calls with a workspace (tp_*_workspace_size() bytes, 256-byte aligned; a
  * smaller one is used as far as it goes, NULL runs the calls above).  It lets a GEMM of
