@@ -467,8 +467,8 @@ tp_status tp_reduce_qkv_gqa_grad(const float* dWp, int64_t d, int n_heads, int n
  *   tp_get_device_status() reports TP_ERR_SHAPE.
  * Backward: g backward hands dY to every shard; shard i adds dY[n] into
  * dE_p[i][id - i V/t] for every token it owns.  Deterministic: the tokens of a
- * row are added in token order (chunks of 8192 tokens are sorted by (id, token)
- * on the device).  dE_p [t][V/t][h] fp32, overwritten (zeroed first) or added
+ * row are added in a fixed order (chunks of 8192 tokens are grouped by id on the
+ * device, the ids in order of first occurrence and each id's tokens in token order).  dE_p [t][V/t][h] fp32, overwritten (zeroed first) or added
  * to when accumulate != 0; ws: tp_vocab_embedding_backward_workspace_size(N)
  * bytes.  The LM head on the same split is the column-parallel GEMM against
  * E^T (tp_column_parallel_forward); the pages define no loss, none is built. */
