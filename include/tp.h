@@ -43,6 +43,15 @@
  *    matching *_workspace_size() gives the minimum.  Too small -> TP_ERR_WORKSPACE.
  *  - Thread safety: calls on different streams may run concurrently; they
  *    share only the device error word.
+ *  - Environment variables (for tuning and tests; none is needed):
+ *      TP_WAIT_TIMEOUT_MS  limit of every bounded wait inside a kernel, 1..60000 ms
+ *                          (default 2000; read once per process);
+ *      TP_GEMM_PAIR=0      single-CTA GEMM kernel instead of the CTA-pair kernel;
+ *      TP_SPLITK=S         K ranges per tile of the M <= 128 cluster split (1 = none);
+ *      TP_SPLITC_NARROW=0|1  256- or 128-column tiles of that split (default: by size);
+ *      TP_STREAMK=0        no split K across CTA pairs even with a workspace;
+ *      TP_SPLIT_CHAIN=0    split K across CTA pairs by counted ranges only.
+ *    All but the first are read at each call.
  */
 #ifndef TPSHARD_TP_H
 #define TPSHARD_TP_H
